@@ -1,0 +1,451 @@
+"""Benchmark of the layout permute on GB300: one JSON line on stdout (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one ``tl_permute`` call over the whole workload (default: 65536 float16
+tiles of 128x64, row-major -> column-major per tile, 1 GiB in + 1 GiB out).  The
+metric is GB/s of algorithmic traffic (every element read once and written once,
+2 * N * elem_bytes per step) and its fraction of the measured HBM copy bandwidth.
+
+* ``value``: device-resident inputs; W warm-up steps, then K steps timed with CUDA
+  events on the launching stream between barriers, max over ranks.  Inputs are
+  larger than L2 (129 MB), so no flush is needed.
+* ``e2e``: the same call with host buffers: every step copies the input from
+  pinned host memory, permutes, and copies the result back, inside the timed region.
+* ``cpu_baseline``: the CPU oracle (test infrastructure) timed on this host's cores
+  on a bounded sample of the same workload; the GPU output is checked against it
+  on that sample (bit-exact).
+* ``--impl reference``: the oracle alone, as the reference arm (rank 0 only).
+
+Under ``torchrun`` each rank permutes its own copy of the workload on its own GPU
+(independent batches, no collective on the data path; weak scaling) and rank 0
+reports the whole-job throughput over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "permute GB/s (read+write bytes) and % of GB300 HBM peak, bit-exact vs oracle"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "tile_transpose"
+# Sources of the kernel the roofline line reports; a traffic figure recorded in
+# profiles/ is only used while these files are unchanged.
+KERNEL_SOURCES = {
+    "tile": ["k_tile.cu", "tile_common.cuh", "tl_device.cuh"],
+    "cluster": ["k_cluster.cu", "tile_common.cuh", "tl_device.cuh"],
+    "rows": ["k_rows.cu", "tl_device.cuh"],
+    "chunk": ["k_chunk.cu", "tl_device.cuh"],
+    "warp": ["k_warp.cu", "tl_device.cuh"],
+    "generic": ["k_generic.cu", "tl_device.cuh"],
+}
+KERNEL_NAMES = {"tile": "k_tile", "cluster": "k_cluster", "rows": "k_rows", "chunk": "k_chunk",
+                "warp": "k_warp", "generic": "k_generic"}
+DTYPES = {"sf_transpose": "f32", "tile_transpose": "f16", "mx_sf": "u8", "attention": "bf16",
+          "t2d_u8": "u8", "t2d_f16": "f16", "t2d_f32": "f32", "t2d_f64": "f64",
+          "t2d_v16": "16-byte"}
+
+
+# ---------------------------------------------------------------------------
+# multi-process helpers (also exercised by the CPU tests with gloo)
+# ---------------------------------------------------------------------------
+def dist_env():
+    """(rank, local_rank, world_size) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Maximum of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def whole_job_gbps(bytes_per_step_per_rank: int, steps: int, world: int, max_ms: float) -> float:
+    """Aggregate GB/s of a weak-scaling run: every rank moves the same bytes."""
+    return bytes_per_step_per_rank * steps * world / (max_ms * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        ids = [v.strip() for v in vis.split(",")] if vis else []
+        self.gpu = ids[local_rank] if local_rank < len(ids) else str(local_rank)
+        self.samples = []          # (wall time, sm, max, power, {reason: active})
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", self.gpu], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm, mx = float(parts[0]), float(parts[1])
+                pw = float(parts[2]) if parts[2] not in ("[N/A]", "N/A") else None
+            except ValueError:
+                continue
+            active = {r: ("Active" in p and "Not" not in p) for r, p in zip(self.REASONS, parts[3:7])}
+            self.samples.append((time.time(), sm, mx, pw, active))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples_in_window": 0,
+                    "note": "nvidia-smi unavailable"}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        n_in = len(inside)
+        if not inside:   # window shorter than the sampling period: nearest samples
+            mid = 0.5 * (t0 + t1)
+            inside = sorted(self.samples, key=lambda s: abs(s[0] - mid))[:2]
+        sms = sorted(s[1] for s in inside)
+        reasons = sorted({r for s in inside for r, a in s[4].items() if a})
+        powers = [s[3] for s in inside if s[3] is not None]
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples_in_window": n_in,
+                "power_w_max": max(powers) if powers else None}
+
+
+# ---------------------------------------------------------------------------
+# roofline inputs
+# ---------------------------------------------------------------------------
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash(path_name: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(path_name, []):
+        with open(os.path.join(ROOT, "movement_tl_permute_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(path_name: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel changed since."""
+    fname = os.path.join(ROOT, "profiles", "%s_%s.md" % (KERNEL_NAMES.get(path_name, path_name),
+                                                          workload))
+    try:
+        with open(fname) as f:
+            text = f.read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_source_hash(path_name):
+        return None
+    try:
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def sample_layout(w, m):
+    """The leading m indices of axis 0 of workload w (same strides)."""
+    return (m,) + tuple(w.shape[1:])
+
+
+def oracle_rate(w, src, dst, threads, budget_s):
+    """Largest leading sample of axis 0 the oracle finishes in about budget_s.
+    Returns (m, seconds for one run of it)."""
+    import oracle
+
+    m = max(1, min(w.shape[0], 8))
+    while True:
+        t0 = time.perf_counter()
+        oracle.permute(src, dst, sample_layout(w, m), w.src_strides, w.dst_strides, w.elem_bytes,
+                       nthreads=threads)
+        dt = time.perf_counter() - t0
+        if m >= w.shape[0] or dt >= 0.05 * budget_s:
+            break
+        m = min(w.shape[0], m * 4)
+    if m < w.shape[0] and dt > 0:
+        m = max(1, min(w.shape[0], int(m * budget_s / dt)))
+        t0 = time.perf_counter()
+        oracle.permute(src, dst, sample_layout(w, m), w.src_strides, w.dst_strides, w.elem_bytes,
+                       nthreads=threads)
+        dt = time.perf_counter() - t0
+    return m, dt
+
+
+def cpu_baseline(w, src, dst, budget_s=10.0):
+    import oracle
+
+    threads = max(1, min(len(os.sched_getaffinity(0)), oracle.max_threads()))
+    m, dt = oracle_rate(w, src, dst, threads, budget_s)
+    runs, total = 1, dt
+    while total < 0.5 * budget_s and runs < 20:
+        t0 = time.perf_counter()
+        oracle.permute(src, dst, sample_layout(w, m), w.src_strides, w.dst_strides, w.elem_bytes,
+                       nthreads=threads)
+        total += time.perf_counter() - t0
+        runs += 1
+    per = total / runs
+    n = m * (w.n_elems // w.shape[0])
+    gbps = 2 * n * w.elem_bytes / per / 1e9
+    return {"value": round(gbps, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "leading %d of %d along axis 0 (%d elements, %.1f MiB read+write), "
+                      "%d run(s), %.2f s each" % (m, w.shape[0], n,
+                                                  2 * n * w.elem_bytes / 2**20, runs, per)}, m
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+def config_of(w, plan):
+    return {"workload": "%s: %s" % (w.name, w.description), "shape": list(w.shape),
+            "src_strides": list(w.src_strides), "dst_strides": list(w.dst_strides),
+            "elem_bytes": w.elem_bytes, "bytes_per_step": w.algorithmic_bytes,
+            "path": plan["path"] if plan else None,
+            "grid": plan["grid"] if plan else None, "block": plan["block"] if plan else None,
+            "l2": "inputs larger than L2 (129 MB): no flush between steps",
+            "seed": w.seed}
+
+
+def run_reference(args, w):
+    import numpy as np
+
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    from movement_tl_permute_gb300 import workloads
+    import oracle
+
+    oracle.build()
+    src = workloads.make_input(w)
+    dst = np.zeros(w.dst_elems * w.elem_bytes, dtype=np.uint8)
+    threads = max(1, min(len(os.sched_getaffinity(0)), oracle.max_threads()))
+    per_step_budget = min(10.0, max(0.05, 90.0 / max(1, args.steps + args.warmup)))
+    m, _ = oracle_rate(w, src, dst, threads, per_step_budget)
+    shape = sample_layout(w, m)
+    for _ in range(args.warmup):
+        oracle.permute(src, dst, shape, w.src_strides, w.dst_strides, w.elem_bytes,
+                       nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.permute(src, dst, shape, w.src_strides, w.dst_strides, w.elem_bytes,
+                       nthreads=threads)
+    dt = time.perf_counter() - t0
+    n = m * (w.n_elems // w.shape[0])
+    per = dt / max(1, args.steps)
+    gbps = 2 * n * w.elem_bytes / per / 1e9
+    sample = ("leading %d of %d along axis 0 (%d elements, %.1f MiB read+write) per step"
+              % (m, w.shape[0], n, 2 * n * w.elem_bytes / 2**20))
+    peak, _ = measured_peak()
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbps, 3), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": DTYPES.get(w.name, "bits"), "data": "synthetic",
+            "config": config_of(w, None), "pct_hbm_peak": round(100 * gbps / peak, 3),
+            "cpu_baseline": {"value": round(gbps, 3), "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(gbps, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import movement_tl_permute_gb300 as tl
+    from movement_tl_permute_gb300 import build as tl_build
+    from movement_tl_permute_gb300 import workloads
+
+    rank, local, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tl_build.build()
+    tl.load()
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    src_np = workloads.make_input(w)
+    nbytes_dst = w.dst_elems * w.elem_bytes
+    s_gpu = torch.from_numpy(src_np).to(dev)
+    d_gpu = torch.empty(nbytes_dst, dtype=torch.uint8, device=dev)
+    args_call = (w.shape, w.src_strides, w.dst_strides, w.elem_bytes)
+    plan = tl.tl_plan(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call)
+
+    def step():
+        tl.tl_permute(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call, sptr)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ------------------------------------------------ device-resident timing
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = tl.tl_launch_count()
+    t_wall0 = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier()
+    launches = tl.tl_launch_count() - launches0
+    ms_local = e0.elapsed_time(e1)
+    ms_max = reduce_max(ms_local, dev if world > 1 else None)
+    clock_summary = clocks.summary(t_wall0, t_wall1)
+
+    # ------------------------------------------------ end to end, host buffers
+    src_pin = torch.from_numpy(src_np).pin_memory()
+    dst_pin = torch.empty(nbytes_dst, dtype=torch.uint8).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        s_gpu.copy_(src_pin, non_blocking=True)
+        tl.tl_permute(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call, sptr)
+        dst_pin.copy_(d_gpu, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), dev if world > 1 else None)
+    clocks.stop()
+
+    if rank != 0:
+        dist.destroy_process_group() if dist.is_initialized() else None
+        return 0
+
+    # ------------------------------------------------ CPU oracle + sampled parity
+    got = dst_pin.numpy()                  # result of the last e2e step (same input)
+    check = got.copy()
+    base, m = cpu_baseline(w, src_np, check, budget_s=args.cpu_budget)
+    parity = bool(np.array_equal(check, got))
+
+    bytes_step = w.algorithmic_bytes
+    value = whole_job_gbps(bytes_step, args.steps, world, ms_max)
+    per_launch_gbps = bytes_step / (ms_local / max(1, args.steps) * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic = recorded_traffic(plan["path"], w.name)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPES.get(w.name, "bits"),
+        "data": "synthetic", "config": config_of(w, plan),
+        "pct_hbm_peak": round(100.0 * value / world / peak, 2),
+        "parity": {"bit_exact": parity,
+                   "checked": "GPU output vs oracle on the cpu_baseline sample"},
+        "roofline": {"bound": "hbm", "achieved": round(per_launch_gbps, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(per_launch_gbps / peak, 4),
+                     "traffic": traffic, "kernel": KERNEL_NAMES.get(plan["path"]),
+                     "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs: copy, burst)" % peak_kind},
+        "cpu_baseline": base,
+        "e2e": {"value": round(whole_job_gbps(bytes_step, e2e_steps, world, e2e_ms), 2),
+                "unit": UNIT, "h2d_bytes_per_step": int(src_np.nbytes),
+                "d2h_bytes_per_step": int(nbytes_dst), "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clock_summary,
+    }
+    print(json.dumps(line), flush=True)
+    if dist.is_initialized():
+        dist.destroy_process_group()
+    return 0 if parity else 3
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the CPU baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from movement_tl_permute_gb300 import workloads
+
+    w = workloads.get(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

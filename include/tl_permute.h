@@ -1,0 +1,225 @@
+/*
+ * tl_permute.h -- C ABI of the GB300 (sm_103a) tensor layout-permute library.
+ *
+ * A layout is a shape with per-axis element strides; the element at logical
+ * coordinate c of a buffer lives at  data + offset + sum_i c[i] * stride[i]
+ * (TVM docs, "Buffers and memory", section "Declaring buffers": a buffer is a
+ * pointer plus a layout, and indexing resolves to that address arithmetic).
+ * Permuting a layout means materialising, for every coordinate c of the shape,
+ *
+ *     dst[sum_i c[i] * dst_strides[i]] = src[sum_i c[i] * src_strides[i]]
+ *
+ * with elements of 1, 2, 4, 8 or 16 bytes moved as raw bits (NaN payloads and
+ * signed zeros survive).  This covers warp-sized transposes such as the 4x32
+ * scale-factor transpose of the TVM "permute_layout" page, batched whole-tile
+ * transposes, and general N-D axis permutes.
+ *
+ * Conventions for every entry point
+ *   - Strides, offsets and extents are counted in ELEMENTS, never bytes.
+ *   - Pointers passed as src/dst are DEVICE pointers (cudaMalloc / PyTorch CUDA
+ *     storage) unless stated otherwise; the caller owns every buffer.  The
+ *     library allocates no device memory and keeps no per-call state; it caches
+ *     device properties and a driver entry point on first use.
+ *   - Return value: TL_OK (0) or a negative tl_status.  Argument errors are
+ *     reported synchronously and launch nothing.  tl_permute* is asynchronous
+ *     and stream-ordered: a kernel fault surfaces later through the CUDA runtime.
+ *   - Thread safety: all entry points may be called from several host threads.
+ */
+#ifndef TL_PERMUTE_H
+#define TL_PERMUTE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TL_MAX_DIMS 8
+#define TL_VERSION 1
+
+#if defined(__GNUC__)
+#define TL_API __attribute__((visibility("default")))
+#else
+#define TL_API
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *tl_stream_t;
+
+/* Status codes.  The first group mirrors the reasons the TVM permute_layout
+ * dispatch gives for declining ("permute_layout", section "What it accepts"). */
+typedef enum tl_status {
+    TL_OK = 0,
+    TL_ERR_ARG = -1,          /* NULL pointer, rank outside 0..8, negative extent or stride */
+    TL_ERR_ELEM_BYTES = -2,   /* element width not one of 1, 2, 4, 8, 16 */
+    TL_ERR_EXTENT = -3,       /* extents not a whole number of warp iterations (32 x P) */
+    TL_ERR_NO_VALID_K = -4,   /* no XOR swizzle leaves both phases bank-conflict-free */
+    TL_ERR_CHUNK = -5,        /* reserved: contiguous chunk under 16 B / not a multiple of 16 */
+    TL_ERR_DST_OVERLAP = -6,  /* two coordinates may land on one dst element */
+    TL_ERR_ALIAS = -7,        /* src and dst byte ranges intersect (outside the in-place case) */
+    TL_ERR_ALIGN = -8,        /* src or dst not aligned to its element width */
+    TL_ERR_PATH = -9,         /* the path forced through tl_permute_opts.flags does not apply */
+    TL_ERR_RANGE = -10,       /* an offset overflows 64 bits, or a region leaves its layout */
+    TL_ERR_CUDA = -11,        /* a CUDA runtime / driver call failed */
+    TL_ERR_TIMEOUT = -12,     /* device side: a bounded wait expired (written to dev_status) */
+    TL_ERR_BOUNDS = -13       /* a layout reaches outside the buffer size given in opts */
+} tl_status;
+
+/* A layout over `ndim` axes: element offset = offset + sum shape-coordinate * stride. */
+typedef struct tl_layout {
+    int32_t ndim;
+    int32_t reserved;
+    int64_t shape[TL_MAX_DIMS];
+    int64_t stride[TL_MAX_DIMS];
+    int64_t offset;
+} tl_layout;
+
+/*
+ * tl_layout_canon -- slice a pair of layouts to a region, canonicalise them and
+ * regroup src to dst's shape (TVM "permute_layout", "Algorithm" step 1; the
+ * contiguous-chunk walk of "copy_async -> dsmem", "Algorithm" step 1).
+ *
+ *   src, dst     layouts of equal ndim and shape (host structs, read only)
+ *   begin,extent region box per axis (host arrays of ndim); begin NULL = all
+ *                zeros, extent NULL = shape - begin
+ *   src_out,
+ *   dst_out      receive the canonical pair: one shared shape (extent-1 axes
+ *                dropped; adjacent axes merged, order kept, where BOTH sides are
+ *                contiguous across them), per-side strides, and offsets moved to
+ *                the region's first element
+ *   chunk_elems  (nullable) length of the common stride-1 chain at the
+ *                innermost end: the last extent when both last strides are 1,
+ *                else 0; 1 for a single-element region, 0 for an empty one.
+ *                A bulk copy needs chunk_elems * elem_bytes >= 16 and % 16 == 0.
+ * Returns TL_OK, TL_ERR_ARG (NULL, ndim mismatch, negative extent) or
+ * TL_ERR_RANGE (region outside the shape).
+ */
+TL_API int tl_layout_canon(const tl_layout *src, const tl_layout *dst, const int64_t *begin,
+                    const int64_t *extent, tl_layout *src_out, tl_layout *dst_out,
+                    int64_t *chunk_elems);
+
+/*
+ * tl_choose_xor_k -- host-side shared-memory bank simulator of the warp
+ * register-staged permute (TVM "permute_layout", "Algorithm" steps 2 and 3).
+ *
+ * Each of the 32 lanes stages P = prod(extent)/32 elements; in iteration r a
+ * lane handles iteration index j = r ^ ((lane >> shift) & mask), at coordinates
+ * decompose(lane + 32*j, extent) (row-major).  The simulator checks, for every r,
+ * the read phase (src_str) and the write phase (dst_str) against 32 banks of
+ * 4 bytes, wavefronts of 128 bytes (32 lanes for widths <= 4, 16 for 8-byte, 8
+ * for 16-byte), counting lanes that touch one bank -- even within one word -- as
+ * a conflict.  It returns the first conflict-free candidate in the order
+ * k = 0..log2(P) (k = 0 only if P is not a power of two), shift = 0..5-k.
+ *
+ *   ndim, extent, src_str, dst_str  host arrays, ndim 1..8, element units
+ *   elem_bytes                      1, 2, 4, 8 or 16
+ *   k, shift, mask                  outputs (mask = 2^k - 1); untouched on error
+ * Returns TL_OK, TL_ERR_ARG, TL_ERR_ELEM_BYTES, TL_ERR_EXTENT (prod(extent) is
+ * 0 or not a multiple of 32, or P > 1024) or TL_ERR_NO_VALID_K.
+ */
+TL_API int tl_choose_xor_k(int ndim, const int64_t *extent, const int64_t *src_str,
+                    const int64_t *dst_str, int elem_bytes, int *k, int *shift, int *mask);
+
+/*
+ * tl_bank_conflicts -- the simulator's worst bank-conflict degree for one
+ * warp-wide shared-memory access: lane_offsets[l] is the element offset lane l
+ * touches (n_lanes <= 32, negative = idle lane).  model 0 = the conservative
+ * rule above; model 1 = hardware rule (lanes reading one word share it).
+ * Returns the degree (1 = conflict-free, 0 = no active lane) or a tl_status < 0.
+ */
+TL_API int tl_bank_conflicts(int n_lanes, const int64_t *lane_offsets, int elem_bytes, int model);
+
+/*
+ * tl_permute -- materialise the permutation on the GPU (the hot path).
+ *
+ *   src          device pointer to the source's element at coordinate 0
+ *   dst          device pointer to the destination's element at coordinate 0
+ *   ndim         0..8 (0 = one element)
+ *   shape        host array of ndim extents (0 allowed: the call is a no-op)
+ *   src_strides,
+ *   dst_strides  host arrays of ndim element strides, each >= 0
+ *   elem_bytes   1, 2, 4, 8 or 16; src and dst must be aligned to
+ *                min(elem_bytes, 16) bytes
+ *   stream       stream to launch on
+ * dst must be non-overlapping (no two coordinates on one element; the check is
+ * the sorted-stride sufficient test).  src may overlap itself.  src and dst byte
+ * ranges must be disjoint, except for the in-place case of the warp path
+ * (identical pointers and per-tile footprints), where every tile is read in
+ * full before it is written.  Kernels are chosen by the planner (generic
+ * strided, contiguous-chunk copy, TMA-staged tile transpose, small-row register
+ * transpose, warp XOR-swizzle transpose).
+ */
+TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape,
+               const int64_t *src_strides, const int64_t *dst_strides, int elem_bytes,
+               tl_stream_t stream);
+
+/* Kernel paths (low 4 bits of tl_permute_opts.flags). */
+#define TL_PATH_AUTO 0u     /* planner's choice */
+#define TL_PATH_GENERIC 1u  /* any layout: one element per step, coordinates decoded */
+#define TL_PATH_CHUNK 2u    /* common contiguous innermost chain, widest aligned vector */
+#define TL_PATH_TILE 3u     /* 2-D/batched transpose: TMA tile into 128B-swizzled smem */
+#define TL_PATH_WARP 4u     /* warp register-staged XOR-swizzle transpose (in-place safe) */
+#define TL_PATH_ROWS 5u     /* short dst runs (<= 16 B): 16 B row loads, register transpose */
+#define TL_PATH_CLUSTER 6u  /* TILE with a 2-CTA cluster handing tiles over through DSMEM */
+#define TL_PATH_MASK 0xFu
+/* Test hook for the cluster path: the producer CTA skips its DSMEM hand-off, so the
+ * consumer's bounded wait must expire and report TL_ERR_TIMEOUT in dev_status. */
+#define TL_FLAG_TEST_DROP_HANDOFF (1u << 8)
+
+/* Options of tl_permute_ex.  Zero-initialise, then set what you need. */
+typedef struct tl_permute_opts {
+    uint32_t flags;       /* TL_PATH_* | TL_FLAG_* */
+    int32_t max_ctas;     /* > 0: cap on the persistent grid (tuning); 0 = planner */
+    int32_t *dev_status;  /* nullable DEVICE int32: a kernel whose bounded wait expires
+                             writes TL_ERR_TIMEOUT here (it is never cleared by the
+                             library; the caller zeroes it).  NULL = not reported. */
+    int64_t src_bytes;    /* > 0: bytes addressable from src; the layout must fit */
+    int64_t dst_bytes;    /* > 0: bytes addressable from dst */
+    int64_t reserved[4];
+} tl_permute_opts;
+
+/* tl_permute with options (path forcing, status word, buffer bounds).
+ * opts may be NULL (same as tl_permute).  A forced path that does not apply
+ * returns TL_ERR_PATH and launches nothing. */
+TL_API int tl_permute_ex(const void *src, void *dst, int ndim, const int64_t *shape,
+                  const int64_t *src_strides, const int64_t *dst_strides, int elem_bytes,
+                  tl_stream_t stream, const tl_permute_opts *opts);
+
+/* What the planner would do for a call (host only; pointers are used for their
+ * alignment only and never dereferenced; no GPU needed except for grid sizing,
+ * which reports 0 when no device is present). */
+typedef struct tl_plan_info {
+    int32_t path;                  /* TL_PATH_* chosen */
+    int32_t ndim;                  /* canonical rank (sorted by dst stride, merged) */
+    int64_t extent[TL_MAX_DIMS];
+    int64_t src_str[TL_MAX_DIMS];
+    int64_t dst_str[TL_MAX_DIMS];
+    int32_t vec_bytes;             /* vector width of global accesses */
+    int32_t in_place;              /* 1 when src == dst and the warp path runs in place */
+    int32_t k, shift, mask;        /* warp path swizzle (else 0) */
+    int32_t tile_rows, tile_cols;  /* tile path: rows (b) x columns (a) per tile */
+    int64_t tiles;                 /* work units (tiles, rows, warps...) */
+    int32_t grid, block;           /* launch shape (0 without a device) */
+    int32_t smem_bytes;            /* dynamic shared memory per CTA */
+    int32_t reserved[5];
+} tl_plan_info;
+
+TL_API int tl_plan(const void *src, const void *dst, int ndim, const int64_t *shape,
+            const int64_t *src_strides, const int64_t *dst_strides, int elem_bytes,
+            const tl_permute_opts *opts, tl_plan_info *out);
+
+/* Human-readable text of a status code (static storage). */
+TL_API const char *tl_status_string(int status);
+
+/* Number of kernels this library has launched in this process. */
+TL_API uint64_t tl_launch_count(void);
+
+/* TL_VERSION of the loaded library. */
+TL_API int tl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TL_PERMUTE_H */

@@ -1,1 +1,257 @@
-"""GB300-native tensor layout permutation (sm_103a)."""
+"""GB300-native tensor layout permutation (sm_103a).
+
+A thin ctypes binding over ``libtl_permute.so`` (the C ABI declared in
+``include/tl_permute.h``).  Every function here only marshals arguments: the
+planning runs in the library's host code and every byte moves in its CUDA
+kernels.  There is no Python or CPU fallback: if the library has not been built,
+loading it raises.
+
+The names follow the C ABI: ``tl_layout_canon``, ``tl_choose_xor_k``,
+``tl_bank_conflicts``, ``tl_permute``, ``tl_permute_ex``, ``tl_plan``,
+``tl_status_string``, ``tl_launch_count``, ``tl_version``.  ``permute`` is the
+same call for PyTorch tensors (it reads their device pointers, byte bounds and
+the current CUDA stream).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "TLError", "TL_MAX_DIMS", "PATHS", "PATH_NAMES", "TL_FLAG_TEST_DROP_HANDOFF",
+    "load", "library_path", "tl_layout_canon", "tl_choose_xor_k", "tl_bank_conflicts",
+    "tl_permute", "tl_permute_ex", "tl_plan", "tl_status_string", "tl_launch_count",
+    "tl_version", "permute",
+]
+
+TL_MAX_DIMS = 8
+PATHS = {"auto": 0, "generic": 1, "chunk": 2, "tile": 3, "warp": 4, "rows": 5, "cluster": 6}
+PATH_NAMES = {v: k for k, v in PATHS.items()}
+TL_FLAG_TEST_DROP_HANDOFF = 1 << 8
+STATUS = {0: "TL_OK", -1: "TL_ERR_ARG", -2: "TL_ERR_ELEM_BYTES", -3: "TL_ERR_EXTENT",
+          -4: "TL_ERR_NO_VALID_K", -5: "TL_ERR_CHUNK", -6: "TL_ERR_DST_OVERLAP",
+          -7: "TL_ERR_ALIAS", -8: "TL_ERR_ALIGN", -9: "TL_ERR_PATH", -10: "TL_ERR_RANGE",
+          -11: "TL_ERR_CUDA", -12: "TL_ERR_TIMEOUT", -13: "TL_ERR_BOUNDS"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libtl_permute.so")
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+
+
+class TLError(RuntimeError):
+    """A tl_* call returned a negative status."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        super().__init__("%s: %s (%s)" % (where, tl_status_string(code), self.name))
+
+
+class TlLayout(ctypes.Structure):
+    _fields_ = [("ndim", _i32), ("reserved", _i32), ("shape", _i64 * TL_MAX_DIMS),
+                ("stride", _i64 * TL_MAX_DIMS), ("offset", _i64)]
+
+
+class TlPermuteOpts(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_uint32), ("max_ctas", _i32), ("dev_status", ctypes.c_void_p),
+                ("src_bytes", _i64), ("dst_bytes", _i64), ("reserved", _i64 * 4)]
+
+
+class TlPlanInfo(ctypes.Structure):
+    _fields_ = [("path", _i32), ("ndim", _i32), ("extent", _i64 * TL_MAX_DIMS),
+                ("src_str", _i64 * TL_MAX_DIMS), ("dst_str", _i64 * TL_MAX_DIMS),
+                ("vec_bytes", _i32), ("in_place", _i32), ("k", _i32), ("shift", _i32),
+                ("mask", _i32), ("tile_rows", _i32), ("tile_cols", _i32), ("tiles", _i64),
+                ("grid", _i32), ("block", _i32), ("smem_bytes", _i32), ("reserved", _i32 * 5)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load the CUDA library; raises if it was not built (no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                "libtl_permute.so is missing (%s): build it with "
+                "`python -m movement_tl_permute_gb300.build` or __graft_entry__.build()"
+                % _LIB_PATH)
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i64p = ctypes.c_void_p, ctypes.POINTER(_i64)
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.tl_layout_canon.argtypes = [ctypes.POINTER(TlLayout), ctypes.POINTER(TlLayout), i64p,
+                                        i64p, ctypes.POINTER(TlLayout), ctypes.POINTER(TlLayout),
+                                        i64p]
+        lib.tl_choose_xor_k.argtypes = [ctypes.c_int, i64p, i64p, i64p, ctypes.c_int, ip, ip, ip]
+        lib.tl_bank_conflicts.argtypes = [ctypes.c_int, i64p, ctypes.c_int, ctypes.c_int]
+        lib.tl_permute.argtypes = [vp, vp, ctypes.c_int, i64p, i64p, i64p, ctypes.c_int, vp]
+        lib.tl_permute_ex.argtypes = [vp, vp, ctypes.c_int, i64p, i64p, i64p, ctypes.c_int, vp,
+                                      ctypes.POINTER(TlPermuteOpts)]
+        lib.tl_plan.argtypes = [vp, vp, ctypes.c_int, i64p, i64p, i64p, ctypes.c_int,
+                                ctypes.POINTER(TlPermuteOpts), ctypes.POINTER(TlPlanInfo)]
+        lib.tl_status_string.argtypes = [ctypes.c_int]
+        lib.tl_status_string.restype = ctypes.c_char_p
+        lib.tl_launch_count.argtypes = []
+        lib.tl_launch_count.restype = ctypes.c_uint64
+        lib.tl_version.argtypes = []
+        for name in ("tl_layout_canon", "tl_choose_xor_k", "tl_bank_conflicts", "tl_permute",
+                     "tl_permute_ex", "tl_plan", "tl_version"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _arr(vals, n=None):
+    vals = [int(v) for v in vals]
+    arr = (_i64 * max(1, len(vals) if n is None else n))()
+    for i, v in enumerate(vals):
+        arr[i] = v
+    return arr
+
+
+def _check(rc: int, where: str) -> int:
+    if rc < 0:
+        raise TLError(rc, where)
+    return rc
+
+
+def _layout(shape, strides, offset=0) -> TlLayout:
+    L = TlLayout()
+    L.ndim = len(shape)
+    for i, (e, s) in enumerate(zip(shape, strides)):
+        L.shape[i] = int(e)
+        L.stride[i] = int(s)
+    L.offset = int(offset)
+    return L
+
+
+def tl_status_string(code: int) -> str:
+    return load().tl_status_string(int(code)).decode()
+
+
+def tl_launch_count() -> int:
+    return int(load().tl_launch_count())
+
+
+def tl_version() -> int:
+    return int(load().tl_version())
+
+
+def tl_layout_canon(shape, src_strides, dst_strides, begin=None, extent=None, src_offset=0,
+                    dst_offset=0) -> dict:
+    """Slice + canonicalise + regroup a layout pair.  Returns the same keys as
+    the oracle's reference: extent, src_str, dst_str, src_offset, dst_offset,
+    chunk_elems."""
+    lib = load()
+    s, d = _layout(shape, src_strides, src_offset), _layout(shape, dst_strides, dst_offset)
+    so, do = TlLayout(), TlLayout()
+    chunk = _i64(0)
+    b = _arr(begin) if begin is not None else None
+    e = _arr(extent) if extent is not None else None
+    _check(lib.tl_layout_canon(ctypes.byref(s), ctypes.byref(d), b, e, ctypes.byref(so),
+                               ctypes.byref(do), ctypes.byref(chunk)), "tl_layout_canon")
+    n = so.ndim
+    return dict(extent=tuple(so.shape[:n]), src_str=tuple(so.stride[:n]),
+                dst_str=tuple(do.stride[:n]), src_offset=so.offset, dst_offset=do.offset,
+                chunk_elems=chunk.value)
+
+
+def tl_choose_xor_k(extent, src_str, dst_str, elem_bytes):
+    """(k, shift, mask) of the warp permute's XOR swizzle; raises TLError if none."""
+    k, shift, mask = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(load().tl_choose_xor_k(len(extent), _arr(extent), _arr(src_str), _arr(dst_str),
+                                  int(elem_bytes), ctypes.byref(k), ctypes.byref(shift),
+                                  ctypes.byref(mask)), "tl_choose_xor_k")
+    return k.value, shift.value, mask.value
+
+
+def tl_bank_conflicts(lane_offsets, elem_bytes, model="conservative") -> int:
+    offs = [-1 if o is None else int(o) for o in lane_offsets]
+    m = {"conservative": 0, "hardware": 1}[model]
+    return _check(load().tl_bank_conflicts(len(offs), _arr(offs), int(elem_bytes), m),
+                  "tl_bank_conflicts")
+
+
+def _opts(flags=0, path="auto", dev_status=0, src_bytes=0, dst_bytes=0, max_ctas=0):
+    o = TlPermuteOpts()
+    o.flags = (PATHS[path] if isinstance(path, str) else int(path)) | int(flags)
+    o.max_ctas = int(max_ctas)
+    o.dev_status = int(dev_status) or None
+    o.src_bytes = int(src_bytes)
+    o.dst_bytes = int(dst_bytes)
+    return o
+
+
+def tl_permute(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides, elem_bytes: int,
+               stream: int = 0) -> None:
+    """dst[sum c*dst_strides] = src[sum c*src_strides] on the GPU (device pointers)."""
+    n = len(shape)
+    _check(load().tl_permute(int(src_ptr) or None, int(dst_ptr) or None, n, _arr(shape),
+                             _arr(src_strides), _arr(dst_strides), int(elem_bytes),
+                             int(stream) or None), "tl_permute")
+
+
+def tl_permute_ex(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides,
+                  elem_bytes: int, stream: int = 0, **opts) -> None:
+    """tl_permute with options: path=..., flags=..., dev_status=<device ptr>,
+    src_bytes=..., dst_bytes=..., max_ctas=..."""
+    o = _opts(**opts)
+    _check(load().tl_permute_ex(int(src_ptr) or None, int(dst_ptr) or None, len(shape),
+                                _arr(shape), _arr(src_strides), _arr(dst_strides),
+                                int(elem_bytes), int(stream) or None, ctypes.byref(o)),
+           "tl_permute_ex")
+
+
+def tl_plan(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides, elem_bytes: int,
+            **opts) -> dict:
+    """What tl_permute_ex would launch (host-only)."""
+    o = _opts(**opts)
+    info = TlPlanInfo()
+    _check(load().tl_plan(int(src_ptr) or None, int(dst_ptr) or None, len(shape), _arr(shape),
+                          _arr(src_strides), _arr(dst_strides), int(elem_bytes),
+                          ctypes.byref(o), ctypes.byref(info)), "tl_plan")
+    n = info.ndim
+    return dict(path=PATH_NAMES[info.path] if info.path else "none", ndim=n,
+                extent=tuple(info.extent[:n]),
+                src_str=tuple(info.src_str[:n]), dst_str=tuple(info.dst_str[:n]),
+                vec_bytes=info.vec_bytes, in_place=bool(info.in_place), k=info.k,
+                shift=info.shift, mask=info.mask, tile_rows=info.tile_rows,
+                tile_cols=info.tile_cols, tiles=info.tiles, grid=info.grid, block=info.block,
+                smem_bytes=info.smem_bytes)
+
+
+def _bytes_after(t) -> int:
+    """Bytes addressable from t.data_ptr() to the end of its storage."""
+    st = t.untyped_storage()
+    return st.nbytes() - (t.data_ptr() - st.data_ptr())
+
+
+def permute(src, dst, shape, src_strides, dst_strides, elem_bytes=None, stream=None, **opts):
+    """Permute between two CUDA tensors used as raw storage.
+
+    ``src``/``dst`` are torch CUDA tensors whose ``data_ptr()`` is coordinate 0;
+    strides are in elements of ``elem_bytes`` (default: the tensors' element
+    size).  Launches on ``stream`` (default: torch's current stream) and checks
+    the layouts against the tensors' storage bounds.
+    """
+    import torch
+
+    if elem_bytes is None:
+        elem_bytes = src.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(src.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    opts.setdefault("src_bytes", _bytes_after(src))
+    opts.setdefault("dst_bytes", _bytes_after(dst))
+    tl_permute_ex(src.data_ptr(), dst.data_ptr(), shape, src_strides, dst_strides, elem_bytes,
+                  stream, **opts)

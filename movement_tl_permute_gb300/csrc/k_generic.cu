@@ -1,0 +1,60 @@
+// k_generic.cu -- the correctness floor: any layout pair, one element per step.
+//
+// Flat index f runs over the canonical shape in dst order (axes sorted by dst
+// stride, so consecutive threads write neighbouring elements); its coordinates
+// are decoded with per-axis divisions and applied to both stride vectors
+// (offset = sum c[i] * stride[i], TVM docs "Buffers and memory", "Declaring
+// buffers").
+#include "tl_kernels.h"
+
+namespace tl {
+namespace {
+
+template <int EB>
+__global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; f < a.total; f += step) {
+        int64_t so = 0, d = 0;
+        if (a.use32) {
+            uint32_t rem = (uint32_t)f;
+#pragma unroll
+            for (int i = TL_MAX_DIMS - 1; i >= 0; --i) {
+                if (i < a.n) {
+                    const uint32_t q = dev::div_u32(rem, a.div[i]);
+                    const uint32_t c = rem - q * a.div[i].d;
+                    rem = q;
+                    so += (int64_t)c * a.ss[i];
+                    d += (int64_t)c * a.ds[i];
+                }
+            }
+        } else {
+            int64_t rem = f;
+#pragma unroll
+            for (int i = TL_MAX_DIMS - 1; i >= 0; --i) {
+                if (i < a.n) {
+                    const int64_t c = rem % a.ext[i];
+                    rem /= a.ext[i];
+                    so += c * a.ss[i];
+                    d += c * a.ds[i];
+                }
+            }
+        }
+        dev::copy_elem<EB>(a.dst + d * EB, a.src + so * EB);
+    }
+}
+
+}  // namespace
+
+template <int EB>
+cudaError_t launch_generic(const GenericArgs& a, int grid, int block, cudaStream_t st) {
+    k_generic<EB><<<grid, block, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_generic<1>(const GenericArgs&, int, int, cudaStream_t);
+template cudaError_t launch_generic<2>(const GenericArgs&, int, int, cudaStream_t);
+template cudaError_t launch_generic<4>(const GenericArgs&, int, int, cudaStream_t);
+template cudaError_t launch_generic<8>(const GenericArgs&, int, int, cudaStream_t);
+template cudaError_t launch_generic<16>(const GenericArgs&, int, int, cudaStream_t);
+
+}  // namespace tl

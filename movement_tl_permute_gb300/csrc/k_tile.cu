@@ -1,0 +1,113 @@
+// k_tile.cu -- batched 2-D transpose through TMA-staged, 128B-swizzled shared memory.
+//
+// Plane: axis a is contiguous in src (stride 1), axis b is contiguous in dst
+// (stride 1); every other axis is a batch axis.  A tile is 128 rows of b by 128
+// BYTES of a (128/EB elements).  One producer warp streams tiles HBM -> shared
+// memory with `cp.async.bulk.tensor` (TMA, SWIZZLE_128B) into a ring of stages
+// guarded by mbarriers; eight consumer warps read each tile column-wise, assemble
+// 16-byte runs along b in registers and store them with 16-byte coalesced stores
+// (each warp store fills whole 128-byte lines of dst).  CTAs are persistent.
+//
+// Shared-memory column reads are made bank-conflict-free the way the TVM
+// "permute_layout" page makes its warp permute conflict-free ("Algorithm", step
+// 2): lanes that would hit the same bank visit their registers in an order
+// XOR-rotated by a field of their lane index.  With the TMA 128-byte swizzle a
+// 16-byte chunk c of row r sits at chunk c ^ (r & 7), so the 8 lane groups of a
+// warp must read rows with 8 distinct (r & 7); group g reads its k-th row as
+// (k ^ x_g), and the registers are put back in order with a conditional-swap
+// network before the stores.  The host bank simulator (tl_bank_conflicts)
+// reproduces these access patterns in the unit tests.
+#include "tile_common.cuh"
+
+namespace tl {
+namespace {
+
+using namespace dev;
+using namespace tile;
+
+template <int EB>
+__global__ void __launch_bounds__(kTileThreads)
+k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full[kTileStages];
+    __shared__ __align__(8) uint64_t empty[kTileStages];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTileStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer: one elected lane issues all TMA loads -------------
+        if (lane == 0) {
+            uint32_t issued = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++issued) {
+                const int s = issued % kTileStages;
+                const uint32_t use = issued / kTileStages;
+                if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const TileCoord tc = tile_coord(t, a);
+                mbar_arrive_expect_tx(&full[s], kTileBytes);
+                tma_load(smem + s * kTileBytes, &tmap, &full[s], a.rank,
+                         (int)(tc.ta * kRowBytes), (int)(tc.tb * kRows), (int)tc.bc[0],
+                         (int)tc.bc[1], (int)tc.bc[2]);
+            }
+            if (!ok) report(a.status, TL_ERR_TIMEOUT);
+            // Do not leave while a load may still write this CTA's shared memory.
+            for (uint32_t i = issued > kTileStages ? issued - kTileStages : 0; i < issued; ++i)
+                mbar_wait(&full[i % kTileStages], (i / kTileStages) & 1, a.timeout_ns);
+        }
+        return;
+    }
+
+    // ---------------- consumers -----------------------------------------------------
+    uint32_t it = 0;
+    for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++it) {
+        const int s = it % kTileStages;
+        if (!mbar_wait(&full[s], (it / kTileStages) & 1, a.timeout_ns)) {
+            if (lane == 0) report(a.status, TL_ERR_TIMEOUT);
+            break;
+        }
+        const TileCtx c = make_ctx<EB>(t, a);
+        consume<EB>(smem_addr(smem + s * kTileBytes), c, warp, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+}
+
+}  // namespace
+
+int tile_smem_bytes() { return kTileStages * kTileBytes + 1024; }
+
+template <int EB>
+const void* tile_kernel() {
+    return reinterpret_cast<const void*>(&k_tile<EB>);
+}
+
+template <int EB>
+cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st) {
+    k_tile<EB><<<grid, kTileThreads, tile_smem_bytes(), st>>>(map, a);
+    return cudaGetLastError();
+}
+
+#define TL_INST(EB)                                                                         \
+    template const void* tile_kernel<EB>();                                                 \
+    template cudaError_t launch_tile<EB>(const CUtensorMap&, const TileArgs&, int, cudaStream_t);
+TL_INST(1)
+TL_INST(2)
+TL_INST(4)
+TL_INST(8)
+TL_INST(16)
+#undef TL_INST
+
+}  // namespace tl

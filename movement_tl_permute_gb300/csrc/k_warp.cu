@@ -1,0 +1,101 @@
+// k_warp.cu -- the warp register-staged permute of the TVM "permute_layout" page
+// ("Algorithm", step 3), one warp tile per batch item.
+//
+// A tile holds 32 * P elements.  In iteration r lane l handles iteration index
+// j = r ^ ((l >> shift) & mask), whose coordinates are the row-major
+// decomposition of l + 32 * j over the tile extent: phase 1 reads all P elements
+// through the src strides into registers, the warp synchronises, phase 2 writes
+// them through the dst strides, and the warp synchronises again.  The (shift,
+// mask) pair comes from the host bank simulator so that both phases are
+// shared-memory bank-conflict-free, and because every read of a tile precedes its
+// writes the kernel is correct in place (src == dst, equal per-tile footprints).
+#include "tl_kernels.h"
+
+namespace tl {
+namespace {
+
+__device__ __forceinline__ void tile_offsets(int64_t f, const WarpArgs& a, int64_t& so,
+                                             int64_t& d) {
+    so = 0;
+    d = 0;
+#pragma unroll
+    for (int i = 3; i >= 0; --i) {
+        if (i < a.tn) {
+            const int64_t c = f % a.text[i];
+            f /= a.text[i];
+            so += c * a.tss[i];
+            d += c * a.tds[i];
+        }
+    }
+}
+
+template <int EB, int P>
+__global__ void __launch_bounds__(128) k_warp(const WarpArgs a) {
+    using T = typename dev::Bits<EB>::T;
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t item = gw; item < a.items; item += nw) {
+        int64_t sb = 0, db = 0, rem = item;
+#pragma unroll
+        for (int i = TL_MAX_DIMS - 1; i >= 0; --i) {
+            if (i < a.bn) {
+                const int64_t c = rem % a.bext[i];
+                rem /= a.bext[i];
+                sb += c * a.bss[i];
+                db += c * a.bds[i];
+            }
+        }
+        T regs[P];
+#pragma unroll
+        for (int r = 0; r < P; ++r) {                     // phase 1: read via src layout
+            const int j = r ^ ((lane >> a.shift) & a.mask);
+            int64_t so, d;
+            tile_offsets(lane + 32LL * j, a, so, d);
+            regs[r] = *reinterpret_cast<const T*>(a.src + (sb + so) * EB);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < P; ++r) {                     // phase 2: write via dst layout
+            const int j = r ^ ((lane >> a.shift) & a.mask);
+            int64_t so, d;
+            tile_offsets(lane + 32LL * j, a, so, d);
+            *reinterpret_cast<T*>(a.dst + (db + d) * EB) = regs[r];
+        }
+        __syncwarp();
+    }
+}
+
+template <int EB, int P>
+cudaError_t go(const WarpArgs& a, int grid, int block, cudaStream_t st) {
+    k_warp<EB, P><<<grid, block, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int EB>
+cudaError_t by_p(int P, const WarpArgs& a, int grid, int block, cudaStream_t st) {
+    switch (P) {
+    case 1: return go<EB, 1>(a, grid, block, st);
+    case 2: return go<EB, 2>(a, grid, block, st);
+    case 4: return go<EB, 4>(a, grid, block, st);
+    case 8: return go<EB, 8>(a, grid, block, st);
+    case 16: if constexpr (EB <= 8) return go<EB, 16>(a, grid, block, st); break;
+    case 32: if constexpr (EB <= 4) return go<EB, 32>(a, grid, block, st); break;
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_warp(int eb, int P, const WarpArgs& a, int grid, int block, cudaStream_t st) {
+    switch (eb) {
+    case 1: return by_p<1>(P, a, grid, block, st);
+    case 2: return by_p<2>(P, a, grid, block, st);
+    case 4: return by_p<4>(P, a, grid, block, st);
+    case 8: return by_p<8>(P, a, grid, block, st);
+    case 16: return by_p<16>(P, a, grid, block, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tl

@@ -1,0 +1,259 @@
+// tile_common.cuh -- pieces shared by the TMA tile transpose (k_tile.cu) and its
+// 2-CTA cluster variant (k_cluster.cu): the 128-byte swizzle address, the
+// bank-conflict-free column reads of a 128 x 128-byte tile, the 16-byte run
+// stores with ragged-edge masking, and the tile-order decode.
+//
+// Shared-memory column reads are made bank-conflict-free the way the TVM
+// "permute_layout" page makes its warp permute conflict-free ("Algorithm", step
+// 2): lanes that would hit the same bank visit their registers in an order
+// XOR-rotated by a field of their lane index.  With the TMA 128-byte swizzle a
+// 16-byte chunk c of row r sits at chunk c ^ (r & 7), so the 8 lane groups of a
+// warp must read rows with 8 distinct (r & 7); group g reads its k-th row as
+// (k ^ x_g), and the registers are put back in order with a conditional-swap
+// network before the stores.  The host bank simulator (tl_bank_conflicts)
+// reproduces these access patterns in the unit tests.
+#pragma once
+
+#include "tl_device.cuh"
+#include "tl_kernels.h"
+
+namespace tl {
+namespace tile {
+
+using namespace dev;
+
+constexpr int kRows = 128;            // tile rows (b)
+constexpr int kRowBytes = 128;        // tile row bytes (a)
+constexpr int kTileBytes = kRows * kRowBytes;
+constexpr int kConsumerWarps = 8;
+
+// Byte address (relative to the tile) of byte `col` of row `row` under the
+// 128-byte TMA swizzle: 16-byte chunk index XOR (row mod 8).
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t col) {
+    return row * kRowBytes + ((((col >> 4) ^ row) & 7u) << 4) + (col & 15u);
+}
+
+template <typename T>
+__device__ __forceinline__ void cswap(bool p, T& a, T& b) {
+    T x = p ? b : a;
+    T y = p ? a : b;
+    a = x;
+    b = y;
+}
+
+// Element e (EB bytes) of a 16-byte vector.
+template <int EB>
+__device__ __forceinline__ void store_elem(uint8_t* p, const uint4& v, int e) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if constexpr (EB == 16) {
+        *reinterpret_cast<uint4*>(p) = v;
+    } else if constexpr (EB == 8) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(w[2 * e], w[2 * e + 1]);
+    } else if constexpr (EB == 4) {
+        *reinterpret_cast<uint32_t*>(p) = w[e];
+    } else if constexpr (EB == 2) {
+        *reinterpret_cast<uint16_t*>(p) = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+    } else {
+        *p = (uint8_t)(w[e >> 2] >> (8 * (e & 3)));
+    }
+}
+
+struct TileCtx {
+    uint8_t* dst;
+    int64_t ext_a, ext_b, ds_a;
+    int64_t dst_base;      // element offset of the tile's (a0, b0) in dst
+    int64_t a0, b0;
+    bool vec;
+};
+
+// Stores the 16-byte run (16/EB consecutive b) at column a, starting at row b.
+template <int EB>
+__device__ __forceinline__ void put(const TileCtx& c, int64_t a, int64_t b, const uint4& v) {
+    constexpr int V = 16 / EB;
+    if (a >= c.ext_a || b >= c.ext_b) return;
+    const int64_t off = c.dst_base + (a - c.a0) * c.ds_a + (b - c.b0);
+    uint8_t* p = c.dst + off * EB;
+    if (c.vec && b + V <= c.ext_b) {
+        stg128(p, v);
+    } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e)
+            if (b + e < c.ext_b) store_elem<EB>(p + e * EB, v, e);
+    }
+}
+
+// Consumer work for one tile: every warp handles its share of the tile.
+template <int EB>
+__device__ __forceinline__ void consume(uint32_t tile, const TileCtx& c, int warp, int lane);
+
+template <>
+__device__ __forceinline__ void consume<4>(uint32_t tile, const TileCtx& c, int warp, int lane) {
+    // warp unit: 32 rows x 4 columns (one 16-byte chunk); 32 units per tile
+    const int cw = lane & 3, g = lane >> 2, x = (lane >> 3) & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int u = warp + kConsumerWarps * i;
+        const int cb = u & 7, rb = u >> 3;
+        const int col = 4 * cb + cw;
+        const int row0 = rb * 32 + 4 * g;
+        uint32_t r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) r[k] = lds32(tile + swz(row0 + (k ^ x), 4 * col));
+        cswap(x & 1, r[0], r[1]);
+        cswap(x & 1, r[2], r[3]);
+        cswap(x & 2, r[0], r[2]);
+        cswap(x & 2, r[1], r[3]);
+        put<4>(c, c.a0 + col, c.b0 + row0, make_uint4(r[0], r[1], r[2], r[3]));
+    }
+}
+
+template <>
+__device__ __forceinline__ void consume<8>(uint32_t tile, const TileCtx& c, int warp, int lane) {
+    // warp unit: 32 rows x 2 columns; half-warp wavefronts of 16 lanes
+    const int cw = lane & 1, g = lane >> 1, x = (lane >> 3) & 1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int u = warp + kConsumerWarps * i;
+        const int cb = u & 7, rb = u >> 3;
+        const int col = 2 * cb + cw;
+        const int row0 = rb * 32 + 2 * g;
+        uint2 r0 = lds64(tile + swz(row0 + x, 8 * col));
+        uint2 r1 = lds64(tile + swz(row0 + (1 ^ x), 8 * col));
+        cswap(x != 0, r0, r1);
+        put<8>(c, c.a0 + col, c.b0 + row0, make_uint4(r0.x, r0.y, r1.x, r1.y));
+    }
+}
+
+template <>
+__device__ __forceinline__ void consume<16>(uint32_t tile, const TileCtx& c, int warp, int lane) {
+    // warp unit: 32 rows x 1 column; quarter-warp wavefronts read 8 distinct chunks
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int u = warp + kConsumerWarps * i;
+        const int cb = u & 7, rb = u >> 3;
+        const int row = rb * 32 + lane;
+        uint4 v = lds128(tile + swz(row, 16 * cb));
+        put<16>(c, c.a0 + cb, c.b0 + row, v);
+    }
+}
+
+template <>
+__device__ __forceinline__ void consume<2>(uint32_t tile, const TileCtx& c, int warp, int lane) {
+    // warp unit: 64 rows x 4 words (8 columns); 16 units per tile
+    const int cw = lane & 3, g = lane >> 2, x = g;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int u = warp + kConsumerWarps * i;
+        const int cb = u & 7, rb = u >> 3;
+        const int word = 4 * cb + cw;
+        const int row0 = rb * 64 + 8 * g;
+        uint32_t r[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) r[k] = lds32(tile + swz(row0 + (k ^ x), 4 * word));
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) cswap(x & 1, r[k], r[k + 1]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (!(k & 2)) cswap(x & 2, r[k], r[k + 2]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cswap(x & 4, r[k], r[k + 4]);
+        uint4 lo, hi;
+        lo.x = __byte_perm(r[0], r[1], 0x5410); hi.x = __byte_perm(r[0], r[1], 0x7632);
+        lo.y = __byte_perm(r[2], r[3], 0x5410); hi.y = __byte_perm(r[2], r[3], 0x7632);
+        lo.z = __byte_perm(r[4], r[5], 0x5410); hi.z = __byte_perm(r[4], r[5], 0x7632);
+        lo.w = __byte_perm(r[6], r[7], 0x5410); hi.w = __byte_perm(r[6], r[7], 0x7632);
+        const int64_t a = c.a0 + 2 * word, b = c.b0 + row0;
+        put<2>(c, a, b, lo);
+        put<2>(c, a + 1, b, hi);
+    }
+}
+
+template <>
+__device__ __forceinline__ void consume<1>(uint32_t tile, const TileCtx& c, int warp, int lane) {
+    // warp unit: 128 rows x 4 words (16 columns); 8 units per tile, one per warp
+    const int cw = lane & 3, g = lane >> 2, x = g;
+    const int cb = warp;
+    const int word = 4 * cb + cw;
+    const int row0 = 16 * g;
+    uint32_t r[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) r[k] = lds32(tile + swz(row0 + (k ^ x), 4 * word));
+#pragma unroll
+    for (int k = 0; k < 16; k += 2) cswap(x & 1, r[k], r[k + 1]);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        if (!(k & 2)) cswap(x & 2, r[k], r[k + 2]);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        if (!(k & 4)) cswap(x & 4, r[k], r[k + 4]);
+    // 4x4 byte transposes: out[cc] word q = byte cc of rows 4q .. 4q+3
+    uint32_t o[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t lo01 = __byte_perm(r[4 * q], r[4 * q + 1], 0x5140);
+        const uint32_t lo23 = __byte_perm(r[4 * q + 2], r[4 * q + 3], 0x5140);
+        const uint32_t hi01 = __byte_perm(r[4 * q], r[4 * q + 1], 0x7362);
+        const uint32_t hi23 = __byte_perm(r[4 * q + 2], r[4 * q + 3], 0x7362);
+        o[0][q] = __byte_perm(lo01, lo23, 0x5410);
+        o[1][q] = __byte_perm(lo01, lo23, 0x7632);
+        o[2][q] = __byte_perm(hi01, hi23, 0x5410);
+        o[3][q] = __byte_perm(hi01, hi23, 0x7632);
+    }
+    const int64_t a = c.a0 + 4 * word, b = c.b0 + row0;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+        put<1>(c, a + cc, b, make_uint4(o[cc][0], o[cc][1], o[cc][2], o[cc][3]));
+}
+
+// Tile t -> (ta, tb, batch coordinates).  Within a batch item tiles are visited in
+// groups of `group_b` tile rows, b fastest inside a group, so concurrently
+// running CTAs read and write runs of several 128-byte lines.
+struct TileCoord {
+    int64_t ta, tb;
+    int64_t bc[3];
+};
+
+__device__ __forceinline__ TileCoord tile_coord(int64_t t, const TileArgs& a) {
+    TileCoord r;
+    const int64_t per_item = a.tiles_a * a.tiles_b;
+    int64_t item = t / per_item;
+    const int64_t local = t - item * per_item;
+    const int64_t grp = local / (a.group_b * a.tiles_a);
+    const int64_t first_tb = grp * a.group_b;
+    const int64_t gsize = min(a.group_b, a.tiles_b - first_tb);
+    const int64_t in_grp = local - grp * a.group_b * a.tiles_a;
+    r.tb = first_tb + in_grp % gsize;
+    r.ta = in_grp / gsize;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        r.bc[i] = 0;
+        if (i < a.nbatch) {
+            r.bc[i] = item % a.bext[i];
+            item /= a.bext[i];
+        }
+    }
+    return r;
+}
+
+
+// Destination context of tile t.
+template <int EB>
+__device__ __forceinline__ TileCtx make_ctx(int64_t t, const TileArgs& a) {
+    const TileCoord tc = tile_coord(t, a);
+    TileCtx c;
+    c.dst = a.dst;
+    c.ext_a = a.ext_a;
+    c.ext_b = a.ext_b;
+    c.ds_a = a.ds_a;
+    c.a0 = tc.ta * (kRowBytes / EB);
+    c.b0 = tc.tb * kRows;
+    c.vec = a.vec_store != 0;
+    int64_t base = c.a0 * a.ds_a + c.b0;
+#pragma unroll
+    for (int i = 0; i < 3; ++i) base += tc.bc[i] * a.bds[i];
+    c.dst_base = base;
+    return c;
+}
+
+}  // namespace tile
+}  // namespace tl

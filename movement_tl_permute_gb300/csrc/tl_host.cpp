@@ -1,0 +1,524 @@
+// tl_host.cpp -- host-side layout logic of the permute library: validation,
+// canonicalisation, the shared-memory bank simulator with its XOR-swizzle search,
+// and the planner that picks a kernel path.  No CUDA calls in this file.
+//
+// A layout maps coordinate c to offset + sum c[i]*stride[i] (TVM docs, "Buffers
+// and memory", section "Declaring buffers").  The warp path follows the TVM
+// "permute_layout" page, section "Algorithm": align the two layouts, pick the
+// XOR swizzle that keeps both phases bank-conflict-free, stage through registers.
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "tl_internal.h"
+
+namespace tl {
+namespace {
+
+bool valid_eb(int eb) { return eb == 1 || eb == 2 || eb == 4 || eb == 8 || eb == 16; }
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
+bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow(a, b, out); }
+
+// Highest offset a layout reaches (all strides >= 0); false on overflow.
+bool layout_span(int n, const int64_t* ext, const int64_t* str, int64_t* span) {
+    int64_t acc = 0;
+    for (int i = 0; i < n; ++i) {
+        if (ext[i] == 0) { *span = -1; return true; }
+        int64_t t;
+        if (!mul_ok(ext[i] - 1, str[i], &t) || !add_ok(acc, t, &acc)) return false;
+    }
+    *span = acc;
+    return true;
+}
+
+// Merge adjacent axes (outer i, inner i+1) where both sides are contiguous across
+// them, after dropping extent-1 axes.  Order is kept.
+void drop_and_merge(const Axes& in, Axes* out) {
+    Axes r;
+    for (int i = 0; i < in.n; ++i) {
+        if (in.ext[i] == 1) continue;
+        if (r.n > 0 && r.ss[r.n - 1] == in.ext[i] * in.ss[i] &&
+            r.ds[r.n - 1] == in.ext[i] * in.ds[i]) {
+            r.ext[r.n - 1] *= in.ext[i];
+            r.ss[r.n - 1] = in.ss[i];
+            r.ds[r.n - 1] = in.ds[i];
+        } else {
+            r.ext[r.n] = in.ext[i];
+            r.ss[r.n] = in.ss[i];
+            r.ds[r.n] = in.ds[i];
+            ++r.n;
+        }
+    }
+    *out = r;
+}
+
+// Sufficient test that a layout never maps two coordinates onto one element:
+// with axes sorted by stride, each stride exceeds everything the smaller axes reach.
+bool non_overlapping(int n, const int64_t* ext, const int64_t* str) {
+    int idx[kMaxDims];
+    int m = 0;
+    for (int i = 0; i < n; ++i)
+        if (ext[i] > 1) idx[m++] = i;
+    std::sort(idx, idx + m, [&](int a, int b) { return str[a] < str[b]; });
+    int64_t reach = 0;
+    for (int t = 0; t < m; ++t) {
+        int i = idx[t];
+        if (str[i] <= reach) return false;
+        int64_t step;
+        if (!mul_ok(ext[i] - 1, str[i], &step) || !add_ok(reach, step, &reach)) return false;
+    }
+    return true;
+}
+
+// Row-major coordinates of flat index f within ext[0..n).
+void decompose(int64_t f, int n, const int64_t* ext, int64_t* coord) {
+    for (int i = n - 1; i >= 0; --i) {
+        coord[i] = f % ext[i];
+        f /= ext[i];
+    }
+}
+
+int64_t dot(int n, const int64_t* c, const int64_t* s) {
+    int64_t o = 0;
+    for (int i = 0; i < n; ++i) o += c[i] * s[i];
+    return o;
+}
+
+// Offsets of one phase, iteration r, for all 32 lanes.
+void phase_offsets(int n, const int64_t* ext, const int64_t* str, int r, int shift, int mask,
+                   int64_t* out) {
+    int64_t coord[kMaxDims];
+    for (int lane = 0; lane < 32; ++lane) {
+        int j = r ^ ((lane >> shift) & mask);
+        decompose(lane + 32LL * j, n, ext, coord);
+        out[lane] = dot(n, coord, str);
+    }
+}
+
+bool phase_free(int n, const int64_t* ext, const int64_t* str, int P, int eb, int shift,
+                int mask) {
+    int64_t offs[32];
+    for (int r = 0; r < P; ++r) {
+        phase_offsets(n, ext, str, r, shift, mask, offs);
+        if (bank_degree(32, offs, eb, false) > 1) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+int bank_degree(int n_lanes, const int64_t* lane_offsets, int eb, bool hardware) {
+    const int per = eb <= 4 ? 32 : 128 / eb;   // lanes per 128-byte wavefront
+    int worst = 0;
+    for (int base = 0; base < n_lanes; base += per) {
+        // per bank: the lanes (conservative) or words (hardware) that touch it
+        int64_t members[32][32];
+        int count[32] = {0};
+        for (int lane = base; lane < std::min(n_lanes, base + per); ++lane) {
+            int64_t o = lane_offsets[lane];
+            if (o < 0) continue;
+            int64_t w0 = (o * eb) >> 2, w1 = (o * eb + eb - 1) >> 2;
+            for (int64_t w = w0; w <= w1; ++w) {
+                int bank = (int)(w & 31);
+                int64_t key = hardware ? w : lane;
+                bool seen = false;
+                for (int q = 0; q < count[bank]; ++q) seen |= members[bank][q] == key;
+                if (!seen) members[bank][count[bank]++] = key;
+            }
+        }
+        for (int b = 0; b < 32; ++b) worst = std::max(worst, count[b]);
+    }
+    return worst;
+}
+
+int choose_xor(int n, const int64_t* ext, const int64_t* ss, const int64_t* ds, int eb, int* k,
+               int* shift, int* mask) {
+    if (n < 1 || n > kMaxDims) return TL_ERR_ARG;
+    if (!valid_eb(eb)) return TL_ERR_ELEM_BYTES;
+    int64_t total = 1;
+    for (int i = 0; i < n; ++i) {
+        if (ext[i] < 0) return TL_ERR_ARG;
+        if (!mul_ok(total, ext[i], &total)) return TL_ERR_EXTENT;
+    }
+    if (total == 0 || total % 32 != 0 || total / 32 > 1024) return TL_ERR_EXTENT;
+    const int P = (int)(total / 32);
+    const bool pow2 = (P & (P - 1)) == 0;
+    int kmax = 0;
+    if (pow2)
+        while ((1 << (kmax + 1)) <= P) ++kmax;
+    for (int kk = 0; kk <= kmax; ++kk) {
+        const int m = (1 << kk) - 1;
+        for (int sh = 0; sh <= (kk == 0 ? 0 : 5 - kk); ++sh) {
+            if (phase_free(n, ext, ss, P, eb, sh, m) && phase_free(n, ext, ds, P, eb, sh, m)) {
+                *k = kk;
+                *shift = sh;
+                *mask = m;
+                return TL_OK;
+            }
+        }
+    }
+    return TL_ERR_NO_VALID_K;
+}
+
+// ---------------------------------------------------------------------------
+// Planner
+// ---------------------------------------------------------------------------
+namespace {
+
+int64_t abs_addr(const void* p) { return (int64_t)(uintptr_t)p; }
+
+bool aligned(int64_t v, int64_t a) { return a <= 1 || v % a == 0; }
+
+// Order-kept canonical pair and its warp tile: the smallest innermost suffix that
+// holds a whole number of warp iterations and admits a swizzle.
+bool plan_warp(Plan* p) {
+    const Axes& kept = p->kept;
+    if (kept.n == 0) return false;
+    int64_t prod = 1;
+    for (int start = kept.n - 1; start >= 0; --start) {
+        prod *= kept.ext[start];
+        if (prod > 32LL * 32) break;
+        int tdims = kept.n - start;
+        if (tdims > kMaxWarpTileDims) break;
+        if (prod % 32 != 0) continue;
+        int P = (int)(prod / 32);
+        if (P * p->eb > kWarpMaxRegBytes || (P & (P - 1)) != 0) continue;
+        int k, sh, m;
+        if (choose_xor(tdims, kept.ext + start, kept.ss + start, kept.ds + start, p->eb, &k, &sh,
+                       &m) != TL_OK)
+            continue;
+        Axes t, b;
+        for (int i = start; i < kept.n; ++i) {
+            t.ext[t.n] = kept.ext[i]; t.ss[t.n] = kept.ss[i]; t.ds[t.n] = kept.ds[i]; ++t.n;
+        }
+        for (int i = 0; i < start; ++i) {
+            b.ext[b.n] = kept.ext[i]; b.ss[b.n] = kept.ss[i]; b.ds[b.n] = kept.ds[i]; ++b.n;
+        }
+        p->wtile = t;
+        p->wbatch = b;
+        p->P = P;
+        p->k = k;
+        p->shift = sh;
+        p->mask = m;
+        return true;
+    }
+    return false;
+}
+
+// In place is only safe on the warp path, with identical pointers, identical
+// batch strides and each tile reading exactly the elements it writes.
+bool warp_in_place_ok(const Plan& p) {
+    for (int i = 0; i < p.wbatch.n; ++i)
+        if (p.wbatch.ss[i] != p.wbatch.ds[i]) return false;
+    const Axes& t = p.wtile;
+    int64_t total = 32LL * p.P;
+    std::vector<int64_t> a(total), b(total);
+    int64_t coord[kMaxDims];
+    for (int64_t f = 0; f < total; ++f) {
+        decompose(f, t.n, t.ext, coord);
+        a[f] = dot(t.n, coord, t.ss);
+        b[f] = dot(t.n, coord, t.ds);
+    }
+    std::sort(a.begin(), a.end());
+    std::sort(b.begin(), b.end());
+    return a == b;
+}
+
+// Plane of the transpose paths: b = dst-innermost axis (dst stride 1), a = the
+// src-contiguous axis (src stride 1), everything else batch.
+bool plan_plane(Plan* p) {
+    const Axes& s = p->sorted;
+    if (s.n < 2) return false;
+    const int b = s.n - 1;
+    if (s.ds[b] != 1 || s.ss[b] == 1) return false;
+    int a = -1;
+    for (int i = 0; i < s.n - 1; ++i)
+        if (s.ss[i] == 1) { a = i; break; }
+    if (a < 0 || s.n - 2 > kMaxBatch) return false;
+    p->ext_a = s.ext[a];
+    p->ext_b = s.ext[b];
+    p->ss_b = s.ss[b];
+    p->ds_a = s.ds[a];
+    Axes bt;
+    int64_t bt_total = 1;
+    for (int i = 0; i < s.n - 1; ++i) {
+        if (i == a) continue;
+        bt.ext[bt.n] = s.ext[i]; bt.ss[bt.n] = s.ss[i]; bt.ds[bt.n] = s.ds[i]; ++bt.n;
+        bt_total *= s.ext[i];
+    }
+    p->batch = bt;
+    p->batch_total = bt_total;
+    return true;
+}
+
+bool rows_ok(const Plan& p, int64_t src, int64_t dst) {
+    const int eb = p.eb;
+    const int64_t R = p.ext_b;
+    const int64_t rw = R * eb;
+    if (R < 2 || rw > 16 || 16 % rw != 0) return false;
+    if (p.ds_a != R) return false;                       // dense plane in dst
+    if ((p.ext_a * eb) % 16 != 0) return false;          // whole 16-byte row pieces
+    if ((p.ss_b * eb) % 16 != 0 || src % 16 || dst % 16) return false;
+    for (int i = 0; i < p.batch.n; ++i)
+        if ((p.batch.ss[i] * eb) % 16 || (p.batch.ds[i] * eb) % 16) return false;
+    return true;
+}
+
+bool tile_ok(const Plan& p, int64_t src) {
+    const int eb = p.eb;
+    if (p.batch.n > kMaxTmaBatch) return false;
+    if (src % 16 != 0) return false;
+    if ((p.ss_b * eb) % 16 != 0) return false;
+    const int64_t lim_coord = (1LL << 31) - 1, lim_stride = 1LL << 40;
+    if (p.ext_a * eb > lim_coord || p.ext_b > lim_coord) return false;
+    if (p.ss_b * eb >= lim_stride) return false;
+    for (int i = 0; i < p.batch.n; ++i) {
+        if ((p.batch.ss[i] * eb) % 16 != 0 || p.batch.ss[i] * eb >= lim_stride) return false;
+        if (p.batch.ext[i] > lim_coord) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
+              const int64_t* src_strides, const int64_t* dst_strides, int eb, uint32_t flags,
+              int64_t src_bytes, int64_t dst_bytes, Plan* plan) {
+    Plan p;
+    if (!valid_eb(eb)) return TL_ERR_ELEM_BYTES;
+    if (ndim < 0 || ndim > kMaxDims) return TL_ERR_ARG;
+    if (ndim > 0 && (!shape || !src_strides || !dst_strides)) return TL_ERR_ARG;
+    const uint32_t forced = flags & TL_PATH_MASK;
+    if (forced > TL_PATH_CLUSTER) return TL_ERR_ARG;
+    p.eb = eb;
+    int64_t total = 1;
+    for (int i = 0; i < ndim; ++i) {
+        if (shape[i] < 0 || src_strides[i] < 0 || dst_strides[i] < 0) return TL_ERR_ARG;
+        if (!mul_ok(total, shape[i], &total)) return TL_ERR_RANGE;
+    }
+    p.total = total;
+    if (total == 0) {           // nothing to move
+        *plan = p;
+        return TL_OK;
+    }
+    if (!src || !dst) return TL_ERR_ARG;
+    const int align = eb < 16 ? eb : 16;
+    if (!aligned(abs_addr(src), align) || !aligned(abs_addr(dst), align)) return TL_ERR_ALIGN;
+
+    int64_t sspan, dspan;
+    if (!layout_span(ndim, shape, src_strides, &sspan) ||
+        !layout_span(ndim, shape, dst_strides, &dspan))
+        return TL_ERR_RANGE;
+    int64_t sbytes, dbytes;
+    if (!mul_ok(sspan + 1, eb, &sbytes) || !mul_ok(dspan + 1, eb, &dbytes)) return TL_ERR_RANGE;
+    if ((src_bytes > 0 && sbytes > src_bytes) || (dst_bytes > 0 && dbytes > dst_bytes))
+        return TL_ERR_BOUNDS;
+    if (!non_overlapping(ndim, shape, dst_strides)) return TL_ERR_DST_OVERLAP;
+
+    // canonical forms
+    Axes raw;
+    raw.n = ndim;
+    for (int i = 0; i < ndim; ++i) {
+        raw.ext[i] = shape[i]; raw.ss[i] = src_strides[i]; raw.ds[i] = dst_strides[i];
+    }
+    drop_and_merge(raw, &p.kept);
+    Axes srt;
+    {
+        int idx[kMaxDims], m = 0;
+        for (int i = 0; i < ndim; ++i)
+            if (shape[i] != 1) idx[m++] = i;
+        std::stable_sort(idx, idx + m, [&](int a, int b) {
+            if (dst_strides[a] != dst_strides[b]) return dst_strides[a] > dst_strides[b];
+            return src_strides[a] > src_strides[b];
+        });
+        Axes t;
+        t.n = m;
+        for (int q = 0; q < m; ++q) {
+            t.ext[q] = shape[idx[q]]; t.ss[q] = src_strides[idx[q]]; t.ds[q] = dst_strides[idx[q]];
+        }
+        drop_and_merge(t, &srt);
+    }
+    p.sorted = srt;
+
+    const int64_t s0 = abs_addr(src), d0 = abs_addr(dst);
+    const bool ranges_meet = s0 < d0 + dbytes && d0 < s0 + sbytes;
+
+    // eligibility of every path
+    const bool warp_ok = plan_warp(&p);
+    bool chunk_ok = false;
+    if (srt.n == 0 || (srt.ds[srt.n - 1] == 1 && srt.ss[srt.n - 1] == 1)) chunk_ok = true;
+    const bool plane = plan_plane(&p);
+    const bool rows = plane && rows_ok(p, s0, d0);
+    const bool tile = plane && tile_ok(p, s0);
+
+    if (ranges_meet) {
+        if (!(s0 == d0 && warp_ok && warp_in_place_ok(p))) return TL_ERR_ALIAS;
+        if (forced != TL_PATH_AUTO && forced != TL_PATH_WARP) return TL_ERR_PATH;
+        p.in_place = true;
+        p.path = TL_PATH_WARP;
+        *plan = p;
+        return TL_OK;
+    }
+
+    int path = 0;
+    switch (forced) {
+    case TL_PATH_AUTO:
+        if (chunk_ok) path = TL_PATH_CHUNK;
+        else if (warp_ok && total <= 8192) path = TL_PATH_WARP;
+        else if (rows) path = TL_PATH_ROWS;
+        else if (tile) path = TL_PATH_TILE;
+        else path = TL_PATH_GENERIC;
+        break;
+    case TL_PATH_GENERIC: path = TL_PATH_GENERIC; break;
+    case TL_PATH_CHUNK: path = chunk_ok ? TL_PATH_CHUNK : 0; break;
+    case TL_PATH_WARP: path = warp_ok ? TL_PATH_WARP : 0; break;
+    case TL_PATH_ROWS: path = rows ? TL_PATH_ROWS : 0; break;
+    case TL_PATH_TILE: path = tile ? TL_PATH_TILE : 0; break;
+    case TL_PATH_CLUSTER: path = tile ? TL_PATH_CLUSTER : 0; break;
+    }
+    if (path == 0) return TL_ERR_PATH;
+    p.path = path;
+
+    if (path == TL_PATH_CHUNK) {
+        Axes o;
+        int64_t row = 1;
+        if (srt.n > 0) {
+            row = srt.ext[srt.n - 1];
+            for (int i = 0; i < srt.n - 1; ++i) {
+                o.ext[o.n] = srt.ext[i]; o.ss[o.n] = srt.ss[i]; o.ds[o.n] = srt.ds[i]; ++o.n;
+            }
+        }
+        p.row_elems = row;
+        p.outer = o;
+        p.rows = total / row;
+        int vb = 16;
+        auto fits = [&](int64_t v) { return v % vb == 0; };
+        while (vb > 1) {
+            bool ok = fits(row * eb) && fits(s0) && fits(d0);
+            for (int i = 0; i < o.n && ok; ++i) ok = fits(o.ss[i] * eb) && fits(o.ds[i] * eb);
+            if (ok) break;
+            vb >>= 1;
+        }
+        p.vec_bytes = vb;
+    } else if (path == TL_PATH_TILE || path == TL_PATH_CLUSTER) {
+        p.tile_cols = 128 / eb;
+        p.tile_rows = 128;
+        bool vs = (d0 % 16 == 0) && (p.ds_a * eb) % 16 == 0;
+        for (int i = 0; i < p.batch.n; ++i) vs = vs && (p.batch.ds[i] * eb) % 16 == 0;
+        p.vec_store = vs;
+        p.vec_bytes = vs ? 16 : eb;
+        const int64_t ta = (p.ext_a + p.tile_cols - 1) / p.tile_cols;
+        const int64_t tb = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
+        p.tiles = ta * tb * p.batch_total;
+    } else if (path == TL_PATH_ROWS) {
+        p.vec_bytes = 16;
+        p.tiles = p.batch_total * (p.ext_a * eb / 16);
+    } else if (path == TL_PATH_WARP) {
+        p.vec_bytes = eb;
+        int64_t nb = 1;
+        for (int i = 0; i < p.wbatch.n; ++i) nb *= p.wbatch.ext[i];
+        p.tiles = nb;
+    } else {
+        p.vec_bytes = eb;
+        p.tiles = total;
+    }
+    *plan = p;
+    return TL_OK;
+}
+
+}  // namespace tl
+
+// ---------------------------------------------------------------------------
+// C ABI: host-only entry points
+// ---------------------------------------------------------------------------
+extern "C" {
+
+int tl_layout_canon(const tl_layout* src, const tl_layout* dst, const int64_t* begin,
+                    const int64_t* extent, tl_layout* src_out, tl_layout* dst_out,
+                    int64_t* chunk_elems) {
+    using namespace tl;
+    if (!src || !dst || !src_out || !dst_out) return TL_ERR_ARG;
+    const int n = src->ndim;
+    if (n < 0 || n > kMaxDims || dst->ndim != n) return TL_ERR_ARG;
+    Axes sl;
+    sl.n = n;
+    int64_t so = src->offset, dof = dst->offset;
+    bool empty = false;
+    for (int i = 0; i < n; ++i) {
+        if (src->shape[i] != dst->shape[i] || src->shape[i] < 0) return TL_ERR_ARG;
+        const int64_t b = begin ? begin[i] : 0;
+        const int64_t e = extent ? extent[i] : src->shape[i] - b;
+        if (b < 0 || e < 0 || b + e > src->shape[i]) return TL_ERR_RANGE;
+        sl.ext[i] = e;
+        sl.ss[i] = src->stride[i];
+        sl.ds[i] = dst->stride[i];
+        int64_t t;
+        if (!mul_ok(b, src->stride[i], &t) || !add_ok(so, t, &so)) return TL_ERR_RANGE;
+        if (!mul_ok(b, dst->stride[i], &t) || !add_ok(dof, t, &dof)) return TL_ERR_RANGE;
+        empty |= e == 0;
+    }
+    tl_layout s{}, d{};
+    s.offset = so;
+    d.offset = dof;
+    int64_t chunk;
+    if (empty) {
+        s.ndim = d.ndim = 1;
+        s.shape[0] = d.shape[0] = 0;
+        s.stride[0] = d.stride[0] = 1;
+        chunk = 0;
+    } else {
+        Axes c;
+        drop_and_merge(sl, &c);
+        s.ndim = d.ndim = c.n;
+        for (int i = 0; i < c.n; ++i) {
+            s.shape[i] = d.shape[i] = c.ext[i];
+            s.stride[i] = c.ss[i];
+            d.stride[i] = c.ds[i];
+        }
+        if (c.n == 0) chunk = 1;
+        else if (c.ss[c.n - 1] == 1 && c.ds[c.n - 1] == 1) chunk = c.ext[c.n - 1];
+        else chunk = 0;
+    }
+    *src_out = s;
+    *dst_out = d;
+    if (chunk_elems) *chunk_elems = chunk;
+    return TL_OK;
+}
+
+int tl_choose_xor_k(int ndim, const int64_t* extent, const int64_t* src_str,
+                    const int64_t* dst_str, int elem_bytes, int* k, int* shift, int* mask) {
+    if (!extent || !src_str || !dst_str || !k || !shift || !mask) return TL_ERR_ARG;
+    return tl::choose_xor(ndim, extent, src_str, dst_str, elem_bytes, k, shift, mask);
+}
+
+int tl_bank_conflicts(int n_lanes, const int64_t* lane_offsets, int elem_bytes, int model) {
+    if (!lane_offsets || n_lanes < 0 || n_lanes > 32 || (model != 0 && model != 1))
+        return TL_ERR_ARG;
+    if (!tl::valid_eb(elem_bytes)) return TL_ERR_ELEM_BYTES;
+    return tl::bank_degree(n_lanes, lane_offsets, elem_bytes, model == 1);
+}
+
+const char* tl_status_string(int status) {
+    switch (status) {
+    case TL_OK: return "ok";
+    case TL_ERR_ARG: return "invalid argument";
+    case TL_ERR_ELEM_BYTES: return "element width must be 1, 2, 4, 8 or 16 bytes";
+    case TL_ERR_EXTENT: return "extent is not a whole number of warp iterations";
+    case TL_ERR_NO_VALID_K: return "no XOR swizzle makes both phases bank-conflict-free";
+    case TL_ERR_CHUNK: return "contiguous chunk is under 16 bytes or not a multiple of 16";
+    case TL_ERR_DST_OVERLAP: return "destination layout may map two coordinates to one element";
+    case TL_ERR_ALIAS: return "source and destination memory overlap";
+    case TL_ERR_ALIGN: return "pointer not aligned to the element width";
+    case TL_ERR_PATH: return "the requested kernel path does not apply to this layout";
+    case TL_ERR_RANGE: return "offset overflow or region outside the layout";
+    case TL_ERR_CUDA: return "CUDA call failed";
+    case TL_ERR_TIMEOUT: return "a bounded device-side wait expired";
+    case TL_ERR_BOUNDS: return "layout reaches outside the given buffer size";
+    default: return "unknown status";
+    }
+}
+
+int tl_version(void) { return TL_VERSION; }
+
+}  // extern "C"

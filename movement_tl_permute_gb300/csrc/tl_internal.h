@@ -1,0 +1,65 @@
+// tl_internal.h -- plan structures shared by the host planner (tl_host.cpp) and
+// the launch code (tl_launch.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/tl_permute.h"
+
+namespace tl {
+
+constexpr int kMaxDims = TL_MAX_DIMS;
+constexpr int kMaxBatch = 6;       // batch axes of the transpose paths
+constexpr int kMaxTmaBatch = 3;    // a TMA tensor map has at most 5 dims: a, b + 3 batch
+constexpr int kMaxWarpTileDims = 4;
+constexpr int kWarpMaxRegBytes = 128;  // P * elem_bytes a lane may stage in registers
+
+// A list of axes with per-side element strides.
+struct Axes {
+    int n = 0;
+    int64_t ext[kMaxDims] = {};
+    int64_t ss[kMaxDims] = {};
+    int64_t ds[kMaxDims] = {};
+};
+
+struct Plan {
+    int path = 0;          // TL_PATH_*; 0 with total == 0 means "nothing to do"
+    int eb = 0;            // element bytes
+    int64_t total = 0;     // elements
+    Axes sorted;           // unit axes dropped, sorted by dst stride (descending), merged
+    Axes kept;             // unit axes dropped, order kept, merged (the page's canon)
+
+    // CHUNK: rows of row_elems contiguous elements on both sides.
+    int64_t row_elems = 0;
+    int vec_bytes = 0;
+    Axes outer;            // axes outside the row, dst order
+    int64_t rows = 0;
+
+    // TILE / ROWS / CLUSTER: plane (b: dst-contiguous, a: src-contiguous) + batch.
+    int64_t ext_a = 0, ext_b = 0, ss_b = 0, ds_a = 0;
+    Axes batch;            // batch axes (outermost first)
+    int64_t batch_total = 1;
+    bool vec_store = false;  // 16-byte aligned dst runs
+    int tile_rows = 0, tile_cols = 0;
+    int64_t tiles = 0;
+
+    // WARP: tile (innermost suffix of `kept`) + batch of the outer `kept` axes.
+    Axes wtile;
+    Axes wbatch;
+    int P = 0, k = 0, shift = 0, mask = 0;
+    bool in_place = false;
+};
+
+// Validates the call and fills `plan`.  Pure host code, no CUDA calls.
+int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
+              const int64_t* src_strides, const int64_t* dst_strides, int elem_bytes,
+              uint32_t flags, int64_t src_bytes, int64_t dst_bytes, Plan* plan);
+
+// The bank simulator: worst conflict degree of one warp-wide access.
+int bank_degree(int n_lanes, const int64_t* lane_offsets, int elem_bytes, bool hardware);
+
+// XOR swizzle search of the warp path; returns TL_OK or a tl_status.
+int choose_xor(int n, const int64_t* ext, const int64_t* ss, const int64_t* ds, int eb,
+               int* k, int* shift, int* mask);
+
+}  // namespace tl

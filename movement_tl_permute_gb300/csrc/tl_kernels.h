@@ -1,0 +1,101 @@
+// tl_kernels.h -- kernel argument blocks and launch wrappers (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/tl_permute.h"
+#include "tl_device.cuh"
+
+namespace tl {
+
+// ---------------------------------------------------------------- generic
+struct GenericArgs {
+    const uint8_t* src;
+    uint8_t* dst;
+    int32_t n;
+    int32_t use32;               // 1: flat index and extents fit in 32 bits
+    int64_t total;
+    int64_t ext[TL_MAX_DIMS];
+    int64_t ss[TL_MAX_DIMS];     // elements
+    int64_t ds[TL_MAX_DIMS];
+    dev::DivU32 div[TL_MAX_DIMS];
+};
+template <int EB>
+cudaError_t launch_generic(const GenericArgs& a, int grid, int block, cudaStream_t st);
+
+// ---------------------------------------------------------------- chunk
+struct ChunkArgs {
+    const uint8_t* src;
+    uint8_t* dst;
+    int64_t rows;                // rows of contiguous bytes
+    int64_t vpr;                 // vectors per row
+    int32_t n;                   // outer axes
+    int32_t log2g;               // lanes per row group = 1 << log2g
+    int32_t use32;
+    int32_t pad;
+    int64_t ext[TL_MAX_DIMS];
+    int64_t ss[TL_MAX_DIMS];     // BYTES
+    int64_t ds[TL_MAX_DIMS];     // BYTES
+    dev::DivU32 div[TL_MAX_DIMS];
+};
+template <int VB>
+cudaError_t launch_chunk(const ChunkArgs& a, int grid, int block, cudaStream_t st);
+
+// ---------------------------------------------------------------- tile (TMA)
+constexpr int kTileStages = 4;
+constexpr int kTileThreads = 9 * 32;   // 8 consumer warps + 1 producer warp
+struct TileArgs {
+    uint8_t* dst;
+    int32_t* status;
+    int64_t ext_a, ext_b, ds_a;          // elements
+    int64_t tiles_a, tiles_b, tiles, group_b;
+    int32_t nbatch, rank, vec_store, pad;
+    int64_t bext[3];
+    int64_t bds[3];                      // dst strides of the batch axes, elements
+    uint64_t timeout_ns;
+};
+int tile_smem_bytes();
+template <int EB>
+const void* tile_kernel();
+template <int EB>
+cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st);
+
+// tile path with a 2-CTA cluster and a DSMEM hand-off (k_cluster.cu)
+int cluster_smem_bytes();
+const void* cluster_kernel(int eb);
+cudaError_t launch_cluster(int eb, const CUtensorMap& map, const TileArgs& a, int grid,
+                           cudaStream_t st);
+
+// ---------------------------------------------------------------- rows
+struct RowsArgs {
+    const uint8_t* src;
+    uint8_t* dst;
+    int64_t units;               // 16-byte source columns over all batch items
+    int64_t upr;                 // units per plane (ext_a * EB / 16)
+    int64_t ss_b;                // src stride of b, elements
+    int32_t n;                   // batch axes
+    int32_t use32;               // 1: unit index and extents fit in 32 bits
+    int64_t ext[TL_MAX_DIMS];
+    int64_t ss[TL_MAX_DIMS];     // elements
+    int64_t ds[TL_MAX_DIMS];
+    dev::DivU32 div_upr;
+    dev::DivU32 div[TL_MAX_DIMS];
+};
+cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, cudaStream_t st);
+
+// ---------------------------------------------------------------- warp
+struct WarpArgs {
+    const uint8_t* src;
+    uint8_t* dst;
+    int32_t tn, bn;              // tile axes, batch axes
+    int32_t shift, mask;
+    int64_t items;               // batch items (one warp tile each)
+    int64_t text[4], tss[4], tds[4];
+    int64_t bext[TL_MAX_DIMS], bss[TL_MAX_DIMS], bds[TL_MAX_DIMS];
+};
+cudaError_t launch_warp(int eb, int P, const WarpArgs& a, int grid, int block, cudaStream_t st);
+
+}  // namespace tl

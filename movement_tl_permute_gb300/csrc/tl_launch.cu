@@ -1,0 +1,382 @@
+// tl_launch.cu -- C ABI entry points that touch the GPU: tl_permute,
+// tl_permute_ex and tl_plan.  Validates and plans on the host (tl_host.cpp),
+// encodes the TMA tensor map for the tile path, sizes persistent grids from the
+// device's SM count and occupancy, and launches one kernel on the caller's stream.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "tl_internal.h"
+#include "tl_kernels.h"
+
+namespace tl {
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s per bounded wait
+constexpr uint64_t kTestTimeoutNs = 50000000ull;        // 50 ms under the test hook
+
+struct DevInfo {
+    bool ready = false;
+    int sms = 0;
+    int tile_occ[5] = {};      // CTAs per SM of k_tile<EB>, index log2(EB)
+    int cluster_occ[5] = {};
+};
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int log2i(int v) {
+    int l = 0;
+    while ((1 << l) < v) ++l;
+    return l;
+}
+
+int get_device_info(DevInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TL_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TL_ERR_CUDA;
+        const void* kt[5] = {tile_kernel<1>(), tile_kernel<2>(), tile_kernel<4>(),
+                             tile_kernel<8>(), tile_kernel<16>()};
+        for (int i = 0; i < 5; ++i) {
+            if (cudaFuncSetAttribute(kt[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     tile_smem_bytes()) != cudaSuccess)
+                return TL_ERR_CUDA;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.tile_occ[i], kt[i], kTileThreads,
+                                                              tile_smem_bytes()) != cudaSuccess)
+                return TL_ERR_CUDA;
+            const void* kc = cluster_kernel(1 << i);
+            if (cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     cluster_smem_bytes()) != cudaSuccess)
+                return TL_ERR_CUDA;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.cluster_occ[i], kc, kTileThreads,
+                                                              cluster_smem_bytes()) != cudaSuccess)
+                return TL_ERR_CUDA;
+        }
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return TL_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    *out = d;
+    return TL_OK;
+}
+
+// Batch axes of the plane, innermost (smallest dst stride) first.
+void batch_inner_first(const Plan& p, int64_t* ext, int64_t* ss, int64_t* ds) {
+    for (int i = 0; i < p.batch.n; ++i) {
+        const int j = p.batch.n - 1 - i;
+        ext[i] = p.batch.ext[j];
+        ss[i] = p.batch.ss[j];
+        ds[i] = p.batch.ds[j];
+    }
+}
+
+// Tensor map over the source plane: dim 0 = a in BYTES (raw bits, type UINT8),
+// dim 1 = b, dims 2.. = batch.  Box = 128 bytes x 128 rows, 128-byte swizzle.
+int encode_tile_map(const Plan& p, const void* src, CUtensorMap* map, int* rank) {
+    if (!g_encode) return TL_ERR_CUDA;
+    const int eb = p.eb;
+    cuuint64_t dims[5];
+    cuuint64_t strides[4];
+    cuuint32_t box[5], es[5] = {1, 1, 1, 1, 1};
+    int64_t bext[3] = {1, 1, 1}, bss[3] = {0, 0, 0}, bds[3] = {0, 0, 0};
+    batch_inner_first(p, bext, bss, bds);
+    dims[0] = (cuuint64_t)(p.ext_a * eb);
+    dims[1] = (cuuint64_t)p.ext_b;
+    strides[0] = (cuuint64_t)(p.ss_b * eb);
+    box[0] = 128;
+    box[1] = 128;
+    for (int i = 0; i < p.batch.n; ++i) {
+        dims[2 + i] = (cuuint64_t)bext[i];
+        strides[1 + i] = (cuuint64_t)(bss[i] * eb);
+        box[2 + i] = 1;
+    }
+    *rank = 2 + p.batch.n;
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)*rank,
+                          const_cast<void*>(src), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TL_OK : TL_ERR_CUDA;
+}
+
+int cap_grid(int64_t want, int64_t cap, int32_t max_ctas) {
+    int64_t g = want < cap ? want : cap;
+    if (max_ctas > 0 && g > max_ctas) g = max_ctas;
+    return (int)(g < 1 ? 1 : g);
+}
+
+struct Launch {
+    int grid = 0, block = 0, smem = 0;
+};
+
+// Launch shape of each path (grid 0 when the device is unknown).
+Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas) {
+    Launch l;
+    const int64_t sms = d ? d->sms : 0;
+    switch (p.path) {
+    case TL_PATH_GENERIC:
+        l.block = 256;
+        if (sms) l.grid = cap_grid((p.total + 255) / 256, sms * 8, max_ctas);
+        break;
+    case TL_PATH_CHUNK: {
+        l.block = 256;
+        const int64_t vpr = p.row_elems * p.eb / p.vec_bytes;
+        int g = 1;
+        while (g < 32 && g < vpr) g <<= 1;
+        const int64_t groups = 256 / g;
+        if (sms) l.grid = cap_grid((p.rows + groups * 4 - 1) / (groups * 4), sms * 8, max_ctas);
+        break;
+    }
+    case TL_PATH_TILE:
+        l.block = kTileThreads;
+        l.smem = tile_smem_bytes();
+        if (sms) l.grid = cap_grid(p.tiles, sms * d->tile_occ[log2i(p.eb)], max_ctas);
+        break;
+    case TL_PATH_CLUSTER:
+        l.block = kTileThreads;
+        l.smem = cluster_smem_bytes();
+        if (sms) {
+            const int64_t pairs = (p.tiles + 1) / 2;
+            int64_t cap = sms * d->cluster_occ[log2i(p.eb)] / 2;
+            if (cap < 1) cap = 1;
+            l.grid = 2 * cap_grid(pairs, cap, max_ctas > 0 ? (max_ctas + 1) / 2 : 0);
+        }
+        break;
+    case TL_PATH_ROWS:
+        l.block = 256;
+        if (sms) l.grid = cap_grid((p.tiles + 511) / 512, sms * 8, max_ctas);
+        break;
+    case TL_PATH_WARP:
+        l.block = 128;
+        if (sms) l.grid = cap_grid((p.tiles + 3) / 4, sms * 16, max_ctas);
+        break;
+    }
+    return l;
+}
+
+void fill_divs(int n, const int64_t* ext, dev::DivU32* div) {
+    for (int i = 0; i < n; ++i) div[i] = dev::make_divu32((uint32_t)ext[i]);
+}
+
+int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_t* ss,
+        const int64_t* ds, int eb, cudaStream_t st, const tl_permute_opts* opts) {
+    const uint32_t flags = opts ? opts->flags : 0u;
+    Plan p;
+    int rc = make_plan(src, dst, ndim, shape, ss, ds, eb, flags, opts ? opts->src_bytes : 0,
+                       opts ? opts->dst_bytes : 0, &p);
+    if (rc != TL_OK) return rc;
+    if (p.total == 0) return TL_OK;
+    DevInfo d;
+    rc = get_device_info(&d);
+    if (rc != TL_OK) return rc;
+    const int32_t max_ctas = opts ? opts->max_ctas : 0;
+    const Launch l = launch_shape(p, &d, max_ctas);
+    const uint8_t* s8 = static_cast<const uint8_t*>(src);
+    uint8_t* d8 = static_cast<uint8_t*>(dst);
+    cudaError_t err = cudaSuccess;
+
+    switch (p.path) {
+    case TL_PATH_GENERIC: {
+        GenericArgs a{};
+        a.src = s8;
+        a.dst = d8;
+        a.n = p.sorted.n;
+        a.total = p.total;
+        a.use32 = p.total < (1LL << 32) ? 1 : 0;
+        for (int i = 0; i < a.n; ++i) {
+            a.ext[i] = p.sorted.ext[i]; a.ss[i] = p.sorted.ss[i]; a.ds[i] = p.sorted.ds[i];
+        }
+        if (a.use32) fill_divs(a.n, a.ext, a.div);
+        switch (eb) {
+        case 1: err = launch_generic<1>(a, l.grid, l.block, st); break;
+        case 2: err = launch_generic<2>(a, l.grid, l.block, st); break;
+        case 4: err = launch_generic<4>(a, l.grid, l.block, st); break;
+        case 8: err = launch_generic<8>(a, l.grid, l.block, st); break;
+        default: err = launch_generic<16>(a, l.grid, l.block, st); break;
+        }
+        break;
+    }
+    case TL_PATH_CHUNK: {
+        ChunkArgs a{};
+        a.src = s8;
+        a.dst = d8;
+        a.rows = p.rows;
+        a.vpr = p.row_elems * eb / p.vec_bytes;
+        int g = 1, lg = 0;
+        while (g < 32 && g < a.vpr) { g <<= 1; ++lg; }
+        a.log2g = lg;
+        a.n = p.outer.n;
+        a.use32 = p.rows < (1LL << 32) ? 1 : 0;
+        for (int i = 0; i < a.n; ++i) {
+            a.ext[i] = p.outer.ext[i];
+            a.ss[i] = p.outer.ss[i] * eb;
+            a.ds[i] = p.outer.ds[i] * eb;
+        }
+        if (a.use32) fill_divs(a.n, a.ext, a.div);
+        switch (p.vec_bytes) {
+        case 16: err = launch_chunk<16>(a, l.grid, l.block, st); break;
+        case 8: err = launch_chunk<8>(a, l.grid, l.block, st); break;
+        case 4: err = launch_chunk<4>(a, l.grid, l.block, st); break;
+        case 2: err = launch_chunk<2>(a, l.grid, l.block, st); break;
+        default: err = launch_chunk<1>(a, l.grid, l.block, st); break;
+        }
+        break;
+    }
+    case TL_PATH_TILE:
+    case TL_PATH_CLUSTER: {
+        alignas(64) CUtensorMap map;
+        TileArgs a{};
+        rc = encode_tile_map(p, src, &map, &a.rank);
+        if (rc != TL_OK) return rc;
+        a.dst = d8;
+        a.status = opts ? opts->dev_status : nullptr;
+        a.ext_a = p.ext_a;
+        a.ext_b = p.ext_b;
+        a.ds_a = p.ds_a;
+        a.tiles_a = (p.ext_a + p.tile_cols - 1) / p.tile_cols;
+        a.tiles_b = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
+        a.tiles = p.tiles;
+        a.group_b = 8;
+        a.nbatch = p.batch.n;
+        a.vec_store = p.vec_store ? 1 : 0;
+        for (int i = 0; i < 3; ++i) { a.bext[i] = 1; a.bds[i] = 0; }
+        int64_t bss[3];
+        batch_inner_first(p, a.bext, bss, a.bds);
+        a.timeout_ns = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? kTestTimeoutNs : kDefaultTimeoutNs;
+        a.pad = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? 1 : 0;
+        if (p.path == TL_PATH_CLUSTER) {
+            err = launch_cluster(eb, map, a, l.grid, st);
+            break;
+        }
+        switch (eb) {
+        case 1: err = launch_tile<1>(map, a, l.grid, st); break;
+        case 2: err = launch_tile<2>(map, a, l.grid, st); break;
+        case 4: err = launch_tile<4>(map, a, l.grid, st); break;
+        case 8: err = launch_tile<8>(map, a, l.grid, st); break;
+        default: err = launch_tile<16>(map, a, l.grid, st); break;
+        }
+        break;
+    }
+    case TL_PATH_ROWS: {
+        RowsArgs a{};
+        a.src = s8;
+        a.dst = d8;
+        a.units = p.tiles;
+        a.upr = p.ext_a * eb / 16;
+        a.ss_b = p.ss_b;
+        a.n = p.batch.n;
+        a.use32 = p.tiles < (1LL << 32) ? 1 : 0;
+        for (int i = 0; i < a.n; ++i) {
+            a.ext[i] = p.batch.ext[i]; a.ss[i] = p.batch.ss[i]; a.ds[i] = p.batch.ds[i];
+        }
+        if (a.use32) {
+            a.div_upr = dev::make_divu32((uint32_t)a.upr);
+            fill_divs(a.n, a.ext, a.div);
+        }
+        err = launch_rows(eb, (int)p.ext_b, a, l.grid, l.block, st);
+        break;
+    }
+    case TL_PATH_WARP: {
+        WarpArgs a{};
+        a.src = s8;
+        a.dst = d8;
+        a.tn = p.wtile.n;
+        a.bn = p.wbatch.n;
+        a.shift = p.shift;
+        a.mask = p.mask;
+        a.items = p.tiles;
+        for (int i = 0; i < a.tn; ++i) {
+            a.text[i] = p.wtile.ext[i]; a.tss[i] = p.wtile.ss[i]; a.tds[i] = p.wtile.ds[i];
+        }
+        for (int i = 0; i < a.bn; ++i) {
+            a.bext[i] = p.wbatch.ext[i]; a.bss[i] = p.wbatch.ss[i]; a.bds[i] = p.wbatch.ds[i];
+        }
+        err = launch_warp(eb, p.P, a, l.grid, l.block, st);
+        break;
+    }
+    default:
+        return TL_ERR_PATH;
+    }
+    if (err != cudaSuccess) return TL_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return TL_OK;
+}
+
+}  // namespace
+}  // namespace tl
+
+extern "C" {
+
+int tl_permute(const void* src, void* dst, int ndim, const int64_t* shape,
+               const int64_t* src_strides, const int64_t* dst_strides, int elem_bytes,
+               tl_stream_t stream) {
+    return tl::run(src, dst, ndim, shape, src_strides, dst_strides, elem_bytes,
+                   reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+int tl_permute_ex(const void* src, void* dst, int ndim, const int64_t* shape,
+                  const int64_t* src_strides, const int64_t* dst_strides, int elem_bytes,
+                  tl_stream_t stream, const tl_permute_opts* opts) {
+    return tl::run(src, dst, ndim, shape, src_strides, dst_strides, elem_bytes,
+                   reinterpret_cast<cudaStream_t>(stream), opts);
+}
+
+int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
+            const int64_t* src_strides, const int64_t* dst_strides, int elem_bytes,
+            const tl_permute_opts* opts, tl_plan_info* out) {
+    using namespace tl;
+    if (!out) return TL_ERR_ARG;
+    Plan p;
+    const uint32_t flags = opts ? opts->flags : 0u;
+    int rc = make_plan(src, dst, ndim, shape, src_strides, dst_strides, elem_bytes, flags,
+                       opts ? opts->src_bytes : 0, opts ? opts->dst_bytes : 0, &p);
+    if (rc != TL_OK) return rc;
+    tl_plan_info info{};
+    info.path = p.path;
+    info.ndim = p.sorted.n;
+    for (int i = 0; i < p.sorted.n; ++i) {
+        info.extent[i] = p.sorted.ext[i];
+        info.src_str[i] = p.sorted.ss[i];
+        info.dst_str[i] = p.sorted.ds[i];
+    }
+    info.vec_bytes = p.vec_bytes;
+    info.in_place = p.in_place ? 1 : 0;
+    if (p.path == TL_PATH_WARP) {
+        info.k = p.k;
+        info.shift = p.shift;
+        info.mask = p.mask;
+    }
+    info.tile_rows = p.tile_rows;
+    info.tile_cols = p.tile_cols;
+    info.tiles = p.tiles;
+    int ndev = 0;
+    DevInfo d;
+    const bool have = p.total > 0 && cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0 &&
+                      get_device_info(&d) == TL_OK;
+    if (!have) cudaGetLastError();   // clear a "no device" error on CPU-only hosts
+    const Launch l = launch_shape(p, have ? &d : nullptr, opts ? opts->max_ctas : 0);
+    info.grid = l.grid;
+    info.block = l.block;
+    info.smem_bytes = l.smem;
+    *out = info;
+    return TL_OK;
+}
+
+uint64_t tl_launch_count(void) { return tl::g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,288 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, bit for bit.
+
+Every kernel path is forced in turn on seeded random layouts that span several
+tiles and end in ragged tails, for every element width.  Destination buffers
+carry canary bytes around and between the permuted elements: the oracle writes
+into an identical canary buffer, so a byte written outside the image (or a byte
+of the image left unwritten) fails the comparison.  Outputs are compared as raw
+bytes, so NaN payloads count.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import movement_tl_permute_gb300 as tl
+import oracle
+from movement_tl_permute_gb300 import workloads
+from oracle import layout_ref as L
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+MARGIN = 256          # canary bytes before the destination (keeps 256-byte alignment)
+CANARY = 0xA5
+NTHREADS = max(1, len(os.sched_getaffinity(0)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    from movement_tl_permute_gb300 import build
+    build.build()
+    oracle.build()
+    tl.load()
+    torch.cuda.init()
+
+
+def _span(shape, strides):
+    return sum((e - 1) * s for e, s in zip(shape, strides)) if all(e > 0 for e in shape) else -1
+
+
+def run_case(shape, ss, ds, eb, path="auto", seed=0, src_off=0, dst_off=0, **opts):
+    """Permute on the GPU and with the oracle; return (got, want) byte arrays."""
+    n_src = (src_off + _span(shape, ss) + 1) * eb
+    n_dst = MARGIN + (dst_off + _span(shape, ds) + 1) * eb + MARGIN
+    src = workloads.random_bits(max(16, n_src), seed)
+    want = np.full(n_dst, CANARY, dtype=np.uint8)
+    oracle.permute(src, want, shape, ss, ds, eb, src_offset=src_off,
+                   dst_offset=MARGIN // eb + dst_off, nthreads=NTHREADS)
+    s_gpu = torch.from_numpy(src).cuda()
+    d_gpu = torch.full((n_dst,), CANARY, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    tl.tl_permute_ex(s_gpu.data_ptr() + src_off * eb, d_gpu.data_ptr() + MARGIN + dst_off * eb,
+                     shape, ss, ds, eb, stream, path=path, **opts)
+    torch.cuda.synchronize()
+    return d_gpu.cpu().numpy(), want
+
+
+def check(shape, ss, ds, eb, path="auto", **kw):
+    got, want = run_case(shape, ss, ds, eb, path, **kw)
+    if not np.array_equal(got, want):
+        bad = np.nonzero(got != want)[0]
+        raise AssertionError("%d bytes differ (first at %d) for shape=%s ss=%s ds=%s eb=%d path=%s"
+                             % (bad.size, bad[0], shape, ss, ds, eb, path))
+
+
+def perm_layouts(shape, perm, pad=None):
+    ss = L.row_major_strides(shape)
+    pshape = tuple(shape[p] for p in perm)
+    pst = L.row_major_strides(pshape)
+    ds = [0] * len(shape)
+    for i, p in enumerate(perm):
+        ds[p] = pst[i]
+    return ss, tuple(ds)
+
+
+WIDTHS = [1, 2, 4, 8, 16]
+
+
+# ---------------------------------------------------------------------------
+# per-path parity on random small layouts
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("eb", WIDTHS)
+def test_generic_path(eb):
+    rng = np.random.default_rng(100 + eb)
+    for i in range(12):
+        nd = int(rng.integers(1, 6))
+        shape = tuple(int(x) for x in rng.integers(1, 9, size=nd))
+        perm = tuple(int(p) for p in rng.permutation(nd))
+        ss, ds = perm_layouts(shape, perm)
+        if i % 3 == 1:                          # padded source, offset views
+            ss = tuple(s * 2 + (1 if j == 0 else 0) for j, s in enumerate(ss))
+        check(shape, ss, ds, eb, "generic", seed=i, src_off=i % 3, dst_off=i % 2)
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
+def test_chunk_path(eb):
+    rng = np.random.default_rng(200 + eb)
+    for i in range(10):
+        inner = int(rng.choice([1, 3, 8, 16, 24, 64, 200]))
+        outer = tuple(int(x) for x in rng.integers(1, 7, size=int(rng.integers(1, 4))))
+        shape = outer + (inner,)
+        perm = tuple(int(p) for p in rng.permutation(len(outer))) + (len(outer),)
+        ss, ds = perm_layouts(shape, perm)
+        check(shape, ss, ds, eb, "chunk", seed=i, src_off=i % 2)
+    # one long contiguous run (a memcpy) and a large row count
+    check((100003,), (1,), (1,), eb, "chunk", seed=11)
+    check((37, 300, 16), (300 * 16, 16, 1), (16, 37 * 16, 1), eb, "chunk", seed=12)
+
+
+TILE_CASES = [
+    # (shape, ss, ds): 2-D transposes with ragged edges, batched tiles, 3-batch
+    ((300, 517), None, None),
+    ((128, 256), None, None),
+    ((1000, 48), None, None),
+    ((33, 1024), None, None),
+]
+
+
+def _tile_shapes(eb):
+    out = []
+    for rows, cols in ((300, 256), (128, 256), (1000, 64), (33, 1024), (257, 384)):
+        c = max(16 // eb, cols // eb) if eb > 1 else cols
+        c = (c + (16 // eb) - 1) // (16 // eb) * (16 // eb)      # src rows 16-byte aligned
+        out.append(((rows, c), (c, 1), (1, rows)))
+    # batched tiles and tiles inside a bigger batch structure
+    a = max(16 // eb, 64 // eb)
+    out.append(((5, 130, a), (130 * a, a, 1), (130 * a, 1, 130)))
+    out.append(((3, 2, 70, 2 * a), (2 * 70 * 2 * a, 70 * 2 * a, 2 * a, 1),
+                (2 * 70 * 2 * a, 70 * 2 * a, 1, 70)))
+    return out
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
+@pytest.mark.parametrize("path", ["tile", "cluster"])
+def test_tile_and_cluster_paths(eb, path):
+    for i, (shape, ss, ds) in enumerate(_tile_shapes(eb)):
+        check(shape, ss, ds, eb, path, seed=i)
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
+def test_tile_path_unaligned_dst_runs(eb):
+    # dst columns of 33 rows: 16-byte runs straddle, the kernel stores element-wise
+    c = max(1, 256 // eb)
+    check((33, c), (c, 1), (1, 33), eb, "tile", seed=3)
+    check((33, c), (c, 1), (1, 33), eb, "tile", seed=4, dst_off=1)
+
+
+@pytest.mark.parametrize("eb,R", [(1, 2), (1, 4), (1, 8), (1, 16), (2, 2), (2, 4), (2, 8),
+                                  (4, 2), (4, 4), (8, 2)])
+def test_rows_path(eb, R):
+    A = 3 * 16 // eb * 2            # whole 16-byte pieces per row, several units
+    for i, batch in enumerate([(1,), (7,), (3, 5)]):
+        shape = batch + (R, A)
+        ss = L.row_major_strides(shape)
+        dss = L.row_major_strides(batch + (A, R))
+        ds = dss[:len(batch)] + (1, R)
+        check(shape, ss, ds, eb, "rows", seed=i)
+
+
+WARP_CASES = [((4, 32), (32, 1), (1, 4)), ((8, 16), (16, 1), (1, 8)), ((2, 64), (64, 1), (1, 2)),
+              ((4, 8, 4), (32, 4, 1), (1, 16, 4)), ((32,), (1,), (1,)), ((16, 16), (16, 1), (1, 16))]
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
+def test_warp_path(eb):
+    ran = 0
+    for i, (ext, ss, ds) in enumerate(WARP_CASES):
+        for batch in (1, 5):
+            n = int(np.prod(ext))
+            shape = (batch,) + ext
+            try:
+                tl.tl_plan(1 << 20, 1 << 30, shape, (n,) + ss, (n,) + ds, eb, path="warp")
+            except tl.TLError as e:
+                assert e.name == "TL_ERR_PATH"
+                continue
+            check(shape, (n,) + ss, (n,) + ds, eb, "warp", seed=i)
+            ran += 1
+    assert ran > 0
+
+
+def test_auto_paths_on_random_layouts():
+    rng = np.random.default_rng(7)
+    seen = set()
+    for i in range(40):
+        eb = int(rng.choice(WIDTHS))
+        nd = int(rng.integers(1, 5))
+        shape = tuple(int(x) for x in rng.integers(1, 40, size=nd))
+        perm = tuple(int(p) for p in rng.permutation(nd))
+        ss, ds = perm_layouts(shape, perm)
+        seen.add(tl.tl_plan(1 << 20, 1 << 34, shape, ss, ds, eb)["path"])
+        check(shape, ss, ds, eb, "auto", seed=i)
+    assert len(seen) >= 3
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+def test_edge_cases():
+    check((), (), (), 4)                                         # one element
+    check((1, 1, 1), (7, 3, 1), (1, 1, 1), 16)
+    check((2,) * 8, L.row_major_strides((2,) * 8),
+          tuple(reversed(L.row_major_strides((2,) * 8))), 2)    # 8 dims, full reversal
+    check((5, 7), (0, 1), (7, 1), 4, "generic")                  # broadcast source rows
+    check((5, 7), (0, 1), (7, 1), 4)
+    check((3, 4, 5), (1, 3, 12), (20, 5, 1), 1, seed=5)          # column-major -> row-major
+    check((64, 96), (96, 1), (1, 64 + 3), 8, "auto")            # padded destination columns
+    check((17, 3), (3, 1), (1, 17), 1, "generic", src_off=1, dst_off=3)   # odd byte offsets
+    # empty shapes are no-ops (no launch)
+    before = tl.tl_launch_count()
+    d = torch.full((64,), CANARY, dtype=torch.uint8, device="cuda")
+    tl.tl_permute(d.data_ptr(), d.data_ptr() + 32, (0, 4), (4, 1), (1, 0), 1)
+    assert tl.tl_launch_count() == before
+    assert bool((d == CANARY).all())
+
+
+def test_in_place_warp_permute():
+    w = workloads.get("sf_transpose")
+    src = workloads.make_input(w)
+    want = np.zeros_like(src)
+    oracle.permute(src, want, w.shape, w.src_strides, w.dst_strides, 4)
+    buf = torch.from_numpy(src.copy()).cuda()
+    tl.tl_permute(buf.data_ptr(), buf.data_ptr(), w.shape, w.src_strides, w.dst_strides, 4,
+                  torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(buf.cpu().numpy(), want)
+
+
+def test_errors_launch_nothing():
+    a = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    before = tl.tl_launch_count()
+    with pytest.raises(tl.TLError) as e:
+        tl.tl_permute(a.data_ptr(), a.data_ptr() + 64, (16, 16), (16, 1), (1, 16), 4)
+    assert e.value.name == "TL_ERR_ALIAS"
+    with pytest.raises(tl.TLError) as e:
+        tl.permute(a[:1024], a[2048:], (16, 16), (16, 1), (1, 16), elem_bytes=8)
+    assert e.value.name == "TL_ERR_BOUNDS"
+    assert tl.tl_launch_count() == before
+
+
+def test_cluster_handoff_timeout_is_reported_and_context_survives():
+    shape, ss, ds = (16, 128, 64), (8192, 64, 1), (8192, 1, 128)
+    src = torch.zeros(16 * 8192, dtype=torch.float16, device="cuda")
+    dst = torch.zeros_like(src)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tl.permute(src, dst, shape, ss, ds, path="cluster", flags=tl.TL_FLAG_TEST_DROP_HANDOFF,
+               dev_status=status.data_ptr())
+    torch.cuda.synchronize()
+    assert int(status.item()) == -12          # TL_ERR_TIMEOUT
+    # the context is still usable and the same call without the hook is correct
+    check(shape, ss, ds, 2, "cluster", seed=9)
+    status.zero_()
+    check(shape, ss, ds, 2, "tile", seed=9, dev_status=status.data_ptr())
+    assert int(status.item()) == 0
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size, in the launch configuration the bench times
+# ---------------------------------------------------------------------------
+FULL = ["sf_transpose", "tile_transpose", "mx_sf", "attention", "t2d_u8", "t2d_f16", "t2d_f32",
+        "t2d_f64", "t2d_v16"]
+
+
+def _full(name, path="auto"):
+    w = workloads.get(name)
+    src = workloads.make_input(w)
+    want = np.empty(w.dst_elems * w.elem_bytes, dtype=np.uint8)
+    oracle.permute(src, want, w.shape, w.src_strides, w.dst_strides, w.elem_bytes,
+                   nthreads=NTHREADS)
+    s_gpu = torch.from_numpy(src).cuda()
+    del src
+    d_gpu = torch.empty(w.dst_elems * w.elem_bytes, dtype=torch.uint8, device="cuda")
+    tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), w.shape, w.src_strides,
+                     w.dst_strides, w.elem_bytes, torch.cuda.current_stream().cuda_stream,
+                     path=path)
+    torch.cuda.synchronize()
+    got = d_gpu.cpu().numpy()
+    del s_gpu, d_gpu
+    assert np.array_equal(got, want), name
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(name):
+    _full(name)
+
+
+def test_full_size_tile_transpose_through_the_cluster_handoff():
+    _full("tile_transpose", "cluster")

@@ -1,0 +1,289 @@
+"""Host-side logic of the C ABI, on CPU: no kernel is launched here.
+
+The library must load on a machine without a GPU, export every function that
+include/tl_permute.h declares, and its host entry points (canonicalisation, the
+bank simulator and XOR chooser, validation and planning) must agree with the
+oracle's independent Python references.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import movement_tl_permute_gb300 as tl
+from movement_tl_permute_gb300 import workloads
+from oracle import layout_ref as L
+from tests.conftest import ROOT
+
+SRC = 0x10000000      # fake, 4 KiB-aligned device addresses: tl_plan never dereferences
+DST = 0x90000000
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from movement_tl_permute_gb300 import build
+    build.build()
+    tl.load()
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "tl_permute.h")) as f:
+        text = f.read()
+    return re.findall(r"TL_API\s+[\w\s\*]+?\b(tl_\w+)\s*\(", text)
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    names = _declared_functions()
+    assert set(names) >= {"tl_layout_canon", "tl_choose_xor_k", "tl_permute", "tl_permute_ex",
+                          "tl_plan", "tl_status_string", "tl_launch_count", "tl_version",
+                          "tl_bank_conflicts"}
+    lib = tl.load()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert tl.tl_version() == 1
+    assert tl.tl_status_string(0) == "ok"
+    assert "alias" in tl.tl_status_string(-7) or "overlap" in tl.tl_status_string(-7)
+
+
+# ---------------------------------------------------------------------------
+# canonicalisation vs the oracle reference
+# ---------------------------------------------------------------------------
+def _rand_layout_pair(rng):
+    nd = int(rng.integers(1, 6))
+    shape = tuple(int(x) for x in rng.integers(1, 5, size=nd))
+    perm = list(rng.permutation(nd))
+    ss = L.row_major_strides(shape)
+    pst = L.row_major_strides(tuple(shape[p] for p in perm))
+    ds = [0] * nd
+    for i, p in enumerate(perm):
+        ds[p] = pst[i]
+    if rng.random() < 0.3:          # padded strides break some merges
+        ss = tuple(s * int(rng.integers(1, 3)) for s in ss)
+    return shape, tuple(ss), tuple(ds)
+
+
+def test_canon_matches_reference():
+    rng = np.random.default_rng(1)
+    for _ in range(400):
+        shape, ss, ds = _rand_layout_pair(rng)
+        begin = extent = None
+        if rng.random() < 0.5:
+            begin = tuple(int(rng.integers(0, e)) for e in shape)
+            extent = tuple(int(rng.integers(0, e - b + 1)) for e, b in zip(shape, begin))
+        so, do = int(rng.integers(0, 9)), int(rng.integers(0, 9))
+        got = tl.tl_layout_canon(shape, ss, ds, begin, extent, so, do)
+        want = L.canon_ref(shape, ss, ds, begin, extent, so, do)
+        assert got == want, (shape, ss, ds, begin, extent)
+
+
+def test_canon_worked_examples():
+    c = tl.tl_layout_canon((2, 1, 4, 32), (128, 128, 32, 1), (128, 128, 1, 4),
+                           begin=(1, 0, 0, 0), extent=(1, 1, 4, 32))
+    assert c["extent"] == (4, 32) and c["src_str"] == (32, 1) and c["dst_str"] == (1, 4)
+    assert c["src_offset"] == 128 and c["chunk_elems"] == 0
+    c = tl.tl_layout_canon((128, 64), (64, 1), (64, 1))
+    assert c["extent"] == (8192,) and c["chunk_elems"] * 2 == 16384
+    with pytest.raises(tl.TLError) as e:
+        tl.tl_layout_canon((4, 4), (4, 1), (1, 4), begin=(3, 0), extent=(2, 4))
+    assert e.value.name == "TL_ERR_RANGE"
+
+
+# ---------------------------------------------------------------------------
+# bank simulator and chooser vs the oracle reference
+# ---------------------------------------------------------------------------
+def test_bank_conflicts_match_reference():
+    rng = np.random.default_rng(2)
+    for _ in range(500):
+        eb = int(rng.choice([1, 2, 4, 8, 16]))
+        offs = [int(x) for x in rng.integers(0, 400, size=32)]
+        if rng.random() < 0.3:
+            for i in rng.choice(32, size=5, replace=False):
+                offs[int(i)] = None
+        for model in ("conservative", "hardware"):
+            assert tl.tl_bank_conflicts(offs, eb, model) == \
+                L.bank_conflict_degree(offs, eb, model), (eb, model)
+
+
+def test_choose_xor_k_matches_reference():
+    rng = np.random.default_rng(3)
+    n = 0
+    for _ in range(300):
+        P = int(rng.choice([1, 2, 4, 8, 3, 6]))
+        total = 32 * P
+        nd = int(rng.integers(1, 4))
+        # random factorisation of total into nd extents
+        ext = [total]
+        for _ in range(nd - 1):
+            divs = [d for d in range(2, ext[0]) if ext[0] % d == 0]
+            if not divs:
+                break
+            d = int(rng.choice(divs))
+            ext = [ext[0] // d, d] + ext[1:]
+        perm = list(rng.permutation(len(ext)))
+        ss = L.row_major_strides(ext)
+        pst = L.row_major_strides(tuple(ext[p] for p in perm))
+        ds = [0] * len(ext)
+        for i, p in enumerate(perm):
+            ds[p] = pst[i]
+        eb = int(rng.choice([1, 2, 4, 8, 16]))
+        want = L.choose_xor_k_ref(ext, ss, ds, eb)
+        if want is None:
+            with pytest.raises(tl.TLError) as e:
+                tl.tl_choose_xor_k(ext, ss, ds, eb)
+            assert e.value.name == "TL_ERR_NO_VALID_K"
+        else:
+            assert tl.tl_choose_xor_k(ext, ss, ds, eb) == want
+            n += 1
+    assert n > 50
+    assert tl.tl_choose_xor_k((4, 32), (32, 1), (1, 4), 4) == (2, 3, 3)
+    with pytest.raises(tl.TLError) as e:
+        tl.tl_choose_xor_k((3, 5), (5, 1), (1, 3), 4)
+    assert e.value.name == "TL_ERR_EXTENT"
+
+
+# ---------------------------------------------------------------------------
+# the tile kernel's shared-memory reads are conflict-free (model of its lanes)
+# ---------------------------------------------------------------------------
+def _swz(row, col):
+    """Byte offset of byte `col` of tile row `row` under the TMA 128-byte swizzle."""
+    return row * 128 + ((((col >> 4) ^ row) & 7) << 4) + (col & 15)
+
+
+def _tile_read_pattern(eb):
+    """Per load instruction: the byte offset each lane reads (mirrors k_tile's lanes)."""
+    out = []
+    if eb == 4:
+        for u in range(32):
+            cb, rb = u & 7, u >> 3
+            for k in range(4):
+                out.append([_swz(rb * 32 + 4 * (l >> 2) + (k ^ ((l >> 3) & 3)), 4 * (4 * cb + (l & 3)))
+                            for l in range(32)])
+    elif eb == 8:
+        for u in range(32):
+            cb, rb = u & 7, u >> 3
+            for k in range(2):
+                out.append([_swz(rb * 32 + 2 * (l >> 1) + (k ^ ((l >> 3) & 1)), 8 * (2 * cb + (l & 1)))
+                            for l in range(32)])
+    elif eb == 16:
+        for u in range(32):
+            cb, rb = u & 7, u >> 3
+            out.append([_swz(rb * 32 + l, 16 * cb) for l in range(32)])
+    elif eb == 2:
+        for u in range(16):
+            cb, rb = u & 7, u >> 3
+            for k in range(8):
+                out.append([_swz(rb * 64 + 8 * (l >> 2) + (k ^ (l >> 2)), 4 * (4 * cb + (l & 3)))
+                            for l in range(32)])
+    else:
+        for cb in range(8):
+            for k in range(16):
+                out.append([_swz(16 * (l >> 2) + (k ^ (l >> 2)), 4 * (4 * cb + (l & 3)))
+                            for l in range(32)])
+    return out
+
+
+@pytest.mark.parametrize("eb", [1, 2, 4, 8, 16])
+def test_tile_kernel_smem_reads_are_conflict_free(eb):
+    access = 4 if eb <= 4 else eb          # widths of the shared loads the kernel issues
+    rows_read = set()
+    for lanes in _tile_read_pattern(eb):
+        assert all(o % access == 0 for o in lanes)
+        elems = [o // access for o in lanes]
+        assert tl.tl_bank_conflicts(elems, access, "hardware") == 1
+        assert L.bank_conflict_degree(elems, access, "hardware") == 1
+        rows_read.update(lanes)
+    # together the loads cover the whole 16 KiB tile, each 4-byte word once
+    words = set()
+    for lanes in _tile_read_pattern(eb):
+        for o in lanes:
+            for b in range(0, access, 4):
+                words.add(o + b)
+    assert len(words) == 16384 // 4
+
+
+# ---------------------------------------------------------------------------
+# planner and validation (tl_plan; no device needed)
+# ---------------------------------------------------------------------------
+def _plan(w, src=SRC, dst=DST, **kw):
+    return tl.tl_plan(src, dst, w.shape, w.src_strides, w.dst_strides, w.elem_bytes, **kw)
+
+
+def test_plans_of_the_workloads():
+    p = _plan(workloads.get("sf_transpose"))
+    assert p["path"] == "warp" and (p["k"], p["shift"], p["mask"]) == (2, 3, 3)
+    p = _plan(workloads.get("tile_transpose"))
+    assert p["path"] == "tile" and p["tiles"] == 65536 and p["vec_bytes"] == 16
+    assert (p["tile_rows"], p["tile_cols"]) == (128, 64)
+    p = _plan(workloads.get("mx_sf"))
+    assert p["path"] == "rows" and p["extent"] == (1 << 21, 32, 4)
+    p = _plan(workloads.get("attention"))
+    assert p["path"] == "chunk" and p["vec_bytes"] == 16
+    for name in ("t2d_u8", "t2d_f16", "t2d_f32", "t2d_f64", "t2d_v16"):
+        p = _plan(workloads.get(name))
+        assert p["path"] == "tile", name
+    p = _plan(workloads.get("tile_transpose"), path="cluster")
+    assert p["path"] == "cluster"
+
+
+def test_forced_paths_that_do_not_apply():
+    w = workloads.get("attention")
+    for path in ("tile", "rows", "cluster"):
+        with pytest.raises(tl.TLError) as e:
+            _plan(w, path=path)
+        assert e.value.name == "TL_ERR_PATH"
+    assert _plan(w, path="generic")["path"] == "generic"
+
+
+def _err(*args, **kw):
+    with pytest.raises(tl.TLError) as e:
+        tl.tl_plan(*args, **kw)
+    return e.value.name
+
+
+def test_validation_errors():
+    assert _err(SRC, DST, (4, 4), (4, 1), (1, 4), 3) == "TL_ERR_ELEM_BYTES"
+    assert _err(SRC, DST, (4, 4), (4, -1), (1, 4), 4) == "TL_ERR_ARG"
+    assert _err(SRC, DST, (4, -4), (4, 1), (1, 4), 4) == "TL_ERR_ARG"
+    assert _err(SRC, DST, (4, 4), (4, 1), (1, 2), 4) == "TL_ERR_DST_OVERLAP"
+    assert _err(SRC, DST, (4, 4), (4, 1), (0, 4), 4) == "TL_ERR_DST_OVERLAP"
+    assert _err(SRC + 2, DST, (4, 4), (4, 1), (1, 4), 4) == "TL_ERR_ALIGN"
+    assert _err(SRC, SRC + 32, (4, 4), (4, 1), (1, 4), 4) == "TL_ERR_ALIAS"
+    assert _err(SRC, DST, (4, 4), (4, 1), (1, 4), 4, dst_bytes=60) == "TL_ERR_BOUNDS"
+    assert _err(SRC, DST, (1 << 40, 1 << 30), (1 << 30, 1), (1, 1 << 40), 1) == "TL_ERR_RANGE"
+    assert _err(0, DST, (4,), (1,), (1,), 4) == "TL_ERR_ARG"
+    assert _err(SRC, DST, (2,) * 9, (1,) * 9, (1,) * 9, 1) == "TL_ERR_ARG"
+    # degenerate calls that are fine
+    assert tl.tl_plan(SRC, DST, (0, 5), (5, 1), (1, 0), 4)["path"] == "none"
+    assert tl.tl_plan(0, 0, (3, 0), (1, 1), (1, 1), 4)["path"] == "none"
+    assert tl.tl_plan(SRC, DST, (), (), (), 16)["path"] == "chunk"
+    assert tl.tl_plan(SRC, DST, (4, 4), (4, 1), (1, 4), 4, dst_bytes=64)["path"] != "none"
+    # sub-element misalignment is allowed for 1-byte elements
+    assert tl.tl_plan(SRC + 1, DST + 3, (64, 64), (64, 1), (1, 64), 1)["path"] == "generic"
+
+
+def test_in_place_only_on_the_warp_path():
+    w = workloads.get("sf_transpose")
+    p = tl.tl_plan(SRC, SRC, w.shape, w.src_strides, w.dst_strides, 4)
+    assert p["path"] == "warp" and p["in_place"]
+    # a transpose whose tile does not read exactly what it writes cannot run in place
+    assert _err(SRC, SRC, (64, 64), (64, 1), (1, 64), 4) == "TL_ERR_ALIAS"
+
+
+def test_dst_overlap_check_is_sound():
+    """Whatever the planner accepts as a destination is truly non-overlapping."""
+    rng = np.random.default_rng(5)
+    accepted = 0
+    for _ in range(300):
+        nd = int(rng.integers(1, 4))
+        shape = tuple(int(x) for x in rng.integers(1, 5, size=nd))
+        ds = tuple(int(x) for x in rng.integers(0, 20, size=nd))
+        ss = L.row_major_strides(shape)
+        try:
+            tl.tl_plan(SRC, DST, shape, ss, ds, 4)
+        except tl.TLError as e:
+            assert e.name == "TL_ERR_DST_OVERLAP"
+            continue
+        accepted += 1
+        assert L.offsets_unique(shape, ds), (shape, ds)
+    assert accepted > 30

@@ -352,17 +352,13 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     const bool rows = plane && rows_ok(p, s0, d0);
     const bool tile = plane && tile_ok(p, s0);
 
+    int path = 0;
     if (ranges_meet) {
         if (!(s0 == d0 && warp_ok && warp_in_place_ok(p))) return TL_ERR_ALIAS;
         if (forced != TL_PATH_AUTO && forced != TL_PATH_WARP) return TL_ERR_PATH;
         p.in_place = true;
-        p.path = TL_PATH_WARP;
-        *plan = p;
-        return TL_OK;
-    }
-
-    int path = 0;
-    switch (forced) {
+        path = TL_PATH_WARP;
+    } else switch (forced) {
     case TL_PATH_AUTO:
         if (chunk_ok) path = TL_PATH_CHUNK;
         else if (warp_ok && total <= 8192) path = TL_PATH_WARP;

@@ -53,13 +53,17 @@ int get_device_info(DevInfo* out) {
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.tile_occ[i], kt[i], kTileThreads,
                                                               tile_smem_bytes()) != cudaSuccess)
                 return TL_ERR_CUDA;
+            // The cluster variant is optional: if its set-up fails it is sized
+            // conservatively (one CTA per SM) and the error is cleared.
             const void* kc = cluster_kernel(1 << i);
             if (cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     cluster_smem_bytes()) != cudaSuccess)
-                return TL_ERR_CUDA;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.cluster_occ[i], kc, kTileThreads,
-                                                              cluster_smem_bytes()) != cudaSuccess)
-                return TL_ERR_CUDA;
+                                     cluster_smem_bytes()) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.cluster_occ[i], kc, kTileThreads,
+                                                              cluster_smem_bytes()) != cudaSuccess ||
+                d.cluster_occ[i] < 1) {
+                cudaGetLastError();
+                d.cluster_occ[i] = 1;
+            }
         }
         if (!g_encode) {
             void* fn = nullptr;

@@ -218,6 +218,47 @@ TL_API uint64_t tl_launch_count(void);
 /* TL_VERSION of the loaded library. */
 TL_API int tl_version(void);
 
+/*
+ * tl_permute_tile_noalloc -- the TMA tile transpose (TL_PATH_TILE) for callers
+ * that cannot allocate device memory.  The TVM pages have no counterpart: it
+ * exists for integration, not for the method.
+ *
+ * Who needs it: code that runs while a stream is being captured into a CUDA
+ * graph (a cudaMalloc there breaks the capture), plug-ins living inside a
+ * framework whose caching allocator already owns the device's memory budget,
+ * and fixed-memory or real-time deployments whose policy forbids allocating
+ * after start-up.  Such callers cannot provide the status word that
+ * tl_permute_ex takes in opts.dev_status.
+ *
+ * What it does: the same launch as tl_permute_ex with TL_PATH_TILE, except that
+ * the kernel's only scratch -- the 4-byte status word it writes when a bounded
+ * wait expires -- lives in a file-scope device array of
+ * TL_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that loads
+ * the library keeps until the process exits.  The call zeroes that word on
+ * `stream`, launches, and, if host_status is not NULL, copies the word into
+ * *host_status on the same stream (0 = ok, TL_ERR_TIMEOUT = a wait expired;
+ * valid once the stream has reached that point; pass pinned host memory to keep
+ * the call asynchronous).  It calls no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *
+ *   src, dst, ndim, shape, src_strides, dst_strides, elem_bytes, stream:
+ *       as tl_permute; the layout must admit the tile path
+ *   host_status  nullable host pointer (see above)
+ * Returns TL_OK; TL_ERR_PATH if the tile path does not apply; TL_ERR_BOUNDS if
+ * the launch would need more scratch than TL_NOALLOC_SCRATCH_BYTES; otherwise
+ * the errors of tl_permute.
+ *
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture begins.  All
+ * calls share the one array and it keeps the last call's contents: calls whose
+ * work overlaps on the GPU (other streams, other host threads) race on the
+ * status word, so one call's report may be cleared or overwritten by another's.
+ */
+#define TL_NOALLOC_SCRATCH_BYTES 256
+TL_API int tl_permute_tile_noalloc(const void *src, void *dst, int ndim, const int64_t *shape,
+                                   const int64_t *src_strides, const int64_t *dst_strides,
+                                   int elem_bytes, tl_stream_t stream, int32_t *host_status);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ __all__ = [
     "TLError", "TL_MAX_DIMS", "PATHS", "PATH_NAMES", "TL_FLAG_TEST_DROP_HANDOFF",
     "load", "library_path", "tl_layout_canon", "tl_choose_xor_k", "tl_bank_conflicts",
     "tl_permute", "tl_permute_ex", "tl_plan", "tl_status_string", "tl_launch_count",
-    "tl_version", "permute",
+    "tl_version", "permute", "tl_permute_tile_noalloc",
 ]
 
 TL_MAX_DIMS = 8
@@ -103,8 +103,10 @@ def load():
         lib.tl_launch_count.argtypes = []
         lib.tl_launch_count.restype = ctypes.c_uint64
         lib.tl_version.argtypes = []
+        lib.tl_permute_tile_noalloc.argtypes = [vp, vp, ctypes.c_int, i64p, i64p, i64p,
+                                                ctypes.c_int, vp, ctypes.POINTER(_i32)]
         for name in ("tl_layout_canon", "tl_choose_xor_k", "tl_bank_conflicts", "tl_permute",
-                     "tl_permute_ex", "tl_plan", "tl_version"):
+                     "tl_permute_ex", "tl_plan", "tl_version", "tl_permute_tile_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -209,6 +211,18 @@ def tl_permute_ex(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides,
                                 _arr(shape), _arr(src_strides), _arr(dst_strides),
                                 int(elem_bytes), int(stream) or None, ctypes.byref(o)),
            "tl_permute_ex")
+
+
+def tl_permute_tile_noalloc(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides,
+                            elem_bytes: int, stream: int = 0, host_status=None) -> None:
+    """The tile path with its status word in the library's static device scratch
+    (for callers that cannot allocate).  ``host_status``: optional ctypes.c_int32
+    that receives the status once the stream reaches it."""
+    _check(load().tl_permute_tile_noalloc(
+        int(src_ptr) or None, int(dst_ptr) or None, len(shape), _arr(shape), _arr(src_strides),
+        _arr(dst_strides), int(elem_bytes), int(stream) or None,
+        ctypes.byref(host_status) if host_status is not None else None),
+        "tl_permute_tile_noalloc")
 
 
 def tl_plan(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides, elem_bytes: int,

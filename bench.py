@@ -335,10 +335,10 @@ def run_ours(args, w):
     s_gpu = torch.from_numpy(src_np).to(dev)
     d_gpu = torch.empty(nbytes_dst, dtype=torch.uint8, device=dev)
     args_call = (w.shape, w.src_strides, w.dst_strides, w.elem_bytes)
-    plan = tl.tl_plan(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call)
+    plan = tl.tl_plan(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call, path=args.path)
 
     def step():
-        tl.tl_permute(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call, sptr)
+        tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call, sptr, path=args.path)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -371,7 +371,7 @@ def run_ours(args, w):
 
     def e2e_step():
         s_gpu.copy_(src_pin, non_blocking=True)
-        tl.tl_permute(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call, sptr)
+        tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call, sptr, path=args.path)
         dst_pin.copy_(d_gpu, non_blocking=True)
 
     e2e_step()
@@ -434,6 +434,11 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--path", default="auto",
+                    choices=["auto", "generic", "chunk", "tile", "warp", "rows", "cluster"],
+                    help="force a kernel path (default: the planner's choice)")
+    ap.add_argument("--leading", type=int, default=0,
+                    help="override the outermost extent (smaller cases for profiling)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the CPU baseline")
     args = ap.parse_args(argv)
@@ -442,6 +447,8 @@ def main(argv=None):
     from movement_tl_permute_gb300 import workloads
 
     w = workloads.get(args.workload)
+    if args.leading:
+        w = workloads.scaled(w, args.leading)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

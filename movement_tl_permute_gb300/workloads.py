@@ -19,7 +19,7 @@ grown to sizes that exercise HBM:
 ``tile_transpose`` 65536 float16 tiles of 128x64, row-major -> column-major per
                    tile (1 GiB); N(0,1) with 0.1 % NaN / Inf bit patterns.
 ``mx_sf``          uint8 (2^20, 2, 4, 32): strides (256,128,32,1) ->
-                   (256,128,1,4); random bytes (512 MiB).
+                   (256,128,1,4); random bytes (256 MiB).
 ``attention``      bfloat16 (B=16, H=32, S=4096, D=128) -> (B, S, H, D)
                    contiguous (512 MiB).
 ``t2d_u8`` ...     2-D row-major -> column-major transposes of ~1 GiB for each
@@ -32,7 +32,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "get", "make_input", "random_bits"]
+__all__ = ["Workload", "WORKLOADS", "get", "scaled", "make_input", "random_bits"]
 
 
 @dataclass(frozen=True)
@@ -93,6 +93,23 @@ WORKLOADS = {
 
 def get(name: str) -> Workload:
     return WORKLOADS[name]
+
+
+def scaled(w: Workload, leading: int) -> Workload:
+    """The same workload with its outermost extent set to ``leading`` (a smaller
+    case for profiling).  The 2-D transposes keep their column count and
+    recompute their column-major destination strides; the batched workloads keep
+    their strides."""
+    if leading < 1:
+        raise ValueError("leading extent must be positive")
+    if "t2d" in w.tags:
+        rows, cols = leading, w.shape[1]
+        return _t2d(w.name, w.elem_bytes, rows, cols, w.seed)
+    ratio_src = w.src_elems // w.shape[0]
+    ratio_dst = w.dst_elems // w.shape[0]
+    return Workload(w.name, w.elem_bytes, (leading,) + tuple(w.shape[1:]), w.src_strides,
+                    w.dst_strides, leading * ratio_src, leading * ratio_dst, w.seed, w.values,
+                    w.description + " (outermost extent %d)" % leading, w.tags)
 
 
 def random_bits(n_bytes: int, seed: int) -> np.ndarray:

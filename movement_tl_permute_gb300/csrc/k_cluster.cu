@@ -108,8 +108,8 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                 if (lane == 0) report(a.status, TL_ERR_TIMEOUT);
                 break;
             }
-            const TileCtx c = make_ctx<EB>(t, a);
-            consume<EB>(smem_addr(smem + s * kTileBytes), c, warp, lane);
+            const TileOut o = make_out<EB>(tile_coord(t, a), a);
+            consume<EB>(smem_addr(smem + s * kTileBytes), o, warp, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(map_to_rank(smem_addr(&freed[s]), 0));
         }

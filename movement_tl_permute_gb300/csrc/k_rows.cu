@@ -5,9 +5,12 @@
 // Plane: b (extent R, dst stride 1, src stride ss_b) by a (src stride 1, dst
 // stride R: the plane is dense in dst), plus batch axes.  A unit is one 16-byte
 // column piece of a (16/EB elements): the thread loads it from each of the R
-// rows (R coalesced 16-byte loads), transposes the R x (16/EB) block in
-// registers with byte permutes, and writes the R contiguous 16-byte vectors of
-// dst the block maps to.  No shared memory is involved.
+// rows (16-byte loads that use whole sectors), transposes the R x (16/EB) block
+// in registers with byte permutes into the R contiguous 16-byte vectors of dst
+// the block maps to, and parks them in a per-warp shared-memory stage.  The
+// warp then stores the stage back lane by lane, so each store instruction
+// writes 512 contiguous bytes whenever consecutive units are adjacent in dst
+// (always within a plane, and across planes when the batch is dense).
 #include "tl_kernels.h"
 
 namespace tl {
@@ -87,21 +90,37 @@ __device__ __forceinline__ void unit_offsets(int64_t u, const RowsArgs& a, int64
     }
 }
 
+// Shared-memory staging of a warp's output: 16-byte chunk c is kept at
+// c ^ (((c >> 3) ^ (c >> 6)) & 7), which spreads both the per-lane writes
+// (chunks lane*R + k) and the contiguous read-back (chunks 32*i + lane) over
+// distinct bank groups in every 8-lane wavefront.
+__device__ __forceinline__ uint32_t stage_chunk(uint32_t c) {
+    return c ^ (((c >> 3) ^ (c >> 6)) & 7u);
+}
+
+// Block size and units in flight per thread: the 16-row variant keeps one unit
+// of 256 bytes in registers and a 32 KiB stage for 4 warps.
+template <int R> __host__ __device__ constexpr int rows_threads() { return R >= 16 ? 128 : 256; }
+template <int R> __host__ __device__ constexpr int rows_units() { return R >= 8 ? 1 : 2; }
+
 template <int EB, int R>
-__global__ void __launch_bounds__(256) k_rows(const RowsArgs a) {
-    constexpr int U = 2;
-    const int64_t step = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t u0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u0 < a.units;
-         u0 += step * U) {
+__global__ void __launch_bounds__(rows_threads<R>()) k_rows(const RowsArgs a) {
+    constexpr int U = rows_units<R>();
+    constexpr int kWarps = rows_threads<R>() / 32;
+    __shared__ __align__(16) uint4 stage[kWarps][32 * R];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t stage_base = dev::smem_addr(&stage[warp][0]);
+    const int64_t nwarps = (int64_t)gridDim.x * kWarps;
+    const int64_t gwarp = (int64_t)blockIdx.x * kWarps + warp;
+    // Each round a warp takes U groups of 32 consecutive units (warp-uniform loop).
+    for (int64_t base = gwarp * 32 * U; base < a.units; base += nwarps * 32 * U) {
         uint4 in[U][R];
         int64_t dofs[U];
-        bool ok[U];
 #pragma unroll
         for (int uu = 0; uu < U; ++uu) {
-            const int64_t u = u0 + uu * step;
-            ok[uu] = u < a.units;
-            dofs[uu] = 0;
-            if (ok[uu]) {
+            const int64_t u = base + uu * 32 + lane;
+            dofs[uu] = -1;
+            if (u < a.units) {
                 int64_t so, d, col;
                 unit_offsets(u, a, so, d, col);
                 const uint8_t* s = a.src + so * EB + col * 16;
@@ -112,17 +131,34 @@ __global__ void __launch_bounds__(256) k_rows(const RowsArgs a) {
         }
 #pragma unroll
         for (int uu = 0; uu < U; ++uu) {
-            if (!ok[uu]) continue;
+            if (base + uu * 32 >= a.units) break;          // warp-uniform
             uint4 out[R];
             transpose_block<EB, R>(in[uu], out);
 #pragma unroll
-            for (int k = 0; k < R; ++k) dev::stg128(a.dst + dofs[uu] + 16 * k, out[k]);
+            for (int k = 0; k < R; ++k) {
+                const uint4 v = out[k];
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 stage_base + 16 * stage_chunk(lane * R + k)),
+                             "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                             : "memory");
+            }
+            __syncwarp();
+            // store chunk 32*i + lane: unit (32*i + lane) / R of this group, piece k
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int c = 32 * i + lane;
+                const int64_t d = __shfl_sync(0xffffffffu, dofs[uu], c / R);
+                const uint4 v = dev::lds128(stage_base + 16 * stage_chunk(c));
+                if (d >= 0) dev::stg128(a.dst + d + 16 * (c % R), v);
+            }
+            __syncwarp();
         }
     }
 }
 
 template <int EB, int R>
 cudaError_t go(const RowsArgs& a, int grid, int block, cudaStream_t st) {
+    if (block != rows_threads<R>()) return cudaErrorInvalidValue;
     k_rows<EB, R><<<grid, block, 0, st>>>(a);
     return cudaGetLastError();
 }

@@ -31,6 +31,7 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full[kTileStages];
     __shared__ __align__(8) uint64_t empty[kTileStages];
+    __shared__ TileOut info[kTileStages];     // destination of the tile in each stage
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -57,6 +58,7 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                     break;
                 }
                 const TileCoord tc = tile_coord(t, a);
+                info[s] = make_out<EB>(tc, a);          // published by the release below
                 mbar_arrive_expect_tx(&full[s], kTileBytes);
                 tma_load(smem + s * kTileBytes, &tmap, &full[s], a.rank,
                          (int)(tc.ta * kRowBytes), (int)(tc.tb * kRows), (int)tc.bc[0],
@@ -78,8 +80,8 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
             if (lane == 0) report(a.status, TL_ERR_TIMEOUT);
             break;
         }
-        const TileCtx c = make_ctx<EB>(t, a);
-        consume<EB>(smem_addr(smem + s * kTileBytes), c, warp, lane);
+        const TileOut o = info[s];
+        consume<EB>(smem_addr(smem + s * kTileBytes), o, warp, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }

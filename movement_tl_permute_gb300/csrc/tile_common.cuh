@@ -58,36 +58,42 @@ __device__ __forceinline__ void store_elem(uint8_t* p, const uint4& v, int e) {
     }
 }
 
-struct TileCtx {
-    uint8_t* dst;
-    int64_t ext_a, ext_b, ds_a;
-    int64_t dst_base;      // element offset of the tile's (a0, b0) in dst
-    int64_t a0, b0;
-    bool vec;
+// Where one tile's columns land in dst, computed once per tile (by the producer
+// of the single-CTA kernel, which publishes it through the stage's full barrier).
+struct TileOut {
+    uint8_t* base;       // dst byte address of the tile's element (a0, b0)
+    int64_t cstride;     // bytes between consecutive columns a in dst
+    int32_t cols, rows;  // valid columns (a) and rows (b) of this tile
+    int32_t full;        // every column and row valid and 16-byte runs aligned
+    int32_t vec;         // 16-byte runs aligned (else element-wise stores)
 };
 
-// Stores the 16-byte run (16/EB consecutive b) at column a, starting at row b.
+// Stores the 16-byte run of (16/EB) consecutive rows starting at tile row `row`
+// of tile column `col`.
 template <int EB>
-__device__ __forceinline__ void put(const TileCtx& c, int64_t a, int64_t b, const uint4& v) {
+__device__ __forceinline__ void put(const TileOut& o, int col, int row, const uint4& v) {
     constexpr int V = 16 / EB;
-    if (a >= c.ext_a || b >= c.ext_b) return;
-    const int64_t off = c.dst_base + (a - c.a0) * c.ds_a + (b - c.b0);
-    uint8_t* p = c.dst + off * EB;
-    if (c.vec && b + V <= c.ext_b) {
+    uint8_t* p = o.base + (int64_t)col * o.cstride + row * EB;
+    if (o.full) {                       // warp-uniform fast path: interior tile
+        stg128(p, v);
+        return;
+    }
+    if (col >= o.cols || row >= o.rows) return;
+    if (o.vec && row + V <= o.rows) {
         stg128(p, v);
     } else {
 #pragma unroll
         for (int e = 0; e < V; ++e)
-            if (b + e < c.ext_b) store_elem<EB>(p + e * EB, v, e);
+            if (row + e < o.rows) store_elem<EB>(p + e * EB, v, e);
     }
 }
 
 // Consumer work for one tile: every warp handles its share of the tile.
 template <int EB>
-__device__ __forceinline__ void consume(uint32_t tile, const TileCtx& c, int warp, int lane);
+__device__ __forceinline__ void consume(uint32_t tile, const TileOut& o, int warp, int lane);
 
 template <>
-__device__ __forceinline__ void consume<4>(uint32_t tile, const TileCtx& c, int warp, int lane) {
+__device__ __forceinline__ void consume<4>(uint32_t tile, const TileOut& o, int warp, int lane) {
     // warp unit: 32 rows x 4 columns (one 16-byte chunk); 32 units per tile
     const int cw = lane & 3, g = lane >> 2, x = (lane >> 3) & 3;
 #pragma unroll
@@ -103,12 +109,12 @@ __device__ __forceinline__ void consume<4>(uint32_t tile, const TileCtx& c, int 
         cswap(x & 1, r[2], r[3]);
         cswap(x & 2, r[0], r[2]);
         cswap(x & 2, r[1], r[3]);
-        put<4>(c, c.a0 + col, c.b0 + row0, make_uint4(r[0], r[1], r[2], r[3]));
+        put<4>(o, col, row0, make_uint4(r[0], r[1], r[2], r[3]));
     }
 }
 
 template <>
-__device__ __forceinline__ void consume<8>(uint32_t tile, const TileCtx& c, int warp, int lane) {
+__device__ __forceinline__ void consume<8>(uint32_t tile, const TileOut& o, int warp, int lane) {
     // warp unit: 32 rows x 2 columns; half-warp wavefronts of 16 lanes
     const int cw = lane & 1, g = lane >> 1, x = (lane >> 3) & 1;
 #pragma unroll
@@ -120,12 +126,12 @@ __device__ __forceinline__ void consume<8>(uint32_t tile, const TileCtx& c, int 
         uint2 r0 = lds64(tile + swz(row0 + x, 8 * col));
         uint2 r1 = lds64(tile + swz(row0 + (1 ^ x), 8 * col));
         cswap(x != 0, r0, r1);
-        put<8>(c, c.a0 + col, c.b0 + row0, make_uint4(r0.x, r0.y, r1.x, r1.y));
+        put<8>(o, col, row0, make_uint4(r0.x, r0.y, r1.x, r1.y));
     }
 }
 
 template <>
-__device__ __forceinline__ void consume<16>(uint32_t tile, const TileCtx& c, int warp, int lane) {
+__device__ __forceinline__ void consume<16>(uint32_t tile, const TileOut& o, int warp, int lane) {
     // warp unit: 32 rows x 1 column; quarter-warp wavefronts read 8 distinct chunks
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -133,12 +139,12 @@ __device__ __forceinline__ void consume<16>(uint32_t tile, const TileCtx& c, int
         const int cb = u & 7, rb = u >> 3;
         const int row = rb * 32 + lane;
         uint4 v = lds128(tile + swz(row, 16 * cb));
-        put<16>(c, c.a0 + cb, c.b0 + row, v);
+        put<16>(o, cb, row, v);
     }
 }
 
 template <>
-__device__ __forceinline__ void consume<2>(uint32_t tile, const TileCtx& c, int warp, int lane) {
+__device__ __forceinline__ void consume<2>(uint32_t tile, const TileOut& o, int warp, int lane) {
     // warp unit: 64 rows x 4 words (8 columns); 16 units per tile
     const int cw = lane & 3, g = lane >> 2, x = g;
 #pragma unroll
@@ -162,14 +168,13 @@ __device__ __forceinline__ void consume<2>(uint32_t tile, const TileCtx& c, int 
         lo.y = __byte_perm(r[2], r[3], 0x5410); hi.y = __byte_perm(r[2], r[3], 0x7632);
         lo.z = __byte_perm(r[4], r[5], 0x5410); hi.z = __byte_perm(r[4], r[5], 0x7632);
         lo.w = __byte_perm(r[6], r[7], 0x5410); hi.w = __byte_perm(r[6], r[7], 0x7632);
-        const int64_t a = c.a0 + 2 * word, b = c.b0 + row0;
-        put<2>(c, a, b, lo);
-        put<2>(c, a + 1, b, hi);
+        put<2>(o, 2 * word, row0, lo);
+        put<2>(o, 2 * word + 1, row0, hi);
     }
 }
 
 template <>
-__device__ __forceinline__ void consume<1>(uint32_t tile, const TileCtx& c, int warp, int lane) {
+__device__ __forceinline__ void consume<1>(uint32_t tile, const TileOut& o, int warp, int lane) {
     // warp unit: 128 rows x 4 words (16 columns); 8 units per tile, one per warp
     const int cw = lane & 3, g = lane >> 2, x = g;
     const int cb = warp;
@@ -187,22 +192,21 @@ __device__ __forceinline__ void consume<1>(uint32_t tile, const TileCtx& c, int 
     for (int k = 0; k < 16; ++k)
         if (!(k & 4)) cswap(x & 4, r[k], r[k + 4]);
     // 4x4 byte transposes: out[cc] word q = byte cc of rows 4q .. 4q+3
-    uint32_t o[4][4];
+    uint32_t w[4][4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const uint32_t lo01 = __byte_perm(r[4 * q], r[4 * q + 1], 0x5140);
         const uint32_t lo23 = __byte_perm(r[4 * q + 2], r[4 * q + 3], 0x5140);
         const uint32_t hi01 = __byte_perm(r[4 * q], r[4 * q + 1], 0x7362);
         const uint32_t hi23 = __byte_perm(r[4 * q + 2], r[4 * q + 3], 0x7362);
-        o[0][q] = __byte_perm(lo01, lo23, 0x5410);
-        o[1][q] = __byte_perm(lo01, lo23, 0x7632);
-        o[2][q] = __byte_perm(hi01, hi23, 0x5410);
-        o[3][q] = __byte_perm(hi01, hi23, 0x7632);
+        w[0][q] = __byte_perm(lo01, lo23, 0x5410);
+        w[1][q] = __byte_perm(lo01, lo23, 0x7632);
+        w[2][q] = __byte_perm(hi01, hi23, 0x5410);
+        w[3][q] = __byte_perm(hi01, hi23, 0x7632);
     }
-    const int64_t a = c.a0 + 4 * word, b = c.b0 + row0;
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc)
-        put<1>(c, a + cc, b, make_uint4(o[cc][0], o[cc][1], o[cc][2], o[cc][3]));
+        put<1>(o, 4 * word + cc, row0, make_uint4(w[cc][0], w[cc][1], w[cc][2], w[cc][3]));
 }
 
 // Tile t -> (ta, tb, batch coordinates).  Within a batch item tiles are visited in
@@ -215,6 +219,27 @@ struct TileCoord {
 
 __device__ __forceinline__ TileCoord tile_coord(int64_t t, const TileArgs& a) {
     TileCoord r;
+    if (a.use32) {
+        // the same decode with 32-bit division by invariant integers
+        const uint32_t t32 = (uint32_t)t;
+        uint32_t item = div_u32(t32, a.d_item);
+        const uint32_t local = t32 - item * a.d_item.d;
+        const uint32_t grp = div_u32(local, a.d_grp);
+        const uint32_t first_tb = grp * a.d_gfull.d;
+        const uint32_t in_grp = local - grp * a.d_grp.d;
+        const bool last = first_tb + a.d_gfull.d > (uint32_t)a.tiles_b;
+        const DivU32& dg = last ? a.d_glast : a.d_gfull;
+        const uint32_t ta = div_u32(in_grp, dg);
+        r.ta = ta;
+        r.tb = first_tb + (in_grp - ta * dg.d);
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const uint32_t q = div_u32(item, a.d_bext[i]);
+            r.bc[i] = item - q * a.d_bext[i].d;
+            item = q;
+        }
+        return r;
+    }
     const int64_t per_item = a.tiles_a * a.tiles_b;
     int64_t item = t / per_item;
     const int64_t local = t - item * per_item;
@@ -235,24 +260,22 @@ __device__ __forceinline__ TileCoord tile_coord(int64_t t, const TileArgs& a) {
     return r;
 }
 
-
-// Destination context of tile t.
+// Destination record of the tile at coordinates tc.
 template <int EB>
-__device__ __forceinline__ TileCtx make_ctx(int64_t t, const TileArgs& a) {
-    const TileCoord tc = tile_coord(t, a);
-    TileCtx c;
-    c.dst = a.dst;
-    c.ext_a = a.ext_a;
-    c.ext_b = a.ext_b;
-    c.ds_a = a.ds_a;
-    c.a0 = tc.ta * (kRowBytes / EB);
-    c.b0 = tc.tb * kRows;
-    c.vec = a.vec_store != 0;
-    int64_t base = c.a0 * a.ds_a + c.b0;
+__device__ __forceinline__ TileOut make_out(const TileCoord& tc, const TileArgs& a) {
+    constexpr int TA = kRowBytes / EB;
+    const int64_t a0 = tc.ta * TA, b0 = tc.tb * kRows;
+    int64_t base = a0 * a.ds_a + b0;
 #pragma unroll
     for (int i = 0; i < 3; ++i) base += tc.bc[i] * a.bds[i];
-    c.dst_base = base;
-    return c;
+    TileOut o;
+    o.base = a.dst + base * EB;
+    o.cstride = a.ds_a * EB;
+    o.cols = (int32_t)min((int64_t)TA, a.ext_a - a0);
+    o.rows = (int32_t)min((int64_t)kRows, a.ext_b - b0);
+    o.vec = a.vec_store;
+    o.full = (o.vec && o.cols == TA && o.rows == kRows) ? 1 : 0;
+    return o;
 }
 
 }  // namespace tile

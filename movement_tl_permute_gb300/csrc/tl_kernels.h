@@ -56,6 +56,12 @@ struct TileArgs {
     int64_t bext[3];
     int64_t bds[3];                      // dst strides of the batch axes, elements
     uint64_t timeout_ns;
+    // 32-bit tile decode (use32 = 1 when tile indices fit in 32 bits)
+    int32_t use32, pad2;
+    dev::DivU32 d_item;                  // tiles per batch item
+    dev::DivU32 d_grp;                   // tiles per group of group_b tile rows
+    dev::DivU32 d_gfull, d_glast;        // full / last group height
+    dev::DivU32 d_bext[3];
 };
 int tile_smem_bytes();
 template <int EB>

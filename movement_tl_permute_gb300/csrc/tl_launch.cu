@@ -162,7 +162,7 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas) {
         }
         break;
     case TL_PATH_ROWS:
-        l.block = 256;
+        l.block = p.ext_b >= 16 ? 128 : 256;   // must match rows_threads<R>() in k_rows.cu
         if (sms) l.grid = cap_grid((p.tiles + 511) / 512, sms * 8, max_ctas);
         break;
     case TL_PATH_WARP:
@@ -261,6 +261,15 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         for (int i = 0; i < 3; ++i) { a.bext[i] = 1; a.bds[i] = 0; }
         int64_t bss[3];
         batch_inner_first(p, a.bext, bss, a.bds);
+        a.use32 = p.tiles < (1LL << 32) ? 1 : 0;
+        if (a.use32) {
+            const int64_t glast = a.tiles_b - ((a.tiles_b - 1) / a.group_b) * a.group_b;
+            a.d_item = dev::make_divu32((uint32_t)(a.tiles_a * a.tiles_b));
+            a.d_grp = dev::make_divu32((uint32_t)(a.group_b * a.tiles_a));
+            a.d_gfull = dev::make_divu32((uint32_t)a.group_b);
+            a.d_glast = dev::make_divu32((uint32_t)glast);
+            fill_divs(3, a.bext, a.d_bext);
+        }
         a.timeout_ns = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? kTestTimeoutNs : kDefaultTimeoutNs;
         a.pad = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? 1 : 0;
         if (p.path == TL_PATH_CLUSTER) {

@@ -287,3 +287,22 @@ def test_dst_overlap_check_is_sound():
         accepted += 1
         assert L.offsets_unique(shape, ds), (shape, ds)
     assert accepted > 30
+
+
+def _stage_chunk(c):
+    """Physical 16-byte chunk of staged chunk c in the rows kernel's warp stage."""
+    return c ^ (((c >> 3) ^ (c >> 6)) & 7)
+
+
+@pytest.mark.parametrize("R", [2, 4, 8, 16])
+def test_rows_kernel_stage_is_conflict_free(R):
+    # writes: lane l parks its k-th output vector as chunk l*R + k
+    for k in range(R):
+        lanes = [_stage_chunk(l * R + k) for l in range(32)]
+        assert tl.tl_bank_conflicts(lanes, 16, "hardware") == 1
+    # read-back: lane l takes chunk 32*i + l, so stores are contiguous per instruction
+    for i in range(R):
+        lanes = [_stage_chunk(32 * i + l) for l in range(32)]
+        assert tl.tl_bank_conflicts(lanes, 16, "hardware") == 1
+    # the swizzle is a permutation of the warp's stage
+    assert sorted(_stage_chunk(c) for c in range(32 * R)) == list(range(32 * R))

@@ -59,7 +59,9 @@ class TlLayout(ctypes.Structure):
 
 class TlPermuteOpts(ctypes.Structure):
     _fields_ = [("flags", ctypes.c_uint32), ("max_ctas", _i32), ("dev_status", ctypes.c_void_p),
-                ("src_bytes", _i64), ("dst_bytes", _i64), ("reserved", _i64 * 4)]
+                ("src_bytes", _i64), ("dst_bytes", _i64), ("tile_group", _i32),
+                ("tile_stages", _i32), ("tile_ctas_per_sm", _i32), ("tile_l2_promotion", _i32),
+                ("reserved", _i64 * 2)]
 
 
 class TlPlanInfo(ctypes.Structure):
@@ -183,8 +185,13 @@ def tl_bank_conflicts(lane_offsets, elem_bytes, model="conservative") -> int:
                   "tl_bank_conflicts")
 
 
-def _opts(flags=0, path="auto", dev_status=0, src_bytes=0, dst_bytes=0, max_ctas=0):
+def _opts(flags=0, path="auto", dev_status=0, src_bytes=0, dst_bytes=0, max_ctas=0,
+          tile_group=0, tile_stages=0, tile_ctas_per_sm=0, tile_l2_promotion=0):
     o = TlPermuteOpts()
+    o.tile_group = int(tile_group)
+    o.tile_stages = int(tile_stages)
+    o.tile_ctas_per_sm = int(tile_ctas_per_sm)
+    o.tile_l2_promotion = int(tile_l2_promotion)
     o.flags = (PATHS[path] if isinstance(path, str) else int(path)) | int(flags)
     o.max_ctas = int(max_ctas)
     o.dev_status = int(dev_status) or None
@@ -205,7 +212,8 @@ def tl_permute(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides, elem
 def tl_permute_ex(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides,
                   elem_bytes: int, stream: int = 0, **opts) -> None:
     """tl_permute with options: path=..., flags=..., dev_status=<device ptr>,
-    src_bytes=..., dst_bytes=..., max_ctas=..."""
+    src_bytes=..., dst_bytes=..., max_ctas=..., and the tile tuning fields
+    tile_group, tile_stages, tile_ctas_per_sm, tile_l2_promotion"""
     o = _opts(**opts)
     _check(load().tl_permute_ex(int(src_ptr) or None, int(dst_ptr) or None, len(shape),
                                 _arr(shape), _arr(src_strides), _arr(dst_strides),

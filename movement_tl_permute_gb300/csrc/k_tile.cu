@@ -29,15 +29,16 @@ template <int EB>
 __global__ void __launch_bounds__(kTileThreads)
 k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full[kTileStages];
-    __shared__ __align__(8) uint64_t empty[kTileStages];
-    __shared__ TileOut info[kTileStages];     // destination of the tile in each stage
+    __shared__ __align__(8) uint64_t full[kMaxTileStages];
+    __shared__ __align__(8) uint64_t empty[kMaxTileStages];
+    __shared__ TileOut info[kMaxTileStages];  // destination of the tile in each stage
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t S = (uint32_t)a.stages;    // ring depth, 2 .. kMaxTileStages
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTileStages; ++s) {
+        for (uint32_t s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
@@ -51,8 +52,8 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
             uint32_t issued = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++issued) {
-                const int s = issued % kTileStages;
-                const uint32_t use = issued / kTileStages;
+                const uint32_t use = issued / S;
+                const uint32_t s = issued - use * S;
                 if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1, a.timeout_ns)) {
                     ok = false;
                     break;
@@ -66,8 +67,8 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
             }
             if (!ok) report(a.status, TL_ERR_TIMEOUT);
             // Do not leave while a load may still write this CTA's shared memory.
-            for (uint32_t i = issued > kTileStages ? issued - kTileStages : 0; i < issued; ++i)
-                mbar_wait(&full[i % kTileStages], (i / kTileStages) & 1, a.timeout_ns);
+            for (uint32_t i = issued > S ? issued - S : 0; i < issued; ++i)
+                mbar_wait(&full[i % S], (i / S) & 1, a.timeout_ns);
         }
         return;
     }
@@ -75,8 +76,9 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
     // ---------------- consumers -----------------------------------------------------
     uint32_t it = 0;
     for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++it) {
-        const int s = it % kTileStages;
-        if (!mbar_wait(&full[s], (it / kTileStages) & 1, a.timeout_ns)) {
+        const uint32_t use = it / S;
+        const uint32_t s = it - use * S;
+        if (!mbar_wait(&full[s], use & 1, a.timeout_ns)) {
             if (lane == 0) report(a.status, TL_ERR_TIMEOUT);
             break;
         }
@@ -89,7 +91,7 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
 
 }  // namespace
 
-int tile_smem_bytes() { return kTileStages * kTileBytes + 1024; }
+int tile_smem_bytes(int stages) { return stages * kTileBytes + 1024; }
 
 template <int EB>
 const void* tile_kernel() {
@@ -98,7 +100,7 @@ const void* tile_kernel() {
 
 template <int EB>
 cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st) {
-    k_tile<EB><<<grid, kTileThreads, tile_smem_bytes(), st>>>(map, a);
+    k_tile<EB><<<grid, kTileThreads, tile_smem_bytes(a.stages), st>>>(map, a);
     return cudaGetLastError();
 }
 

@@ -45,7 +45,8 @@ template <int VB>
 cudaError_t launch_chunk(const ChunkArgs& a, int grid, int block, cudaStream_t st);
 
 // ---------------------------------------------------------------- tile (TMA)
-constexpr int kTileStages = 4;
+constexpr int kTileStages = 4;         // ring depth of the cluster variant
+constexpr int kMaxTileStages = 12;     // ring depth limit of the single-CTA tile kernel
 constexpr int kTileThreads = 9 * 32;   // 8 consumer warps + 1 producer warp
 struct TileArgs {
     uint8_t* dst;
@@ -57,13 +58,14 @@ struct TileArgs {
     int64_t bds[3];                      // dst strides of the batch axes, elements
     uint64_t timeout_ns;
     // 32-bit tile decode (use32 = 1 when tile indices fit in 32 bits)
-    int32_t use32, pad2;
+    int32_t use32;
+    int32_t stages;                      // ring depth of the single-CTA kernel
     dev::DivU32 d_item;                  // tiles per batch item
     dev::DivU32 d_grp;                   // tiles per group of group_b tile rows
     dev::DivU32 d_gfull, d_glast;        // full / last group height
     dev::DivU32 d_bext[3];
 };
-int tile_smem_bytes();
+int tile_smem_bytes(int stages);
 template <int EB>
 const void* tile_kernel();
 template <int EB>

@@ -23,9 +23,34 @@ constexpr uint64_t kTestTimeoutNs = 50000000ull;        // 50 ms under the test 
 struct DevInfo {
     bool ready = false;
     int sms = 0;
-    int tile_occ[5] = {};      // CTAs per SM of k_tile<EB>, index log2(EB)
+    int tile_occ[5][kMaxTileStages + 1] = {};  // CTAs per SM of k_tile<EB> by ring depth
     int cluster_occ[5] = {};
 };
+
+// Tile-path tuning after defaults are applied.  The defaults were measured on
+// GB300 over the batched 128x64 tile transpose and the 2-D transposes of every
+// element width: one CTA per SM with a 4-deep ring (about 600 tiles, 10 MB, in
+// flight GPU-wide) beat deeper rings and denser grids on every workload.
+struct TileTuning {
+    int group = 32;         // tile rows visited together
+    int stages = 4;         // ring depth
+    int ctas_per_sm = 0;    // resident CTAs the grid is sized for (0 = path default)
+    int promotion = 256;    // L2 fill size of the TMA loads (0 = none)
+};
+
+TileTuning tile_tuning(const tl_permute_opts* o) {
+    TileTuning t;
+    if (!o) return t;
+    if (o->tile_group > 0) t.group = o->tile_group;
+    if (o->tile_stages >= 2 && o->tile_stages <= kMaxTileStages) t.stages = o->tile_stages;
+    if (o->tile_ctas_per_sm > 0) t.ctas_per_sm = o->tile_ctas_per_sm;
+    if (o->tile_l2_promotion == 64 || o->tile_l2_promotion == 128 ||
+        o->tile_l2_promotion == 256)
+        t.promotion = o->tile_l2_promotion;
+    else if (o->tile_l2_promotion < 0)
+        t.promotion = 0;
+    return t;
+}
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -48,11 +73,13 @@ int get_device_info(DevInfo* out) {
                              tile_kernel<8>(), tile_kernel<16>()};
         for (int i = 0; i < 5; ++i) {
             if (cudaFuncSetAttribute(kt[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     tile_smem_bytes()) != cudaSuccess)
+                                     tile_smem_bytes(kMaxTileStages)) != cudaSuccess)
                 return TL_ERR_CUDA;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.tile_occ[i], kt[i], kTileThreads,
-                                                              tile_smem_bytes()) != cudaSuccess)
-                return TL_ERR_CUDA;
+            for (int st = 2; st <= kMaxTileStages; ++st)
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                        &d.tile_occ[i][st], kt[i], kTileThreads, tile_smem_bytes(st)) !=
+                    cudaSuccess)
+                    return TL_ERR_CUDA;
             // The cluster variant is optional: if its set-up fails it is sized
             // conservatively (one CTA per SM) and the error is cleared.
             const void* kc = cluster_kernel(1 << i);
@@ -92,7 +119,8 @@ void batch_inner_first(const Plan& p, int64_t* ext, int64_t* ss, int64_t* ds) {
 
 // Tensor map over the source plane: dim 0 = a in BYTES (raw bits, type UINT8),
 // dim 1 = b, dims 2.. = batch.  Box = 128 bytes x 128 rows, 128-byte swizzle.
-int encode_tile_map(const Plan& p, const void* src, CUtensorMap* map, int* rank) {
+int encode_tile_map(const Plan& p, const void* src, int promotion, CUtensorMap* map,
+                    int* rank) {
     if (!g_encode) return TL_ERR_CUDA;
     const int eb = p.eb;
     cuuint64_t dims[5];
@@ -111,10 +139,15 @@ int encode_tile_map(const Plan& p, const void* src, CUtensorMap* map, int* rank)
         box[2 + i] = 1;
     }
     *rank = 2 + p.batch.n;
+    const CUtensorMapL2promotion promo =
+        promotion == 64    ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+        : promotion == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+        : promotion == 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                           : CU_TENSOR_MAP_L2_PROMOTION_NONE;
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)*rank,
                           const_cast<void*>(src), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? TL_OK : TL_ERR_CUDA;
 }
 
@@ -129,7 +162,7 @@ struct Launch {
 };
 
 // Launch shape of each path (grid 0 when the device is unknown).
-Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas) {
+Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const TileTuning& tt) {
     Launch l;
     const int64_t sms = d ? d->sms : 0;
     switch (p.path) {
@@ -148,17 +181,24 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas) {
     }
     case TL_PATH_TILE:
         l.block = kTileThreads;
-        l.smem = tile_smem_bytes();
-        if (sms) l.grid = cap_grid(p.tiles, sms * d->tile_occ[log2i(p.eb)], max_ctas);
+        l.smem = tile_smem_bytes(tt.stages);
+        if (sms) {
+            int per_sm = d->tile_occ[log2i(p.eb)][tt.stages];
+            const int want = tt.ctas_per_sm > 0 ? tt.ctas_per_sm : 1;
+            if (want < per_sm) per_sm = want;
+            l.grid = cap_grid(p.tiles, sms * (per_sm < 1 ? 1 : per_sm), max_ctas);
+        }
         break;
     case TL_PATH_CLUSTER:
         l.block = kTileThreads;
         l.smem = cluster_smem_bytes();
         if (sms) {
-            const int64_t pairs = (p.tiles + 1) / 2;
-            int64_t cap = sms * d->cluster_occ[log2i(p.eb)] / 2;
+            // as many clusters as fit: half of each pair only loads, half only stores
+            int per_sm = d->cluster_occ[log2i(p.eb)];
+            if (tt.ctas_per_sm > 0 && tt.ctas_per_sm < per_sm) per_sm = tt.ctas_per_sm;
+            int64_t cap = sms * (per_sm < 1 ? 1 : per_sm) / 2;
             if (cap < 1) cap = 1;
-            l.grid = 2 * cap_grid(pairs, cap, max_ctas > 0 ? (max_ctas + 1) / 2 : 0);
+            l.grid = 2 * cap_grid(p.tiles, cap, max_ctas > 0 ? (max_ctas + 1) / 2 : 0);
         }
         break;
     case TL_PATH_ROWS:
@@ -189,7 +229,8 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
     rc = get_device_info(&d);
     if (rc != TL_OK) return rc;
     const int32_t max_ctas = opts ? opts->max_ctas : 0;
-    const Launch l = launch_shape(p, &d, max_ctas);
+    const TileTuning tt = tile_tuning(opts);
+    const Launch l = launch_shape(p, &d, max_ctas, tt);
     const uint8_t* s8 = static_cast<const uint8_t*>(src);
     uint8_t* d8 = static_cast<uint8_t*>(dst);
     cudaError_t err = cudaSuccess;
@@ -245,7 +286,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
     case TL_PATH_CLUSTER: {
         alignas(64) CUtensorMap map;
         TileArgs a{};
-        rc = encode_tile_map(p, src, &map, &a.rank);
+        rc = encode_tile_map(p, src, tt.promotion, &map, &a.rank);
         if (rc != TL_OK) return rc;
         a.dst = d8;
         a.status = opts ? opts->dev_status : nullptr;
@@ -255,7 +296,8 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.tiles_a = (p.ext_a + p.tile_cols - 1) / p.tile_cols;
         a.tiles_b = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
         a.tiles = p.tiles;
-        a.group_b = 8;
+        a.group_b = tt.group;
+        a.stages = tt.stages;
         a.nbatch = p.batch.n;
         a.vec_store = p.vec_store ? 1 : 0;
         for (int i = 0; i < 3; ++i) { a.bext[i] = 1; a.bds[i] = 0; }
@@ -382,7 +424,8 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     const bool have = p.total > 0 && cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0 &&
                       get_device_info(&d) == TL_OK;
     if (!have) cudaGetLastError();   // clear a "no device" error on CPU-only hosts
-    const Launch l = launch_shape(p, have ? &d : nullptr, opts ? opts->max_ctas : 0);
+    const Launch l =
+        launch_shape(p, have ? &d : nullptr, opts ? opts->max_ctas : 0, tile_tuning(opts));
     info.grid = l.grid;
     info.block = l.block;
     info.smem_bytes = l.smem;

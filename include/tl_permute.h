@@ -178,7 +178,7 @@ typedef struct tl_permute_opts {
     int64_t dst_bytes;    /* > 0: bytes addressable from dst */
     /* Tuning of the tile path; 0 selects the planner's default for each. */
     int32_t tile_group;   /* tile rows visited together (visit order) */
-    int32_t tile_stages;  /* shared-memory ring depth, 2..12 */
+    int32_t tile_stages;  /* shared-memory ring depth: 2..12 (tile), 2..6 (cluster) */
     int32_t tile_ctas_per_sm;  /* resident CTAs per SM the grid is sized for */
     int32_t tile_l2_promotion; /* L2 fill size of the TMA loads: 64, 128, 256, or -1 = none */
     int64_t reserved[2];

@@ -1,19 +1,22 @@
-// k_cluster.cu -- the tile transpose split across a 2-CTA cluster, with the tile
-// handed from one CTA's shared memory to the other's through distributed shared
-// memory (the "copy_async -> dsmem" page of the TVM docs: the source CTA maps
-// the destination's shared address and mbarrier into its own window with mapa
-// and issues cp.async.bulk.shared::cluster; the bytes landing complete the
+// k_cluster.cu -- the tile transpose split across a 2-CTA cluster, with every
+// tile handed from one CTA's shared memory to the other's through distributed
+// shared memory (the "copy_async -> dsmem" page of the TVM docs: the source CTA
+// maps the destination's shared address and mbarrier into its own window with
+// mapa and issues cp.async.bulk.shared::cluster; the bytes landing complete the
 // destination CTA's mbarrier, which the destination armed with expect_tx).
 //
-// Rank 0 of each cluster is the producer: a loader lane streams tiles from HBM
-// into a ring of staging slots with TMA, and a pusher lane forwards each landed
-// tile (16384 bytes, one contiguous chunk) into the matching receive slot of rank
-// 1.  Rank 1 is the consumer: its eight warps transpose the received tile and
-// store it to dst exactly as the single-CTA tile kernel does, then release the
-// receive slot by arriving on rank 0's barrier through DSMEM.  The hand-off is a
-// plain point-to-point bulk copy, not a multicast.  Every wait is bounded; an
-// expired wait records TL_ERR_TIMEOUT in the status word and the CTA drains its
-// own in-flight copies before leaving.
+// The pair is symmetric.  Each CTA runs three roles on its own tiles of the
+// cluster's sequence (CTA r loads the tiles whose sequence index is r mod 2):
+//   * a loader lane streams its tiles from HBM into a ring of staging slots (TMA);
+//   * a pusher lane forwards each landed tile (16384 bytes, one contiguous
+//     chunk) into the matching receive slot of the peer CTA;
+//   * eight consumer warps transpose the tiles the PEER pushed into this CTA's
+//     receive ring, store them to dst, and release each receive slot by arriving
+//     on the peer's barrier through DSMEM.
+// So every SM both reads and writes HBM, and every tile crosses the SM-to-SM
+// network once.  The hand-off is a point-to-point bulk copy, not a multicast.
+// Every wait is bounded; an expired wait records TL_ERR_TIMEOUT in the status
+// word and the CTA drains its own in-flight copies before leaving.
 #include "tile_common.cuh"
 
 namespace tl {
@@ -22,22 +25,32 @@ namespace {
 using namespace dev;
 using namespace tile;
 
-constexpr int kStages = kTileStages;
+constexpr int kLoaderWarp = kConsumerWarps;        // warp 8
+constexpr int kPusherWarp = kConsumerWarps + 1;    // warp 9
+// DSMEM pushes a pusher keeps going: deeper queues measured slower on GB300
+// (the SM-to-SM network saturates), so one push overlaps the next.
+constexpr int kPushesInFlight = 2;
 
 template <int EB>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTileThreads)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kClusterThreads)
 k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t loaded[kStages];   // rank 0: TMA landed in staging slot
-    __shared__ __align__(8) uint64_t staged[kStages];   // rank 0: staging slot free again
-    __shared__ __align__(8) uint64_t freed[kStages];    // rank 0: rank 1's receive slot free
-    __shared__ __align__(8) uint64_t recv[kStages];     // rank 1: tile landed in receive slot
+    __shared__ __align__(8) uint64_t loaded[kMaxClusterStages];  // TMA landed in staging slot
+    __shared__ __align__(8) uint64_t staged[kMaxClusterStages];  // staging slot free again
+    __shared__ __align__(8) uint64_t freed[kMaxClusterStages];   // the PEER's receive slot free
+    __shared__ __align__(8) uint64_t recv[kMaxClusterStages];    // own receive slot, peer-filled
+    const int kStages = a.stages;                                // ring depth (runtime)
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* staging = smem;                            // kStages tiles
+    uint8_t* receive = smem + kStages * kTileBytes;     // kStages tiles
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_rank();
+    const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
     const int64_t cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
     const bool drop = a.pad != 0;   // test hook: the hand-off is skipped
+    // tiles of this cluster: t_k = cluster + k * nclusters; CTA r loads k = 2j + r
+    // and consumes k = 2j + peer.
+    const int64_t step2 = 2 * nclusters;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -51,57 +64,58 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
     __syncthreads();
     cluster_sync_all();   // both CTAs' barriers exist before any remote access
 
-    if (rank == 0) {
-        if (warp == kConsumerWarps && lane == 0) {
-            // ------------------------------ loader ------------------------------
-            uint32_t issued = 0;
-            bool ok = true;
-            for (int64_t t = cluster; t < a.tiles; t += nclusters, ++issued) {
-                const int s = issued % kStages;
-                const uint32_t use = issued / kStages;
-                if (use > 0 && !mbar_wait(&staged[s], (use - 1) & 1, a.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                const TileCoord tc = tile_coord(t, a);
-                mbar_arrive_expect_tx(&loaded[s], kTileBytes);
-                tma_load(smem + s * kTileBytes, &tmap, &loaded[s], a.rank,
-                         (int)(tc.ta * kRowBytes), (int)(tc.tb * kRows), (int)tc.bc[0],
-                         (int)tc.bc[1], (int)tc.bc[2]);
+    if (warp == kLoaderWarp && lane == 0) {
+        // ---------------------------------- loader ----------------------------------
+        uint32_t issued = 0;
+        bool ok = true;
+        for (int64_t t = cluster + rank * nclusters; t < a.tiles; t += step2, ++issued) {
+            const int s = issued % kStages;
+            const uint32_t use = issued / kStages;
+            if (use > 0 && !mbar_wait(&staged[s], (use - 1) & 1, a.timeout_ns)) {
+                ok = false;
+                break;
             }
-            if (!ok) report(a.status, TL_ERR_TIMEOUT);
-            for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-                mbar_wait(&loaded[i % kStages], (i / kStages) & 1, a.timeout_ns);
-        } else if (warp == kConsumerWarps - 1 && lane == 0) {
-            // ------------------------------ pusher ------------------------------
-            uint32_t n = 0;
-            bool ok = true;
-            for (int64_t t = cluster; t < a.tiles; t += nclusters, ++n) {
-                const int s = n % kStages;
-                const uint32_t use = n / kStages;
-                if (!mbar_wait(&loaded[s], use & 1, a.timeout_ns)) { ok = false; break; }
-                if (use > 0 && !mbar_wait_cluster(&freed[s], (use - 1) & 1, a.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                if (!drop) {
-                    const uint32_t dst = map_to_rank(smem_addr(smem + s * kTileBytes), 1);
-                    const uint32_t bar = map_to_rank(smem_addr(&recv[s]), 1);
-                    bulk_copy_to_peer(dst, smem_addr(smem + s * kTileBytes), kTileBytes, bar);
-                }
-                bulk_commit();
-                // the previous push has finished reading its staging slot
-                bulk_wait_read<1>();
-                if (n > 0) mbar_arrive(&staged[(n - 1) % kStages]);
-            }
-            bulk_wait_read<0>();
-            if (n > 0) mbar_arrive(&staged[(n - 1) % kStages]);
-            if (!ok) report(a.status, TL_ERR_TIMEOUT);
+            const TileCoord tc = tile_coord(t, a);
+            mbar_arrive_expect_tx(&loaded[s], kTileBytes);
+            tma_load(staging + s * kTileBytes, &tmap, &loaded[s], a.rank,
+                     (int)(tc.ta * kRowBytes), (int)(tc.tb * kRows), (int)tc.bc[0],
+                     (int)tc.bc[1], (int)tc.bc[2]);
         }
+        if (!ok) report(a.status, TL_ERR_TIMEOUT);
+        for (uint32_t i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+            mbar_wait(&loaded[i % kStages], (i / kStages) & 1, a.timeout_ns);
+    } else if (warp == kPusherWarp && lane == 0) {
+        // ---------------------------------- pusher ----------------------------------
+        uint32_t n = 0;
+        bool ok = true;
+        for (int64_t t = cluster + rank * nclusters; t < a.tiles; t += step2, ++n) {
+            const int s = n % kStages;
+            const uint32_t use = n / kStages;
+            if (!mbar_wait(&loaded[s], use & 1, a.timeout_ns)) { ok = false; break; }
+            if (use > 0 && !mbar_wait_cluster(&freed[s], (use - 1) & 1, a.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            if (!drop) {
+                const uint32_t dst = map_to_rank(smem_addr(receive + s * kTileBytes), peer);
+                const uint32_t bar = map_to_rank(smem_addr(&recv[s]), peer);
+                bulk_copy_to_peer(dst, smem_addr(staging + s * kTileBytes), kTileBytes, bar);
+            }
+            bulk_commit();
+            // up to kPushesInFlight pushes may still read their staging slots; the
+            // one issued kPushesInFlight - 1 pushes ago has finished
+            bulk_wait_read<kPushesInFlight - 1>();
+            if (n + 1 >= kPushesInFlight)
+                mbar_arrive(&staged[(n + 1 - kPushesInFlight) % kStages]);
+        }
+        bulk_wait_read<0>();
+        for (uint32_t i = n + 1 > kPushesInFlight ? n + 1 - kPushesInFlight : 0; i < n; ++i)
+            mbar_arrive(&staged[i % kStages]);
+        if (!ok) report(a.status, TL_ERR_TIMEOUT);
     } else if (warp < kConsumerWarps) {
-        // ------------------------------ consumer ------------------------------
+        // --------------------------------- consumers --------------------------------
         uint32_t it = 0;
-        for (int64_t t = cluster; t < a.tiles; t += nclusters, ++it) {
+        for (int64_t t = cluster + peer * nclusters; t < a.tiles; t += step2, ++it) {
             const int s = it % kStages;
             if (threadIdx.x == 0) mbar_arrive_expect_tx(&recv[s], kTileBytes);
             if (!mbar_wait_cluster(&recv[s], (it / kStages) & 1, a.timeout_ns)) {
@@ -109,9 +123,9 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                 break;
             }
             const TileOut o = make_out<EB>(tile_coord(t, a), a);
-            consume<EB>(smem_addr(smem + s * kTileBytes), o, warp, lane);
+            consume<EB>(smem_addr(receive + s * kTileBytes), o, warp, lane);
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(map_to_rank(smem_addr(&freed[s]), 0));
+            if (lane == 0) mbar_arrive_remote(map_to_rank(smem_addr(&freed[s]), peer));
         }
     }
     __syncwarp();
@@ -121,13 +135,13 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
 
 template <int EB>
 cudaError_t go(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st) {
-    k_cluster<EB><<<grid, kTileThreads, cluster_smem_bytes(), st>>>(map, a);
+    k_cluster<EB><<<grid, kClusterThreads, cluster_smem_bytes(a.stages), st>>>(map, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int cluster_smem_bytes() { return kStages * kTileBytes + 1024; }
+int cluster_smem_bytes(int stages) { return 2 * stages * kTileBytes + 1024; }
 
 const void* cluster_kernel(int eb) {
     switch (eb) {

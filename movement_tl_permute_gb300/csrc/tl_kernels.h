@@ -45,9 +45,10 @@ template <int VB>
 cudaError_t launch_chunk(const ChunkArgs& a, int grid, int block, cudaStream_t st);
 
 // ---------------------------------------------------------------- tile (TMA)
-constexpr int kTileStages = 4;         // ring depth of the cluster variant
+constexpr int kMaxClusterStages = 6;   // ring depth limit of the cluster variant (x2 rings)
 constexpr int kMaxTileStages = 12;     // ring depth limit of the single-CTA tile kernel
 constexpr int kTileThreads = 9 * 32;   // 8 consumer warps + 1 producer warp
+constexpr int kClusterThreads = 10 * 32;  // 8 consumer warps + loader warp + pusher warp
 struct TileArgs {
     uint8_t* dst;
     int32_t* status;
@@ -59,7 +60,7 @@ struct TileArgs {
     uint64_t timeout_ns;
     // 32-bit tile decode (use32 = 1 when tile indices fit in 32 bits)
     int32_t use32;
-    int32_t stages;                      // ring depth of the single-CTA kernel
+    int32_t stages;                      // ring depth
     dev::DivU32 d_item;                  // tiles per batch item
     dev::DivU32 d_grp;                   // tiles per group of group_b tile rows
     dev::DivU32 d_gfull, d_glast;        // full / last group height
@@ -72,7 +73,7 @@ template <int EB>
 cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st);
 
 // tile path with a 2-CTA cluster and a DSMEM hand-off (k_cluster.cu)
-int cluster_smem_bytes();
+int cluster_smem_bytes(int stages);
 const void* cluster_kernel(int eb);
 cudaError_t launch_cluster(int eb, const CUtensorMap& map, const TileArgs& a, int grid,
                            cudaStream_t st);

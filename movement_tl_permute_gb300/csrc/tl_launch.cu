@@ -24,7 +24,7 @@ struct DevInfo {
     bool ready = false;
     int sms = 0;
     int tile_occ[5][kMaxTileStages + 1] = {};  // CTAs per SM of k_tile<EB> by ring depth
-    int cluster_occ[5] = {};
+    int cluster_occ[5][kMaxClusterStages + 1] = {};   // by ring depth
 };
 
 // Tile-path tuning after defaults are applied.  The defaults were measured on
@@ -36,6 +36,9 @@ struct TileTuning {
     int stages = 4;         // ring depth
     int ctas_per_sm = 0;    // resident CTAs the grid is sized for (0 = path default)
     int promotion = 256;    // L2 fill size of the TMA loads (0 = none)
+    int cluster_stages = 2; // ring depth of the cluster variant (each CTA holds two rings)
+    // The cluster variant is latency-bound per CTA pair, so it runs as many pairs as
+    // fit (measured on GB300: 2-deep rings at 3 CTAs/SM beat deeper rings at 1).
 };
 
 TileTuning tile_tuning(const tl_permute_opts* o) {
@@ -43,6 +46,8 @@ TileTuning tile_tuning(const tl_permute_opts* o) {
     if (!o) return t;
     if (o->tile_group > 0) t.group = o->tile_group;
     if (o->tile_stages >= 2 && o->tile_stages <= kMaxTileStages) t.stages = o->tile_stages;
+    if (o->tile_stages >= 2 && o->tile_stages <= kMaxClusterStages)
+        t.cluster_stages = o->tile_stages;
     if (o->tile_ctas_per_sm > 0) t.ctas_per_sm = o->tile_ctas_per_sm;
     if (o->tile_l2_promotion == 64 || o->tile_l2_promotion == 128 ||
         o->tile_l2_promotion == 256)
@@ -83,13 +88,19 @@ int get_device_info(DevInfo* out) {
             // The cluster variant is optional: if its set-up fails it is sized
             // conservatively (one CTA per SM) and the error is cleared.
             const void* kc = cluster_kernel(1 << i);
-            if (cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     cluster_smem_bytes()) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.cluster_occ[i], kc, kTileThreads,
-                                                              cluster_smem_bytes()) != cudaSuccess ||
-                d.cluster_occ[i] < 1) {
-                cudaGetLastError();
-                d.cluster_occ[i] = 1;
+            const bool attr_ok = cudaFuncSetAttribute(kc,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                      cluster_smem_bytes(kMaxClusterStages)) ==
+                                 cudaSuccess;
+            for (int st = 2; st <= kMaxClusterStages; ++st) {
+                int& occ = d.cluster_occ[i][st];
+                if (!attr_ok || cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                    &occ, kc, kClusterThreads, cluster_smem_bytes(st)) !=
+                                    cudaSuccess ||
+                    occ < 1) {
+                    cudaGetLastError();
+                    occ = 1;
+                }
             }
         }
         if (!g_encode) {
@@ -190,11 +201,11 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         }
         break;
     case TL_PATH_CLUSTER:
-        l.block = kTileThreads;
-        l.smem = cluster_smem_bytes();
+        l.block = kClusterThreads;
+        l.smem = cluster_smem_bytes(tt.cluster_stages);
         if (sms) {
-            // as many clusters as fit: half of each pair only loads, half only stores
-            int per_sm = d->cluster_occ[log2i(p.eb)];
+            // as many clusters as fit
+            int per_sm = d->cluster_occ[log2i(p.eb)][tt.cluster_stages];
             if (tt.ctas_per_sm > 0 && tt.ctas_per_sm < per_sm) per_sm = tt.ctas_per_sm;
             int64_t cap = sms * (per_sm < 1 ? 1 : per_sm) / 2;
             if (cap < 1) cap = 1;
@@ -315,6 +326,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.timeout_ns = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? kTestTimeoutNs : kDefaultTimeoutNs;
         a.pad = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? 1 : 0;
         if (p.path == TL_PATH_CLUSTER) {
+            a.stages = tt.cluster_stages;
             err = launch_cluster(eb, map, a, l.grid, st);
             break;
         }

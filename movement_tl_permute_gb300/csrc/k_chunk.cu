@@ -4,8 +4,10 @@
 // TVM "copy_async -> dsmem" page, "Algorithm" step 1) is one row of `vpr`
 // vectors of VB bytes; the remaining axes (in dst order) place each row.  A
 // group of G = 2^log2g lanes copies one row; consecutive groups take consecutive
-// rows, so a warp writes one contiguous run of dst.  Each thread keeps U rows in
-// flight before it stores.
+// rows, so a warp writes one contiguous run of dst.  A group takes U consecutive
+// rows at a time: it decodes the first row's coordinates and steps the
+// innermost outer axis for the others, and each lane keeps two vectors of each
+// of the U rows in flight before it stores.
 #include "tl_kernels.h"
 
 namespace tl {
@@ -62,31 +64,53 @@ __device__ __forceinline__ void row_offsets(int64_t r, const ChunkArgs& a, int64
 
 template <int VB>
 __global__ void __launch_bounds__(256) k_chunk(const ChunkArgs a) {
-    constexpr int U = 4;
+    constexpr int U = 4;        // consecutive rows per group and round
     using T = typename Vec<VB>::T;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t G = 1LL << a.log2g;
     const int64_t gid = gtid >> a.log2g;
     const int64_t lig = gtid & (G - 1);
     const int64_t ngroups = ((int64_t)gridDim.x * blockDim.x) >> a.log2g;
-    for (int64_t row0 = gid; row0 < a.rows; row0 += ngroups * U) {
+    // innermost outer axis: consecutive rows usually differ only there
+    const int last = a.n - 1;
+    const int64_t ext_last = a.n > 0 ? a.ext[last] : 1;
+    const int64_t ss_last = a.n > 0 ? a.ss[last] : 0, ds_last = a.n > 0 ? a.ds[last] : 0;
+    for (int64_t q = gid; q * U < a.rows; q += ngroups) {
+        const int64_t r0 = q * U;
         int64_t so[U], d[U];
         bool ok[U];
+        row_offsets(r0, a, so[0], d[0]);
+        int64_t c_last = a.n > 0 ? r0 % ext_last : 0;
+        ok[0] = true;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t r = row0 + u * ngroups;
-            ok[u] = r < a.rows;
-            so[u] = d[u] = 0;
-            if (ok[u]) row_offsets(r, a, so[u], d[u]);
+        for (int u = 1; u < U; ++u) {
+            ok[u] = r0 + u < a.rows;
+            if (c_last + 1 < ext_last) {            // step the innermost axis
+                ++c_last;
+                so[u] = so[u - 1] + ss_last;
+                d[u] = d[u - 1] + ds_last;
+            } else {                                // carry: decode afresh
+                c_last = 0;
+                so[u] = d[u] = 0;
+                if (ok[u]) row_offsets(r0 + u, a, so[u], d[u]);
+            }
         }
-        for (int64_t c = lig; c < a.vpr; c += G) {
-            T v[U];
+        // two vectors per lane and row: columns c0 and c0 + G
+        for (int64_t c0 = lig; c0 < a.vpr; c0 += 2 * G) {
+            const bool two = c0 + G < a.vpr;
+            T v0[U], v1[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (ok[u]) v[u] = ld<VB>(a.src + so[u] + c * VB);
+            for (int u = 0; u < U; ++u) {
+                if (!ok[u]) continue;
+                v0[u] = ld<VB>(a.src + so[u] + c0 * VB);
+                if (two) v1[u] = ld<VB>(a.src + so[u] + (c0 + G) * VB);
+            }
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (ok[u]) st<VB>(a.dst + d[u] + c * VB, v[u]);
+            for (int u = 0; u < U; ++u) {
+                if (!ok[u]) continue;
+                st<VB>(a.dst + d[u] + c0 * VB, v0[u]);
+                if (two) st<VB>(a.dst + d[u] + (c0 + G) * VB, v1[u]);
+            }
         }
     }
 }

@@ -162,6 +162,14 @@ int encode_tile_map(const Plan& p, const void* src, int promotion, CUtensorMap* 
     return r == CUDA_SUCCESS ? TL_OK : TL_ERR_CUDA;
 }
 
+// Lanes per row group of the chunk kernel: each lane moves two vectors of a
+// row, so a group has the power of two covering half the row (at most a warp).
+int chunk_group_lanes(int64_t vpr) {
+    int g = 1;
+    while (g < 32 && 2 * g < vpr) g <<= 1;
+    return g;
+}
+
 int cap_grid(int64_t want, int64_t cap, int32_t max_ctas) {
     int64_t g = want < cap ? want : cap;
     if (max_ctas > 0 && g > max_ctas) g = max_ctas;
@@ -184,10 +192,10 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
     case TL_PATH_CHUNK: {
         l.block = 256;
         const int64_t vpr = p.row_elems * p.eb / p.vec_bytes;
-        int g = 1;
-        while (g < 32 && g < vpr) g <<= 1;
+        const int g = chunk_group_lanes(vpr);
         const int64_t groups = 256 / g;
-        if (sms) l.grid = cap_grid((p.rows + groups * 4 - 1) / (groups * 4), sms * 8, max_ctas);
+        // 6 CTAs of 256 threads per SM measured best on GB300 (attention permute)
+        if (sms) l.grid = cap_grid((p.rows + groups * 4 - 1) / (groups * 4), sms * 6, max_ctas);
         break;
     }
     case TL_PATH_TILE:
@@ -273,9 +281,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.dst = d8;
         a.rows = p.rows;
         a.vpr = p.row_elems * eb / p.vec_bytes;
-        int g = 1, lg = 0;
-        while (g < 32 && g < a.vpr) { g <<= 1; ++lg; }
-        a.log2g = lg;
+        a.log2g = log2i(chunk_group_lanes(a.vpr));
         a.n = p.outer.n;
         a.use32 = p.rows < (1LL << 32) ? 1 : 0;
         for (int i = 0; i < a.n; ++i) {

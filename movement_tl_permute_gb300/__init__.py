@@ -114,12 +114,16 @@ def load():
     return _lib
 
 
-def _arr(vals, n=None):
-    vals = [int(v) for v in vals]
-    arr = (_i64 * max(1, len(vals) if n is None else n))()
-    for i, v in enumerate(vals):
-        arr[i] = v
-    return arr
+_ARR_TYPES = [_i64 * n for n in range(TL_MAX_DIMS + 1)]
+
+
+def _arr(vals):
+    n = len(vals)
+    if n == 0:
+        return _ARR_TYPES[1]()
+    if n <= TL_MAX_DIMS:
+        return _ARR_TYPES[n](*vals)
+    return (_i64 * n)(*vals)
 
 
 def _check(rc: int, where: str) -> int:

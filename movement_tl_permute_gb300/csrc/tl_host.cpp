@@ -8,6 +8,7 @@
 // XOR swizzle that keeps both phases bank-conflict-free, stage through registers.
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "tl_internal.h"
@@ -170,9 +171,64 @@ int64_t abs_addr(const void* p) { return (int64_t)(uintptr_t)p; }
 
 bool aligned(int64_t v, int64_t a) { return a <= 1 || v % a == 0; }
 
+// Memo of warp-tile searches: the swizzle search simulates every candidate, and
+// small permutes tend to repeat the same layouts call after call.
+struct WarpMemo {
+    Axes kept;
+    int eb;
+    bool found;
+    int start, P, k, shift, mask;
+};
+std::mutex g_warp_memo_mu;
+std::vector<WarpMemo> g_warp_memo;
+constexpr size_t kWarpMemoMax = 64;
+
+bool same_axes(const Axes& a, const Axes& b) {
+    if (a.n != b.n) return false;
+    for (int i = 0; i < a.n; ++i)
+        if (a.ext[i] != b.ext[i] || a.ss[i] != b.ss[i] || a.ds[i] != b.ds[i]) return false;
+    return true;
+}
+
+bool plan_warp_search(Plan* p);
+
+void apply_warp(Plan* p, int start, int P, int k, int sh, int m) {
+    const Axes& kept = p->kept;
+    Axes t, b;
+    for (int i = start; i < kept.n; ++i) {
+        t.ext[t.n] = kept.ext[i]; t.ss[t.n] = kept.ss[i]; t.ds[t.n] = kept.ds[i]; ++t.n;
+    }
+    for (int i = 0; i < start; ++i) {
+        b.ext[b.n] = kept.ext[i]; b.ss[b.n] = kept.ss[i]; b.ds[b.n] = kept.ds[i]; ++b.n;
+    }
+    p->wtile = t;
+    p->wbatch = b;
+    p->P = P;
+    p->k = k;
+    p->shift = sh;
+    p->mask = m;
+}
+
+bool plan_warp(Plan* p) {
+    {
+        std::lock_guard<std::mutex> lk(g_warp_memo_mu);
+        for (const WarpMemo& e : g_warp_memo)
+            if (e.eb == p->eb && same_axes(e.kept, p->kept)) {
+                if (e.found) apply_warp(p, e.start, e.P, e.k, e.shift, e.mask);
+                return e.found;
+            }
+    }
+    const bool found = plan_warp_search(p);
+    WarpMemo e{p->kept, p->eb, found, p->kept.n - p->wtile.n, p->P, p->k, p->shift, p->mask};
+    std::lock_guard<std::mutex> lk(g_warp_memo_mu);
+    if (g_warp_memo.size() >= kWarpMemoMax) g_warp_memo.erase(g_warp_memo.begin());
+    g_warp_memo.push_back(e);
+    return found;
+}
+
 // Order-kept canonical pair and its warp tile: the smallest innermost suffix that
 // holds a whole number of warp iterations and admits a swizzle.
-bool plan_warp(Plan* p) {
+bool plan_warp_search(Plan* p) {
     const Axes& kept = p->kept;
     if (kept.n == 0) return false;
     int64_t prod = 1;
@@ -188,19 +244,7 @@ bool plan_warp(Plan* p) {
         if (choose_xor(tdims, kept.ext + start, kept.ss + start, kept.ds + start, p->eb, &k, &sh,
                        &m) != TL_OK)
             continue;
-        Axes t, b;
-        for (int i = start; i < kept.n; ++i) {
-            t.ext[t.n] = kept.ext[i]; t.ss[t.n] = kept.ss[i]; t.ds[t.n] = kept.ds[i]; ++t.n;
-        }
-        for (int i = 0; i < start; ++i) {
-            b.ext[b.n] = kept.ext[i]; b.ss[b.n] = kept.ss[i]; b.ds[b.n] = kept.ds[i]; ++b.n;
-        }
-        p->wtile = t;
-        p->wbatch = b;
-        p->P = P;
-        p->k = k;
-        p->shift = sh;
-        p->mask = m;
+        apply_warp(p, start, P, k, sh, m);
         return true;
     }
     return false;
@@ -345,7 +389,11 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     const bool ranges_meet = s0 < d0 + dbytes && d0 < s0 + sbytes;
 
     // eligibility of every path
-    const bool warp_ok = plan_warp(&p);
+    // The warp path's swizzle search simulates every candidate; run it only when
+    // the warp path can be chosen (aliased buffers, forced, or a tiny tensor).
+    const bool warp_wanted = ranges_meet || forced == TL_PATH_WARP ||
+                             (forced == TL_PATH_AUTO && total <= kWarpAutoMaxElems);
+    const bool warp_ok = warp_wanted && plan_warp(&p);
     bool chunk_ok = false;
     if (srt.n == 0 || (srt.ds[srt.n - 1] == 1 && srt.ss[srt.n - 1] == 1)) chunk_ok = true;
     const bool plane = plan_plane(&p);
@@ -361,7 +409,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     } else switch (forced) {
     case TL_PATH_AUTO:
         if (chunk_ok) path = TL_PATH_CHUNK;
-        else if (warp_ok && total <= 8192) path = TL_PATH_WARP;
+        else if (warp_ok) path = TL_PATH_WARP;
         else if (rows) path = TL_PATH_ROWS;
         else if (tile) path = TL_PATH_TILE;
         else path = TL_PATH_GENERIC;

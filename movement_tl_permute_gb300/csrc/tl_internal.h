@@ -13,6 +13,7 @@ constexpr int kMaxBatch = 6;       // batch axes of the transpose paths
 constexpr int kMaxTmaBatch = 3;    // a TMA tensor map has at most 5 dims: a, b + 3 batch
 constexpr int kMaxWarpTileDims = 4;
 constexpr int kWarpMaxRegBytes = 128;  // P * elem_bytes a lane may stage in registers
+constexpr int64_t kWarpAutoMaxElems = 8192;  // tensors the planner gives the warp path
 
 // A list of axes with per-side element strides.
 struct Axes {

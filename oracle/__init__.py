@@ -10,6 +10,8 @@ Contents
 * ``permute`` -- ctypes front of ``permute_ref.c``: the definition
   ``dst[sum c_i*dst_stride_i] = src[sum c_i*src_stride_i]`` for every coordinate
   ``c`` (TVM docs, "Buffers and memory", section "Declaring buffers").
+* ``sample`` -- the same definition evaluated at chosen coordinates one by one,
+  for outputs too large to permute whole on the host.
 * ``layout_ref`` -- pure-Python references for the host logic: slicing and
   canonicalising a pair of layouts, the shared-memory bank model and the XOR
   swizzle chooser of the warp permute (TVM docs, "permute_layout", section
@@ -127,3 +129,23 @@ def permute(src: np.ndarray, dst: np.ndarray, shape, src_strides, dst_strides,
                                 int(elem_bytes), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_permute rejected its arguments (rc=%d)" % rc)
+
+
+def sample(src: np.ndarray, coords: np.ndarray, src_strides, dst_strides, elem_bytes: int,
+           src_offset: int = 0):
+    """The definition at chosen coordinates, one by one.
+
+    ``coords`` is an (n, ndim) integer array.  Returns ``(dst_offsets, values)``:
+    for each coordinate c, the element offset sum(c * dst_strides) it lands at and
+    the elem_bytes bytes found at src[src_offset + sum(c * src_strides)], as an
+    (n, elem_bytes) uint8 array.  For checking outputs too large to permute whole.
+    """
+    coords = np.asarray(coords, dtype=np.int64)
+    ss = np.asarray(src_strides, dtype=np.int64)
+    ds = np.asarray(dst_strides, dtype=np.int64)
+    src_off = src_offset + coords @ ss
+    dst_off = coords @ ds
+    byte_idx = src_off[:, None] * elem_bytes + np.arange(elem_bytes, dtype=np.int64)[None, :]
+    if byte_idx.size and (byte_idx.min() < 0 or byte_idx.max() >= src.nbytes):
+        raise IndexError("sampled coordinate outside the source buffer")
+    return dst_off, src.reshape(-1).view(np.uint8)[byte_idx]

@@ -439,3 +439,20 @@ def test_offsets_unique_brute_force():
     assert not L.offsets_unique((4, 8), (4, 1))
     assert not L.offsets_unique((3,), (0,))
     assert L.offsets_unique((1, 5), (0, 1))
+
+
+def test_sample_agrees_with_whole_permute():
+    """The one-by-one sampler against the whole-tensor loop and numpy."""
+    rng = np.random.default_rng(31)
+    for eb in (1, 2, 16):
+        shape, perm = (5, 7, 3), (2, 0, 1)
+        ss, ds = _perm_layouts(shape, perm)
+        n = int(np.prod(shape))
+        raw = np.frombuffer(rng.bytes(n * eb), dtype=np.uint8).copy()
+        whole = np.zeros_like(raw)
+        oracle.permute(raw, whole, shape, ss, ds, eb)
+        coords = np.array(list(itertools.product(*[range(e) for e in shape])))
+        offs, vals = oracle.sample(raw, coords, ss, ds, eb)
+        got = whole.reshape(-1, eb)[offs]
+        assert np.array_equal(got, vals)
+        assert sorted(offs.tolist()) == list(range(n))            # a bijection

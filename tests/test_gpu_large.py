@@ -73,9 +73,9 @@ def test_tile_path_past_4gib():
 
 def test_chunk_path_past_4gib():
     # (B, H, S, D) -> (B, S, H, D) with 4.3 GB of bf16: row offsets beyond 2^32 bytes
-    shape = (33, 32, 2048, 32)
+    shape = (33, 32, 4096, 512)
     ss = L.row_major_strides(shape)
-    dss = L.row_major_strides((33, 2048, 32, 32))
+    dss = L.row_major_strides((33, 4096, 32, 512))
     ds = (dss[0], dss[2], dss[1], dss[3])
     check_sampled(shape, ss, ds, 2, "chunk", seed=72)
 

@@ -34,7 +34,8 @@ def _sources():
     cu = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     cpp = sorted(glob.glob(os.path.join(CSRC, "*.cpp")))
     deps = (sorted(glob.glob(os.path.join(CSRC, "*.h"))) + sorted(glob.glob(os.path.join(CSRC, "*.cuh")))
-            + sorted(glob.glob(os.path.join(INCLUDE, "*.h"))))
+            + sorted(glob.glob(os.path.join(INCLUDE, "*.h")))
+            + sorted(glob.glob(os.path.join(INCLUDE, "*.cuh"))))
     return cu, cpp, deps
 
 

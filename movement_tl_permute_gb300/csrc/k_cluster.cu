@@ -18,6 +18,7 @@
 // Every wait is bounded; an expired wait records TL_ERR_TIMEOUT in the status
 // word and the CTA drains its own in-flight copies before leaving.
 #include "tile_common.cuh"
+#include "../../include/tl_permute_device.cuh"
 
 namespace tl {
 namespace {
@@ -97,9 +98,11 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                 break;
             }
             if (!drop) {
-                const uint32_t dst = map_to_rank(smem_addr(receive + s * kTileBytes), peer);
-                const uint32_t bar = map_to_rank(smem_addr(&recv[s]), peer);
-                bulk_copy_to_peer(dst, smem_addr(staging + s * kTileBytes), kTileBytes, bar);
+                // the whole 16 KiB tile is one contiguous chunk
+                tl_dev::ChunkLoop one{};
+                one.chunk_bytes = kTileBytes;
+                tl_dev::dsmem_copy_region(receive + s * kTileBytes, staging + s * kTileBytes,
+                                          one, peer, &recv[s]);
             }
             bulk_commit();
             // up to kPushesInFlight pushes may still read their staging slots; the

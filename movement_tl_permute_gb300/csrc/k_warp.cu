@@ -10,31 +10,26 @@
 // shared-memory bank-conflict-free, and because every read of a tile precedes its
 // writes the kernel is correct in place (src == dst, equal per-tile footprints).
 #include "tl_kernels.h"
+#include "../../include/tl_permute_device.cuh"
 
 namespace tl {
 namespace {
 
-__device__ __forceinline__ void tile_offsets(int64_t f, const WarpArgs& a, int64_t& so,
-                                             int64_t& d) {
-    so = 0;
-    d = 0;
-#pragma unroll
-    for (int i = 3; i >= 0; --i) {
-        if (i < a.tn) {
-            const int64_t c = f % a.text[i];
-            f /= a.text[i];
-            so += c * a.tss[i];
-            d += c * a.tds[i];
-        }
-    }
-}
-
 template <int EB, int P>
 __global__ void __launch_bounds__(128) k_warp(const WarpArgs a) {
     using T = typename dev::Bits<EB>::T;
-    const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    tl_dev::WarpTile ts, td;
+    ts.n = td.n = a.tn;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        ts.ext[i] = td.ext[i] = (int32_t)(i < a.tn ? a.text[i] : 1);
+        ts.str[i] = i < a.tn ? a.tss[i] : 0;
+        td.str[i] = i < a.tn ? a.tds[i] : 0;
+    }
+    const T* src = reinterpret_cast<const T*>(a.src);
+    T* dst = reinterpret_cast<T*>(a.dst);
     for (int64_t item = gw; item < a.items; item += nw) {
         int64_t sb = 0, db = 0, rem = item;
 #pragma unroll
@@ -46,23 +41,8 @@ __global__ void __launch_bounds__(128) k_warp(const WarpArgs a) {
                 db += c * a.bds[i];
             }
         }
-        T regs[P];
-#pragma unroll
-        for (int r = 0; r < P; ++r) {                     // phase 1: read via src layout
-            const int j = r ^ ((lane >> a.shift) & a.mask);
-            int64_t so, d;
-            tile_offsets(lane + 32LL * j, a, so, d);
-            regs[r] = *reinterpret_cast<const T*>(a.src + (sb + so) * EB);
-        }
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < P; ++r) {                     // phase 2: write via dst layout
-            const int j = r ^ ((lane >> a.shift) & a.mask);
-            int64_t so, d;
-            tile_offsets(lane + 32LL * j, a, so, d);
-            *reinterpret_cast<T*>(a.dst + (db + d) * EB) = regs[r];
-        }
-        __syncwarp();
+        // phase 1 reads via src strides, warp barrier, phase 2 writes via dst strides
+        tl_dev::warp_permute_layout<P>(dst + db, src + sb, ts, td, a.shift, a.mask);
     }
 }
 

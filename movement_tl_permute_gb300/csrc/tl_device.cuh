@@ -248,19 +248,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
                  : "memory");
 }
 
-// Bulk copy of `bytes` from this CTA's shared memory into another CTA's shared
-// memory; the destination CTA's barrier receives complete_tx(bytes).  Both
-// addresses 16-byte aligned, bytes a multiple of 16 (the rule the TVM
-// "copy_async -> dsmem" page states for its chunk).  Not a multicast.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta,
-                                                  uint32_t bytes, uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
-        " [%0], [%1], %2, [%3];" ::"r"(dst_cluster),
-        "r"(src_cta), "r"(bytes), "r"(bar_cluster)
-        : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

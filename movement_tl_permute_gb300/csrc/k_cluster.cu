@@ -48,7 +48,7 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
     const int64_t cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
-    const bool drop = a.pad != 0;   // test hook: the hand-off is skipped
+    const bool drop = a.drop_handoff != 0;   // test hook: the hand-off is skipped
     // tiles of this cluster: t_k = cluster + k * nclusters; CTA r loads k = 2j + r
     // and consumes k = 2j + peer.
     const int64_t step2 = 2 * nclusters;

@@ -54,7 +54,8 @@ struct TileArgs {
     int32_t* status;
     int64_t ext_a, ext_b, ds_a;          // elements
     int64_t tiles_a, tiles_b, tiles, group_b;
-    int32_t nbatch, rank, vec_store, pad;
+    int32_t nbatch, rank, vec_store;
+    int32_t drop_handoff;                // test hook of the cluster variant
     int64_t bext[3];
     int64_t bds[3];                      // dst strides of the batch axes, elements
     uint64_t timeout_ns;

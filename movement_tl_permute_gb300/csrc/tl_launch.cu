@@ -330,7 +330,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             fill_divs(3, a.bext, a.d_bext);
         }
         a.timeout_ns = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? kTestTimeoutNs : kDefaultTimeoutNs;
-        a.pad = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? 1 : 0;
+        a.drop_handoff = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? 1 : 0;
         if (p.path == TL_PATH_CLUSTER) {
             a.stages = tt.cluster_stages;
             err = launch_cluster(eb, map, a, l.grid, st);

@@ -166,6 +166,10 @@ TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape
 /* Test hook for the cluster path: the producer CTA skips its DSMEM hand-off, so the
  * consumer's bounded wait must expire and report TL_ERR_TIMEOUT in dev_status. */
 #define TL_FLAG_TEST_DROP_HANDOFF (1u << 8)
+/* Launch without programmatic dependent launch (by default a permute may be scheduled
+ * while the previous kernel of the stream drains; it waits for that kernel to complete
+ * before touching global memory, so stream order is unchanged either way). */
+#define TL_FLAG_NO_PDL (1u << 9)
 
 /* Options of tl_permute_ex.  Zero-initialise, then set what you need. */
 typedef struct tl_permute_opts {

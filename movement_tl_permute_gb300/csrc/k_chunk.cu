@@ -64,6 +64,8 @@ __device__ __forceinline__ void row_offsets(int64_t r, const ChunkArgs& a, int64
 
 template <int VB>
 __global__ void __launch_bounds__(256) k_chunk(const ChunkArgs a) {
+    dev::grid_dependency_wait();
+    dev::allow_dependent_launch();
     constexpr int U = 4;        // consecutive rows per group and round
     using T = typename Vec<VB>::T;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -118,15 +120,14 @@ __global__ void __launch_bounds__(256) k_chunk(const ChunkArgs a) {
 }  // namespace
 
 template <int VB>
-cudaError_t launch_chunk(const ChunkArgs& a, int grid, int block, cudaStream_t st) {
-    k_chunk<VB><<<grid, block, 0, st>>>(a);
-    return cudaGetLastError();
+cudaError_t launch_chunk(const ChunkArgs& a, int grid, int block, cudaStream_t st, bool pdl) {
+    return launch_kernel(k_chunk<VB>, dim3(grid), dim3(block), 0, st, pdl, a);
 }
 
-template cudaError_t launch_chunk<1>(const ChunkArgs&, int, int, cudaStream_t);
-template cudaError_t launch_chunk<2>(const ChunkArgs&, int, int, cudaStream_t);
-template cudaError_t launch_chunk<4>(const ChunkArgs&, int, int, cudaStream_t);
-template cudaError_t launch_chunk<8>(const ChunkArgs&, int, int, cudaStream_t);
-template cudaError_t launch_chunk<16>(const ChunkArgs&, int, int, cudaStream_t);
+template cudaError_t launch_chunk<1>(const ChunkArgs&, int, int, cudaStream_t, bool);
+template cudaError_t launch_chunk<2>(const ChunkArgs&, int, int, cudaStream_t, bool);
+template cudaError_t launch_chunk<4>(const ChunkArgs&, int, int, cudaStream_t, bool);
+template cudaError_t launch_chunk<8>(const ChunkArgs&, int, int, cudaStream_t, bool);
+template cudaError_t launch_chunk<16>(const ChunkArgs&, int, int, cudaStream_t, bool);
 
 }  // namespace tl

@@ -64,6 +64,8 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
     }
     __syncthreads();
     cluster_sync_all();   // both CTAs' barriers exist before any remote access
+    grid_dependency_wait();
+    allow_dependent_launch();
 
     if (warp == kLoaderWarp && lane == 0) {
         // ---------------------------------- loader ----------------------------------
@@ -137,9 +139,9 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
 }
 
 template <int EB>
-cudaError_t go(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st) {
-    k_cluster<EB><<<grid, kClusterThreads, cluster_smem_bytes(a.stages), st>>>(map, a);
-    return cudaGetLastError();
+cudaError_t go(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st, bool pdl) {
+    return launch_kernel(k_cluster<EB>, dim3(grid), dim3(kClusterThreads),
+                         cluster_smem_bytes(a.stages), st, pdl, map, a);
 }
 
 }  // namespace
@@ -157,13 +159,13 @@ const void* cluster_kernel(int eb) {
 }
 
 cudaError_t launch_cluster(int eb, const CUtensorMap& map, const TileArgs& a, int grid,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool pdl) {
     switch (eb) {
-    case 1: return go<1>(map, a, grid, st);
-    case 2: return go<2>(map, a, grid, st);
-    case 4: return go<4>(map, a, grid, st);
-    case 8: return go<8>(map, a, grid, st);
-    default: return go<16>(map, a, grid, st);
+    case 1: return go<1>(map, a, grid, st, pdl);
+    case 2: return go<2>(map, a, grid, st, pdl);
+    case 4: return go<4>(map, a, grid, st, pdl);
+    case 8: return go<8>(map, a, grid, st, pdl);
+    default: return go<16>(map, a, grid, st, pdl);
     }
 }
 

@@ -12,6 +12,8 @@ namespace {
 
 template <int EB>
 __global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
+    dev::grid_dependency_wait();
+    dev::allow_dependent_launch();
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
     for (int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; f < a.total; f += step) {
         int64_t so = 0, d = 0;
@@ -46,15 +48,14 @@ __global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
 }  // namespace
 
 template <int EB>
-cudaError_t launch_generic(const GenericArgs& a, int grid, int block, cudaStream_t st) {
-    k_generic<EB><<<grid, block, 0, st>>>(a);
-    return cudaGetLastError();
+cudaError_t launch_generic(const GenericArgs& a, int grid, int block, cudaStream_t st, bool pdl) {
+    return launch_kernel(k_generic<EB>, dim3(grid), dim3(block), 0, st, pdl, a);
 }
 
-template cudaError_t launch_generic<1>(const GenericArgs&, int, int, cudaStream_t);
-template cudaError_t launch_generic<2>(const GenericArgs&, int, int, cudaStream_t);
-template cudaError_t launch_generic<4>(const GenericArgs&, int, int, cudaStream_t);
-template cudaError_t launch_generic<8>(const GenericArgs&, int, int, cudaStream_t);
-template cudaError_t launch_generic<16>(const GenericArgs&, int, int, cudaStream_t);
+template cudaError_t launch_generic<1>(const GenericArgs&, int, int, cudaStream_t, bool);
+template cudaError_t launch_generic<2>(const GenericArgs&, int, int, cudaStream_t, bool);
+template cudaError_t launch_generic<4>(const GenericArgs&, int, int, cudaStream_t, bool);
+template cudaError_t launch_generic<8>(const GenericArgs&, int, int, cudaStream_t, bool);
+template cudaError_t launch_generic<16>(const GenericArgs&, int, int, cudaStream_t, bool);
 
 }  // namespace tl

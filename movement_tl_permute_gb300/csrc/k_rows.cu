@@ -105,6 +105,8 @@ template <int R> __host__ __device__ constexpr int rows_units() { return R >= 8 
 
 template <int EB, int R>
 __global__ void __launch_bounds__(rows_threads<R>()) k_rows(const RowsArgs a) {
+    dev::grid_dependency_wait();
+    dev::allow_dependent_launch();
     constexpr int U = rows_units<R>();
     constexpr int kWarps = rows_threads<R>() / 32;
     __shared__ __align__(16) uint4 stage[kWarps][32 * R];
@@ -157,26 +159,26 @@ __global__ void __launch_bounds__(rows_threads<R>()) k_rows(const RowsArgs a) {
 }
 
 template <int EB, int R>
-cudaError_t go(const RowsArgs& a, int grid, int block, cudaStream_t st) {
+cudaError_t go(const RowsArgs& a, int grid, int block, cudaStream_t st, bool pdl) {
     if (block != rows_threads<R>()) return cudaErrorInvalidValue;
-    k_rows<EB, R><<<grid, block, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(k_rows<EB, R>, dim3(grid), dim3(block), 0, st, pdl, a);
 }
 
 }  // namespace
 
-cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, cudaStream_t st) {
+cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, cudaStream_t st,
+                        bool pdl) {
     switch (eb * 100 + r) {
-    case 102: return go<1, 2>(a, grid, block, st);
-    case 104: return go<1, 4>(a, grid, block, st);
-    case 108: return go<1, 8>(a, grid, block, st);
-    case 116: return go<1, 16>(a, grid, block, st);
-    case 202: return go<2, 2>(a, grid, block, st);
-    case 204: return go<2, 4>(a, grid, block, st);
-    case 208: return go<2, 8>(a, grid, block, st);
-    case 402: return go<4, 2>(a, grid, block, st);
-    case 404: return go<4, 4>(a, grid, block, st);
-    case 802: return go<8, 2>(a, grid, block, st);
+    case 102: return go<1, 2>(a, grid, block, st, pdl);
+    case 104: return go<1, 4>(a, grid, block, st, pdl);
+    case 108: return go<1, 8>(a, grid, block, st, pdl);
+    case 116: return go<1, 16>(a, grid, block, st, pdl);
+    case 202: return go<2, 2>(a, grid, block, st, pdl);
+    case 204: return go<2, 4>(a, grid, block, st, pdl);
+    case 208: return go<2, 8>(a, grid, block, st, pdl);
+    case 402: return go<4, 2>(a, grid, block, st, pdl);
+    case 404: return go<4, 4>(a, grid, block, st, pdl);
+    case 802: return go<8, 2>(a, grid, block, st, pdl);
     default: return cudaErrorInvalidValue;
     }
 }

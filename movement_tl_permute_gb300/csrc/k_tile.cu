@@ -45,6 +45,9 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
         fence_barrier_init();
     }
     __syncthreads();
+    // everything above touched shared memory only
+    grid_dependency_wait();
+    allow_dependent_launch();
 
     if (warp == kConsumerWarps) {
         // ---------------- producer: one elected lane issues all TMA loads -------------
@@ -99,14 +102,16 @@ const void* tile_kernel() {
 }
 
 template <int EB>
-cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st) {
-    k_tile<EB><<<grid, kTileThreads, tile_smem_bytes(a.stages), st>>>(map, a);
-    return cudaGetLastError();
+cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st,
+                        bool pdl) {
+    return launch_kernel(k_tile<EB>, dim3(grid), dim3(kTileThreads), tile_smem_bytes(a.stages), st,
+                         pdl, map, a);
 }
 
 #define TL_INST(EB)                                                                         \
     template const void* tile_kernel<EB>();                                                 \
-    template cudaError_t launch_tile<EB>(const CUtensorMap&, const TileArgs&, int, cudaStream_t);
+    template cudaError_t launch_tile<EB>(const CUtensorMap&, const TileArgs&, int, cudaStream_t, \
+                                         bool);
 TL_INST(1)
 TL_INST(2)
 TL_INST(4)

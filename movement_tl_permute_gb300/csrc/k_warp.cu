@@ -17,6 +17,8 @@ namespace {
 
 template <int EB, int P>
 __global__ void __launch_bounds__(128) k_warp(const WarpArgs a) {
+    dev::grid_dependency_wait();
+    dev::allow_dependent_launch();
     using T = typename dev::Bits<EB>::T;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -47,33 +49,33 @@ __global__ void __launch_bounds__(128) k_warp(const WarpArgs a) {
 }
 
 template <int EB, int P>
-cudaError_t go(const WarpArgs& a, int grid, int block, cudaStream_t st) {
-    k_warp<EB, P><<<grid, block, 0, st>>>(a);
-    return cudaGetLastError();
+cudaError_t go(const WarpArgs& a, int grid, int block, cudaStream_t st, bool pdl) {
+    return launch_kernel(k_warp<EB, P>, dim3(grid), dim3(block), 0, st, pdl, a);
 }
 
 template <int EB>
-cudaError_t by_p(int P, const WarpArgs& a, int grid, int block, cudaStream_t st) {
+cudaError_t by_p(int P, const WarpArgs& a, int grid, int block, cudaStream_t st, bool pdl) {
     switch (P) {
-    case 1: return go<EB, 1>(a, grid, block, st);
-    case 2: return go<EB, 2>(a, grid, block, st);
-    case 4: return go<EB, 4>(a, grid, block, st);
-    case 8: return go<EB, 8>(a, grid, block, st);
-    case 16: if constexpr (EB <= 8) return go<EB, 16>(a, grid, block, st); break;
-    case 32: if constexpr (EB <= 4) return go<EB, 32>(a, grid, block, st); break;
+    case 1: return go<EB, 1>(a, grid, block, st, pdl);
+    case 2: return go<EB, 2>(a, grid, block, st, pdl);
+    case 4: return go<EB, 4>(a, grid, block, st, pdl);
+    case 8: return go<EB, 8>(a, grid, block, st, pdl);
+    case 16: if constexpr (EB <= 8) return go<EB, 16>(a, grid, block, st, pdl); break;
+    case 32: if constexpr (EB <= 4) return go<EB, 32>(a, grid, block, st, pdl); break;
     }
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_warp(int eb, int P, const WarpArgs& a, int grid, int block, cudaStream_t st) {
+cudaError_t launch_warp(int eb, int P, const WarpArgs& a, int grid, int block, cudaStream_t st,
+                        bool pdl) {
     switch (eb) {
-    case 1: return by_p<1>(P, a, grid, block, st);
-    case 2: return by_p<2>(P, a, grid, block, st);
-    case 4: return by_p<4>(P, a, grid, block, st);
-    case 8: return by_p<8>(P, a, grid, block, st);
-    case 16: return by_p<16>(P, a, grid, block, st);
+    case 1: return by_p<1>(P, a, grid, block, st, pdl);
+    case 2: return by_p<2>(P, a, grid, block, st, pdl);
+    case 4: return by_p<4>(P, a, grid, block, st, pdl);
+    case 8: return by_p<8>(P, a, grid, block, st, pdl);
+    case 16: return by_p<16>(P, a, grid, block, st, pdl);
     }
     return cudaErrorInvalidValue;
 }

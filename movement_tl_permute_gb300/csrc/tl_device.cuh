@@ -184,6 +184,17 @@ __device__ __forceinline__ uint4 ldg128(const void* p) {
     return v;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream drains; it
+// must wait for that kernel's completion (and memory visibility) before any
+// global access.  Without the launch attribute both instructions are no-ops.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Records the first error of a launch in the caller's status word (if any).
 __device__ __forceinline__ void report(int32_t* status, int32_t code) {
     if (status) atomicCAS(status, 0, code);

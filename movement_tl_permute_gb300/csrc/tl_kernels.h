@@ -9,7 +9,27 @@
 #include "../../include/tl_permute.h"
 #include "tl_device.cuh"
 
+#include <utility>
+
 namespace tl {
+
+// Launches `kernel` on `st`, with programmatic stream serialization when `pdl`
+// (the kernels call dev::grid_dependency_wait before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- generic
 struct GenericArgs {
@@ -24,7 +44,7 @@ struct GenericArgs {
     dev::DivU32 div[TL_MAX_DIMS];
 };
 template <int EB>
-cudaError_t launch_generic(const GenericArgs& a, int grid, int block, cudaStream_t st);
+cudaError_t launch_generic(const GenericArgs& a, int grid, int block, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- chunk
 struct ChunkArgs {
@@ -42,7 +62,7 @@ struct ChunkArgs {
     dev::DivU32 div[TL_MAX_DIMS];
 };
 template <int VB>
-cudaError_t launch_chunk(const ChunkArgs& a, int grid, int block, cudaStream_t st);
+cudaError_t launch_chunk(const ChunkArgs& a, int grid, int block, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- tile (TMA)
 constexpr int kMaxClusterStages = 6;   // ring depth limit of the cluster variant (x2 rings)
@@ -71,13 +91,14 @@ int tile_smem_bytes(int stages);
 template <int EB>
 const void* tile_kernel();
 template <int EB>
-cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st,
+                        bool pdl);
 
 // tile path with a 2-CTA cluster and a DSMEM hand-off (k_cluster.cu)
 int cluster_smem_bytes(int stages);
 const void* cluster_kernel(int eb);
 cudaError_t launch_cluster(int eb, const CUtensorMap& map, const TileArgs& a, int grid,
-                           cudaStream_t st);
+                           cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- rows
 struct RowsArgs {
@@ -94,7 +115,8 @@ struct RowsArgs {
     dev::DivU32 div_upr;
     dev::DivU32 div[TL_MAX_DIMS];
 };
-cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, cudaStream_t st);
+cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, cudaStream_t st,
+                        bool pdl);
 
 // ---------------------------------------------------------------- warp
 struct WarpArgs {
@@ -106,6 +128,7 @@ struct WarpArgs {
     int64_t text[4], tss[4], tds[4];
     int64_t bext[TL_MAX_DIMS], bss[TL_MAX_DIMS], bds[TL_MAX_DIMS];
 };
-cudaError_t launch_warp(int eb, int P, const WarpArgs& a, int grid, int block, cudaStream_t st);
+cudaError_t launch_warp(int eb, int P, const WarpArgs& a, int grid, int block, cudaStream_t st,
+                        bool pdl);
 
 }  // namespace tl

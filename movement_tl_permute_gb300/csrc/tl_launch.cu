@@ -250,6 +250,8 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
     const int32_t max_ctas = opts ? opts->max_ctas : 0;
     const TileTuning tt = tile_tuning(opts);
     const Launch l = launch_shape(p, &d, max_ctas, tt);
+    // overlap this launch with the drain of the previous kernel in the stream
+    const bool pdl = (flags & TL_FLAG_NO_PDL) == 0;
     const uint8_t* s8 = static_cast<const uint8_t*>(src);
     uint8_t* d8 = static_cast<uint8_t*>(dst);
     cudaError_t err = cudaSuccess;
@@ -267,11 +269,11 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         }
         if (a.use32) fill_divs(a.n, a.ext, a.div);
         switch (eb) {
-        case 1: err = launch_generic<1>(a, l.grid, l.block, st); break;
-        case 2: err = launch_generic<2>(a, l.grid, l.block, st); break;
-        case 4: err = launch_generic<4>(a, l.grid, l.block, st); break;
-        case 8: err = launch_generic<8>(a, l.grid, l.block, st); break;
-        default: err = launch_generic<16>(a, l.grid, l.block, st); break;
+        case 1: err = launch_generic<1>(a, l.grid, l.block, st, pdl); break;
+        case 2: err = launch_generic<2>(a, l.grid, l.block, st, pdl); break;
+        case 4: err = launch_generic<4>(a, l.grid, l.block, st, pdl); break;
+        case 8: err = launch_generic<8>(a, l.grid, l.block, st, pdl); break;
+        default: err = launch_generic<16>(a, l.grid, l.block, st, pdl); break;
         }
         break;
     }
@@ -291,11 +293,11 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         }
         if (a.use32) fill_divs(a.n, a.ext, a.div);
         switch (p.vec_bytes) {
-        case 16: err = launch_chunk<16>(a, l.grid, l.block, st); break;
-        case 8: err = launch_chunk<8>(a, l.grid, l.block, st); break;
-        case 4: err = launch_chunk<4>(a, l.grid, l.block, st); break;
-        case 2: err = launch_chunk<2>(a, l.grid, l.block, st); break;
-        default: err = launch_chunk<1>(a, l.grid, l.block, st); break;
+        case 16: err = launch_chunk<16>(a, l.grid, l.block, st, pdl); break;
+        case 8: err = launch_chunk<8>(a, l.grid, l.block, st, pdl); break;
+        case 4: err = launch_chunk<4>(a, l.grid, l.block, st, pdl); break;
+        case 2: err = launch_chunk<2>(a, l.grid, l.block, st, pdl); break;
+        default: err = launch_chunk<1>(a, l.grid, l.block, st, pdl); break;
         }
         break;
     }
@@ -333,15 +335,15 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.drop_handoff = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? 1 : 0;
         if (p.path == TL_PATH_CLUSTER) {
             a.stages = tt.cluster_stages;
-            err = launch_cluster(eb, map, a, l.grid, st);
+            err = launch_cluster(eb, map, a, l.grid, st, pdl);
             break;
         }
         switch (eb) {
-        case 1: err = launch_tile<1>(map, a, l.grid, st); break;
-        case 2: err = launch_tile<2>(map, a, l.grid, st); break;
-        case 4: err = launch_tile<4>(map, a, l.grid, st); break;
-        case 8: err = launch_tile<8>(map, a, l.grid, st); break;
-        default: err = launch_tile<16>(map, a, l.grid, st); break;
+        case 1: err = launch_tile<1>(map, a, l.grid, st, pdl); break;
+        case 2: err = launch_tile<2>(map, a, l.grid, st, pdl); break;
+        case 4: err = launch_tile<4>(map, a, l.grid, st, pdl); break;
+        case 8: err = launch_tile<8>(map, a, l.grid, st, pdl); break;
+        default: err = launch_tile<16>(map, a, l.grid, st, pdl); break;
         }
         break;
     }
@@ -361,7 +363,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             a.div_upr = dev::make_divu32((uint32_t)a.upr);
             fill_divs(a.n, a.ext, a.div);
         }
-        err = launch_rows(eb, (int)p.ext_b, a, l.grid, l.block, st);
+        err = launch_rows(eb, (int)p.ext_b, a, l.grid, l.block, st, pdl);
         break;
     }
     case TL_PATH_WARP: {
@@ -379,7 +381,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         for (int i = 0; i < a.bn; ++i) {
             a.bext[i] = p.wbatch.ext[i]; a.bss[i] = p.wbatch.ss[i]; a.bds[i] = p.wbatch.ds[i];
         }
-        err = launch_warp(eb, p.P, a, l.grid, l.block, st);
+        err = launch_warp(eb, p.P, a, l.grid, l.block, st, pdl);
         break;
     }
     default:

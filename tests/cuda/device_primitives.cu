@@ -114,8 +114,12 @@ cudaError_t go_frag(const void* src, void* dst, const TileArgs& a) {
     case 404: return FN<4, 4>(src, dst, a);                                    \
     case 408: return FN<4, 8>(src, dst, a);                                    \
     case 416: return FN<4, 16>(src, dst, a);                                   \
+    case 116: return FN<1, 16>(src, dst, a);                                   \
+    case 216: return FN<2, 16>(src, dst, a);                                   \
     case 802: return FN<8, 2>(src, dst, a);                                    \
     case 804: return FN<8, 4>(src, dst, a);                                    \
+    case 808: return FN<8, 8>(src, dst, a);                                    \
+    case 1608: return FN<16, 8>(src, dst, a);                                  \
     case 1602: return FN<16, 2>(src, dst, a);                                  \
     case 1604: return FN<16, 4>(src, dst, a);                                  \
     }                                                                          \

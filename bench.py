@@ -96,20 +96,75 @@ def whole_job_gbps(bytes_per_step_per_rank: int, steps: int, world: int, max_ms:
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
+    """SM clock and clock-event reasons of this rank's GPU, sampled in a thread.
+
+    Uses NVML through ctypes (read-only queries of the driver's library), polled
+    every ~2 ms so that even a few-millisecond timed region holds samples; falls
+    back to `nvidia-smi -lms 50` when NVML cannot be loaded."""
+
+    # NVML clock-event reason bits
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, local_rank: int):
+    def __init__(self, local_rank: int, uuid: str | None = None):
         vis = os.environ.get("CUDA_VISIBLE_DEVICES")
         ids = [v.strip() for v in vis.split(",")] if vis else []
         self.gpu = ids[local_rank] if local_rank < len(ids) else str(local_rank)
+        self.uuid = uuid
         self.samples = []          # (wall time, sm, max, power, {reason: active})
         self.proc = None
         self.thread = None
+        self.stop_flag = threading.Event()
+        self.source = None
+
+    # -- NVML ---------------------------------------------------------------
+    def _nvml_handle(self):
+        import ctypes
+
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None, None
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok and self.gpu.startswith("GPU-"):
+            ok = lib.nvmlDeviceGetHandleByUUID(self.gpu.encode(), ctypes.byref(h)) == 0
+        if not ok and self.gpu.isdigit():
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(int(self.gpu), ctypes.byref(h)) == 0
+        return (lib, h) if ok else (None, None)
+
+    def _poll_nvml(self, lib, h):
+        import ctypes
+
+        sm, mx, pw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+        while not self.stop_flag.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0:
+                r = reasons.value if get_reasons(h, ctypes.byref(reasons)) == 0 else 0
+                p = pw.value / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 \
+                    else None
+                active = {k: bool(r & b) for k, b in self.REASON_BITS.items()}
+                self.samples.append((time.time(), float(sm.value), float(mx.value), p, active))
+            time.sleep(0.002)
 
     def start(self):
+        try:
+            lib, h = self._nvml_handle()
+        except OSError:
+            lib, h = None, None
+        if lib is not None:
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll_nvml, args=(lib, h), daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
@@ -118,6 +173,7 @@ class ClockSampler:
         except OSError:
             self.proc = None
             return
+        self.source = "nvidia-smi"
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
 
@@ -135,29 +191,31 @@ class ClockSampler:
             self.samples.append((time.time(), sm, mx, pw, active))
 
     def stop(self):
+        self.stop_flag.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-            if self.thread is not None:
-                self.thread.join(timeout=5)
+        if self.thread is not None:
+            self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float) -> dict:
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples_in_window": 0,
-                    "note": "nvidia-smi unavailable"}
-        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+                    "note": "no clock samples (NVML and nvidia-smi unavailable)"}
+        samples = list(self.samples)
+        inside = [s for s in samples if t0 <= s[0] <= t1]
         n_in = len(inside)
         if not inside:   # window shorter than the sampling period: nearest samples
             mid = 0.5 * (t0 + t1)
-            inside = sorted(self.samples, key=lambda s: abs(s[0] - mid))[:2]
+            inside = sorted(samples, key=lambda s: abs(s[0] - mid))[:2]
         sms = sorted(s[1] for s in inside)
         reasons = sorted({r for s in inside for r, a in s[4].items() if a})
         powers = [s[3] for s in inside if s[3] is not None]
         return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(s[2] for s in inside),
-                "reasons": reasons, "samples_in_window": n_in,
+                "reasons": reasons, "samples_in_window": n_in, "source": self.source,
                 "power_w_max": max(powers) if powers else None}
 
 
@@ -332,6 +390,13 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
 
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(local, uuid)
+    clocks.start()
     src_np = workloads.make_input(w)
     nbytes_dst = w.dst_elems * w.elem_bytes
     s_gpu = torch.from_numpy(src_np).to(dev)
@@ -342,8 +407,6 @@ def run_ours(args, w):
     def step():
         tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call, sptr, path=args.path)
 
-    clocks = ClockSampler(local)
-    clocks.start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -364,7 +427,6 @@ def run_ours(args, w):
     launches = tl.tl_launch_count() - launches0
     ms_local = e0.elapsed_time(e1)
     ms_max = reduce_max(ms_local, dev if world > 1 else None)
-    clock_summary = clocks.summary(t_wall0, t_wall1)
 
     # ------------------------------------------------ end to end, host buffers
     # Each step copies its input from pinned host memory, permutes and copies the
@@ -405,6 +467,7 @@ def run_ours(args, w):
     e2e_ms = reduce_max(e0.elapsed_time(e1), dev if world > 1 else None)
     dst_pin = dst_pins[(e2e_steps - 1) % 2]
     clocks.stop()
+    clock_summary = clocks.summary(t_wall0, t_wall1)
 
     if rank != 0:
         dist.destroy_process_group() if dist.is_initialized() else None

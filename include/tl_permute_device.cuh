@@ -163,7 +163,10 @@ __device__ __forceinline__ uint32_t chunk_loop_bytes(const ChunkLoop& c) {
  * was written by ordinary stores).  Returns false, issuing nothing, when a chunk
  * is under 16 bytes or not a multiple of 16 (the bulk-copy rule the page states),
  * or when an address or outer stride is not 16-byte aligned.
- * The copy is point to point, never a multicast; nothing here waits. */
+ * The copy is point to point, never a multicast; nothing here waits.  Its only
+ * completion is the peer's barrier: the issuing CTA must not overwrite `src`
+ * until the peer has seen the bytes land (have the peer signal back, e.g. with a
+ * remote mbarrier arrive) -- cp.async.bulk.wait_group does not track this form. */
 __device__ __forceinline__ bool dsmem_copy_region(void* dst, const void* src, const ChunkLoop& c,
                                                   uint32_t peer, uint64_t* peer_bar) {
     if (c.chunk_bytes < 16 || (c.chunk_bytes & 15u) != 0) return false;

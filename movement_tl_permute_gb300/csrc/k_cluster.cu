@@ -12,7 +12,10 @@
 //     chunk) into the matching receive slot of the peer CTA;
 //   * eight consumer warps transpose the tiles the PEER pushed into this CTA's
 //     receive ring, store them to dst, and release each receive slot by arriving
-//     on the peer's barrier through DSMEM.
+//     on the peer's barrier through DSMEM.  As soon as a tile has landed they also
+//     hand the peer's staging slot back: a DSMEM push completes only on the
+//     receiving CTA's barrier (bulk async-groups do not track it), so the peer
+//     learns that its source was read from this arrive.
 // So every SM both reads and writes HBM, and every tile crosses the SM-to-SM
 // network once.  The hand-off is a point-to-point bulk copy, not a multicast.
 // Every wait is bounded; an expired wait records TL_ERR_TIMEOUT in the status
@@ -28,16 +31,14 @@ using namespace tile;
 
 constexpr int kLoaderWarp = kConsumerWarps;        // warp 8
 constexpr int kPusherWarp = kConsumerWarps + 1;    // warp 9
-// DSMEM pushes a pusher keeps going: deeper queues measured slower on GB300
-// (the SM-to-SM network saturates), so one push overlaps the next.
-constexpr int kPushesInFlight = 2;
 
 template <int EB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kClusterThreads)
 k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t loaded[kMaxClusterStages];  // TMA landed in staging slot
-    __shared__ __align__(8) uint64_t staged[kMaxClusterStages];  // staging slot free again
+    __shared__ __align__(8) uint64_t staged[kMaxClusterStages];  // staging slot free: the PEER
+                                                                 // received its push
     __shared__ __align__(8) uint64_t freed[kMaxClusterStages];   // the PEER's receive slot free
     __shared__ __align__(8) uint64_t recv[kMaxClusterStages];    // own receive slot, peer-filled
     const int kStages = a.stages;                                // ring depth (runtime)
@@ -74,7 +75,7 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
         for (int64_t t = cluster + rank * nclusters; t < a.tiles; t += step2, ++issued) {
             const int s = issued % kStages;
             const uint32_t use = issued / kStages;
-            if (use > 0 && !mbar_wait(&staged[s], (use - 1) & 1, a.timeout_ns)) {
+            if (use > 0 && !mbar_wait_cluster(&staged[s], (use - 1) & 1, a.timeout_ns)) {
                 ok = false;
                 break;
             }
@@ -106,16 +107,9 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                 tl_dev::dsmem_copy_region(receive + s * kTileBytes, staging + s * kTileBytes,
                                           one, peer, &recv[s]);
             }
-            bulk_commit();
-            // up to kPushesInFlight pushes may still read their staging slots; the
-            // one issued kPushesInFlight - 1 pushes ago has finished
-            bulk_wait_read<kPushesInFlight - 1>();
-            if (n + 1 >= kPushesInFlight)
-                mbar_arrive(&staged[(n + 1 - kPushesInFlight) % kStages]);
+            // A DSMEM push completes only on the peer's barrier, so the staging slot
+            // is released by the peer once the bytes have landed there.
         }
-        bulk_wait_read<0>();
-        for (uint32_t i = n + 1 > kPushesInFlight ? n + 1 - kPushesInFlight : 0; i < n; ++i)
-            mbar_arrive(&staged[i % kStages]);
         if (!ok) report(a.status, TL_ERR_TIMEOUT);
     } else if (warp < kConsumerWarps) {
         // --------------------------------- consumers --------------------------------
@@ -127,6 +121,9 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                 if (lane == 0) report(a.status, TL_ERR_TIMEOUT);
                 break;
             }
+            // the bytes have landed, so the peer's push has finished reading its
+            // staging slot: hand that slot back to the peer's loader
+            if (threadIdx.x == 0) mbar_arrive_remote(map_to_rank(smem_addr(&staged[s]), peer));
             const TileOut o = make_out<EB>(tile_coord(t, a), a);
             consume<EB>(smem_addr(receive + s * kTileBytes), o, warp, lane);
             __syncwarp();

@@ -256,3 +256,75 @@ extern "C" int tdp_wait(uint32_t* flag, uint32_t* data, uint32_t* out, int32_t* 
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&k_wait), dim3(2), dim3(128),
                                        args, 0, 0);
 }
+
+// ---------------------------------------------------------------------------
+// DSMEM ceiling: the cluster hand-off pattern with no HBM traffic
+// ---------------------------------------------------------------------------
+namespace {
+
+// Each CTA of a pair pushes `iters` 16 KiB tiles into the peer's 2-slot receive
+// ring (one bulk copy each, completing on the peer's barrier); the peer releases
+// each slot back with a remote arrive.  status[blockIdx.x] = 1 done, 0 a bounded
+// wait expired.
+__global__ void __cluster_dims__(2, 1, 1) k_dsmem_stream(int iters, uint64_t timeout_ns,
+                                                          int32_t* status) {
+    constexpr int S = 2;
+    constexpr uint32_t kTile = 16384;
+    extern __shared__ __align__(1024) uint8_t sm[];
+    __shared__ __align__(8) uint64_t recv[S], freed[S];
+    uint8_t* staging = sm;
+    uint8_t* receive = sm + S * kTile;
+    const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tl_dev::smem_u32(&recv[s])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(tl_dev::smem_u32(&freed[s])));
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    cluster_sync();
+    bool ok = true;
+    if (threadIdx.x == 0) {                          // pusher
+        tl_dev::ChunkLoop one{};
+        one.chunk_bytes = kTile;
+        for (int i = 0; i < iters && ok; ++i) {
+            const int s = i % S;
+            if (i >= S) ok = wait_bar(&freed[s], ((i / S) - 1) & 1, timeout_ns);
+            if (ok) tl_dev::dsmem_copy_region(receive + s * kTile, staging + s * kTile, one, peer,
+                                              &recv[s]);
+        }
+    } else if (threadIdx.x == 32) {                  // receiver
+        for (int i = 0; i < iters && ok; ++i) {
+            const int s = i % S;
+            asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                             tl_dev::smem_u32(&recv[s])),
+                         "r"(kTile)
+                         : "memory");
+            ok = wait_bar(&recv[s], (i / S) & 1, timeout_ns);
+            if (ok) {
+                uint32_t remote;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                             : "=r"(remote)
+                             : "r"(tl_dev::smem_u32(&freed[s])), "r"(peer));
+                asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                                 remote)
+                             : "memory");
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 || threadIdx.x == 32) atomicAnd(&status[blockIdx.x], ok ? 1 : 0);
+    cluster_sync();
+}
+
+}  // namespace
+
+extern "C" int tdp_dsmem_stream(int grid, int iters, uint64_t timeout_ns, int32_t* status) {
+    const int smem = 4 * 16384;
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&k_dsmem_stream),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k_dsmem_stream<<<grid, 64, smem>>>(iters, timeout_ns, status);
+    return cudaGetLastError();
+}

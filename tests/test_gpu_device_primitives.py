@@ -66,6 +66,7 @@ def lib():
     h.tdp_fragment.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(TileArgs)]
     h.tdp_dsmem.argtypes = [vp, vp, vp, ctypes.POINTER(RegionArgs)]
     h.tdp_wait.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_uint64]
+    h.tdp_dsmem_stream.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint64, vp]
     return h
 
 
@@ -223,3 +224,24 @@ def test_wait_until_global(lib, publish):
     else:
         assert int(status[0].item()) == 0          # the bounded wait gave up
         assert not bool(out.any())
+
+
+def test_dsmem_stream_ceiling(lib):
+    """The cluster hand-off pattern with no HBM traffic: 16 KiB pushes into 2-slot
+    rings of the peer, released by remote arrives, 3 CTAs per SM.  Prints the
+    SM-to-SM throughput this pattern reaches (the cluster path's own ceiling)."""
+    grid = 2 * ((torch.cuda.get_device_properties(0).multi_processor_count * 3) // 2)
+    iters = 2000
+    status = torch.ones(grid, dtype=torch.int32, device="cuda")
+    for _ in range(2):                                       # warm-up, then timed
+        status.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        assert lib.tdp_dsmem_stream(grid, iters, 2_000_000_000, status.data_ptr()) == 0
+        e1.record()
+        torch.cuda.synchronize()
+    assert bool((status == 1).all())
+    gbs = grid * iters * 16384 / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    print("\nDSMEM hand-off ceiling: %.0f GB/s pushed (grid %d, %d pushes of 16 KiB per CTA)"
+          % (gbs, grid, iters))
+    assert gbs > 100

@@ -125,7 +125,7 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
             // staging slot: hand that slot back to the peer's loader
             if (threadIdx.x == 0) mbar_arrive_remote(map_to_rank(smem_addr(&staged[s]), peer));
             const TileOut o = make_out<EB>(tile_coord(t, a), a);
-            consume<EB>(smem_addr(receive + s * kTileBytes), o, warp, lane);
+            consume<EB>(smem_addr(receive + s * kTileBytes), o, warp, lane, 0);
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(map_to_rank(smem_addr(&freed[s]), peer));
         }

@@ -1,12 +1,14 @@
 // k_tile.cu -- batched 2-D transpose through TMA-staged, 128B-swizzled shared memory.
 //
 // Plane: axis a is contiguous in src (stride 1), axis b is contiguous in dst
-// (stride 1); every other axis is a batch axis.  A tile is 128 rows of b by 128
+// (stride 1); every other axis is a batch axis.  A tile is TB rows of b by 128
 // BYTES of a (128/EB elements).  One producer warp streams tiles HBM -> shared
 // memory with `cp.async.bulk.tensor` (TMA, SWIZZLE_128B) into a ring of stages
 // guarded by mbarriers; eight consumer warps read each tile column-wise, assemble
 // 16-byte runs along b in registers and store them with 16-byte coalesced stores
 // (each warp store fills whole 128-byte lines of dst).  CTAs are persistent.
+// TB is 128 or 256 (a template parameter; the ring holds at most
+// 192 KiB of tiles either way).
 //
 // Shared-memory column reads are made bank-conflict-free the way the TVM
 // "permute_layout" page makes its warp permute conflict-free ("Algorithm", step
@@ -25,9 +27,12 @@ namespace {
 using namespace dev;
 using namespace tile;
 
-template <int EB>
+// TB = tile height in rows of b (128 or 256); the consumers take a tile in 128-row
+// blocks.  Taller tiles halve the TMA requests and barrier round trips per byte.
+template <int EB, int TB>
 __global__ void __launch_bounds__(kTileThreads)
 k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
+    constexpr uint32_t kBytes = (uint32_t)TB * kRowBytes;   // one stage
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full[kMaxTileStages];
     __shared__ __align__(8) uint64_t empty[kMaxTileStages];
@@ -62,10 +67,10 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                     break;
                 }
                 const TileCoord tc = tile_coord(t, a);
-                info[s] = make_out<EB>(tc, a);          // published by the release below
-                mbar_arrive_expect_tx(&full[s], kTileBytes);
-                tma_load(smem + s * kTileBytes, &tmap, &full[s], a.rank,
-                         (int)(tc.ta * kRowBytes), (int)(tc.tb * kRows), (int)tc.bc[0],
+                info[s] = make_out<EB, TB>(tc, a);      // published by the release below
+                mbar_arrive_expect_tx(&full[s], kBytes);
+                tma_load(smem + s * kBytes, &tmap, &full[s], a.rank,
+                         (int)(tc.ta * kRowBytes), (int)(tc.tb * TB), (int)tc.bc[0],
                          (int)tc.bc[1], (int)tc.bc[2]);
             }
             if (!ok) report(a.status, TL_ERR_TIMEOUT);
@@ -86,7 +91,10 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
             break;
         }
         const TileOut o = info[s];
-        consume<EB>(smem_addr(smem + s * kTileBytes), o, warp, lane);
+        const uint32_t base = smem_addr(smem + s * kBytes);
+#pragma unroll
+        for (int rb0 = 0; rb0 < TB; rb0 += kRows)
+            if (rb0 == 0 || rb0 < o.rows) consume<EB>(base, o, warp, lane, rb0);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -94,29 +102,34 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
 
 }  // namespace
 
-int tile_smem_bytes(int stages) { return stages * kTileBytes + 1024; }
+int tile_smem_bytes(int stages, int rows) { return stages * rows * kRowBytes + 1024; }
 
-template <int EB>
+template <int EB, int TB>
 const void* tile_kernel() {
-    return reinterpret_cast<const void*>(&k_tile<EB>);
+    return reinterpret_cast<const void*>(&k_tile<EB, TB>);
 }
 
-template <int EB>
+template <int EB, int TB>
 cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st,
                         bool pdl) {
-    return launch_kernel(k_tile<EB>, dim3(grid), dim3(kTileThreads), tile_smem_bytes(a.stages), st,
-                         pdl, map, a);
+    return launch_kernel(k_tile<EB, TB>, dim3(grid), dim3(kTileThreads),
+                         tile_smem_bytes(a.stages, TB), st, pdl, map, a);
 }
 
-#define TL_INST(EB)                                                                         \
-    template const void* tile_kernel<EB>();                                                 \
-    template cudaError_t launch_tile<EB>(const CUtensorMap&, const TileArgs&, int, cudaStream_t, \
-                                         bool);
-TL_INST(1)
-TL_INST(2)
-TL_INST(4)
-TL_INST(8)
-TL_INST(16)
+#define TL_INST(EB, TB)                                                                     \
+    template const void* tile_kernel<EB, TB>();                                             \
+    template cudaError_t launch_tile<EB, TB>(const CUtensorMap&, const TileArgs&, int,      \
+                                             cudaStream_t, bool);
+TL_INST(1, 128)
+TL_INST(2, 128)
+TL_INST(4, 128)
+TL_INST(8, 128)
+TL_INST(16, 128)
+TL_INST(1, 256)
+TL_INST(2, 256)
+TL_INST(4, 256)
+TL_INST(8, 256)
+TL_INST(16, 256)
 #undef TL_INST
 
 }  // namespace tl

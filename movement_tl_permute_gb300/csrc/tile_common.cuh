@@ -88,12 +88,15 @@ __device__ __forceinline__ void put(const TileOut& o, int col, int row, const ui
     }
 }
 
-// Consumer work for one tile: every warp handles its share of the tile.
+// Consumer work for the 128-row block starting at tile row rb0 (a multiple of
+// 128): every warp handles its share of the block.
 template <int EB>
-__device__ __forceinline__ void consume(uint32_t tile, const TileOut& o, int warp, int lane);
+__device__ __forceinline__ void consume(uint32_t tile, const TileOut& o, int warp, int lane,
+                                        int rb0);
 
 template <>
-__device__ __forceinline__ void consume<4>(uint32_t tile, const TileOut& o, int warp, int lane) {
+__device__ __forceinline__ void consume<4>(uint32_t tile, const TileOut& o, int warp, int lane,
+                                           int rb0) {
     // warp unit: 32 rows x 4 columns (one 16-byte chunk); 32 units per tile
     const int cw = lane & 3, g = lane >> 2, x = (lane >> 3) & 3;
 #pragma unroll
@@ -101,7 +104,7 @@ __device__ __forceinline__ void consume<4>(uint32_t tile, const TileOut& o, int 
         const int u = warp + kConsumerWarps * i;
         const int cb = u & 7, rb = u >> 3;
         const int col = 4 * cb + cw;
-        const int row0 = rb * 32 + 4 * g;
+        const int row0 = rb0 + rb * 32 + 4 * g;
         uint32_t r[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) r[k] = lds32(tile + swz(row0 + (k ^ x), 4 * col));
@@ -114,7 +117,8 @@ __device__ __forceinline__ void consume<4>(uint32_t tile, const TileOut& o, int 
 }
 
 template <>
-__device__ __forceinline__ void consume<8>(uint32_t tile, const TileOut& o, int warp, int lane) {
+__device__ __forceinline__ void consume<8>(uint32_t tile, const TileOut& o, int warp, int lane,
+                                           int rb0) {
     // warp unit: 32 rows x 2 columns; half-warp wavefronts of 16 lanes
     const int cw = lane & 1, g = lane >> 1, x = (lane >> 3) & 1;
 #pragma unroll
@@ -122,7 +126,7 @@ __device__ __forceinline__ void consume<8>(uint32_t tile, const TileOut& o, int 
         const int u = warp + kConsumerWarps * i;
         const int cb = u & 7, rb = u >> 3;
         const int col = 2 * cb + cw;
-        const int row0 = rb * 32 + 2 * g;
+        const int row0 = rb0 + rb * 32 + 2 * g;
         uint2 r0 = lds64(tile + swz(row0 + x, 8 * col));
         uint2 r1 = lds64(tile + swz(row0 + (1 ^ x), 8 * col));
         cswap(x != 0, r0, r1);
@@ -131,20 +135,22 @@ __device__ __forceinline__ void consume<8>(uint32_t tile, const TileOut& o, int 
 }
 
 template <>
-__device__ __forceinline__ void consume<16>(uint32_t tile, const TileOut& o, int warp, int lane) {
+__device__ __forceinline__ void consume<16>(uint32_t tile, const TileOut& o, int warp, int lane,
+                                           int rb0) {
     // warp unit: 32 rows x 1 column; quarter-warp wavefronts read 8 distinct chunks
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int u = warp + kConsumerWarps * i;
         const int cb = u & 7, rb = u >> 3;
-        const int row = rb * 32 + lane;
+        const int row = rb0 + rb * 32 + lane;
         uint4 v = lds128(tile + swz(row, 16 * cb));
         put<16>(o, cb, row, v);
     }
 }
 
 template <>
-__device__ __forceinline__ void consume<2>(uint32_t tile, const TileOut& o, int warp, int lane) {
+__device__ __forceinline__ void consume<2>(uint32_t tile, const TileOut& o, int warp, int lane,
+                                           int rb0) {
     // warp unit: 64 rows x 4 words (8 columns); 16 units per tile
     const int cw = lane & 3, g = lane >> 2, x = g;
 #pragma unroll
@@ -152,7 +158,7 @@ __device__ __forceinline__ void consume<2>(uint32_t tile, const TileOut& o, int 
         const int u = warp + kConsumerWarps * i;
         const int cb = u & 7, rb = u >> 3;
         const int word = 4 * cb + cw;
-        const int row0 = rb * 64 + 8 * g;
+        const int row0 = rb0 + rb * 64 + 8 * g;
         uint32_t r[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) r[k] = lds32(tile + swz(row0 + (k ^ x), 4 * word));
@@ -174,12 +180,13 @@ __device__ __forceinline__ void consume<2>(uint32_t tile, const TileOut& o, int 
 }
 
 template <>
-__device__ __forceinline__ void consume<1>(uint32_t tile, const TileOut& o, int warp, int lane) {
+__device__ __forceinline__ void consume<1>(uint32_t tile, const TileOut& o, int warp, int lane,
+                                           int rb0) {
     // warp unit: 128 rows x 4 words (16 columns); 8 units per tile, one per warp
     const int cw = lane & 3, g = lane >> 2, x = g;
     const int cb = warp;
     const int word = 4 * cb + cw;
-    const int row0 = 16 * g;
+    const int row0 = rb0 + 16 * g;
     uint32_t r[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) r[k] = lds32(tile + swz(row0 + (k ^ x), 4 * word));
@@ -211,7 +218,8 @@ __device__ __forceinline__ void consume<1>(uint32_t tile, const TileOut& o, int 
 
 // Tile t -> (ta, tb, batch coordinates).  Within a batch item tiles are visited in
 // groups of `group_b` tile rows, b fastest inside a group, so concurrently
-// running CTAs read and write runs of several 128-byte lines.
+// running CTAs write runs of many 128-byte lines (one group spanning all of b
+// makes the writes one front-to-back stream).
 struct TileCoord {
     int64_t ta, tb;
     int64_t bc[3];
@@ -260,11 +268,11 @@ __device__ __forceinline__ TileCoord tile_coord(int64_t t, const TileArgs& a) {
     return r;
 }
 
-// Destination record of the tile at coordinates tc.
-template <int EB>
+// Destination record of the tile at coordinates tc (tiles of TB rows).
+template <int EB, int TB = kRows>
 __device__ __forceinline__ TileOut make_out(const TileCoord& tc, const TileArgs& a) {
     constexpr int TA = kRowBytes / EB;
-    const int64_t a0 = tc.ta * TA, b0 = tc.tb * kRows;
+    const int64_t a0 = tc.ta * TA, b0 = tc.tb * TB;
     int64_t base = a0 * a.ds_a + b0;
 #pragma unroll
     for (int i = 0; i < 3; ++i) base += tc.bc[i] * a.bds[i];
@@ -272,9 +280,9 @@ __device__ __forceinline__ TileOut make_out(const TileCoord& tc, const TileArgs&
     o.base = a.dst + base * EB;
     o.cstride = a.ds_a * EB;
     o.cols = (int32_t)min((int64_t)TA, a.ext_a - a0);
-    o.rows = (int32_t)min((int64_t)kRows, a.ext_b - b0);
+    o.rows = (int32_t)min((int64_t)TB, a.ext_b - b0);
     o.vec = a.vec_store;
-    o.full = (o.vec && o.cols == TA && o.rows == kRows) ? 1 : 0;
+    o.full = (o.vec && o.cols == TA && o.rows == TB) ? 1 : 0;
     return o;
 }
 

@@ -87,10 +87,12 @@ struct TileArgs {
     dev::DivU32 d_gfull, d_glast;        // full / last group height
     dev::DivU32 d_bext[3];
 };
-int tile_smem_bytes(int stages);
-template <int EB>
+// dynamic shared memory of the tile kernel: `stages` tiles of `rows` x 128 bytes
+int tile_smem_bytes(int stages, int rows);
+constexpr int kTileRingBytes = kMaxTileStages * 128 * 128;   // ring bound for any tile height
+template <int EB, int TB>
 const void* tile_kernel();
-template <int EB>
+template <int EB, int TB>
 cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st,
                         bool pdl);
 

@@ -23,16 +23,21 @@ constexpr uint64_t kTestTimeoutNs = 50000000ull;        // 50 ms under the test 
 struct DevInfo {
     bool ready = false;
     int sms = 0;
-    int tile_occ[5][kMaxTileStages + 1] = {};  // CTAs per SM of k_tile<EB> by ring depth
+    int tile_occ[5][2][kMaxTileStages + 1] = {};  // CTAs per SM of k_tile<EB, 128|256> by depth
     int cluster_occ[5][kMaxClusterStages + 1] = {};   // by ring depth
 };
 
 // Tile-path tuning after defaults are applied.  The defaults were measured on
 // GB300 over the batched 128x64 tile transpose and the 2-D transposes of every
 // element width: one CTA per SM with a 4-deep ring (about 600 tiles, 10 MB, in
-// flight GPU-wide) beat deeper rings and denser grids on every workload.
+// flight GPU-wide) beat deeper rings and denser grids on every workload, and
+// visiting every tile row of a column block before the next block (the whole b
+// extent as one group) beat groups of 16 to 128 rows: the CTAs then write dst
+// front to back as one sequential stream while their reads stay 128-byte rows.
+// 256-row tiles were slower than 128-row tiles on every workload.
 struct TileTuning {
-    int group = 32;         // tile rows visited together
+    int group = 0;          // tile rows visited together (0 = the whole b extent)
+    int rows = 128;         // tile height (128 or 256)
     int stages = 4;         // ring depth
     int ctas_per_sm = 0;    // resident CTAs the grid is sized for (0 = path default)
     int promotion = 256;    // L2 fill size of the TMA loads (0 = none)
@@ -49,6 +54,9 @@ TileTuning tile_tuning(const tl_permute_opts* o) {
     if (o->tile_stages >= 2 && o->tile_stages <= kMaxClusterStages)
         t.cluster_stages = o->tile_stages;
     if (o->tile_ctas_per_sm > 0) t.ctas_per_sm = o->tile_ctas_per_sm;
+    if (o->tile_rows == 256) t.rows = 256;
+    const int max_stages = kTileRingBytes / (t.rows * 128);
+    if (t.stages > max_stages) t.stages = max_stages;
     if (o->tile_l2_promotion == 64 || o->tile_l2_promotion == 128 ||
         o->tile_l2_promotion == 256)
         t.promotion = o->tile_l2_promotion;
@@ -74,17 +82,23 @@ int get_device_info(DevInfo* out) {
     if (!d.ready) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return TL_ERR_CUDA;
-        const void* kt[5] = {tile_kernel<1>(), tile_kernel<2>(), tile_kernel<4>(),
-                             tile_kernel<8>(), tile_kernel<16>()};
+        const void* kt[5][2] = {{tile_kernel<1, 128>(), tile_kernel<1, 256>()},
+                                {tile_kernel<2, 128>(), tile_kernel<2, 256>()},
+                                {tile_kernel<4, 128>(), tile_kernel<4, 256>()},
+                                {tile_kernel<8, 128>(), tile_kernel<8, 256>()},
+                                {tile_kernel<16, 128>(), tile_kernel<16, 256>()}};
         for (int i = 0; i < 5; ++i) {
-            if (cudaFuncSetAttribute(kt[i], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     tile_smem_bytes(kMaxTileStages)) != cudaSuccess)
-                return TL_ERR_CUDA;
-            for (int st = 2; st <= kMaxTileStages; ++st)
-                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                        &d.tile_occ[i][st], kt[i], kTileThreads, tile_smem_bytes(st)) !=
-                    cudaSuccess)
+            for (int h = 0; h < 2; ++h) {
+                const int rows = 128 << h, max_st = kTileRingBytes / (rows * 128);
+                if (cudaFuncSetAttribute(kt[i][h], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         tile_smem_bytes(max_st, rows)) != cudaSuccess)
                     return TL_ERR_CUDA;
+                for (int st = 2; st <= max_st; ++st)
+                    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                            &d.tile_occ[i][h][st], kt[i][h], kTileThreads,
+                            tile_smem_bytes(st, rows)) != cudaSuccess)
+                        return TL_ERR_CUDA;
+            }
             // The cluster variant is optional: if its set-up fails it is sized
             // conservatively (one CTA per SM) and the error is cleared.
             const void* kc = cluster_kernel(1 << i);
@@ -129,7 +143,7 @@ void batch_inner_first(const Plan& p, int64_t* ext, int64_t* ss, int64_t* ds) {
 }
 
 // Tensor map over the source plane: dim 0 = a in BYTES (raw bits, type UINT8),
-// dim 1 = b, dims 2.. = batch.  Box = 128 bytes x 128 rows, 128-byte swizzle.
+// dim 1 = b, dims 2.. = batch.  Box = 128 bytes x p.tile_rows rows, 128-byte swizzle.
 int encode_tile_map(const Plan& p, const void* src, int promotion, CUtensorMap* map,
                     int* rank) {
     if (!g_encode) return TL_ERR_CUDA;
@@ -143,7 +157,7 @@ int encode_tile_map(const Plan& p, const void* src, int promotion, CUtensorMap* 
     dims[1] = (cuuint64_t)p.ext_b;
     strides[0] = (cuuint64_t)(p.ss_b * eb);
     box[0] = 128;
-    box[1] = 128;
+    box[1] = (cuuint32_t)p.tile_rows;
     for (int i = 0; i < p.batch.n; ++i) {
         dims[2 + i] = (cuuint64_t)bext[i];
         strides[1 + i] = (cuuint64_t)(bss[i] * eb);
@@ -200,9 +214,9 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
     }
     case TL_PATH_TILE:
         l.block = kTileThreads;
-        l.smem = tile_smem_bytes(tt.stages);
+        l.smem = tile_smem_bytes(tt.stages, p.tile_rows);
         if (sms) {
-            int per_sm = d->tile_occ[log2i(p.eb)][tt.stages];
+            int per_sm = d->tile_occ[log2i(p.eb)][p.tile_rows == 256 ? 1 : 0][tt.stages];
             const int want = tt.ctas_per_sm > 0 ? tt.ctas_per_sm : 1;
             if (want < per_sm) per_sm = want;
             l.grid = cap_grid(p.tiles, sms * (per_sm < 1 ? 1 : per_sm), max_ctas);
@@ -232,6 +246,15 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
     return l;
 }
 
+// The tile path's tile height is a launch choice: re-count the tiles for it.
+void apply_tile_rows(Plan& p, const TileTuning& tt) {
+    if (p.path != TL_PATH_TILE || tt.rows == p.tile_rows) return;
+    p.tile_rows = tt.rows;
+    const int64_t ta = (p.ext_a + p.tile_cols - 1) / p.tile_cols;
+    const int64_t tb = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
+    p.tiles = ta * tb * p.batch_total;
+}
+
 void fill_divs(int n, const int64_t* ext, dev::DivU32* div) {
     for (int i = 0; i < n; ++i) div[i] = dev::make_divu32((uint32_t)ext[i]);
 }
@@ -249,6 +272,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
     if (rc != TL_OK) return rc;
     const int32_t max_ctas = opts ? opts->max_ctas : 0;
     const TileTuning tt = tile_tuning(opts);
+    apply_tile_rows(p, tt);
     const Launch l = launch_shape(p, &d, max_ctas, tt);
     // overlap this launch with the drain of the previous kernel in the stream
     const bool pdl = (flags & TL_FLAG_NO_PDL) == 0;
@@ -315,7 +339,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.tiles_a = (p.ext_a + p.tile_cols - 1) / p.tile_cols;
         a.tiles_b = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
         a.tiles = p.tiles;
-        a.group_b = tt.group;
+        a.group_b = tt.group > 0 && tt.group < a.tiles_b ? tt.group : a.tiles_b;
         a.stages = tt.stages;
         a.nbatch = p.batch.n;
         a.vec_store = p.vec_store ? 1 : 0;
@@ -338,12 +362,22 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             err = launch_cluster(eb, map, a, l.grid, st, pdl);
             break;
         }
-        switch (eb) {
-        case 1: err = launch_tile<1>(map, a, l.grid, st, pdl); break;
-        case 2: err = launch_tile<2>(map, a, l.grid, st, pdl); break;
-        case 4: err = launch_tile<4>(map, a, l.grid, st, pdl); break;
-        case 8: err = launch_tile<8>(map, a, l.grid, st, pdl); break;
-        default: err = launch_tile<16>(map, a, l.grid, st, pdl); break;
+        if (p.tile_rows == 256) {
+            switch (eb) {
+            case 1: err = launch_tile<1, 256>(map, a, l.grid, st, pdl); break;
+            case 2: err = launch_tile<2, 256>(map, a, l.grid, st, pdl); break;
+            case 4: err = launch_tile<4, 256>(map, a, l.grid, st, pdl); break;
+            case 8: err = launch_tile<8, 256>(map, a, l.grid, st, pdl); break;
+            default: err = launch_tile<16, 256>(map, a, l.grid, st, pdl); break;
+            }
+        } else {
+            switch (eb) {
+            case 1: err = launch_tile<1, 128>(map, a, l.grid, st, pdl); break;
+            case 2: err = launch_tile<2, 128>(map, a, l.grid, st, pdl); break;
+            case 4: err = launch_tile<4, 128>(map, a, l.grid, st, pdl); break;
+            case 8: err = launch_tile<8, 128>(map, a, l.grid, st, pdl); break;
+            default: err = launch_tile<16, 128>(map, a, l.grid, st, pdl); break;
+            }
         }
         break;
     }
@@ -436,6 +470,8 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         info.shift = p.shift;
         info.mask = p.mask;
     }
+    const TileTuning tt = tile_tuning(opts);
+    apply_tile_rows(p, tt);
     info.tile_rows = p.tile_rows;
     info.tile_cols = p.tile_cols;
     info.tiles = p.tiles;
@@ -445,7 +481,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
                       get_device_info(&d) == TL_OK;
     if (!have) cudaGetLastError();   // clear a "no device" error on CPU-only hosts
     const Launch l =
-        launch_shape(p, have ? &d : nullptr, opts ? opts->max_ctas : 0, tile_tuning(opts));
+        launch_shape(p, have ? &d : nullptr, opts ? opts->max_ctas : 0, tt);
     info.grid = l.grid;
     info.block = l.block;
     info.smem_bytes = l.smem;

@@ -51,7 +51,7 @@ def _random_case(rng):
     return shape, ss, tuple(ds), eb, so, do
 
 
-def _run(shape, ss, ds, eb, so, do, path, seed, stream=None):
+def _run(shape, ss, ds, eb, so, do, path, seed, stream=None, **opts):
     span = lambda st: sum((e - 1) * x for e, x in zip(shape, st)) + 1
     n_src = (so + span(ss)) * eb
     n_dst = 256 + (do + span(ds)) * eb + 256
@@ -63,7 +63,7 @@ def _run(shape, ss, ds, eb, so, do, path, seed, stream=None):
     st = stream if stream is not None else torch.cuda.current_stream()
     with torch.cuda.stream(st):
         tl.tl_permute_ex(s_gpu.data_ptr() + so * eb, d_gpu.data_ptr() + 256 + do * eb, shape,
-                         ss, ds, eb, st.cuda_stream, path=path)
+                         ss, ds, eb, st.cuda_stream, path=path, **opts)
     st.synchronize()
     return d_gpu.cpu().numpy(), want
 
@@ -83,6 +83,9 @@ def test_random_layouts_every_applicable_path():
             got, want = _run(shape, ss, ds, eb, so, do, path, seed=i)
             assert np.array_equal(got, want), (shape, ss, ds, eb, so, do, path)
             ran[path] += 1
+            if path == "tile":                  # the 256-row tile variant as well
+                got, want = _run(shape, ss, ds, eb, so, do, path, seed=i, tile_rows=256)
+                assert np.array_equal(got, want), (shape, ss, ds, eb, so, do, "tile256")
     assert all(ran[p] > 0 for p in ("auto", "generic", "chunk", "tile")), ran
 
 

@@ -139,6 +139,26 @@ def test_tile_and_cluster_paths(eb, path):
 
 
 @pytest.mark.parametrize("eb", WIDTHS)
+@pytest.mark.parametrize("stages", [2, 6])
+def test_tile_path_256_row_tiles(eb, stages):
+    # the taller tile variant: ragged bottom tiles whose second 128-row block is
+    # partly or wholly outside the plane, batched planes, element-wise edges
+    for i, (shape, ss, ds) in enumerate(_tile_shapes(eb)):
+        check(shape, ss, ds, eb, "tile", seed=20 + i, tile_rows=256, tile_stages=stages)
+    c = max(1, 256 // eb)
+    check((33, c), (c, 1), (1, 33), eb, "tile", seed=5, dst_off=1, tile_rows=256)
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
+@pytest.mark.parametrize("group", [1, 3])
+def test_tile_path_visit_groups(eb, group):
+    # tile rows visited in groups smaller than the b extent, the last one ragged
+    for i, (shape, ss, ds) in enumerate(_tile_shapes(eb)):
+        check(shape, ss, ds, eb, "tile", seed=40 + i, tile_group=group)
+        check(shape, ss, ds, eb, "cluster", seed=50 + i, tile_group=group)
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
 def test_tile_path_unaligned_dst_runs(eb):
     # dst columns of 33 rows: 16-byte runs straddle, the kernel stores element-wise
     c = max(1, 256 // eb)

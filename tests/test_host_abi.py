@@ -226,6 +226,20 @@ def test_plans_of_the_workloads():
     assert p["path"] == "cluster"
 
 
+def test_tile_height_option():
+    w = workloads.get("t2d_f32")                      # 16384 x 16384 float32
+    p128 = _plan(w, tile_rows=128)
+    p256 = _plan(w, tile_rows=256)
+    assert p128["tile_rows"] == 128 and p256["tile_rows"] == 256
+    assert p256["tiles"] * 2 == p128["tiles"] == (16384 // 32) * (16384 // 128)
+    assert p256["smem_bytes"] == 4 * 256 * 128 + 1024
+    # ring depth is capped at 192 KiB of tiles, unknown heights fall back to 128
+    assert _plan(w, tile_rows=256, tile_stages=12)["smem_bytes"] == 6 * 256 * 128 + 1024
+    assert _plan(w, tile_rows=200)["tile_rows"] == 128
+    # the cluster variant keeps 128-row tiles
+    assert _plan(w, path="cluster", tile_rows=256)["tile_rows"] == 128
+
+
 def test_forced_paths_that_do_not_apply():
     w = workloads.get("attention")
     for path in ("tile", "rows", "cluster"):

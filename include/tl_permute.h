@@ -183,13 +183,15 @@ typedef struct tl_permute_opts {
     /* Tuning of the tile path; 0 selects the planner's default for each. */
     int32_t tile_group;   /* tile rows visited together (visit order; default all) */
     int32_t tile_stages;  /* shared-memory ring depth: 2..12 (tile, 128-row tiles),
-                             2..6 (tile, 256-row tiles; cluster) */
+                             2..6 (tile, 256-row tiles); cluster: staging ring, 1..8 */
     int32_t tile_ctas_per_sm;  /* resident CTAs per SM the grid is sized for */
     int32_t tile_l2_promotion; /* L2 fill size of the TMA loads: 64, 128, 256, or -1 = none */
     int32_t tile_rows;    /* tile height in rows of the dst-contiguous axis: 128 or 256
                              (tile path only; other values select the default) */
-    int32_t reserved32;
-    int64_t reserved;
+    int32_t cluster_recv_stages; /* cluster: receive ring depth, 1..8 (staging + receive
+                                    slots at most 12) */
+    int32_t cluster_consumer_warps; /* cluster: consumer warps per CTA, 4 or 8 */
+    int32_t reserved;
 } tl_permute_opts;
 
 /* tl_permute with options (path forcing, status word, buffer bounds).

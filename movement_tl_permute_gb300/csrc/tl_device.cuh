@@ -252,10 +252,21 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     }
 }
 
-// Arrive on a barrier of another CTA of the cluster (address from map_to_rank).
+// Arrive on a barrier of another CTA of the cluster (address from map_to_rank),
+// releasing this thread's prior writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
                      cluster_addr)
+                 : "memory");
+}
+
+// The same arrive with a CTA-scope release, for a consumer handing a shared-memory
+// slot back after reading it: the reads are complete (their values already fed
+// the thread's stores), and a cluster-scope release would also wait until the
+// thread's global stores reach L2 (1-2 us per tile measured on GB300 inside the
+// cluster transpose).
+__device__ __forceinline__ void mbar_arrive_remote_slot(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
 }
 

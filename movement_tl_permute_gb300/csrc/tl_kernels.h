@@ -65,10 +65,12 @@ template <int VB>
 cudaError_t launch_chunk(const ChunkArgs& a, int grid, int block, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- tile (TMA)
-constexpr int kMaxClusterStages = 6;   // ring depth limit of the cluster variant (x2 rings)
+constexpr int kMaxClusterStages = 8;   // ring depth limit of each cluster ring
+constexpr int kMaxClusterSlots = 12;   // staging + receive slots of one cluster CTA
 constexpr int kMaxTileStages = 12;     // ring depth limit of the single-CTA tile kernel
 constexpr int kTileThreads = 9 * 32;   // 8 consumer warps + 1 producer warp
-constexpr int kClusterThreads = 10 * 32;  // 8 consumer warps + loader warp + pusher warp
+// block of the cluster variant: ncw consumer warps + loader, pusher and watcher warps
+__host__ __device__ constexpr int cluster_threads(int ncw) { return (ncw + 3) * 32; }
 struct TileArgs {
     uint8_t* dst;
     int32_t* status;
@@ -81,7 +83,8 @@ struct TileArgs {
     uint64_t timeout_ns;
     // 32-bit tile decode (use32 = 1 when tile indices fit in 32 bits)
     int32_t use32;
-    int32_t stages;                      // ring depth
+    int32_t stages;                      // ring depth (cluster: staging ring)
+    int32_t recv_stages;                 // cluster: receive ring depth
     dev::DivU32 d_item;                  // tiles per batch item
     dev::DivU32 d_grp;                   // tiles per group of group_b tile rows
     dev::DivU32 d_gfull, d_glast;        // full / last group height
@@ -97,9 +100,9 @@ cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cud
                         bool pdl);
 
 // tile path with a 2-CTA cluster and a DSMEM hand-off (k_cluster.cu)
-int cluster_smem_bytes(int stages);
-const void* cluster_kernel(int eb);
-cudaError_t launch_cluster(int eb, const CUtensorMap& map, const TileArgs& a, int grid,
+int cluster_smem_bytes(int slots);   // staging + receive slots
+const void* cluster_kernel(int eb, int ncw);   // ncw = consumer warps, 8 or 4
+cudaError_t launch_cluster(int eb, int ncw, const CUtensorMap& map, const TileArgs& a, int grid,
                            cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- rows

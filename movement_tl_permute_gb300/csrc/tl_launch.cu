@@ -24,7 +24,7 @@ struct DevInfo {
     bool ready = false;
     int sms = 0;
     int tile_occ[5][2][kMaxTileStages + 1] = {};  // CTAs per SM of k_tile<EB, 128|256> by depth
-    int cluster_occ[5][kMaxClusterStages + 1] = {};   // by ring depth
+    int cluster_occ[5][2][kMaxClusterSlots + 1] = {}; // by consumer warps (8|4), slots
 };
 
 // Tile-path tuning after defaults are applied.  The defaults were measured on
@@ -41,9 +41,13 @@ struct TileTuning {
     int stages = 4;         // ring depth
     int ctas_per_sm = 0;    // resident CTAs the grid is sized for (0 = path default)
     int promotion = 256;    // L2 fill size of the TMA loads (0 = none)
-    int cluster_stages = 2; // ring depth of the cluster variant (each CTA holds two rings)
-    // The cluster variant is latency-bound per CTA pair, so it runs as many pairs as
-    // fit (measured on GB300: 2-deep rings at 3 CTAs/SM beat deeper rings at 1).
+    int cluster_stages = 2; // staging ring depth of the cluster variant
+    int cluster_recv = 1;   // its receive ring depth
+    int cluster_warps = 4;  // its consumer warps (8 or 4)
+    // The cluster variant is bound by the latency of each pair's hand-off chain
+    // (HBM load, DSMEM push, slot hand-backs), so it runs as many small CTAs as fit:
+    // measured on GB300, 4 consumer warps with a 2-deep staging ring and one receive
+    // slot (4 CTAs per SM) beat 8 warps and deeper rings on every workload.
 };
 
 TileTuning tile_tuning(const tl_permute_opts* o) {
@@ -51,8 +55,14 @@ TileTuning tile_tuning(const tl_permute_opts* o) {
     if (!o) return t;
     if (o->tile_group > 0) t.group = o->tile_group;
     if (o->tile_stages >= 2 && o->tile_stages <= kMaxTileStages) t.stages = o->tile_stages;
-    if (o->tile_stages >= 2 && o->tile_stages <= kMaxClusterStages)
+    if (o->tile_stages >= 1 && o->tile_stages <= kMaxClusterStages)
         t.cluster_stages = o->tile_stages;
+    if (o->cluster_recv_stages >= 1 && o->cluster_recv_stages <= kMaxClusterStages)
+        t.cluster_recv = o->cluster_recv_stages;
+    if (o->cluster_consumer_warps == 4 || o->cluster_consumer_warps == 8)
+        t.cluster_warps = o->cluster_consumer_warps;
+    if (t.cluster_stages + t.cluster_recv > kMaxClusterSlots)
+        t.cluster_recv = kMaxClusterSlots - t.cluster_stages;
     if (o->tile_ctas_per_sm > 0) t.ctas_per_sm = o->tile_ctas_per_sm;
     if (o->tile_rows == 256) t.rows = 256;
     const int max_stages = kTileRingBytes / (t.rows * 128);
@@ -101,19 +111,21 @@ int get_device_info(DevInfo* out) {
             }
             // The cluster variant is optional: if its set-up fails it is sized
             // conservatively (one CTA per SM) and the error is cleared.
-            const void* kc = cluster_kernel(1 << i);
-            const bool attr_ok = cudaFuncSetAttribute(kc,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                      cluster_smem_bytes(kMaxClusterStages)) ==
-                                 cudaSuccess;
-            for (int st = 2; st <= kMaxClusterStages; ++st) {
-                int& occ = d.cluster_occ[i][st];
-                if (!attr_ok || cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                                    &occ, kc, kClusterThreads, cluster_smem_bytes(st)) !=
-                                    cudaSuccess ||
-                    occ < 1) {
-                    cudaGetLastError();
-                    occ = 1;
+            for (int h = 0; h < 2; ++h) {
+                const int ncw = h ? 4 : 8;
+                const void* kc = cluster_kernel(1 << i, ncw);
+                const bool attr_ok =
+                    cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         cluster_smem_bytes(kMaxClusterSlots)) == cudaSuccess;
+                for (int st = 2; st <= kMaxClusterSlots; ++st) {
+                    int& occ = d.cluster_occ[i][h][st];
+                    if (!attr_ok || cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                                        &occ, kc, cluster_threads(ncw), cluster_smem_bytes(st)) !=
+                                        cudaSuccess ||
+                        occ < 1) {
+                        cudaGetLastError();
+                        occ = 1;
+                    }
                 }
             }
         }
@@ -223,11 +235,12 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         }
         break;
     case TL_PATH_CLUSTER:
-        l.block = kClusterThreads;
-        l.smem = cluster_smem_bytes(tt.cluster_stages);
+        l.block = cluster_threads(tt.cluster_warps);
+        l.smem = cluster_smem_bytes(tt.cluster_stages + tt.cluster_recv);
         if (sms) {
             // as many clusters as fit
-            int per_sm = d->cluster_occ[log2i(p.eb)][tt.cluster_stages];
+            int per_sm = d->cluster_occ[log2i(p.eb)][tt.cluster_warps == 4 ? 1 : 0]
+                                       [tt.cluster_stages + tt.cluster_recv];
             if (tt.ctas_per_sm > 0 && tt.ctas_per_sm < per_sm) per_sm = tt.ctas_per_sm;
             int64_t cap = sms * (per_sm < 1 ? 1 : per_sm) / 2;
             if (cap < 1) cap = 1;
@@ -359,7 +372,8 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.drop_handoff = (flags & TL_FLAG_TEST_DROP_HANDOFF) ? 1 : 0;
         if (p.path == TL_PATH_CLUSTER) {
             a.stages = tt.cluster_stages;
-            err = launch_cluster(eb, map, a, l.grid, st, pdl);
+            a.recv_stages = tt.cluster_recv;
+            err = launch_cluster(eb, tt.cluster_warps, map, a, l.grid, st, pdl);
             break;
         }
         if (p.tile_rows == 256) {

@@ -159,6 +159,17 @@ def test_tile_path_visit_groups(eb, group):
 
 
 @pytest.mark.parametrize("eb", WIDTHS)
+@pytest.mark.parametrize("staging,receive,warps", [(1, 1, 8), (3, 1, 8), (1, 3, 8), (4, 2, 8),
+                                                   (8, 4, 8), (2, 1, 4), (2, 2, 4), (1, 3, 4)])
+def test_cluster_ring_depths(eb, staging, receive, warps):
+    # staging and receive rings of unequal depth (slot indices of the two sides
+    # cycle with different periods), and four consumer warps taking two shares each
+    for i, (shape, ss, ds) in enumerate(_tile_shapes(eb)):
+        check(shape, ss, ds, eb, "cluster", seed=60 + i, tile_stages=staging,
+              cluster_recv_stages=receive, cluster_consumer_warps=warps)
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
 def test_tile_path_unaligned_dst_runs(eb):
     # dst columns of 33 rows: 16-byte runs straddle, the kernel stores element-wise
     c = max(1, 256 // eb)

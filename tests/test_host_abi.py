@@ -240,6 +240,22 @@ def test_tile_height_option():
     assert _plan(w, path="cluster", tile_rows=256)["tile_rows"] == 128
 
 
+def test_cluster_ring_options():
+    w = workloads.get("tile_transpose")
+    slot = 128 * 128
+    assert _plan(w, path="cluster")["smem_bytes"] == 3 * slot + 1024          # 2 + 1
+    assert _plan(w, path="cluster", tile_stages=3, cluster_recv_stages=1)["smem_bytes"] == \
+        4 * slot + 1024
+    assert _plan(w, path="cluster", tile_stages=1, cluster_recv_stages=1)["smem_bytes"] == \
+        2 * slot + 1024
+    # at most 12 slots: the receive ring gives way
+    assert _plan(w, path="cluster", tile_stages=8, cluster_recv_stages=8)["smem_bytes"] == \
+        12 * slot + 1024
+    assert _plan(w, path="cluster")["block"] == 7 * 32                # 4 consumer warps
+    assert _plan(w, path="cluster", cluster_consumer_warps=8)["block"] == 11 * 32
+    assert _plan(w, path="cluster", cluster_consumer_warps=5)["block"] == 7 * 32
+
+
 def test_forced_paths_that_do_not_apply():
     w = workloads.get("attention")
     for path in ("tile", "rows", "cluster"):

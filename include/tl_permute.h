@@ -162,6 +162,8 @@ TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape
 #define TL_PATH_WARP 4u     /* warp register-staged XOR-swizzle transpose (in-place safe) */
 #define TL_PATH_ROWS 5u     /* short dst runs (<= 16 B): 16 B row loads, register transpose */
 #define TL_PATH_CLUSTER 6u  /* TILE with a 2-CTA cluster handing tiles over through DSMEM */
+#define TL_PATH_PANEL 7u    /* plane transpose through padded smem, plain loads/stores: any
+                               element alignment, up to 6 batch axes, tiny extents */
 #define TL_PATH_MASK 0xFu
 /* Test hook for the cluster path: the producer CTA skips its DSMEM hand-off, so the
  * consumer's bounded wait must expire and report TL_ERR_TIMEOUT in dev_status. */
@@ -217,7 +219,9 @@ typedef struct tl_plan_info {
     int64_t tiles;                 /* work units (tiles, rows, warps...) */
     int32_t grid, block;           /* launch shape (0 without a device) */
     int32_t smem_bytes;            /* dynamic shared memory per CTA */
-    int32_t reserved[5];
+    int32_t pitch;                 /* panel path: shared-memory bytes per tile row */
+    int32_t panel_mode;            /* panel path: 0 rows of 16-byte blocks, 1 one run */
+    int32_t reserved[3];
 } tl_plan_info;
 
 TL_API int tl_plan(const void *src, const void *dst, int ndim, const int64_t *shape,

@@ -26,7 +26,8 @@ __all__ = [
 ]
 
 TL_MAX_DIMS = 8
-PATHS = {"auto": 0, "generic": 1, "chunk": 2, "tile": 3, "warp": 4, "rows": 5, "cluster": 6}
+PATHS = {"auto": 0, "generic": 1, "chunk": 2, "tile": 3, "warp": 4, "rows": 5, "cluster": 6,
+         "panel": 7}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 TL_FLAG_TEST_DROP_HANDOFF = 1 << 8
 TL_FLAG_NO_PDL = 1 << 9
@@ -71,7 +72,8 @@ class TlPlanInfo(ctypes.Structure):
                 ("src_str", _i64 * TL_MAX_DIMS), ("dst_str", _i64 * TL_MAX_DIMS),
                 ("vec_bytes", _i32), ("in_place", _i32), ("k", _i32), ("shift", _i32),
                 ("mask", _i32), ("tile_rows", _i32), ("tile_cols", _i32), ("tiles", _i64),
-                ("grid", _i32), ("block", _i32), ("smem_bytes", _i32), ("reserved", _i32 * 5)]
+                ("grid", _i32), ("block", _i32), ("smem_bytes", _i32), ("pitch", _i32),
+                ("panel_mode", _i32), ("reserved", _i32 * 3)]
 
 
 def library_path() -> str:
@@ -259,7 +261,7 @@ def tl_plan(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides, elem_by
                 vec_bytes=info.vec_bytes, in_place=bool(info.in_place), k=info.k,
                 shift=info.shift, mask=info.mask, tile_rows=info.tile_rows,
                 tile_cols=info.tile_cols, tiles=info.tiles, grid=info.grid, block=info.block,
-                smem_bytes=info.smem_bytes)
+                smem_bytes=info.smem_bytes, pitch=info.pitch, panel_mode=info.panel_mode)
 
 
 def _bytes_after(t) -> int:

@@ -1,0 +1,196 @@
+// k_panel.cu -- transpose of the plane through shared memory for the layouts the
+// TMA tile path cannot take: rows whose byte pitch is not a multiple of 16, more
+// than three batch axes, or a plane with a tiny extent (an interleaved-channel axis
+// of 3).
+//
+// Plane: axis a is contiguous in src, axis b is contiguous in dst; the rest are
+// batch axes.  A tile is ta elements of a by tb elements of b.  Each CTA runs a
+// ring of kPanelStages shared-memory stages: while it stores one tile, the
+// asynchronous copies (cp.async, 16 bytes each, no registers involved) of the next
+// tiles are in flight.  Each src row of a tile is copied as the aligned 16-byte
+// blocks that cover it, whatever the element alignment (a block that holds a byte
+// of the row never crosses a page the row does not touch), and lands at the same
+// offset inside its first block; when the tile's src rows are packed back to back
+// the whole tile is one run of blocks.
+//
+// The copy walks the tile in src order, so consecutive threads read consecutive
+// src addresses; the store walks it in dst order (element f -> a = f / tb,
+// b = f % tb), so consecutive threads write consecutive dst addresses.  The row
+// pitch in shared memory is chosen on the host by simulating both walks' warp
+// accesses against the banks (the bank model of the TVM "permute_layout" page,
+// "Algorithm", step 2).  Element offsets follow the strided addressing of
+// "Buffers and memory", "Declaring buffers".
+#include "tl_kernels.h"
+
+namespace tl {
+namespace {
+
+// 16-byte asynchronous copy global -> shared, cached in L2 only
+__device__ __forceinline__ void cp_async16(uint32_t saddr, uintptr_t gaddr) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gaddr) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+struct PanelTile {
+    int64_t so, dof;      // element offsets of the tile's (a0, b0) in src and dst
+    uint32_t va, vb;      // valid elements of a and b
+};
+
+// tile t -> (column block of a, row block of b, batch item); b fastest, so
+// concurrently running CTAs write dst front to back
+__device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
+    int64_t item, ia, ib;
+    if (a.use32) {
+        const uint32_t t32 = (uint32_t)t;
+        const uint32_t it = dev::div_u32(t32, a.d_item);
+        const uint32_t local = t32 - it * a.d_item.d;
+        const uint32_t qa = dev::div_u32(local, a.d_tiles_b);
+        item = it;
+        ia = qa;
+        ib = local - qa * a.d_tiles_b.d;
+    } else {
+        const int64_t per_item = a.tiles_a * a.tiles_b;
+        item = t / per_item;
+        const int64_t local = t - item * per_item;
+        ia = local / a.tiles_b;
+        ib = local - ia * a.tiles_b;
+    }
+    const int64_t a0 = ia * a.ta, b0 = ib * a.tb;
+    PanelTile r;
+    r.va = (uint32_t)min((int64_t)a.ta, a.ext_a - a0);
+    r.vb = (uint32_t)min((int64_t)a.tb, a.ext_b - b0);
+    r.so = a0 + b0 * a.ss_b;
+    r.dof = a0 * a.ds_a + b0;
+    for (int i = 0; i < a.nb; ++i) {
+        int64_t c;
+        if (a.use32) {
+            const uint32_t q = dev::div_u32((uint32_t)item, a.d_bext[i]);
+            c = (uint32_t)item - q * a.d_bext[i].d;
+            item = q;
+        } else {
+            c = item % a.bext[i];
+            item /= a.bext[i];
+        }
+        r.so += c * a.bss[i];
+        r.dof += c * a.bds[i];
+    }
+    return r;
+}
+
+// Start the copies of one tile into the stage at shared address `sb`: the
+// 16-byte blocks covering each src row of the tile (or the tile's single run).
+template <int EB>
+__device__ __forceinline__ void issue(const PanelArgs& a, const PanelTile& ti, uint32_t sb) {
+    const uintptr_t base = reinterpret_cast<uintptr_t>(a.src + ti.so * EB);
+    if (a.mode == kPanelRows) {
+        const uint32_t nblk = (uint32_t)a.nblk, n = (uint32_t)a.tb * nblk;
+        const uint32_t pitch = (uint32_t)a.pitch;
+        for (uint32_t g = threadIdx.x; g < n; g += kPanelThreads) {
+            const uint32_t b = dev::div_u32(g, a.d_nblk), k = g - b * nblk;
+            if (b >= ti.vb) continue;
+            const uintptr_t row = base + (uintptr_t)((int64_t)b * a.ss_b * EB);
+            const uint32_t blocks = ((uint32_t)(row & 15) + ti.va * EB + 15) >> 4;
+            if (k < blocks) cp_async16(sb + b * pitch + 16 * k, (row & ~uintptr_t(15)) + 16 * k);
+        }
+    } else {   // kPanelFlat: rows packed back to back (ss_b == ta == va)
+        const uint32_t blocks = ((uint32_t)(base & 15) + ti.vb * (uint32_t)a.ta * EB + 15) >> 4;
+        for (uint32_t k = threadIdx.x; k < blocks; k += kPanelThreads)
+            cp_async16(sb + 16 * k, (base & ~uintptr_t(15)) + 16 * k);
+    }
+}
+
+// Store one landed tile from the stage at `st` to dst, in dst order.
+template <int EB>
+__device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, const uint8_t* st) {
+    using T = typename dev::Bits<EB>::T;
+    T* d = reinterpret_cast<T*>(a.dst) + ti.dof;
+    const uint32_t ta = (uint32_t)a.ta, tb = (uint32_t)a.tb, pitch = (uint32_t)a.pitch;
+    const uint32_t mis0 = (uint32_t)(reinterpret_cast<uintptr_t>(a.src + ti.so * EB) & 15);
+    const uint32_t ssb16 = (uint32_t)((a.ss_b * EB) & 15);
+    const bool rows = a.mode == kPanelRows;
+    if (kPanelThreads % tb == 0) {
+        // each thread keeps one b and steps a by kPanelThreads / tb
+        const uint32_t b = threadIdx.x % tb, de = kPanelThreads / tb;
+        if (b >= ti.vb) return;
+        const uint8_t* sp = rows ? st + b * pitch + ((mis0 + b * ssb16) & 15) : st + mis0 + b * ta * EB;
+        T* dp = d + b;
+        const int64_t dstep = (int64_t)de * a.ds_a;
+        uint32_t e = threadIdx.x / tb;
+        dp += (int64_t)e * a.ds_a;
+#pragma unroll 4
+        for (; e < ti.va; e += de, dp += dstep) *dp = *reinterpret_cast<const T*>(sp + e * EB);
+        return;
+    }
+    const uint32_t n = ta * tb;
+#pragma unroll 4
+    for (uint32_t f = threadIdx.x; f < n; f += kPanelThreads) {
+        const uint32_t e = dev::div_u32(f, a.d_tb), b = f - e * tb;   // a, b in the tile
+        if (e >= ti.va || b >= ti.vb) continue;
+        const uint32_t off = rows ? b * pitch + ((mis0 + b * ssb16) & 15) + e * EB
+                                  : mis0 + (b * ta + e) * EB;
+        d[(int64_t)e * a.ds_a + b] = *reinterpret_cast<const T*>(st + off);
+    }
+}
+
+template <int EB>
+__global__ void __launch_bounds__(kPanelThreads) k_panel(const PanelArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const uint32_t sbase = dev::smem_addr(smem);
+    const uint32_t stage = (uint32_t)a.stage_bytes;
+    dev::grid_dependency_wait();
+    dev::allow_dependent_launch();
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t mine = first < a.tiles ? (a.tiles - first + step - 1) / step : 0;
+
+    // Every thread commits one group per tile slot (empty groups included), so
+    // wait_group counts the same groups in every thread.
+    for (int s = 0; s < kPanelStages - 1; ++s) {
+        if (s < mine) issue<EB>(a, panel_tile(first + s * step, a), sbase + s * stage);
+        cp_async_commit();
+    }
+    uint32_t slot = 0, ahead = kPanelStages - 1;    // stage of tile i and of tile i + S - 1
+    for (int64_t i = 0; i < mine; ++i) {
+        const int64_t nxt = i + kPanelStages - 1;
+        if (nxt < mine) issue<EB>(a, panel_tile(first + nxt * step, a), sbase + ahead * stage);
+        cp_async_commit();
+        cp_async_wait<kPanelStages - 1>();           // tile i has landed (this thread's part)
+        __syncthreads();                             // ... and every other thread's part
+        drain<EB>(a, panel_tile(first + i * step, a), smem + slot * stage);
+        __syncthreads();                             // stage `slot` may be refilled
+        slot = slot + 1 == kPanelStages ? 0 : slot + 1;
+        ahead = ahead + 1 == kPanelStages ? 0 : ahead + 1;
+    }
+    cp_async_wait<0>();
+}
+
+}  // namespace
+
+const void* panel_kernel(int eb) {
+    switch (eb) {
+    case 1: return reinterpret_cast<const void*>(&k_panel<1>);
+    case 2: return reinterpret_cast<const void*>(&k_panel<2>);
+    case 4: return reinterpret_cast<const void*>(&k_panel<4>);
+    case 8: return reinterpret_cast<const void*>(&k_panel<8>);
+    default: return reinterpret_cast<const void*>(&k_panel<16>);
+    }
+}
+
+cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,
+                         bool pdl) {
+    const dim3 g(grid), b(kPanelThreads);
+    switch (eb) {
+    case 1: return launch_kernel(k_panel<1>, g, b, smem, st, pdl, a);
+    case 2: return launch_kernel(k_panel<2>, g, b, smem, st, pdl, a);
+    case 4: return launch_kernel(k_panel<4>, g, b, smem, st, pdl, a);
+    case 8: return launch_kernel(k_panel<8>, g, b, smem, st, pdl, a);
+    default: return launch_kernel(k_panel<16>, g, b, smem, st, pdl, a);
+    }
+}
+
+}  // namespace tl

@@ -324,6 +324,112 @@ bool tile_ok(const Plan& p, int64_t src) {
     return true;
 }
 
+// Tile-path fit: tiles at least half full (64 rows of b, 64 bytes of a).  Below
+// that the panel kernel moves fewer idle bytes.
+bool tile_fits(const Plan& p) { return p.ext_b >= 64 && p.ext_a * p.eb >= 64; }
+
+// Panel path: the plane needs one extent of at least 16 elements (else the
+// batch is the long dimension and the generic kernel walks it as well).
+bool panel_ok(const Plan& p) { return p.ext_a >= 16 || p.ext_b >= 16; }
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// Panel pitch: the byte pitch (a multiple of 16) of the rows of the shared-memory
+// tile, chosen by simulating both walks' warp accesses on the banks (hardware
+// model).  The copy walk takes item g, a 16-byte block, at (b = g / blocks_per_row,
+// k = g % blocks_per_row); the store walk takes tile element f at (a = f / tb,
+// b = f % tb), whose row starts (r + b * (ss_b * eb mod 16)) mod 16 bytes into its
+// first block, simulated for every residue r of the tile's base address.  A warp
+// covers 32 consecutive items.  The first pitch with the lowest summed degree wins.
+struct PanelMemo {
+    int ta, tb, eb, ssb16, pitch;
+};
+std::mutex g_panel_memo_mu;
+std::vector<PanelMemo> g_panel_memo;
+
+int panel_blocks_per_row(int64_t ta, int eb) { return (int)((ta * eb + 30) / 16); }
+
+int panel_pitch(int ta, int tb, int eb, int ssb16) {
+    {
+        std::lock_guard<std::mutex> lk(g_panel_memo_mu);
+        for (const PanelMemo& e : g_panel_memo)
+            if (e.ta == ta && e.tb == tb && e.eb == eb && e.ssb16 == ssb16) return e.pitch;
+    }
+    const int64_t nblk = panel_blocks_per_row(ta, eb);
+    const int64_t n_copy = nblk * tb, n_store = (int64_t)ta * tb;
+    const int64_t samples = 32 * 64;
+    int best = (int)(16 * nblk);
+    int64_t best_cost = -1;
+    for (int64_t q = nblk; q < nblk + 8; ++q) {
+        const int64_t pitch = 16 * q;
+        int64_t cost = 0, ideal = 0;
+        for (int64_t g0 = 0; g0 < std::min(n_copy, samples); g0 += 32, ++ideal) {
+            int64_t o[32];
+            int m = 0;
+            for (int64_t g = g0; g < g0 + 32 && g < n_copy; ++g, ++m)
+                o[m] = (g / nblk) * q + g % nblk;                  // 16-byte units
+            cost += bank_degree(m, o, 16, true);
+        }
+        for (int r = 0; r < 16; r += eb) {
+            for (int64_t f0 = 0; f0 < std::min(n_store, samples); f0 += 32, ++ideal) {
+                int64_t o[32];
+                int m = 0;
+                for (int64_t f = f0; f < f0 + 32 && f < n_store; ++f, ++m) {
+                    const int64_t a = f / tb, b = f % tb;
+                    o[m] = (b * pitch + ((r + b * ssb16) & 15) + a * eb) / eb;
+                }
+                cost += bank_degree(m, o, eb, true);
+            }
+        }
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = (int)pitch;
+        }
+        if (best_cost == ideal) break;   // degree 1 everywhere
+    }
+    std::lock_guard<std::mutex> lk(g_panel_memo_mu);
+    if (g_panel_memo.size() >= 64) g_panel_memo.erase(g_panel_memo.begin());
+    g_panel_memo.push_back({ta, tb, eb, ssb16, best});
+    return best;
+}
+
+// Panel tile of about 8 KiB: a tiny extent is taken whole and the other one
+// fills the tile; otherwise 64 (eb <= 2) or 32 rows of b by 8 KiB of a; no tile
+// side exceeds its extent.  Src rows packed back to back are copied as one run.
+void plan_panel(Plan* p) {
+    const int eb = p->eb;
+    const int64_t E = 8192 / eb;
+    int64_t ta, tb;
+    if (p->ext_b <= 16) {
+        tb = p->ext_b;
+        ta = std::min(round_up((E + tb - 1) / tb, 32), p->ext_a);
+    } else if (p->ext_a <= 16) {
+        ta = p->ext_a;
+        tb = std::min(round_up((E + ta - 1) / ta, 32), p->ext_b);
+    } else {
+        tb = std::min<int64_t>(eb <= 2 ? 64 : 32, p->ext_b);
+        ta = std::min(E / tb, p->ext_a);
+    }
+    p->tile_cols = (int)ta;
+    p->tile_rows = (int)tb;
+    int64_t stage;
+    if (ta == p->ext_a && p->ss_b == ta) {
+        p->panel_mode = 1;
+        p->pitch = 0;
+        p->panel_nblk = 0;
+        stage = 16 * ((ta * tb * eb + 30) / 16);
+    } else {
+        p->panel_mode = 0;
+        p->panel_nblk = panel_blocks_per_row(ta, eb);
+        p->pitch = panel_pitch((int)ta, (int)tb, eb, (int)((p->ss_b * eb) & 15));
+        stage = tb * p->pitch;
+    }
+    p->panel_stage = (int)stage;
+    const int64_t na = (p->ext_a + ta - 1) / ta, nb = (p->ext_b + tb - 1) / tb;
+    p->tiles = na * nb * p->batch_total;
+    p->vec_bytes = eb;
+}
+
 }  // namespace
 
 int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
@@ -334,7 +440,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     if (ndim < 0 || ndim > kMaxDims) return TL_ERR_ARG;
     if (ndim > 0 && (!shape || !src_strides || !dst_strides)) return TL_ERR_ARG;
     const uint32_t forced = flags & TL_PATH_MASK;
-    if (forced > TL_PATH_CLUSTER) return TL_ERR_ARG;
+    if (forced > TL_PATH_PANEL) return TL_ERR_ARG;
     p.eb = eb;
     int64_t total = 1;
     for (int i = 0; i < ndim; ++i) {
@@ -399,6 +505,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     const bool plane = plan_plane(&p);
     const bool rows = plane && rows_ok(p, s0, d0);
     const bool tile = plane && tile_ok(p, s0);
+    const bool panel = plane && panel_ok(p);
 
     int path = 0;
     if (ranges_meet) {
@@ -411,6 +518,8 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         if (chunk_ok) path = TL_PATH_CHUNK;
         else if (warp_ok) path = TL_PATH_WARP;
         else if (rows) path = TL_PATH_ROWS;
+        else if (tile && tile_fits(p)) path = TL_PATH_TILE;
+        else if (panel) path = TL_PATH_PANEL;
         else if (tile) path = TL_PATH_TILE;
         else path = TL_PATH_GENERIC;
         break;
@@ -420,6 +529,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     case TL_PATH_ROWS: path = rows ? TL_PATH_ROWS : 0; break;
     case TL_PATH_TILE: path = tile ? TL_PATH_TILE : 0; break;
     case TL_PATH_CLUSTER: path = tile ? TL_PATH_CLUSTER : 0; break;
+    case TL_PATH_PANEL: path = panel ? TL_PATH_PANEL : 0; break;
     }
     if (path == 0) return TL_ERR_PATH;
     p.path = path;
@@ -455,6 +565,8 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         const int64_t ta = (p.ext_a + p.tile_cols - 1) / p.tile_cols;
         const int64_t tb = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
         p.tiles = ta * tb * p.batch_total;
+    } else if (path == TL_PATH_PANEL) {
+        plan_panel(&p);
     } else if (path == TL_PATH_ROWS) {
         p.vec_bytes = 16;
         p.tiles = p.batch_total * (p.ext_a * eb / 16);

@@ -41,7 +41,11 @@ struct Plan {
     Axes batch;            // batch axes (outermost first)
     int64_t batch_total = 1;
     bool vec_store = false;  // 16-byte aligned dst runs
-    int tile_rows = 0, tile_cols = 0;
+    int tile_rows = 0, tile_cols = 0;   // TILE: 128 x 128/eb; PANEL: tb x ta elements
+    int pitch = 0;                      // PANEL: shared-memory bytes per tile row
+    int panel_mode = 0;                 // PANEL: PanelMode (block rows, one block run)
+    int panel_nblk = 0;                 // PANEL: 16-byte blocks copied per row (at most)
+    int panel_stage = 0;                // PANEL: shared-memory bytes of one ring stage
     int64_t tiles = 0;
 
     // WARP: tile (innermost suffix of `kept`) + batch of the outer `kept` axes.

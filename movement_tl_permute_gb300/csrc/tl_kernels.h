@@ -123,6 +123,41 @@ struct RowsArgs {
 cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, cudaStream_t st,
                         bool pdl);
 
+// ---------------------------------------------------------------- panel
+// Transpose of (ta x tb)-element tiles of the plane through shared memory: the
+// 16-byte blocks covering each tile row are copied asynchronously (cp.async) into
+// a ring of stages, then stored in dst order; any element alignment, up to 6 batch
+// axes, tiny extents.
+constexpr int kPanelThreads = 256;
+constexpr int kPanelStages = 3;
+enum PanelMode : int32_t {
+    kPanelRows = 0,    // row b copied as the 16-byte blocks covering it, at byte
+                       // b * pitch; element a at byte (row address mod 16) + a * eb
+    kPanelFlat = 1,    // src rows packed back to back (ss_b == ta == ext_a): the tile's
+                       // src bytes are one run; element (a, b) at mis + (b*ta + a)*eb
+};
+struct PanelArgs {
+    const uint8_t* src;
+    uint8_t* dst;
+    int64_t ext_a, ext_b;        // plane: a src-contiguous, b dst-contiguous
+    int64_t ss_b, ds_a;          // src stride of b, dst stride of a (elements)
+    int32_t ta, tb;              // tile: ta elements of a x tb elements of b
+    int32_t pitch;               // kPanelRows: shared-memory bytes per row (multiple of 16)
+    int32_t mode;                // PanelMode
+    int32_t nblk;                // kPanelRows: 16-byte blocks copied per row (at most)
+    int32_t stage_bytes;         // shared memory of one stage (multiple of 16)
+    int32_t nb;                  // batch axes (innermost first)
+    int32_t use32;               // tile indices fit in 32 bits
+    int64_t tiles_a, tiles_b, tiles;
+    int64_t bext[TL_MAX_DIMS], bss[TL_MAX_DIMS], bds[TL_MAX_DIMS];
+    dev::DivU32 d_tb, d_nblk;    // divisors of the per-tile walks
+    dev::DivU32 d_item, d_tiles_b;
+    dev::DivU32 d_bext[TL_MAX_DIMS];
+};
+const void* panel_kernel(int eb);
+cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,
+                         bool pdl);
+
 // ---------------------------------------------------------------- warp
 struct WarpArgs {
     const uint8_t* src;

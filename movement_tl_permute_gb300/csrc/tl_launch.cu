@@ -247,6 +247,21 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
             l.grid = 2 * cap_grid(p.tiles, cap, max_ctas > 0 ? (max_ctas + 1) / 2 : 0);
         }
         break;
+    case TL_PATH_PANEL:
+        l.block = kPanelThreads;
+        l.smem = kPanelStages * p.panel_stage;
+        if (sms) {
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, panel_kernel(p.eb),
+                                                              kPanelThreads, l.smem) !=
+                    cudaSuccess ||
+                per_sm < 1) {
+                cudaGetLastError();
+                per_sm = 1;
+            }
+            l.grid = cap_grid(p.tiles, sms * per_sm, max_ctas);
+        }
+        break;
     case TL_PATH_ROWS:
         l.block = p.ext_b >= 16 ? 128 : 256;   // must match rows_threads<R>() in k_rows.cu
         if (sms) l.grid = cap_grid((p.tiles + 511) / 512, sms * 8, max_ctas);
@@ -395,6 +410,40 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         }
         break;
     }
+    case TL_PATH_PANEL: {
+        PanelArgs a{};
+        a.src = s8;
+        a.dst = d8;
+        a.ext_a = p.ext_a;
+        a.ext_b = p.ext_b;
+        a.ss_b = p.ss_b;
+        a.ds_a = p.ds_a;
+        a.ta = p.tile_cols;
+        a.tb = p.tile_rows;
+        a.pitch = p.pitch;
+        a.mode = p.panel_mode;
+        a.nblk = p.panel_nblk;
+        a.stage_bytes = p.panel_stage;
+        a.d_nblk = dev::make_divu32((uint32_t)(p.panel_nblk > 0 ? p.panel_nblk : 1));
+        a.tiles_a = (p.ext_a + a.ta - 1) / a.ta;
+        a.tiles_b = (p.ext_b + a.tb - 1) / a.tb;
+        a.tiles = p.tiles;
+        a.nb = p.batch.n;
+        for (int i = 0; i < TL_MAX_DIMS; ++i) { a.bext[i] = 1; a.bss[i] = 0; a.bds[i] = 0; }
+        for (int i = 0; i < a.nb; ++i) {               // innermost (smallest dst stride) first
+            const int j = a.nb - 1 - i;
+            a.bext[i] = p.batch.ext[j]; a.bss[i] = p.batch.ss[j]; a.bds[i] = p.batch.ds[j];
+        }
+        a.d_tb = dev::make_divu32((uint32_t)a.tb);
+        a.use32 = p.tiles < (1LL << 32) ? 1 : 0;
+        if (a.use32) {
+            a.d_item = dev::make_divu32((uint32_t)(a.tiles_a * a.tiles_b));
+            a.d_tiles_b = dev::make_divu32((uint32_t)a.tiles_b);
+            fill_divs(a.nb, a.bext, a.d_bext);
+        }
+        err = launch_panel(eb, a, l.grid, l.smem, st, pdl);
+        break;
+    }
     case TL_PATH_ROWS: {
         RowsArgs a{};
         a.src = s8;
@@ -488,6 +537,8 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     apply_tile_rows(p, tt);
     info.tile_rows = p.tile_rows;
     info.tile_cols = p.tile_cols;
+    info.pitch = p.pitch;
+    info.panel_mode = p.panel_mode;
     info.tiles = p.tiles;
     int ndev = 0;
     DevInfo d;

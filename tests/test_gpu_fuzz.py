@@ -18,7 +18,7 @@ from oracle import layout_ref as L
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-PATHS = ["auto", "generic", "chunk", "tile", "rows", "warp", "cluster"]
+PATHS = ["auto", "generic", "chunk", "tile", "rows", "warp", "cluster", "panel"]
 CANARY = 0x3C
 
 
@@ -86,7 +86,7 @@ def test_random_layouts_every_applicable_path():
             if path == "tile":                  # the 256-row tile variant as well
                 got, want = _run(shape, ss, ds, eb, so, do, path, seed=i, tile_rows=256)
                 assert np.array_equal(got, want), (shape, ss, ds, eb, so, do, "tile256")
-    assert all(ran[p] > 0 for p in ("auto", "generic", "chunk", "tile")), ran
+    assert all(ran[p] > 0 for p in ("auto", "generic", "chunk", "tile", "panel")), ran
 
 
 def test_concurrent_calls_from_host_threads():

@@ -71,6 +71,12 @@ def test_tile_path_past_4gib():
     check_sampled((R, C), (C, 1), (1, R), 2, "tile", seed=71)
 
 
+def test_panel_path_past_4gib():
+    # u8 65537 x 65539 (odd row pitch, no TMA) row-major -> column-major: 4.3 GB each way
+    R, C = 65537, 65539
+    check_sampled((R, C), (C, 1), (1, R), 1, "panel", seed=75)
+
+
 def test_chunk_path_past_4gib():
     # (B, H, S, D) -> (B, S, H, D) with 4.3 GB of bf16: row offsets beyond 2^32 bytes
     shape = (33, 32, 4096, 512)

@@ -177,6 +177,40 @@ def test_tile_path_unaligned_dst_runs(eb):
     check((33, c), (c, 1), (1, 33), eb, "tile", seed=4, dst_off=1)
 
 
+def _panel_cases(eb):
+    out = []
+    # odd row pitches with ragged tiles on both sides
+    for rows, cols in ((300, 517), (33, 1001), (1001, 33), (129, 65), (2, 700), (700, 2)):
+        out.append(((rows, cols), (cols, 1), (1, rows)))
+    # interleaved channels <-> planes, 1..16 channels
+    for c in (3, 5, 16):
+        out.append(((70, 90, c), (90 * c, c, 1), (90, 1, 70 * 90)))        # HWC -> CHW
+        out.append(((c, 70, 90), (70 * 90, 90, 1), (1, 90 * c, c)))        # CHW -> HWC
+    # more than three batch axes, with padded source strides
+    shape = (3, 2, 4, 2, 40, 36)
+    ss, ds = perm_layouts(shape, (5, 3, 1, 4, 2, 0))
+    out.append((shape, ss, ds))
+    ss2 = tuple(x * 2 for x in ss[:-1]) + (1,)
+    out.append((shape, ss2, ds))
+    return out
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
+def test_panel_path(eb):
+    for i, (shape, ss, ds) in enumerate(_panel_cases(eb)):
+        check(shape, ss, ds, eb, "panel", seed=70 + i)
+        check(shape, ss, ds, eb, "panel", seed=80 + i, src_off=1, dst_off=3)
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
+def test_auto_takes_panel_for_untiled_planes(eb):
+    # a 3-channel interleave and an odd-pitch transpose go to the panel kernel
+    for shape, ss, ds in ((( 64, 96, 3), (96 * 3, 3, 1), (96, 1, 64 * 96)),
+                          ((3, 64, 96), (64 * 96, 96, 1), (1, 96 * 3, 3))):
+        assert tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb)["path"] in ("panel", "rows")
+        check(shape, ss, ds, eb, "auto", seed=90)
+
+
 @pytest.mark.parametrize("eb,R", [(1, 2), (1, 4), (1, 8), (1, 16), (2, 2), (2, 4), (2, 8),
                                   (4, 2), (4, 4), (8, 2)])
 def test_rows_path(eb, R):
@@ -221,7 +255,7 @@ def test_auto_paths_on_random_layouts():
         ss, ds = perm_layouts(shape, perm)
         seen.add(tl.tl_plan(1 << 20, 1 << 34, shape, ss, ds, eb)["path"])
         check(shape, ss, ds, eb, "auto", seed=i)
-    assert len(seen) >= 3
+    assert {"chunk", "panel"} <= seen, seen
 
 
 # ---------------------------------------------------------------------------

@@ -202,6 +202,78 @@ def test_tile_kernel_smem_reads_are_conflict_free(eb):
     assert len(words) == 16384 // 4
 
 
+def _perm_layout(shape, perm):
+    ss = L.row_major_strides(shape)
+    pst = L.row_major_strides(tuple(shape[p] for p in perm))
+    ds = [0] * len(shape)
+    for i, p in enumerate(perm):
+        ds[p] = pst[i]
+    return ss, tuple(ds)
+
+
+PANEL_LAYOUTS = [
+    # odd row pitches (no TMA), every width but 16 (16-byte rows always suit TMA)
+    ((16383, 16385), (1, 0), 1), ((16383, 16385), (1, 0), 2), ((16383, 16385), (1, 0), 4),
+    ((16383, 16385), (1, 0), 8),
+    # interleaved channels <-> planes
+    ((1024, 1024, 3), (2, 0, 1), 4), ((3, 1024, 1024), (1, 2, 0), 4),
+    ((1024, 1024, 3), (2, 0, 1), 1), ((3, 1024, 1024), (1, 2, 0), 1),
+    ((1024, 1024, 6), (2, 0, 1), 2),
+    # more than three batch axes
+    ((8, 4, 8, 4, 64, 64), (5, 3, 1, 4, 2, 0), 4),
+]
+
+
+def _panel_degrees(ta, tb, eb, pitch, ssb):
+    """Per-warp bank-conflict degrees (oracle model, hardware mode) of the panel
+    kernel's two walks for a block-row layout of byte pitch `pitch`: the copy walk
+    (16-byte blocks, row b at b * pitch) and the store walk (tile element f at
+    a = f // tb, b = f % tb, row b starting (r + b * ss_b * eb) mod 16 bytes into
+    its first block, for every base residue r)."""
+    nblk = (ta * eb + 30) // 16
+    q = pitch // 16
+    copy = [L.bank_conflict_degree([(g // nblk) * q + g % nblk
+                                    for g in range(g0, min(nblk * tb, g0 + 32))], 16, "hardware")
+            for g0 in range(0, nblk * tb, 32)]
+    store = []
+    for r in range(0, 16, eb):
+        for f0 in range(0, ta * tb, 32):
+            offs = [((f % tb) * pitch + ((r + (f % tb) * ssb * eb) & 15) + (f // tb) * eb) // eb
+                    for f in range(f0, min(ta * tb, f0 + 32))]
+            store.append(L.bank_conflict_degree(offs, eb, "hardware"))
+    return copy, store
+
+
+@pytest.mark.parametrize("shape,perm,eb", PANEL_LAYOUTS)
+def test_panel_layout_against_the_bank_model(shape, perm, eb):
+    """The shared-memory layout the planner picks for the panel kernel, replayed
+    through the oracle's bank model.  Rows copied as 16-byte blocks start on a
+    16-byte boundary plus the row's own misalignment, so the column-wise store walk
+    cannot be conflict-free in general: the padding the planner picks must do no
+    worse than no padding, keep the copy walk within 2-way and the store walk within
+    4-way.  Packed src rows are one run: the store walk stays within 2-way."""
+    ss, ds = _perm_layout(shape, perm)
+    p = tl.tl_plan(SRC, DST, shape, ss, ds, eb)
+    assert p["path"] == "panel"
+    ta, tb, pitch, mode = p["tile_cols"], p["tile_rows"], p["pitch"], p["panel_mode"]
+    ssb = [x for x, d in zip(p["src_str"], p["dst_str"]) if d == 1][0]
+    n = ta * tb
+    if mode == 0:
+        nblk = (ta * eb + 30) // 16
+        assert pitch % 16 == 0 and 16 * nblk <= pitch < 16 * (nblk + 8)
+        assert p["smem_bytes"] == 3 * tb * pitch
+        copy, store = _panel_degrees(ta, tb, eb, pitch, ssb)
+        copy0, store0 = _panel_degrees(ta, tb, eb, 16 * nblk, ssb)
+        assert sum(copy) + sum(store) <= sum(copy0) + sum(store0)
+        assert max(copy) <= 2 and max(store) <= 4
+    else:
+        assert mode == 1 and ssb == ta and p["pitch"] == 0      # packed src rows
+        assert p["smem_bytes"] == 3 * 16 * ((n * eb + 30) // 16)
+        for f0 in range(0, n, 32):
+            offs = [(f % tb) * ta + f // tb for f in range(f0, min(n, f0 + 32))]
+            assert L.bank_conflict_degree(offs, eb, "hardware") <= 2
+
+
 # ---------------------------------------------------------------------------
 # planner and validation (tl_plan; no device needed)
 # ---------------------------------------------------------------------------
@@ -258,7 +330,7 @@ def test_cluster_ring_options():
 
 def test_forced_paths_that_do_not_apply():
     w = workloads.get("attention")
-    for path in ("tile", "rows", "cluster"):
+    for path in ("tile", "rows", "cluster", "panel"):
         with pytest.raises(tl.TLError) as e:
             _plan(w, path=path)
         assert e.value.name == "TL_ERR_PATH"
@@ -289,7 +361,7 @@ def test_validation_errors():
     assert tl.tl_plan(SRC, DST, (), (), (), 16)["path"] == "chunk"
     assert tl.tl_plan(SRC, DST, (4, 4), (4, 1), (1, 4), 4, dst_bytes=64)["path"] != "none"
     # sub-element misalignment is allowed for 1-byte elements
-    assert tl.tl_plan(SRC + 1, DST + 3, (64, 64), (64, 1), (1, 64), 1)["path"] == "generic"
+    assert tl.tl_plan(SRC + 1, DST + 3, (64, 64), (64, 1), (1, 64), 1)["path"] == "panel"
 
 
 def test_in_place_only_on_the_warp_path():

@@ -183,7 +183,8 @@ typedef struct tl_permute_opts {
     int64_t src_bytes;    /* > 0: bytes addressable from src; the layout must fit */
     int64_t dst_bytes;    /* > 0: bytes addressable from dst */
     /* Tuning of the tile path; 0 selects the planner's default for each. */
-    int32_t tile_group;   /* tile rows visited together (visit order; default all) */
+    int32_t tile_group;   /* tile rows visited together (tile and panel visit order;
+                             default: the whole extent) */
     int32_t tile_stages;  /* shared-memory ring depth: 2..12 (tile, 128-row tiles),
                              2..6 (tile, 256-row tiles); cluster: staging ring, 1..8 */
     int32_t tile_ctas_per_sm;  /* resident CTAs per SM the grid is sized for */
@@ -193,7 +194,8 @@ typedef struct tl_permute_opts {
     int32_t cluster_recv_stages; /* cluster: receive ring depth, 1..8 (staging + receive
                                     slots at most 12) */
     int32_t cluster_consumer_warps; /* cluster: consumer warps per CTA, 4 or 8 */
-    int32_t reserved;
+    int32_t panel_tile_kib;       /* panel path: tile size, 4..32 KiB (default 32, or 16
+                                     with an extent of 16 or less) */
 } tl_permute_opts;
 
 /* tl_permute with options (path forcing, status word, buffer bounds).

@@ -64,7 +64,7 @@ class TlPermuteOpts(ctypes.Structure):
                 ("src_bytes", _i64), ("dst_bytes", _i64), ("tile_group", _i32),
                 ("tile_stages", _i32), ("tile_ctas_per_sm", _i32), ("tile_l2_promotion", _i32),
                 ("tile_rows", _i32), ("cluster_recv_stages", _i32),
-                ("cluster_consumer_warps", _i32), ("reserved", _i32)]
+                ("cluster_consumer_warps", _i32), ("panel_tile_kib", _i32)]
 
 
 class TlPlanInfo(ctypes.Structure):
@@ -195,8 +195,9 @@ def tl_bank_conflicts(lane_offsets, elem_bytes, model="conservative") -> int:
 
 def _opts(flags=0, path="auto", dev_status=0, src_bytes=0, dst_bytes=0, max_ctas=0,
           tile_group=0, tile_stages=0, tile_ctas_per_sm=0, tile_l2_promotion=0, tile_rows=0,
-          cluster_recv_stages=0, cluster_consumer_warps=0):
+          cluster_recv_stages=0, cluster_consumer_warps=0, panel_tile_kib=0):
     o = TlPermuteOpts()
+    o.panel_tile_kib = int(panel_tile_kib)
     o.cluster_consumer_warps = int(cluster_consumer_warps)
     o.tile_rows = int(tile_rows)
     o.cluster_recv_stages = int(cluster_recv_stages)
@@ -226,7 +227,7 @@ def tl_permute_ex(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides,
     """tl_permute with options: path=..., flags=..., dev_status=<device ptr>,
     src_bytes=..., dst_bytes=..., max_ctas=..., and the tile tuning fields
     tile_group, tile_stages, tile_ctas_per_sm, tile_l2_promotion, tile_rows,
-    cluster_recv_stages, cluster_consumer_warps"""
+    cluster_recv_stages, cluster_consumer_warps, panel_tile_kib"""
     o = _opts(**opts)
     _check(load().tl_permute_ex(int(src_ptr) or None, int(dst_ptr) or None, len(shape),
                                 _arr(shape), _arr(src_strides), _arr(dst_strides),

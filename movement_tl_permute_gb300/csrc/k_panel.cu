@@ -42,24 +42,35 @@ struct PanelTile {
     uint32_t va, vb;      // valid elements of a and b
 };
 
-// tile t -> (column block of a, row block of b, batch item); b fastest, so
-// concurrently running CTAs write dst front to back
+// tile t -> (column block of a, row block of b, batch item).  Tile rows are
+// visited in groups of group_b, b fastest inside a group: concurrently running
+// CTAs then write runs of group_b * tb elements of dst rows while the tiles beside
+// each other along a, which share the 16-byte blocks at their row ends, are in
+// flight together and meet those blocks in L2.
 __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
     int64_t item, ia, ib;
     if (a.use32) {
         const uint32_t t32 = (uint32_t)t;
         const uint32_t it = dev::div_u32(t32, a.d_item);
         const uint32_t local = t32 - it * a.d_item.d;
-        const uint32_t qa = dev::div_u32(local, a.d_tiles_b);
+        const uint32_t grp = dev::div_u32(local, a.d_grp);
+        const uint32_t first = grp * a.d_gfull.d;
+        const uint32_t in_grp = local - grp * a.d_grp.d;
+        const dev::DivU32& dg = first + a.d_gfull.d > (uint32_t)a.tiles_b ? a.d_glast : a.d_gfull;
+        const uint32_t qa = dev::div_u32(in_grp, dg);
         item = it;
         ia = qa;
-        ib = local - qa * a.d_tiles_b.d;
+        ib = first + (in_grp - qa * dg.d);
     } else {
         const int64_t per_item = a.tiles_a * a.tiles_b;
         item = t / per_item;
         const int64_t local = t - item * per_item;
-        ia = local / a.tiles_b;
-        ib = local - ia * a.tiles_b;
+        const int64_t grp = local / (a.group_b * a.tiles_a);
+        const int64_t first = grp * a.group_b;
+        const int64_t gsize = min(a.group_b, a.tiles_b - first);
+        const int64_t in_grp = local - grp * a.group_b * a.tiles_a;
+        ia = in_grp / gsize;
+        ib = first + in_grp % gsize;
     }
     const int64_t a0 = ia * a.ta, b0 = ib * a.tb;
     PanelTile r;

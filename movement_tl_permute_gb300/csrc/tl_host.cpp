@@ -393,12 +393,16 @@ int panel_pitch(int ta, int tb, int eb, int ssb16) {
     return best;
 }
 
-// Panel tile of about 8 KiB: a tiny extent is taken whole and the other one
-// fills the tile; otherwise 64 (eb <= 2) or 32 rows of b by 8 KiB of a; no tile
+// Panel tile of about tile_bytes: a tiny extent is taken whole and the other one
+// fills the tile; otherwise 64 (eb <= 2) or 32 rows of b by the rest; no tile
 // side exceeds its extent.  Src rows packed back to back are copied as one run.
-void plan_panel(Plan* p) {
+}  // namespace
+
+void plan_panel(Plan* p, int tile_bytes) {
     const int eb = p->eb;
-    const int64_t E = 8192 / eb;
+    const bool tiny = p->ext_a <= 16 || p->ext_b <= 16;
+    if (tile_bytes <= 0) tile_bytes = tiny ? 16384 : 32768;
+    const int64_t E = tile_bytes / eb;
     int64_t ta, tb;
     if (p->ext_b <= 16) {
         tb = p->ext_b;
@@ -429,8 +433,6 @@ void plan_panel(Plan* p) {
     p->tiles = na * nb * p->batch_total;
     p->vec_bytes = eb;
 }
-
-}  // namespace
 
 int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
               const int64_t* src_strides, const int64_t* dst_strides, int eb, uint32_t flags,
@@ -566,7 +568,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         const int64_t tb = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
         p.tiles = ta * tb * p.batch_total;
     } else if (path == TL_PATH_PANEL) {
-        plan_panel(&p);
+        plan_panel(&p, 0);
     } else if (path == TL_PATH_ROWS) {
         p.vec_bytes = 16;
         p.tiles = p.batch_total * (p.ext_a * eb / 16);

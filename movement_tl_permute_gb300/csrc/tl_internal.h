@@ -60,6 +60,12 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
               const int64_t* src_strides, const int64_t* dst_strides, int elem_bytes,
               uint32_t flags, int64_t src_bytes, int64_t dst_bytes, Plan* plan);
 
+// Tile shape and shared-memory layout of the panel path for tiles of about
+// tile_bytes (0: the default size; a tuning option may redo it).  Measured on
+// GB300: 32 KiB tiles for planes with two long extents, 16 KiB when one extent is
+// 16 or less.
+void plan_panel(Plan* p, int tile_bytes);
+
 // The bank simulator: worst conflict degree of one warp-wide access.
 int bank_degree(int n_lanes, const int64_t* lane_offsets, int elem_bytes, bool hardware);
 

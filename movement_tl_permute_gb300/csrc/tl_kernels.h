@@ -130,6 +130,7 @@ cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, c
 // axes, tiny extents.
 constexpr int kPanelThreads = 256;
 constexpr int kPanelStages = 3;
+constexpr int kPanelMaxSmem = 160 * 1024; // ring of 3 stages of <= 32 KiB tiles + row padding
 enum PanelMode : int32_t {
     kPanelRows = 0,    // row b copied as the 16-byte blocks covering it, at byte
                        // b * pitch; element a at byte (row address mod 16) + a * eb
@@ -149,9 +150,10 @@ struct PanelArgs {
     int32_t nb;                  // batch axes (innermost first)
     int32_t use32;               // tile indices fit in 32 bits
     int64_t tiles_a, tiles_b, tiles;
+    int64_t group_b;             // tile rows visited together (b fastest inside a group)
     int64_t bext[TL_MAX_DIMS], bss[TL_MAX_DIMS], bds[TL_MAX_DIMS];
     dev::DivU32 d_tb, d_nblk;    // divisors of the per-tile walks
-    dev::DivU32 d_item, d_tiles_b;
+    dev::DivU32 d_item, d_grp, d_gfull, d_glast;
     dev::DivU32 d_bext[TL_MAX_DIMS];
 };
 const void* panel_kernel(int eb);

@@ -4,6 +4,7 @@
 // device's SM count and occupancy, and launches one kernel on the caller's stream.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -109,6 +110,10 @@ int get_device_info(DevInfo* out) {
                             tile_smem_bytes(st, rows)) != cudaSuccess)
                         return TL_ERR_CUDA;
             }
+            if (cudaFuncSetAttribute(panel_kernel(1 << i),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kPanelMaxSmem) != cudaSuccess)
+                return TL_ERR_CUDA;
             // The cluster variant is optional: if its set-up fails it is sized
             // conservatively (one CTA per SM) and the error is cleared.
             for (int h = 0; h < 2; ++h) {
@@ -249,7 +254,7 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         break;
     case TL_PATH_PANEL:
         l.block = kPanelThreads;
-        l.smem = kPanelStages * p.panel_stage;
+        l.smem = kPanelStages * p.panel_stage;   // <= kPanelMaxSmem for tiles of <= 32 KiB
         if (sms) {
             int per_sm = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, panel_kernel(p.eb),
@@ -272,6 +277,13 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         break;
     }
     return l;
+}
+
+// The panel tile size is a tuning option: re-plan the panel layout for it.
+void apply_panel_tile(Plan& p, const tl_permute_opts* o) {
+    if (p.path != TL_PATH_PANEL || !o || o->panel_tile_kib < 4 || o->panel_tile_kib > 32) return;
+    plan_panel(&p, o->panel_tile_kib * 1024);
+    if (kPanelStages * p.panel_stage > kPanelMaxSmem) plan_panel(&p, 0);
 }
 
 // The tile path's tile height is a launch choice: re-count the tiles for it.
@@ -301,6 +313,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
     const int32_t max_ctas = opts ? opts->max_ctas : 0;
     const TileTuning tt = tile_tuning(opts);
     apply_tile_rows(p, tt);
+    apply_panel_tile(p, opts);
     const Launch l = launch_shape(p, &d, max_ctas, tt);
     // overlap this launch with the drain of the previous kernel in the stream
     const bool pdl = (flags & TL_FLAG_NO_PDL) == 0;
@@ -436,9 +449,16 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         }
         a.d_tb = dev::make_divu32((uint32_t)a.tb);
         a.use32 = p.tiles < (1LL << 32) ? 1 : 0;
+        // whole b extent by default (dst written front to back; measured best)
+        a.group_b = opts && opts->tile_group > 0 && opts->tile_group < a.tiles_b
+                        ? opts->tile_group
+                        : a.tiles_b;
         if (a.use32) {
+            const int64_t glast = a.tiles_b - ((a.tiles_b - 1) / a.group_b) * a.group_b;
             a.d_item = dev::make_divu32((uint32_t)(a.tiles_a * a.tiles_b));
-            a.d_tiles_b = dev::make_divu32((uint32_t)a.tiles_b);
+            a.d_grp = dev::make_divu32((uint32_t)(a.group_b * a.tiles_a));
+            a.d_gfull = dev::make_divu32((uint32_t)a.group_b);
+            a.d_glast = dev::make_divu32((uint32_t)glast);
             fill_divs(a.nb, a.bext, a.d_bext);
         }
         err = launch_panel(eb, a, l.grid, l.smem, st, pdl);
@@ -535,6 +555,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     }
     const TileTuning tt = tile_tuning(opts);
     apply_tile_rows(p, tt);
+    apply_panel_tile(p, opts);
     info.tile_rows = p.tile_rows;
     info.tile_cols = p.tile_cols;
     info.pitch = p.pitch;

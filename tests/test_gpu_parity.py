@@ -196,10 +196,11 @@ def _panel_cases(eb):
 
 
 @pytest.mark.parametrize("eb", WIDTHS)
-def test_panel_path(eb):
+@pytest.mark.parametrize("kib", [0, 4, 32])
+def test_panel_path(eb, kib):
     for i, (shape, ss, ds) in enumerate(_panel_cases(eb)):
-        check(shape, ss, ds, eb, "panel", seed=70 + i)
-        check(shape, ss, ds, eb, "panel", seed=80 + i, src_off=1, dst_off=3)
+        check(shape, ss, ds, eb, "panel", seed=70 + i, panel_tile_kib=kib)
+        check(shape, ss, ds, eb, "panel", seed=80 + i, src_off=1, dst_off=3, panel_tile_kib=kib)
 
 
 @pytest.mark.parametrize("eb", WIDTHS)

@@ -48,14 +48,16 @@ KERNEL_SOURCES = {
     "cluster": ["k_cluster.cu", "tile_common.cuh", "tl_device.cuh"],
     "rows": ["k_rows.cu", "tl_device.cuh"],
     "chunk": ["k_chunk.cu", "tl_device.cuh"],
+    "panel": ["k_panel.cu", "tl_device.cuh"],
     "warp": ["k_warp.cu", "tl_device.cuh"],
     "generic": ["k_generic.cu", "tl_device.cuh"],
 }
 KERNEL_NAMES = {"tile": "k_tile", "cluster": "k_cluster", "rows": "k_rows", "chunk": "k_chunk",
+                "panel": "k_panel",
                 "warp": "k_warp", "generic": "k_generic"}
 DTYPES = {"sf_transpose": "f32", "tile_transpose": "f16", "mx_sf": "u8", "attention": "bf16",
           "t2d_u8": "u8", "t2d_f16": "f16", "t2d_f32": "f32", "t2d_f64": "f64",
-          "t2d_v16": "16-byte"}
+          "t2d_v16": "16-byte", "t2d_odd_f32": "f32", "hwc_chw_u8": "u8", "nd6_f32": "f32"}
 
 
 # ---------------------------------------------------------------------------

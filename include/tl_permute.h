@@ -223,7 +223,9 @@ typedef struct tl_plan_info {
     int32_t smem_bytes;            /* dynamic shared memory per CTA */
     int32_t pitch;                 /* panel path: shared-memory bytes per tile row */
     int32_t panel_mode;            /* panel path: 0 rows of 16-byte blocks, 1 one run */
-    int32_t reserved[3];
+    int32_t panel_b1;              /* panel path: > 0 when the dst-contiguous axis (extent
+                                      panel_b1) and the next dst axis are walked as one */
+    int32_t reserved[2];
 } tl_plan_info;
 
 TL_API int tl_plan(const void *src, const void *dst, int ndim, const int64_t *shape,

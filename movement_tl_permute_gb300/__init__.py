@@ -73,7 +73,7 @@ class TlPlanInfo(ctypes.Structure):
                 ("vec_bytes", _i32), ("in_place", _i32), ("k", _i32), ("shift", _i32),
                 ("mask", _i32), ("tile_rows", _i32), ("tile_cols", _i32), ("tiles", _i64),
                 ("grid", _i32), ("block", _i32), ("smem_bytes", _i32), ("pitch", _i32),
-                ("panel_mode", _i32), ("reserved", _i32 * 3)]
+                ("panel_mode", _i32), ("panel_b1", _i32), ("reserved", _i32 * 2)]
 
 
 def library_path() -> str:
@@ -262,7 +262,8 @@ def tl_plan(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides, elem_by
                 vec_bytes=info.vec_bytes, in_place=bool(info.in_place), k=info.k,
                 shift=info.shift, mask=info.mask, tile_rows=info.tile_rows,
                 tile_cols=info.tile_cols, tiles=info.tiles, grid=info.grid, block=info.block,
-                smem_bytes=info.smem_bytes, pitch=info.pitch, panel_mode=info.panel_mode)
+                smem_bytes=info.smem_bytes, pitch=info.pitch, panel_mode=info.panel_mode,
+                panel_b1=info.panel_b1)
 
 
 def _bytes_after(t) -> int:

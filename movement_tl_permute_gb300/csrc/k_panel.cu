@@ -39,8 +39,23 @@ __device__ __forceinline__ void cp_async_wait() {
 
 struct PanelTile {
     int64_t so, dof;      // element offsets of the tile's (a0, b0) in src and dst
+    int64_t b0;           // first b of the tile
     uint32_t va, vb;      // valid elements of a and b
 };
+
+// src offset of b (elements); b is one axis of stride ss_b, or two merged axes
+__device__ __forceinline__ int64_t b_offset(int64_t b, const PanelArgs& a) {
+    if (!a.merged) return b * a.ss_b;
+    const uint32_t hi = dev::div_u32((uint32_t)b, a.d_b1);
+    return (int64_t)((uint32_t)b - hi * a.d_b1.d) * a.ss_b + (int64_t)hi * a.ss_b2;
+}
+
+// src offset of tile row bb relative to the tile's first row
+__device__ __forceinline__ int64_t row_offset(uint32_t bb, const PanelTile& ti,
+                                              const PanelArgs& a) {
+    if (!a.merged) return (int64_t)bb * a.ss_b;
+    return b_offset(ti.b0 + bb, a) - b_offset(ti.b0, a);
+}
 
 // tile t -> (column block of a, row block of b, batch item).  Tile rows are
 // visited in groups of group_b, b fastest inside a group: concurrently running
@@ -76,7 +91,8 @@ __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
     PanelTile r;
     r.va = (uint32_t)min((int64_t)a.ta, a.ext_a - a0);
     r.vb = (uint32_t)min((int64_t)a.tb, a.ext_b - b0);
-    r.so = a0 + b0 * a.ss_b;
+    r.b0 = b0;
+    r.so = a0 + b_offset(b0, a);
     r.dof = a0 * a.ds_a + b0;
     for (int i = 0; i < a.nb; ++i) {
         int64_t c;
@@ -105,7 +121,7 @@ __device__ __forceinline__ void issue(const PanelArgs& a, const PanelTile& ti, u
         for (uint32_t g = threadIdx.x; g < n; g += kPanelThreads) {
             const uint32_t b = dev::div_u32(g, a.d_nblk), k = g - b * nblk;
             if (b >= ti.vb) continue;
-            const uintptr_t row = base + (uintptr_t)((int64_t)b * a.ss_b * EB);
+            const uintptr_t row = base + (uintptr_t)(row_offset(b, ti, a) * EB);
             const uint32_t blocks = ((uint32_t)(row & 15) + ti.va * EB + 15) >> 4;
             if (k < blocks) cp_async16(sb + b * pitch + 16 * k, (row & ~uintptr_t(15)) + 16 * k);
         }
@@ -123,13 +139,14 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
     T* d = reinterpret_cast<T*>(a.dst) + ti.dof;
     const uint32_t ta = (uint32_t)a.ta, tb = (uint32_t)a.tb, pitch = (uint32_t)a.pitch;
     const uint32_t mis0 = (uint32_t)(reinterpret_cast<uintptr_t>(a.src + ti.so * EB) & 15);
-    const uint32_t ssb16 = (uint32_t)((a.ss_b * EB) & 15);
     const bool rows = a.mode == kPanelRows;
+    // byte offset of tile row b inside its first 16-byte block
+    auto mis = [&](uint32_t b) { return (mis0 + (uint32_t)(row_offset(b, ti, a) * EB)) & 15u; };
     if (kPanelThreads % tb == 0) {
         // each thread keeps one b and steps a by kPanelThreads / tb
         const uint32_t b = threadIdx.x % tb, de = kPanelThreads / tb;
         if (b >= ti.vb) return;
-        const uint8_t* sp = rows ? st + b * pitch + ((mis0 + b * ssb16) & 15) : st + mis0 + b * ta * EB;
+        const uint8_t* sp = rows ? st + b * pitch + mis(b) : st + mis0 + b * ta * EB;
         T* dp = d + b;
         const int64_t dstep = (int64_t)de * a.ds_a;
         uint32_t e = threadIdx.x / tb;
@@ -143,8 +160,7 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
     for (uint32_t f = threadIdx.x; f < n; f += kPanelThreads) {
         const uint32_t e = dev::div_u32(f, a.d_tb), b = f - e * tb;   // a, b in the tile
         if (e >= ti.va || b >= ti.vb) continue;
-        const uint32_t off = rows ? b * pitch + ((mis0 + b * ssb16) & 15) + e * EB
-                                  : mis0 + (b * ta + e) * EB;
+        const uint32_t off = rows ? b * pitch + mis(b) + e * EB : mis0 + (b * ta + e) * EB;
         d[(int64_t)e * a.ds_a + b] = *reinterpret_cast<const T*>(st + off);
     }
 }

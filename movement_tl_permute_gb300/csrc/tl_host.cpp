@@ -328,9 +328,18 @@ bool tile_ok(const Plan& p, int64_t src) {
 // that the panel kernel moves fewer idle bytes.
 bool tile_fits(const Plan& p) { return p.ext_b >= 64 && p.ext_a * p.eb >= 64; }
 
+// Extent of b once a short b takes in the next dst axis (see panel_merge_b).
+int64_t panel_b_extent(const Plan& p) {
+    if (p.ext_b >= 64) return p.ext_b;
+    for (int i = 0; i < p.batch.n; ++i)
+        if (p.batch.ds[i] == p.ext_b && p.ext_b * p.batch.ext[i] < (1LL << 31))
+            return p.ext_b * p.batch.ext[i];
+    return p.ext_b;
+}
+
 // Panel path: the plane needs one extent of at least 16 elements (else the
 // batch is the long dimension and the generic kernel walks it as well).
-bool panel_ok(const Plan& p) { return p.ext_a >= 16 || p.ext_b >= 16; }
+bool panel_ok(const Plan& p) { return p.ext_a >= 16 || panel_b_extent(p) >= 16; }
 
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
@@ -342,18 +351,31 @@ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 // first block, simulated for every residue r of the tile's base address.  A warp
 // covers 32 consecutive items.  The first pitch with the lowest summed degree wins.
 struct PanelMemo {
-    int ta, tb, eb, ssb16, pitch;
+    int ta, tb, eb, pitch;
+    int64_t ssb, b1, ssb2;
 };
 std::mutex g_panel_memo_mu;
 std::vector<PanelMemo> g_panel_memo;
 
 int panel_blocks_per_row(int64_t ta, int eb) { return (int)((ta * eb + 30) / 16); }
 
-int panel_pitch(int ta, int tb, int eb, int ssb16) {
+// src byte offset of b modulo 16: b is one axis (stride ss_b) or, when b1 > 0, two
+// merged axes (b % b1 with stride ss_b, b / b1 with stride ss_b2)
+int64_t b_mis16(int64_t b, int eb, int64_t ssb, int64_t b1, int64_t ssb2) {
+    const int64_t off = b1 > 0 ? (b % b1) * ssb + (b / b1) * ssb2 : b * ssb;
+    return (off * eb) & 15;
+}
+
+int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2) {
+    // the row misalignments repeat with a period of 16 rows (one axis) or are
+    // sampled over the tile's rows (merged axes); normalise the memo key
+    const int64_t ssb_k = b1 > 0 ? ssb : (ssb * eb) & 15;
     {
         std::lock_guard<std::mutex> lk(g_panel_memo_mu);
         for (const PanelMemo& e : g_panel_memo)
-            if (e.ta == ta && e.tb == tb && e.eb == eb && e.ssb16 == ssb16) return e.pitch;
+            if (e.ta == ta && e.tb == tb && e.eb == eb && e.ssb == ssb_k && e.b1 == b1 &&
+                e.ssb2 == ssb2)
+                return e.pitch;
     }
     const int64_t nblk = panel_blocks_per_row(ta, eb);
     const int64_t n_copy = nblk * tb, n_store = (int64_t)ta * tb;
@@ -376,7 +398,7 @@ int panel_pitch(int ta, int tb, int eb, int ssb16) {
                 int m = 0;
                 for (int64_t f = f0; f < f0 + 32 && f < n_store; ++f, ++m) {
                     const int64_t a = f / tb, b = f % tb;
-                    o[m] = (b * pitch + ((r + b * ssb16) & 15) + a * eb) / eb;
+                    o[m] = (b * pitch + ((r + b_mis16(b, eb, ssb, b1, ssb2)) & 15) + a * eb) / eb;
                 }
                 cost += bank_degree(m, o, eb, true);
             }
@@ -389,14 +411,37 @@ int panel_pitch(int ta, int tb, int eb, int ssb16) {
     }
     std::lock_guard<std::mutex> lk(g_panel_memo_mu);
     if (g_panel_memo.size() >= 64) g_panel_memo.erase(g_panel_memo.begin());
-    g_panel_memo.push_back({ta, tb, eb, ssb16, best});
+    g_panel_memo.push_back({ta, tb, eb, best, ssb_k, b1, ssb2});
     return best;
 }
 
 // Panel tile of about tile_bytes: a tiny extent is taken whole and the other one
-// fills the tile; otherwise 64 (eb <= 2) or 32 rows of b by the rest; no tile
-// side exceeds its extent.  Src rows packed back to back are copied as one run.
+// fills the tile; otherwise 64 (eb <= 2) or 32 rows of b by the rest of a, or more
+// rows when a runs out; no tile side exceeds its extent.  Src rows packed back to back are copied as one run.
 }  // namespace
+
+// A short b axis (under 64 elements) takes in the next dst axis when dst is dense
+// across the two (that axis's dst stride equals the b extent): the tile's dst runs
+// and its row count grow, its src rows stay contiguous.
+void panel_merge_b(Plan* p) {
+    if (p->ext_b >= 64) return;
+    for (int i = 0; i < p->batch.n; ++i) {
+        if (p->batch.ds[i] != p->ext_b) continue;
+        const int64_t merged = p->ext_b * p->batch.ext[i];
+        if (merged >= (1LL << 31)) return;     // same rule as panel_b_extent
+        p->panel_b1 = p->ext_b;
+        p->panel_ss_b2 = p->batch.ss[i];
+        p->ext_b = merged;
+        p->batch_total /= p->batch.ext[i];
+        for (int j = i; j + 1 < p->batch.n; ++j) {
+            p->batch.ext[j] = p->batch.ext[j + 1];
+            p->batch.ss[j] = p->batch.ss[j + 1];
+            p->batch.ds[j] = p->batch.ds[j + 1];
+        }
+        --p->batch.n;
+        return;
+    }
+}
 
 void plan_panel(Plan* p, int tile_bytes) {
     const int eb = p->eb;
@@ -413,20 +458,34 @@ void plan_panel(Plan* p, int tile_bytes) {
     } else {
         tb = std::min<int64_t>(eb <= 2 ? 64 : 32, p->ext_b);
         ta = std::min(E / tb, p->ext_a);
+        if (ta * tb < E)            // a short a extent: the tile grows along b instead
+            tb = std::min(round_up((E + ta - 1) / ta, 32), p->ext_b);
     }
-    p->tile_cols = (int)ta;
-    p->tile_rows = (int)tb;
     int64_t stage;
-    if (ta == p->ext_a && p->ss_b == ta) {
-        p->panel_mode = 1;
-        p->pitch = 0;
-        p->panel_nblk = 0;
-        stage = 16 * ((ta * tb * eb + 30) / 16);
-    } else {
-        p->panel_mode = 0;
-        p->panel_nblk = panel_blocks_per_row(ta, eb);
-        p->pitch = panel_pitch((int)ta, (int)tb, eb, (int)((p->ss_b * eb) & 15));
-        stage = tb * p->pitch;
+    for (;;) {
+        p->tile_cols = (int)ta;
+        p->tile_rows = (int)tb;
+        // src rows packed back to back over the whole b range (merged axes too)
+        const bool packed = ta == p->ext_a && p->ss_b == ta &&
+                            (p->panel_b1 == 0 || p->panel_ss_b2 == p->panel_b1 * ta);
+        if (packed) {
+            p->panel_mode = 1;
+            p->pitch = 0;
+            p->panel_nblk = 0;
+            stage = 16 * ((ta * tb * eb + 30) / 16);
+        } else {
+            p->panel_mode = 0;
+            p->panel_nblk = panel_blocks_per_row(ta, eb);
+            // rows of 1..2 blocks cost up to 32 bytes each: check the ring before the
+            // pitch search
+            stage = tb * 16 * (p->panel_nblk + 7);
+            if (kPanelStages * stage <= kPanelMaxSmem) {
+                p->pitch = panel_pitch((int)ta, (int)tb, eb, p->ss_b, p->panel_b1, p->panel_ss_b2);
+                stage = tb * p->pitch;
+            }
+        }
+        if (kPanelStages * stage <= kPanelMaxSmem || (ta <= 1 && tb <= 1)) break;
+        if (tb >= ta) tb = (tb + 1) / 2; else ta = (ta + 1) / 2;   // halve the longer side
     }
     p->panel_stage = (int)stage;
     const int64_t na = (p->ext_a + ta - 1) / ta, nb = (p->ext_b + tb - 1) / tb;
@@ -568,6 +627,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         const int64_t tb = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
         p.tiles = ta * tb * p.batch_total;
     } else if (path == TL_PATH_PANEL) {
+        panel_merge_b(&p);
         plan_panel(&p, 0);
     } else if (path == TL_PATH_ROWS) {
         p.vec_bytes = 16;

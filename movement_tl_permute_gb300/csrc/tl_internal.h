@@ -46,6 +46,8 @@ struct Plan {
     int panel_mode = 0;                 // PANEL: PanelMode (block rows, one block run)
     int panel_nblk = 0;                 // PANEL: 16-byte blocks copied per row (at most)
     int panel_stage = 0;                // PANEL: shared-memory bytes of one ring stage
+    int64_t panel_b1 = 0;               // PANEL: inner extent of b when two axes are merged
+    int64_t panel_ss_b2 = 0;            // PANEL: src stride of the outer merged axis
     int64_t tiles = 0;
 
     // WARP: tile (innermost suffix of `kept`) + batch of the outer `kept` axes.
@@ -59,6 +61,11 @@ struct Plan {
 int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
               const int64_t* src_strides, const int64_t* dst_strides, int elem_bytes,
               uint32_t flags, int64_t src_bytes, int64_t dst_bytes, Plan* plan);
+
+// Panel ring: stages per CTA and the dynamic shared memory the kernels are set up
+// for; plan_panel shrinks a tile until its ring fits.
+constexpr int kPanelStages = 3;
+constexpr int kPanelMaxSmem = 160 * 1024;
 
 // Tile shape and shared-memory layout of the panel path for tiles of about
 // tile_bytes (0: the default size; a tuning option may redo it).  Measured on

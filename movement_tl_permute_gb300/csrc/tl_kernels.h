@@ -8,6 +8,7 @@
 
 #include "../../include/tl_permute.h"
 #include "tl_device.cuh"
+#include "tl_internal.h"
 
 #include <utility>
 
@@ -129,8 +130,6 @@ cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, c
 // a ring of stages, then stored in dst order; any element alignment, up to 6 batch
 // axes, tiny extents.
 constexpr int kPanelThreads = 256;
-constexpr int kPanelStages = 3;
-constexpr int kPanelMaxSmem = 160 * 1024; // ring of 3 stages of <= 32 KiB tiles + row padding
 enum PanelMode : int32_t {
     kPanelRows = 0,    // row b copied as the 16-byte blocks covering it, at byte
                        // b * pitch; element a at byte (row address mod 16) + a * eb
@@ -142,6 +141,9 @@ struct PanelArgs {
     uint8_t* dst;
     int64_t ext_a, ext_b;        // plane: a src-contiguous, b dst-contiguous
     int64_t ss_b, ds_a;          // src stride of b, dst stride of a (elements)
+    // b may be two axes merged because dst is dense across them: b = hi * b1 + lo,
+    // src offset lo * ss_b + hi * ss_b2 (b1 >= ext_b when nothing is merged)
+    int64_t b1, ss_b2;
     int32_t ta, tb;              // tile: ta elements of a x tb elements of b
     int32_t pitch;               // kPanelRows: shared-memory bytes per row (multiple of 16)
     int32_t mode;                // PanelMode
@@ -153,6 +155,9 @@ struct PanelArgs {
     int64_t group_b;             // tile rows visited together (b fastest inside a group)
     int64_t bext[TL_MAX_DIMS], bss[TL_MAX_DIMS], bds[TL_MAX_DIMS];
     dev::DivU32 d_tb, d_nblk;    // divisors of the per-tile walks
+    dev::DivU32 d_b1;            // b -> (hi, lo) when two axes are merged (b fits 32 bits)
+    int32_t merged;              // 1 when b is two merged axes
+    int32_t pad;
     dev::DivU32 d_item, d_grp, d_gfull, d_glast;
     dev::DivU32 d_bext[TL_MAX_DIMS];
 };

@@ -436,6 +436,10 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.pitch = p.pitch;
         a.mode = p.panel_mode;
         a.nblk = p.panel_nblk;
+        a.merged = p.panel_b1 > 0 ? 1 : 0;
+        a.b1 = a.merged ? p.panel_b1 : p.ext_b;
+        a.ss_b2 = p.panel_ss_b2;
+        a.d_b1 = dev::make_divu32((uint32_t)a.b1);
         a.stage_bytes = p.panel_stage;
         a.d_nblk = dev::make_divu32((uint32_t)(p.panel_nblk > 0 ? p.panel_nblk : 1));
         a.tiles_a = (p.ext_a + a.ta - 1) / a.ta;
@@ -560,6 +564,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     info.tile_cols = p.tile_cols;
     info.pitch = p.pitch;
     info.panel_mode = p.panel_mode;
+    info.panel_b1 = (int32_t)p.panel_b1;
     info.tiles = p.tiles;
     int ndev = 0;
     DevInfo d;

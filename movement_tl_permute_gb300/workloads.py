@@ -25,6 +25,17 @@ grown to sizes that exercise HBM:
 ``t2d_u8`` ...     2-D row-major -> column-major transposes of ~1 GiB for each
                    element width 1, 2, 4, 8, 16 bytes; random bits.
 =================  =========================================================
+
+Three more describe general permutes whose layouts a TMA tensor map cannot take
+(the ``B.permute`` case of "Buffers and memory", "Buffer APIs"):
+
+=================  =========================================================
+``t2d_odd_f32``    float32 16383 x 16385 row-major -> column-major: row pitches
+                   that are not multiples of 16 bytes (1 GiB).
+``hwc_chw_u8``     uint8 image 8192 x 8192 x 3 channels (HWC) -> 3 planes (CHW).
+``nd6_f32``        float32 (16,16,16,16,64,64) permuted (5,3,1,4,2,0): four
+                   batch axes around the transposed plane (1 GiB).
+=================  =========================================================
 """
 from __future__ import annotations
 
@@ -68,6 +79,38 @@ def _t2d(name, eb, rows, cols, seed):
                     "%d-byte %dx%d row-major -> column-major" % (eb, rows, cols), ("t2d",))
 
 
+def _rm(shape):
+    st, acc = [], 1
+    for e in reversed(shape):
+        st.append(acc)
+        acc *= e
+    return tuple(reversed(st))
+
+
+def _perm_dst(shape, perm):
+    # dst holds the axes in the order `perm`, row-major: stride of source axis perm[i]
+    pst = _rm(tuple(shape[p] for p in perm))
+    ds = [0] * len(shape)
+    for i, p in enumerate(perm):
+        ds[p] = pst[i]
+    return tuple(ds)
+
+
+def _hwc_chw(h, w=8192, c=3):
+    # (H, W, C) interleaved -> C planes of H x W
+    return Workload("hwc_chw_u8", 1, (h, w, c), (w * c, c, 1), (w, 1, h * w), h * w * c,
+                    h * w * c, 56, "bits",
+                    "uint8 %dx%dx%d interleaved channels -> %d planes" % (h, w, c, c),
+                    ("general",))
+
+
+def _nd6(lead):
+    shape = (lead, 16, 16, 16, 64, 64)
+    n = lead * 16 * 16 * 16 * 64 * 64
+    return Workload("nd6_f32", 4, shape, _rm(shape), _perm_dst(shape, (5, 3, 1, 4, 2, 0)), n, n,
+                    57, "bits", "float32 %s permuted (5,3,1,4,2,0)" % (shape,), ("general",))
+
+
 WORKLOADS = {
     w.name: w for w in [
         Workload("sf_transpose", 4, (2, 1, 4, 32), (128, 128, 32, 1), (128, 128, 1, 4),
@@ -87,6 +130,9 @@ WORKLOADS = {
         _t2d("t2d_f32", 4, 16384, 16384, 52),
         _t2d("t2d_f64", 8, 8192, 16384, 53),
         _t2d("t2d_v16", 16, 8192, 8192, 54),
+        _t2d("t2d_odd_f32", 4, 16383, 16385, 55),
+        _hwc_chw(8192),
+        _nd6(16),
     ]
 }
 
@@ -105,6 +151,10 @@ def scaled(w: Workload, leading: int) -> Workload:
     if "t2d" in w.tags:
         rows, cols = leading, w.shape[1]
         return _t2d(w.name, w.elem_bytes, rows, cols, w.seed)
+    if w.name == "hwc_chw_u8":          # dst plane size follows the leading extent
+        return _hwc_chw(leading, w.shape[1], w.shape[2])
+    if w.name == "nd6_f32":             # the leading axis is innermost in dst
+        return _nd6(leading)
     ratio_src = w.src_elems // w.shape[0]
     ratio_dst = w.dst_elems // w.shape[0]
     return Workload(w.name, w.elem_bytes, (leading,) + tuple(w.shape[1:]), w.src_strides,

@@ -192,6 +192,12 @@ def _panel_cases(eb):
     out.append((shape, ss, ds))
     ss2 = tuple(x * 2 for x in ss[:-1]) + (1,)
     out.append((shape, ss2, ds))
+    # a short dst-contiguous axis walked together with the next dst axis; tile rows
+    # cross the boundary between the two (7 and 5 do not divide the tile)
+    for shape, perm in (((7, 5, 300), (2, 1, 0)), ((4,) * 7, (6, 5, 4, 3, 2, 1, 0)),
+                        ((3, 9, 11, 130), (3, 2, 1, 0))):
+        ss, ds = perm_layouts(shape, perm)
+        out.append((shape, ss, ds))
     return out
 
 
@@ -321,10 +327,10 @@ def test_cluster_handoff_timeout_is_reported_and_context_survives():
 
 
 # ---------------------------------------------------------------------------
-# the five workloads at full size, in the launch configuration the bench times
+# every bench workload at full size, in the launch configuration the bench times
 # ---------------------------------------------------------------------------
 FULL = ["sf_transpose", "tile_transpose", "mx_sf", "attention", "t2d_u8", "t2d_f16", "t2d_f32",
-        "t2d_f64", "t2d_v16"]
+        "t2d_f64", "t2d_v16", "t2d_odd_f32", "hwc_chw_u8", "nd6_f32"]
 
 
 def _full(name, path="auto"):

@@ -224,12 +224,13 @@ PANEL_LAYOUTS = [
 ]
 
 
-def _panel_degrees(ta, tb, eb, pitch, ssb):
+def _panel_degrees(ta, tb, eb, pitch, row_off):
     """Per-warp bank-conflict degrees (oracle model, hardware mode) of the panel
     kernel's two walks for a block-row layout of byte pitch `pitch`: the copy walk
     (16-byte blocks, row b at b * pitch) and the store walk (tile element f at
-    a = f // tb, b = f % tb, row b starting (r + b * ss_b * eb) mod 16 bytes into
-    its first block, for every base residue r)."""
+    a = f // tb, b = f % tb, row b starting (r + row_off(b) * eb) mod 16 bytes into
+    its first block, for every base residue r; row_off(b) is the src element offset
+    of row b)."""
     nblk = (ta * eb + 30) // 16
     q = pitch // 16
     copy = [L.bank_conflict_degree([(g // nblk) * q + g % nblk
@@ -238,7 +239,7 @@ def _panel_degrees(ta, tb, eb, pitch, ssb):
     store = []
     for r in range(0, 16, eb):
         for f0 in range(0, ta * tb, 32):
-            offs = [((f % tb) * pitch + ((r + (f % tb) * ssb * eb) & 15) + (f // tb) * eb) // eb
+            offs = [((f % tb) * pitch + ((r + row_off(f % tb) * eb) & 15) + (f // tb) * eb) // eb
                     for f in range(f0, min(ta * tb, f0 + 32))]
             store.append(L.bank_conflict_degree(offs, eb, "hardware"))
     return copy, store
@@ -257,13 +258,19 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
     assert p["path"] == "panel"
     ta, tb, pitch, mode = p["tile_cols"], p["tile_rows"], p["pitch"], p["panel_mode"]
     ssb = [x for x, d in zip(p["src_str"], p["dst_str"]) if d == 1][0]
+    b1 = p["panel_b1"]
+    if b1:      # b walks the dst-contiguous axis and the next dst axis (stride b1) as one
+        ssb2 = [x for x, d in zip(p["src_str"], p["dst_str"]) if d == b1][0]
+        row_off = lambda b: (b % b1) * ssb + (b // b1) * ssb2
+    else:
+        row_off = lambda b: b * ssb
     n = ta * tb
     if mode == 0:
         nblk = (ta * eb + 30) // 16
         assert pitch % 16 == 0 and 16 * nblk <= pitch < 16 * (nblk + 8)
         assert p["smem_bytes"] == 3 * tb * pitch
-        copy, store = _panel_degrees(ta, tb, eb, pitch, ssb)
-        copy0, store0 = _panel_degrees(ta, tb, eb, 16 * nblk, ssb)
+        copy, store = _panel_degrees(ta, tb, eb, pitch, row_off)
+        copy0, store0 = _panel_degrees(ta, tb, eb, 16 * nblk, row_off)
         assert sum(copy) + sum(store) <= sum(copy0) + sum(store0)
         assert max(copy) <= 2 and max(store) <= 4
     else:

@@ -320,13 +320,18 @@ def cpu_baseline(w, src, dst, budget_s=10.0):
 # ---------------------------------------------------------------------------
 # arms
 # ---------------------------------------------------------------------------
+L2_BYTES = 129 * 1000 * 1000
+
+
 def config_of(w, plan):
     return {"workload": "%s: %s" % (w.name, w.description), "shape": list(w.shape),
             "src_strides": list(w.src_strides), "dst_strides": list(w.dst_strides),
             "elem_bytes": w.elem_bytes, "bytes_per_step": w.algorithmic_bytes,
             "path": plan["path"] if plan else None,
             "grid": plan["grid"] if plan else None, "block": plan["block"] if plan else None,
-            "l2": "inputs larger than L2 (129 MB): no flush between steps",
+            "l2": ("inputs larger than L2 (129 MB): no flush between steps"
+                   if w.src_elems * w.elem_bytes > L2_BYTES else
+                   "L2-resident working set: a latency measurement, not an HBM one"),
             "seed": w.seed}
 
 
@@ -413,6 +418,20 @@ def run_ours(args, w):
         step()
     torch.cuda.synchronize(dev)
 
+    use_graph = args.launch == "graph" or (args.launch == "auto" and "small" in w.tags)
+    graph = None
+    if use_graph:
+        # the K timed steps captured once; the replay launches every kernel again
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream(dev).cuda_stream
+            for _ in range(args.steps):
+                tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), *args_call, cap,
+                                 path=args.path)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+
     # ------------------------------------------------ device-resident timing
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
@@ -420,13 +439,17 @@ def run_ours(args, w):
     launches0 = tl.tl_launch_count()
     t_wall0 = time.time()
     e0.record(stream)
-    for _ in range(args.steps):
-        step()
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(args.steps):
+            step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.time()
     barrier()
-    launches = tl.tl_launch_count() - launches0
+    # a replayed graph launches the captured kernels without host calls
+    launches = args.steps if graph is not None else tl.tl_launch_count() - launches0
     ms_local = e0.elapsed_time(e1)
     ms_max = reduce_max(ms_local, dev if world > 1 else None)
 
@@ -491,7 +514,8 @@ def run_ours(args, w):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPES.get(w.name, "bits"),
-        "data": "synthetic", "config": config_of(w, plan),
+        "data": "synthetic",
+        "config": dict(config_of(w, plan), launch="cuda_graph" if graph is not None else "stream"),
         "pct_hbm_peak": round(100.0 * value / world / peak, 2),
         "parity": {"bit_exact": parity,
                    "checked": "GPU output vs oracle on the cpu_baseline sample"},
@@ -520,12 +544,17 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--path", default="auto",
-                    choices=["auto", "generic", "chunk", "tile", "warp", "rows", "cluster"],
+                    choices=["auto", "generic", "chunk", "tile", "warp", "rows", "cluster",
+                             "panel"],
                     help="force a kernel path (default: the planner's choice)")
     ap.add_argument("--leading", type=int, default=0,
                     help="override the outermost extent (smaller cases for profiling)")
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the CPU baseline")
+    ap.add_argument("--launch", choices=["auto", "stream", "graph"], default="auto",
+                    help="timed steps as stream launches, or replayed from one CUDA graph that "
+                         "holds all of them (auto: graph for the one-warp workload, whose "
+                         "step is shorter than a host-side launch)"),
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -335,6 +335,12 @@ def test_cluster_ring_options():
     assert _plan(w, path="cluster", cluster_consumer_warps=5)["block"] == 7 * 32
 
 
+def test_smoke_cases_take_the_paths_they_name():
+    import __graft_entry__ as g
+    for name, shape, ss, ds, eb, path in g.SMOKE_CASES:
+        assert tl.tl_plan(SRC, DST, shape, ss, ds, eb)["path"] == path, name
+
+
 def test_forced_paths_that_do_not_apply():
     w = workloads.get("attention")
     for path in ("tile", "rows", "cluster", "panel"):

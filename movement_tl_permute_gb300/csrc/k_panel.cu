@@ -142,6 +142,64 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
     const bool rows = a.mode == kPanelRows;
     // byte offset of tile row b inside its first 16-byte block
     auto mis = [&](uint32_t b) { return (mis0 + (uint32_t)(row_offset(b, ti, a) * EB)) & 15u; };
+    if constexpr (EB < 4) {
+        if (!rows) {
+            // Packed src rows (a short a axis, such as interleaved channels): each dst
+            // row a gets its run of b in 4-byte words, a lane packing 4 / EB elements
+            // that sit ta elements apart in the stage (lanes 4 * ta bytes apart: odd
+            // or small word strides, so the byte reads spread over the banks).  The
+            // elements before the first 4-byte boundary of the row and after the last
+            // one are stored singly.
+            constexpr uint32_t V = 4 / EB;
+            auto elem = [&](uint32_t b, uint32_t e) {
+                return *reinterpret_cast<const T*>(st + mis0 + (b * ta + e) * EB);
+            };
+            for (uint32_t e = 0; e < ti.va; ++e) {
+                T* drow = d + (int64_t)e * a.ds_a;
+                const uint32_t lead = (uint32_t)((4 - (reinterpret_cast<uintptr_t>(drow) & 3)) & 3);
+                const uint32_t head = min(ti.vb, lead / EB);
+                const uint32_t nw = (ti.vb - head) / V, tail = head + nw * V;
+                if (threadIdx.x < head) drow[threadIdx.x] = elem(threadIdx.x, e);
+                if (tail + threadIdx.x < ti.vb) drow[tail + threadIdx.x] = elem(tail + threadIdx.x, e);
+                uint32_t* wrow = reinterpret_cast<uint32_t*>(drow + head);
+                for (uint32_t w = threadIdx.x; w < nw; w += kPanelThreads) {
+                    uint32_t word = 0;
+#pragma unroll
+                    for (uint32_t k = 0; k < V; ++k)
+                        word |= (uint32_t)elem(head + w * V + k, e) << (8 * EB * k);
+                    wrow[w] = word;
+                }
+            }
+            return;
+        }
+        if (tb <= 16 && a.ds_a == (int64_t)tb && tb == a.ext_b && !a.merged) {
+            // A short b axis packed in dst (planes -> interleaved channels): the tile's
+            // dst is one run of va * tb elements, stored as 4-byte words; element f of
+            // the run is (a, b) = (f / tb, f % tb).
+            constexpr uint32_t V = 4 / EB;
+            const uint32_t ssb16 = (uint32_t)((a.ss_b * EB) & 15);
+            auto elem = [&](uint32_t f) {
+                const uint32_t e = dev::div_u32(f, a.d_tb), b = f - e * tb;
+                return *reinterpret_cast<const T*>(st + b * pitch + ((mis0 + b * ssb16) & 15) +
+                                                   e * EB);
+            };
+            const uint32_t n = ti.va * tb;
+            const uint32_t lead = (uint32_t)((4 - (reinterpret_cast<uintptr_t>(d) & 3)) & 3);
+            const uint32_t head = min(n, lead / EB);
+            const uint32_t nw = (n - head) / V, tail = head + nw * V;
+            if (threadIdx.x < head) d[threadIdx.x] = elem(threadIdx.x);
+            if (tail + threadIdx.x < n) d[tail + threadIdx.x] = elem(tail + threadIdx.x);
+            uint32_t* wrun = reinterpret_cast<uint32_t*>(d + head);
+            for (uint32_t w = threadIdx.x; w < nw; w += kPanelThreads) {
+                uint32_t word = 0;
+#pragma unroll
+                for (uint32_t k = 0; k < V; ++k)
+                    word |= (uint32_t)elem(head + w * V + k) << (8 * EB * k);
+                wrun[w] = word;
+            }
+            return;
+        }
+    }
     if (kPanelThreads % tb == 0) {
         // each thread keeps one b and steps a by kPanelThreads / tb
         const uint32_t b = threadIdx.x % tb, de = kPanelThreads / tb;

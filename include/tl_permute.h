@@ -147,8 +147,9 @@ TL_API int tl_bank_conflicts(int n_lanes, const int64_t *lane_offsets, int elem_
  * ranges must be disjoint, except for the in-place case of the warp path
  * (identical pointers and per-tile footprints), where every tile is read in
  * full before it is written.  Kernels are chosen by the planner (generic
- * strided, contiguous-chunk copy, TMA-staged tile transpose, small-row register
- * transpose, warp XOR-swizzle transpose).
+ * strided, contiguous-chunk copy, TMA-staged tile transpose, cp.async-staged panel
+ * transpose for planes TMA cannot describe, small-row register transpose, warp
+ * XOR-swizzle transpose).
  */
 TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape,
                const int64_t *src_strides, const int64_t *dst_strides, int elem_bytes,
@@ -162,8 +163,9 @@ TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape
 #define TL_PATH_WARP 4u     /* warp register-staged XOR-swizzle transpose (in-place safe) */
 #define TL_PATH_ROWS 5u     /* short dst runs (<= 16 B): 16 B row loads, register transpose */
 #define TL_PATH_CLUSTER 6u  /* TILE with a 2-CTA cluster handing tiles over through DSMEM */
-#define TL_PATH_PANEL 7u    /* plane transpose through padded smem, plain loads/stores: any
-                               element alignment, up to 6 batch axes, tiny extents */
+#define TL_PATH_PANEL 7u    /* plane transpose staged in smem by cp.async of the 16-byte
+                               blocks covering each src row: any element alignment, up
+                               to 6 batch axes, tiny extents */
 #define TL_PATH_MASK 0xFu
 /* Test hook for the cluster path: the producer CTA skips its DSMEM hand-off, so the
  * consumer's bounded wait must expire and report TL_ERR_TIMEOUT in dev_status. */
@@ -182,7 +184,8 @@ typedef struct tl_permute_opts {
                              library; the caller zeroes it).  NULL = not reported. */
     int64_t src_bytes;    /* > 0: bytes addressable from src; the layout must fit */
     int64_t dst_bytes;    /* > 0: bytes addressable from dst */
-    /* Tuning of the tile path; 0 selects the planner's default for each. */
+    /* Tuning of the tile, cluster and panel paths; 0 selects the planner's default
+     * for each, as do values outside the ranges given. */
     int32_t tile_group;   /* tile rows visited together (tile and panel visit order;
                              default: the whole extent) */
     int32_t tile_stages;  /* shared-memory ring depth: 2..12 (tile, 128-row tiles),
@@ -217,7 +220,8 @@ typedef struct tl_plan_info {
     int32_t vec_bytes;             /* vector width of global accesses */
     int32_t in_place;              /* 1 when src == dst and the warp path runs in place */
     int32_t k, shift, mask;        /* warp path swizzle (else 0) */
-    int32_t tile_rows, tile_cols;  /* tile path: rows (b) x columns (a) per tile */
+    int32_t tile_rows, tile_cols;  /* tile/panel path: rows (b) x columns (a) per tile,
+                                      in elements */
     int64_t tiles;                 /* work units (tiles, rows, warps...) */
     int32_t grid, block;           /* launch shape (0 without a device) */
     int32_t smem_bytes;            /* dynamic shared memory per CTA */

@@ -46,6 +46,27 @@ def test_library_loads_and_exports_every_declared_symbol():
     assert "alias" in tl.tl_status_string(-7) or "overlap" in tl.tl_status_string(-7)
 
 
+def test_plain_c_client(tmp_path):
+    """A C99 program that includes only the public header and links only the
+    library (tests/c/abi_client.c) runs the host entry points on the pages'
+    worked examples."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    libdir = os.path.dirname(os.path.abspath(tl.load()._name))
+    exe = str(tmp_path / "abi_client")
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(root, "include"), os.path.join(here, "c", "abi_client.c"),
+                    "-L", libdir, "-ltl_permute", "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "0 failure(s)" in r.stdout
+
+
 # ---------------------------------------------------------------------------
 # canonicalisation vs the oracle reference
 # ---------------------------------------------------------------------------

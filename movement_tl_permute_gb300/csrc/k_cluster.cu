@@ -131,7 +131,11 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                 report(a.status, TL_ERR_TIMEOUT);
                 break;
             }
-            mbar_arrive_remote(map_to_rank(smem_addr(&staged[it % SS]), peer));
+            // CTA-scope release: the push's reads of the peer's slot are complete
+            // (they completed this barrier, which the acquire above observed), and a
+            // cluster-scope release here cost ~2 us per tile before the peer's loader
+            // saw the arrive (per-tile timestamp trace on GB300)
+            mbar_arrive_remote_slot(map_to_rank(smem_addr(&staged[it % SS]), peer));
         }
     } else if (warp < NCW) {
         // --------------------------------- consumers --------------------------------

@@ -43,13 +43,25 @@ struct TileTuning {
     int ctas_per_sm = 0;    // resident CTAs the grid is sized for (0 = path default)
     int promotion = 256;    // L2 fill size of the TMA loads (0 = none)
     int cluster_stages = 2; // staging ring depth of the cluster variant
-    int cluster_recv = 1;   // its receive ring depth
+    int cluster_recv = 0;   // its receive ring depth (0 = by layout, cluster_defaults)
     int cluster_warps = 4;  // its consumer warps (8 or 4)
-    // The cluster variant is bound by the latency of each pair's hand-off chain
-    // (HBM load, DSMEM push, slot hand-backs), so it runs as many small CTAs as fit:
-    // measured on GB300, 4 consumer warps with a 2-deep staging ring and one receive
-    // slot (4 CTAs per SM) beat 8 warps and deeper rings on every workload.
+    int cluster_ctas = 0;   // its CTAs per SM (0 = by layout; tile_ctas_per_sm overrides)
 };
+
+// The cluster variant, with its slot hand-backs released at CTA scope, is paced by
+// the loads it keeps in flight GPU-wide, like the single-CTA kernel (throughput
+// falls off a cliff past about 600-700 strided tiles).  Measured on GB300 with 4
+// consumer warps and a 2-deep staging ring: tiles that are one contiguous 16 KiB
+// run of src (the batched tile transpose) do best with 2 receive slots at 3 CTAs
+// per SM (about 900 tiles in flight, 6.72 TB/s); strided tiles (2-D transposes)
+// with 1 receive slot at 2 CTAs per SM (about 600, 5.8-6.1 TB/s).
+void cluster_defaults(const Plan& p, TileTuning& t) {
+    const bool contiguous = p.ext_a * p.eb == 128 && p.ss_b * p.eb == 128;
+    if (t.cluster_recv == 0) t.cluster_recv = contiguous ? 2 : 1;
+    if (t.cluster_stages + t.cluster_recv > kMaxClusterSlots)
+        t.cluster_recv = kMaxClusterSlots - t.cluster_stages;
+    if (t.cluster_ctas == 0) t.cluster_ctas = contiguous ? 0 : 2;
+}
 
 TileTuning tile_tuning(const tl_permute_opts* o) {
     TileTuning t;
@@ -62,8 +74,6 @@ TileTuning tile_tuning(const tl_permute_opts* o) {
         t.cluster_recv = o->cluster_recv_stages;
     if (o->cluster_consumer_warps == 4 || o->cluster_consumer_warps == 8)
         t.cluster_warps = o->cluster_consumer_warps;
-    if (t.cluster_stages + t.cluster_recv > kMaxClusterSlots)
-        t.cluster_recv = kMaxClusterSlots - t.cluster_stages;
     if (o->tile_ctas_per_sm > 0) t.ctas_per_sm = o->tile_ctas_per_sm;
     if (o->tile_rows == 256) t.rows = 256;
     const int max_stages = kTileRingBytes / (t.rows * 128);
@@ -246,7 +256,8 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
             // as many clusters as fit
             int per_sm = d->cluster_occ[log2i(p.eb)][tt.cluster_warps == 4 ? 1 : 0]
                                        [tt.cluster_stages + tt.cluster_recv];
-            if (tt.ctas_per_sm > 0 && tt.ctas_per_sm < per_sm) per_sm = tt.ctas_per_sm;
+            const int want = tt.ctas_per_sm > 0 ? tt.ctas_per_sm : tt.cluster_ctas;
+            if (want > 0 && want < per_sm) per_sm = want;
             int64_t cap = sms * (per_sm < 1 ? 1 : per_sm) / 2;
             if (cap < 1) cap = 1;
             l.grid = 2 * cap_grid(p.tiles, cap, max_ctas > 0 ? (max_ctas + 1) / 2 : 0);
@@ -311,7 +322,8 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
     rc = get_device_info(&d);
     if (rc != TL_OK) return rc;
     const int32_t max_ctas = opts ? opts->max_ctas : 0;
-    const TileTuning tt = tile_tuning(opts);
+    TileTuning tt = tile_tuning(opts);
+    cluster_defaults(p, tt);
     apply_tile_rows(p, tt);
     apply_panel_tile(p, opts);
     const Launch l = launch_shape(p, &d, max_ctas, tt);
@@ -557,7 +569,8 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         info.shift = p.shift;
         info.mask = p.mask;
     }
-    const TileTuning tt = tile_tuning(opts);
+    TileTuning tt = tile_tuning(opts);
+    cluster_defaults(p, tt);
     apply_tile_rows(p, tt);
     apply_panel_tile(p, opts);
     info.tile_rows = p.tile_rows;

@@ -343,7 +343,9 @@ def test_tile_height_option():
 def test_cluster_ring_options():
     w = workloads.get("tile_transpose")
     slot = 128 * 128
-    assert _plan(w, path="cluster")["smem_bytes"] == 3 * slot + 1024          # 2 + 1
+    # contiguous 16 KiB tiles: 2 staging + 2 receive slots; strided tiles: 2 + 1
+    assert _plan(w, path="cluster")["smem_bytes"] == 4 * slot + 1024
+    assert _plan(workloads.get("t2d_f32"), path="cluster")["smem_bytes"] == 3 * slot + 1024
     assert _plan(w, path="cluster", tile_stages=3, cluster_recv_stages=1)["smem_bytes"] == \
         4 * slot + 1024
     assert _plan(w, path="cluster", tile_stages=1, cluster_recv_stages=1)["smem_bytes"] == \

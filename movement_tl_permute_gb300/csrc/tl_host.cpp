@@ -607,6 +607,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         p.row_elems = row;
         p.outer = o;
         p.rows = total / row;
+        p.tiles = p.rows;                  // work units: rows
         int vb = 16;
         auto fits = [&](int64_t v) { return v % vb == 0; };
         while (vb > 1) {

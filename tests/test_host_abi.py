@@ -358,6 +358,44 @@ def test_cluster_ring_options():
     assert _plan(w, path="cluster", cluster_consumer_warps=5)["block"] == 7 * 32
 
 
+def test_planner_invariants_on_random_layouts():
+    """Every path the planner accepts for a random layout launches within the
+    device limits (block <= 1024 threads, dynamic shared memory <= 227 KiB), covers
+    the tensor with a positive number of work units, and reports a canonical shape
+    with the tensor's element count; refusals are TL_ERR_PATH only."""
+    rng = np.random.default_rng(4242)
+    seen = set()
+    for _ in range(400):
+        eb = int(rng.choice([1, 2, 4, 8, 16]))
+        nd = int(rng.integers(1, 8))
+        hi = 600 if nd <= 2 else (60 if nd <= 4 else 9)
+        shape = tuple(int(x) for x in rng.integers(1, hi, size=nd))
+        perm = [int(p) for p in rng.permutation(nd)]
+        pad = [int(x) for x in rng.integers(0, 3, size=nd)] if rng.random() < 0.4 else [0] * nd
+        ss, acc = [], 1
+        for e, p_ in zip(reversed(shape), reversed(pad)):
+            ss.append(acc)
+            acc *= e + p_
+        ss = tuple(reversed(ss))
+        pst = L.row_major_strides(tuple(shape[p] for p in perm))
+        ds = [0] * nd
+        for i, p in enumerate(perm):
+            ds[p] = pst[i]
+        n = int(np.prod(shape))
+        so = int(rng.integers(0, 4)) * eb
+        for path in tl.PATHS:
+            try:
+                plan = tl.tl_plan(SRC + so, DST, shape, ss, tuple(ds), eb, path=path)
+            except tl.TLError as e:
+                assert e.name == "TL_ERR_PATH", (shape, path, e.name)
+                continue
+            seen.add(plan["path"])
+            assert int(np.prod(plan["extent"])) == n
+            assert plan["tiles"] > 0 and 0 < plan["block"] <= 1024
+            assert 0 <= plan["smem_bytes"] <= 227 * 1024, (shape, ss, ds, eb, path, plan)
+    assert {"chunk", "panel", "tile", "generic", "warp", "rows", "cluster"} <= seen, seen
+
+
 def test_smoke_cases_take_the_paths_they_name():
     import __graft_entry__ as g
     for name, shape, ss, ds, eb, path in g.SMOKE_CASES:

@@ -28,18 +28,19 @@ struct DevInfo {
     int cluster_occ[5][2][kMaxClusterSlots + 1] = {}; // by consumer warps (8|4), slots
 };
 
-// Tile-path tuning after defaults are applied.  The defaults were measured on
-// GB300 over the batched 128x64 tile transpose and the 2-D transposes of every
-// element width: one CTA per SM with a 4-deep ring (about 600 tiles, 10 MB, in
-// flight GPU-wide) beat deeper rings and denser grids on every workload, and
-// visiting every tile row of a column block before the next block (the whole b
-// extent as one group) beat groups of 16 to 128 rows: the CTAs then write dst
-// front to back as one sequential stream while their reads stay 128-byte rows.
-// 256-row tiles were slower than 128-row tiles on every workload.
+// Tile-path tuning.  The defaults were measured on GB300 over the batched 128x64
+// tile transpose and the 2-D transposes of every element width: about 600-700
+// tiles (10-11 MB) in flight GPU-wide (ring depth and grid: tile_defaults) beat
+// deeper rings and denser grids on every workload, and visiting every tile row of
+// a column block before the next block (the whole b extent as one group) beat
+// groups of 16 to 128 rows: the CTAs then write dst front to back as one
+// sequential stream while their reads stay 128-byte rows.  256-row tiles were
+// slower than 128-row tiles on every workload.
 struct TileTuning {
     int group = 0;          // tile rows visited together (0 = the whole b extent)
     int rows = 128;         // tile height (128 or 256)
-    int stages = 4;         // ring depth
+    int stages = 0;         // ring depth (0 = by element width, tile_defaults)
+    int grid_per_152 = 0;   // tile grid per 152 SMs (0 = one CTA per SM)
     int ctas_per_sm = 0;    // resident CTAs the grid is sized for (0 = path default)
     int promotion = 256;    // L2 fill size of the TMA loads (0 = none)
     int cluster_stages = 2; // staging ring depth of the cluster variant
@@ -47,6 +48,25 @@ struct TileTuning {
     int cluster_warps = 4;  // its consumer warps (8 or 4)
     int cluster_ctas = 0;   // its CTAs per SM (0 = by layout; tile_ctas_per_sm overrides)
 };
+
+// Tile-path ring depth and grid by element width.  Throughput against the tiles in
+// flight is not smooth (a sweep of 3-6 stages x 96-152 CTAs on GB300 moved by up to
+// 25 % between neighbouring points, repeatably); the best measured point was one CTA
+// per SM with 4 stages for 1-, 4-, 8- and 16-byte elements and 136 CTAs with 5
+// stages for 2-byte elements (batched 128x64 tiles 6.75 -> 6.83 TB/s, 2-D 6.58 ->
+// 6.70 TB/s, repeated on separate boxes).  Explicit options replace both.
+void tile_defaults(const Plan& p, const tl_permute_opts* o, TileTuning& t) {
+    const bool user = o && o->tile_stages >= 2 && o->tile_stages <= kMaxTileStages;
+    if (user) return;
+    if (p.eb == 2 && t.rows == 128) {
+        t.stages = 5;
+        if (!(o && (o->tile_ctas_per_sm > 0 || o->max_ctas > 0))) t.grid_per_152 = 136;
+    } else {
+        t.stages = 4;
+    }
+    const int max_stages = kTileRingBytes / (t.rows * 128);
+    if (t.stages > max_stages) t.stages = max_stages;
+}
 
 // The cluster variant, with its slot hand-backs released at CTA scope, is paced by
 // the loads it keeps in flight GPU-wide, like the single-CTA kernel (throughput
@@ -246,7 +266,9 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
             int per_sm = d->tile_occ[log2i(p.eb)][p.tile_rows == 256 ? 1 : 0][tt.stages];
             const int want = tt.ctas_per_sm > 0 ? tt.ctas_per_sm : 1;
             if (want < per_sm) per_sm = want;
-            l.grid = cap_grid(p.tiles, sms * (per_sm < 1 ? 1 : per_sm), max_ctas);
+            int64_t cap = sms * (per_sm < 1 ? 1 : per_sm);
+            if (tt.grid_per_152 > 0) cap = (sms * tt.grid_per_152 + 151) / 152;
+            l.grid = cap_grid(p.tiles, cap, max_ctas);
         }
         break;
     case TL_PATH_CLUSTER:
@@ -323,6 +345,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
     if (rc != TL_OK) return rc;
     const int32_t max_ctas = opts ? opts->max_ctas : 0;
     TileTuning tt = tile_tuning(opts);
+    tile_defaults(p, opts, tt);
     cluster_defaults(p, tt);
     apply_tile_rows(p, tt);
     apply_panel_tile(p, opts);
@@ -570,6 +593,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         info.mask = p.mask;
     }
     TileTuning tt = tile_tuning(opts);
+    tile_defaults(p, opts, tt);
     cluster_defaults(p, tt);
     apply_tile_rows(p, tt);
     apply_panel_tile(p, opts);

@@ -268,6 +268,25 @@ def test_auto_paths_on_random_layouts():
 # ---------------------------------------------------------------------------
 # edge cases
 # ---------------------------------------------------------------------------
+def test_tensor_level_permute_matches_torch():
+    """The README's example at a smaller size: a (B, H, S, D) -> (B, S, H, D)
+    bfloat16 permute through tl.permute on torch CUDA tensors equals torch's own
+    transpose, and the planner names the chunk path; an fp32 2-D transpose into a
+    transposed view equals .t()."""
+    x = torch.randn(2, 8, 256, 128, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(2, 256, 8, 128, dtype=torch.bfloat16, device="cuda")
+    ds = (y.stride(0), y.stride(2), y.stride(1), y.stride(3))
+    tl.permute(x, y, x.shape, x.stride(), ds)
+    torch.cuda.synchronize()
+    assert torch.equal(y, x.transpose(1, 2))
+    assert tl.tl_plan(x.data_ptr(), y.data_ptr(), x.shape, x.stride(), ds, 2)["path"] == "chunk"
+    a = torch.randn(300, 520, device="cuda")
+    b = torch.empty(520, 300, device="cuda")
+    tl.permute(a, b, a.shape, a.stride(), (1, 300))
+    torch.cuda.synchronize()
+    assert torch.equal(b, a.t())
+
+
 def test_edge_cases():
     check((), (), (), 4)                                         # one element
     check((1, 1, 1), (7, 3, 1), (1, 1, 1), 16)

@@ -108,15 +108,6 @@ def test_chunk_path(eb):
     check((37, 300, 16), (300 * 16, 16, 1), (16, 37 * 16, 1), eb, "chunk", seed=12)
 
 
-TILE_CASES = [
-    # (shape, ss, ds): 2-D transposes with ragged edges, batched tiles, 3-batch
-    ((300, 517), None, None),
-    ((128, 256), None, None),
-    ((1000, 48), None, None),
-    ((33, 1024), None, None),
-]
-
-
 def _tile_shapes(eb):
     out = []
     for rows, cols in ((300, 256), (128, 256), (1000, 64), (33, 1024), (257, 384)):

@@ -1,4 +1,6 @@
-// k_generic.cu -- the correctness floor: any layout pair, one element per step.
+// k_generic.cu -- the correctness floor: any layout pair, one element per step, or
+// 16 bytes of dst per step when dst's innermost axis is contiguous (gathers from
+// strided views).
 //
 // Flat index f runs over the canonical shape in dst order (axes sorted by dst
 // stride, so consecutive threads write neighbouring elements); its coordinates
@@ -10,7 +12,7 @@
 namespace tl {
 namespace {
 
-template <int EB>
+template <int EB, int VM>
 __global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
@@ -41,7 +43,21 @@ __global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
                 }
             }
         }
-        dev::copy_elem<EB>(a.dst + d * EB, a.src + so * EB);
+        if constexpr (VM == 0) {
+            dev::copy_elem<EB>(a.dst + d * EB, a.src + so * EB);
+        } else {
+            using T = typename dev::Bits<EB>::T;
+            constexpr int V = 16 / EB;
+            union {
+                uint4 v;
+                T e[V];
+            } u;
+            // gather V strided elements, one 16-byte store
+#pragma unroll
+            for (int k = 0; k < V; ++k)
+                u.e[k] = *reinterpret_cast<const T*>(a.src + (so + k * a.vstep) * EB);
+            dev::stg128(a.dst + d * EB, u.v);
+        }
     }
 }
 
@@ -49,7 +65,10 @@ __global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
 
 template <int EB>
 cudaError_t launch_generic(const GenericArgs& a, int grid, int block, cudaStream_t st, bool pdl) {
-    return launch_kernel(k_generic<EB>, dim3(grid), dim3(block), 0, st, pdl, a);
+    if constexpr (EB < 16) {
+        if (a.vmode == 1) return launch_kernel(k_generic<EB, 1>, dim3(grid), dim3(block), 0, st, pdl, a);
+    }
+    return launch_kernel(k_generic<EB, 0>, dim3(grid), dim3(block), 0, st, pdl, a);
 }
 
 template cudaError_t launch_generic<1>(const GenericArgs&, int, int, cudaStream_t, bool);

@@ -38,7 +38,13 @@ struct GenericArgs {
     uint8_t* dst;
     int32_t n;
     int32_t use32;               // 1: flat index and extents fit in 32 bits
-    int64_t total;
+    int64_t total;               // steps: elements, or 16-byte groups (vmode 1, 2)
+    // vmode 1: a step is 16/EB consecutive dst elements (one 16-byte store, loads
+    // vstep apart in src).  The innermost axis below is then counted in groups (its
+    // extent divided, its strides multiplied, by 16/EB).
+    int32_t vmode;
+    int32_t pad;
+    int64_t vstep;
     int64_t ext[TL_MAX_DIMS];
     int64_t ss[TL_MAX_DIMS];     // elements
     int64_t ds[TL_MAX_DIMS];

@@ -328,6 +328,36 @@ void apply_tile_rows(Plan& p, const TileTuning& tt) {
     p.tiles = ta * tb * p.batch_total;
 }
 
+// 16 bytes per step for the generic kernel when dst's innermost axis is contiguous
+// and src is a strided view (a gather): the innermost axis is counted in groups of
+// 16/eb elements, every group 16-byte aligned in dst.
+void generic_vector_mode(GenericArgs& a, int eb, uintptr_t dst) {
+    a.vmode = 0;
+    if (eb >= 16 || a.n < 1) return;
+    const int64_t V = 16 / eb;
+    const int in = a.n - 1;
+    if (a.ext[in] % V != 0) return;
+    auto aligned_side = [&](uintptr_t base, const int64_t* str) {
+        if (base % 16 != 0) return false;
+        for (int i = 0; i < in; ++i)
+            if ((str[i] * eb) % 16 != 0) return false;
+        return true;
+    };
+    // Only gathers (dst contiguous): a scatter from 16-byte loads would spread each
+    // warp store over 32 sectors (measured 2.5 -> 1.7 TB/s), where per-element steps
+    // keep consecutive lanes on consecutive strided addresses.
+    if (a.ds[in] == 1 && aligned_side(dst, a.ds)) {
+        a.vmode = 1;
+        a.vstep = a.ss[in];
+    } else {
+        return;
+    }
+    a.ext[in] /= V;
+    a.ss[in] *= V;
+    a.ds[in] *= V;
+    a.total /= V;
+}
+
 void fill_divs(int n, const int64_t* ext, dev::DivU32* div) {
     for (int i = 0; i < n; ++i) div[i] = dev::make_divu32((uint32_t)ext[i]);
 }
@@ -367,6 +397,8 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         for (int i = 0; i < a.n; ++i) {
             a.ext[i] = p.sorted.ext[i]; a.ss[i] = p.sorted.ss[i]; a.ds[i] = p.sorted.ds[i];
         }
+        generic_vector_mode(a, eb, reinterpret_cast<uintptr_t>(dst));
+        a.use32 = a.total < (1LL << 32) ? 1 : 0;
         if (a.use32) fill_divs(a.n, a.ext, a.div);
         switch (eb) {
         case 1: err = launch_generic<1>(a, l.grid, l.block, st, pdl); break;

@@ -94,6 +94,21 @@ def test_generic_path(eb):
 
 
 @pytest.mark.parametrize("eb", WIDTHS)
+def test_generic_path_strided_views(eb):
+    # strided views on one side, contiguous innermost on the other: the generic
+    # kernel moves 16 bytes per step (gather into dst, or scatter from src) when the
+    # contiguous side is 16-byte aligned, one element per step otherwise
+    v = max(1, 16 // eb)
+    for i, (shape, ss, ds) in enumerate((
+            ((37, 8 * v), (2 * 8 * v * 2, 2), (8 * v, 1)),          # x[::2, ::2] -> contiguous
+            ((37, 8 * v), (8 * v, 1), (2 * 8 * v, 2)),              # contiguous -> y[:, ::2]
+            ((5, 3, 4 * v), (0, 4 * v * 3, 3), (12 * v, 4 * v, 1)),  # broadcast, stride-3 gather
+            ((9, 2 * v), (1, 9 * 3), (2 * v, 1)))):                  # column gather, stride 27
+        check(shape, ss, ds, eb, "generic", seed=110 + i)
+        check(shape, ss, ds, eb, "generic", seed=120 + i, src_off=1, dst_off=1)
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
 def test_chunk_path(eb):
     rng = np.random.default_rng(200 + eb)
     for i in range(10):

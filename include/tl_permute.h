@@ -174,6 +174,15 @@ TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape
  * while the previous kernel of the stream drains; it waits for that kernel to complete
  * before touching global memory, so stream order is unchanged either way). */
 #define TL_FLAG_NO_PDL (1u << 9)
+/* Checked run (a sanitizer stand-in): the generic kernel moves every element after
+ * checking its src and dst byte ranges against opts.src_bytes / opts.dst_bytes (a
+ * side given as 0 is not checked); an element outside is skipped and
+ * TL_ERR_BOUNDS written to dev_status.  Forces the generic path (another forced path
+ * returns TL_ERR_PATH).  The host-side layout check still runs first. */
+#define TL_FLAG_DEBUG_CHECKS (1u << 10)
+/* Test hook, only with TL_FLAG_DEBUG_CHECKS (else TL_ERR_ARG): skip the host-side
+ * TL_ERR_BOUNDS check so that a test can show the device-side one. */
+#define TL_FLAG_TEST_SKIP_HOST_BOUNDS (1u << 11)
 
 /* Options of tl_permute_ex.  Zero-initialise, then set what you need. */
 typedef struct tl_permute_opts {

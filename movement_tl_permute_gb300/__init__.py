@@ -20,6 +20,7 @@ import threading
 
 __all__ = [
     "TLError", "TL_MAX_DIMS", "PATHS", "PATH_NAMES", "TL_FLAG_TEST_DROP_HANDOFF", "TL_FLAG_NO_PDL",
+    "TL_FLAG_DEBUG_CHECKS", "TL_FLAG_TEST_SKIP_HOST_BOUNDS",
     "load", "library_path", "tl_layout_canon", "tl_choose_xor_k", "tl_bank_conflicts",
     "tl_permute", "tl_permute_ex", "tl_plan", "tl_status_string", "tl_launch_count",
     "tl_version", "permute", "tl_permute_tile_noalloc",
@@ -31,6 +32,8 @@ PATHS = {"auto": 0, "generic": 1, "chunk": 2, "tile": 3, "warp": 4, "rows": 5, "
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 TL_FLAG_TEST_DROP_HANDOFF = 1 << 8
 TL_FLAG_NO_PDL = 1 << 9
+TL_FLAG_DEBUG_CHECKS = 1 << 10
+TL_FLAG_TEST_SKIP_HOST_BOUNDS = 1 << 11
 STATUS = {0: "TL_OK", -1: "TL_ERR_ARG", -2: "TL_ERR_ELEM_BYTES", -3: "TL_ERR_EXTENT",
           -4: "TL_ERR_NO_VALID_K", -5: "TL_ERR_CHUNK", -6: "TL_ERR_DST_OVERLAP",
           -7: "TL_ERR_ALIAS", -8: "TL_ERR_ALIGN", -9: "TL_ERR_PATH", -10: "TL_ERR_RANGE",

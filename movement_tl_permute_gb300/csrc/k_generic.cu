@@ -12,7 +12,9 @@
 namespace tl {
 namespace {
 
-template <int EB, int VM>
+// CK: the checked run -- each element's byte ranges are compared with the buffer
+// sizes first; an element outside is skipped and TL_ERR_BOUNDS recorded.
+template <int EB, int VM, bool CK>
 __global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
@@ -43,6 +45,14 @@ __global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
                 }
             }
         }
+        if constexpr (CK) {
+            const bool in = (a.src_bytes <= 0 || (so + 1) * EB <= a.src_bytes) &&
+                            (a.dst_bytes <= 0 || (d + 1) * EB <= a.dst_bytes);
+            if (!in) {
+                dev::report(a.status, TL_ERR_BOUNDS);
+                continue;
+            }
+        }
         if constexpr (VM == 0) {
             dev::copy_elem<EB>(a.dst + d * EB, a.src + so * EB);
         } else {
@@ -65,10 +75,13 @@ __global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
 
 template <int EB>
 cudaError_t launch_generic(const GenericArgs& a, int grid, int block, cudaStream_t st, bool pdl) {
+    if (a.checked)
+        return launch_kernel(k_generic<EB, 0, true>, dim3(grid), dim3(block), 0, st, pdl, a);
     if constexpr (EB < 16) {
-        if (a.vmode == 1) return launch_kernel(k_generic<EB, 1>, dim3(grid), dim3(block), 0, st, pdl, a);
+        if (a.vmode == 1)
+            return launch_kernel(k_generic<EB, 1, false>, dim3(grid), dim3(block), 0, st, pdl, a);
     }
-    return launch_kernel(k_generic<EB, 0>, dim3(grid), dim3(block), 0, st, pdl, a);
+    return launch_kernel(k_generic<EB, 0, false>, dim3(grid), dim3(block), 0, st, pdl, a);
 }
 
 template cudaError_t launch_generic<1>(const GenericArgs&, int, int, cudaStream_t, bool);

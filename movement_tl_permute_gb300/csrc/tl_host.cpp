@@ -500,8 +500,14 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     if (!valid_eb(eb)) return TL_ERR_ELEM_BYTES;
     if (ndim < 0 || ndim > kMaxDims) return TL_ERR_ARG;
     if (ndim > 0 && (!shape || !src_strides || !dst_strides)) return TL_ERR_ARG;
-    const uint32_t forced = flags & TL_PATH_MASK;
+    uint32_t forced = flags & TL_PATH_MASK;
     if (forced > TL_PATH_PANEL) return TL_ERR_ARG;
+    const bool checked = (flags & TL_FLAG_DEBUG_CHECKS) != 0;
+    if ((flags & TL_FLAG_TEST_SKIP_HOST_BOUNDS) && !checked) return TL_ERR_ARG;
+    if (checked) {                 // the checked run is the generic kernel
+        if (forced != TL_PATH_AUTO && forced != TL_PATH_GENERIC) return TL_ERR_PATH;
+        forced = TL_PATH_GENERIC;
+    }
     p.eb = eb;
     int64_t total = 1;
     for (int i = 0; i < ndim; ++i) {
@@ -523,7 +529,8 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         return TL_ERR_RANGE;
     int64_t sbytes, dbytes;
     if (!mul_ok(sspan + 1, eb, &sbytes) || !mul_ok(dspan + 1, eb, &dbytes)) return TL_ERR_RANGE;
-    if ((src_bytes > 0 && sbytes > src_bytes) || (dst_bytes > 0 && dbytes > dst_bytes))
+    if (((src_bytes > 0 && sbytes > src_bytes) || (dst_bytes > 0 && dbytes > dst_bytes)) &&
+        !(flags & TL_FLAG_TEST_SKIP_HOST_BOUNDS))
         return TL_ERR_BOUNDS;
     if (!non_overlapping(ndim, shape, dst_strides)) return TL_ERR_DST_OVERLAP;
 

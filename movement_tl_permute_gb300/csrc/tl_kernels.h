@@ -43,8 +43,10 @@ struct GenericArgs {
     // vstep apart in src).  The innermost axis below is then counted in groups (its
     // extent divided, its strides multiplied, by 16/EB).
     int32_t vmode;
-    int32_t pad;
+    int32_t checked;             // 1: TL_FLAG_DEBUG_CHECKS (bounds below, status word)
     int64_t vstep;
+    int64_t src_bytes, dst_bytes;    // checked run: addressable bytes (0 = unchecked)
+    int32_t* status;
     int64_t ext[TL_MAX_DIMS];
     int64_t ss[TL_MAX_DIMS];     // elements
     int64_t ds[TL_MAX_DIMS];

@@ -397,7 +397,14 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         for (int i = 0; i < a.n; ++i) {
             a.ext[i] = p.sorted.ext[i]; a.ss[i] = p.sorted.ss[i]; a.ds[i] = p.sorted.ds[i];
         }
-        generic_vector_mode(a, eb, reinterpret_cast<uintptr_t>(dst));
+        a.checked = (flags & TL_FLAG_DEBUG_CHECKS) ? 1 : 0;
+        if (a.checked) {
+            a.src_bytes = opts ? opts->src_bytes : 0;
+            a.dst_bytes = opts ? opts->dst_bytes : 0;
+            a.status = opts ? opts->dev_status : nullptr;
+        } else {
+            generic_vector_mode(a, eb, reinterpret_cast<uintptr_t>(dst));
+        }
         a.use32 = a.total < (1LL << 32) ? 1 : 0;
         if (a.use32) fill_divs(a.n, a.ext, a.div);
         switch (eb) {

@@ -293,6 +293,33 @@ def test_tensor_level_permute_matches_torch():
     assert torch.equal(b, a.t())
 
 
+@pytest.mark.parametrize("eb", [1, 4, 16])
+def test_checked_run(eb):
+    """TL_FLAG_DEBUG_CHECKS: a valid layout gives the oracle's bytes and a clean
+    status; with the host check skipped and dst declared half its real size, the
+    device check skips every element past the declared bytes (which stay canary),
+    writes the rest exactly, and records TL_ERR_BOUNDS.  The real buffer covers the
+    whole layout, so no access could leave the allocation even if a check failed."""
+    shape, ss, ds = (64, 48), (48, 1), (1, 64)
+    check(shape, ss, ds, eb, "auto", seed=7, flags=tl.TL_FLAG_DEBUG_CHECKS,
+          src_bytes=64 * 48 * eb, dst_bytes=64 * 48 * eb)
+    src = workloads.random_bits(64 * 48 * eb, 8)
+    want = np.full(64 * 48 * eb, CANARY, dtype=np.uint8)
+    oracle.permute(src, want, shape, ss, ds, eb)
+    declared = 64 * 48 * eb // 2
+    want[declared:] = CANARY                           # skipped by the device check
+    s_gpu = torch.from_numpy(src).cuda()
+    d_gpu = torch.full((64 * 48 * eb,), CANARY, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), shape, ss, ds, eb,
+                     torch.cuda.current_stream().cuda_stream,
+                     flags=tl.TL_FLAG_DEBUG_CHECKS | tl.TL_FLAG_TEST_SKIP_HOST_BOUNDS,
+                     dev_status=status.data_ptr(), src_bytes=64 * 48 * eb, dst_bytes=declared)
+    torch.cuda.synchronize()
+    assert int(status.item()) == {v: k for k, v in tl.STATUS.items()}["TL_ERR_BOUNDS"]
+    assert np.array_equal(d_gpu.cpu().numpy(), want)
+
+
 def test_edge_cases():
     check((), (), (), 4)                                         # one element
     check((1, 1, 1), (7, 3, 1), (1, 1, 1), 16)

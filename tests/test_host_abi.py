@@ -396,6 +396,21 @@ def test_planner_invariants_on_random_layouts():
     assert {"chunk", "panel", "tile", "generic", "warp", "rows", "cluster"} <= seen, seen
 
 
+def test_checked_run_flags():
+    w = workloads.get("t2d_f32")
+    dbg = tl.TL_FLAG_DEBUG_CHECKS
+    assert _plan(w, flags=dbg)["path"] == "generic"                 # the checked kernel
+    assert _plan(w, flags=dbg, path="generic")["path"] == "generic"
+    assert _err(SRC, DST, w.shape, w.src_strides, w.dst_strides, 4, flags=dbg,
+                path="tile") == "TL_ERR_PATH"
+    skip = tl.TL_FLAG_TEST_SKIP_HOST_BOUNDS
+    assert _err(SRC, DST, w.shape, w.src_strides, w.dst_strides, 4, flags=skip) == "TL_ERR_ARG"
+    small = dict(dst_bytes=1024)
+    assert _err(SRC, DST, w.shape, w.src_strides, w.dst_strides, 4, flags=dbg,
+                **small) == "TL_ERR_BOUNDS"
+    assert _plan(w, flags=dbg | skip, **small)["path"] == "generic"
+
+
 def test_smoke_cases_take_the_paths_they_name():
     import __graft_entry__ as g
     for name, shape, ss, ds, eb, path in g.SMOKE_CASES:

@@ -335,6 +335,11 @@ def config_of(w, plan):
             "seed": w.seed}
 
 
+def input_digest(buf) -> str:
+    """SHA-256 of the input bytes (first 16 hex digits), logged with the seed."""
+    return hashlib.sha256(memoryview(buf).cast("B")).hexdigest()[:16]
+
+
 def run_reference(args, w):
     import numpy as np
 
@@ -453,6 +458,18 @@ def run_ours(args, w):
     ms_local = e0.elapsed_time(e1)
     ms_max = reduce_max(ms_local, dev if world > 1 else None)
 
+    # per-launch spread: a few steps timed one by one (outside the timed region)
+    singles = []
+    if graph is None:
+        for _ in range(min(20, args.steps)):
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            step()
+            s1.record(stream)
+            s1.synchronize()
+            singles.append(s0.elapsed_time(s1))
+    singles.sort()
+
     # ------------------------------------------------ end to end, host buffers
     # Each step copies its input from pinned host memory, permutes and copies the
     # result back.  Consecutive steps alternate between two buffer sets on two
@@ -515,7 +532,8 @@ def run_ours(args, w):
         "ms_per_step": round(ms_max / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPES.get(w.name, "bits"),
         "data": "synthetic",
-        "config": dict(config_of(w, plan), launch="cuda_graph" if graph is not None else "stream"),
+        "config": dict(config_of(w, plan), launch="cuda_graph" if graph is not None else "stream",
+                       input_sha256=input_digest(src_np)),
         "pct_hbm_peak": round(100.0 * value / world / peak, 2),
         "parity": {"bit_exact": parity,
                    "checked": "GPU output vs oracle on the cpu_baseline sample"},
@@ -528,6 +546,10 @@ def run_ours(args, w):
                 "unit": UNIT, "h2d_bytes_per_step": int(src_np.nbytes),
                 "d2h_bytes_per_step": int(nbytes_dst), "steps": e2e_steps},
         "gpu_launches": int(launches),
+        "per_launch_ms": ({"median": round(singles[len(singles) // 2], 5),
+                           "min": round(singles[0], 5), "n": len(singles),
+                           "note": "steps timed one at a time after the timed region"}
+                          if singles else None),
         "clocks": clock_summary,
     }
     print(json.dumps(line), flush=True)

@@ -183,6 +183,9 @@ TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape
 /* Test hook, only with TL_FLAG_DEBUG_CHECKS (else TL_ERR_ARG): skip the host-side
  * TL_ERR_BOUNDS check so that a test can show the device-side one. */
 #define TL_FLAG_TEST_SKIP_HOST_BOUNDS (1u << 11)
+/* Panel path: store the tile element by element even where its dst rows would take
+ * 16-byte runs (tuning and comparison; the result is the same). */
+#define TL_FLAG_PANEL_ELEMENT_STORES (1u << 12)
 
 /* Options of tl_permute_ex.  Zero-initialise, then set what you need. */
 typedef struct tl_permute_opts {
@@ -238,7 +241,9 @@ typedef struct tl_plan_info {
     int32_t panel_mode;            /* panel path: 0 rows of 16-byte blocks, 1 one run */
     int32_t panel_b1;              /* panel path: > 0 when the dst-contiguous axis (extent
                                       panel_b1) and the next dst axis are walked as one */
-    int32_t reserved[2];
+    int32_t panel_vec;             /* panel path: 1 when tiles are stored as 16-byte dst
+                                      runs, 0 element by element */
+    int32_t reserved;
 } tl_plan_info;
 
 TL_API int tl_plan(const void *src, const void *dst, int ndim, const int64_t *shape,

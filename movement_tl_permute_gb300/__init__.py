@@ -20,7 +20,7 @@ import threading
 
 __all__ = [
     "TLError", "TL_MAX_DIMS", "PATHS", "PATH_NAMES", "TL_FLAG_TEST_DROP_HANDOFF", "TL_FLAG_NO_PDL",
-    "TL_FLAG_DEBUG_CHECKS", "TL_FLAG_TEST_SKIP_HOST_BOUNDS",
+    "TL_FLAG_DEBUG_CHECKS", "TL_FLAG_TEST_SKIP_HOST_BOUNDS", "TL_FLAG_PANEL_ELEMENT_STORES",
     "load", "library_path", "tl_layout_canon", "tl_choose_xor_k", "tl_bank_conflicts",
     "tl_permute", "tl_permute_ex", "tl_plan", "tl_status_string", "tl_launch_count",
     "tl_version", "permute", "tl_permute_tile_noalloc",
@@ -34,6 +34,7 @@ TL_FLAG_TEST_DROP_HANDOFF = 1 << 8
 TL_FLAG_NO_PDL = 1 << 9
 TL_FLAG_DEBUG_CHECKS = 1 << 10
 TL_FLAG_TEST_SKIP_HOST_BOUNDS = 1 << 11
+TL_FLAG_PANEL_ELEMENT_STORES = 1 << 12
 STATUS = {0: "TL_OK", -1: "TL_ERR_ARG", -2: "TL_ERR_ELEM_BYTES", -3: "TL_ERR_EXTENT",
           -4: "TL_ERR_NO_VALID_K", -5: "TL_ERR_CHUNK", -6: "TL_ERR_DST_OVERLAP",
           -7: "TL_ERR_ALIAS", -8: "TL_ERR_ALIGN", -9: "TL_ERR_PATH", -10: "TL_ERR_RANGE",
@@ -76,7 +77,8 @@ class TlPlanInfo(ctypes.Structure):
                 ("vec_bytes", _i32), ("in_place", _i32), ("k", _i32), ("shift", _i32),
                 ("mask", _i32), ("tile_rows", _i32), ("tile_cols", _i32), ("tiles", _i64),
                 ("grid", _i32), ("block", _i32), ("smem_bytes", _i32), ("pitch", _i32),
-                ("panel_mode", _i32), ("panel_b1", _i32), ("reserved", _i32 * 2)]
+                ("panel_mode", _i32), ("panel_b1", _i32), ("panel_vec", _i32),
+                ("reserved", _i32)]
 
 
 def library_path() -> str:
@@ -266,7 +268,7 @@ def tl_plan(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides, elem_by
                 shift=info.shift, mask=info.mask, tile_rows=info.tile_rows,
                 tile_cols=info.tile_cols, tiles=info.tiles, grid=info.grid, block=info.block,
                 smem_bytes=info.smem_bytes, pitch=info.pitch, panel_mode=info.panel_mode,
-                panel_b1=info.panel_b1)
+                panel_b1=info.panel_b1, panel_vec=info.panel_vec)
 
 
 def _bytes_after(t) -> int:

@@ -115,7 +115,17 @@ __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
 template <int EB>
 __device__ __forceinline__ void issue(const PanelArgs& a, const PanelTile& ti, uint32_t sb) {
     const uintptr_t base = reinterpret_cast<uintptr_t>(a.src + ti.so * EB);
-    if (a.mode == kPanelRows) {
+    if (a.mode == kPanelRows && a.aligned) {
+        // every row starts on a block boundary: nblk blocks per full row, the valid
+        // rows only
+        const uint32_t nblk = (uint32_t)a.nblk, n = ti.vb * nblk;
+        const uint32_t blocks = (ti.va * EB + 15) >> 4, pitch = (uint32_t)a.pitch;
+        for (uint32_t g = threadIdx.x; g < n; g += kPanelThreads) {
+            const uint32_t b = dev::div_u32(g, a.d_nblk), k = g - b * nblk;
+            if (k < blocks)
+                cp_async16(sb + b * pitch + 16 * k, base + (uintptr_t)(row_offset(b, ti, a) * EB) + 16 * k);
+        }
+    } else if (a.mode == kPanelRows) {
         const uint32_t nblk = (uint32_t)a.nblk, n = (uint32_t)a.tb * nblk;
         const uint32_t pitch = (uint32_t)a.pitch;
         for (uint32_t g = threadIdx.x; g < n; g += kPanelThreads) {
@@ -132,9 +142,82 @@ __device__ __forceinline__ void issue(const PanelArgs& a, const PanelTile& ti, u
     }
 }
 
+template <typename T>
+__device__ __forceinline__ void cswap(bool p, T& x, T& y) {
+    const T u = p ? y : x, v = p ? x : y;
+    x = u;
+    y = v;
+}
+
+// V = 16 / EB elements in b order as one 16-byte vector
+__device__ __forceinline__ uint4 pack16(const uint2 (&v)[2]) {
+    return make_uint4(v[0].x, v[0].y, v[1].x, v[1].y);
+}
+__device__ __forceinline__ uint4 pack16(const uint32_t (&v)[4]) {
+    return make_uint4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ uint4 pack16(const uint16_t (&v)[8]) {
+    auto w = [&](int i) { return (uint32_t)v[2 * i] | ((uint32_t)v[2 * i + 1] << 16); };
+    return make_uint4(w(0), w(1), w(2), w(3));
+}
+
+// Store one landed tile as 16-byte dst runs (used when the dst rows of every tile
+// start on 16-byte boundaries and tb * EB is a multiple of 128).  Unit (e, q) is
+// dst row e of the tile, block q of it (elements b = qV .. qV + V - 1, V = 16 / EB).
+// A warp takes 4 rows x 8 blocks, so each of its stores writes four whole 128-byte
+// lines.  The lane of block q reads its V elements down column e of the stage, the
+// k-th from row qV + (k ^ r) with r = (q / max(8 / V, 1)) mod V: the warp's 8 blocks
+// then read rows that differ mod 8 at every step, which an odd row pitch in 16-byte
+// units puts in distinct bank groups (the XOR rotation of the TVM "permute_layout"
+// page, "Algorithm" step 2, applied to the stage; the host's pitch search simulates
+// exactly these reads).  A conditional-swap network restores b order.
+template <int EB>
+__device__ __forceinline__ void drain_vec(const PanelArgs& a, const PanelTile& ti,
+                                          const uint8_t* st) {
+    using T = typename dev::Bits<EB>::T;
+    constexpr uint32_t V = 16 / EB, QD = V >= 8 ? 1 : 8 / V;
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t qb8 = a.d_qb8.d, units = ((ti.va + 3) >> 2) * qb8;
+    const uint32_t mis0 = (uint32_t)(reinterpret_cast<uintptr_t>(a.src + ti.so * EB) & 15);
+    const uint32_t P = (uint32_t)a.vpitch, delta = (uint32_t)a.vdelta;
+    uint8_t* dbase = a.dst + ti.dof * EB;
+    for (uint32_t u = warp; u < units; u += kPanelThreads / 32) {
+        const uint32_t g4 = dev::div_u32(u, a.d_qb8), qg = u - g4 * qb8;
+        const uint32_t e = 4 * g4 + (lane >> 3), q = 8 * qg + (lane & 7), b0 = q * V;
+        if (e >= ti.va || b0 >= ti.vb) continue;
+        const uint32_t r = (q / QD) & (V - 1);
+        const uint8_t* col = st + e * EB;
+        T v[V];
+#pragma unroll
+        for (uint32_t k = 0; k < V; ++k) {
+            const uint32_t b = b0 + (k ^ r);
+            v[k] = *reinterpret_cast<const T*>(col + b * P + ((mis0 + b * delta) & 15u));
+        }
+#pragma unroll
+        for (uint32_t lv = 1; lv < V; lv <<= 1)
+#pragma unroll
+            for (uint32_t k = 0; k < V; ++k)
+                if (!(k & lv)) cswap((r & lv) != 0, v[k], v[k | lv]);
+        uint8_t* dp = dbase + ((int64_t)e * a.ds_a + b0) * EB;
+        if (b0 + V <= ti.vb) {
+            dev::stg128(dp, pack16(v));
+        } else {
+#pragma unroll
+            for (uint32_t k = 0; k < V; ++k)
+                if (b0 + k < ti.vb) *reinterpret_cast<T*>(dp + k * EB) = v[k];
+        }
+    }
+}
+
 // Store one landed tile from the stage at `st` to dst, in dst order.
 template <int EB>
 __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, const uint8_t* st) {
+    if constexpr (EB >= 2 && EB <= 8) {
+        if (a.vec) {
+            drain_vec<EB>(a, ti, st);
+            return;
+        }
+    }
     using T = typename dev::Bits<EB>::T;
     T* d = reinterpret_cast<T*>(a.dst) + ti.dof;
     const uint32_t ta = (uint32_t)a.ta, tb = (uint32_t)a.tb, pitch = (uint32_t)a.pitch;

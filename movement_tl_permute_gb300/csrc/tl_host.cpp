@@ -345,14 +345,19 @@ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
 // Panel pitch: the byte pitch (a multiple of 16) of the rows of the shared-memory
 // tile, chosen by simulating both walks' warp accesses on the banks (hardware
-// model).  The copy walk takes item g, a 16-byte block, at (b = g / blocks_per_row,
-// k = g % blocks_per_row); the store walk takes tile element f at (a = f / tb,
-// b = f % tb), whose row starts (r + b * (ss_b * eb mod 16)) mod 16 bytes into its
-// first block, simulated for every residue r of the tile's base address.  A warp
-// covers 32 consecutive items.  The first pitch with the lowest summed degree wins.
+// model).  The copy walk takes item g, a 16-byte block, at (b = g / nblk,
+// k = g % nblk), a warp covering 32 consecutive items.  In the store walk a row b
+// starts (r + b * (ss_b * eb mod 16)) mod 16 bytes into its first block, simulated
+// for every residue r of the tile's base address (r = 0 only when every row is
+// aligned).  Element stores: a warp takes 32 consecutive tile elements f at
+// (a = f / tb, b = f % tb).  16-byte dst runs (vec): a warp takes 4 rows a by 8
+// blocks q; at step k lane (a, q) reads row b = qV + (k ^ rot(q)), V = 16 / eb,
+// rot(q) = (q / max(8 / V, 1)) mod V, the reads of the panel kernel's drain_vec.
+// The first pitch with the lowest summed degree wins.
 struct PanelMemo {
     int ta, tb, eb, pitch;
     int64_t ssb, b1, ssb2;
+    int nblk, aligned, vec;
 };
 std::mutex g_panel_memo_mu;
 std::vector<PanelMemo> g_panel_memo;
@@ -366,7 +371,8 @@ int64_t b_mis16(int64_t b, int eb, int64_t ssb, int64_t b1, int64_t ssb2) {
     return (off * eb) & 15;
 }
 
-int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2) {
+int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2, int nblk,
+                bool aligned, bool vec) {
     // the row misalignments repeat with a period of 16 rows (one axis) or are
     // sampled over the tile's rows (merged axes); normalise the memo key
     const int64_t ssb_k = b1 > 0 ? ssb : (ssb * eb) & 15;
@@ -374,13 +380,16 @@ int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2) {
         std::lock_guard<std::mutex> lk(g_panel_memo_mu);
         for (const PanelMemo& e : g_panel_memo)
             if (e.ta == ta && e.tb == tb && e.eb == eb && e.ssb == ssb_k && e.b1 == b1 &&
-                e.ssb2 == ssb2)
+                e.ssb2 == ssb2 && e.nblk == nblk && e.aligned == (int)aligned &&
+                e.vec == (int)vec)
                 return e.pitch;
     }
-    const int64_t nblk = panel_blocks_per_row(ta, eb);
-    const int64_t n_copy = nblk * tb, n_store = (int64_t)ta * tb;
+    const int64_t n_copy = (int64_t)nblk * tb, n_store = (int64_t)ta * tb;
     const int64_t samples = 32 * 64;
-    int best = (int)(16 * nblk);
+    const int V = 16 / eb, QD = V >= 8 ? 1 : 8 / V;
+    const int64_t qb8 = vec ? (int64_t)tb * eb / 128 : 1;
+    const int64_t units = vec ? (int64_t)((ta + 3) / 4) * qb8 : 0;
+    int best = 16 * nblk;
     int64_t best_cost = -1;
     for (int64_t q = nblk; q < nblk + 8; ++q) {
         const int64_t pitch = 16 * q;
@@ -392,14 +401,30 @@ int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2) {
                 o[m] = (g / nblk) * q + g % nblk;                  // 16-byte units
             cost += bank_degree(m, o, 16, true);
         }
-        for (int r = 0; r < 16; r += eb) {
+        for (int r = 0; r < (aligned ? 1 : 16); r += eb) {
+            auto off = [&](int64_t a, int64_t b) {
+                return (b * pitch + ((r + b_mis16(b, eb, ssb, b1, ssb2)) & 15) + a * eb) / eb;
+            };
+            if (vec) {
+                for (int64_t u = 0; u < std::min(units, samples / 32); ++u) {
+                    const int64_t g4 = u / qb8, qg = u % qb8;
+                    for (int k = 0; k < V; ++k, ++ideal) {
+                        int64_t o[32];
+                        for (int l = 0; l < 32; ++l) {
+                            const int64_t a = 4 * g4 + l / 8, qq = 8 * qg + l % 8;
+                            const int64_t b = qq * V + (k ^ ((qq / QD) & (V - 1)));
+                            o[l] = a < ta ? off(a, b) : -1;
+                        }
+                        cost += bank_degree(32, o, eb, true);
+                    }
+                }
+                continue;
+            }
             for (int64_t f0 = 0; f0 < std::min(n_store, samples); f0 += 32, ++ideal) {
                 int64_t o[32];
                 int m = 0;
-                for (int64_t f = f0; f < f0 + 32 && f < n_store; ++f, ++m) {
-                    const int64_t a = f / tb, b = f % tb;
-                    o[m] = (b * pitch + ((r + b_mis16(b, eb, ssb, b1, ssb2)) & 15) + a * eb) / eb;
-                }
+                for (int64_t f = f0; f < f0 + 32 && f < n_store; ++f, ++m)
+                    o[m] = off(f / tb, f % tb);
                 cost += bank_degree(m, o, eb, true);
             }
         }
@@ -411,7 +436,7 @@ int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2) {
     }
     std::lock_guard<std::mutex> lk(g_panel_memo_mu);
     if (g_panel_memo.size() >= 64) g_panel_memo.erase(g_panel_memo.begin());
-    g_panel_memo.push_back({ta, tb, eb, best, ssb_k, b1, ssb2});
+    g_panel_memo.push_back({ta, tb, eb, best, ssb_k, b1, ssb2, nblk, (int)aligned, (int)vec});
     return best;
 }
 
@@ -443,23 +468,52 @@ void panel_merge_b(Plan* p) {
     }
 }
 
+namespace {
+
+// Every src row of every tile starts on a 16-byte boundary: the base, the tile
+// column step ta, the row strides and the batch strides are all multiples of 16 bytes.
+bool panel_src_aligned(const Plan& p, int64_t ta) {
+    const int eb = p.eb;
+    bool ok = p.src_mis16 == 0 && (ta * eb) % 16 == 0 && (p.ss_b * eb) % 16 == 0 &&
+              (p.panel_b1 == 0 || (p.panel_ss_b2 * eb) % 16 == 0);
+    for (int i = 0; i < p.batch.n; ++i) ok = ok && (p.batch.ss[i] * eb) % 16 == 0;
+    return ok;
+}
+
+// 16-byte dst runs: 2-, 4- or 8-byte elements, tb * eb a multiple of 128 (whole
+// 8-block groups), every dst row of every tile on a 16-byte boundary, and a row
+// misalignment in the stage that follows b linearly (packed rows, one b axis, or
+// merged axes whose src strides are multiples of 16 bytes).
+bool panel_dst_vec(const Plan& p, int64_t tb, bool packed) {
+    const int eb = p.eb;
+    if (p.panel_elem_stores || eb < 2 || eb > 8 || (tb * eb) % 128 != 0) return false;
+    bool ok = p.dst_mis16 == 0 && (p.ds_a * eb) % 16 == 0;
+    for (int i = 0; i < p.batch.n; ++i) ok = ok && (p.batch.ds[i] * eb) % 16 == 0;
+    if (p.panel_b1 > 0 && !packed)
+        ok = ok && (p.ss_b * eb) % 16 == 0 && (p.panel_ss_b2 * eb) % 16 == 0;
+    return ok;
+}
+
+}  // namespace
+
 void plan_panel(Plan* p, int tile_bytes) {
     const int eb = p->eb;
     const bool tiny = p->ext_a <= 16 || p->ext_b <= 16;
     if (tile_bytes <= 0) tile_bytes = tiny ? 16384 : 32768;
     const int64_t E = tile_bytes / eb;
+    const int64_t ru = eb == 2 ? 64 : 32;   // rows of b: whole 128-byte dst runs for 2-byte elements
     int64_t ta, tb;
     if (p->ext_b <= 16) {
         tb = p->ext_b;
         ta = std::min(round_up((E + tb - 1) / tb, 32), p->ext_a);
     } else if (p->ext_a <= 16) {
         ta = p->ext_a;
-        tb = std::min(round_up((E + ta - 1) / ta, 32), p->ext_b);
+        tb = std::min(round_up((E + ta - 1) / ta, ru), p->ext_b);
     } else {
         tb = std::min<int64_t>(eb <= 2 ? 64 : 32, p->ext_b);
         ta = std::min(E / tb, p->ext_a);
         if (ta * tb < E)            // a short a extent: the tile grows along b instead
-            tb = std::min(round_up((E + ta - 1) / ta, 32), p->ext_b);
+            tb = std::min(round_up((E + ta - 1) / ta, ru), p->ext_b);
     }
     int64_t stage;
     for (;;) {
@@ -468,19 +522,25 @@ void plan_panel(Plan* p, int tile_bytes) {
         // src rows packed back to back over the whole b range (merged axes too)
         const bool packed = ta == p->ext_a && p->ss_b == ta &&
                             (p->panel_b1 == 0 || p->panel_ss_b2 == p->panel_b1 * ta);
+        p->panel_aligned = false;
+        p->panel_vec = false;
         if (packed) {
             p->panel_mode = 1;
             p->pitch = 0;
             p->panel_nblk = 0;
+            p->panel_vec = panel_dst_vec(*p, tb, true);
             stage = 16 * ((ta * tb * eb + 30) / 16);
         } else {
             p->panel_mode = 0;
-            p->panel_nblk = panel_blocks_per_row(ta, eb);
+            p->panel_aligned = panel_src_aligned(*p, ta);
+            p->panel_vec = panel_dst_vec(*p, tb, false);
+            p->panel_nblk = p->panel_aligned ? (int)(ta * eb / 16) : panel_blocks_per_row(ta, eb);
             // rows of 1..2 blocks cost up to 32 bytes each: check the ring before the
             // pitch search
             stage = tb * 16 * (p->panel_nblk + 7);
             if (kPanelStages * stage <= kPanelMaxSmem) {
-                p->pitch = panel_pitch((int)ta, (int)tb, eb, p->ss_b, p->panel_b1, p->panel_ss_b2);
+                p->pitch = panel_pitch((int)ta, (int)tb, eb, p->ss_b, p->panel_b1, p->panel_ss_b2,
+                                       p->panel_nblk, p->panel_aligned, p->panel_vec);
                 stage = tb * p->pitch;
             }
         }
@@ -490,7 +550,7 @@ void plan_panel(Plan* p, int tile_bytes) {
     p->panel_stage = (int)stage;
     const int64_t na = (p->ext_a + ta - 1) / ta, nb = (p->ext_b + tb - 1) / tb;
     p->tiles = na * nb * p->batch_total;
-    p->vec_bytes = eb;
+    p->vec_bytes = p->panel_vec ? 16 : eb;
 }
 
 int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
@@ -635,6 +695,9 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         const int64_t tb = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
         p.tiles = ta * tb * p.batch_total;
     } else if (path == TL_PATH_PANEL) {
+        p.src_mis16 = s0 & 15;
+        p.dst_mis16 = d0 & 15;
+        p.panel_elem_stores = (flags & TL_FLAG_PANEL_ELEMENT_STORES) != 0;
         panel_merge_b(&p);
         plan_panel(&p, 0);
     } else if (path == TL_PATH_ROWS) {

@@ -48,6 +48,10 @@ struct Plan {
     int panel_stage = 0;                // PANEL: shared-memory bytes of one ring stage
     int64_t panel_b1 = 0;               // PANEL: inner extent of b when two axes are merged
     int64_t panel_ss_b2 = 0;            // PANEL: src stride of the outer merged axis
+    bool panel_aligned = false;         // PANEL: every src row starts on a 16-byte boundary
+    bool panel_vec = false;             // PANEL: tiles stored as 16-byte dst runs
+    bool panel_elem_stores = false;     // PANEL: 16-byte dst runs declined by the caller
+    int64_t src_mis16 = 0, dst_mis16 = 0;   // base addresses mod 16
     int64_t tiles = 0;
 
     // WARP: tile (innermost suffix of `kept`) + batch of the outer `kept` axes.

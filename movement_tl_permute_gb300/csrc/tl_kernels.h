@@ -165,9 +165,13 @@ struct PanelArgs {
     dev::DivU32 d_tb, d_nblk;    // divisors of the per-tile walks
     dev::DivU32 d_b1;            // b -> (hi, lo) when two axes are merged (b fits 32 bits)
     int32_t merged;              // 1 when b is two merged axes
-    int32_t pad;
+    int32_t aligned;             // kPanelRows: every src row starts on a 16-byte boundary
     dev::DivU32 d_item, d_grp, d_gfull, d_glast;
     dev::DivU32 d_bext[TL_MAX_DIMS];
+    // 16-byte dst runs (vec = 1): dst rows of every tile 16-byte aligned and tb * eb a
+    // multiple of 128; row b of a stage starts at b * vpitch + ((mis0 + b * vdelta) & 15)
+    int32_t vec, vpitch, vdelta, pad;
+    dev::DivU32 d_qb8;           // 8-block groups of one dst row of a tile (tb * eb / 128)
 };
 const void* panel_kernel(int eb);
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,

@@ -516,6 +516,11 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.d_b1 = dev::make_divu32((uint32_t)a.b1);
         a.stage_bytes = p.panel_stage;
         a.d_nblk = dev::make_divu32((uint32_t)(p.panel_nblk > 0 ? p.panel_nblk : 1));
+        a.aligned = p.panel_aligned ? 1 : 0;
+        a.vec = p.panel_vec ? 1 : 0;
+        a.vpitch = p.panel_mode == kPanelRows ? p.pitch : p.tile_cols * eb;
+        a.vdelta = p.panel_mode == kPanelRows && !a.merged ? (int32_t)((p.ss_b * eb) & 15) : 0;
+        a.d_qb8 = dev::make_divu32((uint32_t)std::max<int64_t>(1, (int64_t)p.tile_rows * eb / 128));
         a.tiles_a = (p.ext_a + a.ta - 1) / a.ta;
         a.tiles_b = (p.ext_b + a.tb - 1) / a.tb;
         a.tiles = p.tiles;
@@ -641,6 +646,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     info.pitch = p.pitch;
     info.panel_mode = p.panel_mode;
     info.panel_b1 = (int32_t)p.panel_b1;
+    info.panel_vec = p.panel_vec ? 1 : 0;
     info.tiles = p.tiles;
     int ndev = 0;
     DevInfo d;

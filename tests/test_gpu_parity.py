@@ -215,6 +215,45 @@ def test_panel_path(eb, kib):
         check(shape, ss, ds, eb, "panel", seed=80 + i, src_off=1, dst_off=3, panel_tile_kib=kib)
 
 
+def _panel_vec_cases(eb):
+    v = 16 // eb
+    out = []
+    # odd src row pitch (rows misaligned in the stage), dst rows on 16-byte boundaries
+    out.append(((264, 517), (517, 1), (1, 264)))
+    # padded dst rows whose extent is no multiple of 16 bytes: the last block of each
+    # dst row of a tile is partial
+    out.append(((261, 517), (517, 1), (1, 272)))
+    out.append(((40 * v + 3, 300), (300, 1), (1, 48 * v)))
+    # more than three batch axes, aligned src rows, the short b merged with the next
+    # dst axis (tile rows cross the merge boundary for 2-byte elements)
+    shape = (4 * v, 2, 4, 2, 40, 16 * v)
+    ss, ds = perm_layouts(shape, (5, 3, 1, 4, 2, 0))
+    out.append((shape, ss, ds))
+    # packed src rows (3 interleaved channels -> planes)
+    out.append(((70, 96, 3), (96 * 3, 3, 1), (96, 1, 70 * 96)))
+    return out
+
+
+@pytest.mark.parametrize("eb", [2, 4, 8])
+@pytest.mark.parametrize("kib", [0, 4])
+def test_panel_vector_stores(eb, kib):
+    """Tiles whose dst rows start on 16-byte boundaries are stored as 16-byte runs
+    (read down the stage with the XOR-rotated row order); the same layouts with
+    element stores, and with an unaligned dst, give the same bytes."""
+    for i, (shape, ss, ds) in enumerate(_panel_vec_cases(eb)):
+        plan = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb, path="panel",
+                          panel_tile_kib=kib)
+        assert plan["panel_vec"] == 1, (shape, plan)
+        off = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb, path="panel",
+                         panel_tile_kib=kib, flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
+        assert off["panel_vec"] == 0
+        check(shape, ss, ds, eb, "panel", seed=300 + i, panel_tile_kib=kib)
+        check(shape, ss, ds, eb, "panel", seed=310 + i, src_off=1, panel_tile_kib=kib)
+        check(shape, ss, ds, eb, "panel", seed=320 + i, panel_tile_kib=kib,
+              flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
+        check(shape, ss, ds, eb, "panel", seed=330 + i, dst_off=1, panel_tile_kib=kib)
+
+
 @pytest.mark.parametrize("eb", WIDTHS)
 def test_auto_takes_panel_for_untiled_planes(eb):
     # a 3-channel interleave and an odd-pitch transpose go to the panel kernel

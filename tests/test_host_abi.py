@@ -245,23 +245,35 @@ PANEL_LAYOUTS = [
 ]
 
 
-def _panel_degrees(ta, tb, eb, pitch, row_off):
+def _panel_degrees(ta, tb, eb, pitch, row_off, nblk, aligned, vec):
     """Per-warp bank-conflict degrees (oracle model, hardware mode) of the panel
     kernel's two walks for a block-row layout of byte pitch `pitch`: the copy walk
-    (16-byte blocks, row b at b * pitch) and the store walk (tile element f at
-    a = f // tb, b = f % tb, row b starting (r + row_off(b) * eb) mod 16 bytes into
-    its first block, for every base residue r; row_off(b) is the src element offset
-    of row b)."""
-    nblk = (ta * eb + 30) // 16
+    (16-byte blocks, nblk per row, row b at b * pitch) and the store walk, row b
+    starting (r + row_off(b) * eb) mod 16 bytes into its first block for every base
+    residue r (r = 0 only when every row is aligned); row_off(b) is the src element
+    offset of row b.  Element stores: a warp takes tile elements f at a = f // tb,
+    b = f % tb.  16-byte dst runs: a warp takes 4 dst rows a by 8 blocks q of
+    V = 16 / eb elements, and at step k the lane of block q reads row
+    q * V + (k ^ rot(q)), rot(q) = (q // max(8 // V, 1)) % V."""
     q = pitch // 16
     copy = [L.bank_conflict_degree([(g // nblk) * q + g % nblk
                                     for g in range(g0, min(nblk * tb, g0 + 32))], 16, "hardware")
             for g0 in range(0, nblk * tb, 32)]
     store = []
-    for r in range(0, 16, eb):
+    for r in range(0, 1 if aligned else 16, eb):
+        off = lambda a, b: (b * pitch + ((r + row_off(b) * eb) & 15) + a * eb) // eb
+        if vec:
+            V = 16 // eb
+            qd = max(8 // V, 1)
+            for a0 in range(0, ta, 4):
+                for q0 in range(0, tb // V, 8):
+                    for k in range(V):
+                        lanes = [(a0 + l // 8, q0 + l % 8) for l in range(32)]
+                        offs = [off(a, qq * V + (k ^ ((qq // qd) % V))) for a, qq in lanes if a < ta]
+                        store.append(L.bank_conflict_degree(offs, eb, "hardware"))
+            continue
         for f0 in range(0, ta * tb, 32):
-            offs = [((f % tb) * pitch + ((r + row_off(f % tb) * eb) & 15) + (f // tb) * eb) // eb
-                    for f in range(f0, min(ta * tb, f0 + 32))]
+            offs = [off(f // tb, f % tb) for f in range(f0, min(ta * tb, f0 + 32))]
             store.append(L.bank_conflict_degree(offs, eb, "hardware"))
     return copy, store
 
@@ -273,7 +285,8 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
     16-byte boundary plus the row's own misalignment, so the column-wise store walk
     cannot be conflict-free in general: the padding the planner picks must do no
     worse than no padding, keep the copy walk within 2-way and the store walk within
-    4-way.  Packed src rows are one run: the store walk stays within 2-way."""
+    4-way; with every row aligned and 16-byte dst runs the store walk is
+    conflict-free.  Packed src rows are one run: the store walk stays within 2-way."""
     ss, ds = _perm_layout(shape, perm)
     p = tl.tl_plan(SRC, DST, shape, ss, ds, eb)
     assert p["path"] == "panel"
@@ -287,13 +300,27 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         row_off = lambda b: b * ssb
     n = ta * tb
     if mode == 0:
-        nblk = (ta * eb + 30) // 16
+        # every src row on a 16-byte boundary: base, tile step ta and every src
+        # stride but a's (1) multiples of 16 bytes
+        aligned = SRC % 16 == 0 and (ta * eb) % 16 == 0 and all(
+            (x * eb) % 16 == 0 for x in p["src_str"] if x != 1)
+        # 16-byte dst runs: 2..8-byte elements, whole 128-byte row pieces, every dst
+        # stride but b's (1) a multiple of 16 bytes
+        vec = 2 <= eb <= 8 and (tb * eb) % 128 == 0 and DST % 16 == 0 and all(
+            (x * eb) % 16 == 0 for x in p["dst_str"] if x not in (1, b1))
+        if b1:
+            vec = vec and (ssb * eb) % 16 == 0 and (ssb2 * eb) % 16 == 0
+        assert p["panel_vec"] == int(vec)
+        assert p["vec_bytes"] == (16 if vec else eb)
+        nblk = ta * eb // 16 if aligned else (ta * eb + 30) // 16
         assert pitch % 16 == 0 and 16 * nblk <= pitch < 16 * (nblk + 8)
         assert p["smem_bytes"] == 3 * tb * pitch
-        copy, store = _panel_degrees(ta, tb, eb, pitch, row_off)
-        copy0, store0 = _panel_degrees(ta, tb, eb, 16 * nblk, row_off)
+        copy, store = _panel_degrees(ta, tb, eb, pitch, row_off, nblk, aligned, vec)
+        copy0, store0 = _panel_degrees(ta, tb, eb, 16 * nblk, row_off, nblk, aligned, vec)
         assert sum(copy) + sum(store) <= sum(copy0) + sum(store0)
         assert max(copy) <= 2 and max(store) <= 4
+        if aligned and vec:
+            assert max(store) == 1
     else:
         assert mode == 1 and ssb == ta and p["pitch"] == 0      # packed src rows
         assert p["smem_bytes"] == 3 * 16 * ((n * eb + 30) // 16)

@@ -205,7 +205,8 @@ typedef struct tl_permute_opts {
     int32_t tile_ctas_per_sm;  /* resident CTAs per SM the grid is sized for */
     int32_t tile_l2_promotion; /* L2 fill size of the TMA loads: 64, 128, 256, or -1 = none */
     int32_t tile_rows;    /* tile height in rows of the dst-contiguous axis: 128 or 256
-                             (tile path only; other values select the default) */
+                             on the tile path, 16..1024 on the panel path (where both
+                             plane extents exceed 16); other values select the default */
     int32_t cluster_recv_stages; /* cluster: receive ring depth, 1..8 (staging + receive
                                     slots at most 12) */
     int32_t cluster_consumer_warps; /* cluster: consumer warps per CTA, 4 or 8 */

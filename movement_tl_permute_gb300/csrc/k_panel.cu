@@ -115,6 +115,10 @@ __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
 template <int EB>
 __device__ __forceinline__ void issue(const PanelArgs& a, const PanelTile& ti, uint32_t sb) {
     const uintptr_t base = reinterpret_cast<uintptr_t>(a.src + ti.so * EB);
+    // row b of a block-row stage: b * pitch, plus 16 bytes per V = 16 / EB rows when
+    // the stage is skewed for 16-byte dst runs
+    constexpr uint32_t V = 16 / EB;
+    const uint32_t skew = a.vskew ? 16u : 0u;
     if (a.mode == kPanelRows && a.aligned) {
         // every row starts on a block boundary: nblk blocks per full row, the valid
         // rows only
@@ -123,7 +127,8 @@ __device__ __forceinline__ void issue(const PanelArgs& a, const PanelTile& ti, u
         for (uint32_t g = threadIdx.x; g < n; g += kPanelThreads) {
             const uint32_t b = dev::div_u32(g, a.d_nblk), k = g - b * nblk;
             if (k < blocks)
-                cp_async16(sb + b * pitch + 16 * k, base + (uintptr_t)(row_offset(b, ti, a) * EB) + 16 * k);
+                cp_async16(sb + b * pitch + (b / V) * skew + 16 * k,
+                           base + (uintptr_t)(row_offset(b, ti, a) * EB) + 16 * k);
         }
     } else if (a.mode == kPanelRows) {
         const uint32_t nblk = (uint32_t)a.nblk, n = (uint32_t)a.tb * nblk;
@@ -133,20 +138,14 @@ __device__ __forceinline__ void issue(const PanelArgs& a, const PanelTile& ti, u
             if (b >= ti.vb) continue;
             const uintptr_t row = base + (uintptr_t)(row_offset(b, ti, a) * EB);
             const uint32_t blocks = ((uint32_t)(row & 15) + ti.va * EB + 15) >> 4;
-            if (k < blocks) cp_async16(sb + b * pitch + 16 * k, (row & ~uintptr_t(15)) + 16 * k);
+            if (k < blocks)
+                cp_async16(sb + b * pitch + (b / V) * skew + 16 * k, (row & ~uintptr_t(15)) + 16 * k);
         }
     } else {   // kPanelFlat: rows packed back to back (ss_b == ta == va)
         const uint32_t blocks = ((uint32_t)(base & 15) + ti.vb * (uint32_t)a.ta * EB + 15) >> 4;
         for (uint32_t k = threadIdx.x; k < blocks; k += kPanelThreads)
             cp_async16(sb + 16 * k, (base & ~uintptr_t(15)) + 16 * k);
     }
-}
-
-template <typename T>
-__device__ __forceinline__ void cswap(bool p, T& x, T& y) {
-    const T u = p ? y : x, v = p ? x : y;
-    x = u;
-    y = v;
 }
 
 // V = 16 / EB elements in b order as one 16-byte vector
@@ -165,46 +164,64 @@ __device__ __forceinline__ uint4 pack16(const uint16_t (&v)[8]) {
 // start on 16-byte boundaries and tb * EB is a multiple of 128).  Unit (e, q) is
 // dst row e of the tile, block q of it (elements b = qV .. qV + V - 1, V = 16 / EB).
 // A warp takes 4 rows x 8 blocks, so each of its stores writes four whole 128-byte
-// lines.  The lane of block q reads its V elements down column e of the stage, the
-// k-th from row qV + (k ^ r) with r = (q / max(8 / V, 1)) mod V: the warp's 8 blocks
-// then read rows that differ mod 8 at every step, which an odd row pitch in 16-byte
-// units puts in distinct bank groups (the XOR rotation of the TVM "permute_layout"
-// page, "Algorithm" step 2, applied to the stage; the host's pitch search simulates
-// exactly these reads).  A conditional-swap network restores b order.
+// lines; a thread keeps its block q for the whole tile and walks e, so the V row
+// addresses are computed once.  Block-row stages are skewed: row b starts 16 bytes
+// further per V rows (at b * pitch + 16 * (b / V)), so the 8 blocks of a warp read
+// 8 distinct 16-byte bank groups at every step whatever the pitch (the host's pitch
+// search replays these reads on the bank model of the TVM "permute_layout" page,
+// "Algorithm" step 2).
 template <int EB>
 __device__ __forceinline__ void drain_vec(const PanelArgs& a, const PanelTile& ti,
                                           const uint8_t* st) {
     using T = typename dev::Bits<EB>::T;
-    constexpr uint32_t V = 16 / EB, QD = V >= 8 ? 1 : 8 / V;
+    constexpr uint32_t V = 16 / EB, kWarps = kPanelThreads / 32;
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t qb8 = a.d_qb8.d, units = ((ti.va + 3) >> 2) * qb8;
+    const uint32_t qb8 = (uint32_t)a.qb8;
+    // the warp's 8-block groups (qg, stepping kWarps) and 4-row groups (g4)
+    uint32_t qg0 = warp, g40 = 0, gstep = 1;
+    if (qb8 < kWarps) {
+        const uint32_t per = kWarps / qb8;
+        if (warp >= per * qb8) return;
+        qg0 = warp % qb8;
+        g40 = warp / qb8;
+        gstep = per;
+    }
     const uint32_t mis0 = (uint32_t)(reinterpret_cast<uintptr_t>(a.src + ti.so * EB) & 15);
     const uint32_t P = (uint32_t)a.vpitch, delta = (uint32_t)a.vdelta;
-    uint8_t* dbase = a.dst + ti.dof * EB;
-    for (uint32_t u = warp; u < units; u += kPanelThreads / 32) {
-        const uint32_t g4 = dev::div_u32(u, a.d_qb8), qg = u - g4 * qb8;
-        const uint32_t e = 4 * g4 + (lane >> 3), q = 8 * qg + (lane & 7), b0 = q * V;
-        if (e >= ti.va || b0 >= ti.vb) continue;
-        const uint32_t r = (q / QD) & (V - 1);
-        const uint8_t* col = st + e * EB;
-        T v[V];
+    const uint32_t skew = a.vskew ? 16u : 0u;
+    const int64_t dstep = (int64_t)4 * gstep * a.ds_a * EB;
+    // row addresses as offsets into the dynamic shared memory, so that every read is
+    // a shared-window load
+    extern __shared__ __align__(16) uint8_t smem_rows[];
+    const uint32_t st0 = (uint32_t)(st - smem_rows);
+    for (uint32_t qg = qg0; qg < qb8; qg += kWarps) {
+        const uint32_t q = 8 * qg + (lane & 7), b0 = q * V;
+        if (b0 >= ti.vb) continue;
+        uint32_t ro[V];
 #pragma unroll
         for (uint32_t k = 0; k < V; ++k) {
-            const uint32_t b = b0 + (k ^ r);
-            v[k] = *reinterpret_cast<const T*>(col + b * P + ((mis0 + b * delta) & 15u));
+            const uint32_t b = b0 + k;
+            ro[k] = st0 + b * P + q * skew + ((mis0 + b * delta) & 15u);
         }
-#pragma unroll
-        for (uint32_t lv = 1; lv < V; lv <<= 1)
-#pragma unroll
-            for (uint32_t k = 0; k < V; ++k)
-                if (!(k & lv)) cswap((r & lv) != 0, v[k], v[k | lv]);
-        uint8_t* dp = dbase + ((int64_t)e * a.ds_a + b0) * EB;
+        uint32_t e = 4 * g40 + (lane >> 3);
+        uint8_t* dp = a.dst + (ti.dof + (int64_t)e * a.ds_a + b0) * EB;
         if (b0 + V <= ti.vb) {
-            dev::stg128(dp, pack16(v));
-        } else {
+#pragma unroll 2
+            for (; e < ti.va; e += 4 * gstep, dp += dstep) {
+                T v[V];
 #pragma unroll
-            for (uint32_t k = 0; k < V; ++k)
-                if (b0 + k < ti.vb) *reinterpret_cast<T*>(dp + k * EB) = v[k];
+                for (uint32_t k = 0; k < V; ++k)
+                    v[k] = *reinterpret_cast<const T*>(&smem_rows[ro[k] + e * EB]);
+                dev::stg128(dp, pack16(v));
+            }
+        } else {           // the block holds the last valid rows of a ragged tile
+            for (; e < ti.va; e += 4 * gstep, dp += dstep) {
+#pragma unroll
+                for (uint32_t k = 0; k < V; ++k)
+                    if (b0 + k < ti.vb)
+                        *reinterpret_cast<T*>(dp + k * EB) =
+                            *reinterpret_cast<const T*>(&smem_rows[ro[k] + e * EB]);
+            }
         }
     }
 }
@@ -307,7 +324,7 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
 }
 
 template <int EB>
-__global__ void __launch_bounds__(kPanelThreads) k_panel(const PanelArgs a) {
+__global__ void __launch_bounds__(kPanelThreads, 3) k_panel(const PanelArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const uint32_t sbase = dev::smem_addr(smem);
     const uint32_t stage = (uint32_t)a.stage_bytes;

@@ -72,10 +72,11 @@ constexpr int kPanelStages = 3;
 constexpr int kPanelMaxSmem = 160 * 1024;
 
 // Tile shape and shared-memory layout of the panel path for tiles of about
-// tile_bytes (0: the default size; a tuning option may redo it).  Measured on
+// tile_bytes (0: the default size; tuning options may redo it).  Measured on
 // GB300: 32 KiB tiles for planes with two long extents, 16 KiB when one extent is
 // 16 or less.
-void plan_panel(Plan* p, int tile_bytes);
+// rows > 0 asks for that many rows of b per tile when both extents exceed 16.
+void plan_panel(Plan* p, int tile_bytes, int rows = 0);
 
 // The bank simulator: worst conflict degree of one warp-wide access.
 int bank_degree(int n_lanes, const int64_t* lane_offsets, int elem_bytes, bool hardware);

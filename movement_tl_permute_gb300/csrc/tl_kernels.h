@@ -169,9 +169,11 @@ struct PanelArgs {
     dev::DivU32 d_item, d_grp, d_gfull, d_glast;
     dev::DivU32 d_bext[TL_MAX_DIMS];
     // 16-byte dst runs (vec = 1): dst rows of every tile 16-byte aligned and tb * eb a
-    // multiple of 128; row b of a stage starts at b * vpitch + ((mis0 + b * vdelta) & 15)
-    int32_t vec, vpitch, vdelta, pad;
-    dev::DivU32 d_qb8;           // 8-block groups of one dst row of a tile (tb * eb / 128)
+    // multiple of 128.  Row b of a stage starts at
+    // b * vpitch + (vskew ? 16 * (b / (16 / eb)) : 0) + ((mis0 + b * vdelta) & 15).
+    int32_t vec, vpitch, vdelta, vskew;
+    int32_t qb8;                 // 8-block groups of one dst row of a tile (tb * eb / 128)
+    int32_t pad;
 };
 const void* panel_kernel(int eb);
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,

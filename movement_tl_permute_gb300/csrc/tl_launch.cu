@@ -312,10 +312,13 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
     return l;
 }
 
-// The panel tile size is a tuning option: re-plan the panel layout for it.
+// The panel tile size and height are tuning options: re-plan the panel layout for them.
 void apply_panel_tile(Plan& p, const tl_permute_opts* o) {
-    if (p.path != TL_PATH_PANEL || !o || o->panel_tile_kib < 4 || o->panel_tile_kib > 32) return;
-    plan_panel(&p, o->panel_tile_kib * 1024);
+    if (p.path != TL_PATH_PANEL || !o) return;
+    const bool kib = o->panel_tile_kib >= 4 && o->panel_tile_kib <= 32;
+    const bool rows = o->tile_rows >= 16 && o->tile_rows <= 1024;
+    if (!kib && !rows) return;
+    plan_panel(&p, kib ? o->panel_tile_kib * 1024 : 0, rows ? o->tile_rows : 0);
     if (kPanelStages * p.panel_stage > kPanelMaxSmem) plan_panel(&p, 0);
 }
 
@@ -520,7 +523,8 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.vec = p.panel_vec ? 1 : 0;
         a.vpitch = p.panel_mode == kPanelRows ? p.pitch : p.tile_cols * eb;
         a.vdelta = p.panel_mode == kPanelRows && !a.merged ? (int32_t)((p.ss_b * eb) & 15) : 0;
-        a.d_qb8 = dev::make_divu32((uint32_t)std::max<int64_t>(1, (int64_t)p.tile_rows * eb / 128));
+        a.vskew = a.vec && p.panel_mode == kPanelRows ? 1 : 0;
+        a.qb8 = (int32_t)std::max<int64_t>(1, (int64_t)p.tile_rows * eb / 128);
         a.tiles_a = (p.ext_a + a.ta - 1) / a.ta;
         a.tiles_b = (p.ext_b + a.tb - 1) / a.tb;
         a.tiles = p.tiles;

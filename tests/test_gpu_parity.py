@@ -238,12 +238,14 @@ def _panel_vec_cases(eb):
 @pytest.mark.parametrize("kib", [0, 4])
 def test_panel_vector_stores(eb, kib):
     """Tiles whose dst rows start on 16-byte boundaries are stored as 16-byte runs
-    (read down the stage with the XOR-rotated row order); the same layouts with
-    element stores, and with an unaligned dst, give the same bytes."""
+    (read down a skewed stage); the same layouts with element stores, and with an
+    unaligned dst, give the same bytes.  4-byte elements with src rows off the
+    16-byte grid keep element stores (the faster choice there)."""
     for i, (shape, ss, ds) in enumerate(_panel_vec_cases(eb)):
         plan = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb, path="panel",
                           panel_tile_kib=kib)
-        assert plan["panel_vec"] == 1, (shape, plan)
+        odd_rows = plan["panel_mode"] == 0 and any((x * eb) % 16 for x in ss if x != 1)
+        assert plan["panel_vec"] == (0 if eb == 4 and odd_rows else 1), (shape, plan)
         off = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb, path="panel",
                          panel_tile_kib=kib, flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
         assert off["panel_vec"] == 0

@@ -252,24 +252,24 @@ def _panel_degrees(ta, tb, eb, pitch, row_off, nblk, aligned, vec):
     starting (r + row_off(b) * eb) mod 16 bytes into its first block for every base
     residue r (r = 0 only when every row is aligned); row_off(b) is the src element
     offset of row b.  Element stores: a warp takes tile elements f at a = f // tb,
-    b = f % tb.  16-byte dst runs: a warp takes 4 dst rows a by 8 blocks q of
-    V = 16 / eb elements, and at step k the lane of block q reads row
-    q * V + (k ^ rot(q)), rot(q) = (q // max(8 // V, 1)) % V."""
+    b = f % tb.  16-byte dst runs: rows are skewed by 16 bytes per V = 16 / eb rows,
+    a warp takes 4 dst rows a by 8 blocks q of V elements, and at step k the lane of
+    block q reads row q * V + k."""
     q = pitch // 16
-    copy = [L.bank_conflict_degree([(g // nblk) * q + g % nblk
+    skew = (lambda b: b // (16 // eb)) if vec else (lambda b: 0)
+    copy = [L.bank_conflict_degree([(g // nblk) * q + skew(g // nblk) + g % nblk
                                     for g in range(g0, min(nblk * tb, g0 + 32))], 16, "hardware")
             for g0 in range(0, nblk * tb, 32)]
     store = []
     for r in range(0, 1 if aligned else 16, eb):
-        off = lambda a, b: (b * pitch + ((r + row_off(b) * eb) & 15) + a * eb) // eb
+        off = lambda a, b: (b * pitch + 16 * skew(b) + ((r + row_off(b) * eb) & 15) + a * eb) // eb
         if vec:
             V = 16 // eb
-            qd = max(8 // V, 1)
             for a0 in range(0, ta, 4):
                 for q0 in range(0, tb // V, 8):
                     for k in range(V):
                         lanes = [(a0 + l // 8, q0 + l % 8) for l in range(32)]
-                        offs = [off(a, qq * V + (k ^ ((qq // qd) % V))) for a, qq in lanes if a < ta]
+                        offs = [off(a, qq * V + k) for a, qq in lanes if a < ta]
                         store.append(L.bank_conflict_degree(offs, eb, "hardware"))
             continue
         for f0 in range(0, ta * tb, 32):
@@ -310,11 +310,12 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
             (x * eb) % 16 == 0 for x in p["dst_str"] if x not in (1, b1))
         if b1:
             vec = vec and (ssb * eb) % 16 == 0 and (ssb2 * eb) % 16 == 0
+        vec = vec and not (eb == 4 and not aligned)   # measured: element stores win there
         assert p["panel_vec"] == int(vec)
         assert p["vec_bytes"] == (16 if vec else eb)
         nblk = ta * eb // 16 if aligned else (ta * eb + 30) // 16
         assert pitch % 16 == 0 and 16 * nblk <= pitch < 16 * (nblk + 8)
-        assert p["smem_bytes"] == 3 * tb * pitch
+        assert p["smem_bytes"] == 3 * (tb * pitch + (16 * (tb * eb // 16) if vec else 0))
         copy, store = _panel_degrees(ta, tb, eb, pitch, row_off, nblk, aligned, vec)
         copy0, store0 = _panel_degrees(ta, tb, eb, 16 * nblk, row_off, nblk, aligned, vec)
         assert sum(copy) + sum(store) <= sum(copy0) + sum(store0)

@@ -159,6 +159,13 @@ __device__ __forceinline__ uint4 pack16(const uint16_t (&v)[8]) {
     auto w = [&](int i) { return (uint32_t)v[2 * i] | ((uint32_t)v[2 * i + 1] << 16); };
     return make_uint4(w(0), w(1), w(2), w(3));
 }
+__device__ __forceinline__ uint4 pack16(const uint8_t (&v)[16]) {
+    auto w = [&](int i) {
+        return (uint32_t)v[4 * i] | ((uint32_t)v[4 * i + 1] << 8) |
+               ((uint32_t)v[4 * i + 2] << 16) | ((uint32_t)v[4 * i + 3] << 24);
+    };
+    return make_uint4(w(0), w(1), w(2), w(3));
+}
 
 // Store one landed tile as 16-byte dst runs (used when the dst rows of every tile
 // start on 16-byte boundaries and tb * EB is a multiple of 128).  Unit (e, q) is
@@ -226,14 +233,14 @@ __device__ __forceinline__ void drain_vec(const PanelArgs& a, const PanelTile& t
     }
 }
 
-// Store one landed tile from the stage at `st` to dst, in dst order.
-template <int EB>
+// Store one landed tile from the stage at `st` to dst, in dst order: 16-byte runs
+// (VEC), or element by element (4-byte words for packed rows of 1- and 2-byte
+// elements).
+template <int EB, bool VEC>
 __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, const uint8_t* st) {
-    if constexpr (EB >= 2 && EB <= 8) {
-        if (a.vec) {
-            drain_vec<EB>(a, ti, st);
-            return;
-        }
+    if constexpr (VEC) {
+        drain_vec<EB>(a, ti, st);
+        return;
     }
     using T = typename dev::Bits<EB>::T;
     T* d = reinterpret_cast<T*>(a.dst) + ti.dof;
@@ -323,8 +330,10 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
     }
 }
 
-template <int EB>
-__global__ void __launch_bounds__(kPanelThreads, 3) k_panel(const PanelArgs a) {
+// The two store modes are separate kernels so that each keeps its own register
+// budget (the element-store kernel fits four CTAs per SM).
+template <int EB, bool VEC>
+__global__ void __launch_bounds__(kPanelThreads, VEC ? 3 : 4) k_panel(const PanelArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const uint32_t sbase = dev::smem_addr(smem);
     const uint32_t stage = (uint32_t)a.stage_bytes;
@@ -346,7 +355,7 @@ __global__ void __launch_bounds__(kPanelThreads, 3) k_panel(const PanelArgs a) {
         cp_async_commit();
         cp_async_wait<kPanelStages - 1>();           // tile i has landed (this thread's part)
         __syncthreads();                             // ... and every other thread's part
-        drain<EB>(a, panel_tile(first + i * step, a), smem + slot * stage);
+        drain<EB, VEC>(a, panel_tile(first + i * step, a), smem + slot * stage);
         __syncthreads();                             // stage `slot` may be refilled
         slot = slot + 1 == kPanelStages ? 0 : slot + 1;
         ahead = ahead + 1 == kPanelStages ? 0 : ahead + 1;
@@ -356,25 +365,34 @@ __global__ void __launch_bounds__(kPanelThreads, 3) k_panel(const PanelArgs a) {
 
 }  // namespace
 
-const void* panel_kernel(int eb) {
+const void* panel_kernel(int eb, bool vec) {
     switch (eb) {
-    case 1: return reinterpret_cast<const void*>(&k_panel<1>);
-    case 2: return reinterpret_cast<const void*>(&k_panel<2>);
-    case 4: return reinterpret_cast<const void*>(&k_panel<4>);
-    case 8: return reinterpret_cast<const void*>(&k_panel<8>);
-    default: return reinterpret_cast<const void*>(&k_panel<16>);
+    case 1: return vec ? reinterpret_cast<const void*>(&k_panel<1, true>)
+                       : reinterpret_cast<const void*>(&k_panel<1, false>);
+    case 2: return vec ? reinterpret_cast<const void*>(&k_panel<2, true>)
+                       : reinterpret_cast<const void*>(&k_panel<2, false>);
+    case 4: return vec ? reinterpret_cast<const void*>(&k_panel<4, true>)
+                       : reinterpret_cast<const void*>(&k_panel<4, false>);
+    case 8: return vec ? reinterpret_cast<const void*>(&k_panel<8, true>)
+                       : reinterpret_cast<const void*>(&k_panel<8, false>);
+    default: return reinterpret_cast<const void*>(&k_panel<16, false>);
     }
 }
 
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,
                          bool pdl) {
     const dim3 g(grid), b(kPanelThreads);
+    const bool v = a.vec != 0;
     switch (eb) {
-    case 1: return launch_kernel(k_panel<1>, g, b, smem, st, pdl, a);
-    case 2: return launch_kernel(k_panel<2>, g, b, smem, st, pdl, a);
-    case 4: return launch_kernel(k_panel<4>, g, b, smem, st, pdl, a);
-    case 8: return launch_kernel(k_panel<8>, g, b, smem, st, pdl, a);
-    default: return launch_kernel(k_panel<16>, g, b, smem, st, pdl, a);
+    case 1: return v ? launch_kernel(k_panel<1, true>, g, b, smem, st, pdl, a)
+                     : launch_kernel(k_panel<1, false>, g, b, smem, st, pdl, a);
+    case 2: return v ? launch_kernel(k_panel<2, true>, g, b, smem, st, pdl, a)
+                     : launch_kernel(k_panel<2, false>, g, b, smem, st, pdl, a);
+    case 4: return v ? launch_kernel(k_panel<4, true>, g, b, smem, st, pdl, a)
+                     : launch_kernel(k_panel<4, false>, g, b, smem, st, pdl, a);
+    case 8: return v ? launch_kernel(k_panel<8, true>, g, b, smem, st, pdl, a)
+                     : launch_kernel(k_panel<8, false>, g, b, smem, st, pdl, a);
+    default: return launch_kernel(k_panel<16, false>, g, b, smem, st, pdl, a);
     }
 }
 

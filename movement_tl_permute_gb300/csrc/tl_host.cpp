@@ -443,7 +443,8 @@ int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2, i
 }
 
 // Panel tile of about tile_bytes: a tiny extent is taken whole and the other one
-// fills the tile; otherwise 64 (eb <= 4) or 32 rows of b by the rest of a, or more
+// fills the tile; otherwise 128 (eb = 1), 64 (eb = 2, 4) or 32 rows of b by the rest
+// of a (whole 128-byte dst runs for 1- and 2-byte elements), or more
 // rows when a runs out; no tile side exceeds its extent.  64 rows of 4-byte
 // elements (256 dst bytes per tile row) measured 6.0 against 4.5 TB/s for 32 rows on
 // fp32 transposes whose dst rows are not 16-byte aligned (half as many tile edges
@@ -485,17 +486,19 @@ bool panel_src_aligned(const Plan& p, int64_t ta) {
     return ok;
 }
 
-// 16-byte dst runs: 2-, 4- or 8-byte elements, tb * eb a multiple of 128 (whole
+// 16-byte dst runs: 1-, 2-, 4- or 8-byte elements, tb * eb a multiple of 128 (whole
 // 8-block groups), every dst row of every tile on a 16-byte boundary, and a row
 // misalignment in the stage that follows b linearly (packed rows, one b axis, or
 // merged axes whose src strides are multiples of 16 bytes).  Measured on GB300:
 // 4-byte elements whose src rows are not 16-byte aligned store faster element by
-// element (6.2 against 5.7 TB/s on odd-pitch fp32 transposes); the other layouts
-// gain from the runs (by up to 30 % on 2-byte elements and packed channels).
+// element (6.2 against 5.7 TB/s on odd-pitch fp32 transposes), and packed 1-byte
+// rows keep the kernel's 4-byte word stores (4.8 against 3.6 TB/s on 3 channels);
+// the other layouts gain from the runs (by up to 30 % on 2-byte elements and
+// packed 2- and 4-byte channels, 64 % on 1-byte transposes).
 bool panel_dst_vec(const Plan& p, int64_t tb, bool packed, bool aligned) {
     const int eb = p.eb;
-    if (p.panel_elem_stores || eb < 2 || eb > 8 || (tb * eb) % 128 != 0) return false;
-    if (eb == 4 && !packed && !aligned) return false;
+    if (p.panel_elem_stores || eb > 8 || (tb * eb) % 128 != 0) return false;
+    if ((eb == 4 && !packed && !aligned) || (eb == 1 && packed)) return false;
     bool ok = p.dst_mis16 == 0 && (p.ds_a * eb) % 16 == 0;
     for (int i = 0; i < p.batch.n; ++i) ok = ok && (p.batch.ds[i] * eb) % 16 == 0;
     if (p.panel_b1 > 0 && !packed)
@@ -510,7 +513,7 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
     const bool tiny = p->ext_a <= 16 || p->ext_b <= 16;
     if (tile_bytes <= 0) tile_bytes = tiny ? 16384 : 32768;
     const int64_t E = tile_bytes / eb;
-    const int64_t ru = eb == 2 ? 64 : 32;   // rows of b: whole 128-byte dst runs for 2-byte elements
+    const int64_t ru = std::max(32, 128 / eb);   // rows of b: whole 128-byte dst runs
     int64_t ta, tb;
     if (p->ext_b <= 16) {
         tb = p->ext_b;
@@ -519,7 +522,7 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
         ta = p->ext_a;
         tb = std::min(round_up((E + ta - 1) / ta, ru), p->ext_b);
     } else {
-        tb = std::min<int64_t>(rows > 0 ? rows : eb <= 4 ? 64 : 32, p->ext_b);
+        tb = std::min<int64_t>(rows > 0 ? rows : eb == 1 ? 128 : eb <= 4 ? 64 : 32, p->ext_b);
         ta = std::max<int64_t>(1, std::min(E / tb, p->ext_a));
         if (ta * tb < E)            // a short a extent: the tile grows along b instead
             tb = std::min(round_up((E + ta - 1) / ta, ru), p->ext_b);

@@ -175,7 +175,7 @@ struct PanelArgs {
     int32_t qb8;                 // 8-block groups of one dst row of a tile (tb * eb / 128)
     int32_t pad;
 };
-const void* panel_kernel(int eb);
+const void* panel_kernel(int eb, bool vec);   // vec: the 16-byte dst run kernel
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,
                          bool pdl);
 

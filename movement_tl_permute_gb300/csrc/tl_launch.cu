@@ -140,10 +140,11 @@ int get_device_info(DevInfo* out) {
                             tile_smem_bytes(st, rows)) != cudaSuccess)
                         return TL_ERR_CUDA;
             }
-            if (cudaFuncSetAttribute(panel_kernel(1 << i),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kPanelMaxSmem) != cudaSuccess)
-                return TL_ERR_CUDA;
+            for (int v = 0; v < 2; ++v)
+                if (cudaFuncSetAttribute(panel_kernel(1 << i, v != 0),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPanelMaxSmem) != cudaSuccess)
+                    return TL_ERR_CUDA;
             // The cluster variant is optional: if its set-up fails it is sized
             // conservatively (one CTA per SM) and the error is cleared.
             for (int h = 0; h < 2; ++h) {
@@ -290,7 +291,8 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         l.smem = kPanelStages * p.panel_stage;   // <= kPanelMaxSmem for tiles of <= 32 KiB
         if (sms) {
             int per_sm = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, panel_kernel(p.eb),
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm,
+                                                              panel_kernel(p.eb, p.panel_vec),
                                                               kPanelThreads, l.smem) !=
                     cudaSuccess ||
                 per_sm < 1) {

@@ -219,14 +219,14 @@ def _panel_vec_cases(eb):
     v = 16 // eb
     out = []
     # odd src row pitch (rows misaligned in the stage), dst rows on 16-byte boundaries
-    out.append(((264, 517), (517, 1), (1, 264)))
+    out.append(((272, 517), (517, 1), (1, 272)))
     # padded dst rows whose extent is no multiple of 16 bytes: the last block of each
     # dst row of a tile is partial
     out.append(((261, 517), (517, 1), (1, 272)))
     out.append(((40 * v + 3, 300), (300, 1), (1, 48 * v)))
     # more than three batch axes, aligned src rows, the short b merged with the next
     # dst axis (tile rows cross the merge boundary for 2-byte elements)
-    shape = (4 * v, 2, 4, 2, 40, 16 * v)
+    shape = (min(4 * v, 32), 2, 4, 2, 40, 16 * v)
     ss, ds = perm_layouts(shape, (5, 3, 1, 4, 2, 0))
     out.append((shape, ss, ds))
     # packed src rows (3 interleaved channels -> planes)
@@ -234,18 +234,20 @@ def _panel_vec_cases(eb):
     return out
 
 
-@pytest.mark.parametrize("eb", [2, 4, 8])
+@pytest.mark.parametrize("eb", [1, 2, 4, 8])
 @pytest.mark.parametrize("kib", [0, 4])
 def test_panel_vector_stores(eb, kib):
     """Tiles whose dst rows start on 16-byte boundaries are stored as 16-byte runs
     (read down a skewed stage); the same layouts with element stores, and with an
     unaligned dst, give the same bytes.  4-byte elements with src rows off the
-    16-byte grid keep element stores (the faster choice there)."""
+    16-byte grid, and packed 1-byte rows, keep their element and word stores (the
+    faster choice there)."""
     for i, (shape, ss, ds) in enumerate(_panel_vec_cases(eb)):
         plan = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb, path="panel",
                           panel_tile_kib=kib)
         odd_rows = plan["panel_mode"] == 0 and any((x * eb) % 16 for x in ss if x != 1)
-        assert plan["panel_vec"] == (0 if eb == 4 and odd_rows else 1), (shape, plan)
+        keep = (eb == 4 and odd_rows) or (eb == 1 and plan["panel_mode"] == 1)
+        assert plan["panel_vec"] == (0 if keep else 1), (shape, plan)
         off = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb, path="panel",
                          panel_tile_kib=kib, flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
         assert off["panel_vec"] == 0

@@ -304,9 +304,9 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         # stride but a's (1) multiples of 16 bytes
         aligned = SRC % 16 == 0 and (ta * eb) % 16 == 0 and all(
             (x * eb) % 16 == 0 for x in p["src_str"] if x != 1)
-        # 16-byte dst runs: 2..8-byte elements, whole 128-byte row pieces, every dst
+        # 16-byte dst runs: 1..8-byte elements, whole 128-byte row pieces, every dst
         # stride but b's (1) a multiple of 16 bytes
-        vec = 2 <= eb <= 8 and (tb * eb) % 128 == 0 and DST % 16 == 0 and all(
+        vec = eb <= 8 and (tb * eb) % 128 == 0 and DST % 16 == 0 and all(
             (x * eb) % 16 == 0 for x in p["dst_str"] if x not in (1, b1))
         if b1:
             vec = vec and (ssb * eb) % 16 == 0 and (ssb2 * eb) % 16 == 0
@@ -325,6 +325,10 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
     else:
         assert mode == 1 and ssb == ta and p["pitch"] == 0      # packed src rows
         assert p["smem_bytes"] == 3 * 16 * ((n * eb + 30) // 16)
+        # 16-byte dst runs for 2..8-byte elements (1-byte ones keep word stores)
+        vec = 2 <= eb <= 8 and (tb * eb) % 128 == 0 and DST % 16 == 0 and all(
+            (x * eb) % 16 == 0 for x in p["dst_str"] if x not in (1, b1))
+        assert p["panel_vec"] == int(vec)
         for f0 in range(0, n, 32):
             offs = [(f % tb) * ta + f // tb for f in range(f0, min(n, f0 + 32))]
             assert L.bank_conflict_degree(offs, eb, "hardware") <= 2

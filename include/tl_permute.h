@@ -210,7 +210,7 @@ typedef struct tl_permute_opts {
     int32_t cluster_recv_stages; /* cluster: receive ring depth, 1..8 (staging + receive
                                     slots at most 12) */
     int32_t cluster_consumer_warps; /* cluster: consumer warps per CTA, 4 or 8 */
-    int32_t panel_tile_kib;       /* panel path: tile size, 4..32 KiB (default 32, or 16
+    int32_t panel_tile_kib;       /* panel path: tile size, 4..32 KiB (default 32, or 24
                                      with an extent of 16 or less) */
 } tl_permute_opts;
 
@@ -244,7 +244,8 @@ typedef struct tl_plan_info {
                                       panel_b1) and the next dst axis are walked as one */
     int32_t panel_vec;             /* panel path: 1 when tiles are stored as 16-byte dst
                                       runs, 0 element by element */
-    int32_t reserved;
+    int32_t panel_wrot;            /* panel path, packed rows stored as 4-byte words: the
+                                      lanes' read rotation, shift | multiplier << 8 */
 } tl_plan_info;
 
 TL_API int tl_plan(const void *src, const void *dst, int ndim, const int64_t *shape,

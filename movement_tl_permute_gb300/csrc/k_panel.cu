@@ -253,11 +253,15 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
         if (!rows) {
             // Packed src rows (a short a axis, such as interleaved channels): each dst
             // row a gets its run of b in 4-byte words, a lane packing 4 / EB elements
-            // that sit ta elements apart in the stage (lanes 4 * ta bytes apart: odd
-            // or small word strides, so the byte reads spread over the banks).  The
-            // elements before the first 4-byte boundary of the row and after the last
-            // one are stored singly.
+            // that sit ta elements apart in the stage (lanes 4 * ta bytes apart).  An
+            // even ta puts lanes on the same banks, so lane l reads its k-th element
+            // as element (k + wrot_m * (l >> wrot_s)) mod (4 / EB) of its word, the
+            // rotation picked on the host by simulating the banks (the XOR rotation
+            // of the TVM "permute_layout" page, "Algorithm" step 2, as a modular
+            // one).  The elements before the first 4-byte boundary of the row and
+            // after the last one are stored singly.
             constexpr uint32_t V = 4 / EB;
+            const uint32_t rot = (uint32_t)a.wrot_m * ((threadIdx.x & 31) >> a.wrot_s);
             auto elem = [&](uint32_t b, uint32_t e) {
                 return *reinterpret_cast<const T*>(st + mis0 + (b * ta + e) * EB);
             };
@@ -269,12 +273,24 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
                 if (threadIdx.x < head) drow[threadIdx.x] = elem(threadIdx.x, e);
                 if (tail + threadIdx.x < ti.vb) drow[tail + threadIdx.x] = elem(tail + threadIdx.x, e);
                 uint32_t* wrow = reinterpret_cast<uint32_t*>(drow + head);
-                for (uint32_t w = threadIdx.x; w < nw; w += kPanelThreads) {
-                    uint32_t word = 0;
+                if (a.wrot_m == 0) {         // no rotation: constant element positions
+                    for (uint32_t w = threadIdx.x; w < nw; w += kPanelThreads) {
+                        uint32_t word = 0;
 #pragma unroll
-                    for (uint32_t k = 0; k < V; ++k)
-                        word |= (uint32_t)elem(head + w * V + k, e) << (8 * EB * k);
-                    wrow[w] = word;
+                        for (uint32_t k = 0; k < V; ++k)
+                            word |= (uint32_t)elem(head + w * V + k, e) << (8 * EB * k);
+                        wrow[w] = word;
+                    }
+                } else {
+                    for (uint32_t w = threadIdx.x; w < nw; w += kPanelThreads) {
+                        uint32_t word = 0;
+#pragma unroll
+                        for (uint32_t k = 0; k < V; ++k) {
+                            const uint32_t kk = (k + rot) & (V - 1);
+                            word |= (uint32_t)elem(head + w * V + kk, e) << (8 * EB * kk);
+                        }
+                        wrow[w] = word;
+                    }
                 }
             }
             return;

@@ -353,7 +353,10 @@ int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 // (a = f / tb, b = f % tb).  16-byte dst runs (vec): rows are skewed (row b at
 // b * pitch + 16 * (b / V), V = 16 / eb) and a warp takes 4 rows a by 8 blocks q;
 // at step k lane (a, q) reads row b = qV + k, the reads of the panel kernel's
-// drain_vec.  The first pitch with the lowest summed degree wins.
+// drain_vec.  Among the pitches with the lowest summed degree of the store walk the
+// narrowest whose copy walk stays within 2-way wins (stage capacity decides the
+// bytes in flight, which bound this kernel, more than conflicts among the copy
+// walk's asynchronous writes), else the one with the lowest copy-walk degree.
 struct PanelMemo {
     int ta, tb, eb, pitch;
     int64_t ssb, b1, ssb2;
@@ -390,17 +393,24 @@ int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2, i
     const int64_t qb8 = vec ? (int64_t)tb * eb / 128 : 1;
     auto skew = [&](int64_t b) { return vec ? b / V : 0; };          // 16-byte units
     const int64_t units = vec ? (int64_t)((ta + 3) / 4) * qb8 : 0;
-    int best = 16 * nblk;
-    int64_t best_cost = -1;
+    struct Cand {
+        int pitch;
+        int64_t store, copy;
+        int copy_max;
+    };
+    std::vector<Cand> cands;
     for (int64_t q = nblk; q < nblk + 8; ++q) {
         const int64_t pitch = 16 * q;
-        int64_t cost = 0, ideal = 0;
-        for (int64_t g0 = 0; g0 < std::min(n_copy, samples); g0 += 32, ++ideal) {
+        int64_t copy = 0, store = 0, ideal_copy = 0, ideal_store = 0;
+        int copy_max = 0;
+        for (int64_t g0 = 0; g0 < std::min(n_copy, samples); g0 += 32, ++ideal_copy) {
             int64_t o[32];
             int m = 0;
             for (int64_t g = g0; g < g0 + 32 && g < n_copy; ++g, ++m)
                 o[m] = (g / nblk) * q + skew(g / nblk) + g % nblk;   // 16-byte units
-            cost += bank_degree(m, o, 16, true);
+            const int d = bank_degree(m, o, 16, true);
+            copy += d;
+            copy_max = std::max(copy_max, d);
         }
         for (int r = 0; r < (aligned ? 1 : 16); r += eb) {
             auto off = [&](int64_t a, int64_t b) {
@@ -410,36 +420,101 @@ int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2, i
             if (vec) {
                 for (int64_t u = 0; u < std::min(units, samples / 32); ++u) {
                     const int64_t g4 = u / qb8, qg = u % qb8;
-                    for (int k = 0; k < V; ++k, ++ideal) {
+                    for (int k = 0; k < V; ++k, ++ideal_store) {
                         int64_t o[32];
                         for (int l = 0; l < 32; ++l) {
                             const int64_t a = 4 * g4 + l / 8, qq = 8 * qg + l % 8;
                             const int64_t b = qq * V + k;
                             o[l] = a < ta ? off(a, b) : -1;
                         }
-                        cost += bank_degree(32, o, eb, true);
+                        store += bank_degree(32, o, eb, true);
                     }
                 }
                 continue;
             }
-            for (int64_t f0 = 0; f0 < std::min(n_store, samples); f0 += 32, ++ideal) {
+            for (int64_t f0 = 0; f0 < std::min(n_store, samples); f0 += 32, ++ideal_store) {
                 int64_t o[32];
                 int m = 0;
                 for (int64_t f = f0; f < f0 + 32 && f < n_store; ++f, ++m)
                     o[m] = off(f / tb, f % tb);
-                cost += bank_degree(m, o, eb, true);
+                store += bank_degree(m, o, eb, true);
             }
         }
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = (int)pitch;
+        cands.push_back({(int)pitch, store, copy, copy_max});
+        if (store == ideal_store && copy == ideal_copy) break;   // degree 1 everywhere
+    }
+    int64_t min_store = cands[0].store;
+    for (const Cand& c : cands) min_store = std::min(min_store, c.store);
+    int best = -1;
+    int64_t best_copy = -1;
+    for (const Cand& c : cands) {
+        if (c.store != min_store) continue;
+        if (c.copy_max <= 2) {
+            best = c.pitch;
+            break;
         }
-        if (best_cost == ideal) break;   // degree 1 everywhere
+        if (best_copy < 0 || c.copy < best_copy) {
+            best_copy = c.copy;
+            best = c.pitch;
+        }
     }
     std::lock_guard<std::mutex> lk(g_panel_memo_mu);
     if (g_panel_memo.size() >= 64) g_panel_memo.erase(g_panel_memo.begin());
     g_panel_memo.push_back({ta, tb, eb, best, ssb_k, b1, ssb2, nblk, (int)aligned, (int)vec});
     return best;
+}
+
+// Word-store rotation for packed rows of 1- and 2-byte elements (the panel
+// kernel's word walk): lane l of a warp packs word w = l of a dst row, reading its
+// k-th element from stage element ((w * V + k') * ta + e), V = 4 / eb,
+// k' = (k + m * (l >> s)) mod V.  Every (s, m) is simulated on the bank model
+// (hardware mode) for the tile's ta, every dst row e of the first four, every step k
+// and every start of the run within a 4-byte word; the lowest summed degree wins, the
+// unrotated walk (m = 0) on ties.
+// Worst bank-conflict degree of the 16-byte run walk over packed rows (stage
+// element (b * ta + e), a warp taking 4 rows e by 8 blocks q, lane (e, q) reading
+// b = qV + k at step k), over every start of the run within a 16-byte block.
+int panel_packed_vec_degree(int ta, int eb) {
+    const int V = 16 / eb;
+    int worst = 0;
+    for (int r = 0; r < V; ++r)
+        for (int k = 0; k < V; ++k) {
+            int64_t o[32];
+            for (int l = 0; l < 32; ++l) {
+                const int e = l / 8, q = l % 8;
+                o[l] = e < ta ? (int64_t)(q * V + k) * ta + e + r : -1;
+            }
+            worst = std::max(worst, bank_degree(32, o, eb, true));
+        }
+    return worst;
+}
+
+void panel_word_rotation(int ta, int eb, int* rs, int* rm) {
+    const int V = 4 / eb;
+    int64_t best = -1;
+    *rs = 0;
+    *rm = 0;
+    for (int m = 0; m < V; ++m) {
+        for (int sh = 0; sh <= 4; ++sh) {
+            if (m == 0 && sh > 0) break;
+            int64_t cost = 0;
+            for (int r = 0; r < V; ++r)
+                for (int e = 0; e < std::min(ta, 4); ++e)
+                    for (int k = 0; k < V; ++k) {
+                        int64_t o[32];
+                        for (int l = 0; l < 32; ++l) {
+                            const int kk = (k + m * (l >> sh)) & (V - 1);
+                            o[l] = (int64_t)(l * V + kk) * ta + e + r;
+                        }
+                        cost += bank_degree(32, o, eb, true);
+                    }
+            if (best < 0 || cost < best) {
+                best = cost;
+                *rs = sh;
+                *rm = m;
+            }
+        }
+    }
 }
 
 // Panel tile of about tile_bytes: a tiny extent is taken whole and the other one
@@ -511,7 +586,7 @@ bool panel_dst_vec(const Plan& p, int64_t tb, bool packed, bool aligned) {
 void plan_panel(Plan* p, int tile_bytes, int rows) {
     const int eb = p->eb;
     const bool tiny = p->ext_a <= 16 || p->ext_b <= 16;
-    if (tile_bytes <= 0) tile_bytes = tiny ? 16384 : 32768;
+    if (tile_bytes <= 0) tile_bytes = tiny ? 24576 : 32768;
     const int64_t E = tile_bytes / eb;
     const int64_t ru = std::max(32, 128 / eb);   // rows of b: whole 128-byte dst runs
     int64_t ta, tb;
@@ -531,27 +606,38 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
     for (;;) {
         p->tile_cols = (int)ta;
         p->tile_rows = (int)tb;
-        // src rows packed back to back over the whole b range (merged axes too)
+        // src rows packed back to back over the whole b range (merged axes too);
+        // packed rows that are whole 16-byte blocks on the 16-byte grid are staged
+        // as block rows instead, whose skewed layout the 16-byte run walk reads
+        // without bank conflicts
         const bool packed = ta == p->ext_a && p->ss_b == ta &&
-                            (p->panel_b1 == 0 || p->panel_ss_b2 == p->panel_b1 * ta);
+                            (p->panel_b1 == 0 || p->panel_ss_b2 == p->panel_b1 * ta) &&
+                            !((ta * eb) % 16 == 0 && panel_src_aligned(*p, ta) &&
+                              panel_dst_vec(*p, tb, false, true));
         p->panel_aligned = false;
         p->panel_vec = false;
+        p->panel_wrot_s = p->panel_wrot_m = 0;
         if (packed) {
             p->panel_mode = 1;
             p->pitch = 0;
             p->panel_nblk = 0;
             p->panel_vec = panel_dst_vec(*p, tb, true, false);
+            // 2-byte runs over packed rows whose reads collide on the banks keep the
+            // word stores (with their rotation) instead
+            if (eb == 2 && p->panel_vec && panel_packed_vec_degree((int)ta, eb) > 2)
+                p->panel_vec = false;
+            if (eb < 4 && !p->panel_vec)
+                panel_word_rotation((int)ta, eb, &p->panel_wrot_s, &p->panel_wrot_m);
             stage = 16 * ((ta * tb * eb + 30) / 16);
         } else {
             p->panel_mode = 0;
             p->panel_aligned = panel_src_aligned(*p, ta);
             p->panel_vec = panel_dst_vec(*p, tb, false, p->panel_aligned);
             p->panel_nblk = p->panel_aligned ? (int)(ta * eb / 16) : panel_blocks_per_row(ta, eb);
-            // rows of 1..2 blocks cost up to 32 bytes each: check the ring before the
-            // pitch search
-            // skewed rows for 16-byte dst runs: 16 more bytes per 16 / eb rows
+            // skewed rows for 16-byte dst runs: 16 more bytes per 16 / eb rows; the
+            // pitch search runs when at least its narrowest pitch fits
             const int64_t skew = p->panel_vec ? 16 * (tb / (16 / eb)) : 0;
-            stage = tb * 16 * (p->panel_nblk + 7) + skew;
+            stage = tb * 16 * p->panel_nblk + skew;
             if (kPanelStages * stage <= kPanelMaxSmem) {
                 p->pitch = panel_pitch((int)ta, (int)tb, eb, p->ss_b, p->panel_b1, p->panel_ss_b2,
                                        p->panel_nblk, p->panel_aligned, p->panel_vec);

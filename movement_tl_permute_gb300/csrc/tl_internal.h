@@ -52,6 +52,7 @@ struct Plan {
     bool panel_vec = false;             // PANEL: tiles stored as 16-byte dst runs
     bool panel_elem_stores = false;     // PANEL: 16-byte dst runs declined by the caller
     int64_t src_mis16 = 0, dst_mis16 = 0;   // base addresses mod 16
+    int panel_wrot_s = 0, panel_wrot_m = 0; // PANEL: word-store rotation (packed rows, eb < 4)
     int64_t tiles = 0;
 
     // WARP: tile (innermost suffix of `kept`) + batch of the outer `kept` axes.
@@ -73,8 +74,8 @@ constexpr int kPanelMaxSmem = 160 * 1024;
 
 // Tile shape and shared-memory layout of the panel path for tiles of about
 // tile_bytes (0: the default size; tuning options may redo it).  Measured on
-// GB300: 32 KiB tiles for planes with two long extents, 16 KiB when one extent is
-// 16 or less.
+// GB300: 32 KiB tiles for planes with two long extents, 24 KiB when one extent is
+// 16 or less (interleaved channels: 5.5-6.1 TB/s against 4.8-5.5 with 16 KiB).
 // rows > 0 asks for that many rows of b per tile when both extents exceed 16.
 void plan_panel(Plan* p, int tile_bytes, int rows = 0);
 

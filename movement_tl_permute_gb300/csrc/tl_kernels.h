@@ -173,6 +173,9 @@ struct PanelArgs {
     // b * vpitch + (vskew ? 16 * (b / (16 / eb)) : 0) + ((mis0 + b * vdelta) & 15).
     int32_t vec, vpitch, vdelta, vskew;
     int32_t qb8;                 // 8-block groups of one dst row of a tile (tb * eb / 128)
+    // packed rows of 1- and 2-byte elements stored as words: lane l reads the k-th
+    // element of its word as (k + wrot_m * (l >> wrot_s)) mod (4 / eb)
+    int32_t wrot_s, wrot_m;
     int32_t pad;
 };
 const void* panel_kernel(int eb, bool vec);   // vec: the 16-byte dst run kernel

@@ -527,6 +527,8 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.vdelta = p.panel_mode == kPanelRows && !a.merged ? (int32_t)((p.ss_b * eb) & 15) : 0;
         a.vskew = a.vec && p.panel_mode == kPanelRows ? 1 : 0;
         a.qb8 = (int32_t)std::max<int64_t>(1, (int64_t)p.tile_rows * eb / 128);
+        a.wrot_s = p.panel_wrot_s;
+        a.wrot_m = p.panel_wrot_m;
         a.tiles_a = (p.ext_a + a.ta - 1) / a.ta;
         a.tiles_b = (p.ext_b + a.tb - 1) / a.tb;
         a.tiles = p.tiles;
@@ -653,6 +655,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     info.panel_mode = p.panel_mode;
     info.panel_b1 = (int32_t)p.panel_b1;
     info.panel_vec = p.panel_vec ? 1 : 0;
+    info.panel_wrot = p.panel_wrot_s | (p.panel_wrot_m << 8);
     info.tiles = p.tiles;
     int ndev = 0;
     DevInfo d;

@@ -283,10 +283,10 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
     """The shared-memory layout the planner picks for the panel kernel, replayed
     through the oracle's bank model.  Rows copied as 16-byte blocks start on a
     16-byte boundary plus the row's own misalignment, so the column-wise store walk
-    cannot be conflict-free in general: the padding the planner picks must do no
-    worse than no padding, keep the copy walk within 2-way and the store walk within
-    4-way; with every row aligned and 16-byte dst runs the store walk is
-    conflict-free.  Packed src rows are one run: the store walk stays within 2-way."""
+    cannot be conflict-free in general: the padding the planner picks must give a
+    store walk no worse than no padding, keep the copy walk within 2-way and the
+    store walk within 4-way; with every row aligned and 16-byte dst runs the store
+    walk is conflict-free.  Packed src rows are one run: the store walk stays within 2-way."""
     ss, ds = _perm_layout(shape, perm)
     p = tl.tl_plan(SRC, DST, shape, ss, ds, eb)
     assert p["path"] == "panel"
@@ -318,8 +318,8 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         assert p["smem_bytes"] == 3 * (tb * pitch + (16 * (tb * eb // 16) if vec else 0))
         copy, store = _panel_degrees(ta, tb, eb, pitch, row_off, nblk, aligned, vec)
         copy0, store0 = _panel_degrees(ta, tb, eb, 16 * nblk, row_off, nblk, aligned, vec)
-        assert sum(copy) + sum(store) <= sum(copy0) + sum(store0)
-        assert max(copy) <= 2 and max(store) <= 4
+        assert sum(store) <= sum(store0)        # the store walk first ...
+        assert max(copy) <= 2 and max(store) <= 4   # ... then a copy walk within 2-way
         if aligned and vec:
             assert max(store) == 1
     else:

@@ -489,6 +489,23 @@ int panel_packed_vec_degree(int ta, int eb) {
     return worst;
 }
 
+// 16-byte runs over packed rows (a short a axis of ta elements): a warp's 32 lanes
+// take 4 rows a by 8 blocks, so rows beyond ta leave lanes idle.  Measured on GB300
+// (interleaved channels -> planes, 2..7 channels): 1-byte rows keep the word
+// stores; 2-byte rows take the runs with at least 4 rows, 3 of 4 lanes busy and
+// reads within 2-way conflicts (word stores are faster otherwise: 6.0 against 3.3
+// TB/s at 2 channels); 4-byte rows take them but for 2 channels; 8-byte rows with 3
+// of 4 lanes busy.
+bool panel_packed_vec_ok(int ta, int eb) {
+    const bool busy = 4 * ta >= 3 * (4 * ((ta + 3) / 4));
+    switch (eb) {
+    case 1: return false;
+    case 2: return ta >= 4 && busy && panel_packed_vec_degree(ta, eb) <= 2;
+    case 4: return ta != 2;
+    default: return busy;
+    }
+}
+
 void panel_word_rotation(int ta, int eb, int* rs, int* rm) {
     const int V = 4 / eb;
     int64_t best = -1;
@@ -566,14 +583,13 @@ bool panel_src_aligned(const Plan& p, int64_t ta) {
 // misalignment in the stage that follows b linearly (packed rows, one b axis, or
 // merged axes whose src strides are multiples of 16 bytes).  Measured on GB300:
 // 4-byte elements whose src rows are not 16-byte aligned store faster element by
-// element (6.2 against 5.7 TB/s on odd-pitch fp32 transposes), and packed 1-byte
-// rows keep the kernel's 4-byte word stores (4.8 against 3.6 TB/s on 3 channels);
-// the other layouts gain from the runs (by up to 30 % on 2-byte elements and
-// packed 2- and 4-byte channels, 64 % on 1-byte transposes).
+// element (6.2 against 5.7 TB/s on odd-pitch fp32 transposes); the other block-row
+// layouts gain from the runs (by up to 30 % on 2-byte elements, 64 % on 1-byte
+// transposes).  Packed rows are decided by panel_packed_vec_ok as well.
 bool panel_dst_vec(const Plan& p, int64_t tb, bool packed, bool aligned) {
     const int eb = p.eb;
     if (p.panel_elem_stores || eb > 8 || (tb * eb) % 128 != 0) return false;
-    if ((eb == 4 && !packed && !aligned) || (eb == 1 && packed)) return false;
+    if (eb == 4 && !packed && !aligned) return false;
     bool ok = p.dst_mis16 == 0 && (p.ds_a * eb) % 16 == 0;
     for (int i = 0; i < p.batch.n; ++i) ok = ok && (p.batch.ds[i] * eb) % 16 == 0;
     if (p.panel_b1 > 0 && !packed)
@@ -610,9 +626,12 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
         // packed rows that are whole 16-byte blocks on the 16-byte grid are staged
         // as block rows instead, whose skewed layout the 16-byte run walk reads
         // without bank conflicts
-        const bool packed = ta == p->ext_a && p->ss_b == ta &&
-                            (p->panel_b1 == 0 || p->panel_ss_b2 == p->panel_b1 * ta) &&
-                            !((ta * eb) % 16 == 0 && panel_src_aligned(*p, ta) &&
+        // (rows of whole blocks leave no lane idle when 4 rows a fill a warp's rows)
+        const bool packed_rows = ta == p->ext_a && p->ss_b == ta &&
+                                 (p->panel_b1 == 0 || p->panel_ss_b2 == p->panel_b1 * ta);
+        const bool packed_vec = packed_rows && panel_packed_vec_ok((int)ta, eb);
+        const bool packed = packed_rows &&
+                            !((ta * eb) % 16 == 0 && ta % 4 == 0 && panel_src_aligned(*p, ta) &&
                               panel_dst_vec(*p, tb, false, true));
         p->panel_aligned = false;
         p->panel_vec = false;
@@ -621,11 +640,7 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
             p->panel_mode = 1;
             p->pitch = 0;
             p->panel_nblk = 0;
-            p->panel_vec = panel_dst_vec(*p, tb, true, false);
-            // 2-byte runs over packed rows whose reads collide on the banks keep the
-            // word stores (with their rotation) instead
-            if (eb == 2 && p->panel_vec && panel_packed_vec_degree((int)ta, eb) > 2)
-                p->panel_vec = false;
+            p->panel_vec = packed_vec && panel_dst_vec(*p, tb, true, false);
             if (eb < 4 && !p->panel_vec)
                 panel_word_rotation((int)ta, eb, &p->panel_wrot_s, &p->panel_wrot_m);
             stage = 16 * ((ta * tb * eb + 30) / 16);

@@ -188,8 +188,9 @@ def _panel_cases(eb):
     # odd row pitches with ragged tiles on both sides
     for rows, cols in ((300, 517), (33, 1001), (1001, 33), (129, 65), (2, 700), (700, 2)):
         out.append(((rows, cols), (cols, 1), (1, rows)))
-    # interleaved channels <-> planes, 1..16 channels
-    for c in (3, 5, 16):
+    # interleaved channels <-> planes, 2..16 channels (even counts take rotated
+    # word stores for 1- and 2-byte elements)
+    for c in (2, 3, 4, 5, 16):
         out.append(((70, 90, c), (90 * c, c, 1), (90, 1, 70 * 90)))        # HWC -> CHW
         out.append(((c, 70, 90), (70 * 90, 90, 1), (1, 90 * c, c)))        # CHW -> HWC
     # more than three batch axes, with padded source strides
@@ -229,8 +230,9 @@ def _panel_vec_cases(eb):
     shape = (min(4 * v, 32), 2, 4, 2, 40, 16 * v)
     ss, ds = perm_layouts(shape, (5, 3, 1, 4, 2, 0))
     out.append((shape, ss, ds))
-    # packed src rows (3 interleaved channels -> planes)
-    out.append(((70, 96, 3), (96 * 3, 3, 1), (96, 1, 70 * 96)))
+    # packed src rows (interleaved channels -> planes; 1-byte rows keep word stores)
+    c = {1: 3, 2: 6, 4: 3, 8: 3}[eb]
+    out.append(((70, 96, c), (96 * c, c, 1), (96, 1, 70 * 96)))
     return out
 
 

@@ -242,8 +242,11 @@ typedef struct tl_plan_info {
     int32_t panel_mode;            /* panel path: 0 rows of 16-byte blocks, 1 one run */
     int32_t panel_b1;              /* panel path: > 0 when the dst-contiguous axis (extent
                                       panel_b1) and the next dst axis are walked as one */
-    int32_t panel_vec;             /* panel path: 1 when tiles are stored as 16-byte dst
-                                      runs, 0 element by element */
+    int32_t panel_vec;             /* panel path store mode: 1 tiles stored as 16-byte dst
+                                      runs along their rows, 2 as 16-byte pieces of the
+                                      single dst run of a tile (a short dst-contiguous
+                                      axis), 0 element by element (4-byte words for
+                                      packed rows of 1- and 2-byte elements) */
     int32_t panel_wrot;            /* panel path, packed rows stored as 4-byte words: the
                                       lanes' read rotation, shift | multiplier << 8 */
 } tl_plan_info;

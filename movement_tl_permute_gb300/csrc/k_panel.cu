@@ -233,6 +233,54 @@ __device__ __forceinline__ void drain_vec(const PanelArgs& a, const PanelTile& t
     }
 }
 
+// Store one landed tile whose dst is a single run (a short b axis packed in dst, as
+// planes -> interleaved channels: tb == ext_b <= 16, ds_a == tb) as 16-byte pieces
+// of that run, V = 16 / EB elements each: element f of the run is stage row
+// b = f % tb, column a = f / tb; one division per piece, then b steps and wraps.
+// Stage row b starts at b * vpitch + ((mis0 + b * vdelta) & 15) (block rows, or
+// packed rows with vpitch = ta * EB).  The elements before the run's first 16-byte
+// boundary and after its last one are stored singly.
+template <int EB>
+__device__ __forceinline__ void drain_run(const PanelArgs& a, const PanelTile& ti,
+                                          const uint8_t* st) {
+    using T = typename dev::Bits<EB>::T;
+    constexpr uint32_t V = 16 / EB;
+    extern __shared__ __align__(16) uint8_t smem_run[];
+    const uint32_t tb = (uint32_t)a.tb, P = (uint32_t)a.vpitch, delta = (uint32_t)a.vdelta;
+    const uint32_t st0 = (uint32_t)(st - smem_run);
+    const uint32_t mis0 = (uint32_t)(reinterpret_cast<uintptr_t>(a.src + ti.so * EB) & 15);
+    auto at = [&](uint32_t b, uint32_t e) {
+        return *reinterpret_cast<const T*>(
+            &smem_run[st0 + b * P + ((mis0 + b * delta) & 15u) + e * EB]);
+    };
+    uint8_t* d = a.dst + ti.dof * EB;
+    const uint32_t n = ti.va * tb;
+    const uint32_t lead = (uint32_t)((16 - (reinterpret_cast<uintptr_t>(d) & 15)) & 15) / EB;
+    const uint32_t head = min(n, lead);
+    const uint32_t nu = (n - head) / V, tail = head + nu * V;
+    if (threadIdx.x < head) {
+        const uint32_t e = dev::div_u32(threadIdx.x, a.d_tb);
+        reinterpret_cast<T*>(d)[threadIdx.x] = at(threadIdx.x - e * tb, e);
+    }
+    if (tail + threadIdx.x < n) {
+        const uint32_t f = tail + threadIdx.x, e = dev::div_u32(f, a.d_tb);
+        reinterpret_cast<T*>(d)[f] = at(f - e * tb, e);
+    }
+    for (uint32_t u = threadIdx.x; u < nu; u += kPanelThreads) {
+        const uint32_t f0 = head + u * V;
+        uint32_t e = dev::div_u32(f0, a.d_tb), b = f0 - e * tb;
+        T v[V];
+#pragma unroll
+        for (uint32_t k = 0; k < V; ++k) {
+            v[k] = at(b, e);
+            const bool wrap = ++b == tb;
+            b = wrap ? 0 : b;
+            e += wrap ? 1 : 0;
+        }
+        dev::stg128(d + (size_t)f0 * EB, pack16(v));
+    }
+}
+
 // Store one landed tile from the stage at `st` to dst, in dst order: 16-byte runs
 // (VEC), or element by element (4-byte words for packed rows of 1- and 2-byte
 // elements).
@@ -241,6 +289,12 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
     if constexpr (VEC) {
         drain_vec<EB>(a, ti, st);
         return;
+    }
+    if constexpr (EB <= 8) {
+        if (a.run) {
+            drain_run<EB>(a, ti, st);
+            return;
+        }
     }
     using T = typename dev::Bits<EB>::T;
     T* d = reinterpret_cast<T*>(a.dst) + ti.dof;

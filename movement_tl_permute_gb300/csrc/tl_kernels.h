@@ -176,7 +176,8 @@ struct PanelArgs {
     // packed rows of 1- and 2-byte elements stored as words: lane l reads the k-th
     // element of its word as (k + wrot_m * (l >> wrot_s)) mod (4 / eb)
     int32_t wrot_s, wrot_m;
-    int32_t pad;
+    // the tile's dst is one run (tb == ext_b <= 16, ds_a == tb): stored as 16-byte pieces
+    int32_t run;
 };
 const void* panel_kernel(int eb, bool vec);   // vec: the 16-byte dst run kernel
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,

@@ -260,6 +260,26 @@ def test_panel_vector_stores(eb, kib):
         check(shape, ss, ds, eb, "panel", seed=330 + i, dst_off=1, panel_tile_kib=kib)
 
 
+@pytest.mark.parametrize("eb", [1, 2, 4])
+def test_panel_run_stores(eb):
+    """Planes -> interleaved channels: a tile's dst is one run, stored as 16-byte
+    pieces (store mode 2) with single elements before the first and after the last
+    16-byte boundary; the element and word stores give the same bytes."""
+    for i, c in enumerate((2, 3, 4, 7, 16)):
+        shape, ss, ds = (c, 70, 90), (70 * 90, 90, 1), (1, 90 * c, c)
+        plan = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb, path="panel")
+        # (16-byte runs along the tile rows take precedence where they apply)
+        want = 1 if (c * eb) % 128 == 0 else 2
+        assert plan["panel_vec"] == want and plan["vec_bytes"] == 16, (c, plan)
+        off = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb, path="panel",
+                         flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
+        assert off["panel_vec"] == 0
+        for j, (so, do) in enumerate(((0, 0), (1, 0), (0, 1), (3, 5))):
+            check(shape, ss, ds, eb, "panel", seed=400 + 10 * i + j, src_off=so, dst_off=do)
+        check(shape, ss, ds, eb, "panel", seed=450 + i, flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
+        check(shape, ss, ds, eb, "panel", seed=460 + i, panel_tile_kib=4)
+
+
 @pytest.mark.parametrize("eb", WIDTHS)
 def test_auto_takes_panel_for_untiled_planes(eb):
     # a 3-channel interleave and an odd-pitch transpose go to the panel kernel

@@ -311,8 +311,13 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         if b1:
             vec = vec and (ssb * eb) % 16 == 0 and (ssb2 * eb) % 16 == 0
         vec = vec and not (eb == 4 and not aligned)   # measured: element stores win there
-        assert p["panel_vec"] == int(vec)
-        assert p["vec_bytes"] == (16 if vec else eb)
+        # else 16-byte pieces of one dst run per tile: a short b (the whole extent in
+        # one tile) packed in dst next to a
+        ext_b = [x for x, d in zip(p["extent"], p["dst_str"]) if d == 1][0]
+        ds_a = [d for x, d in zip(p["src_str"], p["dst_str"]) if x == 1][0]
+        run = not vec and eb <= 4 and tb <= 16 and tb == ext_b and ds_a == tb and not b1
+        assert p["panel_vec"] == (1 if vec else 2 if run else 0)
+        assert p["vec_bytes"] == (16 if vec or run else eb)
         nblk = ta * eb // 16 if aligned else (ta * eb + 30) // 16
         assert pitch % 16 == 0 and 16 * nblk <= pitch < 16 * (nblk + 8)
         assert p["smem_bytes"] == 3 * (tb * pitch + (16 * (tb * eb // 16) if vec else 0))
@@ -331,7 +336,10 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         ok = {1: False, 2: ta >= 4 and busy, 4: ta != 2, 8: busy}[eb]
         vec = ok and (tb * eb) % 128 == 0 and DST % 16 == 0 and all(
             (x * eb) % 16 == 0 for x in p["dst_str"] if x not in (1, b1))
-        assert p["panel_vec"] == int(vec)
+        ext_b = [x for x, d in zip(p["extent"], p["dst_str"]) if d == 1][0]
+        ds_a = [d for x, d in zip(p["src_str"], p["dst_str"]) if x == 1][0]
+        run = not vec and eb <= 4 and tb <= 16 and tb == ext_b and ds_a == tb and not b1
+        assert p["panel_vec"] == (1 if vec else 2 if run else 0)
         for f0 in range(0, n, 32):
             offs = [(f % tb) * ta + f // tb for f in range(f0, min(n, f0 + 32))]
             assert L.bank_conflict_degree(offs, eb, "hardware") <= 2

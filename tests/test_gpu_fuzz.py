@@ -89,6 +89,65 @@ def test_random_layouts_every_applicable_path():
     assert all(ran[p] > 0 for p in ("auto", "generic", "chunk", "tile", "panel")), ran
 
 
+def _panel_case(rng):
+    """A layout aimed at the panel kernel's store modes: 2-D transposes with odd or
+    padded pitches, interleaved channels <-> planes, or 4-5-D permutes of short
+    axes; offsets mostly 0 so that aligned dst rows (16-byte runs) occur."""
+    eb = int(rng.choice([1, 2, 4, 8, 16]))
+    kind = int(rng.integers(0, 3))
+    if kind == 0:
+        R, C = (int(x) for x in rng.integers(17, 300, size=2))
+        ds_a = R + (int(rng.integers(0, 24)) if rng.random() < 0.5 else 0)
+        shape, ss, ds = (R, C), (C, 1), (1, ds_a)
+    elif kind == 1:
+        c, H, W = int(rng.integers(2, 17)), int(rng.integers(2, 40)), int(rng.integers(17, 200))
+        if rng.random() < 0.5:          # HWC -> CHW
+            shape, ss, ds = (H, W, c), (W * c, c, 1), (W, 1, H * W)
+        else:                           # CHW -> HWC
+            shape, ss, ds = (c, H, W), (H * W, W, 1), (1, W * c, c)
+    else:
+        nd = int(rng.integers(4, 6))
+        shape = tuple(int(x) for x in rng.integers(2, 12, size=nd))
+        shape = shape[:-1] + (int(rng.choice([4, 8, 16, 33])),)
+        perm = tuple(int(p) for p in rng.permutation(nd))
+        ss = L.row_major_strides(shape)
+        pst = L.row_major_strides(tuple(shape[p] for p in perm))
+        ds = [0] * nd
+        for i, p in enumerate(perm):
+            ds[p] = pst[i]
+        ds = tuple(ds)
+    so = int(rng.integers(1, 4)) if rng.random() < 0.3 else 0
+    do = int(rng.integers(1, 4)) if rng.random() < 0.3 else 0
+    return shape, tuple(ss), ds, eb, so, do
+
+
+def test_random_panel_layouts_every_store_mode():
+    """The panel kernel's store modes (element/word, 16-byte runs along tile rows,
+    16-byte pieces of one dst run, rotated words) on seeded layouts, with random tile
+    sizes and heights, each against the oracle, and again with element stores
+    forced; every mode must occur."""
+    rng = np.random.default_rng(4242)
+    modes = set()
+    for i in range(120):
+        shape, ss, ds, eb, so, do = _panel_case(rng)
+        opts = dict(panel_tile_kib=int(rng.choice([0, 4, 8, 16, 24, 32])),
+                    tile_rows=int(rng.choice([0, 0, 16, 32, 64, 128])))
+        try:
+            plan = tl.tl_plan((1 << 20) + so * eb, (1 << 36) + 256 + do * eb, shape, ss, ds, eb,
+                              path="panel", **opts)
+        except tl.TLError as e:
+            assert e.name == "TL_ERR_PATH", e
+            continue
+        modes.add(plan["panel_vec"])
+        if plan["panel_wrot"][1]:
+            modes.add("rotated")
+        for flags in (0, tl.TL_FLAG_PANEL_ELEMENT_STORES):
+            got, want = _run(shape, ss, ds, eb, so, do, "panel", seed=5000 + i, flags=flags,
+                             **opts)
+            assert np.array_equal(got, want), (shape, ss, ds, eb, so, do, opts, flags)
+    assert {0, 1, 2, "rotated"} <= modes, modes
+
+
 def test_concurrent_calls_from_host_threads():
     """Eight host threads, each on its own stream, permute different layouts at once."""
     rng = np.random.default_rng(99)

@@ -281,6 +281,67 @@ __device__ __forceinline__ void drain_run(const PanelArgs& a, const PanelTile& t
     }
 }
 
+// Store one landed tile of 1-byte elements in block rows whose dst rows are not on the
+// 16-byte grid, as 4-byte words (written for 4 / EB elements a word; 2-byte elements
+// measured faster with element stores, so only 1-byte tiles take it): warp i takes the tile's dst rows a = i, i + 8,
+// ..., lane w packing word w (4 / EB consecutive b) of each from 4 / EB stage rows.  The
+// dst rows of one warp are 8 pitches apart, a multiple of 4 bytes, so they share their
+// head (the elements before the first 4-byte boundary) and the lanes' stage rows:
+// those addresses and the packing shifts are computed once per tile.  Lane w reads its
+// k-th element as (k + wrot_m * (w >> wrot_s)) mod (4 / EB) of its word, the rotation
+// chosen on the host together with the row pitch by simulating these reads on the
+// banks.  Head and tail elements are stored singly.
+template <int EB>
+__device__ __forceinline__ void drain_words(const PanelArgs& a, const PanelTile& ti,
+                                            const uint8_t* st) {
+    using T = typename dev::Bits<EB>::T;
+    constexpr uint32_t V = 4 / EB, kWarps = kPanelThreads / 32;
+    extern __shared__ __align__(16) uint8_t smem_w[];
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (warp >= ti.va) return;
+    const uint32_t st0 = (uint32_t)(st - smem_w);
+    const uint32_t pitch = (uint32_t)a.pitch, delta = (uint32_t)a.vdelta;
+    const uint32_t mis0 = (uint32_t)(reinterpret_cast<uintptr_t>(a.src + ti.so * EB) & 15);
+    auto row = [&](uint32_t b) { return st0 + b * pitch + ((mis0 + b * delta) & 15u); };
+    uint8_t* d0 = a.dst + (ti.dof + (int64_t)warp * a.ds_a) * EB;   // first dst row of the warp
+    const int64_t dstep = (int64_t)kWarps * a.ds_a * EB;
+    const uint32_t lead = (uint32_t)((4 - (reinterpret_cast<uintptr_t>(d0) & 3)) & 3) / EB;
+    const uint32_t head = min(ti.vb, lead);
+    const uint32_t nw = (ti.vb - head) / V, tail = head + nw * V;
+    for (uint32_t w = lane; w < nw; w += 32) {
+        const uint32_t rot = (uint32_t)a.wrot_m * (w >> a.wrot_s);
+        uint32_t ro[V], sh[V];
+#pragma unroll
+        for (uint32_t k = 0; k < V; ++k) {
+            const uint32_t kk = (k + rot) & (V - 1);
+            ro[k] = row(head + w * V + kk);
+            sh[k] = 8 * EB * kk;
+        }
+        uint8_t* dp = d0 + (size_t)(head + w * V) * EB;
+        for (uint32_t e = warp; e < ti.va; e += kWarps, dp += dstep) {
+            uint32_t word = 0;
+#pragma unroll
+            for (uint32_t k = 0; k < V; ++k)
+                word |= (uint32_t)(*reinterpret_cast<const T*>(&smem_w[ro[k] + e * EB])) << sh[k];
+            *reinterpret_cast<uint32_t*>(dp) = word;
+        }
+    }
+    // head and tail elements: lane j < head stores element j, lane j < vb - tail
+    // element tail + j, of every dst row of the warp
+    const uint32_t nh = ti.vb - tail;
+    if (lane < head || lane < nh) {
+        const uint32_t rh = row(lane), rt = row(tail + lane);
+        uint8_t* dp = d0;
+        for (uint32_t e = warp; e < ti.va; e += kWarps, dp += dstep) {
+            if (lane < head)
+                reinterpret_cast<T*>(dp)[lane] = *reinterpret_cast<const T*>(&smem_w[rh + e * EB]);
+            if (lane < nh)
+                reinterpret_cast<T*>(dp)[tail + lane] =
+                    *reinterpret_cast<const T*>(&smem_w[rt + e * EB]);
+        }
+    }
+}
+
 // Store one landed tile from the stage at `st` to dst, in dst order: 16-byte runs
 // (VEC), or element by element (4-byte words for packed rows of 1- and 2-byte
 // elements).
@@ -293,6 +354,12 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
     if constexpr (EB <= 8) {
         if (a.run) {
             drain_run<EB>(a, ti, st);
+            return;
+        }
+    }
+    if constexpr (EB == 1) {
+        if (a.words) {
+            drain_words<EB>(a, ti, st);
             return;
         }
     }

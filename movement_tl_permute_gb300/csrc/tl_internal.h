@@ -54,6 +54,7 @@ struct Plan {
     int64_t src_mis16 = 0, dst_mis16 = 0;   // base addresses mod 16
     int panel_wrot_s = 0, panel_wrot_m = 0; // PANEL: word-store rotation (packed rows, eb < 4)
     bool panel_run = false;             // PANEL: each tile's dst is one run, stored in 16-byte pieces
+    bool panel_words = false;           // PANEL: block rows of 1-/2-byte elements stored as words
     int64_t tiles = 0;
 
     // WARP: tile (innermost suffix of `kept`) + batch of the outer `kept` axes.

@@ -178,6 +178,9 @@ struct PanelArgs {
     int32_t wrot_s, wrot_m;
     // the tile's dst is one run (tb == ext_b <= 16, ds_a == tb): stored as 16-byte pieces
     int32_t run;
+    // block rows of 1- and 2-byte elements stored as 4-byte words per dst row (rotation
+    // in wrot_s / wrot_m, indexed by the word)
+    int32_t words;
 };
 const void* panel_kernel(int eb, bool vec);   // vec: the 16-byte dst run kernel
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,

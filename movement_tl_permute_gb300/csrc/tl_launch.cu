@@ -530,6 +530,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.wrot_s = p.panel_wrot_s;
         a.wrot_m = p.panel_wrot_m;
         a.run = p.panel_run ? 1 : 0;
+        a.words = p.panel_words ? 1 : 0;
         a.tiles_a = (p.ext_a + a.ta - 1) / a.ta;
         a.tiles_b = (p.ext_b + a.tb - 1) / a.tb;
         a.tiles = p.tiles;
@@ -655,7 +656,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     info.pitch = p.pitch;
     info.panel_mode = p.panel_mode;
     info.panel_b1 = (int32_t)p.panel_b1;
-    info.panel_vec = p.panel_vec ? 1 : p.panel_run ? 2 : 0;
+    info.panel_vec = p.panel_vec ? 1 : p.panel_run ? 2 : p.panel_words ? 3 : 0;
     info.panel_wrot = p.panel_wrot_s | (p.panel_wrot_m << 8);
     info.tiles = p.tiles;
     int ndev = 0;

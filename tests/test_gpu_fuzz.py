@@ -122,8 +122,9 @@ def _panel_case(rng):
 
 
 def test_random_panel_layouts_every_store_mode():
-    """The panel kernel's store modes (element/word, 16-byte runs along tile rows,
-    16-byte pieces of one dst run, rotated words) on seeded layouts, with random tile
+    """The panel kernel's store modes (elements or packed-row words, 16-byte runs
+    along tile rows, 16-byte pieces of one dst run, words per dst row of block rows,
+    rotated reads) on seeded layouts, with random tile
     sizes and heights, each against the oracle, and again with element stores
     forced; every mode must occur."""
     rng = np.random.default_rng(4242)
@@ -145,7 +146,7 @@ def test_random_panel_layouts_every_store_mode():
             got, want = _run(shape, ss, ds, eb, so, do, "panel", seed=5000 + i, flags=flags,
                              **opts)
             assert np.array_equal(got, want), (shape, ss, ds, eb, so, do, opts, flags)
-    assert {0, 1, 2, "rotated"} <= modes, modes
+    assert {0, 1, 2, 3, "rotated"} <= modes, modes
 
 
 def test_concurrent_calls_from_host_threads():

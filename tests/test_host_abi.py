@@ -278,6 +278,26 @@ def _panel_degrees(ta, tb, eb, pitch, row_off, nblk, aligned, vec):
     return copy, store
 
 
+def _word_degrees(ta, tb, eb, pitch, row_off, rs, rm, aligned):
+    """Bank-conflict degrees (oracle model, hardware mode) of the panel kernel's word
+    walk over block rows: one warp per dst row a (the first four), lane w reading the
+    k-th element of its word from row h + V4 w + ((k + rm (w >> rs)) mod V4), V4 = 4 / eb,
+    for every head h and every base residue r."""
+    V4 = 4 // eb
+    out = []
+    for r in (range(1) if aligned else range(0, 16, eb)):
+        for h in range(V4):
+            for a in range(min(ta, 4)):
+                for k in range(V4):
+                    offs = []
+                    for l in range(32):
+                        b = h + V4 * l + ((k + rm * (l >> rs)) % V4)
+                        if b < tb:
+                            offs.append((b * pitch + ((r + row_off(b) * eb) & 15) + a * eb) // eb)
+                    out.append(L.bank_conflict_degree(offs, eb, "hardware"))
+    return out
+
+
 @pytest.mark.parametrize("shape,perm,eb", PANEL_LAYOUTS)
 def test_panel_layout_against_the_bank_model(shape, perm, eb):
     """The shared-memory layout the planner picks for the panel kernel, replayed
@@ -316,11 +336,22 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         ext_b = [x for x, d in zip(p["extent"], p["dst_str"]) if d == 1][0]
         ds_a = [d for x, d in zip(p["src_str"], p["dst_str"]) if x == 1][0]
         run = not vec and eb <= 4 and tb <= 16 and tb == ext_b and ds_a == tb and not b1
-        assert p["panel_vec"] == (1 if vec else 2 if run else 0)
-        assert p["vec_bytes"] == (16 if vec or run else eb)
+        # else 4-byte words per dst row for 1-byte elements (one b axis)
+        words = not vec and not run and eb == 1 and not b1
+        assert p["panel_vec"] == (1 if vec else 2 if run else 3 if words else 0)
+        assert p["vec_bytes"] == (16 if vec or run else 4 if words else eb)
         nblk = ta * eb // 16 if aligned else (ta * eb + 30) // 16
         assert pitch % 16 == 0 and 16 * nblk <= pitch < 16 * (nblk + 8)
         assert p["smem_bytes"] == 3 * (tb * pitch + (16 * (tb * eb // 16) if vec else 0))
+        if words:
+            # the word walk: lane w packs word w of one dst row from rows h + V4 w + k',
+            # k' = (k + m (w >> s)) mod V4 with the planner's (s, m); the rotation must
+            # beat or match the unrotated walk and reach 2-way
+            rs, rm = p["panel_wrot"]
+            store = _word_degrees(ta, tb, eb, pitch, row_off, rs, rm, aligned)
+            store0 = _word_degrees(ta, tb, eb, pitch, row_off, 0, 0, aligned)
+            assert sum(store) <= sum(store0) and max(store) <= 2
+            return
         copy, store = _panel_degrees(ta, tb, eb, pitch, row_off, nblk, aligned, vec)
         copy0, store0 = _panel_degrees(ta, tb, eb, 16 * nblk, row_off, nblk, aligned, vec)
         assert sum(store) <= sum(store0)        # the store walk first ...

@@ -554,7 +554,22 @@ bool panel_packed_vec_ok(int ta, int eb) {
     }
 }
 
+struct RotMemo {
+    int ta, eb, rs, rm;
+};
+std::mutex g_rot_memo_mu;
+std::vector<RotMemo> g_rot_memo;
+
 void panel_word_rotation(int ta, int eb, int* rs, int* rm) {
+    {
+        std::lock_guard<std::mutex> lk(g_rot_memo_mu);
+        for (const RotMemo& e : g_rot_memo)
+            if (e.ta == ta && e.eb == eb) {
+                *rs = e.rs;
+                *rm = e.rm;
+                return;
+            }
+    }
     const int V = 4 / eb;
     int64_t best = -1;
     *rs = 0;
@@ -580,6 +595,9 @@ void panel_word_rotation(int ta, int eb, int* rs, int* rm) {
             }
         }
     }
+    std::lock_guard<std::mutex> lk(g_rot_memo_mu);
+    if (g_rot_memo.size() >= 64) g_rot_memo.erase(g_rot_memo.begin());
+    g_rot_memo.push_back({ta, eb, *rs, *rm});
 }
 
 // Panel tile of about tile_bytes: a tiny extent is taken whole and the other one

@@ -49,11 +49,12 @@ KERNEL_SOURCES = {
     "rows": ["k_rows.cu", "tl_device.cuh"],
     "chunk": ["k_chunk.cu", "tl_device.cuh"],
     "panel": ["k_panel.cu", "tl_device.cuh"],
+    "cols": ["k_cols.cu", "tl_device.cuh"],
     "warp": ["k_warp.cu", "tl_device.cuh"],
     "generic": ["k_generic.cu", "tl_device.cuh"],
 }
 KERNEL_NAMES = {"tile": "k_tile", "cluster": "k_cluster", "rows": "k_rows", "chunk": "k_chunk",
-                "panel": "k_panel",
+                "panel": "k_panel", "cols": "k_cols",
                 "warp": "k_warp", "generic": "k_generic"}
 DTYPES = {"sf_transpose": "f32", "tile_transpose": "f16", "mx_sf": "u8", "attention": "bf16",
           "t2d_u8": "u8", "t2d_f16": "f16", "t2d_f32": "f32", "t2d_f64": "f64",
@@ -567,7 +568,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--path", default="auto",
                     choices=["auto", "generic", "chunk", "tile", "warp", "rows", "cluster",
-                             "panel"],
+                             "panel", "cols"],
                     help="force a kernel path (default: the planner's choice)")
     ap.add_argument("--leading", type=int, default=0,
                     help="override the outermost extent (smaller cases for profiling)")

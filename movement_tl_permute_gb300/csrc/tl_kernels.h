@@ -132,6 +132,27 @@ struct RowsArgs {
 cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, cudaStream_t st,
                         bool pdl);
 
+// ---------------------------------------------------------------- cols
+// Short src runs (pixels of A elements, A * eb <= 32 bytes, dense in src) -> one dst
+// plane per a; a unit is one 16-byte piece (n_px = 16 / eb pixels) of every plane.
+constexpr int kColsThreads = 256;
+struct ColsArgs {
+    const uint8_t* src;
+    uint8_t* dst;
+    int64_t units;               // pieces over all planes' b and batch items
+    int64_t upp;                 // units per batch item (ext_b / n_px)
+    int64_t ds_a;                // dst stride of a (elements): plane to plane
+    int32_t A, n_px;             // elements per pixel, pixels per piece
+    int32_t n;                   // batch axes
+    int32_t use32;               // 1: unit index and extents fit in 32 bits
+    int64_t ext[TL_MAX_DIMS];
+    int64_t ss[TL_MAX_DIMS];     // elements
+    int64_t ds[TL_MAX_DIMS];
+    dev::DivU32 div_upp;
+    dev::DivU32 div[TL_MAX_DIMS];
+};
+cudaError_t launch_cols(int eb, const ColsArgs& a, int grid, cudaStream_t st, bool pdl);
+
 // ---------------------------------------------------------------- panel
 // Transpose of (ta x tb)-element tiles of the plane through shared memory: the
 // 16-byte blocks covering each tile row are copied asynchronously (cp.async) into

@@ -306,6 +306,10 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         l.block = p.ext_b >= 16 ? 128 : 256;   // must match rows_threads<R>() in k_rows.cu
         if (sms) l.grid = cap_grid((p.tiles + 511) / 512, sms * 8, max_ctas);
         break;
+    case TL_PATH_COLS:
+        l.block = kColsThreads;
+        if (sms) l.grid = cap_grid((p.tiles + kColsThreads - 1) / kColsThreads, sms * 8, max_ctas);
+        break;
     case TL_PATH_WARP:
         l.block = 128;
         if (sms) l.grid = cap_grid((p.tiles + 3) / 4, sms * 16, max_ctas);
@@ -555,6 +559,27 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             fill_divs(a.nb, a.bext, a.d_bext);
         }
         err = launch_panel(eb, a, l.grid, l.smem, st, pdl);
+        break;
+    }
+    case TL_PATH_COLS: {
+        ColsArgs a{};
+        a.src = s8;
+        a.dst = d8;
+        a.units = p.tiles;
+        a.n_px = p.tile_rows;
+        a.A = (int32_t)p.ext_a;
+        a.upp = p.ext_b / a.n_px;
+        a.ds_a = p.ds_a;
+        a.n = p.batch.n;
+        a.use32 = p.tiles < (1LL << 32) && a.upp < (1LL << 32) ? 1 : 0;
+        for (int i = 0; i < a.n; ++i) {
+            a.ext[i] = p.batch.ext[i]; a.ss[i] = p.batch.ss[i]; a.ds[i] = p.batch.ds[i];
+        }
+        if (a.use32) {
+            a.div_upp = dev::make_divu32((uint32_t)a.upp);
+            fill_divs(a.n, a.ext, a.div);
+        }
+        err = launch_cols(eb, a, l.grid, st, pdl);
         break;
     }
     case TL_PATH_ROWS: {

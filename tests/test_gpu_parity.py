@@ -282,11 +282,34 @@ def test_panel_run_stores(eb):
 
 @pytest.mark.parametrize("eb", WIDTHS)
 def test_auto_takes_panel_for_untiled_planes(eb):
-    # a 3-channel interleave and an odd-pitch transpose go to the panel kernel
+    # 3-channel interleaves go to the panel kernel (or to the rows / cols register
+    # transposes where whole 16-byte pieces allow)
     for shape, ss, ds in ((( 64, 96, 3), (96 * 3, 3, 1), (96, 1, 64 * 96)),
                           ((3, 64, 96), (64 * 96, 96, 1), (1, 96 * 3, 3))):
-        assert tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb)["path"] in ("panel", "rows")
+        assert tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb)["path"] in ("panel", "rows", "cols")
         check(shape, ss, ds, eb, "auto", seed=90)
+
+
+@pytest.mark.parametrize("eb", [1, 2, 4, 8])
+def test_cols_path(eb):
+    """Interleaved channels -> planes with whole 16-byte plane pieces: the cols kernel
+    (pixel loads, register transpose, one store per plane), with batch axes, padded
+    planes and offset views; a plane extent off the 16-byte grid goes to the panel
+    kernel instead."""
+    n = 16 // eb
+    for i, c in enumerate(range(2, min(8, 24 // eb) + 1)):
+        H, W = 3, 5 * n
+        for j, (shape, ss, ds) in enumerate((
+                ((H, W, c), (W * c, c, 1), (W, 1, H * W)),                      # HWC -> CHW
+                ((2, H, W, c), (H * W * c, W * c, c, 1), (c * H * W, W, 1, H * W)),  # NHWC -> NCHW
+                ((H, W, c), (W * c, c, 1), (W, 1, H * W + 2 * n)))):            # padded planes
+            assert tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb)["path"] == "cols", (shape, c)
+            check(shape, ss, ds, eb, "auto", seed=600 + 10 * i + j)
+            check(shape, ss, ds, eb, "cols", seed=650 + 10 * i + j, src_off=n, dst_off=2 * n)
+        # a plane extent that is not a whole number of pieces
+        shape, ss, ds = (H, W + 1, c), ((W + 1) * c, c, 1), (W + 1, 1, H * (W + 1))
+        assert tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb)["path"] != "cols"
+        check(shape, ss, ds, eb, "auto", seed=690 + i)
 
 
 @pytest.mark.parametrize("eb,R", [(1, 2), (1, 4), (1, 8), (1, 16), (2, 2), (2, 4), (2, 8),

@@ -308,7 +308,7 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
     store walk within 4-way; with every row aligned and 16-byte dst runs the store
     walk is conflict-free.  Packed src rows are one run: the store walk stays within 2-way."""
     ss, ds = _perm_layout(shape, perm)
-    p = tl.tl_plan(SRC, DST, shape, ss, ds, eb)
+    p = tl.tl_plan(SRC, DST, shape, ss, ds, eb, path="panel")
     assert p["path"] == "panel"
     ta, tb, pitch, mode = p["tile_cols"], p["tile_rows"], p["pitch"], p["panel_mode"]
     ssb = [x for x, d in zip(p["src_str"], p["dst_str"]) if d == 1][0]

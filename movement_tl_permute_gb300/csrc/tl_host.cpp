@@ -340,9 +340,11 @@ bool tile_ok(const Plan& p, int64_t src) {
     return true;
 }
 
-// Tile-path fit: tiles at least half full (64 rows of b, 64 bytes of a).  Below
-// that the panel kernel moves fewer idle bytes.
-bool tile_fits(const Plan& p) { return p.ext_b >= 64 && p.ext_a * p.eb >= 64; }
+// Tile-path fit: 64 rows of b and whole 128-byte rows of a.  Measured on GB300:
+// transposes with 64-byte rows of a run at 3.7-5.1 TB/s on half-empty TMA tiles and
+// 6.0-6.1 on the panel kernel, 96-byte rows about even (4.9-6.1 against 5.9-6.0),
+// 128-byte rows faster on tiles (6.2-6.8 against 5.7-6.0).
+bool tile_fits(const Plan& p) { return p.ext_b >= 64 && p.ext_a * p.eb >= 128; }
 
 // Extent of b once a short b takes in the next dst axis (see panel_merge_b).
 int64_t panel_b_extent(const Plan& p) {

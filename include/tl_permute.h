@@ -237,7 +237,8 @@ typedef struct tl_plan_info {
     int32_t in_place;              /* 1 when src == dst and the warp path runs in place */
     int32_t k, shift, mask;        /* warp path swizzle (else 0) */
     int32_t tile_rows, tile_cols;  /* tile/panel path: rows (b) x columns (a) per tile,
-                                      in elements */
+                                      in elements; cols path: pixels per 16-byte piece x
+                                      elements per pixel */
     int64_t tiles;                 /* work units (tiles, rows, warps...) */
     int32_t grid, block;           /* launch shape (0 without a device) */
     int32_t smem_bytes;            /* dynamic shared memory per CTA */
@@ -248,10 +249,12 @@ typedef struct tl_plan_info {
     int32_t panel_vec;             /* panel path store mode: 1 tiles stored as 16-byte dst
                                       runs along their rows, 2 as 16-byte pieces of the
                                       single dst run of a tile (a short dst-contiguous
-                                      axis), 0 element by element (4-byte words for
-                                      packed rows of 1- and 2-byte elements) */
-    int32_t panel_wrot;            /* panel path, packed rows stored as 4-byte words: the
-                                      lanes' read rotation, shift | multiplier << 8 */
+                                      axis), 3 as 4-byte words per dst row (1-byte block
+                                      rows off the 16-byte grid), 0 element by element
+                                      (4-byte words for packed rows of 1- and 2-byte
+                                      elements) */
+    int32_t panel_wrot;            /* panel path, modes stored as 4-byte words: the lanes'
+                                      read rotation, shift | multiplier << 8 */
 } tl_plan_info;
 
 TL_API int tl_plan(const void *src, const void *dst, int ndim, const int64_t *shape,

@@ -1,4 +1,5 @@
-// k_rows.cu -- transposes whose dst runs along b are short (R * EB <= 16 bytes),
+// k_rows.cu -- transposes whose dst runs along b are short (R * EB <= 16 bytes: R a
+// power of two, or 3, 5, 6, 7),
 // such as the 4 x 32 scale-factor blocks of the TVM "permute_layout" page
 // ("Demonstration program") stored as bytes.
 //
@@ -90,12 +91,16 @@ __device__ __forceinline__ void unit_offsets(int64_t u, const RowsArgs& a, int64
     }
 }
 
-// Shared-memory staging of a warp's output: 16-byte chunk c is kept at
-// c ^ (((c >> 3) ^ (c >> 6)) & 7), which spreads both the per-lane writes
+// Shared-memory staging of a warp's output: for R a power of two, 16-byte chunk c
+// is kept at c ^ (((c >> 3) ^ (c >> 6)) & 7), which spreads both the per-lane writes
 // (chunks lane*R + k) and the contiguous read-back (chunks 32*i + lane) over
-// distinct bank groups in every 8-lane wavefront.
+// distinct bank groups in every 8-lane wavefront.  Other R keep c: an odd stride R
+// already gives 8 lanes 8 distinct bank groups, and for R = 6 no swizzle of this
+// form does better than the plain 2-way.
+template <int R>
 __device__ __forceinline__ uint32_t stage_chunk(uint32_t c) {
-    return c ^ (((c >> 3) ^ (c >> 6)) & 7u);
+    if constexpr ((R & (R - 1)) == 0) return c ^ (((c >> 3) ^ (c >> 6)) & 7u);
+    return c;
 }
 
 // Block size and units in flight per thread: the 16-row variant keeps one unit
@@ -140,7 +145,7 @@ __global__ void __launch_bounds__(rows_threads<R>()) k_rows(const RowsArgs a) {
             for (int k = 0; k < R; ++k) {
                 const uint4 v = out[k];
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                 stage_base + 16 * stage_chunk(lane * R + k)),
+                                 stage_base + 16 * stage_chunk<R>(lane * R + k)),
                              "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                              : "memory");
             }
@@ -150,7 +155,7 @@ __global__ void __launch_bounds__(rows_threads<R>()) k_rows(const RowsArgs a) {
             for (int i = 0; i < R; ++i) {
                 const int c = 32 * i + lane;
                 const int64_t d = __shfl_sync(0xffffffffu, dofs[uu], c / R);
-                const uint4 v = dev::lds128(stage_base + 16 * stage_chunk(c));
+                const uint4 v = dev::lds128(stage_base + 16 * stage_chunk<R>(c));
                 if (d >= 0) dev::stg128(a.dst + d + 16 * (c % R), v);
             }
             __syncwarp();
@@ -170,13 +175,22 @@ cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, c
                         bool pdl) {
     switch (eb * 100 + r) {
     case 102: return go<1, 2>(a, grid, block, st, pdl);
+    case 103: return go<1, 3>(a, grid, block, st, pdl);
     case 104: return go<1, 4>(a, grid, block, st, pdl);
+    case 105: return go<1, 5>(a, grid, block, st, pdl);
+    case 106: return go<1, 6>(a, grid, block, st, pdl);
+    case 107: return go<1, 7>(a, grid, block, st, pdl);
     case 108: return go<1, 8>(a, grid, block, st, pdl);
     case 116: return go<1, 16>(a, grid, block, st, pdl);
     case 202: return go<2, 2>(a, grid, block, st, pdl);
+    case 203: return go<2, 3>(a, grid, block, st, pdl);
     case 204: return go<2, 4>(a, grid, block, st, pdl);
+    case 205: return go<2, 5>(a, grid, block, st, pdl);
+    case 206: return go<2, 6>(a, grid, block, st, pdl);
+    case 207: return go<2, 7>(a, grid, block, st, pdl);
     case 208: return go<2, 8>(a, grid, block, st, pdl);
     case 402: return go<4, 2>(a, grid, block, st, pdl);
+    case 403: return go<4, 3>(a, grid, block, st, pdl);
     case 404: return go<4, 4>(a, grid, block, st, pdl);
     case 802: return go<8, 2>(a, grid, block, st, pdl);
     default: return cudaErrorInvalidValue;

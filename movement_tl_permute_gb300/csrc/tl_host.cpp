@@ -300,7 +300,9 @@ bool rows_ok(const Plan& p, int64_t src, int64_t dst) {
     const int eb = p.eb;
     const int64_t R = p.ext_b;
     const int64_t rw = R * eb;
-    if (R < 2 || rw > 16 || 16 % rw != 0) return false;
+    // R a power of two up to 16 bytes, or 3, 5, 6, 7 (planes -> 3..7 interleaved
+    // channels of up to 16 bytes)
+    if (R < 2 || rw > 16 || (16 % rw != 0 && R > 7)) return false;
     if (p.ds_a != R) return false;                       // dense plane in dst
     if ((p.ext_a * eb) % 16 != 0) return false;          // whole 16-byte row pieces
     if ((p.ss_b * eb) % 16 != 0 || src % 16 || dst % 16) return false;

@@ -312,8 +312,9 @@ def test_cols_path(eb):
         check(shape, ss, ds, eb, "auto", seed=690 + i)
 
 
-@pytest.mark.parametrize("eb,R", [(1, 2), (1, 4), (1, 8), (1, 16), (2, 2), (2, 4), (2, 8),
-                                  (4, 2), (4, 4), (8, 2)])
+@pytest.mark.parametrize("eb,R", [(1, 2), (1, 3), (1, 4), (1, 5), (1, 6), (1, 7), (1, 8), (1, 16),
+                                  (2, 2), (2, 3), (2, 4), (2, 5), (2, 6), (2, 7), (2, 8),
+                                  (4, 2), (4, 3), (4, 4), (8, 2)])
 def test_rows_path(eb, R):
     A = 3 * 16 // eb * 2            # whole 16-byte pieces per row, several units
     for i, batch in enumerate([(1,), (7,), (3, 5)]):

@@ -554,20 +554,22 @@ def test_dst_overlap_check_is_sound():
     assert accepted > 30
 
 
-def _stage_chunk(c):
-    """Physical 16-byte chunk of staged chunk c in the rows kernel's warp stage."""
-    return c ^ (((c >> 3) ^ (c >> 6)) & 7)
+def _stage_chunk(c, R):
+    """Physical 16-byte chunk of staged chunk c in the rows kernel's warp stage: an
+    XOR swizzle for R a power of two, the plain index otherwise."""
+    return c ^ (((c >> 3) ^ (c >> 6)) & 7) if R & (R - 1) == 0 else c
 
 
-@pytest.mark.parametrize("R", [2, 4, 8, 16])
+@pytest.mark.parametrize("R", [2, 3, 4, 5, 6, 7, 8, 16])
 def test_rows_kernel_stage_is_conflict_free(R):
-    # writes: lane l parks its k-th output vector as chunk l*R + k
+    # writes: lane l parks its k-th output vector as chunk l*R + k (2-way for R = 6,
+    # which no swizzle of this form improves)
     for k in range(R):
-        lanes = [_stage_chunk(l * R + k) for l in range(32)]
-        assert tl.tl_bank_conflicts(lanes, 16, "hardware") == 1
+        lanes = [_stage_chunk(l * R + k, R) for l in range(32)]
+        assert tl.tl_bank_conflicts(lanes, 16, "hardware") == (2 if R == 6 else 1)
     # read-back: lane l takes chunk 32*i + l, so stores are contiguous per instruction
     for i in range(R):
-        lanes = [_stage_chunk(32 * i + l) for l in range(32)]
+        lanes = [_stage_chunk(32 * i + l, R) for l in range(32)]
         assert tl.tl_bank_conflicts(lanes, 16, "hardware") == 1
     # the swizzle is a permutation of the warp's stage
-    assert sorted(_stage_chunk(c) for c in range(32 * R)) == list(range(32 * R))
+    assert sorted(_stage_chunk(c, R) for c in range(32 * R)) == list(range(32 * R))

@@ -41,7 +41,18 @@ struct PanelTile {
     int64_t so, dof;      // element offsets of the tile's (a0, b0) in src and dst
     int64_t b0;           // first b of the tile
     uint32_t va, vb;      // valid elements of a and b
+    int64_t a0;           // first a of the tile
+    int32_t c[3];         // coordinates on the three innermost batch axes
 };
+
+// Byte offset of tile row b in a block-row stage: b * pitch, or, for stages that
+// TMA phase maps fill, row b / phi of the block of phase b % phi.
+__device__ __forceinline__ uint32_t stage_row(const PanelArgs& a, uint32_t b) {
+    if (a.tma)
+        return (b & ((1u << a.phi_lg) - 1u)) * (uint32_t)a.phase_bytes +
+               (b >> a.phi_lg) * (uint32_t)a.pitch;
+    return b * (uint32_t)a.pitch;
+}
 
 // src offset of b (elements); b is one axis of stride ss_b, or two merged axes
 __device__ __forceinline__ int64_t b_offset(int64_t b, const PanelArgs& a) {
@@ -92,9 +103,13 @@ __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
     r.va = (uint32_t)min((int64_t)a.ta, a.ext_a - a0);
     r.vb = (uint32_t)min((int64_t)a.tb, a.ext_b - b0);
     r.b0 = b0;
+    r.a0 = a0;
     r.so = a0 + b_offset(b0, a);
     r.dof = a0 * a.ds_a + b0;
-    for (int i = 0; i < a.nb; ++i) {
+    r.c[0] = r.c[1] = r.c[2] = 0;
+#pragma unroll
+    for (int i = 0; i < TL_MAX_DIMS; ++i) {
+        if (i >= a.nb) break;
         int64_t c;
         if (a.use32) {
             const uint32_t q = dev::div_u32((uint32_t)item, a.d_bext[i]);
@@ -104,6 +119,7 @@ __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
             c = item % a.bext[i];
             item /= a.bext[i];
         }
+        if (i < 3) r.c[i] = (int32_t)c;
         r.so += c * a.bss[i];
         r.dof += c * a.bds[i];
     }
@@ -300,9 +316,9 @@ __device__ __forceinline__ void drain_words(const PanelArgs& a, const PanelTile&
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (warp >= ti.va) return;
     const uint32_t st0 = (uint32_t)(st - smem_w);
-    const uint32_t pitch = (uint32_t)a.pitch, delta = (uint32_t)a.vdelta;
+    const uint32_t delta = (uint32_t)a.vdelta;
     const uint32_t mis0 = (uint32_t)(reinterpret_cast<uintptr_t>(a.src + ti.so * EB) & 15);
-    auto row = [&](uint32_t b) { return st0 + b * pitch + ((mis0 + b * delta) & 15u); };
+    auto row = [&](uint32_t b) { return st0 + stage_row(a, b) + ((mis0 + b * delta) & 15u); };
     uint8_t* d0 = a.dst + (ti.dof + (int64_t)warp * a.ds_a) * EB;   // first dst row of the warp
     const int64_t dstep = (int64_t)kWarps * a.ds_a * EB;
     const uint32_t lead = (uint32_t)((4 - (reinterpret_cast<uintptr_t>(d0) & 3)) & 3) / EB;
@@ -448,7 +464,7 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
         // each thread keeps one b and steps a by kPanelThreads / tb
         const uint32_t b = threadIdx.x % tb, de = kPanelThreads / tb;
         if (b >= ti.vb) return;
-        const uint8_t* sp = rows ? st + b * pitch + mis(b) : st + mis0 + b * ta * EB;
+        const uint8_t* sp = rows ? st + stage_row(a, b) + mis(b) : st + mis0 + b * ta * EB;
         T* dp = d + b;
         const int64_t dstep = (int64_t)de * a.ds_a;
         uint32_t e = threadIdx.x / tb;
@@ -462,7 +478,7 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
     for (uint32_t f = threadIdx.x; f < n; f += kPanelThreads) {
         const uint32_t e = dev::div_u32(f, a.d_tb), b = f - e * tb;   // a, b in the tile
         if (e >= ti.va || b >= ti.vb) continue;
-        const uint32_t off = rows ? b * pitch + mis(b) + e * EB : mis0 + (b * ta + e) * EB;
+        const uint32_t off = rows ? stage_row(a, b) + mis(b) + e * EB : mis0 + (b * ta + e) * EB;
         d[(int64_t)e * a.ds_a + b] = *reinterpret_cast<const T*>(st + off);
     }
 }
@@ -500,7 +516,97 @@ __global__ void __launch_bounds__(kPanelThreads, VEC ? 3 : 4) k_panel(const Pane
     cp_async_wait<0>();
 }
 
+// The panel transpose for block rows whose pitch TMA cannot take directly (a row
+// pitch P that is not a multiple of 16 bytes, or an unaligned base): the rows
+// b = j mod phi (phi = 16 / gcd(P, 16)) form a tensor of pitch phi * P, a multiple
+// of 16, whose base is aligned down to 16 bytes; phase map j describes it.  One
+// thread fills each stage with phi TMA tile loads, box (ta + 16 / EB) x (tb / phi)
+// elements at x = a0 (a0 * EB is a multiple of 16 bytes), y = b0 / phi, landing as
+// phi blocks of tb / phi rows of pitch ta * EB + 16 bytes; each row holds its
+// elements at the row's own offset inside its first 16 bytes, exactly where the
+// cp.async copy puts them, so the same drains read the stage (stage_row maps b to
+// its phase block).  Completion is one mbarrier per stage; every thread waits on it
+// with a bounded wait, and on expiry all of them stop, the status word records
+// TL_ERR_TIMEOUT, and the loading thread waits (bounded) for its loads in flight
+// before the CTA leaves.
+template <int EB>
+__global__ void __launch_bounds__(kPanelThreads, 4)
+k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full[kPanelStages];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const uint32_t stage = (uint32_t)a.stage_bytes;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPanelStages; ++s) dev::mbar_init(&full[s], 1);
+        dev::fence_barrier_init();
+    }
+    __syncthreads();
+    dev::grid_dependency_wait();
+    dev::allow_dependent_launch();
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t mine = first < a.tiles ? (a.tiles - first + step - 1) / step : 0;
+    const uint32_t phi = 1u << a.phi_lg;
+    const uint32_t box_bytes = ((uint32_t)a.ta * EB + 16) * ((uint32_t)a.tb >> a.phi_lg);
+    auto load = [&](int64_t i, uint32_t s) {          // one thread: tile i into stage s
+        const PanelTile ti = panel_tile(first + i * step, a);
+        dev::mbar_arrive_expect_tx(&full[s], phi * box_bytes);
+        for (uint32_t j = 0; j < phi; ++j)
+            dev::tma_load(smem + s * stage + j * (uint32_t)a.phase_bytes, &maps.m[j], &full[s],
+                          a.tma_rank, (int)ti.a0, (int)(ti.b0 >> a.phi_lg), ti.c[0], ti.c[1],
+                          ti.c[2]);
+    };
+    int64_t issued = 0;
+    if (threadIdx.x == 0)
+        for (; issued < kPanelStages - 1 && issued < mine; ++issued) load(issued, (uint32_t)issued);
+    uint32_t slot = 0, ahead = kPanelStages - 1;
+    int64_t i = 0;
+    for (; i < mine; ++i) {
+        const int64_t nxt = i + kPanelStages - 1;
+        if (threadIdx.x == 0 && nxt < mine) {
+            dev::fence_proxy_async_smem();          // the stage's last reads came before
+            load(nxt, ahead);
+            issued = nxt + 1;
+        }
+        const bool ok = dev::mbar_wait(&full[slot], (uint32_t)(i / kPanelStages) & 1u,
+                                       (uint64_t)a.timeout_ns);
+        if (__syncthreads_or(!ok)) break;           // every thread leaves together
+        drain<EB, false>(a, panel_tile(first + i * step, a), smem + slot * stage);
+        __syncthreads();                            // stage `slot` may be refilled
+        slot = slot + 1 == kPanelStages ? 0 : slot + 1;
+        ahead = ahead + 1 == kPanelStages ? 0 : ahead + 1;
+    }
+    if (threadIdx.x == 0 && i < mine) {
+        dev::report(a.status, TL_ERR_TIMEOUT);
+        // do not leave while a load may still write this CTA's shared memory
+        for (int64_t k = i; k < issued; ++k)
+            dev::mbar_wait(&full[k % kPanelStages], (uint32_t)(k / kPanelStages) & 1u,
+                           (uint64_t)a.timeout_ns);
+    }
+}
+
 }  // namespace
+
+const void* panel_tma_kernel(int eb) {
+    switch (eb) {
+    case 1: return reinterpret_cast<const void*>(&k_panel_tma<1>);
+    case 2: return reinterpret_cast<const void*>(&k_panel_tma<2>);
+    case 4: return reinterpret_cast<const void*>(&k_panel_tma<4>);
+    default: return reinterpret_cast<const void*>(&k_panel_tma<8>);
+    }
+}
+
+cudaError_t launch_panel_tma(int eb, const PanelArgs& a, const PanelMaps& maps, int grid,
+                             int smem, cudaStream_t st, bool pdl) {
+    const dim3 g(grid), b(kPanelThreads);
+    switch (eb) {
+    case 1: return launch_kernel(k_panel_tma<1>, g, b, smem, st, pdl, maps, a);
+    case 2: return launch_kernel(k_panel_tma<2>, g, b, smem, st, pdl, maps, a);
+    case 4: return launch_kernel(k_panel_tma<4>, g, b, smem, st, pdl, maps, a);
+    case 8: return launch_kernel(k_panel_tma<8>, g, b, smem, st, pdl, maps, a);
+    default: return cudaErrorInvalidValue;
+    }
+}
 
 const void* panel_kernel(int eb, bool vec) {
     switch (eb) {

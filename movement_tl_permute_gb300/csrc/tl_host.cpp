@@ -694,6 +694,31 @@ bool panel_dst_run(const Plan& p, int64_t tb) {
            p.ds_a == tb && p.panel_b1 == 0;
 }
 
+// TMA phase maps for block rows (k_panel_tma): one b axis, at most three batch
+// axes on the 16-byte grid, element stores or words (the drains that take the phase
+// layout), a row pitch P whose phase count phi = 16 / gcd(P, 16) divides the tile
+// height, and boxes within the TMA limits (at most 256 elements a side).  Returns
+// phi, or 0 when the tile cannot take the maps.
+int panel_tma_phases(const Plan& p, int64_t ta, int64_t tb) {
+    const int eb = p.eb;
+    // (1-byte tiles keep the cp.async copy: their word walk's rotation is searched for
+    // the block-row stage, not for this one)
+    if (eb == 1 || eb > 8 || p.panel_b1 != 0 || p.batch.n > 3 || p.panel_vec || p.panel_run)
+        return 0;
+    // rows of ta * eb + 16 bytes, an odd number of 16-byte blocks: the phase blocks'
+    // rows then fall in distinct bank groups
+    if (tb <= 16 || (ta * eb) % 32 != 0 || ta + 16 / eb > 256) return 0;
+    for (int i = 0; i < p.batch.n; ++i)
+        if ((p.batch.ss[i] * eb) % 16 != 0 || p.batch.ss[i] * eb >= (1LL << 40)) return 0;
+    const int64_t P = p.ss_b * eb;
+    int64_t g = 16;
+    while (P % g != 0) g >>= 1;
+    const int phi = (int)(16 / g);
+    if (phi == 1 && p.src_mis16 == 0) return 0;       // the tile path takes aligned pitches
+    if (tb % phi != 0 || tb / phi > 256 || p.ext_b < phi || phi * P >= (1LL << 40)) return 0;
+    return phi;
+}
+
 }  // namespace
 
 void plan_panel(Plan* p, int tile_bytes, int rows) {
@@ -712,7 +737,12 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
     } else {
         tb = std::min<int64_t>(rows > 0 ? rows : eb == 1 ? 128 : eb <= 4 ? 64 : 32, p->ext_b);
         ta = std::max<int64_t>(1, std::min(E / tb, p->ext_a));
-        if (ta * tb < E)            // a short a extent: the tile grows along b instead
+        // rows off the 16-byte grid: a TMA phase box holds at most 256 elements
+        // (ta + 16 / eb of them), and a row of ta * eb + 16 bytes spans an odd number
+        // of 16-byte blocks (ta * eb a multiple of 32); the tile keeps its height
+        const bool capped = (p->ss_b * eb) % 16 != 0 && ta + 16 / eb > 256;
+        if (capped) ta = (256 - 16 / eb) / (32 / eb) * (32 / eb);
+        if (ta * tb < E && !capped)   // a short a extent: the tile grows along b instead
             tb = std::min(round_up((E + ta - 1) / ta, ru), p->ext_b);
     }
     int64_t stage;
@@ -735,6 +765,7 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
         p->panel_wrot_s = p->panel_wrot_m = 0;
         p->panel_run = false;
         p->panel_words = false;
+        p->panel_tma = false;
         if (packed) {
             p->panel_mode = 1;
             p->pitch = 0;
@@ -759,7 +790,19 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
             // pitch search runs when at least its narrowest pitch fits
             const int64_t skew = p->panel_vec ? 16 * (tb / (16 / eb)) : 0;
             stage = tb * 16 * p->panel_nblk + skew;
-            if (kPanelStages * stage <= kPanelMaxSmem) {
+            const int phi = p->panel_elem_stores ? 0 : panel_tma_phases(*p, ta, tb);
+            if (phi > 0) {
+                // phase-major stage: phi blocks of tb / phi rows of ta * eb + 16 bytes,
+                // each block on a 128-byte boundary
+                p->panel_tma = true;
+                p->panel_phi_lg = 0;
+                while ((1 << p->panel_phi_lg) < phi) ++p->panel_phi_lg;
+                p->pitch = (int)(ta * eb + 16);
+                p->panel_phase_bytes = (int)round_up((tb / phi) * p->pitch, 128);
+                p->panel_nblk = panel_blocks_per_row(ta, eb);   // for the cp.async fallback
+                p->panel_aligned = false;
+                stage = phi * p->panel_phase_bytes;
+            } else if (kPanelStages * stage <= kPanelMaxSmem) {
                 const int walk = p->panel_vec ? kWalkRuns : p->panel_words ? kWalkWords : kWalkElems;
                 p->pitch = panel_pitch((int)ta, (int)tb, eb, p->ss_b, p->panel_b1, p->panel_ss_b2,
                                        p->panel_nblk, p->panel_aligned, walk, &p->panel_wrot_s,

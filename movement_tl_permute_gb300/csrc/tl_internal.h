@@ -55,6 +55,9 @@ struct Plan {
     int panel_wrot_s = 0, panel_wrot_m = 0; // PANEL: word-store rotation (packed rows, eb < 4)
     bool panel_run = false;             // PANEL: each tile's dst is one run, stored in 16-byte pieces
     bool panel_words = false;           // PANEL: block rows of 1-/2-byte elements stored as words
+    bool panel_tma = false;             // PANEL: stages filled by TMA phase maps
+    int panel_phi_lg = 0;               // PANEL (TMA): log2 of the phase count phi
+    int panel_phase_bytes = 0;          // PANEL (TMA): shared-memory bytes of one phase block
     int64_t tiles = 0;
 
     // WARP: tile (innermost suffix of `kept`) + batch of the outer `kept` axes.

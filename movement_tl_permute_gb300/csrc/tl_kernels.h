@@ -202,7 +202,20 @@ struct PanelArgs {
     // block rows of 1- and 2-byte elements stored as 4-byte words per dst row (rotation
     // in wrot_s / wrot_m, indexed by the word)
     int32_t words;
+    // stages filled by TMA phase maps (k_panel_tma): tile row b sits in the block of
+    // phase b % 2^phi_lg (phase_bytes apart), at row b >> phi_lg of pitch bytes
+    int32_t tma, phi_lg, phase_bytes, tma_rank;
+    int64_t timeout_ns;
+    int32_t* status;
 };
+// The phase maps of k_panel_tma: map j covers the src rows b = j mod phi of the
+// plane (stride phi * row pitch), its base aligned down to 16 bytes.
+struct PanelMaps {
+    CUtensorMap m[16];
+};
+cudaError_t launch_panel_tma(int eb, const PanelArgs& a, const PanelMaps& maps, int grid,
+                             int smem, cudaStream_t st, bool pdl);
+const void* panel_tma_kernel(int eb);
 const void* panel_kernel(int eb, bool vec);   // vec: the 16-byte dst run kernel
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,
                          bool pdl);

@@ -145,6 +145,10 @@ int get_device_info(DevInfo* out) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kPanelMaxSmem) != cudaSuccess)
                     return TL_ERR_CUDA;
+            if (i < 4 && cudaFuncSetAttribute(panel_tma_kernel(1 << i),
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              kPanelMaxSmem + 128) != cudaSuccess)
+                return TL_ERR_CUDA;
             // The cluster variant is optional: if its set-up fails it is sized
             // conservatively (one CTA per SM) and the error is cleared.
             for (int h = 0; h < 2; ++h) {
@@ -224,6 +228,47 @@ int encode_tile_map(const Plan& p, const void* src, int promotion, CUtensorMap* 
     return r == CUDA_SUCCESS ? TL_OK : TL_ERR_CUDA;
 }
 
+// The phase maps of the TMA panel kernel: map j covers the src rows b = j mod phi
+// of the plane, base aligned down to 16 bytes, element type of the element width;
+// dim 0 = a (elements, from the aligned base), dim 1 = b / phi (stride phi * pitch),
+// dims 2.. = batch (innermost first).  Box = (ta + 16 / eb) x (tb / phi), no swizzle.
+int encode_panel_maps(const Plan& p, const uint8_t* src, PanelMaps* maps, int* rank) {
+    if (!g_encode) return TL_ERR_CUDA;
+    const int eb = p.eb;
+    const int phi = 1 << p.panel_phi_lg;
+    const int64_t P = p.ss_b * eb;
+    const CUtensorMapDataType type = eb == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                     : eb == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                               : CU_TENSOR_MAP_DATA_TYPE_UINT64;
+    int64_t bext[3] = {1, 1, 1}, bss[3] = {0, 0, 0}, bds[3] = {0, 0, 0};
+    batch_inner_first(p, bext, bss, bds);
+    *rank = 2 + p.batch.n;
+    for (int j = 0; j < phi; ++j) {
+        const uintptr_t row0 = reinterpret_cast<uintptr_t>(src) + (uintptr_t)(j * P);
+        const uintptr_t base = row0 & ~uintptr_t(15);
+        const int64_t shift = (int64_t)(row0 - base) / eb;     // elements before a = 0
+        cuuint64_t dims[5], strides[4];
+        cuuint32_t box[5], es[5] = {1, 1, 1, 1, 1};
+        dims[0] = (cuuint64_t)(p.ext_a + shift);
+        dims[1] = (cuuint64_t)((p.ext_b - j + phi - 1) / phi);
+        strides[0] = (cuuint64_t)(phi * P);
+        box[0] = (cuuint32_t)(p.tile_cols + 16 / eb);
+        box[1] = (cuuint32_t)(p.tile_rows / phi);
+        for (int i = 0; i < p.batch.n; ++i) {
+            dims[2 + i] = (cuuint64_t)bext[i];
+            strides[1 + i] = (cuuint64_t)(bss[i] * eb);
+            box[2 + i] = 1;
+        }
+        const CUresult r =
+            g_encode(&maps->m[j], type, (cuuint32_t)*rank, reinterpret_cast<void*>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return TL_ERR_CUDA;
+    }
+    return TL_OK;
+}
+
 // Lanes per row group of the chunk kernel: each lane moves two vectors of a
 // row, so a group has the power of two covering half the row (at most a warp).
 int chunk_group_lanes(int64_t vpr) {
@@ -289,10 +334,12 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
     case TL_PATH_PANEL:
         l.block = kPanelThreads;
         l.smem = kPanelStages * p.panel_stage;   // <= kPanelMaxSmem for tiles of <= 32 KiB
+        if (p.panel_tma) l.smem += 128;           // the stages start on a 128-byte boundary
         if (sms) {
             int per_sm = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm,
-                                                              panel_kernel(p.eb, p.panel_vec),
+                                                              p.panel_tma ? panel_tma_kernel(p.eb)
+                                                                          : panel_kernel(p.eb, p.panel_vec),
                                                               kPanelThreads, l.smem) !=
                     cudaSuccess ||
                 per_sm < 1) {
@@ -558,6 +605,23 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             a.d_glast = dev::make_divu32((uint32_t)glast);
             fill_divs(a.nb, a.bext, a.d_bext);
         }
+        a.timeout_ns = kDefaultTimeoutNs;
+        a.status = opts ? opts->dev_status : nullptr;
+        if (p.panel_tma) {
+            PanelMaps maps;
+            if (encode_panel_maps(p, s8, &maps, &a.tma_rank) == TL_OK) {
+                a.tma = 1;
+                a.phi_lg = p.panel_phi_lg;
+                a.phase_bytes = p.panel_phase_bytes;
+                err = launch_panel_tma(eb, a, maps, l.grid, l.smem, st, pdl);
+                break;
+            }
+            // no maps for this layout: the cp.async copy takes the same tile (its pitch,
+            // ta * eb + 16, is the one the misaligned rows need)
+            a.nblk = p.panel_nblk;
+            a.d_nblk = dev::make_divu32((uint32_t)p.panel_nblk);
+            a.aligned = 0;
+        }
         err = launch_panel(eb, a, l.grid, l.smem, st, pdl);
         break;
     }
@@ -679,7 +743,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     info.tile_rows = p.tile_rows;
     info.tile_cols = p.tile_cols;
     info.pitch = p.pitch;
-    info.panel_mode = p.panel_mode;
+    info.panel_mode = p.panel_tma ? 2 : p.panel_mode;
     info.panel_b1 = (int32_t)p.panel_b1;
     info.panel_vec = p.panel_vec ? 1 : p.panel_run ? 2 : p.panel_words ? 3 : 0;
     info.panel_wrot = p.panel_wrot_s | (p.panel_wrot_m << 8);

@@ -260,6 +260,30 @@ def test_panel_vector_stores(eb, kib):
         check(shape, ss, ds, eb, "panel", seed=330 + i, dst_off=1, panel_tile_kib=kib)
 
 
+@pytest.mark.parametrize("eb", [2, 4, 8])
+def test_panel_tma_phase_maps(eb):
+    """Block rows whose pitch is off the 16-byte grid, loaded by TMA phase maps (rows
+    b = j mod phi as tensors of pitch phi * P, bases aligned down): ragged tiles on
+    both sides, an unaligned base, a batch axis on the 16-byte grid; the same bytes as
+    the oracle and as the cp.async copy (forced with the element-store flag)."""
+    # dst rows off the 16-byte grid too (padded to an odd pitch), so that the tiles
+    # store element by element, the store mode the phase layout serves
+    cases = [((300, 517), (517, 1), (1, 301)),
+             ((4, 150, 303), (45456, 303, 1), (45753, 1, 151)),
+             ((150, 1001), (1001, 1), (1, 151))]
+    for i, (shape, ss, ds) in enumerate(cases):
+        for so in (0, 1):
+            plan = tl.tl_plan((1 << 20) + so * eb, 1 << 36, shape, ss, ds, eb, path="panel")
+            assert plan["panel_mode"] == 2, (shape, so, plan)
+            off = tl.tl_plan((1 << 20) + so * eb, 1 << 36, shape, ss, ds, eb, path="panel",
+                             flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
+            assert off["panel_mode"] == 0
+            check(shape, ss, ds, eb, "panel", seed=700 + 10 * i + so, src_off=so)
+            check(shape, ss, ds, eb, "panel", seed=750 + 10 * i + so, src_off=so, dst_off=1)
+            check(shape, ss, ds, eb, "panel", seed=780 + 10 * i + so, src_off=so,
+                  flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
+
+
 @pytest.mark.parametrize("eb", [1, 2, 4])
 def test_panel_run_stores(eb):
     """Planes -> interleaved channels: a tile's dst is one run, stored as 16-byte

@@ -319,6 +319,30 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
     else:
         row_off = lambda b: b * ssb
     n = ta * tb
+    if mode == 2:
+        # rows loaded by TMA phase maps: phi = 16 / gcd(row pitch, 16) maps, the stage
+        # phase-major (row b in block b % phi, at row b // phi of ta * eb + 16 bytes,
+        # an odd number of 16-byte blocks; blocks on 128-byte boundaries); the element
+        # walk over it reads 4- and 8-byte elements conflict-free, 2-byte ones 2-way
+        assert not b1 and eb in (2, 4, 8) and (ssb * eb) % 16 != 0
+        g = 16
+        while (ssb * eb) % g:
+            g //= 2
+        phi = 16 // g
+        assert tb % phi == 0 and pitch == ta * eb + 16 and (pitch // 16) % 2 == 1
+        assert ta + 16 // eb <= 256 and tb // phi <= 256
+        pb = -(-(tb // phi) * pitch // 128) * 128
+        assert p["smem_bytes"] == 3 * phi * pb + 128
+        assert p["panel_vec"] == 0
+        srow = lambda b: (b % phi) * pb + (b // phi) * pitch
+        degs = []
+        for r in range(0, 16, eb):
+            for f0 in range(0, min(n, 4096), 32):
+                offs = [(srow(f % tb) + ((r + row_off(f % tb) * eb) & 15) + (f // tb) * eb) // eb
+                        for f in range(f0, min(n, f0 + 32))]
+                degs.append(L.bank_conflict_degree(offs, eb, "hardware"))
+        assert max(degs) == (2 if eb == 2 else 1)
+        return
     if mode == 0:
         # every src row on a 16-byte boundary: base, tile step ta and every src
         # stride but a's (1) multiples of 16 bytes

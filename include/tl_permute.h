@@ -206,7 +206,8 @@ typedef struct tl_permute_opts {
     int32_t tile_stages;  /* shared-memory ring depth: 2..12 (tile, 128-row tiles),
                              2..6 (tile, 256-row tiles); cluster: staging ring, 1..8 */
     int32_t tile_ctas_per_sm;  /* resident CTAs per SM the grid is sized for */
-    int32_t tile_l2_promotion; /* L2 fill size of the TMA loads: 64, 128, 256, or -1 = none */
+    int32_t tile_l2_promotion; /* L2 fill size of the TMA loads (tile path, panel phase
+                                  maps): 64, 128, 256, or -1 = none */
     int32_t tile_rows;    /* tile height in rows of the dst-contiguous axis: 128 or 256
                              on the tile path, 16..1024 on the panel path (where both
                              plane extents exceed 16); other values select the default */

@@ -701,9 +701,11 @@ bool panel_dst_run(const Plan& p, int64_t tb) {
 // phi, or 0 when the tile cannot take the maps.
 int panel_tma_phases(const Plan& p, int64_t ta, int64_t tb) {
     const int eb = p.eb;
-    // (1-byte tiles keep the cp.async copy: their word walk's rotation is searched for
-    // the block-row stage, not for this one)
-    if (eb == 1 || eb > 8 || p.panel_b1 != 0 || p.batch.n > 3 || p.panel_vec || p.panel_run)
+    // Measured on GB300 (odd-pitch transposes, against the cp.async copy of the same
+    // tile): fp16 4.4 -> 5.5 TB/s, fp64 5.4 -> 5.6; fp32 slower (5.3 against 6.0), so
+    // 4-byte tiles keep the cp.async copy, as do 1-byte ones (their word walk's
+    // rotation is searched for the block-row stage, not for this one).
+    if ((eb != 2 && eb != 8) || p.panel_b1 != 0 || p.batch.n > 3 || p.panel_vec || p.panel_run)
         return 0;
     // rows of ta * eb + 16 bytes, an odd number of 16-byte blocks: the phase blocks'
     // rows then fall in distinct bank groups

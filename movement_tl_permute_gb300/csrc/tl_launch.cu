@@ -232,7 +232,8 @@ int encode_tile_map(const Plan& p, const void* src, int promotion, CUtensorMap* 
 // of the plane, base aligned down to 16 bytes, element type of the element width;
 // dim 0 = a (elements, from the aligned base), dim 1 = b / phi (stride phi * pitch),
 // dims 2.. = batch (innermost first).  Box = (ta + 16 / eb) x (tb / phi), no swizzle.
-int encode_panel_maps(const Plan& p, const uint8_t* src, PanelMaps* maps, int* rank) {
+int encode_panel_maps(const Plan& p, const uint8_t* src, int promotion, PanelMaps* maps,
+                      int* rank) {
     if (!g_encode) return TL_ERR_CUDA;
     const int eb = p.eb;
     const int phi = 1 << p.panel_phi_lg;
@@ -260,10 +261,15 @@ int encode_panel_maps(const Plan& p, const uint8_t* src, PanelMaps* maps, int* r
             strides[1 + i] = (cuuint64_t)(bss[i] * eb);
             box[2 + i] = 1;
         }
+        const CUtensorMapL2promotion promo =
+            promotion == 64    ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+            : promotion == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+            : promotion == 256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                               : CU_TENSOR_MAP_L2_PROMOTION_NONE;
         const CUresult r =
             g_encode(&maps->m[j], type, (cuuint32_t)*rank, reinterpret_cast<void*>(base), dims,
                      strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return TL_ERR_CUDA;
     }
     return TL_OK;
@@ -609,7 +615,10 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.status = opts ? opts->dev_status : nullptr;
         if (p.panel_tma) {
             PanelMaps maps;
-            if (encode_panel_maps(p, s8, &maps, &a.tma_rank) == TL_OK) {
+            // 64-byte L2 fills unless the caller asked for another (measured best for
+            // the phase maps' rows of 0.5-1 KiB at odd offsets)
+            const int promo = opts && opts->tile_l2_promotion != 0 ? tt.promotion : 64;
+            if (encode_panel_maps(p, s8, promo, &maps, &a.tma_rank) == TL_OK) {
                 a.tma = 1;
                 a.phi_lg = p.panel_phi_lg;
                 a.phase_bytes = p.panel_phase_bytes;

@@ -323,8 +323,8 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         # rows loaded by TMA phase maps: phi = 16 / gcd(row pitch, 16) maps, the stage
         # phase-major (row b in block b % phi, at row b // phi of ta * eb + 16 bytes,
         # an odd number of 16-byte blocks; blocks on 128-byte boundaries); the element
-        # walk over it reads 4- and 8-byte elements conflict-free, 2-byte ones 2-way
-        assert not b1 and eb in (2, 4, 8) and (ssb * eb) % 16 != 0
+        # walk over it reads 8-byte elements conflict-free, 2-byte ones 2-way
+        assert not b1 and eb in (2, 8) and (ssb * eb) % 16 != 0
         g = 16
         while (ssb * eb) % g:
             g //= 2

@@ -278,6 +278,80 @@ def _panel_degrees(ta, tb, eb, pitch, row_off, nblk, aligned, vec):
     return copy, store
 
 
+def test_interleaved_channel_paths():
+    """The planner's kernel for interleaved channels <-> planes (H x W x C, W * H a
+    whole number of 16-byte pieces): planes -> interleaved takes the rows register
+    transpose for pixels of at most 16 bytes with C a power of two or at most 7;
+    interleaved -> planes takes the cols transpose for 2..8 channels of at most 24 bytes;
+    everything else that is a plane goes to the tile or panel kernels."""
+    H, W = 64, 96
+    for eb in (1, 2, 4, 8):
+        for C in range(2, 17):
+            hwc = ((H, W, C), (W * C, C, 1), (W, 1, H * W))
+            chw = ((C, H, W), (H * W, W, 1), (1, W * C, C))
+            got = tl.tl_plan(SRC, DST, *hwc, eb)["path"]
+            want_cols = C <= 8 and C * eb <= 24
+            assert (got == "cols") == want_cols, ("hwc->chw", C, eb, got)
+            if not want_cols:
+                assert got in ("panel", "tile"), ("hwc->chw", C, eb, got)
+            got = tl.tl_plan(SRC, DST, *chw, eb)["path"]
+            want_rows = C * eb <= 16 and (C & (C - 1) == 0 or C <= 7)
+            assert (got == "rows") == want_rows, ("chw->hwc", C, eb, got)
+            if not want_rows:
+                assert got in ("panel", "tile"), ("chw->hwc", C, eb, got)
+
+
+def test_panel_tma_phase_map_invariants():
+    """Every plan that loads rows by TMA phase maps keeps the TMA rules by
+    construction, over seeded odd-pitch layouts: the box's x coordinate a0 * eb and its
+    row of ta * eb + 16 bytes on the 16-byte grid (an odd number of 16-byte blocks),
+    boxes of at most 256 elements a side, tb a multiple of phi, phi * pitch and every
+    batch stride multiples of 16 bytes, at most three batch axes, one b axis, and the
+    three-stage ring within the shared memory the kernel is set up for."""
+    rng = np.random.default_rng(77)
+    seen = 0
+    for _ in range(400):
+        eb = int(rng.choice([1, 2, 4, 8]))
+        R, C = (int(x) for x in rng.integers(17, 5000, size=2))
+        nb = int(rng.integers(0, 4))
+        batch = tuple(int(x) for x in rng.integers(2, 5, size=nb))
+        # src rows of pitch C (often odd), batch strides padded to the 16-byte grid
+        plane = R * C
+        bst, acc = [], -(-plane * eb // 16) * 16 // eb
+        for e in reversed(batch):
+            bst.insert(0, acc)
+            acc *= e
+        shape = batch + (R, C)
+        ss = tuple(bst) + (C, 1)
+        ds_plane = R + int(rng.integers(0, 3))
+        dacc, dst_b = ds_plane * C, []
+        for e in reversed(batch):
+            dst_b.insert(0, dacc)
+            dacc *= e
+        ds = tuple(dst_b) + (1, ds_plane)
+        so = int(rng.integers(0, 3))
+        try:
+            p = tl.tl_plan(SRC + so * eb, DST, shape, ss, ds, eb, path="panel")
+        except tl.TLError:
+            continue
+        if p["panel_mode"] != 2:
+            continue
+        seen += 1
+        ta, tb, pitch = p["tile_cols"], p["tile_rows"], p["pitch"]
+        P = C * eb
+        g = 16
+        while P % g:
+            g //= 2
+        phi = 16 // g
+        assert eb in (2, 8) and nb <= 3
+        assert (ta * eb) % 32 == 0 and pitch == ta * eb + 16 and (pitch // 16) % 2 == 1
+        assert ta + 16 // eb <= 256 and tb % phi == 0 and tb // phi <= 256 and R >= phi
+        assert (phi * P) % 16 == 0 and all((x * eb) % 16 == 0 for x in bst)
+        pb = -(-(tb // phi) * pitch // 128) * 128
+        assert p["smem_bytes"] == 3 * phi * pb + 128 <= 160 * 1024 + 128
+    assert seen > 20, seen
+
+
 def _word_degrees(ta, tb, eb, pitch, row_off, rs, rm, aligned):
     """Bank-conflict degrees (oracle model, hardware mode) of the panel kernel's word
     walk over block rows: one warp per dst row a (the first four), lane w reading the

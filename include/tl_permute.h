@@ -245,8 +245,9 @@ typedef struct tl_plan_info {
     int32_t smem_bytes;            /* dynamic shared memory per CTA */
     int32_t pitch;                 /* panel path: shared-memory bytes per tile row */
     int32_t panel_mode;            /* panel path: 0 rows of 16-byte blocks, 1 one run,
-                                      2 rows loaded by TMA phase maps (a row pitch off
-                                      the 16-byte grid) */
+                                      2 rows loaded by TMA phase maps into a phase-major
+                                      stage (a row pitch off the 16-byte grid), 3 the
+                                      same stage filled by cp.async */
     int32_t panel_b1;              /* panel path: > 0 when the dst-contiguous axis (extent
                                       panel_b1) and the next dst axis are walked as one */
     int32_t panel_vec;             /* panel path store mode: 1 tiles stored as 16-byte dst

@@ -45,10 +45,11 @@ struct PanelTile {
     int32_t c[3];         // coordinates on the three innermost batch axes
 };
 
-// Byte offset of tile row b in a block-row stage: b * pitch, or, for stages that
-// TMA phase maps fill, row b / phi of the block of phase b % phi.
+// Byte offset of tile row b in a block-row stage: b * pitch, or, for phase-major
+// stages (filled by TMA phase maps or by cp.async in the same arrangement), row
+// b / phi of the block of phase b % phi.
 __device__ __forceinline__ uint32_t stage_row(const PanelArgs& a, uint32_t b) {
-    if (a.tma)
+    if (a.phase)
         return (b & ((1u << a.phi_lg) - 1u)) * (uint32_t)a.phase_bytes +
                (b >> a.phi_lg) * (uint32_t)a.pitch;
     return b * (uint32_t)a.pitch;
@@ -155,7 +156,8 @@ __device__ __forceinline__ void issue(const PanelArgs& a, const PanelTile& ti, u
             const uintptr_t row = base + (uintptr_t)(row_offset(b, ti, a) * EB);
             const uint32_t blocks = ((uint32_t)(row & 15) + ti.va * EB + 15) >> 4;
             if (k < blocks)
-                cp_async16(sb + b * pitch + (b / V) * skew + 16 * k, (row & ~uintptr_t(15)) + 16 * k);
+                cp_async16(sb + (skew ? b * pitch + (b / V) * skew : stage_row(a, b)) + 16 * k,
+                           (row & ~uintptr_t(15)) + 16 * k);
         }
     } else {   // kPanelFlat: rows packed back to back (ss_b == ta == va)
         const uint32_t blocks = ((uint32_t)(base & 15) + ti.vb * (uint32_t)a.ta * EB + 15) >> 4;
@@ -587,25 +589,16 @@ k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
 
 }  // namespace
 
+// The planner takes TMA phase maps for 2-byte elements only (measured; the other
+// widths fill the phase-major stage by cp.async).
 const void* panel_tma_kernel(int eb) {
-    switch (eb) {
-    case 1: return reinterpret_cast<const void*>(&k_panel_tma<1>);
-    case 2: return reinterpret_cast<const void*>(&k_panel_tma<2>);
-    case 4: return reinterpret_cast<const void*>(&k_panel_tma<4>);
-    default: return reinterpret_cast<const void*>(&k_panel_tma<8>);
-    }
+    return eb == 2 ? reinterpret_cast<const void*>(&k_panel_tma<2>) : nullptr;
 }
 
 cudaError_t launch_panel_tma(int eb, const PanelArgs& a, const PanelMaps& maps, int grid,
                              int smem, cudaStream_t st, bool pdl) {
-    const dim3 g(grid), b(kPanelThreads);
-    switch (eb) {
-    case 1: return launch_kernel(k_panel_tma<1>, g, b, smem, st, pdl, maps, a);
-    case 2: return launch_kernel(k_panel_tma<2>, g, b, smem, st, pdl, maps, a);
-    case 4: return launch_kernel(k_panel_tma<4>, g, b, smem, st, pdl, maps, a);
-    case 8: return launch_kernel(k_panel_tma<8>, g, b, smem, st, pdl, maps, a);
-    default: return cudaErrorInvalidValue;
-    }
+    if (eb != 2) return cudaErrorInvalidValue;
+    return launch_kernel(k_panel_tma<2>, dim3(grid), dim3(kPanelThreads), smem, st, pdl, maps, a);
 }
 
 const void* panel_kernel(int eb, bool vec) {

@@ -694,18 +694,17 @@ bool panel_dst_run(const Plan& p, int64_t tb) {
            p.ds_a == tb && p.panel_b1 == 0;
 }
 
-// TMA phase maps for block rows (k_panel_tma): one b axis, at most three batch
-// axes on the 16-byte grid, element stores or words (the drains that take the phase
-// layout), a row pitch P whose phase count phi = 16 / gcd(P, 16) divides the tile
-// height, and boxes within the TMA limits (at most 256 elements a side).  Returns
-// phi, or 0 when the tile cannot take the maps.
+// Phase-major stage for block rows (TMA phase maps, k_panel_tma, or cp.async into
+// the same arrangement): one b axis, at most three batch axes on the 16-byte grid,
+// element stores (the drain that takes the phase layout), a row pitch P whose phase
+// count phi = 16 / gcd(P, 16) divides the tile height, and boxes within the TMA
+// limits (at most 256 elements a side).  Returns phi, or 0 when the tile cannot take
+// the arrangement.
 int panel_tma_phases(const Plan& p, int64_t ta, int64_t tb) {
     const int eb = p.eb;
-    // Measured on GB300 (odd-pitch transposes, against the cp.async copy of the same
-    // tile): fp16 4.4 -> 5.5 TB/s, fp64 5.4 -> 5.6; fp32 slower (5.3 against 6.0), so
-    // 4-byte tiles keep the cp.async copy, as do 1-byte ones (their word walk's
-    // rotation is searched for the block-row stage, not for this one).
-    if ((eb != 2 && eb != 8) || p.panel_b1 != 0 || p.batch.n > 3 || p.panel_vec || p.panel_run)
+    // (1-byte tiles keep the block-row stage: their word walk's rotation is searched
+    // for it)
+    if (eb == 1 || eb > 8 || p.panel_b1 != 0 || p.batch.n > 3 || p.panel_vec || p.panel_run)
         return 0;
     // rows of ta * eb + 16 bytes, an odd number of 16-byte blocks: the phase blocks'
     // rows then fall in distinct bank groups
@@ -768,6 +767,7 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
         p->panel_run = false;
         p->panel_words = false;
         p->panel_tma = false;
+        p->panel_phase = false;
         if (packed) {
             p->panel_mode = 1;
             p->pitch = 0;
@@ -795,8 +795,13 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
             const int phi = p->panel_elem_stores ? 0 : panel_tma_phases(*p, ta, tb);
             if (phi > 0) {
                 // phase-major stage: phi blocks of tb / phi rows of ta * eb + 16 bytes,
-                // each block on a 128-byte boundary
-                p->panel_tma = true;
+                // each block on a 128-byte boundary.  Measured on GB300 (odd-pitch
+                // transposes, against block rows filled by cp.async, one box per A/B):
+                // TMA phase maps fp16 4.18 -> 5.39 TB/s; for fp32 and fp64 the maps
+                // measured 0.89x and 0.89-1.03x, while cp.async into the phase-major
+                // stage gains 2 % (fp32 5.71 -> 5.82) and 4 % (fp64 6.09 -> 6.36).
+                p->panel_phase = true;
+                p->panel_tma = eb == 2;
                 p->panel_phi_lg = 0;
                 while ((1 << p->panel_phi_lg) < phi) ++p->panel_phi_lg;
                 p->pitch = (int)(ta * eb + 16);

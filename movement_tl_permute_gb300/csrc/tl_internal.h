@@ -56,6 +56,7 @@ struct Plan {
     bool panel_run = false;             // PANEL: each tile's dst is one run, stored in 16-byte pieces
     bool panel_words = false;           // PANEL: block rows of 1-/2-byte elements stored as words
     bool panel_tma = false;             // PANEL: stages filled by TMA phase maps
+    bool panel_phase = false;           // PANEL: phase-major stages (TMA or cp.async)
     int panel_phi_lg = 0;               // PANEL (TMA): log2 of the phase count phi
     int panel_phase_bytes = 0;          // PANEL (TMA): shared-memory bytes of one phase block
     int64_t tiles = 0;

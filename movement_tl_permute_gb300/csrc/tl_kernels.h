@@ -202,9 +202,10 @@ struct PanelArgs {
     // block rows of 1- and 2-byte elements stored as 4-byte words per dst row (rotation
     // in wrot_s / wrot_m, indexed by the word)
     int32_t words;
-    // stages filled by TMA phase maps (k_panel_tma): tile row b sits in the block of
-    // phase b % 2^phi_lg (phase_bytes apart), at row b >> phi_lg of pitch bytes
-    int32_t tma, phi_lg, phase_bytes, tma_rank;
+    // phase-major stages (phase = 1): tile row b sits in the block of phase
+    // b % 2^phi_lg (phase_bytes apart), at row b >> phi_lg of pitch bytes; filled by
+    // TMA phase maps (k_panel_tma, tma = 1) or by cp.async
+    int32_t tma, phase, phi_lg, phase_bytes, tma_rank, pad2;
     int64_t timeout_ns;
     int32_t* status;
 };

@@ -145,9 +145,10 @@ int get_device_info(DevInfo* out) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kPanelMaxSmem) != cudaSuccess)
                     return TL_ERR_CUDA;
-            if (i < 4 && cudaFuncSetAttribute(panel_tma_kernel(1 << i),
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              kPanelMaxSmem + 128) != cudaSuccess)
+            if (panel_tma_kernel(1 << i) &&
+                cudaFuncSetAttribute(panel_tma_kernel(1 << i),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kPanelMaxSmem + 128) != cudaSuccess)
                 return TL_ERR_CUDA;
             // The cluster variant is optional: if its set-up fails it is sized
             // conservatively (one CTA per SM) and the error is cleared.
@@ -613,6 +614,14 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         }
         a.timeout_ns = kDefaultTimeoutNs;
         a.status = opts ? opts->dev_status : nullptr;
+        if (p.panel_phase) {
+            a.phase = 1;
+            a.phi_lg = p.panel_phi_lg;
+            a.phase_bytes = p.panel_phase_bytes;
+            a.nblk = p.panel_nblk;                 // the cp.async copy of the same tile
+            a.d_nblk = dev::make_divu32((uint32_t)p.panel_nblk);
+            a.aligned = 0;
+        }
         if (p.panel_tma) {
             PanelMaps maps;
             // 64-byte L2 fills unless the caller asked for another (measured best for
@@ -620,16 +629,11 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             const int promo = opts && opts->tile_l2_promotion != 0 ? tt.promotion : 64;
             if (encode_panel_maps(p, s8, promo, &maps, &a.tma_rank) == TL_OK) {
                 a.tma = 1;
-                a.phi_lg = p.panel_phi_lg;
-                a.phase_bytes = p.panel_phase_bytes;
                 err = launch_panel_tma(eb, a, maps, l.grid, l.smem, st, pdl);
                 break;
             }
-            // no maps for this layout: the cp.async copy takes the same tile (its pitch,
-            // ta * eb + 16, is the one the misaligned rows need)
-            a.nblk = p.panel_nblk;
-            a.d_nblk = dev::make_divu32((uint32_t)p.panel_nblk);
-            a.aligned = 0;
+            // no maps for this layout: cp.async fills the same phase-major stage (its
+            // row pitch, ta * eb + 16, holds the blocks of a misaligned row)
         }
         err = launch_panel(eb, a, l.grid, l.smem, st, pdl);
         break;
@@ -752,7 +756,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     info.tile_rows = p.tile_rows;
     info.tile_cols = p.tile_cols;
     info.pitch = p.pitch;
-    info.panel_mode = p.panel_tma ? 2 : p.panel_mode;
+    info.panel_mode = p.panel_tma ? 2 : p.panel_phase ? 3 : p.panel_mode;
     info.panel_b1 = (int32_t)p.panel_b1;
     info.panel_vec = p.panel_vec ? 1 : p.panel_run ? 2 : p.panel_words ? 3 : 0;
     info.panel_wrot = p.panel_wrot_s | (p.panel_wrot_m << 8);

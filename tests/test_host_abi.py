@@ -334,21 +334,22 @@ def test_panel_tma_phase_map_invariants():
             p = tl.tl_plan(SRC + so * eb, DST, shape, ss, ds, eb, path="panel")
         except tl.TLError:
             continue
-        if p["panel_mode"] != 2:
+        if p["panel_mode"] not in (2, 3):
             continue
         seen += 1
+        assert (p["panel_mode"] == 2) == (eb == 2)
         ta, tb, pitch = p["tile_cols"], p["tile_rows"], p["pitch"]
         P = C * eb
         g = 16
         while P % g:
             g //= 2
         phi = 16 // g
-        assert eb in (2, 8) and nb <= 3
+        assert eb in (2, 4, 8) and nb <= 3
         assert (ta * eb) % 32 == 0 and pitch == ta * eb + 16 and (pitch // 16) % 2 == 1
         assert ta + 16 // eb <= 256 and tb % phi == 0 and tb // phi <= 256 and R >= phi
         assert (phi * P) % 16 == 0 and all((x * eb) % 16 == 0 for x in bst)
         pb = -(-(tb // phi) * pitch // 128) * 128
-        assert p["smem_bytes"] == 3 * phi * pb + 128 <= 160 * 1024 + 128
+        assert p["smem_bytes"] == 3 * phi * pb + (128 if eb == 2 else 0) <= 160 * 1024 + 128
     assert seen > 20, seen
 
 
@@ -393,12 +394,14 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
     else:
         row_off = lambda b: b * ssb
     n = ta * tb
-    if mode == 2:
-        # rows loaded by TMA phase maps: phi = 16 / gcd(row pitch, 16) maps, the stage
-        # phase-major (row b in block b % phi, at row b // phi of ta * eb + 16 bytes,
-        # an odd number of 16-byte blocks; blocks on 128-byte boundaries); the element
-        # walk over it reads 8-byte elements conflict-free, 2-byte ones 2-way
-        assert not b1 and eb in (2, 8) and (ssb * eb) % 16 != 0
+    if mode in (2, 3):
+        # phase-major stage (mode 2: loaded by TMA phase maps, 2- and 8-byte elements;
+        # mode 3: by cp.async, 4-byte elements): phi = 16 / gcd(row pitch, 16), row b in
+        # block b % phi, at row b // phi of ta * eb + 16 bytes, an odd number of 16-byte
+        # blocks; blocks on 128-byte boundaries; the element walk over it reads 4- and
+        # 8-byte elements conflict-free, 2-byte ones 2-way
+        assert not b1 and (ssb * eb) % 16 != 0
+        assert eb in ((2,) if mode == 2 else (4, 8))
         g = 16
         while (ssb * eb) % g:
             g //= 2
@@ -406,7 +409,7 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         assert tb % phi == 0 and pitch == ta * eb + 16 and (pitch // 16) % 2 == 1
         assert ta + 16 // eb <= 256 and tb // phi <= 256
         pb = -(-(tb // phi) * pitch // 128) * 128
-        assert p["smem_bytes"] == 3 * phi * pb + 128
+        assert p["smem_bytes"] == 3 * phi * pb + (128 if mode == 2 else 0)
         assert p["panel_vec"] == 0
         srow = lambda b: (b % phi) * pb + (b // phi) * pitch
         degs = []

@@ -738,10 +738,11 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
     } else {
         tb = std::min<int64_t>(rows > 0 ? rows : eb == 1 ? 128 : eb <= 4 ? 64 : 32, p->ext_b);
         ta = std::max<int64_t>(1, std::min(E / tb, p->ext_a));
-        // rows off the 16-byte grid: a TMA phase box holds at most 256 elements
-        // (ta + 16 / eb of them), and a row of ta * eb + 16 bytes spans an odd number
-        // of 16-byte blocks (ta * eb a multiple of 32); the tile keeps its height
-        const bool capped = (p->ss_b * eb) % 16 != 0 && ta + 16 / eb > 256;
+        // rows off the 16-byte grid (widths that take a phase-major stage): a TMA
+        // phase box holds at most 256 elements (ta + 16 / eb of them), and a row of
+        // ta * eb + 16 bytes spans an odd number of 16-byte blocks (ta * eb a multiple
+        // of 32); the tile keeps its height
+        const bool capped = eb >= 2 && eb <= 8 && (p->ss_b * eb) % 16 != 0 && ta + 16 / eb > 256;
         if (capped) ta = (256 - 16 / eb) / (32 / eb) * (32 / eb);
         if (ta * tb < E && !capped)   // a short a extent: the tile grows along b instead
             tb = std::min(round_up((E + ta - 1) / ta, ru), p->ext_b);

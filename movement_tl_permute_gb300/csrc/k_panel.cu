@@ -14,12 +14,17 @@
 // the whole tile is one run of blocks.
 //
 // The copy walks the tile in src order, so consecutive threads read consecutive
-// src addresses; the store walks it in dst order (element f -> a = f / tb,
-// b = f % tb), so consecutive threads write consecutive dst addresses.  The row
-// pitch in shared memory is chosen on the host by simulating both walks' warp
-// accesses against the banks (the bank model of the TVM "permute_layout" page,
-// "Algorithm", step 2).  Element offsets follow the strided addressing of
-// "Buffers and memory", "Declaring buffers".
+// src addresses; the stores walk it in dst order, so consecutive threads write
+// consecutive dst addresses: element by element (f -> a = f / tb, b = f % tb), as
+// 4-byte words (packed 1- and 2-byte rows, and 1-byte rows per dst row), as 16-byte
+// runs along the tile rows when the dst rows are 16-byte aligned (drain_vec), or as
+// 16-byte pieces of the tile's single dst run (drain_run).  Rows whose pitch is off
+// the 16-byte grid are staged phase-major (rows b = j mod phi together), filled by
+// cp.async or, in k_panel_tma, by TMA loads through one tensor map per phase.  The
+// row pitch and the lanes' read rotations are chosen on the host by simulating the
+// walks' warp accesses against the banks (the bank model of the TVM
+// "permute_layout" page, "Algorithm", step 2).  Element offsets follow the strided
+// addressing of "Buffers and memory", "Declaring buffers".
 #include "tl_kernels.h"
 
 namespace tl {

@@ -170,8 +170,10 @@ TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape
                                2..8 elements, <= 24 bytes): 16-byte pixel loads, register
                                transpose, one 16-byte store per plane */
 #define TL_PATH_MASK 0xFu
-/* Test hook for the cluster path: the producer CTA skips its DSMEM hand-off, so the
- * consumer's bounded wait must expire and report TL_ERR_TIMEOUT in dev_status. */
+/* Test hook for the cluster path (the producer CTA skips its DSMEM hand-off) and for
+ * panel tiles loaded by TMA phase maps (the loading thread skips one phase load of its
+ * first tile): the bounded wait (50 ms under the hook) must expire and report
+ * TL_ERR_TIMEOUT in dev_status; the kernel returns without a fault. */
 #define TL_FLAG_TEST_DROP_HANDOFF (1u << 8)
 /* Launch without programmatic dependent launch (by default a permute may be scheduled
  * while the previous kernel of the stream drains; it waits for that kernel to complete

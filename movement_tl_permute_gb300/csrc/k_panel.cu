@@ -558,10 +558,12 @@ k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
     auto load = [&](int64_t i, uint32_t s) {          // one thread: tile i into stage s
         const PanelTile ti = panel_tile(first + i * step, a);
         dev::mbar_arrive_expect_tx(&full[s], phi * box_bytes);
-        for (uint32_t j = 0; j < phi; ++j)
+        for (uint32_t j = 0; j < phi; ++j) {
+            if (a.drop_load && i == 0 && j == 0) continue;   // test hook: the wait expires
             dev::tma_load(smem + s * stage + j * (uint32_t)a.phase_bytes, &maps.m[j], &full[s],
                           a.tma_rank, (int)ti.a0, (int)(ti.b0 >> a.phi_lg), ti.c[0], ti.c[1],
                           ti.c[2]);
+        }
     };
     int64_t issued = 0;
     if (threadIdx.x == 0)

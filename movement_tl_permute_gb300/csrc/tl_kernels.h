@@ -205,7 +205,8 @@ struct PanelArgs {
     // phase-major stages (phase = 1): tile row b sits in the block of phase
     // b % 2^phi_lg (phase_bytes apart), at row b >> phi_lg of pitch bytes; filled by
     // TMA phase maps (k_panel_tma, tma = 1) or by cp.async
-    int32_t tma, phase, phi_lg, phase_bytes, tma_rank, pad2;
+    int32_t tma, phase, phi_lg, phase_bytes, tma_rank;
+    int32_t drop_load;           // test hook: skip one phase load of the first tile
     int64_t timeout_ns;
     int32_t* status;
 };

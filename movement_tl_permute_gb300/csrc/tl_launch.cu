@@ -612,8 +612,10 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             a.d_glast = dev::make_divu32((uint32_t)glast);
             fill_divs(a.nb, a.bext, a.d_bext);
         }
-        a.timeout_ns = kDefaultTimeoutNs;
+        const bool drop = (flags & TL_FLAG_TEST_DROP_HANDOFF) != 0;
+        a.timeout_ns = drop ? kTestTimeoutNs : kDefaultTimeoutNs;
         a.status = opts ? opts->dev_status : nullptr;
+        a.drop_load = drop && p.panel_tma ? 1 : 0;
         if (p.panel_phase) {
             a.phase = 1;
             a.phi_lg = p.panel_phi_lg;

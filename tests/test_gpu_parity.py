@@ -492,6 +492,25 @@ def test_cluster_handoff_timeout_is_reported_and_context_survives():
     assert int(status.item()) == 0
 
 
+def test_panel_tma_timeout_is_reported_and_context_survives():
+    """A panel tile loaded by TMA phase maps whose load never lands (the test hook
+    skips one phase load): every thread's bounded wait expires together, the status
+    word reads TL_ERR_TIMEOUT, and the context still runs the same permute correctly."""
+    R, C, ds_a = 300, 517, 301
+    shape, ss, ds = (R, C), (C, 1), (1, ds_a)
+    assert tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, 2, path="panel")["panel_mode"] == 2
+    src = torch.zeros(R * C, dtype=torch.int16, device="cuda")
+    dst = torch.zeros(C * ds_a, dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tl.permute(src, dst, shape, ss, ds, path="panel", flags=tl.TL_FLAG_TEST_DROP_HANDOFF,
+               dev_status=status.data_ptr())
+    torch.cuda.synchronize()
+    assert int(status.item()) == -12          # TL_ERR_TIMEOUT
+    status.zero_()
+    check(shape, ss, ds, 2, "panel", seed=19, dev_status=status.data_ptr())
+    assert int(status.item()) == 0
+
+
 # ---------------------------------------------------------------------------
 # every bench workload at full size, in the launch configuration the bench times
 # ---------------------------------------------------------------------------

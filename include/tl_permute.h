@@ -167,7 +167,7 @@ TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape
                                blocks covering each src row: any element alignment, up
                                to 6 batch axes, tiny extents */
 #define TL_PATH_COLS 8u     /* short src runs (interleaved channels -> planes, pixels of
-                               2..8 elements, <= 24 bytes): 16-byte pixel loads, register
+                               2..16 elements, <= 24 bytes): 16-byte pixel loads, register
                                transpose, one 16-byte store per plane */
 #define TL_PATH_MASK 0xFu
 /* Test hook for the cluster path (the producer CTA skips its DSMEM hand-off) and for

@@ -1,5 +1,5 @@
 // k_cols.cu -- transposes whose src runs along a are short (interleaved channels ->
-// planes: pixels of A elements, A * EB <= 24 bytes, stored back to back).
+// planes: pixels of A = 2..16 elements, A * EB <= 24 bytes, stored back to back).
 //
 // Plane: a (extent A, src stride 1, dst stride ds_a: one dst plane per a) by b (src
 // stride A: the pixels are dense in src, dst stride 1), plus batch axes.  A unit is
@@ -139,6 +139,19 @@ cudaError_t go_eb(const ColsArgs& a, int grid, cudaStream_t st, bool pdl) {
         switch (a.A) {
         case 7: return go<EB, 7>(a, grid, st, pdl);
         case 8: return go<EB, 8>(a, grid, st, pdl);
+        case 9: return go<EB, 9>(a, grid, st, pdl);
+        case 10: return go<EB, 10>(a, grid, st, pdl);
+        case 11: return go<EB, 11>(a, grid, st, pdl);
+        case 12: return go<EB, 12>(a, grid, st, pdl);
+        default: break;
+        }
+    }
+    if constexpr (EB == 1) {
+        switch (a.A) {
+        case 13: return go<EB, 13>(a, grid, st, pdl);
+        case 14: return go<EB, 14>(a, grid, st, pdl);
+        case 15: return go<EB, 15>(a, grid, st, pdl);
+        case 16: return go<EB, 16>(a, grid, st, pdl);
         default: break;
         }
     }

@@ -1,5 +1,5 @@
-// k_rows.cu -- transposes whose dst runs along b are short (R * EB <= 16 bytes: R a
-// power of two, or 3, 5, 6, 7),
+// k_rows.cu -- transposes whose dst runs along b are short (R * EB <= 16 bytes, any
+// R >= 2),
 // such as the 4 x 32 scale-factor blocks of the TVM "permute_layout" page
 // ("Demonstration program") stored as bytes.
 //
@@ -94,12 +94,14 @@ __device__ __forceinline__ void unit_offsets(int64_t u, const RowsArgs& a, int64
 // Shared-memory staging of a warp's output: for R a power of two, 16-byte chunk c
 // is kept at c ^ (((c >> 3) ^ (c >> 6)) & 7), which spreads both the per-lane writes
 // (chunks lane*R + k) and the contiguous read-back (chunks 32*i + lane) over
-// distinct bank groups in every 8-lane wavefront.  Other R keep c: an odd stride R
-// already gives 8 lanes 8 distinct bank groups, and for R = 6 no swizzle of this
-// form does better than the plain 2-way.
+// distinct bank groups in every 8-lane wavefront; R = 12 keeps c ^ ((c >> 3) & 7)
+// (2-way writes, 4-way without).  Other R keep c: an odd stride R already gives 8
+// lanes 8 distinct bank groups, and for R = 6, 10, 14 no swizzle of these forms does
+// better than the plain 2-way.
 template <int R>
 __device__ __forceinline__ uint32_t stage_chunk(uint32_t c) {
     if constexpr ((R & (R - 1)) == 0) return c ^ (((c >> 3) ^ (c >> 6)) & 7u);
+    if constexpr (R % 4 == 0) return c ^ ((c >> 3) & 7u);
     return c;
 }
 
@@ -181,6 +183,13 @@ cudaError_t launch_rows(int eb, int r, const RowsArgs& a, int grid, int block, c
     case 106: return go<1, 6>(a, grid, block, st, pdl);
     case 107: return go<1, 7>(a, grid, block, st, pdl);
     case 108: return go<1, 8>(a, grid, block, st, pdl);
+    case 109: return go<1, 9>(a, grid, block, st, pdl);
+    case 110: return go<1, 10>(a, grid, block, st, pdl);
+    case 111: return go<1, 11>(a, grid, block, st, pdl);
+    case 112: return go<1, 12>(a, grid, block, st, pdl);
+    case 113: return go<1, 13>(a, grid, block, st, pdl);
+    case 114: return go<1, 14>(a, grid, block, st, pdl);
+    case 115: return go<1, 15>(a, grid, block, st, pdl);
     case 116: return go<1, 16>(a, grid, block, st, pdl);
     case 202: return go<2, 2>(a, grid, block, st, pdl);
     case 203: return go<2, 3>(a, grid, block, st, pdl);

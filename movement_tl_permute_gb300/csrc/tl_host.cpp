@@ -300,9 +300,8 @@ bool rows_ok(const Plan& p, int64_t src, int64_t dst) {
     const int eb = p.eb;
     const int64_t R = p.ext_b;
     const int64_t rw = R * eb;
-    // R a power of two up to 16 bytes, or 3, 5, 6, 7 (planes -> 3..7 interleaved
-    // channels of up to 16 bytes)
-    if (R < 2 || rw > 16 || (16 % rw != 0 && R > 7)) return false;
+    // any R whose run fits 16 bytes (planes -> 2..16 interleaved channels)
+    if (R < 2 || rw > 16) return false;
     if (p.ds_a != R) return false;                       // dense plane in dst
     if ((p.ext_a * eb) % 16 != 0) return false;          // whole 16-byte row pieces
     if ((p.ss_b * eb) % 16 != 0 || src % 16 || dst % 16) return false;
@@ -311,7 +310,7 @@ bool rows_ok(const Plan& p, int64_t src, int64_t dst) {
     return true;
 }
 
-// Short src runs: pixels of A = ext_a elements (2..8, at most 24 bytes) packed back
+// Short src runs: pixels of A = ext_a elements (2..16, at most 24 bytes) packed back
 // to back along b, one dst plane per a; whole 16-byte pieces of every plane (ext_b a
 // multiple of 16 / eb) and every piece, pixel run and plane on the 16-byte grid.
 // Measured on GB300 (interleaved -> planes): 1.0-1.6x the panel kernel up to 24-byte
@@ -319,7 +318,7 @@ bool rows_ok(const Plan& p, int64_t src, int64_t dst) {
 bool cols_ok(const Plan& p, int64_t src, int64_t dst) {
     const int eb = p.eb;
     const int64_t A = p.ext_a;
-    if (eb > 8 || A < 2 || A > 8 || A * eb > 24) return false;
+    if (eb > 8 || A < 2 || A > 16 || A * eb > 24) return false;
     if (p.ss_b != A || p.ext_b % (16 / eb) != 0) return false;
     if (src % 16 || dst % 16 || (p.ds_a * eb) % 16) return false;
     for (int i = 0; i < p.batch.n; ++i)

@@ -322,7 +322,7 @@ def test_cols_path(eb):
     planes and offset views; a plane extent off the 16-byte grid goes to the panel
     kernel instead."""
     n = 16 // eb
-    for i, c in enumerate(range(2, min(8, 24 // eb) + 1)):
+    for i, c in enumerate(range(2, min(16, 24 // eb) + 1)):
         H, W = 3, 5 * n
         for j, (shape, ss, ds) in enumerate((
                 ((H, W, c), (W * c, c, 1), (W, 1, H * W)),                      # HWC -> CHW
@@ -337,7 +337,8 @@ def test_cols_path(eb):
         check(shape, ss, ds, eb, "auto", seed=690 + i)
 
 
-@pytest.mark.parametrize("eb,R", [(1, 2), (1, 3), (1, 4), (1, 5), (1, 6), (1, 7), (1, 8), (1, 16),
+@pytest.mark.parametrize("eb,R", [(1, 2), (1, 3), (1, 4), (1, 5), (1, 6), (1, 7), (1, 8), (1, 9),
+                                  (1, 10), (1, 11), (1, 12), (1, 13), (1, 14), (1, 15), (1, 16),
                                   (2, 2), (2, 3), (2, 4), (2, 5), (2, 6), (2, 7), (2, 8),
                                   (4, 2), (4, 3), (4, 4), (8, 2)])
 def test_rows_path(eb, R):

@@ -568,7 +568,22 @@ def test_planner_invariants_on_random_layouts():
             assert int(np.prod(plan["extent"])) == n
             assert plan["tiles"] > 0 and 0 < plan["block"] <= 1024
             assert 0 <= plan["smem_bytes"] <= 227 * 1024, (shape, ss, ds, eb, path, plan)
-    assert {"chunk", "panel", "tile", "generic", "warp", "rows", "cluster"} <= seen, seen
+            if plan["path"] == "panel":
+                # store and copy modes, and the panel ring within its shared memory
+                mode, store = plan["panel_mode"], plan["panel_vec"]
+                assert mode in (0, 1, 2, 3) and store in (0, 1, 2, 3)
+                assert plan["smem_bytes"] <= 160 * 1024 + 128
+                assert plan["vec_bytes"] == (16 if store in (1, 2) else 4 if store == 3 else eb)
+                if mode in (2, 3):          # phase-major stages: rows off the 16-byte grid
+                    assert store == 0 and eb in (2, 4, 8) and (mode == 2) == (eb == 2)
+                if store == 3:
+                    assert eb == 1 and mode == 0
+                seen.add(("panel", mode, store))
+            if plan["path"] == "cols":
+                A, npx = plan["tile_cols"], plan["tile_rows"]
+                assert 2 <= A <= 16 and A * eb <= 24 and npx * eb == 16
+    assert {"chunk", "panel", "tile", "generic", "warp", "rows", "cluster", "cols"} <= seen, seen
+    assert {("panel", 0, 0), ("panel", 0, 1)} <= seen, seen
 
 
 def test_checked_run_flags():

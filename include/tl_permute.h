@@ -216,7 +216,7 @@ typedef struct tl_permute_opts {
     int32_t cluster_recv_stages; /* cluster: receive ring depth, 1..8 (staging + receive
                                     slots at most 12) */
     int32_t cluster_consumer_warps; /* cluster: consumer warps per CTA, 4 or 8 */
-    int32_t panel_tile_kib;       /* panel path: tile size, 4..32 KiB (default 32, or 24
+    int32_t panel_tile_kib;       /* panel path: tile size, 4..48 KiB (default 32, or 24
                                      with an extent of 16 or less) */
 } tl_permute_opts;
 
@@ -261,6 +261,10 @@ typedef struct tl_plan_info {
                                       elements) */
     int32_t panel_wrot;            /* panel path, modes stored as 4-byte words: the lanes'
                                       read rotation, shift | multiplier << 8 */
+    int32_t panel_a1;              /* panel path: > 0 when a short src-contiguous axis a
+                                      was merged with the next src axis (src dense across
+                                      the two); the inner extent, each tile row's dst
+                                      offset then splits a into its two axes */
 } tl_plan_info;
 
 TL_API int tl_plan(const void *src, const void *dst, int ndim, const int64_t *shape,

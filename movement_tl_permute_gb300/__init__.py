@@ -78,7 +78,7 @@ class TlPlanInfo(ctypes.Structure):
                 ("mask", _i32), ("tile_rows", _i32), ("tile_cols", _i32), ("tiles", _i64),
                 ("grid", _i32), ("block", _i32), ("smem_bytes", _i32), ("pitch", _i32),
                 ("panel_mode", _i32), ("panel_b1", _i32), ("panel_vec", _i32),
-                ("panel_wrot", _i32)]
+                ("panel_wrot", _i32), ("panel_a1", _i32)]
 
 
 def library_path() -> str:
@@ -269,7 +269,8 @@ def tl_plan(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides, elem_by
                 tile_cols=info.tile_cols, tiles=info.tiles, grid=info.grid, block=info.block,
                 smem_bytes=info.smem_bytes, pitch=info.pitch, panel_mode=info.panel_mode,
                 panel_b1=info.panel_b1, panel_vec=info.panel_vec,
-                panel_wrot=(info.panel_wrot & 0xFF, info.panel_wrot >> 8))
+                panel_wrot=(info.panel_wrot & 0xFF, info.panel_wrot >> 8),
+                panel_a1=info.panel_a1)
 
 
 def _bytes_after(t) -> int:

@@ -44,11 +44,25 @@ __device__ __forceinline__ void cp_async_wait() {
 
 struct PanelTile {
     int64_t so, dof;      // element offsets of the tile's (a0, b0) in src and dst
+    int64_t dob;          // dst offset of (b0, batch item) alone
     int64_t b0;           // first b of the tile
     uint32_t va, vb;      // valid elements of a and b
     int64_t a0;           // first a of the tile
     int32_t c[3];         // coordinates on the three innermost batch axes
 };
+
+// dst element offset of the tile's row a0 + e at b0: e * ds_a past the tile's origin,
+// or, when a is two merged axes (AM, its own kernels), from the split of the absolute a
+template <bool AM>
+__device__ __forceinline__ int64_t drow_off(const PanelArgs& a, const PanelTile& ti, uint32_t e) {
+    if constexpr (!AM) {
+        return ti.dof + (int64_t)e * a.ds_a;
+    } else {
+        const uint32_t x = (uint32_t)ti.a0 + e;
+        const uint32_t hi = dev::div_u32(x, a.d_a1);
+        return ti.dob + (int64_t)(x - hi * a.d_a1.d) * a.ds_a + (int64_t)hi * a.ds_a2;
+    }
+}
 
 // Byte offset of tile row b in a block-row stage: b * pitch, or, for phase-major
 // stages (filled by TMA phase maps or by cp.async in the same arrangement), row
@@ -79,6 +93,7 @@ __device__ __forceinline__ int64_t row_offset(uint32_t bb, const PanelTile& ti,
 // CTAs then write runs of group_b * tb elements of dst rows while the tiles beside
 // each other along a, which share the 16-byte blocks at their row ends, are in
 // flight together and meet those blocks in L2.
+template <bool AM>
 __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
     int64_t item, ia, ib;
     if (a.use32) {
@@ -111,7 +126,7 @@ __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
     r.b0 = b0;
     r.a0 = a0;
     r.so = a0 + b_offset(b0, a);
-    r.dof = a0 * a.ds_a + b0;
+    r.dof = AM ? b0 : a0 * a.ds_a + b0;
     r.c[0] = r.c[1] = r.c[2] = 0;
 #pragma unroll
     for (int i = 0; i < TL_MAX_DIMS; ++i) {
@@ -128,6 +143,11 @@ __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
         if (i < 3) r.c[i] = (int32_t)c;
         r.so += c * a.bss[i];
         r.dof += c * a.bds[i];
+    }
+    if constexpr (AM) {          // (b0, batch item) alone, then the split of a0
+        const uint32_t hi = dev::div_u32((uint32_t)a0, a.d_a1);
+        r.dob = r.dof;
+        r.dof += (int64_t)((uint32_t)a0 - hi * a.d_a1.d) * a.ds_a + (int64_t)hi * a.ds_a2;
     }
     return r;
 }
@@ -200,7 +220,34 @@ __device__ __forceinline__ uint4 pack16(const uint8_t (&v)[16]) {
 // 8 distinct 16-byte bank groups at every step whatever the pitch (the host's pitch
 // search replays these reads on the bank model of the TVM "permute_layout" page,
 // "Algorithm" step 2).
+// dst address of the 16-byte run of tile row a0 + e at b0, for a walk whose e steps
+// by de: a pointer advanced by de * ds_a, or, for merged a, the split of each e
+template <int EB, bool AM>
+struct RunPtr {
+    uint8_t* p;
+    int64_t step;
+    __device__ __forceinline__ RunPtr(const PanelArgs& a, const PanelTile& ti, uint32_t e,
+                                      uint32_t b0, uint32_t de)
+        : p(a.dst + (ti.dof + (int64_t)e * a.ds_a + b0) * EB), step((int64_t)de * a.ds_a * EB) {}
+    __device__ __forceinline__ uint8_t* at(const PanelArgs&, const PanelTile&, uint32_t) const {
+        return p;
+    }
+    __device__ __forceinline__ void next() { p += step; }
+};
 template <int EB>
+struct RunPtr<EB, true> {
+    uint32_t b0;
+    __device__ __forceinline__ RunPtr(const PanelArgs&, const PanelTile&, uint32_t, uint32_t b,
+                                      uint32_t)
+        : b0(b) {}
+    __device__ __forceinline__ uint8_t* at(const PanelArgs& a, const PanelTile& ti,
+                                           uint32_t e) const {
+        return a.dst + (drow_off<true>(a, ti, e) + b0) * EB;
+    }
+    __device__ __forceinline__ void next() {}
+};
+
+template <int EB, bool AM>
 __device__ __forceinline__ void drain_vec(const PanelArgs& a, const PanelTile& ti,
                                           const uint8_t* st) {
     using T = typename dev::Bits<EB>::T;
@@ -219,7 +266,6 @@ __device__ __forceinline__ void drain_vec(const PanelArgs& a, const PanelTile& t
     const uint32_t mis0 = (uint32_t)(reinterpret_cast<uintptr_t>(a.src + ti.so * EB) & 15);
     const uint32_t P = (uint32_t)a.vpitch, delta = (uint32_t)a.vdelta;
     const uint32_t skew = a.vskew ? 16u : 0u;
-    const int64_t dstep = (int64_t)4 * gstep * a.ds_a * EB;
     // row addresses as offsets into the dynamic shared memory, so that every read is
     // a shared-window load
     extern __shared__ __align__(16) uint8_t smem_rows[];
@@ -234,18 +280,19 @@ __device__ __forceinline__ void drain_vec(const PanelArgs& a, const PanelTile& t
             ro[k] = st0 + b * P + q * skew + ((mis0 + b * delta) & 15u);
         }
         uint32_t e = 4 * g40 + (lane >> 3);
-        uint8_t* dp = a.dst + (ti.dof + (int64_t)e * a.ds_a + b0) * EB;
+        RunPtr<EB, AM> rp(a, ti, e, b0, 4 * gstep);
         if (b0 + V <= ti.vb) {
 #pragma unroll 2
-            for (; e < ti.va; e += 4 * gstep, dp += dstep) {
+            for (; e < ti.va; e += 4 * gstep, rp.next()) {
                 T v[V];
 #pragma unroll
                 for (uint32_t k = 0; k < V; ++k)
                     v[k] = *reinterpret_cast<const T*>(&smem_rows[ro[k] + e * EB]);
-                dev::stg128(dp, pack16(v));
+                dev::stg128(rp.at(a, ti, e), pack16(v));
             }
         } else {           // the block holds the last valid rows of a ragged tile
-            for (; e < ti.va; e += 4 * gstep, dp += dstep) {
+            for (; e < ti.va; e += 4 * gstep, rp.next()) {
+                uint8_t* dp = rp.at(a, ti, e);
 #pragma unroll
                 for (uint32_t k = 0; k < V; ++k)
                     if (b0 + k < ti.vb)
@@ -368,19 +415,20 @@ __device__ __forceinline__ void drain_words(const PanelArgs& a, const PanelTile&
 // Store one landed tile from the stage at `st` to dst, in dst order: 16-byte runs
 // (VEC), or element by element (4-byte words for packed rows of 1- and 2-byte
 // elements).
-template <int EB, bool VEC>
+template <int EB, bool VEC, bool AM>
 __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, const uint8_t* st) {
     if constexpr (VEC) {
-        drain_vec<EB>(a, ti, st);
+        drain_vec<EB, AM>(a, ti, st);
         return;
     }
-    if constexpr (EB <= 8) {
+    // (the run and word walks need one dst offset step per row of a: not merged)
+    if constexpr (EB <= 8 && !AM) {
         if (a.run) {
             drain_run<EB>(a, ti, st);
             return;
         }
     }
-    if constexpr (EB == 1) {
+    if constexpr (EB == 1 && !AM) {
         if (a.words) {
             drain_words<EB>(a, ti, st);
             return;
@@ -410,7 +458,8 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
                 return *reinterpret_cast<const T*>(st + mis0 + (b * ta + e) * EB);
             };
             for (uint32_t e = 0; e < ti.va; ++e) {
-                T* drow = d + (int64_t)e * a.ds_a;
+                T* drow = AM ? reinterpret_cast<T*>(a.dst) + drow_off<AM>(a, ti, e)
+                             : d + (int64_t)e * a.ds_a;
                 const uint32_t lead = (uint32_t)((4 - (reinterpret_cast<uintptr_t>(drow) & 3)) & 3);
                 const uint32_t head = min(ti.vb, lead / EB);
                 const uint32_t nw = (ti.vb - head) / V, tail = head + nw * V;
@@ -439,7 +488,7 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
             }
             return;
         }
-        if (tb <= 16 && a.ds_a == (int64_t)tb && tb == a.ext_b && !a.merged) {
+        if (tb <= 16 && a.ds_a == (int64_t)tb && tb == a.ext_b && !a.merged && !AM) {
             // A short b axis packed in dst (planes -> interleaved channels): the tile's
             // dst is one run of va * tb elements, stored as 4-byte words; element f of
             // the run is (a, b) = (f / tb, f % tb).
@@ -472,9 +521,16 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
         const uint32_t b = threadIdx.x % tb, de = kPanelThreads / tb;
         if (b >= ti.vb) return;
         const uint8_t* sp = rows ? st + stage_row(a, b) + mis(b) : st + mis0 + b * ta * EB;
+        uint32_t e = threadIdx.x / tb;
+        if constexpr (AM) {          // two-level dst offsets of a: one split per row
+            T* dst = reinterpret_cast<T*>(a.dst) + b;
+#pragma unroll 4
+            for (; e < ti.va; e += de)
+                dst[drow_off<AM>(a, ti, e)] = *reinterpret_cast<const T*>(sp + e * EB);
+            return;
+        }
         T* dp = d + b;
         const int64_t dstep = (int64_t)de * a.ds_a;
-        uint32_t e = threadIdx.x / tb;
         dp += (int64_t)e * a.ds_a;
 #pragma unroll 4
         for (; e < ti.va; e += de, dp += dstep) *dp = *reinterpret_cast<const T*>(sp + e * EB);
@@ -486,13 +542,14 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
         const uint32_t e = dev::div_u32(f, a.d_tb), b = f - e * tb;   // a, b in the tile
         if (e >= ti.va || b >= ti.vb) continue;
         const uint32_t off = rows ? stage_row(a, b) + mis(b) + e * EB : mis0 + (b * ta + e) * EB;
-        d[(int64_t)e * a.ds_a + b] = *reinterpret_cast<const T*>(st + off);
+        T* drow = AM ? reinterpret_cast<T*>(a.dst) + drow_off<AM>(a, ti, e) : d + (int64_t)e * a.ds_a;
+        drow[b] = *reinterpret_cast<const T*>(st + off);
     }
 }
 
 // The two store modes are separate kernels so that each keeps its own register
 // budget (the element-store kernel fits four CTAs per SM).
-template <int EB, bool VEC>
+template <int EB, bool VEC, bool AM>
 __global__ void __launch_bounds__(kPanelThreads, VEC ? 3 : 4) k_panel(const PanelArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const uint32_t sbase = dev::smem_addr(smem);
@@ -505,17 +562,17 @@ __global__ void __launch_bounds__(kPanelThreads, VEC ? 3 : 4) k_panel(const Pane
     // Every thread commits one group per tile slot (empty groups included), so
     // wait_group counts the same groups in every thread.
     for (int s = 0; s < kPanelStages - 1; ++s) {
-        if (s < mine) issue<EB>(a, panel_tile(first + s * step, a), sbase + s * stage);
+        if (s < mine) issue<EB>(a, panel_tile<AM>(first + s * step, a), sbase + s * stage);
         cp_async_commit();
     }
     uint32_t slot = 0, ahead = kPanelStages - 1;    // stage of tile i and of tile i + S - 1
     for (int64_t i = 0; i < mine; ++i) {
         const int64_t nxt = i + kPanelStages - 1;
-        if (nxt < mine) issue<EB>(a, panel_tile(first + nxt * step, a), sbase + ahead * stage);
+        if (nxt < mine) issue<EB>(a, panel_tile<AM>(first + nxt * step, a), sbase + ahead * stage);
         cp_async_commit();
         cp_async_wait<kPanelStages - 1>();           // tile i has landed (this thread's part)
         __syncthreads();                             // ... and every other thread's part
-        drain<EB, VEC>(a, panel_tile(first + i * step, a), smem + slot * stage);
+        drain<EB, VEC, AM>(a, panel_tile<AM>(first + i * step, a), smem + slot * stage);
         __syncthreads();                             // stage `slot` may be refilled
         slot = slot + 1 == kPanelStages ? 0 : slot + 1;
         ahead = ahead + 1 == kPanelStages ? 0 : ahead + 1;
@@ -556,7 +613,7 @@ k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
     const uint32_t phi = 1u << a.phi_lg;
     const uint32_t box_bytes = ((uint32_t)a.ta * EB + 16) * ((uint32_t)a.tb >> a.phi_lg);
     auto load = [&](int64_t i, uint32_t s) {          // one thread: tile i into stage s
-        const PanelTile ti = panel_tile(first + i * step, a);
+        const PanelTile ti = panel_tile<false>(first + i * step, a);
         dev::mbar_arrive_expect_tx(&full[s], phi * box_bytes);
         for (uint32_t j = 0; j < phi; ++j) {
             if (a.drop_load && i == 0 && j == 0) continue;   // test hook: the wait expires
@@ -580,7 +637,7 @@ k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
         const bool ok = dev::mbar_wait(&full[slot], (uint32_t)(i / kPanelStages) & 1u,
                                        (uint64_t)a.timeout_ns);
         if (__syncthreads_or(!ok)) break;           // every thread leaves together
-        drain<EB, false>(a, panel_tile(first + i * step, a), smem + slot * stage);
+        drain<EB, false, false>(a, panel_tile<false>(first + i * step, a), smem + slot * stage);
         __syncthreads();                            // stage `slot` may be refilled
         slot = slot + 1 == kPanelStages ? 0 : slot + 1;
         ahead = ahead + 1 == kPanelStages ? 0 : ahead + 1;
@@ -608,35 +665,29 @@ cudaError_t launch_panel_tma(int eb, const PanelArgs& a, const PanelMaps& maps, 
     return launch_kernel(k_panel_tma<2>, dim3(grid), dim3(kPanelThreads), smem, st, pdl, maps, a);
 }
 
-const void* panel_kernel(int eb, bool vec) {
+namespace {
+template <int EB, bool VEC>
+const void* pick(bool am) {
+    return am ? reinterpret_cast<const void*>(&k_panel<EB, VEC, true>)
+              : reinterpret_cast<const void*>(&k_panel<EB, VEC, false>);
+}
+}  // namespace
+
+const void* panel_kernel(int eb, bool vec, bool am) {
     switch (eb) {
-    case 1: return vec ? reinterpret_cast<const void*>(&k_panel<1, true>)
-                       : reinterpret_cast<const void*>(&k_panel<1, false>);
-    case 2: return vec ? reinterpret_cast<const void*>(&k_panel<2, true>)
-                       : reinterpret_cast<const void*>(&k_panel<2, false>);
-    case 4: return vec ? reinterpret_cast<const void*>(&k_panel<4, true>)
-                       : reinterpret_cast<const void*>(&k_panel<4, false>);
-    case 8: return vec ? reinterpret_cast<const void*>(&k_panel<8, true>)
-                       : reinterpret_cast<const void*>(&k_panel<8, false>);
-    default: return reinterpret_cast<const void*>(&k_panel<16, false>);
+    case 1: return vec ? pick<1, true>(am) : pick<1, false>(am);
+    case 2: return vec ? pick<2, true>(am) : pick<2, false>(am);
+    case 4: return vec ? pick<4, true>(am) : pick<4, false>(am);
+    case 8: return vec ? pick<8, true>(am) : pick<8, false>(am);
+    default: return pick<16, false>(am);
     }
 }
 
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,
                          bool pdl) {
-    const dim3 g(grid), b(kPanelThreads);
-    const bool v = a.vec != 0;
-    switch (eb) {
-    case 1: return v ? launch_kernel(k_panel<1, true>, g, b, smem, st, pdl, a)
-                     : launch_kernel(k_panel<1, false>, g, b, smem, st, pdl, a);
-    case 2: return v ? launch_kernel(k_panel<2, true>, g, b, smem, st, pdl, a)
-                     : launch_kernel(k_panel<2, false>, g, b, smem, st, pdl, a);
-    case 4: return v ? launch_kernel(k_panel<4, true>, g, b, smem, st, pdl, a)
-                     : launch_kernel(k_panel<4, false>, g, b, smem, st, pdl, a);
-    case 8: return v ? launch_kernel(k_panel<8, true>, g, b, smem, st, pdl, a)
-                     : launch_kernel(k_panel<8, false>, g, b, smem, st, pdl, a);
-    default: return launch_kernel(k_panel<16, false>, g, b, smem, st, pdl, a);
-    }
+    using Kernel = void (*)(const PanelArgs);
+    const Kernel k = reinterpret_cast<Kernel>(panel_kernel(eb, a.vec != 0, a.amerged != 0));
+    return launch_kernel(k, dim3(grid), dim3(kPanelThreads), smem, st, pdl, a);
 }
 
 }  // namespace tl

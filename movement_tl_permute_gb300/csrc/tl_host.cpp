@@ -417,7 +417,7 @@ int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2, i
     const int64_t n_copy = (int64_t)nblk * tb, n_store = (int64_t)ta * tb;
     const int64_t samples = 32 * 64;
     const int V = 16 / eb;
-    const int64_t qb8 = vec ? (int64_t)tb * eb / 128 : 1;
+    const int64_t qb8 = vec ? ((int64_t)tb * eb + 127) / 128 : 1;
     auto skew = [&](int64_t b) { return vec ? b / V : 0; };          // 16-byte units
     const int64_t units = vec ? (int64_t)((ta + 3) / 4) * qb8 : 0;
     struct Cand {
@@ -488,7 +488,7 @@ int panel_pitch(int ta, int tb, int eb, int64_t ssb, int64_t b1, int64_t ssb2, i
                         for (int l = 0; l < 32; ++l) {
                             const int64_t a = 4 * g4 + l / 8, qq = 8 * qg + l % 8;
                             const int64_t b = qq * V + k;
-                            o[l] = a < ta ? off(a, b) : -1;
+                            o[l] = a < ta && b < tb ? off(a, b) : -1;
                         }
                         store += bank_degree(32, o, eb, true);
                     }
@@ -671,11 +671,20 @@ bool panel_src_aligned(const Plan& p, int64_t ta) {
 // element (6.2 against 5.7 TB/s on odd-pitch fp32 transposes); the other block-row
 // layouts gain from the runs (by up to 30 % on 2-byte elements, 64 % on 1-byte
 // transposes).  Packed rows are decided by panel_packed_vec_ok as well.
+// Tile heights whose dst row pieces the 16-byte run walk covers: whole 16-byte units,
+// at least one 128-byte group of them, and at least 3/4 of the lanes of the 8-unit
+// groups busy (a height of 100 4-byte elements: 25 units in 4 groups).
+bool panel_vec_rows_ok(int64_t tb, int eb) {
+    const int64_t bytes = tb * eb, units = bytes / 16, groups = (units + 7) / 8;
+    return bytes % 16 == 0 && bytes >= 128 && 4 * units >= 3 * 8 * groups;
+}
+
 bool panel_dst_vec(const Plan& p, int64_t tb, bool packed, bool aligned) {
     const int eb = p.eb;
-    if (p.panel_elem_stores || eb > 8 || (tb * eb) % 128 != 0) return false;
+    if (p.panel_elem_stores || eb > 8 || !panel_vec_rows_ok(tb, eb)) return false;
     if (eb == 4 && !packed && !aligned) return false;
-    bool ok = p.dst_mis16 == 0 && (p.ds_a * eb) % 16 == 0;
+    bool ok = p.dst_mis16 == 0 && (p.ds_a * eb) % 16 == 0 &&
+              (p.panel_a1 == 0 || (p.panel_ds_a2 * eb) % 16 == 0);
     for (int i = 0; i < p.batch.n; ++i) ok = ok && (p.batch.ds[i] * eb) % 16 == 0;
     if (p.panel_b1 > 0 && !packed)
         ok = ok && (p.ss_b * eb) % 16 == 0 && (p.panel_ss_b2 * eb) % 16 == 0;
@@ -690,7 +699,7 @@ bool panel_dst_vec(const Plan& p, int64_t tb, bool packed, bool aligned) {
 // fast element by element, and keep doing so.
 bool panel_dst_run(const Plan& p, int64_t tb) {
     return !p.panel_vec && !p.panel_elem_stores && p.eb <= 4 && tb <= 16 && tb == p.ext_b &&
-           p.ds_a == tb && p.panel_b1 == 0;
+           p.ds_a == tb && p.panel_b1 == 0 && p.panel_a1 == 0;
 }
 
 // Phase-major stage for block rows (TMA phase maps, k_panel_tma, or cp.async into
@@ -703,7 +712,8 @@ int panel_tma_phases(const Plan& p, int64_t ta, int64_t tb) {
     const int eb = p.eb;
     // (1-byte tiles keep the block-row stage: their word walk's rotation is searched
     // for it)
-    if (eb == 1 || eb > 8 || p.panel_b1 != 0 || p.batch.n > 3 || p.panel_vec || p.panel_run)
+    if (eb == 1 || eb > 8 || p.panel_b1 != 0 || p.panel_a1 != 0 || p.batch.n > 3 ||
+        p.panel_vec || p.panel_run)
         return 0;
     // rows of ta * eb + 16 bytes, an odd number of 16-byte blocks: the phase blocks'
     // rows then fall in distinct bank groups
@@ -720,6 +730,35 @@ int panel_tma_phases(const Plan& p, int64_t ta, int64_t tb) {
 }
 
 }  // namespace
+
+// A short a axis (under 64 elements) takes in the next src axis when src is dense
+// across the two (that axis's src stride equals the a extent): the tile's src rows
+// stay contiguous and grow, and each tile row's dst offset splits a into its two
+// axes (the panel kernel's drow_off).  Only where the whole a x b plane is under
+// 16 KiB: high-rank permutes of short axes otherwise get tiles of a few KiB.
+// Measured on GB300 (one box, merged against unmerged): 10^8 reversed fp32 3.98
+// against 0.95 TB/s and fp64 3.54 against 2.58, 16^7 reversed fp16 4.89 against
+// 2.35; planes of 27 KiB and more stay faster unmerged (24^6 fp16 4.47 against 4.05,
+// a 6-D fp32 with a = 28 4.71 against 4.10).
+void panel_merge_a(Plan* p) {
+    if (p->ext_a >= 64 || p->ext_a * p->ext_b * p->eb >= 16384) return;
+    for (int i = 0; i < p->batch.n; ++i) {
+        if (p->batch.ss[i] != p->ext_a) continue;
+        const int64_t merged = p->ext_a * p->batch.ext[i];
+        if (merged >= (1LL << 31)) return;
+        p->panel_a1 = p->ext_a;
+        p->panel_ds_a2 = p->batch.ds[i];
+        p->ext_a = merged;
+        p->batch_total /= p->batch.ext[i];
+        for (int j = i; j + 1 < p->batch.n; ++j) {
+            p->batch.ext[j] = p->batch.ext[j + 1];
+            p->batch.ss[j] = p->batch.ss[j + 1];
+            p->batch.ds[j] = p->batch.ds[j + 1];
+        }
+        --p->batch.n;
+        return;
+    }
+}
 
 void plan_panel(Plan* p, int tile_bytes, int rows) {
     const int eb = p->eb;
@@ -745,6 +784,15 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
         if (capped) ta = (256 - 16 / eb) / (32 / eb) * (32 / eb);
         if (ta * tb < E && !capped)   // a short a extent: the tile grows along b instead
             tb = std::min(round_up((E + ta - 1) / ta, ru), p->ext_b);
+        // the same number of tiles along b, evened out (whole 16-byte dst pieces): b =
+        // 100 4-byte elements takes 52 + 48 rows instead of 96 + 4 (measured on 10^8
+        // reversed fp32 with a merged a: the 4-row tiles cost 30 %)
+        if (tb < p->ext_b) {
+            const int64_t nb = (p->ext_b + tb - 1) / tb;
+            const int64_t even = round_up((p->ext_b + nb - 1) / nb, std::max(1, 16 / eb));
+            if (even < tb && (panel_vec_rows_ok(even, eb) || !panel_vec_rows_ok(tb, eb)))
+                tb = even;
+        }
     }
     int64_t stage;
     for (;;) {
@@ -786,7 +834,7 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
             // row (measured on odd-pitch transposes: u8 3.2 -> 3.6 TB/s; 2-byte elements
             // stay faster element by element, 4.4 against 3.4)
             p->panel_words = !p->panel_vec && !p->panel_run && !p->panel_elem_stores &&
-                             eb == 1 && p->panel_b1 == 0;
+                             eb == 1 && p->panel_b1 == 0 && p->panel_a1 == 0;
             p->panel_nblk = p->panel_aligned ? (int)(ta * eb / 16) : panel_blocks_per_row(ta, eb);
             // skewed rows for 16-byte dst runs: 16 more bytes per 16 / eb rows; the
             // pitch search runs when at least its narrowest pitch fits
@@ -975,6 +1023,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         p.dst_mis16 = d0 & 15;
         p.panel_elem_stores = (flags & TL_FLAG_PANEL_ELEMENT_STORES) != 0;
         panel_merge_b(&p);
+        panel_merge_a(&p);
         plan_panel(&p, 0);
     } else if (path == TL_PATH_COLS) {
         p.vec_bytes = 16;

@@ -48,6 +48,8 @@ struct Plan {
     int panel_stage = 0;                // PANEL: shared-memory bytes of one ring stage
     int64_t panel_b1 = 0;               // PANEL: inner extent of b when two axes are merged
     int64_t panel_ss_b2 = 0;            // PANEL: src stride of the outer merged axis
+    int64_t panel_a1 = 0;               // PANEL: inner extent of a when two axes are merged
+    int64_t panel_ds_a2 = 0;            // PANEL: dst stride of the outer merged a axis
     bool panel_aligned = false;         // PANEL: every src row starts on a 16-byte boundary
     bool panel_vec = false;             // PANEL: tiles stored as 16-byte dst runs
     bool panel_elem_stores = false;     // PANEL: 16-byte dst runs declined by the caller

@@ -207,6 +207,11 @@ struct PanelArgs {
     // TMA phase maps (k_panel_tma, tma = 1) or by cp.async
     int32_t tma, phase, phi_lg, phase_bytes, tma_rank;
     int32_t drop_load;           // test hook: skip one phase load of the first tile
+    // a may be two src-contiguous axes merged (amerged = 1): a = hi * a1 + lo, dst
+    // offset lo * ds_a + hi * ds_a2 (a fits 32 bits)
+    int32_t amerged, pad3;
+    int64_t ds_a2;
+    dev::DivU32 d_a1;
     int64_t timeout_ns;
     int32_t* status;
 };
@@ -218,7 +223,8 @@ struct PanelMaps {
 cudaError_t launch_panel_tma(int eb, const PanelArgs& a, const PanelMaps& maps, int grid,
                              int smem, cudaStream_t st, bool pdl);
 const void* panel_tma_kernel(int eb);
-const void* panel_kernel(int eb, bool vec);   // vec: the 16-byte dst run kernel
+// vec: the 16-byte dst run kernel; am: a is two merged axes (two-level dst offsets)
+const void* panel_kernel(int eb, bool vec, bool am);
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,
                          bool pdl);
 

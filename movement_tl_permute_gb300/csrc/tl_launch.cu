@@ -140,8 +140,8 @@ int get_device_info(DevInfo* out) {
                             tile_smem_bytes(st, rows)) != cudaSuccess)
                         return TL_ERR_CUDA;
             }
-            for (int v = 0; v < 2; ++v)
-                if (cudaFuncSetAttribute(panel_kernel(1 << i, v != 0),
+            for (int v = 0; v < 4; ++v)
+                if (cudaFuncSetAttribute(panel_kernel(1 << i, (v & 1) != 0, (v & 2) != 0),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kPanelMaxSmem) != cudaSuccess)
                     return TL_ERR_CUDA;
@@ -346,7 +346,7 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
             int per_sm = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm,
                                                               p.panel_tma ? panel_tma_kernel(p.eb)
-                                                                          : panel_kernel(p.eb, p.panel_vec),
+                                                                          : panel_kernel(p.eb, p.panel_vec, p.panel_a1 > 0),
                                                               kPanelThreads, l.smem) !=
                     cudaSuccess ||
                 per_sm < 1) {
@@ -375,7 +375,7 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
 // The panel tile size and height are tuning options: re-plan the panel layout for them.
 void apply_panel_tile(Plan& p, const tl_permute_opts* o) {
     if (p.path != TL_PATH_PANEL || !o) return;
-    const bool kib = o->panel_tile_kib >= 4 && o->panel_tile_kib <= 32;
+    const bool kib = o->panel_tile_kib >= 4 && o->panel_tile_kib <= 48;
     const bool rows = o->tile_rows >= 16 && o->tile_rows <= 1024;
     if (!kib && !rows) return;
     plan_panel(&p, kib ? o->panel_tile_kib * 1024 : 0, rows ? o->tile_rows : 0);
@@ -584,9 +584,12 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.vpitch = p.panel_mode == kPanelRows ? p.pitch : p.tile_cols * eb;
         a.vdelta = p.panel_mode == kPanelRows && !a.merged ? (int32_t)((p.ss_b * eb) & 15) : 0;
         a.vskew = a.vec && p.panel_mode == kPanelRows ? 1 : 0;
-        a.qb8 = (int32_t)std::max<int64_t>(1, (int64_t)p.tile_rows * eb / 128);
+        a.qb8 = (int32_t)std::max<int64_t>(1, ((int64_t)p.tile_rows * eb + 127) / 128);
         a.wrot_s = p.panel_wrot_s;
         a.wrot_m = p.panel_wrot_m;
+        a.amerged = p.panel_a1 > 0 ? 1 : 0;
+        a.ds_a2 = p.panel_ds_a2;
+        a.d_a1 = dev::make_divu32((uint32_t)(p.panel_a1 > 0 ? p.panel_a1 : 1));
         a.run = p.panel_run ? 1 : 0;
         a.words = p.panel_words ? 1 : 0;
         a.tiles_a = (p.ext_a + a.ta - 1) / a.ta;
@@ -762,6 +765,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     info.panel_b1 = (int32_t)p.panel_b1;
     info.panel_vec = p.panel_vec ? 1 : p.panel_run ? 2 : p.panel_words ? 3 : 0;
     info.panel_wrot = p.panel_wrot_s | (p.panel_wrot_m << 8);
+    info.panel_a1 = (int32_t)p.panel_a1;
     info.tiles = p.tiles;
     int ndev = 0;
     DevInfo d;

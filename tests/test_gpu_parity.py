@@ -285,6 +285,43 @@ def test_panel_tma_phase_maps(eb):
                   flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
 
 
+def _merged_a_cases():
+    # high-rank permutes of short axes: the src-contiguous axis a (under 64 elements)
+    # is merged with the next src axis, and the tile columns cross the boundary
+    # between the two (7, 5, 9 and 6 do not divide the tile); the last case's src is
+    # padded past the merged pair, which stays dense
+    out = []
+    for shape, perm in (((6,) * 7, (6, 5, 4, 3, 2, 1, 0)),
+                        ((8,) * 6, (5, 4, 3, 2, 1, 0)),
+                        ((5, 7, 9, 11, 13), (4, 3, 2, 1, 0)),
+                        ((16, 3, 40, 7, 9), (1, 3, 0, 4, 2)),
+                        ((3, 4, 5, 6, 7, 8), (5, 2, 4, 1, 3, 0))):
+        ss, ds = perm_layouts(shape, perm)
+        out.append((shape, ss, ds))
+    shape = (9, 33, 5, 6)
+    ss, ds = perm_layouts(shape, (3, 2, 1, 0))
+    out.append((shape, (ss[0] * 2, ss[1] * 2, ss[2], ss[3]), ds))
+    return out
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
+def test_panel_merged_a(eb):
+    """A short src-contiguous axis merged with the next src axis where the a x b
+    plane is under 16 KiB: each tile row's dst offset splits a into its two axes.
+    Vector, word and element stores, unaligned bases and small tiles give the
+    oracle's bytes; planes past the bound stay unmerged and give the same bytes."""
+    for i, (shape, ss, ds) in enumerate(_merged_a_cases()):
+        plan = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb, path="panel")
+        a1 = shape[list(ss).index(1)]
+        assert plan["path"] == "panel", (shape, plan)
+        assert plan["panel_a1"] == a1 or (eb == 16 and plan["panel_a1"] == 0), (shape, plan)
+        check(shape, ss, ds, eb, "panel", seed=900 + i)
+        check(shape, ss, ds, eb, "panel", seed=910 + i, src_off=1, dst_off=3)
+        check(shape, ss, ds, eb, "panel", seed=920 + i, panel_tile_kib=4)
+        check(shape, ss, ds, eb, "panel", seed=930 + i,
+              flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
+
+
 @pytest.mark.parametrize("eb", [1, 2, 4])
 def test_panel_run_stores(eb):
     """Planes -> interleaved channels: a tile's dst is one run, stored as 16-byte

@@ -301,6 +301,56 @@ def test_interleaved_channel_paths():
                 assert got in ("panel", "tile"), ("chw->hwc", C, eb, got)
 
 
+def _permuted(shape, perm):
+    ss = L.row_major_strides(shape)
+    pst = L.row_major_strides(tuple(shape[p] for p in perm))
+    ds = [0] * len(shape)
+    for i, p in enumerate(perm):
+        ds[p] = pst[i]
+    return tuple(ss), tuple(ds)
+
+
+def test_panel_merges_short_a_with_its_dense_src_neighbour():
+    """A short src-contiguous axis a takes in the next src axis only where src is dense
+    across the two and the a x b plane is under 16 KiB; merged tiles never take the
+    walks that step one dst offset per row (runs, words) or the phase maps."""
+    for eb in (1, 2, 4, 8, 16):
+        shape = (10,) * 8
+        ss, ds = _permuted(shape, tuple(range(7, -1, -1)))
+        p = tl.tl_plan(SRC, DST, shape, ss, ds, eb, path="panel")
+        # the plane is a (10) x b (10 x 10 merged in dst): 1000 * eb bytes
+        assert p["panel_a1"] == (10 if 1000 * eb < 16384 else 0), (eb, p)
+        if p["panel_a1"]:
+            assert p["panel_vec"] in (0, 1) and p["panel_mode"] in (0, 1), p
+            # the merged a spans the tile columns: 100 elements, tiles of at most 100
+            assert p["tile_cols"] <= 100
+        # src padded past the pair: the merge needs ss of the next axis == ext_a
+        ss_pad = tuple(x * 2 if i < 7 else x for i, x in enumerate(ss))
+        q = tl.tl_plan(SRC, 1 << 40, shape, ss_pad, ds, eb, path="panel")
+        assert q["panel_a1"] == 0, (eb, q)
+    # a plane of 16 KiB or more stays unmerged (24^6 fp16: 24 x 576 x 2 bytes)
+    shape = (24,) * 6
+    ss, ds = _permuted(shape, (5, 0, 4, 1, 3, 2))
+    assert tl.tl_plan(SRC, DST, shape, ss, ds, 2, path="panel")["panel_a1"] == 0
+    # a of 64 elements or more is never merged
+    shape = (4, 4, 64, 64)
+    ss, ds = _permuted(shape, (3, 2, 1, 0))
+    assert tl.tl_plan(SRC, DST, shape, ss, ds, 1, path="panel")["panel_a1"] == 0
+
+
+def test_panel_tile_heights_are_even():
+    """The tile count along b is kept and the rows spread evenly in whole 16-byte units
+    (b = 100 fp32 rows: 52 + 48, not 96 + 4), unless that loses the 16-byte run walk."""
+    shape = (10,) * 8
+    ss, ds = _permuted(shape, tuple(range(7, -1, -1)))
+    p = tl.tl_plan(SRC, DST, shape, ss, ds, 4, path="panel")
+    assert p["tile_rows"] == 52 and p["panel_vec"] == 1, p
+    # 1-byte rows: 272 rows at 128 per tile would even out to 96 rows, under the 128
+    # bytes the run walk needs, so the tile keeps 128 rows
+    p = tl.tl_plan(SRC, DST, (272, 517), (517, 1), (1, 272), 1, path="panel")
+    assert p["tile_rows"] == 128 and p["panel_vec"] == 1, p
+
+
 def test_panel_tma_phase_map_invariants():
     """Every plan that loads rows by TMA phase maps keeps the TMA rules by
     construction, over seeded odd-pitch layouts: the box's x coordinate a0 * eb and its
@@ -373,6 +423,14 @@ def _word_degrees(ta, tb, eb, pitch, row_off, rs, rm, aligned):
     return out
 
 
+def _vec_rows_ok(tb, eb):
+    """Tile heights the 16-byte run walk covers: whole 16-byte units, at least 128
+    bytes, 8-unit groups at least 3/4 busy."""
+    units = tb * eb // 16
+    groups = -(-units // 8)
+    return (tb * eb) % 16 == 0 and tb * eb >= 128 and 4 * units >= 24 * groups
+
+
 @pytest.mark.parametrize("shape,perm,eb", PANEL_LAYOUTS)
 def test_panel_layout_against_the_bank_model(shape, perm, eb):
     """The shared-memory layout the planner picks for the panel kernel, replayed
@@ -425,9 +483,10 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         # stride but a's (1) multiples of 16 bytes
         aligned = SRC % 16 == 0 and (ta * eb) % 16 == 0 and all(
             (x * eb) % 16 == 0 for x in p["src_str"] if x != 1)
-        # 16-byte dst runs: 1..8-byte elements, whole 128-byte row pieces, every dst
-        # stride but b's (1) a multiple of 16 bytes
-        vec = eb <= 8 and (tb * eb) % 128 == 0 and DST % 16 == 0 and all(
+        # 16-byte dst runs: 1..8-byte elements, row pieces of whole 16-byte units
+        # that keep 3/4 of the walk's lanes busy, every dst stride but b's (1) a
+        # multiple of 16 bytes
+        vec = eb <= 8 and _vec_rows_ok(tb, eb) and DST % 16 == 0 and all(
             (x * eb) % 16 == 0 for x in p["dst_str"] if x not in (1, b1))
         if b1:
             vec = vec and (ssb * eb) % 16 == 0 and (ssb2 * eb) % 16 == 0
@@ -466,7 +525,7 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         # are busy (the planner's measured rule; 1-byte rows keep word stores)
         busy = 4 * ta >= 3 * 4 * ((ta + 3) // 4)
         ok = {1: False, 2: ta >= 4 and busy, 4: ta != 2, 8: busy}[eb]
-        vec = ok and (tb * eb) % 128 == 0 and DST % 16 == 0 and all(
+        vec = ok and _vec_rows_ok(tb, eb) and DST % 16 == 0 and all(
             (x * eb) % 16 == 0 for x in p["dst_str"] if x not in (1, b1))
         ext_b = [x for x, d in zip(p["extent"], p["dst_str"]) if d == 1][0]
         ds_a = [d for x, d in zip(p["src_str"], p["dst_str"]) if x == 1][0]

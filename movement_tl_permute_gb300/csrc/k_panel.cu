@@ -67,10 +67,14 @@ __device__ __forceinline__ int64_t drow_off(const PanelArgs& a, const PanelTile&
 // Byte offset of tile row b in a block-row stage: b * pitch, or, for phase-major
 // stages (filled by TMA phase maps or by cp.async in the same arrangement), row
 // b / phi of the block of phase b % phi.
+// (1-byte elements never take a phase-major stage: their block rows stay b * pitch)
+template <int EB>
 __device__ __forceinline__ uint32_t stage_row(const PanelArgs& a, uint32_t b) {
-    if (a.phase)
-        return (b & ((1u << a.phi_lg) - 1u)) * (uint32_t)a.phase_bytes +
-               (b >> a.phi_lg) * (uint32_t)a.pitch;
+    if constexpr (EB != 1) {
+        if (a.phase)
+            return (b & ((1u << a.phi_lg) - 1u)) * (uint32_t)a.phase_bytes +
+                   (b >> a.phi_lg) * (uint32_t)a.pitch;
+    }
     return b * (uint32_t)a.pitch;
 }
 
@@ -93,7 +97,10 @@ __device__ __forceinline__ int64_t row_offset(uint32_t bb, const PanelTile& ti,
 // CTAs then write runs of group_b * tb elements of dst rows while the tiles beside
 // each other along a, which share the 16-byte blocks at their row ends, are in
 // flight together and meet those blocks in L2.
-template <bool AM>
+// The batch loop is unrolled over TL_MAX_DIMS (keeping the coordinates) or a plain
+// loop: measured per width, 1-byte tiles store a third faster with the plain loop
+// (odd-pitch u8 transposes 2.4 -> 3.6 TB/s), the wider ones keep the unrolled one.
+template <bool AM, bool UNROLLED>
 __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
     int64_t item, ia, ib;
     if (a.use32) {
@@ -127,10 +134,7 @@ __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
     r.a0 = a0;
     r.so = a0 + b_offset(b0, a);
     r.dof = AM ? b0 : a0 * a.ds_a + b0;
-    r.c[0] = r.c[1] = r.c[2] = 0;
-#pragma unroll
-    for (int i = 0; i < TL_MAX_DIMS; ++i) {
-        if (i >= a.nb) break;
+    auto axis = [&](int i) {           // batch axis i: its coordinate, offsets added
         int64_t c;
         if (a.use32) {
             const uint32_t q = dev::div_u32((uint32_t)item, a.d_bext[i]);
@@ -140,9 +144,20 @@ __device__ __forceinline__ PanelTile panel_tile(int64_t t, const PanelArgs& a) {
             c = item % a.bext[i];
             item /= a.bext[i];
         }
-        if (i < 3) r.c[i] = (int32_t)c;
         r.so += c * a.bss[i];
         r.dof += c * a.bds[i];
+        return c;
+    };
+    r.c[0] = r.c[1] = r.c[2] = 0;
+    if constexpr (UNROLLED) {          // (the TMA loads take the three innermost coordinates)
+#pragma unroll
+        for (int i = 0; i < TL_MAX_DIMS; ++i) {
+            if (i >= a.nb) break;
+            const int64_t c = axis(i);
+            if (i < 3) r.c[i] = (int32_t)c;
+        }
+    } else {
+        for (int i = 0; i < a.nb; ++i) axis(i);
     }
     if constexpr (AM) {          // (b0, batch item) alone, then the split of a0
         const uint32_t hi = dev::div_u32((uint32_t)a0, a.d_a1);
@@ -181,7 +196,7 @@ __device__ __forceinline__ void issue(const PanelArgs& a, const PanelTile& ti, u
             const uintptr_t row = base + (uintptr_t)(row_offset(b, ti, a) * EB);
             const uint32_t blocks = ((uint32_t)(row & 15) + ti.va * EB + 15) >> 4;
             if (k < blocks)
-                cp_async16(sb + (skew ? b * pitch + (b / V) * skew : stage_row(a, b)) + 16 * k,
+                cp_async16(sb + (skew ? b * pitch + (b / V) * skew : stage_row<EB>(a, b)) + 16 * k,
                            (row & ~uintptr_t(15)) + 16 * k);
         }
     } else {   // kPanelFlat: rows packed back to back (ss_b == ta == va)
@@ -210,16 +225,6 @@ __device__ __forceinline__ uint4 pack16(const uint8_t (&v)[16]) {
     return make_uint4(w(0), w(1), w(2), w(3));
 }
 
-// Store one landed tile as 16-byte dst runs (used when the dst rows of every tile
-// start on 16-byte boundaries and tb * EB is a multiple of 128).  Unit (e, q) is
-// dst row e of the tile, block q of it (elements b = qV .. qV + V - 1, V = 16 / EB).
-// A warp takes 4 rows x 8 blocks, so each of its stores writes four whole 128-byte
-// lines; a thread keeps its block q for the whole tile and walks e, so the V row
-// addresses are computed once.  Block-row stages are skewed: row b starts 16 bytes
-// further per V rows (at b * pitch + 16 * (b / V)), so the 8 blocks of a warp read
-// 8 distinct 16-byte bank groups at every step whatever the pitch (the host's pitch
-// search replays these reads on the bank model of the TVM "permute_layout" page,
-// "Algorithm" step 2).
 // dst address of the 16-byte run of tile row a0 + e at b0, for a walk whose e steps
 // by de: a pointer advanced by de * ds_a, or, for merged a, the split of each e
 template <int EB, bool AM>
@@ -247,6 +252,17 @@ struct RunPtr<EB, true> {
     __device__ __forceinline__ void next() {}
 };
 
+// Store one landed tile as 16-byte dst runs (used when the dst rows of every tile
+// start on 16-byte boundaries and tb * EB is a whole number of 16-byte blocks).
+// Unit (e, q) is dst row e of the tile, block q of it (elements b = qV .. qV + V - 1,
+// V = 16 / EB).  A warp takes 4 rows x 8 blocks, so each of its stores writes four
+// 128-byte pieces (lanes past the last block of a row idle); a thread keeps its block
+// q for the whole tile and walks e, so the V row addresses
+// are computed once.  Block-row stages are skewed: row b starts 16 bytes
+// further per V rows (at b * pitch + 16 * (b / V)), so the 8 blocks of a warp read
+// 8 distinct 16-byte bank groups at every step whatever the pitch (the host's pitch
+// search replays these reads on the bank model of the TVM "permute_layout" page,
+// "Algorithm" step 2).
 template <int EB, bool AM>
 __device__ __forceinline__ void drain_vec(const PanelArgs& a, const PanelTile& ti,
                                           const uint8_t* st) {
@@ -372,7 +388,7 @@ __device__ __forceinline__ void drain_words(const PanelArgs& a, const PanelTile&
     const uint32_t st0 = (uint32_t)(st - smem_w);
     const uint32_t delta = (uint32_t)a.vdelta;
     const uint32_t mis0 = (uint32_t)(reinterpret_cast<uintptr_t>(a.src + ti.so * EB) & 15);
-    auto row = [&](uint32_t b) { return st0 + stage_row(a, b) + ((mis0 + b * delta) & 15u); };
+    auto row = [&](uint32_t b) { return st0 + stage_row<EB>(a, b) + ((mis0 + b * delta) & 15u); };
     uint8_t* d0 = a.dst + (ti.dof + (int64_t)warp * a.ds_a) * EB;   // first dst row of the warp
     const int64_t dstep = (int64_t)kWarps * a.ds_a * EB;
     const uint32_t lead = (uint32_t)((4 - (reinterpret_cast<uintptr_t>(d0) & 3)) & 3) / EB;
@@ -520,7 +536,7 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
         // each thread keeps one b and steps a by kPanelThreads / tb
         const uint32_t b = threadIdx.x % tb, de = kPanelThreads / tb;
         if (b >= ti.vb) return;
-        const uint8_t* sp = rows ? st + stage_row(a, b) + mis(b) : st + mis0 + b * ta * EB;
+        const uint8_t* sp = rows ? st + stage_row<EB>(a, b) + mis(b) : st + mis0 + b * ta * EB;
         uint32_t e = threadIdx.x / tb;
         if constexpr (AM) {          // two-level dst offsets of a: one split per row
             T* dst = reinterpret_cast<T*>(a.dst) + b;
@@ -541,7 +557,7 @@ __device__ __forceinline__ void drain(const PanelArgs& a, const PanelTile& ti, c
     for (uint32_t f = threadIdx.x; f < n; f += kPanelThreads) {
         const uint32_t e = dev::div_u32(f, a.d_tb), b = f - e * tb;   // a, b in the tile
         if (e >= ti.va || b >= ti.vb) continue;
-        const uint32_t off = rows ? stage_row(a, b) + mis(b) + e * EB : mis0 + (b * ta + e) * EB;
+        const uint32_t off = rows ? stage_row<EB>(a, b) + mis(b) + e * EB : mis0 + (b * ta + e) * EB;
         T* drow = AM ? reinterpret_cast<T*>(a.dst) + drow_off<AM>(a, ti, e) : d + (int64_t)e * a.ds_a;
         drow[b] = *reinterpret_cast<const T*>(st + off);
     }
@@ -562,17 +578,17 @@ __global__ void __launch_bounds__(kPanelThreads, VEC ? 3 : 4) k_panel(const Pane
     // Every thread commits one group per tile slot (empty groups included), so
     // wait_group counts the same groups in every thread.
     for (int s = 0; s < kPanelStages - 1; ++s) {
-        if (s < mine) issue<EB>(a, panel_tile<AM>(first + s * step, a), sbase + s * stage);
+        if (s < mine) issue<EB>(a, panel_tile<AM, EB != 1>(first + s * step, a), sbase + s * stage);
         cp_async_commit();
     }
     uint32_t slot = 0, ahead = kPanelStages - 1;    // stage of tile i and of tile i + S - 1
     for (int64_t i = 0; i < mine; ++i) {
         const int64_t nxt = i + kPanelStages - 1;
-        if (nxt < mine) issue<EB>(a, panel_tile<AM>(first + nxt * step, a), sbase + ahead * stage);
+        if (nxt < mine) issue<EB>(a, panel_tile<AM, EB != 1>(first + nxt * step, a), sbase + ahead * stage);
         cp_async_commit();
         cp_async_wait<kPanelStages - 1>();           // tile i has landed (this thread's part)
         __syncthreads();                             // ... and every other thread's part
-        drain<EB, VEC, AM>(a, panel_tile<AM>(first + i * step, a), smem + slot * stage);
+        drain<EB, VEC, AM>(a, panel_tile<AM, EB != 1>(first + i * step, a), smem + slot * stage);
         __syncthreads();                             // stage `slot` may be refilled
         slot = slot + 1 == kPanelStages ? 0 : slot + 1;
         ahead = ahead + 1 == kPanelStages ? 0 : ahead + 1;
@@ -613,7 +629,7 @@ k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
     const uint32_t phi = 1u << a.phi_lg;
     const uint32_t box_bytes = ((uint32_t)a.ta * EB + 16) * ((uint32_t)a.tb >> a.phi_lg);
     auto load = [&](int64_t i, uint32_t s) {          // one thread: tile i into stage s
-        const PanelTile ti = panel_tile<false>(first + i * step, a);
+        const PanelTile ti = panel_tile<false, true>(first + i * step, a);
         dev::mbar_arrive_expect_tx(&full[s], phi * box_bytes);
         for (uint32_t j = 0; j < phi; ++j) {
             if (a.drop_load && i == 0 && j == 0) continue;   // test hook: the wait expires
@@ -637,7 +653,7 @@ k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
         const bool ok = dev::mbar_wait(&full[slot], (uint32_t)(i / kPanelStages) & 1u,
                                        (uint64_t)a.timeout_ns);
         if (__syncthreads_or(!ok)) break;           // every thread leaves together
-        drain<EB, false, false>(a, panel_tile<false>(first + i * step, a), smem + slot * stage);
+        drain<EB, false, false>(a, panel_tile<false, true>(first + i * step, a), smem + slot * stage);
         __syncthreads();                            // stage `slot` may be refilled
         slot = slot + 1 == kPanelStages ? 0 : slot + 1;
         ahead = ahead + 1 == kPanelStages ? 0 : ahead + 1;

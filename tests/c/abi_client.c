@@ -82,6 +82,25 @@ int main(void) {
     expect(rc == TL_OK && info.path == (int32_t)TL_PATH_WARP, "tl_plan chooses the warp path");
     expect(info.k == 2 && info.shift == 3 && info.mask == 3, "tl_plan reports the swizzle");
 
+    /* a high-rank permute of short axes: 10^8 reversed, 4-byte elements; the short
+       src-contiguous axis is merged with the next src axis (dense across the two) */
+    {
+        int64_t shp[8], ss8[8], ds8[8];
+        for (int i = 0; i < 8; ++i) {
+            int64_t st = 1;
+            for (int j = i + 1; j < 8; ++j) st *= 10;
+            shp[i] = 10;
+            ss8[i] = st;                   /* row-major */
+            int64_t dt = 1;
+            for (int j = 0; j < i; ++j) dt *= 10;
+            ds8[i] = dt;                   /* axes reversed */
+        }
+        rc = tl_plan((const void *)(uintptr_t)(1u << 20), (const void *)((uintptr_t)1 << 36), 8,
+                     shp, ss8, ds8, 4, NULL, &info);
+        expect(rc == TL_OK && info.path == (int32_t)TL_PATH_PANEL && info.panel_a1 == 10,
+               "tl_plan merges the short a axis (panel_a1 = 10)");
+    }
+
     /* validation launches nothing and needs no device */
     rc = tl_permute(NULL, NULL, 4, sf_shape, sf_src, sf_dst, 3, NULL);
     expect(rc == TL_ERR_ELEM_BYTES, "elem_bytes 3 -> TL_ERR_ELEM_BYTES");

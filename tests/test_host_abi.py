@@ -338,6 +338,40 @@ def test_panel_merges_short_a_with_its_dense_src_neighbour():
     assert tl.tl_plan(SRC, DST, shape, ss, ds, 1, path="panel")["panel_a1"] == 0
 
 
+def test_panel_merge_invariants_on_seeded_high_rank_layouts():
+    """Seeded high-rank permutes of short axes: wherever the planner merges a, the
+    merged axis is the src-contiguous one with its dense src neighbour, the plane was
+    under 16 KiB, the merged tiles take neither the run nor the word walk nor a phase
+    map, and the stage fits the panel kernel's shared memory."""
+    rng = np.random.default_rng(77)
+    merged = 0
+    for _ in range(300):
+        nd = int(rng.integers(4, 9))
+        shape = tuple(int(x) for x in rng.integers(2, 13, size=nd))
+        perm = tuple(int(x) for x in rng.permutation(nd))
+        eb = int(rng.choice([1, 2, 4, 8, 16]))
+        ss, ds = _permuted(shape, perm)
+        try:
+            p = tl.tl_plan(SRC, DST, shape, ss, ds, eb, path="panel")
+        except tl.TLError as e:
+            assert e.name == "TL_ERR_PATH", e
+            continue
+        assert p["smem_bytes"] <= 3 * (160 * 1024 // 3) + 128
+        if not p["panel_a1"]:
+            continue
+        merged += 1
+        ext, cs, cd = p["extent"], p["src_str"], p["dst_str"]   # canonical layout
+        ia = list(cs).index(1)                          # the src-contiguous axis
+        a1 = ext[ia]
+        assert p["panel_a1"] == a1 < 64, (shape, perm, p)
+        nxt = [i for i, x in enumerate(cs) if x == a1]  # its dense src neighbour
+        assert nxt and cd[nxt[0]] != cd[ia] * a1, (shape, perm, p)
+        assert cd[nxt[0]] != 1                          # a batch axis, not b
+        assert p["panel_vec"] in (0, 1) and p["panel_mode"] in (0, 1), p
+        assert p["tile_cols"] <= a1 * ext[nxt[0]]
+    assert merged >= 20, merged
+
+
 def test_panel_tile_heights_are_even():
     """The tile count along b is kept and the rows spread evenly in whole 16-byte units
     (b = 100 fp32 rows: 52 + 48, not 96 + 4), unless that loses the 16-byte run walk."""

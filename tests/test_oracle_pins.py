@@ -456,3 +456,48 @@ def test_sample_agrees_with_whole_permute():
         got = whole.reshape(-1, eb)[offs]
         assert np.array_equal(got, vals)
         assert sorted(offs.tolist()) == list(range(n))            # a bijection
+
+
+@pytest.mark.parametrize("eb", [1, 2, 4, 8, 16])
+def test_sample_with_offset_and_padded_strides_equals_numpy(eb):
+    """The sampler's src_offset: a padded, offset source view (numpy as_strided) read
+    at every coordinate, against numpy's own view of the same bytes and against the
+    whole-tensor loop given the same offset ("Buffers and memory", "Declaring
+    buffers": the address is data + elem_offset + the layout's offset of c)."""
+    rng = np.random.default_rng(7 * eb + 1)
+    dt = NP_BY_WIDTH[eb]
+    for _ in range(12):
+        nd = int(rng.integers(1, 5))
+        shape = tuple(int(x) for x in rng.integers(1, 6, size=nd))
+        pad = [int(x) for x in rng.integers(0, 3, size=nd)]
+        strides, acc = [], 1
+        for e, p in zip(reversed(shape), reversed(pad)):
+            strides.append(acc)
+            acc *= e + p
+        strides = tuple(reversed(strides))
+        off = int(rng.integers(1, 9))
+        raw = np.frombuffer(rng.bytes((off + acc) * eb), dtype=np.uint8).copy()
+        view = np.lib.stride_tricks.as_strided(raw.view(dt)[off:], shape=shape,
+                                               strides=tuple(s * eb for s in strides))
+        perm = tuple(int(p) for p in rng.permutation(nd))
+        _, ds = _perm_layouts(shape, perm)
+        coords = np.array(list(itertools.product(*[range(e) for e in shape])),
+                          dtype=np.int64).reshape(-1, nd)
+        offs, vals = oracle.sample(raw, coords, strides, ds, eb, src_offset=off)
+        # numpy reads element c of the offset view directly
+        want_vals = np.stack([_bytes(view[tuple(c)]) for c in coords])
+        assert np.array_equal(vals, want_vals)
+        # the dst offsets are those of the transposed dense output
+        want = _bytes(np.transpose(view, perm))
+        got = np.zeros(int(np.prod(shape)) * eb, dtype=np.uint8)
+        got.reshape(-1, eb)[offs] = vals
+        assert np.array_equal(got, want)
+        # and the sampler agrees with the whole-tensor loop at the same offset
+        whole = np.zeros_like(got)
+        oracle.permute(raw, whole, shape, strides, ds, eb, src_offset=off)
+        assert np.array_equal(whole, got)
+        # an offset of zero reads different bytes (the offset is not ignored)
+        _, vals0 = oracle.sample(raw, coords, strides, ds, eb, src_offset=0)
+        want0 = np.lib.stride_tricks.as_strided(raw.view(dt), shape=shape,
+                                                strides=tuple(s * eb for s in strides))
+        assert np.array_equal(vals0, np.stack([_bytes(want0[tuple(c)]) for c in coords]))

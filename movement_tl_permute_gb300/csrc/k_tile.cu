@@ -36,7 +36,8 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full[kMaxTileStages];
     __shared__ __align__(8) uint64_t empty[kMaxTileStages];
-    __shared__ TileOut info[kMaxTileStages];  // destination of the tile in each stage
+    // destination of the tile in each stage, packed into one 16-byte word
+    __shared__ __align__(16) uint4 info[kMaxTileStages];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -67,7 +68,8 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                     break;
                 }
                 const TileCoord tc = tile_coord(t, a);
-                info[s] = make_out<EB, TB>(tc, a);      // published by the release below
+                // one 16-byte store, published by the release below
+                sts128(smem_addr(&info[s]), pack_out<EB, TB>(tc, a));
                 mbar_arrive_expect_tx(&full[s], kBytes);
                 tma_load(smem + s * kBytes, &tmap, &full[s], a.rank,
                          (int)(tc.ta * kRowBytes), (int)(tc.tb * TB), (int)tc.bc[0],
@@ -90,7 +92,7 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
             if (lane == 0) report(a.status, TL_ERR_TIMEOUT);
             break;
         }
-        const TileOut o = info[s];
+        const TileOut o = unpack_out<EB>(lds128(smem_addr(&info[s])), a);
         const uint32_t base = smem_addr(smem + s * kBytes);
 #pragma unroll
         for (int rb0 = 0; rb0 < TB; rb0 += kRows)

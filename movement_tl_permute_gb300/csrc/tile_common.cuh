@@ -220,9 +220,10 @@ __device__ __forceinline__ void consume<1>(uint32_t tile, const TileOut& o, int 
 // groups of `group_b` tile rows, b fastest inside a group, so concurrently
 // running CTAs write runs of many 128-byte lines (one group spanning all of b
 // makes the writes one front-to-back stream).
+// Every coordinate is a TMA box coordinate, so each fits in 32 bits.
 struct TileCoord {
-    int64_t ta, tb;
-    int64_t bc[3];
+    int32_t ta, tb;
+    int32_t bc[3];
 };
 
 __device__ __forceinline__ TileCoord tile_coord(int64_t t, const TileArgs& a) {
@@ -255,13 +256,13 @@ __device__ __forceinline__ TileCoord tile_coord(int64_t t, const TileArgs& a) {
     const int64_t first_tb = grp * a.group_b;
     const int64_t gsize = min(a.group_b, a.tiles_b - first_tb);
     const int64_t in_grp = local - grp * a.group_b * a.tiles_a;
-    r.tb = first_tb + in_grp % gsize;
-    r.ta = in_grp / gsize;
+    r.tb = (int32_t)(first_tb + in_grp % gsize);
+    r.ta = (int32_t)(in_grp / gsize);
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
         r.bc[i] = 0;
         if (i < a.nbatch) {
-            r.bc[i] = item % a.bext[i];
+            r.bc[i] = (int32_t)(item % a.bext[i]);
             item /= a.bext[i];
         }
     }
@@ -283,6 +284,30 @@ __device__ __forceinline__ TileOut make_out(const TileCoord& tc, const TileArgs&
     o.rows = (int32_t)min((int64_t)TB, a.ext_b - b0);
     o.vec = a.vec_store;
     o.full = (o.vec && o.cols == TA && o.rows == TB) ? 1 : 0;
+    return o;
+}
+
+// The record of a tile as one 16-byte word (the producer stores it with one aligned
+// 16-byte store, each consumer warp reads it with one 16-byte load): the dst
+// address, then valid columns (bits 0-8), valid rows (9-17) and "full" (bit 18).
+// The column stride and the run alignment are the same for every tile.
+template <int EB, int TB = kRows>
+__device__ __forceinline__ uint4 pack_out(const TileCoord& tc, const TileArgs& a) {
+    const TileOut o = make_out<EB, TB>(tc, a);
+    const uint64_t p = reinterpret_cast<uint64_t>(o.base);
+    return make_uint4((uint32_t)p, (uint32_t)(p >> 32),
+                      (uint32_t)o.cols | ((uint32_t)o.rows << 9) | ((uint32_t)o.full << 18), 0u);
+}
+
+template <int EB>
+__device__ __forceinline__ TileOut unpack_out(const uint4 v, const TileArgs& a) {
+    TileOut o;
+    o.base = reinterpret_cast<uint8_t*>((uint64_t)v.x | ((uint64_t)v.y << 32));
+    o.cstride = a.ds_a * EB;
+    o.cols = (int32_t)(v.z & 511u);
+    o.rows = (int32_t)((v.z >> 9) & 511u);
+    o.full = (int32_t)((v.z >> 18) & 1u);
+    o.vec = a.vec_store;
     return o;
 }
 

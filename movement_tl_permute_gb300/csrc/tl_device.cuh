@@ -170,6 +170,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     return v;
 }
 
+// 16-byte shared-memory store (one aligned vector store).
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // 16-byte global store / load.
 __device__ __forceinline__ void stg128(void* p, uint4 v) {
     asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),

@@ -165,6 +165,24 @@ def test_tile_path_visit_groups(eb, group):
 
 
 @pytest.mark.parametrize("eb", WIDTHS)
+def test_tile_walk_across_grid_sizes(eb):
+    # Each CTA walks its tiles by adding the grid size to the tile coordinates digit
+    # by digit (tb, ta, three batch axes).  Grids of 1 .. more than the 72 tiles make
+    # every digit carry, several digits at once, and the walk leave the range.
+    a = 272 // eb                       # 3 tiles along a (the last one 16 bytes wide)
+    shape = (3, 2, 2, 200, a)           # 2 tiles along b (the last 72 rows)
+    ss, ds = perm_layouts(shape, (2, 1, 0, 4, 3))   # batch axes reversed: none merge
+    for i, ctas in enumerate((1, 5, 7, 11, 24, 71, 72, 200)):
+        check(shape, ss, ds, eb, "tile", seed=300 + i, max_ctas=ctas)
+        check(shape, ss, ds, eb, "cluster", seed=310 + i, max_ctas=2 * ctas)
+    # a batch axis between the plane's two axes in dst, and odd batch extents
+    shape = (5, 3, 130, a)
+    ss, ds = perm_layouts(shape, (1, 3, 0, 2))
+    for i, ctas in enumerate((3, 13, 64)):
+        check(shape, ss, ds, eb, "tile", seed=320 + i, max_ctas=ctas)
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
 @pytest.mark.parametrize("staging,receive,warps", [(1, 1, 8), (3, 1, 8), (1, 3, 8), (4, 2, 8),
                                                    (8, 4, 8), (2, 1, 4), (2, 2, 4), (1, 3, 4)])
 def test_cluster_ring_depths(eb, staging, receive, warps):

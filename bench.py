@@ -318,6 +318,25 @@ def cpu_baseline(w, src, dst, budget_s=10.0):
                                                   2 * n * w.elem_bytes / 2**20, runs, per)}, m
 
 
+def sampled_parity(w, src, got, m, threads):
+    """Bit-exact check of the GPU output ``got`` on the oracle's leading-m sample.
+
+    The oracle writes the sample's image into two buffers filled with different
+    canary bytes: the bytes where the two agree are exactly the ones the sample
+    writes, and only those are compared (the rest of dst is not checked here).
+    Returns (bit_exact, bytes compared)."""
+    import numpy as np
+    import oracle
+
+    a = np.full(got.nbytes, 0xA5, dtype=np.uint8)
+    b = np.full(got.nbytes, 0x5A, dtype=np.uint8)
+    for buf in (a, b):
+        oracle.permute(src, buf, sample_layout(w, m), w.src_strides, w.dst_strides,
+                       w.elem_bytes, nthreads=threads)
+    mask = a == b
+    return bool(np.array_equal(got[mask], a[mask])), int(mask.sum())
+
+
 # ---------------------------------------------------------------------------
 # arms
 # ---------------------------------------------------------------------------
@@ -382,6 +401,100 @@ def run_reference(args, w):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+# The five configurations of the headline metric, each measured in the same run:
+# (entry name, workload, forced path).  The first is the one-warp latency case.
+CONFIG_RUNS = [("tile_transpose", "tile_transpose", "auto"),
+               ("tile_transpose_cluster", "tile_transpose", "cluster"),
+               ("mx_sf", "mx_sf", "auto"), ("attention", "attention", "auto"),
+               ("t2d_u8", "t2d_u8", "auto"), ("t2d_f16", "t2d_f16", "auto"),
+               ("t2d_f32", "t2d_f32", "auto"), ("t2d_f64", "t2d_f64", "auto"),
+               ("t2d_v16", "t2d_v16", "auto")]
+
+
+def all_configs(args, tl, dev, stream, head_name, head_src):
+    """Every configuration of the headline metric, one at a time (buffers freed in
+    between): ``[GB/s, fraction of the measured HBM peak, bit_exact]`` per HBM
+    workload (K back-to-back launches timed with CUDA events after 3 warm-ups;
+    parity on an oracle sample of about a second), and the one-warp scale-factor
+    transpose as microseconds per call, host launches and graph replay."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from movement_tl_permute_gb300 import workloads
+
+    peak, _ = measured_peak()
+    sptr = stream.cuda_stream
+    threads = max(1, min(len(os.sched_getaffinity(0)), oracle.max_threads()))
+    steps = max(10, min(args.steps, 100))
+    out = {}
+
+    # config 1: the one-warp SF transpose (latency; L2-resident)
+    w = workloads.get("sf_transpose")
+    src_np = workloads.make_input(w)
+    s_gpu = torch.from_numpy(src_np).to(dev)
+    d_gpu = torch.zeros(w.dst_elems * w.elem_bytes, dtype=torch.uint8, device=dev)
+    call = (w.shape, w.src_strides, w.dst_strides, w.elem_bytes)
+    reps = 2000
+    for _ in range(5):
+        tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), *call, sptr)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), *call, sptr)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us_stream = e0.elapsed_time(e1) * 1e3 / reps
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        cap = torch.cuda.current_stream(dev).cuda_stream
+        for _ in range(reps):
+            tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), *call, cap)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us_graph = e0.elapsed_time(e1) * 1e3 / reps
+    want = np.zeros(w.dst_elems * w.elem_bytes, dtype=np.uint8)
+    oracle.permute(src_np, want, *call)
+    out["sf_transpose"] = {"us_per_call_stream": round(us_stream, 3),
+                           "us_per_call_graph": round(us_graph, 3),
+                           "bit_exact": bool(np.array_equal(d_gpu.cpu().numpy(), want))}
+    del graph, s_gpu, d_gpu
+
+    # configs 2-5 (HBM-bound)
+    for name, wname, path in CONFIG_RUNS:
+        w = workloads.get(wname)
+        src_np = head_src if wname == head_name else workloads.make_input(w)
+        s_gpu = torch.from_numpy(src_np).to(dev)
+        d_gpu = torch.empty(w.dst_elems * w.elem_bytes, dtype=torch.uint8, device=dev)
+        call = (w.shape, w.src_strides, w.dst_strides, w.elem_bytes)
+
+        def one():
+            tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), *call, sptr, path=path)
+
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(steps):
+            one()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        gbps = w.algorithmic_bytes / (e0.elapsed_time(e1) / steps * 1e-3) / 1e9
+        got = d_gpu.cpu().numpy()
+        del s_gpu, d_gpu
+        torch.cuda.empty_cache()
+        m, _ = oracle_rate(w, src_np, np.empty_like(got), threads, 0.5)
+        ok, _ = sampled_parity(w, src_np, got, m, threads)
+        out[name] = [round(gbps, 1), round(gbps / peak, 4), ok]
+        del got
+    return out
 
 
 def run_ours(args, w):
@@ -518,9 +631,14 @@ def run_ours(args, w):
 
     # ------------------------------------------------ CPU oracle + sampled parity
     got = dst_pin.numpy()                  # result of the last e2e step (same input)
-    check = got.copy()
-    base, m = cpu_baseline(w, src_np, check, budget_s=args.cpu_budget)
-    parity = bool(np.array_equal(check, got))
+    scratch = np.empty_like(got)
+    base, m = cpu_baseline(w, src_np, scratch, budget_s=args.cpu_budget)
+    del scratch
+    parity, n_checked = sampled_parity(w, src_np, got, m, base["cores"])
+    del got
+    configs = (all_configs(args, tl, dev, stream, w.name, src_np)
+               if args.configs == "all" or (args.configs == "auto" and w.name == DEFAULT_WORKLOAD
+                                            and not args.leading and world == 1) else None)
 
     bytes_step = w.algorithmic_bytes
     value = whole_job_gbps(bytes_step, args.steps, world, ms_max)
@@ -537,7 +655,8 @@ def run_ours(args, w):
                        input_sha256=input_digest(src_np)),
         "pct_hbm_peak": round(100.0 * value / world / peak, 2),
         "parity": {"bit_exact": parity,
-                   "checked": "GPU output vs oracle on the cpu_baseline sample"},
+                   "checked": "GPU output vs oracle on the cpu_baseline sample: the %d dst "
+                              "bytes it writes, of %d" % (n_checked, nbytes_dst)},
         "roofline": {"bound": "hbm", "achieved": round(per_launch_gbps, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(per_launch_gbps / peak, 4),
                      "traffic": traffic, "kernel": KERNEL_NAMES.get(plan["path"]),
@@ -553,6 +672,10 @@ def run_ours(args, w):
                           if singles else None),
         "clocks": clock_summary,
     }
+    if configs is not None:
+        line["configs"] = configs
+        parity = parity and all(v[2] for k, v in configs.items() if isinstance(v, list)) and \
+            configs["sf_transpose"]["bit_exact"]
     print(json.dumps(line), flush=True)
     if dist.is_initialized():
         dist.destroy_process_group()
@@ -578,6 +701,9 @@ def main(argv=None):
                     help="timed steps as stream launches, or replayed from one CUDA graph that "
                          "holds all of them (auto: graph for the one-warp workload, whose "
                          "step is shorter than a host-side launch)"),
+    ap.add_argument("--configs", choices=["auto", "all", "none"], default="auto",
+                    help="also measure every configuration of the metric (auto: with the "
+                         "default workload at full size on one GPU)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -443,8 +443,10 @@ def all_configs(args, tl, dev, stream, head_name, head_src):
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    h0 = time.perf_counter()
     for _ in range(reps):
         tl.tl_permute_ex(s_gpu.data_ptr(), d_gpu.data_ptr(), *call, sptr)
+    host_us = (time.perf_counter() - h0) * 1e6 / reps
     e1.record(stream)
     torch.cuda.synchronize(dev)
     us_stream = e0.elapsed_time(e1) * 1e3 / reps
@@ -463,6 +465,7 @@ def all_configs(args, tl, dev, stream, head_name, head_src):
     want = np.zeros(w.dst_elems * w.elem_bytes, dtype=np.uint8)
     oracle.permute(src_np, want, *call)
     out["sf_transpose"] = {"us_per_call_stream": round(us_stream, 3),
+                           "host_us_per_call": round(host_us, 3),
                            "us_per_call_graph": round(us_graph, 3),
                            "bit_exact": bool(np.array_equal(d_gpu.cpu().numpy(), want))}
     del graph, s_gpu, d_gpu

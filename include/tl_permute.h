@@ -131,7 +131,13 @@ TL_API int tl_choose_xor_k(int ndim, const int64_t *extent, const int64_t *src_s
 TL_API int tl_bank_conflicts(int n_lanes, const int64_t *lane_offsets, int elem_bytes, int model);
 
 /*
- * tl_permute -- materialise the permutation on the GPU (the hot path).
+ * tl_permute -- materialise the permutation on the GPU (the hot path): for every
+ * coordinate c of shape, the element at src + sum(c_i * src_strides_i) is copied to
+ * dst + sum(c_i * dst_strides_i) (TVM "Buffers and memory", section "Declaring
+ * buffers": an element's address is the data pointer plus the element offset plus
+ * the layout's offset of its coordinate; `B.permute` of "Buffer APIs" is this copy
+ * with dst strides of the permuted row-major layout), as raw bits of one of the
+ * widths "permute_layout" admits ("What it accepts").
  *
  *   src          device pointer to the source's element at coordinate 0
  *   dst          device pointer to the destination's element at coordinate 0
@@ -220,9 +226,14 @@ typedef struct tl_permute_opts {
                                      with an extent of 16 or less) */
 } tl_permute_opts;
 
-/* tl_permute with options (path forcing, status word, buffer bounds).
- * opts may be NULL (same as tl_permute).  A forced path that does not apply
- * returns TL_ERR_PATH and launches nothing. */
+/* tl_permute with options (path forcing, status word, buffer bounds): the same
+ * operation ("Buffers and memory", "Declaring buffers"; "permute_layout", "What it
+ * accepts").  Forcing a path is the dispatch choice "permute_layout" describes as a
+ * variant that accepts or declines a call ("What it accepts"): a forced path that
+ * does not apply returns TL_ERR_PATH and launches nothing, as a declined variant
+ * does.  The status word reports the bounded waits of the mbarrier completions
+ * ("copy_async -> dsmem", "Algorithm"; the wait_until pull request, "The
+ * operation").  opts may be NULL (same as tl_permute). */
 TL_API int tl_permute_ex(const void *src, void *dst, int ndim, const int64_t *shape,
                   const int64_t *src_strides, const int64_t *dst_strides, int elem_bytes,
                   tl_stream_t stream, const tl_permute_opts *opts);
@@ -271,11 +282,24 @@ TL_API int tl_plan(const void *src, const void *dst, int ndim, const int64_t *sh
             const int64_t *src_strides, const int64_t *dst_strides, int elem_bytes,
             const tl_permute_opts *opts, tl_plan_info *out);
 
-/* Human-readable text of a status code (static storage). */
+/* Human-readable text of a status code (static storage).  The decline reasons
+ * are worded after the reasons the permute_layout dispatch gives ("permute_layout",
+ * "What it accepts"); the others name this library's own errors. */
 TL_API const char *tl_status_string(int status);
 
 /* Number of kernels this library has launched in this process. */
 TL_API uint64_t tl_launch_count(void);
+
+/*
+ * Number of tl_permute / tl_permute_ex / tl_plan calls served from the plan cache.
+ * The library keeps the plans of recent calls (256 slots, process-wide, guarded by
+ * a mutex): a call whose layout, element width, flags, tuning options, device and
+ * base-address offsets within 16 bytes match an earlier call's reuses its plan and
+ * launch shape.  The checks that depend on the pointers themselves (null pointers,
+ * caller-given bounds, overlap of the two byte ranges) still run on every call, and
+ * calls whose ranges meet (in place, or rejected as aliased) are planned afresh.
+ */
+TL_API uint64_t tl_plan_cache_hits(void);
 
 /* TL_VERSION of the loaded library. */
 TL_API int tl_version(void);
@@ -285,12 +309,12 @@ TL_API int tl_version(void);
  * that cannot allocate device memory.  The TVM pages have no counterpart: it
  * exists for integration, not for the method.
  *
- * Who needs it: code that runs while a stream is being captured into a CUDA
- * graph (a cudaMalloc there breaks the capture), plug-ins living inside a
- * framework whose caching allocator already owns the device's memory budget,
- * and fixed-memory or real-time deployments whose policy forbids allocating
- * after start-up.  Such callers cannot provide the status word that
- * tl_permute_ex takes in opts.dev_status.
+ * Who needs it: plug-ins living inside a framework whose caching allocator
+ * already owns the device's memory budget (a cudaMalloc of their own would
+ * compete with it), code on latency-critical paths where cudaMalloc's implicit
+ * device synchronisation is not acceptable, and fixed-memory or real-time
+ * deployments whose policy forbids allocating after start-up.  Such callers
+ * cannot provide the status word that tl_permute_ex takes in opts.dev_status.
  *
  * What it does: the same launch as tl_permute_ex with TL_PATH_TILE, except that
  * the kernel's only scratch -- the 4-byte status word it writes when a bounded
@@ -315,6 +339,8 @@ TL_API int tl_version(void);
  * calls share the one array and it keeps the last call's contents: calls whose
  * work overlaps on the GPU (other streams, other host threads) race on the
  * status word, so one call's report may be cleared or overwritten by another's.
+ * The looked-up address is kept for the life of the process: after a
+ * cudaDeviceReset of a device, do not call this entry point on it again.
  */
 #define TL_NOALLOC_SCRATCH_BYTES 256
 TL_API int tl_permute_tile_noalloc(const void *src, void *dst, int ndim, const int64_t *shape,

@@ -8,13 +8,14 @@ loading it raises.
 
 The names follow the C ABI: ``tl_layout_canon``, ``tl_choose_xor_k``,
 ``tl_bank_conflicts``, ``tl_permute``, ``tl_permute_ex``, ``tl_plan``,
-``tl_status_string``, ``tl_launch_count``, ``tl_version``.  ``permute`` is the
+``tl_status_string``, ``tl_launch_count``, ``tl_plan_cache_hits``, ``tl_version``.  ``permute`` is the
 same call for PyTorch tensors (it reads their device pointers, byte bounds and
 the current CUDA stream).
 """
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -23,6 +24,7 @@ __all__ = [
     "TL_FLAG_DEBUG_CHECKS", "TL_FLAG_TEST_SKIP_HOST_BOUNDS", "TL_FLAG_PANEL_ELEMENT_STORES",
     "load", "library_path", "tl_layout_canon", "tl_choose_xor_k", "tl_bank_conflicts",
     "tl_permute", "tl_permute_ex", "tl_plan", "tl_status_string", "tl_launch_count",
+    "tl_plan_cache_hits",
     "tl_version", "permute", "tl_permute_tile_noalloc",
 ]
 
@@ -113,6 +115,8 @@ def load():
         lib.tl_status_string.restype = ctypes.c_char_p
         lib.tl_launch_count.argtypes = []
         lib.tl_launch_count.restype = ctypes.c_uint64
+        lib.tl_plan_cache_hits.argtypes = []
+        lib.tl_plan_cache_hits.restype = ctypes.c_uint64
         lib.tl_version.argtypes = []
         lib.tl_permute_tile_noalloc.argtypes = [vp, vp, ctypes.c_int, i64p, i64p, i64p,
                                                 ctypes.c_int, vp, ctypes.POINTER(_i32)]
@@ -133,6 +137,25 @@ def _arr(vals):
     if n <= TL_MAX_DIMS:
         return _ARR_TYPES[n](*vals)
     return (_i64 * n)(*vals)
+
+
+# The launch calls pass the same few shapes, strides and options again and again;
+# the C side only reads them, so their ctypes forms are built once and reused.
+@functools.lru_cache(maxsize=4096)
+def _arr_of(t):
+    return _arr(t)
+
+
+def _carr(vals):
+    try:
+        return _arr_of(tuple(vals))
+    except TypeError:                    # unhashable values: build afresh
+        return _arr(vals)
+
+
+@functools.lru_cache(maxsize=1024)
+def _opts_of(items):
+    return _opts(**dict(items))
 
 
 def _check(rc: int, where: str) -> int:
@@ -157,6 +180,10 @@ def tl_status_string(code: int) -> str:
 
 def tl_launch_count() -> int:
     return int(load().tl_launch_count())
+
+
+def tl_plan_cache_hits() -> int:
+    return int(load().tl_plan_cache_hits())
 
 
 def tl_version() -> int:
@@ -222,8 +249,8 @@ def tl_permute(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides, elem
                stream: int = 0) -> None:
     """dst[sum c*dst_strides] = src[sum c*src_strides] on the GPU (device pointers)."""
     n = len(shape)
-    _check(load().tl_permute(int(src_ptr) or None, int(dst_ptr) or None, n, _arr(shape),
-                             _arr(src_strides), _arr(dst_strides), int(elem_bytes),
+    _check(load().tl_permute(int(src_ptr) or None, int(dst_ptr) or None, n, _carr(shape),
+                             _carr(src_strides), _carr(dst_strides), int(elem_bytes),
                              int(stream) or None), "tl_permute")
 
 
@@ -233,9 +260,12 @@ def tl_permute_ex(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides,
     src_bytes=..., dst_bytes=..., max_ctas=..., and the tile tuning fields
     tile_group, tile_stages, tile_ctas_per_sm, tile_l2_promotion, tile_rows,
     cluster_recv_stages, cluster_consumer_warps, panel_tile_kib"""
-    o = _opts(**opts)
+    try:
+        o = _opts_of(tuple(sorted(opts.items())))
+    except TypeError:                    # unhashable option values: build afresh
+        o = _opts(**opts)
     _check(load().tl_permute_ex(int(src_ptr) or None, int(dst_ptr) or None, len(shape),
-                                _arr(shape), _arr(src_strides), _arr(dst_strides),
+                                _carr(shape), _carr(src_strides), _carr(dst_strides),
                                 int(elem_bytes), int(stream) or None, ctypes.byref(o)),
            "tl_permute_ex")
 

@@ -95,7 +95,7 @@ k_cluster(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
         }
         if (!ok) report(a.status, TL_ERR_TIMEOUT);
         for (uint32_t i = issued > SS ? issued - SS : 0; i < issued; ++i)
-            mbar_wait(&loaded[i % SS], (i / SS) & 1, a.timeout_ns);
+            mbar_wait(&loaded[i % SS], (i / SS) & 1, kDrainFactor * a.timeout_ns);
     } else if (warp == kPusherWarp && lane == 0) {
         // ---------------------------------- pusher ----------------------------------
         uint32_t n = 0;

@@ -660,10 +660,11 @@ k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
     }
     if (threadIdx.x == 0 && i < mine) {
         dev::report(a.status, TL_ERR_TIMEOUT);
-        // do not leave while a load may still write this CTA's shared memory
+        // do not leave while a load may still write this CTA's shared memory (a
+        // longer bound than the wait that expired; past it the CTA leaves anyway)
         for (int64_t k = i; k < issued; ++k)
             dev::mbar_wait(&full[k % kPanelStages], (uint32_t)(k / kPanelStages) & 1u,
-                           (uint64_t)a.timeout_ns);
+                           dev::kDrainFactor * (uint64_t)a.timeout_ns);
     }
 }
 

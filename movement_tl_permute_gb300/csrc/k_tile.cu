@@ -76,9 +76,10 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                          (int)tc.bc[1], (int)tc.bc[2]);
             }
             if (!ok) report(a.status, TL_ERR_TIMEOUT);
-            // Do not leave while a load may still write this CTA's shared memory.
+            // Do not leave while a load may still write this CTA's shared memory (a
+            // longer bound than the wait that expired; past it the CTA leaves anyway).
             for (uint32_t i = issued > S ? issued - S : 0; i < issued; ++i)
-                mbar_wait(&full[i % S], (i / S) & 1, a.timeout_ns);
+                mbar_wait(&full[i % S], (i / S) & 1, kDrainFactor * a.timeout_ns);
         }
         return;
     }

@@ -101,6 +101,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// After a bounded wait has expired, a CTA waits this many times as long for its own
+// loads in flight before it leaves (a load that never lands leaves it anyway).
+constexpr uint64_t kDrainFactor = 4;
+
 // Waits for the phase of parity `parity` to complete.  Bounded: returns false once
 // `timeout_ns` of wall time has passed without completion.  Each try_wait already
 // suspends the thread for a while, so the loop does not spin hot.

@@ -910,6 +910,8 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         return TL_ERR_RANGE;
     int64_t sbytes, dbytes;
     if (!mul_ok(sspan + 1, eb, &sbytes) || !mul_ok(dspan + 1, eb, &dbytes)) return TL_ERR_RANGE;
+    p.sbytes = sbytes;
+    p.dbytes = dbytes;
     if (((src_bytes > 0 && sbytes > src_bytes) || (dst_bytes > 0 && dbytes > dst_bytes)) &&
         !(flags & TL_FLAG_TEST_SKIP_HOST_BOUNDS))
         return TL_ERR_BOUNDS;

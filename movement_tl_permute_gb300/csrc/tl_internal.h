@@ -27,6 +27,7 @@ struct Plan {
     int path = 0;          // TL_PATH_*; 0 with total == 0 means "nothing to do"
     int eb = 0;            // element bytes
     int64_t total = 0;     // elements
+    int64_t sbytes = 0, dbytes = 0;   // bytes each layout reaches from its base
     Axes sorted;           // unit axes dropped, sorted by dst stride (descending), merged
     Axes kept;             // unit axes dropped, order kept, merged (the page's canon)
 

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "tl_internal.h"
@@ -425,24 +426,166 @@ void fill_divs(int n, const int64_t* ext, dev::DivU32* div) {
     for (int i = 0; i < n; ++i) div[i] = dev::make_divu32((uint32_t)ext[i]);
 }
 
+// ---------------------------------------------------------------- plan cache
+// What a launch needs besides the pointers themselves: the plan, the tile tuning and
+// the launch shape.  They depend on the layout, the element width, the flags and
+// tuning options, the device, and the two base addresses only through their offsets
+// within 16 bytes (vector widths, the panel's row misalignment) and through whether
+// the two byte ranges meet (in-place and alias cases, never cached).  A repeated
+// call with the same key skips the planner; the checks that depend on the pointer
+// values themselves (null pointers, caller-given bounds, overlap of the two ranges)
+// still run on every call.
+struct Prepared {
+    Plan p;
+    TileTuning tt;
+    Launch l;
+};
+
+struct PlanKey {
+    int32_t dev, ndim, eb, smis, dmis;
+    uint32_t flags;
+    int32_t o[9];                  // the tuning options of tl_permute_opts
+    int32_t pad;
+    int64_t shape[kMaxDims], ss[kMaxDims], ds[kMaxDims];
+};
+
+constexpr int kPlanCacheSlots = 256;
+struct PlanSlot {
+    bool used = false;
+    PlanKey key;
+    Prepared val;
+};
+std::mutex g_cache_mu;
+PlanSlot g_cache[kPlanCacheSlots];
+std::atomic<uint64_t> g_cache_hits{0};
+std::atomic<int> g_have_device{-1};   // -1 unknown, 0 no CUDA device in this process, 1 yes
+
+// The current device, or -1 when the process has no CUDA device (remembered after
+// the first failed query: a device does not appear in a running process).
+int current_device() {
+    if (g_have_device.load(std::memory_order_relaxed) == 0) return -1;
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) {
+        if (g_have_device.load(std::memory_order_relaxed) < 0) {
+            const bool any = cudaGetDeviceCount(&n) == cudaSuccess && n > 0;
+            if (!any) cudaGetLastError();
+            g_have_device.store(any ? 1 : 0, std::memory_order_relaxed);
+            if (!any) return -1;
+        }
+        return dev;
+    }
+    cudaGetLastError();
+    g_have_device.store(0, std::memory_order_relaxed);
+    return -1;
+}
+
+// FNV-1a over the key's 64-bit words, then a final mix of the high bits.
+uint64_t key_hash(const PlanKey& k) {
+    static_assert(sizeof(PlanKey) % 8 == 0, "the key hashes as whole 64-bit words");
+    uint64_t w[sizeof(PlanKey) / 8];
+    std::memcpy(w, &k, sizeof w);
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < sizeof(PlanKey) / 8; ++i) h = (h ^ w[i]) * 1099511628211ull;
+    return h ^ (h >> 29);
+}
+
+// Validates the call and fills `out`: from the cache when the same key was planned
+// before, else by planning (and, with a device, sizing the launch) and caching the
+// result.  `launch`: a device is required (tl_permute_ex); otherwise the launch
+// shape is left at 0 when there is none (tl_plan).
+int prepare(const void* src, const void* dst, int ndim, const int64_t* shape,
+            const int64_t* ss, const int64_t* ds, int eb, const tl_permute_opts* opts,
+            bool launch, Prepared* out) {
+    const uint32_t flags = opts ? opts->flags : 0u;
+    const int dev = current_device();
+    const bool keyable = src && dst && ndim >= 0 && ndim <= kMaxDims &&
+                         (ndim == 0 || (shape && ss && ds)) && (dev >= 0 || !launch);
+    PlanKey key;
+    uint64_t h = 0;
+    if (keyable) {
+        std::memset(&key, 0, sizeof key);      // padding and unused axes compare equal
+        key.dev = dev;
+        key.ndim = ndim;
+        key.eb = eb;
+        key.smis = (int32_t)(reinterpret_cast<uintptr_t>(src) & 15);
+        key.dmis = (int32_t)(reinterpret_cast<uintptr_t>(dst) & 15);
+        key.flags = flags;
+        if (opts) {
+            const int32_t o[9] = {opts->max_ctas, opts->tile_group, opts->tile_stages,
+                                  opts->tile_ctas_per_sm, opts->tile_l2_promotion,
+                                  opts->tile_rows, opts->cluster_recv_stages,
+                                  opts->cluster_consumer_warps, opts->panel_tile_kib};
+            std::memcpy(key.o, o, sizeof o);
+        }
+        for (int i = 0; i < ndim; ++i) {
+            key.shape[i] = shape[i];
+            key.ss[i] = ss[i];
+            key.ds[i] = ds[i];
+        }
+        h = key_hash(key);
+        bool hit = false;
+        {
+            std::lock_guard<std::mutex> lk(g_cache_mu);
+            const PlanSlot& slot = g_cache[h % kPlanCacheSlots];
+            if (slot.used && std::memcmp(&slot.key, &key, sizeof key) == 0) {
+                *out = slot.val;
+                hit = true;
+            }
+        }
+        if (hit) {
+            // the checks on the pointer values themselves
+            const Plan& p = out->p;
+            if (p.total == 0) return TL_OK;
+            const int64_t sb = opts ? opts->src_bytes : 0, db = opts ? opts->dst_bytes : 0;
+            if (((sb > 0 && p.sbytes > sb) || (db > 0 && p.dbytes > db)) &&
+                !(flags & TL_FLAG_TEST_SKIP_HOST_BOUNDS))
+                return TL_ERR_BOUNDS;
+            const int64_t s0 = (int64_t)(uintptr_t)src, d0 = (int64_t)(uintptr_t)dst;
+            if (!(s0 < d0 + p.dbytes && d0 < s0 + p.sbytes)) {
+                g_cache_hits.fetch_add(1, std::memory_order_relaxed);
+                return TL_OK;
+            }
+            // the two ranges meet: plan afresh (in-place or alias), as on a miss
+        }
+    }
+    Prepared pr;
+    int rc = make_plan(src, dst, ndim, shape, ss, ds, eb, flags, opts ? opts->src_bytes : 0,
+                       opts ? opts->dst_bytes : 0, &pr.p);
+    if (rc != TL_OK) return rc;
+    pr.tt = tile_tuning(opts);
+    tile_defaults(pr.p, opts, pr.tt);
+    cluster_defaults(pr.p, pr.tt);
+    apply_tile_rows(pr.p, pr.tt);
+    apply_panel_tile(pr.p, opts);
+    DevInfo d;
+    const bool have = pr.p.total > 0 && dev >= 0 && get_device_info(&d) == TL_OK;
+    if (!have) {
+        if (dev >= 0) cudaGetLastError();
+        if (launch && pr.p.total > 0) return TL_ERR_CUDA;
+    }
+    pr.l = launch_shape(pr.p, have ? &d : nullptr, opts ? opts->max_ctas : 0, pr.tt);
+    *out = pr;
+    // cache plans whose ranges do not meet (and, for launches, whose shape is sized)
+    if (keyable && !pr.p.in_place && (have || !launch)) {
+        std::lock_guard<std::mutex> lk(g_cache_mu);
+        PlanSlot& slot = g_cache[h % kPlanCacheSlots];
+        slot.used = true;
+        slot.key = key;
+        slot.val = pr;
+    }
+    return TL_OK;
+}
+
 int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_t* ss,
         const int64_t* ds, int eb, cudaStream_t st, const tl_permute_opts* opts) {
     const uint32_t flags = opts ? opts->flags : 0u;
-    Plan p;
-    int rc = make_plan(src, dst, ndim, shape, ss, ds, eb, flags, opts ? opts->src_bytes : 0,
-                       opts ? opts->dst_bytes : 0, &p);
+    Prepared pr;
+    int rc = prepare(src, dst, ndim, shape, ss, ds, eb, opts, true, &pr);
     if (rc != TL_OK) return rc;
+    const Plan& p = pr.p;
     if (p.total == 0) return TL_OK;
-    DevInfo d;
-    rc = get_device_info(&d);
-    if (rc != TL_OK) return rc;
-    const int32_t max_ctas = opts ? opts->max_ctas : 0;
-    TileTuning tt = tile_tuning(opts);
-    tile_defaults(p, opts, tt);
-    cluster_defaults(p, tt);
-    apply_tile_rows(p, tt);
-    apply_panel_tile(p, opts);
-    const Launch l = launch_shape(p, &d, max_ctas, tt);
+    const TileTuning& tt = pr.tt;
+    const Launch& l = pr.l;
     // overlap this launch with the drain of the previous kernel in the stream
     const bool pdl = (flags & TL_FLAG_NO_PDL) == 0;
     const uint8_t* s8 = static_cast<const uint8_t*>(src);
@@ -733,11 +876,11 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
             const tl_permute_opts* opts, tl_plan_info* out) {
     using namespace tl;
     if (!out) return TL_ERR_ARG;
-    Plan p;
-    const uint32_t flags = opts ? opts->flags : 0u;
-    int rc = make_plan(src, dst, ndim, shape, src_strides, dst_strides, elem_bytes, flags,
-                       opts ? opts->src_bytes : 0, opts ? opts->dst_bytes : 0, &p);
+    Prepared pr;
+    int rc = prepare(src, dst, ndim, shape, src_strides, dst_strides, elem_bytes, opts, false,
+                     &pr);
     if (rc != TL_OK) return rc;
+    const Plan& p = pr.p;
     tl_plan_info info{};
     info.path = p.path;
     info.ndim = p.sorted.n;
@@ -753,11 +896,6 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         info.shift = p.shift;
         info.mask = p.mask;
     }
-    TileTuning tt = tile_tuning(opts);
-    tile_defaults(p, opts, tt);
-    cluster_defaults(p, tt);
-    apply_tile_rows(p, tt);
-    apply_panel_tile(p, opts);
     info.tile_rows = p.tile_rows;
     info.tile_cols = p.tile_cols;
     info.pitch = p.pitch;
@@ -767,13 +905,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     info.panel_wrot = p.panel_wrot_s | (p.panel_wrot_m << 8);
     info.panel_a1 = (int32_t)p.panel_a1;
     info.tiles = p.tiles;
-    int ndev = 0;
-    DevInfo d;
-    const bool have = p.total > 0 && cudaGetDeviceCount(&ndev) == cudaSuccess && ndev > 0 &&
-                      get_device_info(&d) == TL_OK;
-    if (!have) cudaGetLastError();   // clear a "no device" error on CPU-only hosts
-    const Launch l =
-        launch_shape(p, have ? &d : nullptr, opts ? opts->max_ctas : 0, tt);
+    const Launch& l = pr.l;
     info.grid = l.grid;
     info.block = l.block;
     info.smem_bytes = l.smem;
@@ -782,5 +914,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
 }
 
 uint64_t tl_launch_count(void) { return tl::g_launches.load(std::memory_order_relaxed); }
+
+uint64_t tl_plan_cache_hits(void) { return tl::g_cache_hits.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -10,7 +10,8 @@
 // The array's name is a host-side stand-in in host code, not a device address:
 // its device address is fetched once per device with cudaGetSymbolAddress (the
 // first call on each device does this set-up, with that device current) and then
-// passed to the kernel.
+// passed to the kernel.  The address is kept for the life of the process, so the
+// entry point is not for use on a device after a cudaDeviceReset of it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -53,6 +54,7 @@ extern "C" TL_API int tl_permute_tile_noalloc(const void* src, void* dst, int nd
     if (needed > TL_NOALLOC_SCRATCH_BYTES) return TL_ERR_BOUNDS;
 
     // Validate and plan first (host only), so a rejected call touches no device state.
+    // The plan is cached: the launch below reuses it instead of planning again.
     tl_plan_info info;
     tl_permute_opts opts{};
     opts.flags = TL_PATH_TILE;

@@ -445,8 +445,8 @@ def test_auto_paths_on_random_layouts():
 # edge cases
 # ---------------------------------------------------------------------------
 def test_tensor_level_permute_matches_torch():
-    """The README's example at a smaller size: a (B, H, S, D) -> (B, S, H, D)
-    bfloat16 permute through tl.permute on torch CUDA tensors equals torch's own
+    """An attention-style (B, H, S, D) -> (B, S, H, D) bfloat16 permute at a small
+    size, through tl.permute on torch CUDA tensors, equals torch's own
     transpose, and the planner names the chunk path; an fp32 2-D transpose into a
     transposed view equals .t()."""
     x = torch.randn(2, 8, 256, 128, dtype=torch.bfloat16, device="cuda")

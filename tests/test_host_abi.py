@@ -785,3 +785,62 @@ def test_rows_kernel_stage_is_conflict_free(R):
         assert tl.tl_bank_conflicts(lanes, 16, "hardware") == 1
     # the swizzle is a permutation of the warp's stage
     assert sorted(_stage_chunk(c, R) for c in range(32 * R)) == list(range(32 * R))
+
+
+# ---------------------------------------------------------------------------
+# plan cache
+# ---------------------------------------------------------------------------
+def test_plan_cache_hit_costs_under_a_microsecond(tmp_path):
+    """A repeated tl_plan (the planning half of every tl_permute) is served from the
+    plan cache: timed in C, without binding overhead."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    libdir = os.path.dirname(os.path.abspath(tl.load()._name))
+    exe = str(tmp_path / "plan_timing")
+    subprocess.run([cc, "-std=c99", "-O2", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(here, "c", "plan_timing.c"), "-L", libdir, "-ltl_permute",
+                    "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    hits = int(r.stdout.split("hits ")[1].split()[0])
+    ns = float(r.stdout.split("ns per call ")[1])
+    print("\ntl_plan cache hit: %.0f ns per call" % ns)
+    assert hits == 500000
+    assert ns < 1000.0
+
+
+def test_plan_cache_keys_on_pointer_offsets_bounds_and_overlap():
+    """Cached plans are reused only where they hold: another offset within 16 bytes
+    re-plans (vector width), caller-given bounds are checked on every call, and
+    buffers whose byte ranges meet are planned afresh (in place or rejected)."""
+    shape, ss, ds = (37, 300, 16), (300 * 16, 16, 1), (16, 37 * 16, 1)   # chunk path
+    base = 1 << 32
+    h0 = tl.tl_plan_cache_hits()
+    p0 = tl.tl_plan(base, base + (1 << 30), shape, ss, ds, 2)
+    p1 = tl.tl_plan(base + (1 << 20), base + (1 << 30) + (1 << 20), shape, ss, ds, 2)
+    assert tl.tl_plan_cache_hits() == h0 + 1 and p1 == p0 and p0["vec_bytes"] == 16
+    p2 = tl.tl_plan(base + 2, base + (1 << 30), shape, ss, ds, 2)      # src off by 2 bytes
+    assert p2["path"] == "chunk" and p2["vec_bytes"] == 2
+    p3 = tl.tl_plan(base + 8, base + (1 << 30) + 8, shape, ss, ds, 2)
+    assert p3["vec_bytes"] == 8
+    # bounds: the cached plan, then a src buffer one byte too small
+    need = ((37 - 1) * 300 * 16 + 299 * 16 + 15 + 1) * 2
+    tl.tl_plan(base, base + (1 << 30), shape, ss, ds, 2, src_bytes=need)
+    with pytest.raises(tl.TLError) as e:
+        tl.tl_plan(base, base + (1 << 30), shape, ss, ds, 2, src_bytes=need - 1)
+    assert e.value.name == "TL_ERR_BOUNDS"
+    # overlap after a cached disjoint plan: the SF warp tile in place, then aliased
+    sf = ((2, 1, 4, 32), (128, 128, 32, 1), (128, 128, 1, 4))
+    assert tl.tl_plan(base, base + (1 << 20), *sf, 4)["in_place"] is False
+    assert tl.tl_plan(base, base + (1 << 20), *sf, 4)["in_place"] is False
+    assert tl.tl_plan(base, base, *sf, 4)["in_place"] is True
+    with pytest.raises(tl.TLError) as e:
+        tl.tl_plan(base, base + 64, *sf, 4)
+    assert e.value.name == "TL_ERR_ALIAS"
+    # and a null pointer is still an error on a layout planned before
+    with pytest.raises(tl.TLError):
+        tl.tl_plan(0, base + (1 << 30), shape, ss, ds, 2)

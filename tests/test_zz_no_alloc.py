@@ -1,12 +1,14 @@
 """tl_permute_tile_noalloc: the tile transpose for callers that cannot allocate.
 
-Such callers (code inside a CUDA graph capture, plug-ins whose host framework's
-allocator owns the device memory, fixed-memory deployments) cannot hand the
-library a status word, so this entry point keeps it in the library's own static
-device scratch.  The test calls it through the C ABI twice in a row, with
+Such callers (plug-ins whose host framework's allocator owns the device memory,
+latency-critical code that cannot take cudaMalloc's implicit synchronisation,
+fixed-memory deployments) cannot hand the library a status word, so this entry
+point keeps it in the library's own static device scratch.  The test calls it
+through the C ABI twice in a row, with
 different inputs, and requires each result to equal, byte for byte, what the
 ordinary tl_permute entry point produces for the same input; it also requires
-the status it reports to be 0.  This file sorts last so that a run stopping at
+the status it reports to be 0, and the device's free memory to stay the same
+across calls.  This file sorts last so that a run stopping at
 its first failure has already run every other test.
 """
 import ctypes
@@ -52,6 +54,29 @@ def test_noalloc_matches_tl_permute_on_two_calls_in_a_row(shape, ss, ds, eb):
         torch.cuda.synchronize()
         assert status.value == 0, "call %d reported status %d" % (call, status.value)
         assert torch.equal(out, ref), "call %d differs from tl_permute" % call
+
+
+def test_noalloc_call_allocates_no_device_memory():
+    """Once the first call on the device has looked up the scratch address, a call
+    leaves the device's free memory and torch's allocator untouched."""
+    shape, ss, ds, eb = CASES[0]
+    n = int(np.prod(shape)) * eb
+    stream = torch.cuda.current_stream().cuda_stream
+    src = torch.from_numpy(workloads.random_bits(n, 13)).cuda()
+    out = torch.empty(n, dtype=torch.uint8, device="cuda")
+    status = ctypes.c_int32(-1)
+    tl.tl_permute_tile_noalloc(src.data_ptr(), out.data_ptr(), shape, ss, ds, eb, stream,
+                               host_status=status)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for _ in range(3):
+        tl.tl_permute_tile_noalloc(src.data_ptr(), out.data_ptr(), shape, ss, ds, eb, stream,
+                                   host_status=status)
+    torch.cuda.synchronize()
+    assert status.value == 0
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
 
 
 def test_noalloc_rejects_layouts_without_the_tile_path():

@@ -50,15 +50,17 @@ KERNEL_SOURCES = {
     "chunk": ["k_chunk.cu", "tl_device.cuh"],
     "panel": ["k_panel.cu", "tl_device.cuh"],
     "cols": ["k_cols.cu", "tl_device.cuh"],
+    "block": ["k_block.cu", "tl_device.cuh"],
     "warp": ["k_warp.cu", "tl_device.cuh"],
     "generic": ["k_generic.cu", "tl_device.cuh"],
 }
 KERNEL_NAMES = {"tile": "k_tile", "cluster": "k_cluster", "rows": "k_rows", "chunk": "k_chunk",
-                "panel": "k_panel", "cols": "k_cols",
+                "panel": "k_panel", "cols": "k_cols", "block": "k_block",
                 "warp": "k_warp", "generic": "k_generic"}
 DTYPES = {"sf_transpose": "f32", "tile_transpose": "f16", "mx_sf": "u8", "attention": "bf16",
           "t2d_u8": "u8", "t2d_f16": "f16", "t2d_f32": "f32", "t2d_f64": "f64",
-          "t2d_v16": "16-byte", "t2d_odd_f32": "f32", "hwc_chw_u8": "u8", "nd6_f32": "f32"}
+          "t2d_v16": "16-byte", "t2d_odd_f32": "f32", "hwc_chw_u8": "u8", "nd6_f32": "f32",
+          "nd8_f32": "f32"}
 
 
 # ---------------------------------------------------------------------------
@@ -694,7 +696,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--path", default="auto",
                     choices=["auto", "generic", "chunk", "tile", "warp", "rows", "cluster",
-                             "panel", "cols"],
+                             "panel", "cols", "block"],
                     help="force a kernel path (default: the planner's choice)")
     ap.add_argument("--leading", type=int, default=0,
                     help="override the outermost extent (smaller cases for profiling)")

@@ -175,6 +175,9 @@ TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape
 #define TL_PATH_COLS 8u     /* short src runs (interleaved channels -> planes, pixels of
                                2..16 elements, <= 24 bytes): 16-byte pixel loads, register
                                transpose, one 16-byte store per plane */
+#define TL_PATH_BLOCK 9u    /* a tile of up to four axes that is a few long contiguous runs
+                               on both sides (high-rank permutes of short axes): src runs
+                               staged in smem by cp.async, stores along the dst runs */
 #define TL_PATH_MASK 0xFu
 /* Test hook for the cluster path (the producer CTA skips its DSMEM hand-off) and for
  * panel tiles loaded by TMA phase maps (the loading thread skips one phase load of its
@@ -252,11 +255,13 @@ typedef struct tl_plan_info {
     int32_t k, shift, mask;        /* warp path swizzle (else 0) */
     int32_t tile_rows, tile_cols;  /* tile/panel path: rows (b) x columns (a) per tile,
                                       in elements; cols path: pixels per 16-byte piece x
-                                      elements per pixel */
+                                      elements per pixel; block path: the dst run x the
+                                      src run of a tile, in elements */
     int64_t tiles;                 /* work units (tiles, rows, warps...) */
     int32_t grid, block;           /* launch shape (0 without a device) */
     int32_t smem_bytes;            /* dynamic shared memory per CTA */
-    int32_t pitch;                 /* panel path: shared-memory bytes per tile row */
+    int32_t pitch;                 /* panel path: shared-memory bytes per tile row;
+                                      block path: per src run */
     int32_t panel_mode;            /* panel path: 0 rows of 16-byte blocks, 1 one run,
                                       2 rows loaded by TMA phase maps into a phase-major
                                       stage (a row pitch off the 16-byte grid), 3 the

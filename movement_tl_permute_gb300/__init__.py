@@ -30,7 +30,7 @@ __all__ = [
 
 TL_MAX_DIMS = 8
 PATHS = {"auto": 0, "generic": 1, "chunk": 2, "tile": 3, "warp": 4, "rows": 5, "cluster": 6,
-         "panel": 7, "cols": 8}
+         "panel": 7, "cols": 8, "block": 9}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 TL_FLAG_TEST_DROP_HANDOFF = 1 << 8
 TL_FLAG_NO_PDL = 1 << 9

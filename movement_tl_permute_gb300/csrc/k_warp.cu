@@ -16,7 +16,7 @@ namespace tl {
 namespace {
 
 template <int EB, int P>
-__global__ void __launch_bounds__(128) k_warp(const WarpArgs a) {
+__global__ void __launch_bounds__(128, 4) k_warp(const WarpArgs a) {
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
     using T = typename dev::Bits<EB>::T;

@@ -874,6 +874,214 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
     p->vec_bytes = p->panel_vec || p->panel_run ? 16 : p->panel_words ? 4 : eb;
 }
 
+// ---------------------------------------------------------------- block path
+// A tile of up to four axes that is a few long contiguous runs on both sides: the
+// dense chain of axes from src stride 1 (S) and from dst stride 1 (D); T is a prefix
+// of S joined with a prefix of D.  Every (S prefix, D prefix) pair with at most four
+// axes is tried, with at most one axis split into chunks so the tile fits its bytes
+// (the last axis of each run it belongs to, so both runs stay dense); the tile whose
+// shorter run (capped at 512 bytes) is longest wins, then the bigger tile.  The
+// shared-memory pitch of the src runs is chosen by replaying the store walk's warp
+// reads on the bank model (hardware mode).
+namespace {
+
+// mixed-radix digits of x over `n` extents (innermost first)
+void digits(int64_t x, int n, const int64_t* ext, int64_t* d) {
+    for (int k = 0; k < n; ++k) {
+        d[k] = x % ext[k];
+        x /= ext[k];
+    }
+}
+
+// Stage offset in bytes of the element at dst-run position i of dst run j (mis 0):
+// the store walk's read, as the block kernel's tables compute it.
+int64_t block_stage_off(const BlockPlan& b, int eb, int pitch, int64_t i, int64_t j) {
+    int64_t coord[kBlockAxes] = {};
+    int64_t e[kBlockAxes], d[kBlockAxes];
+    for (int k = 0; k < b.nd; ++k) e[k] = b.tile[b.dax[k]];
+    digits(i, b.nd, e, d);
+    for (int k = 0; k < b.nd; ++k) coord[b.dax[k]] = d[k];
+    for (int k = 0; k < b.nj; ++k) e[k] = b.tile[b.jax[k]];
+    digits(j, b.nj, e, d);
+    for (int k = 0; k < b.nj; ++k) coord[b.jax[k]] = d[k];
+    int64_t sp = 0, r = 0, rw = 1;
+    for (int k = 0; k < b.ns; ++k) sp += coord[b.sax[k]] * b.ss[b.sax[k]];
+    for (int k = 0; k < b.nr; ++k) {
+        r += coord[b.rax[k]] * rw;
+        rw *= b.tile[b.rax[k]];
+    }
+    return r * pitch + sp * eb;
+}
+
+int block_pitch(const BlockPlan& b, int eb) {
+    const int base = (int)((b.Ls * eb + 15 + 15) / 16 * 16);
+    const int64_t n = b.Ld * b.Rd;
+    int best = base;
+    int64_t best_cost = -1;
+    for (int extra = 0; extra < 8; ++extra) {
+        const int P = base + 16 * extra;
+        if (b.Rs * P > 48 * 1024) break;
+        int64_t cost = 0;
+        for (int64_t w = 0; w < 64 && 32 * w < n; ++w) {
+            int64_t o[32];
+            for (int l = 0; l < 32; ++l) {
+                const int64_t f = 32 * w + l;
+                o[l] = f < n ? block_stage_off(b, eb, P, f % b.Ld, f / b.Ld) / eb : -1;
+            }
+            cost += bank_degree(32, o, eb, true);
+        }
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = P;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+int64_t plan_block(Plan* p, int64_t tile_bytes) {
+    const Axes& s = p->sorted;
+    const int n = s.n, eb = p->eb;
+    // measured on GB300 (12^8 permutes, 9^8 permutes): 12 KiB tiles for 1- and 2-byte
+    // elements (u16 1.92 -> 2.08, u8 0.66 -> 1.24 TB/s against 32 KiB), 32 KiB for
+    // wider ones (fp32 2.59 at 12 KiB -> 2.89 TB/s)
+    if (tile_bytes <= 0) tile_bytes = eb <= 2 ? 12288 : 32768;
+    if (n < 2) return 0;
+    // the dense chains from src stride 1 and from dst stride 1
+    auto chain = [&](const int64_t* str, int* out) {
+        int m = 0;
+        int64_t prod = 1;
+        bool used[kMaxDims] = {};
+        for (;;) {
+            int next = -1;
+            for (int i = 0; i < n; ++i)
+                if (!used[i] && str[i] == prod) { next = i; break; }
+            if (next < 0 || m == kMaxDims) break;
+            used[next] = true;
+            out[m++] = next;
+            prod *= s.ext[next];
+        }
+        return m;
+    };
+    int S[kMaxDims], D[kMaxDims];
+    const int nS = chain(s.ss, S), nD = chain(s.ds, D);
+    if (nS == 0 || nD == 0 || S[0] == D[0]) return 0;
+    BlockPlan best;
+    int64_t best_score = -1, best_run = 0;
+    for (int i = 1; i <= nS; ++i) {
+        for (int j = 1; j <= nD; ++j) {
+            int T[kMaxDims], nt = 0;
+            auto add = [&](int ax) {
+                for (int q = 0; q < nt; ++q)
+                    if (T[q] == ax) return;
+                T[nt++] = ax;
+            };
+            for (int q = 0; q < i; ++q) add(S[q]);
+            for (int q = 0; q < j; ++q) add(D[q]);
+            if (nt > kBlockAxes) continue;
+            auto in_t = [&](int ax) {
+                for (int q = 0; q < nt; ++q)
+                    if (T[q] == ax) return q;
+                return -1;
+            };
+            // the runs: the longest prefixes of S and D inside T
+            int sr = 0, dr0 = 0;
+            while (sr < nS && in_t(S[sr]) >= 0) ++sr;
+            while (dr0 < nD && in_t(D[dr0]) >= 0) ++dr0;
+            int64_t full = 1;
+            for (int q = 0; q < nt; ++q) full *= s.ext[T[q]];
+            // candidates for the chunked axis: none, or an axis that is the last of
+            // each run it belongs to; a dst run longer than the kernel's position
+            // table is cut to a shorter prefix of D (the cut-off axes index dst runs
+            // that lie back to back)
+            for (int c = -1; c < nt; ++c) {
+                int64_t tile[kBlockAxes];
+                for (int q = 0; q < nt; ++q) tile[q] = s.ext[T[q]];
+                int dr = dr0;
+                auto ld_of = [&](int m) {
+                    int64_t v = 1;
+                    for (int q = 0; q < m; ++q) v *= tile[in_t(D[q])];
+                    return v;
+                };
+                if (c < 0) {
+                    if (full * eb > tile_bytes) continue;
+                    while (dr > 1 && ld_of(dr) > kBlockMaxLd) --dr;
+                } else {
+                    const int ax = T[c];
+                    if (full * eb <= tile_bytes) continue;
+                    const int64_t rest = full / s.ext[ax];
+                    int64_t k = tile_bytes / (rest * eb);
+                    if (k < 1) continue;
+                    const int64_t nc = (s.ext[ax] + k - 1) / k;
+                    tile[c] = (s.ext[ax] + nc - 1) / nc;           // chunks evened out
+                    while (dr > 1 && ld_of(dr) > kBlockMaxLd) --dr;
+                    bool ok = true;
+                    for (int q = 0; q < sr - 1; ++q) ok = ok && S[q] != ax;
+                    for (int q = 0; q < dr - 1; ++q) ok = ok && D[q] != ax;
+                    if (!ok) continue;
+                }
+                BlockPlan b;
+                b.nt = nt;
+                b.chunk = c;
+                for (int q = 0; q < nt; ++q) {
+                    b.idx[q] = T[q];
+                    b.ext[q] = s.ext[T[q]];
+                    b.ss[q] = s.ss[T[q]];
+                    b.ds[q] = s.ds[T[q]];
+                    b.tile[q] = tile[q];
+                }
+                b.Ls = b.Ld = 1;
+                for (int q = 0; q < sr; ++q) {
+                    b.sax[b.ns++] = in_t(S[q]);
+                    b.Ls *= tile[in_t(S[q])];
+                }
+                for (int q = 0; q < dr; ++q) {
+                    b.dax[b.nd++] = in_t(D[q]);
+                    b.Ld *= tile[in_t(D[q])];
+                }
+                int64_t tot = 1;
+                for (int q = 0; q < nt; ++q) {
+                    tot *= tile[q];
+                    bool in_s = false, in_d = false;
+                    for (int u = 0; u < b.ns; ++u) in_s = in_s || b.sax[u] == q;
+                    for (int u = 0; u < b.nd; ++u) in_d = in_d || b.dax[u] == q;
+                    if (!in_s) b.rax[b.nr++] = q;
+                    if (!in_d) b.jax[b.nj++] = q;
+                }
+                b.Rs = tot / b.Ls;
+                b.Rd = tot / b.Ld;
+                if (b.Ld > kBlockMaxLd || b.Rd > kBlockMaxRuns || b.Rs > kBlockMaxRuns) continue;
+                if (b.Ls >= (1 << 24) || b.Rs * ((b.Ls * eb + 30) / 16 * 16) > 48 * 1024) continue;
+                const int64_t run = std::min(b.Ls, b.Ld) * eb;
+                const int64_t score = std::min<int64_t>(run, 512) * (int64_t(1) << 32) + tot;
+                if (score > best_score) {
+                    best_score = score;
+                    best_run = run;
+                    best = b;
+                }
+            }
+        }
+    }
+    if (best_score < 0) return 0;
+    // the axes outside T: the batch (dst order, outermost first)
+    Axes bt;
+    for (int q = 0; q < n; ++q) {
+        bool in = false;
+        for (int u = 0; u < best.nt; ++u) in = in || best.idx[u] == q;
+        if (in) continue;
+        bt.ext[bt.n] = s.ext[q]; bt.ss[bt.n] = s.ss[q]; bt.ds[bt.n] = s.ds[q]; ++bt.n;
+    }
+    best.batch = bt;
+    best.pitch = block_pitch(best, eb);
+    int64_t tiles = 1;
+    for (int q = 0; q < best.nt; ++q) tiles *= (best.ext[q] + best.tile[q] - 1) / best.tile[q];
+    for (int q = 0; q < bt.n; ++q) tiles *= bt.ext[q];
+    p->blk = best;
+    p->tiles = tiles;
+    return best_run;
+}
+
 int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
               const int64_t* src_strides, const int64_t* dst_strides, int eb, uint32_t flags,
               int64_t src_bytes, int64_t dst_bytes, Plan* plan) {
@@ -882,7 +1090,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     if (ndim < 0 || ndim > kMaxDims) return TL_ERR_ARG;
     if (ndim > 0 && (!shape || !src_strides || !dst_strides)) return TL_ERR_ARG;
     uint32_t forced = flags & TL_PATH_MASK;
-    if (forced > TL_PATH_COLS) return TL_ERR_ARG;
+    if (forced > TL_PATH_BLOCK) return TL_ERR_ARG;
     const bool checked = (flags & TL_FLAG_DEBUG_CHECKS) != 0;
     if ((flags & TL_FLAG_TEST_SKIP_HOST_BOUNDS) && !checked) return TL_ERR_ARG;
     if (checked) {                 // the checked run is the generic kernel
@@ -984,8 +1192,55 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     case TL_PATH_CLUSTER: path = tile ? TL_PATH_CLUSTER : 0; break;
     case TL_PATH_PANEL: path = panel ? TL_PATH_PANEL : 0; break;
     case TL_PATH_COLS: path = cols ? TL_PATH_COLS : 0; break;
+    case TL_PATH_BLOCK: {
+        Plan q = p;
+        path = plan_block(&q) > 0 ? TL_PATH_BLOCK : 0;
+        break;
+    }
     }
     if (path == 0) return TL_ERR_PATH;
+    p.src_mis16 = s0 & 15;
+    p.dst_mis16 = d0 & 15;
+    // The panel tile of the plane: merged short axes, tile shape, stage layout.
+    auto setup_panel = [&](Plan& q) {
+        q.panel_elem_stores = (flags & TL_FLAG_PANEL_ELEMENT_STORES) != 0;
+        panel_merge_b(&q);
+        panel_merge_a(&q);
+        plan_panel(&q, 0);
+    };
+    // The block tile takes layouts of canonical rank 3 or more whose panel tile would
+    // move short runs on one side (high-rank permutes of short axes) when its own
+    // shorter run is 128 bytes or more and at least twice as long (or as long, where
+    // the panel tile would be stored element by element).
+    if (forced == TL_PATH_AUTO && !ranges_meet && srt.n >= 3 &&
+        (path == TL_PATH_PANEL || path == TL_PATH_GENERIC)) {
+        Plan q = p;
+        const int64_t brun = plan_block(&q);
+        if (brun >= 128) {
+            int64_t prun = 0;
+            bool r_vec = false, r_run = false;
+            if (path == TL_PATH_PANEL) {
+                Plan r = p;
+                setup_panel(r);
+                const int64_t ta = r.tile_cols, tb = r.tile_rows;
+                // src rows back to back (one run per tile) or one run per tile row
+                const bool packed = ta == r.ext_a && r.ss_b == ta &&
+                                    (r.panel_b1 == 0 || r.panel_ss_b2 == r.panel_b1 * ta);
+                const int64_t srun = packed ? ta * tb * eb : ta * eb;
+                const int64_t drun = r.panel_run ? ta * tb * eb : tb * eb;
+                prun = std::min(srun, drun);
+                r_vec = r.panel_vec;
+                r_run = r.panel_run;
+            }
+            // (a panel tile stored as 16-byte dst runs keeps the panel unless the block
+            // runs are twice as long; element-stored panel tiles yield at equal runs:
+            // measured on GB300, 9^8 fp32 permutes whose panel tiles are 81 x 81 with
+            // element stores run 1.2-1.4x faster as blocks, reversed 8^8 / 10^8 fp32
+            // and a 6-D fp32 permute with 16-byte runs 0.6-0.8x)
+            const bool vec = path == TL_PATH_PANEL && (r_vec || r_run);
+            if (brun >= 2 * prun || (!vec && brun >= prun)) path = TL_PATH_BLOCK;
+        }
+    }
     p.path = path;
 
     if (path == TL_PATH_CHUNK) {
@@ -1021,12 +1276,10 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         const int64_t tb = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
         p.tiles = ta * tb * p.batch_total;
     } else if (path == TL_PATH_PANEL) {
-        p.src_mis16 = s0 & 15;
-        p.dst_mis16 = d0 & 15;
-        p.panel_elem_stores = (flags & TL_FLAG_PANEL_ELEMENT_STORES) != 0;
-        panel_merge_b(&p);
-        panel_merge_a(&p);
-        plan_panel(&p, 0);
+        setup_panel(p);
+    } else if (path == TL_PATH_BLOCK) {
+        plan_block(&p);
+        p.vec_bytes = eb;
     } else if (path == TL_PATH_COLS) {
         p.vec_bytes = 16;
         p.tile_cols = (int)p.ext_a;          // elements per pixel

@@ -23,6 +23,30 @@ struct Axes {
     int64_t ds[kMaxDims] = {};
 };
 
+// BLOCK path: a tile of up to kBlockAxes axes (T) that is a few long contiguous runs
+// on both sides.  The src run is the longest chain of T's axes, from the one of src
+// stride 1, each of src stride the product of the extents before it; the axes of T
+// outside it index the src runs.  The dst run and its index axes likewise, from the
+// axis of dst stride 1.  At most one axis of T is split into chunks (the last axis
+// of each run it belongs to), so both runs stay dense.
+constexpr int kBlockAxes = 4;
+constexpr int kBlockMaxLd = 2048;     // dst run positions (per-CTA table entries)
+constexpr int kBlockMaxRuns = 512;    // src runs and dst runs of a tile
+struct BlockPlan {
+    int nt = 0;                        // axes of T
+    int idx[kBlockAxes] = {};          // their positions in the sorted canonical axes
+    int64_t ext[kBlockAxes] = {}, ss[kBlockAxes] = {}, ds[kBlockAxes] = {};
+    int64_t tile[kBlockAxes] = {};     // extent of the tile along each axis of T
+    int chunk = -1;                    // the axis of T split into chunks (-1: none)
+    int ns = 0, sax[kBlockAxes] = {};  // src-run axes (innermost first)
+    int nd = 0, dax[kBlockAxes] = {};  // dst-run axes (innermost first)
+    int nr = 0, rax[kBlockAxes] = {};  // src-run index axes
+    int nj = 0, jax[kBlockAxes] = {};  // dst-run index axes
+    int64_t Ls = 0, Rs = 0, Ld = 0, Rd = 0;   // run lengths and counts of a full tile
+    int pitch = 0;                     // shared-memory bytes per src run
+    Axes batch;                        // the axes outside T (dst order, outermost first)
+};
+
 struct Plan {
     int path = 0;          // TL_PATH_*; 0 with total == 0 means "nothing to do"
     int eb = 0;            // element bytes
@@ -63,6 +87,7 @@ struct Plan {
     int panel_phi_lg = 0;               // PANEL (TMA): log2 of the phase count phi
     int panel_phase_bytes = 0;          // PANEL (TMA): shared-memory bytes of one phase block
     int64_t tiles = 0;
+    BlockPlan blk;                      // BLOCK
 
     // WARP: tile (innermost suffix of `kept`) + batch of the outer `kept` axes.
     Axes wtile;
@@ -87,6 +112,10 @@ constexpr int kPanelMaxSmem = 160 * 1024;
 // 16 or less (interleaved channels: 5.5-6.1 TB/s against 4.8-5.5 with 16 KiB).
 // rows > 0 asks for that many rows of b per tile when both extents exceed 16.
 void plan_panel(Plan* p, int tile_bytes, int rows = 0);
+
+// BLOCK path: the tile of up to four axes whose shorter run (src or dst) is longest;
+// fills p->blk and p->tiles.  Returns the shorter run in bytes, 0 if none applies.
+int64_t plan_block(Plan* p, int64_t tile_bytes = 0);
 
 // The bank simulator: worst conflict degree of one warp-wide access.
 int bank_degree(int n_lanes, const int64_t* lane_offsets, int elem_bytes, bool hardware);

@@ -228,6 +228,49 @@ const void* panel_kernel(int eb, bool vec, bool am);
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,
                          bool pdl);
 
+// ---------------------------------------------------------------- block
+// A tile of up to four axes (T) that is a few long contiguous runs on both sides.
+// Per-CTA tables (built once in shared memory) map a dst-run position i and a dst
+// run j to the src run and the position inside it: the element of (j, i) sits in the
+// stage at runbase[r_i + r_j] + (p_i + p_j) * EB, and in dst at dof + dst_j + i.
+constexpr int kBlockThreads = 256;
+constexpr int kBlockStages = 3;
+constexpr int kBlockMaxSmem = 200 * 1024;   // stages of at most 48 KiB + the tables
+struct BlockArgs {
+    const uint8_t* src;
+    uint8_t* dst;
+    // tables: the axes whose digits make i (dst-run axes), j (dst-run index axes)
+    // and r (src-run index axes), innermost first, with the tile's extents; for
+    // each, its src-run position stride (elements, 0 off the src run), its src-run
+    // index stride (0 on the src run), whether it is the chunked axis, and (j, r)
+    // its dst and src strides
+    int32_t nd, nj, nr;
+    int32_t dext[4], jext[4], rext[4];
+    int64_t dsp[4], jsp[4];
+    int32_t drs[4], jrs[4];
+    int32_t dck, jck, rck;       // index of the chunked axis in each list (-1: none)
+    int64_t jds[4], rss[4];
+    int32_t Ld, Rd, Rs, Ls;      // run lengths and counts of a full tile
+    int32_t ls_inner;            // src run length without the chunked axis (when it is
+                                 // the src run's last axis; else Ls)
+    int32_t pitch, nblk, stage_bytes;
+    int32_t table_off;           // byte offset of the tables in dynamic shared memory
+    // the chunked axis: extent, tile extent, chunks, strides
+    int64_t c_ext, c_ss, c_ds, nc;
+    int32_t c_k, use32;
+    // tiles: chunk index fastest, then the batch axes (innermost first)
+    int32_t nb;
+    int32_t umis;                // every src run at the same offset inside its 16-byte
+                                 // block (run and tile strides multiples of 16 bytes)
+    int64_t tiles;
+    int64_t bext[TL_MAX_DIMS], bss[TL_MAX_DIMS], bds[TL_MAX_DIMS];
+    dev::DivU32 d_nc, d_Ld, d_nblk;
+    dev::DivU32 d_bext[TL_MAX_DIMS];
+};
+int block_smem_bytes(const BlockArgs& a);
+const void* block_kernel(int eb);
+cudaError_t launch_block(int eb, const BlockArgs& a, int grid, cudaStream_t st, bool pdl);
+
 // ---------------------------------------------------------------- warp
 struct WarpArgs {
     const uint8_t* src;

@@ -146,6 +146,10 @@ int get_device_info(DevInfo* out) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kPanelMaxSmem) != cudaSuccess)
                     return TL_ERR_CUDA;
+            if (cudaFuncSetAttribute(block_kernel(1 << i),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kBlockMaxSmem) != cudaSuccess)
+                return TL_ERR_CUDA;
             if (panel_tma_kernel(1 << i) &&
                 cudaFuncSetAttribute(panel_tma_kernel(1 << i),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -295,6 +299,94 @@ struct Launch {
     int grid = 0, block = 0, smem = 0;
 };
 
+// The block kernel's arguments from the plan (pointers left null): the tables' axes,
+// the chunked axis, the batch axes innermost first, and the shared-memory layout.
+BlockArgs block_args(const Plan& p) {
+    const BlockPlan& b = p.blk;
+    const int eb = p.eb;
+    BlockArgs a{};
+    int64_t rw[kBlockAxes] = {};           // src-run index weight of each axis of T
+    {
+        int64_t w = 1;
+        for (int k = 0; k < b.nr; ++k) {
+            rw[b.rax[k]] = w;
+            w *= b.tile[b.rax[k]];
+        }
+    }
+    auto in_srun = [&](int q) {
+        for (int k = 0; k < b.ns; ++k)
+            if (b.sax[k] == q) return true;
+        return false;
+    };
+    a.nd = b.nd;
+    a.nj = b.nj;
+    a.nr = b.nr;
+    a.dck = a.jck = a.rck = -1;
+    for (int k = 0; k < b.nd; ++k) {
+        const int q = b.dax[k];
+        a.dext[k] = (int32_t)b.tile[q];
+        a.dsp[k] = in_srun(q) ? b.ss[q] : 0;
+        a.drs[k] = (int32_t)rw[q];
+        if (q == b.chunk) a.dck = k;
+    }
+    for (int k = 0; k < b.nj; ++k) {
+        const int q = b.jax[k];
+        a.jext[k] = (int32_t)b.tile[q];
+        a.jsp[k] = in_srun(q) ? b.ss[q] : 0;
+        a.jrs[k] = (int32_t)rw[q];
+        a.jds[k] = b.ds[q];
+        if (q == b.chunk) a.jck = k;
+    }
+    for (int k = 0; k < b.nr; ++k) {
+        const int q = b.rax[k];
+        a.rext[k] = (int32_t)b.tile[q];
+        a.rss[k] = b.ss[q];
+        if (q == b.chunk) a.rck = k;
+    }
+    a.Ld = (int32_t)b.Ld;
+    a.Rd = (int32_t)b.Rd;
+    a.Rs = (int32_t)b.Rs;
+    a.Ls = (int32_t)b.Ls;
+    a.ls_inner = a.Ls;
+    if (b.chunk >= 0 && in_srun(b.chunk)) a.ls_inner = (int32_t)(b.Ls / b.tile[b.chunk]);
+    a.pitch = b.pitch;
+    a.nblk = (int32_t)((b.Ls * eb + 30) / 16);
+    a.stage_bytes = (int32_t)(b.Rs * b.pitch);
+    a.table_off = kBlockStages * a.stage_bytes;
+    if (b.chunk >= 0) {
+        const int q = b.chunk;
+        a.c_ext = b.ext[q];
+        a.c_k = (int32_t)b.tile[q];
+        a.c_ss = b.ss[q];
+        a.c_ds = b.ds[q];
+        a.nc = (b.ext[q] + b.tile[q] - 1) / b.tile[q];
+    } else {
+        a.c_ext = 1;
+        a.c_k = 1;
+        a.nc = 1;
+    }
+    a.nb = b.batch.n;
+    for (int i = 0; i < a.nb; ++i) {           // innermost (smallest dst stride) first
+        const int j = a.nb - 1 - i;
+        a.bext[i] = b.batch.ext[j];
+        a.bss[i] = b.batch.ss[j];
+        a.bds[i] = b.batch.ds[j];
+    }
+    a.tiles = p.tiles;
+    a.use32 = p.tiles < (1LL << 32) ? 1 : 0;
+    // every src run of a tile at the same offset inside its 16-byte block: the
+    // strides between runs are multiples of 16 bytes
+    bool um = true;
+    for (int k = 0; k < a.nr; ++k) um = um && (a.rss[k] * eb) % 16 == 0;
+    a.umis = um ? 1 : 0;
+    a.d_nc = dev::make_divu32((uint32_t)a.nc);
+    a.d_Ld = dev::make_divu32((uint32_t)a.Ld);
+    a.d_nblk = dev::make_divu32((uint32_t)a.nblk);
+    if (a.use32)
+        for (int i = 0; i < a.nb; ++i) a.d_bext[i] = dev::make_divu32((uint32_t)a.bext[i]);
+    return a;
+}
+
 // Launch shape of each path (grid 0 when the device is unknown).
 Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const TileTuning& tt) {
     Launch l;
@@ -357,6 +449,17 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
             l.grid = cap_grid(p.tiles, sms * per_sm, max_ctas);
         }
         break;
+    case TL_PATH_BLOCK: {
+        l.block = kBlockThreads;
+        l.smem = block_smem_bytes(block_args(p));
+        if (sms) {
+            // resident CTAs by shared memory (228 KiB per SM, 1 KiB reserved per CTA)
+            int per_sm = 233472 / (l.smem + 1024);
+            per_sm = per_sm < 1 ? 1 : per_sm > 8 ? 8 : per_sm;
+            l.grid = cap_grid(p.tiles, sms * per_sm, max_ctas);
+        }
+        break;
+    }
     case TL_PATH_ROWS:
         l.block = p.ext_b >= 16 ? 128 : 256;   // must match rows_threads<R>() in k_rows.cu
         if (sms) l.grid = cap_grid((p.tiles + 511) / 512, sms * 8, max_ctas);
@@ -375,6 +478,11 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
 
 // The panel tile size and height are tuning options: re-plan the panel layout for them.
 void apply_panel_tile(Plan& p, const tl_permute_opts* o) {
+    if (p.path == TL_PATH_BLOCK && o && o->panel_tile_kib >= 4 && o->panel_tile_kib <= 48) {
+        Plan q = p;                      // the block tile of the asked size, if one fits
+        if (plan_block(&q, o->panel_tile_kib * 1024) > 0) p = q;
+        return;
+    }
     if (p.path != TL_PATH_PANEL || !o) return;
     const bool kib = o->panel_tile_kib >= 4 && o->panel_tile_kib <= 48;
     const bool rows = o->tile_rows >= 16 && o->tile_rows <= 1024;
@@ -786,6 +894,13 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         err = launch_panel(eb, a, l.grid, l.smem, st, pdl);
         break;
     }
+    case TL_PATH_BLOCK: {
+        BlockArgs a = block_args(p);
+        a.src = s8;
+        a.dst = d8;
+        err = launch_block(eb, a, l.grid, st, pdl);
+        break;
+    }
     case TL_PATH_COLS: {
         ColsArgs a{};
         a.src = s8;
@@ -899,6 +1014,11 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     info.tile_rows = p.tile_rows;
     info.tile_cols = p.tile_cols;
     info.pitch = p.pitch;
+    if (p.path == TL_PATH_BLOCK) {            // block tile: run lengths and the run pitch
+        info.tile_rows = (int32_t)p.blk.Ld;
+        info.tile_cols = (int32_t)p.blk.Ls;
+        info.pitch = p.blk.pitch;
+    }
     info.panel_mode = p.panel_tma ? 2 : p.panel_phase ? 3 : p.panel_mode;
     info.panel_b1 = (int32_t)p.panel_b1;
     info.panel_vec = p.panel_vec ? 1 : p.panel_run ? 2 : p.panel_words ? 3 : 0;

@@ -35,6 +35,9 @@ Three more describe general permutes whose layouts a TMA tensor map cannot take
 ``hwc_chw_u8``     uint8 image 8192 x 8192 x 3 channels (HWC) -> 3 planes (CHW).
 ``nd6_f32``        float32 (16,16,16,16,64,64) permuted (5,3,1,4,2,0): four
                    batch axes around the transposed plane (1 GiB).
+``nd8_f32``        float32 (9,)*8 permuted (1,4,2,3,7,5,6,0): a high-rank permute
+                   of short axes whose src- and dst-contiguous axes are 36 bytes
+                   long (172 MB).
 =================  =========================================================
 """
 from __future__ import annotations
@@ -111,6 +114,14 @@ def _nd6(lead):
                     57, "bits", "float32 %s permuted (5,3,1,4,2,0)" % (shape,), ("general",))
 
 
+def _nd8(lead):
+    shape = (lead,) + (9,) * 7
+    n = lead * 9 ** 7
+    return Workload("nd8_f32", 4, shape, _rm(shape), _perm_dst(shape, (1, 4, 2, 3, 7, 5, 6, 0)),
+                    n, n, 58, "bits", "float32 %s permuted (1,4,2,3,7,5,6,0)" % (shape,),
+                    ("general",))
+
+
 WORKLOADS = {
     w.name: w for w in [
         Workload("sf_transpose", 4, (2, 1, 4, 32), (128, 128, 32, 1), (128, 128, 1, 4),
@@ -133,6 +144,7 @@ WORKLOADS = {
         _t2d("t2d_odd_f32", 4, 16383, 16385, 55),
         _hwc_chw(8192),
         _nd6(16),
+        _nd8(9),
     ]
 }
 
@@ -155,6 +167,8 @@ def scaled(w: Workload, leading: int) -> Workload:
         return _hwc_chw(leading, w.shape[1], w.shape[2])
     if w.name == "nd6_f32":             # the leading axis is innermost in dst
         return _nd6(leading)
+    if w.name == "nd8_f32":             # the leading axis is innermost in dst
+        return _nd8(leading)
     ratio_src = w.src_elems // w.shape[0]
     ratio_dst = w.dst_elems // w.shape[0]
     return Workload(w.name, w.elem_bytes, (leading,) + tuple(w.shape[1:]), w.src_strides,

@@ -442,6 +442,44 @@ def test_auto_paths_on_random_layouts():
 
 
 # ---------------------------------------------------------------------------
+# block path: high-rank permutes of short axes
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("eb", WIDTHS)
+def test_block_path_random_high_rank_permutes(eb):
+    """The block tile (up to four axes, a few long runs on both sides) forced on
+    random permutes of 3-7 short axes: chunked axes with ragged last chunks, batch
+    axes outside the tile, unaligned src and dst bases."""
+    rng = np.random.default_rng(400 + eb)
+    done = 0
+    for i in range(40):
+        nd = int(rng.integers(3, 8))
+        shape = tuple(int(x) for x in rng.integers(2, 10, size=nd))
+        if int(np.prod(shape)) * eb > (64 << 20):
+            continue
+        perm = tuple(int(p) for p in rng.permutation(nd))
+        ss, ds = perm_layouts(shape, perm)
+        try:
+            tl.tl_plan(1 << 32, 1 << 44, shape, ss, ds, eb, path="block")
+        except tl.TLError:
+            continue                                  # no block tile for this layout
+        check(shape, ss, ds, eb, "block", seed=400 + i, src_off=i % 3, dst_off=(i // 3) % 2)
+        done += 1
+    assert done >= 20
+
+
+@pytest.mark.parametrize("eb", WIDTHS)
+def test_block_path_named_layouts(eb):
+    """Permutes the planner gives the block tile: the interleaved order of 12^k and a
+    permute of 9^k whose src and dst share two middle axes, at sizes of a few MiB."""
+    for i, (shape, perm) in enumerate((((12,) * 5, (4, 2, 0, 1, 3)),
+                                       ((9,) * 6, (1, 4, 2, 3, 5, 0)),
+                                       ((7, 9, 5, 11, 6), (3, 0, 4, 2, 1)))):
+        ss, ds = perm_layouts(shape, perm)
+        check(shape, ss, ds, eb, "block", seed=450 + i)
+        check(shape, ss, ds, eb, "auto", seed=460 + i, src_off=1, dst_off=1)
+
+
+# ---------------------------------------------------------------------------
 # edge cases
 # ---------------------------------------------------------------------------
 def test_tensor_level_permute_matches_torch():
@@ -571,7 +609,7 @@ def test_panel_tma_timeout_is_reported_and_context_survives():
 # every bench workload at full size, in the launch configuration the bench times
 # ---------------------------------------------------------------------------
 FULL = ["sf_transpose", "tile_transpose", "mx_sf", "attention", "t2d_u8", "t2d_f16", "t2d_f32",
-        "t2d_f64", "t2d_v16", "t2d_odd_f32", "hwc_chw_u8", "nd6_f32"]
+        "t2d_f64", "t2d_v16", "t2d_odd_f32", "hwc_chw_u8", "nd6_f32", "nd8_f32"]
 
 
 def _full(name, path="auto"):

@@ -35,7 +35,7 @@ extern "C" {
 #endif
 
 #define TL_MAX_DIMS 8
-#define TL_VERSION 1
+#define TL_VERSION 2
 
 #if defined(__GNUC__)
 #define TL_API __attribute__((visibility("default")))
@@ -226,7 +226,13 @@ typedef struct tl_permute_opts {
                                     slots at most 12) */
     int32_t cluster_consumer_warps; /* cluster: consumer warps per CTA, 4 or 8 */
     int32_t panel_tile_kib;       /* panel path: tile size, 4..48 KiB (default 32, or 24
-                                     with an extent of 16 or less) */
+                                     with an extent of 16 or less); block path: its
+                                     tile's bytes */
+    int32_t reserved;
+    uint64_t *cta_times;  /* nullable DEVICE array (measurement): the tile, rows, panel
+                             and block kernels write each CTA's start and finish time
+                             (%globaltimer, ns) to cta_times[2 * b] and [2 * b + 1] for
+                             CTA b of the grid tl_plan reports */
 } tl_permute_opts;
 
 /* tl_permute with options (path forcing, status word, buffer bounds): the same
@@ -286,6 +292,27 @@ typedef struct tl_plan_info {
 TL_API int tl_plan(const void *src, const void *dst, int ndim, const int64_t *shape,
             const int64_t *src_strides, const int64_t *dst_strides, int elem_bytes,
             const tl_permute_opts *opts, tl_plan_info *out);
+
+/*
+ * tl_thread_axis_check -- validate a warp's thread-axis layout (TVM "Buffers and
+ * memory", "Buffer APIs", "Registers -- local": S[(32, 8) : (1 @ laneid, 1)] with
+ * R.local(8) puts element (l, j) in register j of lane l) and count the registers
+ * each lane holds.  Host only; the device side is tl_dev::ThreadAxisLayout with
+ * warp_load_lanes / warp_store_lanes in tl_permute_device.cuh.
+ *
+ *   ndim        1..4
+ *   extent      host array of ndim extents (>= 1)
+ *   lane_str    host array: the "s @ laneid" stride of each axis, 0 if the axis is
+ *               a register axis
+ *   reg_str     host array: the register stride of each axis, 0 if the axis is a
+ *               lane axis
+ *   registers   out: registers per lane (P)
+ * Returns TL_OK when every axis is on exactly one side and the coordinates fall on
+ * 32 lanes x P registers once each; TL_ERR_EXTENT otherwise; TL_ERR_ARG for null
+ * pointers or ndim out of range.
+ */
+TL_API int tl_thread_axis_check(int ndim, const int64_t *extent, const int64_t *lane_str,
+                                const int64_t *reg_str, int *registers);
 
 /* Human-readable text of a status code (static storage).  The decline reasons
  * are worded after the reasons the permute_layout dispatch gives ("permute_layout",

@@ -14,6 +14,15 @@
  *       Turns the rotated registers into the plain lane-major fragment (register j
  *       of lane l = element l + 32*j of the tile), the thread-axis layout a
  *       consumer such as an MMA operand expects.
+ *   ThreadAxisLayout / warp_load_lanes / warp_store_lanes
+ *       Thread-axis ("1 @ laneid") layouts of the "Buffers and memory" page
+ *       ("Buffer APIs", "Registers -- local"): every axis is bound either to the
+ *       lane index with a lane stride or to the lane's registers with a register
+ *       stride, so coordinate c sits in register sum(c * reg_str) of lane
+ *       sum(c * lane_str); the load / store move a lane's registers (its `local`
+ *       slice) from / to memory holding the same tensor under memory strides.
+ *       tl_thread_axis_check (host C ABI) validates a layout and counts its
+ *       registers.
  *   dsmem_copy_region
  *       The "copy_async -> dsmem" page ("Algorithm", steps 1-3): one thread maps
  *       the destination buffer and mbarrier into another CTA of the cluster (mapa)
@@ -21,8 +30,9 @@
  *       destination CTA arms its mbarrier with the total bytes and waits.
  *   wait_until_global
  *       The spin wait of the TVM wait_until pull request: relaxed polls of one
- *       global word until a predicate holds, then one acquire load closing the
- *       edge (its value discarded), with a wall-clock bound added.
+ *       global word (32 or 64 bits, at a chosen scope, with an opt-in backoff)
+ *       until a predicate holds, then one acquire load closing the edge (its value
+ *       discarded), with a wall-clock bound added.
  *
  * Element types are raw bits: use uint8_t, uint16_t, uint32_t, uint2 or uint4 for
  * 1, 2, 4, 8 and 16-byte elements.
@@ -130,6 +140,65 @@ __device__ __forceinline__ void warp_fragment_rotate(T (&regs)[P], int shift, in
 }
 
 // ---------------------------------------------------------------------------
+// Thread-axis layouts ("Buffers and memory", "Buffer APIs", "Registers -- local")
+// ---------------------------------------------------------------------------
+
+/* A warp's thread-axis layout over up to 4 axes: axis k is bound to the lane index
+ * (lane_str[k] > 0, reg_str[k] == 0) or to the lane's registers (reg_str[k] > 0,
+ * lane_str[k] == 0); the coordinate c lives in register sum(c * reg_str) of lane
+ * sum(c * lane_str).  The page's S[(32, 8) : (1 @ laneid, 1)] is n = 2, ext = (32, 8),
+ * lane_str = (1, 0), reg_str = (0, 1): element (l, j) in register j of lane l.
+ * mem_str are the element strides of the same tensor in memory.  Lane and register
+ * strides must place the prod(ext) coordinates on 32 lanes x P registers once each
+ * (tl_thread_axis_check verifies a layout on the host and returns P). */
+struct ThreadAxisLayout {
+    int32_t n;
+    int32_t ext[4];
+    int32_t lane_str[4];
+    int32_t reg_str[4];
+    int64_t mem_str[4];
+};
+
+/* Memory offset (elements) of the part of a coordinate that the lane index fixes. */
+__device__ __forceinline__ int64_t lane_offset(const ThreadAxisLayout& t, int lane) {
+    int64_t off = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (k < t.n && t.lane_str[k] > 0)
+            off += (int64_t)((lane / t.lane_str[k]) % t.ext[k]) * t.mem_str[k];
+    return off;
+}
+
+/* Memory offset (elements) of the part of a coordinate that register j fixes. */
+__device__ __forceinline__ int64_t register_offset(const ThreadAxisLayout& t, int j) {
+    int64_t off = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (k < t.n && t.reg_str[k] > 0)
+            off += (int64_t)((j / t.reg_str[k]) % t.ext[k]) * t.mem_str[k];
+    return off;
+}
+
+/* The calling lane's P registers of layout `t` from memory at `src` (every lane of
+ * the warp calls it; no synchronisation is needed, each lane reads its own). */
+template <int P, typename T>
+__device__ __forceinline__ void warp_load_lanes(T (&regs)[P], const T* src,
+                                                const ThreadAxisLayout& t) {
+    const T* base = src + lane_offset(t, lane_id());
+#pragma unroll
+    for (int j = 0; j < P; ++j) regs[j] = base[register_offset(t, j)];
+}
+
+/* The calling lane's P registers of layout `t` to memory at `dst`. */
+template <int P, typename T>
+__device__ __forceinline__ void warp_store_lanes(const T (&regs)[P], T* dst,
+                                                 const ThreadAxisLayout& t) {
+    T* base = dst + lane_offset(t, lane_id());
+#pragma unroll
+    for (int j = 0; j < P; ++j) base[register_offset(t, j)] = regs[j];
+}
+
+// ---------------------------------------------------------------------------
 // DSMEM region copy ("copy_async -> dsmem")
 // ---------------------------------------------------------------------------
 
@@ -210,37 +279,88 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+/* Memory scope of the polls and of the closing acquire (the pull request's
+ * `scope`): .cta, .cluster, .gpu or .sys. */
+enum class WaitScope { cta, cluster, gpu, sys };
+
+/* Relaxed and acquire loads of a 32- or 64-bit global word at scope S (the pull
+ * request's ptx_type: any 4- or 8-byte type is read as its raw bits; 128 bits is
+ * refused at compile time, its value is not a scalar a predicate can test). */
+template <WaitScope S, typename W>
+__device__ __forceinline__ W ld_wait_word(const W* p, bool acquire) {
+    static_assert(sizeof(W) == 4 || sizeof(W) == 8, "wait words are 32 or 64 bits");
+    if constexpr (sizeof(W) == 4) {
+        uint32_t v;
+#define TL_LD32(SEM, SC)                                                                   \
+    asm volatile("ld." SEM "." SC ".global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory")
+        if (acquire) {
+            if constexpr (S == WaitScope::cta) TL_LD32("acquire", "cta");
+            else if constexpr (S == WaitScope::cluster) TL_LD32("acquire", "cluster");
+            else if constexpr (S == WaitScope::gpu) TL_LD32("acquire", "gpu");
+            else TL_LD32("acquire", "sys");
+        } else {
+            if constexpr (S == WaitScope::cta) TL_LD32("relaxed", "cta");
+            else if constexpr (S == WaitScope::cluster) TL_LD32("relaxed", "cluster");
+            else if constexpr (S == WaitScope::gpu) TL_LD32("relaxed", "gpu");
+            else TL_LD32("relaxed", "sys");
+        }
+#undef TL_LD32
+        W w;
+        __builtin_memcpy(&w, &v, 4);
+        return w;
+    } else {
+        uint64_t v;
+#define TL_LD64(SEM, SC)                                                                   \
+    asm volatile("ld." SEM "." SC ".global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory")
+        if (acquire) {
+            if constexpr (S == WaitScope::cta) TL_LD64("acquire", "cta");
+            else if constexpr (S == WaitScope::cluster) TL_LD64("acquire", "cluster");
+            else if constexpr (S == WaitScope::gpu) TL_LD64("acquire", "gpu");
+            else TL_LD64("acquire", "sys");
+        } else {
+            if constexpr (S == WaitScope::cta) TL_LD64("relaxed", "cta");
+            else if constexpr (S == WaitScope::cluster) TL_LD64("relaxed", "cluster");
+            else if constexpr (S == WaitScope::gpu) TL_LD64("relaxed", "gpu");
+            else TL_LD64("relaxed", "sys");
+        }
+#undef TL_LD64
+        W w;
+        __builtin_memcpy(&w, &v, 8);
+        return w;
+    }
+}
+
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+    return ld_wait_word<WaitScope::gpu>(p, false);
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+    return ld_wait_word<WaitScope::gpu>(p, true);
 }
 
-/* Spin on *word with relaxed loads (the first one peeled) until pred(value)
- * holds, then issue one acquire load of the word whose value is discarded (it
- * may be later than the accepted one).  The accepted value goes to *value.
- * Returns false, without the acquire, once timeout_ns of wall time has passed.
- * Publishers release the word (st.release, atom, red).  Waits inside a CTA or a
- * cluster belong on an mbarrier instead. */
-template <typename Pred>
-__device__ __forceinline__ bool wait_until_global(const uint32_t* word, Pred pred,
-                                                  uint64_t timeout_ns, uint32_t* value) {
-    uint32_t v = ld_relaxed_gpu(word);
+/* Spin on *word with relaxed loads at scope S (the first one peeled) until
+ * pred(value) holds, then issue one acquire load of the word whose value is
+ * discarded (it may be later than the accepted one).  The accepted value goes to
+ * *value.  backoff_ns > 0 sleeps that long (__nanosleep) between polls, which the
+ * pull request measured as never faster (+1.35 % at 20 ns, +30 % at 2 us), so it
+ * is opt-in.  Returns false, without the acquire, once timeout_ns of wall time has
+ * passed.  W is a 32- or 64-bit word type.  Publishers release the word
+ * (st.release, atom, red).  Waits inside a CTA or a cluster belong on an
+ * mbarrier instead (shared memory is not a global word). */
+template <WaitScope S = WaitScope::gpu, typename W, typename Pred>
+__device__ __forceinline__ bool wait_until_global(const W* word, Pred pred, uint64_t timeout_ns,
+                                                  W* value, uint32_t backoff_ns = 0) {
+    W v = ld_wait_word<S>(word, false);
     if (!pred(v)) {
         const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
         do {
             if (global_timer_ns() - t0 > timeout_ns) return false;
-            v = ld_relaxed_gpu(word);
+            if (backoff_ns) __nanosleep(backoff_ns);
+            v = ld_wait_word<S>(word, false);
         } while (!pred(v));
     }
-    (void)ld_acquire_gpu(word);
+    (void)ld_wait_word<S>(word, true);
     *value = v;
     return true;
 }
@@ -248,6 +368,9 @@ __device__ __forceinline__ bool wait_until_global(const uint32_t* word, Pred pre
 /* The publishing side: a release store of a word. */
 __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_gpu(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 }  // namespace tl_dev

@@ -24,7 +24,7 @@ __all__ = [
     "TL_FLAG_DEBUG_CHECKS", "TL_FLAG_TEST_SKIP_HOST_BOUNDS", "TL_FLAG_PANEL_ELEMENT_STORES",
     "load", "library_path", "tl_layout_canon", "tl_choose_xor_k", "tl_bank_conflicts",
     "tl_permute", "tl_permute_ex", "tl_plan", "tl_status_string", "tl_launch_count",
-    "tl_plan_cache_hits",
+    "tl_plan_cache_hits", "tl_thread_axis_check",
     "tl_version", "permute", "tl_permute_tile_noalloc",
 ]
 
@@ -70,7 +70,8 @@ class TlPermuteOpts(ctypes.Structure):
                 ("src_bytes", _i64), ("dst_bytes", _i64), ("tile_group", _i32),
                 ("tile_stages", _i32), ("tile_ctas_per_sm", _i32), ("tile_l2_promotion", _i32),
                 ("tile_rows", _i32), ("cluster_recv_stages", _i32),
-                ("cluster_consumer_warps", _i32), ("panel_tile_kib", _i32)]
+                ("cluster_consumer_warps", _i32), ("panel_tile_kib", _i32),
+                ("reserved", _i32), ("cta_times", ctypes.c_void_p)]
 
 
 class TlPlanInfo(ctypes.Structure):
@@ -105,6 +106,7 @@ def load():
                                         i64p, ctypes.POINTER(TlLayout), ctypes.POINTER(TlLayout),
                                         i64p]
         lib.tl_choose_xor_k.argtypes = [ctypes.c_int, i64p, i64p, i64p, ctypes.c_int, ip, ip, ip]
+        lib.tl_thread_axis_check.argtypes = [ctypes.c_int, i64p, i64p, i64p, ip]
         lib.tl_bank_conflicts.argtypes = [ctypes.c_int, i64p, ctypes.c_int, ctypes.c_int]
         lib.tl_permute.argtypes = [vp, vp, ctypes.c_int, i64p, i64p, i64p, ctypes.c_int, vp]
         lib.tl_permute_ex.argtypes = [vp, vp, ctypes.c_int, i64p, i64p, i64p, ctypes.c_int, vp,
@@ -209,6 +211,16 @@ def tl_layout_canon(shape, src_strides, dst_strides, begin=None, extent=None, sr
                 chunk_elems=chunk.value)
 
 
+def tl_thread_axis_check(extent, lane_strides, reg_strides) -> int:
+    """Registers per lane of a warp's thread-axis ("1 @ laneid") layout; raises
+    TLError if the layout does not place its coordinates on 32 lanes once each."""
+    p = ctypes.c_int()
+    _check(load().tl_thread_axis_check(len(extent), _arr(extent), _arr(lane_strides),
+                                       _arr(reg_strides), ctypes.byref(p)),
+           "tl_thread_axis_check")
+    return p.value
+
+
 def tl_choose_xor_k(extent, src_str, dst_str, elem_bytes):
     """(k, shift, mask) of the warp permute's XOR swizzle; raises TLError if none."""
     k, shift, mask = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
@@ -227,8 +239,9 @@ def tl_bank_conflicts(lane_offsets, elem_bytes, model="conservative") -> int:
 
 def _opts(flags=0, path="auto", dev_status=0, src_bytes=0, dst_bytes=0, max_ctas=0,
           tile_group=0, tile_stages=0, tile_ctas_per_sm=0, tile_l2_promotion=0, tile_rows=0,
-          cluster_recv_stages=0, cluster_consumer_warps=0, panel_tile_kib=0):
+          cluster_recv_stages=0, cluster_consumer_warps=0, panel_tile_kib=0, cta_times=0):
     o = TlPermuteOpts()
+    o.cta_times = int(cta_times) or None
     o.panel_tile_kib = int(panel_tile_kib)
     o.cluster_consumer_warps = int(cluster_consumer_warps)
     o.tile_rows = int(tile_rows)

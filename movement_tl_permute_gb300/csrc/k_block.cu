@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kBlockThreads) k_block(const BlockArgs a) {
     __syncthreads();
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
+    dev::cta_start(a.cta_times);
 
     const int64_t first = blockIdx.x, step = gridDim.x;
     const int64_t mine = first < a.tiles ? (a.tiles - first + step - 1) / step : 0;
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(kBlockThreads) k_block(const BlockArgs a) {
         ahead = ahead + 1 == kBlockStages ? 0 : ahead + 1;
     }
     cp_async_wait<0>();
+    dev::cta_finish(a.cta_times);
 }
 
 }  // namespace

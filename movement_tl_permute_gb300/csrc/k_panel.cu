@@ -572,6 +572,7 @@ __global__ void __launch_bounds__(kPanelThreads, VEC ? 3 : 4) k_panel(const Pane
     const uint32_t stage = (uint32_t)a.stage_bytes;
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
+    dev::cta_start(a.cta_times);
     const int64_t first = blockIdx.x, step = gridDim.x;
     const int64_t mine = first < a.tiles ? (a.tiles - first + step - 1) / step : 0;
 
@@ -594,6 +595,7 @@ __global__ void __launch_bounds__(kPanelThreads, VEC ? 3 : 4) k_panel(const Pane
         ahead = ahead + 1 == kPanelStages ? 0 : ahead + 1;
     }
     cp_async_wait<0>();
+    dev::cta_finish(a.cta_times);
 }
 
 // The panel transpose for block rows whose pitch TMA cannot take directly (a row
@@ -624,6 +626,7 @@ k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
     __syncthreads();
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
+    dev::cta_start(a.cta_times);
     const int64_t first = blockIdx.x, step = gridDim.x;
     const int64_t mine = first < a.tiles ? (a.tiles - first + step - 1) / step : 0;
     const uint32_t phi = 1u << a.phi_lg;
@@ -666,6 +669,7 @@ k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
             dev::mbar_wait(&full[k % kPanelStages], (uint32_t)(k / kPanelStages) & 1u,
                            dev::kDrainFactor * (uint64_t)a.timeout_ns);
     }
+    dev::cta_finish(a.cta_times);
 }
 
 }  // namespace

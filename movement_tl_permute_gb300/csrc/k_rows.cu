@@ -114,6 +114,7 @@ template <int EB, int R>
 __global__ void __launch_bounds__(rows_threads<R>()) k_rows(const RowsArgs a) {
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
+    dev::cta_start(a.cta_times);
     constexpr int U = rows_units<R>();
     constexpr int kWarps = rows_threads<R>() / 32;
     __shared__ __align__(16) uint4 stage[kWarps][32 * R];
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(rows_threads<R>()) k_rows(const RowsArgs a) {
             __syncwarp();
         }
     }
+    dev::cta_finish(a.cta_times);
 }
 
 template <int EB, int R>

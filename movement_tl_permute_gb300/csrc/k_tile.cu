@@ -54,6 +54,7 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
     // everything above touched shared memory only
     grid_dependency_wait();
     allow_dependent_launch();
+    cta_start(a.cta_times);
 
     if (warp == kConsumerWarps) {
         // ---------------- producer: one elected lane issues all TMA loads -------------
@@ -81,6 +82,7 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
             for (uint32_t i = issued > S ? issued - S : 0; i < issued; ++i)
                 mbar_wait(&full[i % S], (i / S) & 1, kDrainFactor * a.timeout_ns);
         }
+        cta_finish(a.cta_times);
         return;
     }
 
@@ -101,6 +103,7 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
+    cta_finish(a.cta_times);
 }
 
 }  // namespace

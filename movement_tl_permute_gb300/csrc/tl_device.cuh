@@ -206,6 +206,17 @@ __device__ __forceinline__ void allow_dependent_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Per-CTA timing (measurement): thread 0 records the CTA's start, and every warp
+// that calls cta_finish raises its finish to the time it got there (%globaltimer).
+__device__ __forceinline__ void cta_start(uint64_t* times) {
+    if (times && threadIdx.x == 0) times[2 * blockIdx.x] = global_timer_ns();
+}
+__device__ __forceinline__ void cta_finish(uint64_t* times) {
+    if (times && (threadIdx.x & 31) == 0)
+        atomicMax(reinterpret_cast<unsigned long long*>(&times[2 * blockIdx.x + 1]),
+                  (unsigned long long)global_timer_ns());
+}
+
 // Records the first error of a launch in the caller's status word (if any).
 __device__ __forceinline__ void report(int32_t* status, int32_t code) {
     if (status) atomicCAS(status, 0, code);

@@ -1360,6 +1360,38 @@ int tl_layout_canon(const tl_layout* src, const tl_layout* dst, const int64_t* b
     return TL_OK;
 }
 
+int tl_thread_axis_check(int ndim, const int64_t* extent, const int64_t* lane_str,
+                         const int64_t* reg_str, int* registers) {
+    if (ndim < 1 || ndim > 4 || !extent || !lane_str || !reg_str || !registers)
+        return TL_ERR_ARG;
+    int64_t total = 1;
+    for (int k = 0; k < ndim; ++k) {
+        if (extent[k] < 1 || lane_str[k] < 0 || reg_str[k] < 0) return TL_ERR_EXTENT;
+        if ((lane_str[k] > 0) == (reg_str[k] > 0)) return TL_ERR_EXTENT;   // one side each
+        total *= extent[k];
+        if (total > 32 * 256) return TL_ERR_EXTENT;        // at most 256 registers a lane
+    }
+    if (total % 32 != 0) return TL_ERR_EXTENT;
+    const int64_t P = total / 32;
+    // every coordinate once on (lane, register), enumerated
+    std::vector<char> seen((size_t)total, 0);
+    for (int64_t f = 0; f < total; ++f) {
+        int64_t x = f, lane = 0, reg = 0;
+        for (int k = ndim - 1; k >= 0; --k) {
+            const int64_t c = x % extent[k];
+            x /= extent[k];
+            lane += c * lane_str[k];
+            reg += c * reg_str[k];
+        }
+        if (lane >= 32 || reg >= P) return TL_ERR_EXTENT;
+        char& s = seen[(size_t)(lane * P + reg)];
+        if (s) return TL_ERR_EXTENT;
+        s = 1;
+    }
+    *registers = (int)P;
+    return TL_OK;
+}
+
 int tl_choose_xor_k(int ndim, const int64_t* extent, const int64_t* src_str,
                     const int64_t* dst_str, int elem_bytes, int* k, int* shift, int* mask) {
     if (!extent || !src_str || !dst_str || !k || !shift || !mask) return TL_ERR_ARG;

@@ -83,6 +83,7 @@ __host__ __device__ constexpr int cluster_threads(int ncw) { return (ncw + 3) * 
 struct TileArgs {
     uint8_t* dst;
     int32_t* status;
+    uint64_t* cta_times;                 // measurement: per-CTA start / finish (or null)
     int64_t ext_a, ext_b, ds_a;          // elements
     int64_t tiles_a, tiles_b, tiles, group_b;
     int32_t nbatch, rank, vec_store;
@@ -118,6 +119,7 @@ cudaError_t launch_cluster(int eb, int ncw, const CUtensorMap& map, const TileAr
 struct RowsArgs {
     const uint8_t* src;
     uint8_t* dst;
+    uint64_t* cta_times;         // measurement: per-CTA start / finish (or null)
     int64_t units;               // 16-byte source columns over all batch items
     int64_t upr;                 // units per plane (ext_a * EB / 16)
     int64_t ss_b;                // src stride of b, elements
@@ -214,6 +216,7 @@ struct PanelArgs {
     dev::DivU32 d_a1;
     int64_t timeout_ns;
     int32_t* status;
+    uint64_t* cta_times;         // measurement: per-CTA start / finish (or null)
 };
 // The phase maps of k_panel_tma: map j covers the src rows b = j mod phi of the
 // plane (stride phi * row pitch), its base aligned down to 16 bytes.
@@ -239,6 +242,7 @@ constexpr int kBlockMaxSmem = 200 * 1024;   // stages of at most 48 KiB + the ta
 struct BlockArgs {
     const uint8_t* src;
     uint8_t* dst;
+    uint64_t* cta_times;         // measurement: per-CTA start / finish (or null)
     // tables: the axes whose digits make i (dst-run axes), j (dst-run index axes)
     // and r (src-run index axes), innermost first, with the tile's extents; for
     // each, its src-run position stride (elements, 0 off the src run), its src-run

@@ -762,6 +762,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         if (rc != TL_OK) return rc;
         a.dst = d8;
         a.status = opts ? opts->dev_status : nullptr;
+        a.cta_times = opts ? opts->cta_times : nullptr;
         a.ext_a = p.ext_a;
         a.ext_b = p.ext_b;
         a.ds_a = p.ds_a;
@@ -869,6 +870,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         const bool drop = (flags & TL_FLAG_TEST_DROP_HANDOFF) != 0;
         a.timeout_ns = drop ? kTestTimeoutNs : kDefaultTimeoutNs;
         a.status = opts ? opts->dev_status : nullptr;
+        a.cta_times = opts ? opts->cta_times : nullptr;
         a.drop_load = drop && p.panel_tma ? 1 : 0;
         if (p.panel_phase) {
             a.phase = 1;
@@ -898,6 +900,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         BlockArgs a = block_args(p);
         a.src = s8;
         a.dst = d8;
+        a.cta_times = opts ? opts->cta_times : nullptr;
         err = launch_block(eb, a, l.grid, st, pdl);
         break;
     }
@@ -926,6 +929,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         RowsArgs a{};
         a.src = s8;
         a.dst = d8;
+        a.cta_times = opts ? opts->cta_times : nullptr;
         a.units = p.tiles;
         a.upr = p.ext_a * eb / 16;
         a.ss_b = p.ss_b;

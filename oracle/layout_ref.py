@@ -11,6 +11,8 @@ plus an element offset; coordinate ``c`` maps to ``offset + sum(c[i]*stride[i])`
 """
 from __future__ import annotations
 
+import itertools
+
 from itertools import product
 
 WARP = 32           # lanes per warp
@@ -253,6 +255,61 @@ def warp_permute_ref(buf_src, buf_dst, extent, src_str, dst_str, k, shift,
     for r, lanes in enumerate(writes):                                # phase 2
         for lane, o in enumerate(lanes):
             buf_dst[o] = regs[r][lane]
+
+
+# ---------------------------------------------------------------------------
+# Thread-axis layouts ("Buffers and memory", "Buffer APIs", "Registers -- local")
+# ---------------------------------------------------------------------------
+def thread_axis_places(shape, lane_strides, reg_strides):
+    """Where each coordinate of a warp's thread-axis ``local`` layout lives.
+
+    An axis either carries a stride ``s @ laneid`` (``lane_strides[k] = s``,
+    ``reg_strides[k] = 0``) or a plain register stride (``reg_strides[k] = s``,
+    ``lane_strides[k] = 0``): coordinate c sits in lane sum(c * lane_strides) and in
+    that lane's register sum(c * reg_strides), the "local" slice of the page's
+    ``S[(32, 8) : (1 @ laneid, 1)]`` example taken one lane at a time.  Returns
+    ``{coord: (lane, register)}`` for every coordinate, row-major."""
+    out = {}
+    for c in itertools.product(*[range(e) for e in shape]):
+        lane = sum(ci * s for ci, s in zip(c, lane_strides))
+        reg = sum(ci * s for ci, s in zip(c, reg_strides))
+        out[c] = (lane, reg)
+    return out
+
+
+def thread_axis_registers(shape, lane_strides, reg_strides):
+    """Registers per lane of a valid thread-axis layout, else None.  Valid: every
+    axis on exactly one side, and the map coordinate -> (lane, register) a bijection
+    onto 32 lanes x P registers (checked by enumerating it)."""
+    if any((ls != 0) == (rs != 0) for ls, rs in zip(lane_strides, reg_strides)):
+        return None
+    if any(ls < 0 or rs < 0 for ls, rs in zip(lane_strides, reg_strides)):
+        return None
+    n = 1
+    for e in shape:
+        n *= e
+    if n % 32:
+        return None
+    P = n // 32
+    places = thread_axis_places(shape, lane_strides, reg_strides)
+    seen = set(places.values())
+    if len(seen) != n or seen != {(l, r) for l in range(32) for r in range(P)}:
+        return None
+    return P
+
+
+def thread_axis_fragment(buf, shape, mem_strides, lane_strides, reg_strides, offset=0):
+    """Lane l's registers of a thread-axis layout loaded from a memory buffer that
+    holds the same logical tensor under ``mem_strides``: an array [32, P] whose
+    entry (l, j) is buf[offset + sum(c * mem_strides)] for the coordinate c placed
+    in lane l, register j."""
+    P = thread_axis_registers(shape, lane_strides, reg_strides)
+    if P is None:
+        raise ValueError("not a thread-axis layout of one warp")
+    out = [[None] * P for _ in range(32)]
+    for c, (lane, reg) in thread_axis_places(shape, lane_strides, reg_strides).items():
+        out[lane][reg] = buf[offset + apply(c, mem_strides)]
+    return out
 
 
 # ---------------------------------------------------------------------------

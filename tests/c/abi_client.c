@@ -39,7 +39,7 @@ static tl_layout layout(int n, const int64_t *shape, const int64_t *stride) {
 }
 
 int main(void) {
-    expect(tl_version() == 1, "tl_version is 1");
+    expect(tl_version() == 2, "tl_version is 2");
     expect(strcmp(tl_status_string(TL_OK), "ok") == 0, "tl_status_string(TL_OK)");
 
     /* the SF transpose of the permute_layout page */

@@ -138,6 +138,60 @@ extern "C" int tdp_fragment(const void* src, void* dst, int eb, int P, const Til
 }
 
 // ---------------------------------------------------------------------------
+// Thread-axis layouts: one warp loads its registers through layout L from `src`
+// and writes them out lane-major (regs[j] of lane l to frag[l * P + j]); a second
+// launch reads them back from `frag` and stores them through L into `dst`.
+namespace {
+template <int EB, int P>
+__global__ void k_lanes_load(const uint8_t* src, uint8_t* frag, tl_dev::ThreadAxisLayout t) {
+    using T = typename Raw<EB>::T;
+    T regs[P];
+    tl_dev::warp_load_lanes<P>(regs, reinterpret_cast<const T*>(src), t);
+    T* f = reinterpret_cast<T*>(frag) + tl_dev::lane_id() * P;
+#pragma unroll
+    for (int j = 0; j < P; ++j) f[j] = regs[j];
+}
+
+template <int EB, int P>
+__global__ void k_lanes_store(const uint8_t* frag, uint8_t* dst, tl_dev::ThreadAxisLayout t) {
+    using T = typename Raw<EB>::T;
+    T regs[P];
+    const T* f = reinterpret_cast<const T*>(frag) + tl_dev::lane_id() * P;
+#pragma unroll
+    for (int j = 0; j < P; ++j) regs[j] = f[j];
+    tl_dev::warp_store_lanes<P>(regs, reinterpret_cast<T*>(dst), t);
+}
+
+template <int EB, int P>
+cudaError_t go_lanes(const void* src, void* frag, void* dst, const tl_dev::ThreadAxisLayout& t) {
+    k_lanes_load<EB, P><<<1, 32>>>(static_cast<const uint8_t*>(src), static_cast<uint8_t*>(frag), t);
+    k_lanes_store<EB, P><<<1, 32>>>(static_cast<const uint8_t*>(frag), static_cast<uint8_t*>(dst), t);
+    return cudaGetLastError();
+}
+}  // namespace
+
+extern "C" int tdp_lanes(const void* src, void* frag, void* dst, int eb, int P,
+                         const tl_dev::ThreadAxisLayout* layout) {
+    const tl_dev::ThreadAxisLayout t = *layout;
+    switch (eb * 100 + P) {
+    case 101: return go_lanes<1, 1>(src, frag, dst, t);
+    case 102: return go_lanes<1, 2>(src, frag, dst, t);
+    case 108: return go_lanes<1, 8>(src, frag, dst, t);
+    case 202: return go_lanes<2, 2>(src, frag, dst, t);
+    case 208: return go_lanes<2, 8>(src, frag, dst, t);
+    case 401: return go_lanes<4, 1>(src, frag, dst, t);
+    case 402: return go_lanes<4, 2>(src, frag, dst, t);
+    case 404: return go_lanes<4, 4>(src, frag, dst, t);
+    case 408: return go_lanes<4, 8>(src, frag, dst, t);
+    case 416: return go_lanes<4, 16>(src, frag, dst, t);
+    case 804: return go_lanes<8, 4>(src, frag, dst, t);
+    case 808: return go_lanes<8, 8>(src, frag, dst, t);
+    case 1602: return go_lanes<16, 2>(src, frag, dst, t);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
 // DSMEM region copy between the two CTAs of a cluster
 // ---------------------------------------------------------------------------
 namespace {
@@ -239,7 +293,45 @@ __global__ void k_wait(uint32_t* flag, uint32_t* data, uint32_t* out, int32_t* s
         for (int i = threadIdx.x; i < n; i += blockDim.x) out[i] = data[i];
 }
 
+// The same protocol on a 64-bit word: relaxed polls at system scope with a 100 ns
+// backoff between them, the publisher releasing 2^40 + 7 (so that only a 64-bit
+// read sees the value its predicate wants).
+__global__ void k_wait64(uint64_t* flag, uint32_t* data, uint32_t* out, int32_t* status, int n,
+                         int publish, uint64_t timeout_ns) {
+    if (blockIdx.x == 0) {
+        if (!publish) return;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) data[i] = 2246822519u * i + 7u;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const uint64_t t0 = tl_dev::global_timer_ns();
+            while (tl_dev::global_timer_ns() - t0 < 200000) {}
+            tl_dev::st_release_gpu(flag, (1ull << 40) + 7ull);
+        }
+        return;
+    }
+    __shared__ int ok;
+    if (threadIdx.x == 0) {
+        uint64_t v = 0;
+        ok = tl_dev::wait_until_global<tl_dev::WaitScope::sys>(
+                 flag, [](uint64_t x) { return x > (1ull << 32); }, timeout_ns, &v, 100u)
+                 ? 1 : 0;
+        status[0] = ok;
+        status[1] = (int32_t)(v >> 32);
+        status[2] = (int32_t)(v & 0xffffffffu);
+    }
+    __syncthreads();
+    if (ok)
+        for (int i = threadIdx.x; i < n; i += blockDim.x) out[i] = data[i];
+}
+
 }  // namespace
+
+extern "C" int tdp_wait64(uint64_t* flag, uint32_t* data, uint32_t* out, int32_t* status, int n,
+                          int publish, uint64_t timeout_ns) {
+    void* args[] = {&flag, &data, &out, &status, &n, &publish, &timeout_ns};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&k_wait64), dim3(2),
+                                       dim3(128), args, 0, 0);
+}
 
 extern "C" int tdp_dsmem(const void* src, void* dst, int32_t* status, const RegionArgs* args) {
     const RegionArgs a = *args;

@@ -35,6 +35,11 @@ class TileArgs(ctypes.Structure):
                 ("shift", _i32), ("mask", _i32), ("in_place", _i32), ("items", _i32)]
 
 
+class ThreadAxisLayout(ctypes.Structure):
+    _fields_ = [("n", _i32), ("ext", _i32 * 4), ("lane_str", _i32 * 4), ("reg_str", _i32 * 4),
+                ("mem_str", _i64 * 4)]
+
+
 class ChunkLoop(ctypes.Structure):
     _fields_ = [("chunk_bytes", ctypes.c_uint32), ("outer_n", _i32), ("outer_ext", _i32 * 4),
                 ("src_stride", _i64 * 4), ("dst_stride", _i64 * 4)]
@@ -64,8 +69,11 @@ def lib():
     vp = ctypes.c_void_p
     h.tdp_warp_smem.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(TileArgs)]
     h.tdp_fragment.argtypes = [vp, vp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(TileArgs)]
+    h.tdp_lanes.argtypes = [vp, vp, vp, ctypes.c_int, ctypes.c_int,
+                            ctypes.POINTER(ThreadAxisLayout)]
     h.tdp_dsmem.argtypes = [vp, vp, vp, ctypes.POINTER(RegionArgs)]
     h.tdp_wait.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_uint64]
+    h.tdp_wait64.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_uint64]
     h.tdp_dsmem_stream.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_uint64, vp]
     return h
 
@@ -226,6 +234,28 @@ def test_wait_until_global(lib, publish):
         assert not bool(out.any())
 
 
+@pytest.mark.parametrize("publish", [1, 0])
+def test_wait_until_global_64_bit_word_system_scope_with_backoff(lib, publish):
+    """The pull request's other parameters ("Other parameters"): a 64-bit word read
+    as raw bits, polls at system scope, an opt-in backoff between polls; the
+    accepted value is the whole 64-bit word, and the bounded wait still gives up
+    when nobody publishes."""
+    n = 4096
+    flag = torch.zeros(1, dtype=torch.int64, device="cuda")
+    data = torch.zeros(n, dtype=torch.int32, device="cuda")
+    out = torch.zeros(n, dtype=torch.int32, device="cuda")
+    status = torch.full((3,), -1, dtype=torch.int32, device="cuda")
+    assert lib.tdp_wait64(flag.data_ptr(), data.data_ptr(), out.data_ptr(), status.data_ptr(),
+                          n, publish, 20_000_000) == 0
+    torch.cuda.synchronize()
+    if publish:
+        assert status.tolist() == [1, 1 << 8, 7]
+        assert torch.equal(out, data) and int(data[1].item()) != 0
+    else:
+        assert int(status[0].item()) == 0
+        assert not bool(out.any())
+
+
 def test_dsmem_stream_ceiling(lib):
     """The cluster hand-off pattern with no HBM traffic: 16 KiB pushes into 2-slot
     rings of the peer, released by remote arrives, 3 CTAs per SM.  Prints the
@@ -245,3 +275,58 @@ def test_dsmem_stream_ceiling(lib):
     print("\nDSMEM hand-off ceiling: %.0f GB/s pushed (grid %d, %d pushes of 16 KiB per CTA)"
           % (gbs, grid, iters))
     assert gbs > 100
+
+
+# ---------------------------------------------------------------------------
+# thread-axis ("1 @ laneid") layouts: a lane's local registers
+# ---------------------------------------------------------------------------
+LANE_LAYOUTS = [
+    # the page's S[(32, 8) : (1 @ laneid, 1)] over a row-major and a transposed buffer
+    ((32, 8), (1, 0), (0, 1), (8, 1)),
+    ((32, 8), (1, 0), (0, 1), (1, 32)),
+    # lanes over two axes, one register axis
+    ((4, 8, 2), (8, 1, 0), (0, 0, 1), (16, 2, 1)),
+    # the lane axis in the middle, registers from the outer and inner axes, two orders
+    ((2, 32, 4), (0, 1, 0), (4, 0, 1), (128, 4, 1)),
+    ((2, 32, 4), (0, 1, 0), (1, 0, 2), (128, 4, 1)),
+    # lanes split around a register axis, memory padded
+    ((8, 16, 4), (4, 0, 1), (0, 1, 0), (100, 6, 1)),
+]
+
+
+@pytest.mark.parametrize("eb", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("case", range(len(LANE_LAYOUTS)))
+def test_thread_axis_load_and_store_match_the_oracle(lib, eb, case):
+    """warp_load_lanes puts in lane l's register j the element the oracle places
+    there (thread_axis_fragment), for every element width; warp_store_lanes puts it
+    back where it came from, leaving the padding untouched."""
+    shape, ls, rs, ms = LANE_LAYOUTS[case]
+    P = tl.tl_thread_axis_check(shape, ls, rs)
+    assert P == L.thread_axis_registers(shape, ls, rs)
+    if (eb, P) not in {(1, 1), (1, 2), (1, 8), (2, 2), (2, 8), (4, 1), (4, 2), (4, 4), (4, 8),
+                       (4, 16), (8, 4), (8, 8), (16, 2)}:
+        pytest.skip("no test kernel for this register count and width")
+    span = sum((e - 1) * m for e, m in zip(shape, ms)) + 1
+    src = workloads.random_bits(span * eb, 700 + case)
+    lay = ThreadAxisLayout()
+    lay.n = len(shape)
+    for k in range(len(shape)):
+        lay.ext[k], lay.lane_str[k], lay.reg_str[k], lay.mem_str[k] = shape[k], ls[k], rs[k], ms[k]
+    s_gpu = torch.from_numpy(src).cuda()
+    frag = torch.zeros(32 * P * eb, dtype=torch.uint8, device="cuda")
+    back = torch.full((span * eb,), 0x3C, dtype=torch.uint8, device="cuda")
+    assert lib.tdp_lanes(s_gpu.data_ptr(), frag.data_ptr(), back.data_ptr(), eb, P,
+                         ctypes.byref(lay)) == 0
+    torch.cuda.synchronize()
+    elems = src.reshape(-1, eb)
+    want = L.thread_axis_fragment([bytes(e) for e in elems], shape, ms, ls, rs)
+    got = frag.cpu().numpy().reshape(32, P, eb)
+    for lane in range(32):
+        for j in range(P):
+            assert bytes(got[lane, j]) == want[lane][j], (lane, j)
+    # the store writes exactly the layout's elements back
+    expect = np.full(span * eb, 0x3C, dtype=np.uint8).reshape(-1, eb)
+    for c in L.thread_axis_places(shape, ls, rs):
+        o = L.apply(c, ms)
+        expect[o] = elems[o]
+    assert np.array_equal(back.cpu().numpy(), expect.reshape(-1))

@@ -479,6 +479,25 @@ def test_block_path_named_layouts(eb):
         check(shape, ss, ds, eb, "auto", seed=460 + i, src_off=1, dst_off=1)
 
 
+def test_per_cta_times_are_recorded_without_changing_the_result():
+    """The measurement option: the tile, rows, panel and block kernels write each
+    CTA's start and finish time, every CTA of the grid tl_plan reports once, and the
+    permute is the same."""
+    cases = [((300, 520), (520, 1), (1, 300), 4, "tile"),
+             ((1024, 2, 4, 32), (256, 128, 32, 1), (256, 128, 1, 4), 1, "rows"),
+             ((301, 517), (517, 1), (1, 301), 4, "panel"),
+             ((12,) * 5, None, None, 2, "block")]
+    for i, (shape, ss, ds, eb, path) in enumerate(cases):
+        if ss is None:
+            ss, ds = perm_layouts(shape, (4, 2, 0, 1, 3))
+        grid = tl.tl_plan(1 << 32, 1 << 44, shape, ss, ds, eb, path=path)["grid"]
+        times = torch.zeros(2 * grid, dtype=torch.int64, device="cuda")
+        check(shape, ss, ds, eb, path, seed=500 + i, cta_times=times.data_ptr())
+        t = times.cpu().numpy().reshape(grid, 2)
+        assert (t[:, 0] > 0).all() and (t[:, 1] >= t[:, 0]).all(), path
+        assert t[:, 1].max() - t[:, 0].min() < 10**9, path       # within a second
+
+
 # ---------------------------------------------------------------------------
 # edge cases
 # ---------------------------------------------------------------------------

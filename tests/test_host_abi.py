@@ -41,7 +41,7 @@ def test_library_loads_and_exports_every_declared_symbol():
     lib = tl.load()
     for n in names:
         assert hasattr(lib, n), n
-    assert tl.tl_version() == 1
+    assert tl.tl_version() == 2
     assert tl.tl_status_string(0) == "ok"
     assert "alias" in tl.tl_status_string(-7) or "overlap" in tl.tl_status_string(-7)
 
@@ -900,3 +900,63 @@ def test_block_path_taken_for_high_rank_short_axes():
     assert plan((9,) * 8, (1, 4, 2, 3, 7, 5, 6, 0), 4) == "block"
     assert plan((8,) * 8, tuple(range(7, -1, -1)), 4) == "panel"
     assert plan((10,) * 8, tuple(range(7, -1, -1)), 4) == "panel"
+
+
+def _random_thread_axis(rng):
+    """A valid thread-axis layout: 32 lanes split over 1-2 axes and P registers over
+    0-2 axes, each side's strides dense in a random order, the axes shuffled."""
+    def split(total, parts):
+        ext = []
+        for _ in range(parts - 1):
+            e = int(rng.choice([d for d in (1, 2, 4, 8) if total % d == 0]))
+            ext.append(e)
+            total //= e
+        return ext + [total]
+    lanes = split(32, int(rng.integers(1, 3)))
+    regs = split(int(rng.choice([1, 2, 4, 8])), int(rng.integers(0, 3))) if rng.random() < 0.9 else []
+    axes = []
+    for side, exts in (("lane", lanes), ("reg", regs)):
+        order = rng.permutation(len(exts))
+        stride = 1
+        strides = [0] * len(exts)
+        for k in order:
+            strides[k] = stride
+            stride *= exts[k]
+        axes += [(side, e, st) for e, st in zip(exts, strides)]
+    axes = [axes[k] for k in rng.permutation(len(axes))][:4]
+    shape = tuple(e for _, e, _ in axes)
+    lane = [st if side == "lane" else 0 for side, _, st in axes]
+    reg = [st if side == "reg" else 0 for side, _, st in axes]
+    return shape, lane, reg
+
+
+def test_thread_axis_check_matches_the_oracle():
+    """tl_thread_axis_check against the oracle's enumeration on the page's example
+    (8 registers), on seeded valid layouts of 1-4 axes, and on each of them broken
+    (a stride doubled, a side swapped)."""
+    assert tl.tl_thread_axis_check((32, 8), (1, 0), (0, 1)) == 8
+    rng = np.random.default_rng(17)
+    valid = 0
+    for _ in range(200):
+        shape, lane, reg = _random_thread_axis(rng)
+        variants = [(lane, reg)]
+        k = int(rng.integers(0, len(shape)))
+        l2, r2 = list(lane), list(reg)
+        if l2[k]:
+            l2[k] *= 2
+        else:
+            r2[k] *= 2
+        variants.append((l2, r2))
+        variants.append((list(reg), list(lane)))
+        for ls, rs in variants:
+            want = L.thread_axis_registers(shape, ls, rs)
+            try:
+                got = tl.tl_thread_axis_check(shape, ls, rs)
+            except tl.TLError as e:
+                assert e.name == "TL_ERR_EXTENT" and want is None, (shape, ls, rs)
+                continue
+            assert got == want, (shape, ls, rs)
+            valid += 1
+    assert valid >= 200
+    with pytest.raises(tl.TLError):
+        tl.tl_thread_axis_check((32, 8), (1, 1), (0, 1))

@@ -501,3 +501,58 @@ def test_sample_with_offset_and_padded_strides_equals_numpy(eb):
         want0 = np.lib.stride_tricks.as_strided(raw.view(dt), shape=shape,
                                                 strides=tuple(s * eb for s in strides))
         assert np.array_equal(vals0, np.stack([_bytes(want0[tuple(c)]) for c in coords]))
+
+
+# ---------------------------------------------------------------------------
+# thread-axis ("1 @ laneid") layouts and the lane's local registers
+# ---------------------------------------------------------------------------
+def test_thread_axis_page_example():
+    """The page's S[(32, 8) : (1 @ laneid, 1)] with R.local(8): 8 registers per lane,
+    element (l, j) in register j of lane l (tests/golden/thread_axis_local.txt)."""
+    rows, kv = read_golden("thread_axis_local.txt")
+    shape = tuple(int(x) for x in kv["shape"].split())
+    ls = tuple(int(x) for x in kv["lane_strides"].split())
+    rs = tuple(int(x) for x in kv["reg_strides"].split())
+    assert L.thread_axis_registers(shape, ls, rs) == int(kv["registers"])
+    places = L.thread_axis_places(shape, ls, rs)
+    for coord, where in rows:
+        c = tuple(int(x) for x in coord.split())
+        assert places[c] == tuple(int(x) for x in where.split())
+    assert all(places[(l, j)] == (l, j) for l in range(32) for j in range(8))
+    # loaded from a row-major (32, 8) buffer: lane l's registers are its row
+    buf = list(range(256))
+    frag = L.thread_axis_fragment(buf, shape, L.row_major_strides(shape), ls, rs)
+    assert frag == [[8 * l + j for j in range(8)] for l in range(32)]
+
+
+def test_thread_axis_fragments_equal_numpy_transposes():
+    """Other thread-axis layouts against numpy (library routine) on iota buffers:
+    the fragment [lane, register] is the tensor with its lane axes moved first."""
+    buf = np.arange(256)
+    # lanes over two axes (8 @ laneid, 1 @ laneid), one register axis
+    frag = L.thread_axis_fragment(list(range(64)), (4, 8, 2), (16, 2, 1),
+                                  (8, 1, 0), (0, 0, 1))
+    assert np.array_equal(np.array(frag), np.arange(64).reshape(4, 8, 2).reshape(32, 2))
+    # the lane axis in the middle, registers from the outer and inner axes (4 * c0 + c2)
+    shape, ls, rs = (2, 32, 4), (0, 1, 0), (4, 0, 1)
+    frag = L.thread_axis_fragment(list(buf), shape, L.row_major_strides(shape), ls, rs)
+    want = buf.reshape(2, 32, 4).transpose(1, 0, 2).reshape(32, 8)
+    assert np.array_equal(np.array(frag), want)
+    # the same registers with their two axes swapped (c0 + 2 * c2)
+    frag = L.thread_axis_fragment(list(buf), shape, L.row_major_strides(shape), ls, (1, 0, 2))
+    want = buf.reshape(2, 32, 4).transpose(1, 2, 0).reshape(32, 8)
+    assert np.array_equal(np.array(frag), want)
+    # a transposed memory layout of the page's example: element (l, j) at j * 32 + l
+    frag = L.thread_axis_fragment(list(buf), (32, 8), (1, 32), (1, 0), (0, 1))
+    assert np.array_equal(np.array(frag), buf.reshape(8, 32).T)
+
+
+def test_thread_axis_layouts_that_are_not_one_warp():
+    """Rejected: an axis on both sides or on neither, lanes that do not cover 0..31
+    once, registers with holes."""
+    assert L.thread_axis_registers((32, 8), (1, 1), (0, 1)) is None     # both sides
+    assert L.thread_axis_registers((32, 8), (1, 0), (0, 0)) is None     # neither
+    assert L.thread_axis_registers((32, 8), (2, 0), (0, 1)) is None     # lanes 0, 2, ..
+    assert L.thread_axis_registers((16, 8), (1, 0), (0, 1)) is None     # 16 lanes
+    assert L.thread_axis_registers((32, 8), (1, 0), (0, 2)) is None     # registers 0, 2, ..
+    assert L.thread_axis_registers((8, 4, 2), (4, 1, 0), (0, 0, 1)) == 2

@@ -12,6 +12,8 @@ Contents
   ``c`` (TVM docs, "Buffers and memory", section "Declaring buffers").
 * ``sample`` -- the same definition evaluated at chosen coordinates one by one,
   for outputs too large to permute whole on the host.
+* ``permute_cast`` -- the same definition with every element converted on the way
+  (``cast_ref``: IEEE 754 binary32 <-> binary16 / bfloat16).
 * ``layout_ref`` -- pure-Python references for the host logic: slicing and
   canonicalising a pair of layouts, the shared-memory bank model and the XOR
   swizzle chooser of the warp permute (TVM docs, "permute_layout", section
@@ -30,6 +32,7 @@ import threading
 
 import numpy as np
 
+from . import cast_ref  # noqa: F401  (re-exported)
 from . import layout_ref  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -149,3 +152,25 @@ def sample(src: np.ndarray, coords: np.ndarray, src_strides, dst_strides, elem_b
     if byte_idx.size and (byte_idx.min() < 0 or byte_idx.max() >= src.nbytes):
         raise IndexError("sampled coordinate outside the source buffer")
     return dst_off, src.reshape(-1).view(np.uint8)[byte_idx]
+
+
+def permute_cast(src: np.ndarray, dst: np.ndarray, shape, src_strides, dst_strides, cast: str,
+                 src_offset: int = 0, dst_offset: int = 0) -> None:
+    """dst[sum c*dst_strides + dst_offset] = convert(src[sum c*src_strides + src_offset])
+    for every coordinate c, with ``convert`` one of ``cast_ref.CASTS`` (strides and
+    offsets in elements of each side's own type).  Small inputs: the coordinates
+    are enumerated."""
+    src_eb, dst_eb = cast_ref.CASTS[cast]
+    shape = [int(x) for x in shape]
+    if any(e == 0 for e in shape):
+        return
+    coords = np.indices(shape).reshape(len(shape), -1).T.astype(np.int64)
+    so = src_offset + coords @ np.asarray(src_strides, dtype=np.int64)
+    do = dst_offset + coords @ np.asarray(dst_strides, dtype=np.int64)
+    sb = so[:, None] * src_eb + np.arange(src_eb)[None, :]
+    db = do[:, None] * dst_eb + np.arange(dst_eb)[None, :]
+    if sb.min() < 0 or sb.max() >= src.nbytes or db.min() < 0 or db.max() >= dst.nbytes:
+        raise IndexError("layout reaches outside its buffer")
+    vals = src.reshape(-1).view(np.uint8)[sb]
+    out = cast_ref.convert_bytes(vals, cast).reshape(-1, dst_eb)
+    dst.reshape(-1).view(np.uint8)[db] = out

@@ -556,3 +556,104 @@ def test_thread_axis_layouts_that_are_not_one_warp():
     assert L.thread_axis_registers((16, 8), (1, 0), (0, 1)) is None     # 16 lanes
     assert L.thread_axis_registers((32, 8), (1, 0), (0, 2)) is None     # registers 0, 2, ..
     assert L.thread_axis_registers((8, 4, 2), (4, 1, 0), (0, 0, 1)) == 2
+
+
+# ---------------------------------------------------------------------------
+# element conversions of the fused permute + cast (IEEE 754)
+# ---------------------------------------------------------------------------
+from oracle import cast_ref as C  # noqa: E402
+
+
+def _f32(vals):
+    return np.asarray(vals, dtype=np.float32).view(np.uint32)
+
+
+def test_f32_to_f16_equals_numpy_on_every_class_of_value():
+    """binary32 -> binary16, ties to even, against numpy's astype (library routine):
+    random bit patterns, exact ties, the subnormal and overflow boundaries, signed
+    zeros, infinities and NaN payloads."""
+    rng = np.random.default_rng(61)
+    bits = [rng.integers(0, 2**32, size=200000, dtype=np.uint64).astype(np.uint32)]
+    # ties: halfway between two binary16 neighbours (a 1 just past the kept bits)
+    h = rng.integers(0, 0x7BFF, size=5000, dtype=np.uint64).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float32).view(np.uint32)
+    hi = (h + 1).view(np.float16).astype(np.float32)
+    mid = ((lo.view(np.float32).astype(np.float64) + hi.astype(np.float64)) / 2).astype(np.float32)
+    bits.append(mid.view(np.uint32))
+    special = [0.0, -0.0, 65504.0, 65519.0, 65520.0, 65536.0, 2.0**-24, 2.0**-25, 3 * 2.0**-26,
+               2.0**-14, 2.0**-14 - 2.0**-25, np.inf, -np.inf, 1e-40]
+    bits.append(_f32(special))
+    bits.append(np.array([0x7FC00000, 0x7F800001, 0xFFC00001, 0x7F802000, 0x7FFFFFFF,
+                          0xFF800001], dtype=np.uint32))
+    u = np.concatenate(bits)
+    want = u.view(np.float32).astype(np.float16).view(np.uint16)
+    assert np.array_equal(C.f32_to_f16_bits(u), want)
+
+
+def test_f16_to_f32_equals_numpy_for_all_65536_patterns():
+    u = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    assert np.array_equal(C.f16_to_f32_bits(u), u.view(np.float16).astype(np.float32).view(np.uint32))
+
+
+def test_f32_to_bf16_is_the_nearest_bf16_with_ties_to_even():
+    """binary32 -> bfloat16 by brute force: the result's neighbours on the bfloat16
+    grid are never nearer, a tie takes the even one, overflow gives infinity, and
+    NaNs stay NaNs of the same sign with their upper payload bits."""
+    rng = np.random.default_rng(62)
+    u = rng.integers(0, 2**32, size=100000, dtype=np.uint64).astype(np.uint32)
+    ties = ((rng.integers(0, 0x7F7F, size=2000, dtype=np.uint64).astype(np.uint32) << 16)
+            | np.uint32(0x8000))                       # exactly halfway
+    u = np.concatenate([u, ties, _f32([0.0, -0.0, 1.0, np.inf, -np.inf, 3.3895313892515355e38,
+                                      3.4e38, 1e-45])])
+    got = C.f32_to_bf16_bits(u)
+    x = u.view(np.float32).astype(np.float64)
+    fin = np.isfinite(x)
+    as_f = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    v = as_f(got)
+    for d in (-1, 1):                                  # the two grid neighbours of v
+        nb = got.astype(np.int64) + d
+        ok = (nb >= 0) & (nb < 0x10000)
+        ok &= ((nb & 0x7F80) != 0x7F80)                # neighbours that are finite
+        w = as_f(np.where(ok, nb, 0).astype(np.uint16))
+        closer = np.abs(w - x) < np.abs(v - x)
+        tie = np.abs(w - x) == np.abs(v - x)
+        bad = fin & ok & np.isfinite(v) & (closer | (tie & ((got & 1) == 1)))
+        assert not bad.any(), u[bad][:4]
+    # overflow and exact values
+    assert C.f32_to_bf16_bits(_f32([3.4e38]))[0] == 0x7F80
+    assert C.f32_to_bf16_bits(_f32([1.0]))[0] == 0x3F80
+    assert C.f32_to_bf16_bits(_f32([-0.0]))[0] == 0x8000
+    assert C.f32_to_bf16_bits(np.array([0x3F808000], dtype=np.uint32))[0] == 0x3F80   # tie -> even
+    assert C.f32_to_bf16_bits(np.array([0x3F818000], dtype=np.uint32))[0] == 0x3F82   # tie -> even
+    nan = np.array([0x7FC00000, 0x7F800001, 0xFF812345], dtype=np.uint32)
+    assert C.f32_to_bf16_bits(nan).tolist() == [0x7FC0, 0x7F81, 0xFF81]
+
+
+def test_bf16_round_trips_through_f32():
+    """bfloat16 -> binary32 is exact: back to bfloat16 gives every pattern again
+    (NaN payloads included)."""
+    u = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    assert np.array_equal(C.f32_to_bf16_bits(C.bf16_to_f32_bits(u)), u)
+    f = C.bf16_to_f32_bits(u).view(np.float32)
+    fin = (u & 0x7F80) != 0x7F80
+    assert np.array_equal(f[fin].view(np.uint32) >> 16, u[fin])
+
+
+def test_permute_cast_equals_numpy_transpose_and_astype():
+    """The fused permute + cast against numpy: a transpose, then astype (binary16) or
+    the bfloat16 view of the rounded values."""
+    rng = np.random.default_rng(63)
+    shape, perm = (5, 7, 9), (2, 0, 1)
+    ss, ds = _perm_layouts(shape, perm)
+    x = rng.standard_normal(int(np.prod(shape))).astype(np.float32)
+    dst = np.zeros(int(np.prod(shape)) * 2, dtype=np.uint8)
+    oracle.permute_cast(x.view(np.uint8), dst, shape, ss, ds, "f32_to_f16")
+    want = np.transpose(x.reshape(shape), perm).astype(np.float16)
+    assert np.array_equal(dst.view(np.float16), want.reshape(-1))
+    h = want.reshape(-1).view(np.uint16)
+    back = np.zeros(int(np.prod(shape)) * 4, dtype=np.uint8)
+    ss2, ds2 = _perm_layouts(tuple(shape[p] for p in perm), (1, 2, 0))
+    oracle.permute_cast(h.view(np.uint8), back, tuple(shape[p] for p in perm), ss2, ds2,
+                        "f16_to_f32")
+    assert np.array_equal(back.view(np.float32),
+                          x.reshape(shape).astype(np.float16).astype(np.float32).reshape(-1))

@@ -201,6 +201,17 @@ TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape
  * 16-byte runs (tuning and comparison; the result is the same). */
 #define TL_FLAG_PANEL_ELEMENT_STORES (1u << 12)
 
+/* Fused permute + cast (tl_permute_opts.cast): a widening of the equal-dtype rule of
+ * "permute_layout" ("What it accepts"), each element converted as IEEE 754 does,
+ * rounding to nearest with ties to even; a NaN keeps its sign and upper payload bits
+ * when narrowed (the lowest payload bit set if those are all zero) and its payload
+ * when widened. */
+#define TL_CAST_NONE 0
+#define TL_CAST_F32_TO_BF16 1   /* float32 -> bfloat16 */
+#define TL_CAST_F32_TO_F16 2    /* float32 -> float16 */
+#define TL_CAST_BF16_TO_F32 3   /* bfloat16 -> float32 (exact) */
+#define TL_CAST_F16_TO_F32 4    /* float16 -> float32 (exact) */
+
 /* Options of tl_permute_ex.  Zero-initialise, then set what you need. */
 typedef struct tl_permute_opts {
     uint32_t flags;       /* TL_PATH_* | TL_FLAG_* */
@@ -228,7 +239,10 @@ typedef struct tl_permute_opts {
     int32_t panel_tile_kib;       /* panel path: tile size, 4..48 KiB (default 32, or 24
                                      with an extent of 16 or less); block path: its
                                      tile's bytes */
-    int32_t reserved;
+    int32_t cast;         /* TL_CAST_*: convert every element on the way (elem_bytes
+                             and src_strides are the source type's, dst_strides the
+                             destination type's); the tile, chunk and generic paths
+                             take casts, a forced other path returns TL_ERR_PATH */
     uint64_t *cta_times;  /* nullable DEVICE array (measurement): the tile, rows, panel
                              and block kernels write each CTA's start and finish time
                              (%globaltimer, ns) to cta_times[2 * b] and [2 * b + 1] for

@@ -20,7 +20,7 @@ import os
 import threading
 
 __all__ = [
-    "TLError", "TL_MAX_DIMS", "PATHS", "PATH_NAMES", "TL_FLAG_TEST_DROP_HANDOFF", "TL_FLAG_NO_PDL",
+    "TLError", "TL_MAX_DIMS", "PATHS", "PATH_NAMES", "CASTS", "TL_FLAG_TEST_DROP_HANDOFF", "TL_FLAG_NO_PDL",
     "TL_FLAG_DEBUG_CHECKS", "TL_FLAG_TEST_SKIP_HOST_BOUNDS", "TL_FLAG_PANEL_ELEMENT_STORES",
     "load", "library_path", "tl_layout_canon", "tl_choose_xor_k", "tl_bank_conflicts",
     "tl_permute", "tl_permute_ex", "tl_plan", "tl_status_string", "tl_launch_count",
@@ -32,6 +32,8 @@ TL_MAX_DIMS = 8
 PATHS = {"auto": 0, "generic": 1, "chunk": 2, "tile": 3, "warp": 4, "rows": 5, "cluster": 6,
          "panel": 7, "cols": 8, "block": 9}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
+# fused permute + cast (tl_permute_opts.cast): name -> TL_CAST_*
+CASTS = {"none": 0, "f32_to_bf16": 1, "f32_to_f16": 2, "bf16_to_f32": 3, "f16_to_f32": 4}
 TL_FLAG_TEST_DROP_HANDOFF = 1 << 8
 TL_FLAG_NO_PDL = 1 << 9
 TL_FLAG_DEBUG_CHECKS = 1 << 10
@@ -71,7 +73,7 @@ class TlPermuteOpts(ctypes.Structure):
                 ("tile_stages", _i32), ("tile_ctas_per_sm", _i32), ("tile_l2_promotion", _i32),
                 ("tile_rows", _i32), ("cluster_recv_stages", _i32),
                 ("cluster_consumer_warps", _i32), ("panel_tile_kib", _i32),
-                ("reserved", _i32), ("cta_times", ctypes.c_void_p)]
+                ("cast", _i32), ("cta_times", ctypes.c_void_p)]
 
 
 class TlPlanInfo(ctypes.Structure):
@@ -239,9 +241,11 @@ def tl_bank_conflicts(lane_offsets, elem_bytes, model="conservative") -> int:
 
 def _opts(flags=0, path="auto", dev_status=0, src_bytes=0, dst_bytes=0, max_ctas=0,
           tile_group=0, tile_stages=0, tile_ctas_per_sm=0, tile_l2_promotion=0, tile_rows=0,
-          cluster_recv_stages=0, cluster_consumer_warps=0, panel_tile_kib=0, cta_times=0):
+          cluster_recv_stages=0, cluster_consumer_warps=0, panel_tile_kib=0, cta_times=0,
+          cast="none"):
     o = TlPermuteOpts()
     o.cta_times = int(cta_times) or None
+    o.cast = CASTS[cast] if isinstance(cast, str) else int(cast)
     o.panel_tile_kib = int(panel_tile_kib)
     o.cluster_consumer_warps = int(cluster_consumer_warps)
     o.tile_rows = int(tile_rows)

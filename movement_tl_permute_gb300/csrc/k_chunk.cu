@@ -62,12 +62,42 @@ __device__ __forceinline__ void row_offsets(int64_t r, const ChunkArgs& a, int64
     }
 }
 
-template <int VB>
+// Destination vector bytes for a source vector of VB bytes.
+template <int CAST, int VB> struct DstVec {
+    static constexpr int kBytes = VB / dev::Cast<CAST>::kSrc * dev::Cast<CAST>::kDst;
+};
+template <int VB> struct DstVec<TL_CAST_NONE, VB> { static constexpr int kBytes = VB; };
+
+// The converted vector of a cast: the VB / ES source elements of v, each converted
+// (ES, ED: source and destination element bytes).
+template <int CAST, int VB>
+__device__ __forceinline__ auto convert_vec(const typename Vec<VB>::T& v) {
+    using C = dev::Cast<CAST>;
+    constexpr int N = VB / C::kSrc, DVB = N * C::kDst;
+    uint32_t in[(VB + 3) / 4] = {};
+    __builtin_memcpy(in, &v, VB);
+    uint32_t out[(DVB + 3) / 4] = {};
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+        const uint32_t x = C::kSrc == 4 ? in[k] : (in[k / 2] >> (16 * (k & 1))) & 0xFFFFu;
+        const uint32_t y = C::cvt(x);
+        if constexpr (C::kDst == 4) out[k] = y;
+        else out[k / 2] |= y << (16 * (k & 1));
+    }
+    typename Vec<DVB>::T r;
+    __builtin_memcpy(&r, out, DVB);
+    return r;
+}
+
+// CAST (TL_CAST_*): each element converted on the way; VB is the source vector, the
+// destination vector holds as many elements (row offsets are bytes of each side).
+template <int VB, int CAST = TL_CAST_NONE>
 __global__ void __launch_bounds__(256) k_chunk(const ChunkArgs a) {
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
     constexpr int U = 4;        // consecutive rows per group and round
     using T = typename Vec<VB>::T;
+    constexpr int DVB = DstVec<CAST, VB>::kBytes;
     const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t G = 1LL << a.log2g;
     const int64_t gid = gtid >> a.log2g;
@@ -110,8 +140,13 @@ __global__ void __launch_bounds__(256) k_chunk(const ChunkArgs a) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (!ok[u]) continue;
-                st<VB>(a.dst + d[u] + c0 * VB, v0[u]);
-                if (two) st<VB>(a.dst + d[u] + (c0 + G) * VB, v1[u]);
+                if constexpr (CAST == TL_CAST_NONE) {
+                    st<VB>(a.dst + d[u] + c0 * VB, v0[u]);
+                    if (two) st<VB>(a.dst + d[u] + (c0 + G) * VB, v1[u]);
+                } else {
+                    st<DVB>(a.dst + d[u] + c0 * DVB, convert_vec<CAST, VB>(v0[u]));
+                    if (two) st<DVB>(a.dst + d[u] + (c0 + G) * DVB, convert_vec<CAST, VB>(v1[u]));
+                }
             }
         }
     }
@@ -122,6 +157,20 @@ __global__ void __launch_bounds__(256) k_chunk(const ChunkArgs a) {
 template <int VB>
 cudaError_t launch_chunk(const ChunkArgs& a, int grid, int block, cudaStream_t st, bool pdl) {
     return launch_kernel(k_chunk<VB>, dim3(grid), dim3(block), 0, st, pdl, a);
+}
+
+// the cast kernels: source vectors of 4, 2 or 1 elements
+cudaError_t launch_chunk_cast(int cast, int vb, const ChunkArgs& a, int grid, int block,
+                              cudaStream_t st, bool pdl) {
+#define TL_CC(C, V)                                                                        \
+    if (cast == C && vb == V)                                                              \
+        return launch_kernel(k_chunk<V, C>, dim3(grid), dim3(block), 0, st, pdl, a);
+    TL_CC(TL_CAST_F32_TO_BF16, 16) TL_CC(TL_CAST_F32_TO_BF16, 8) TL_CC(TL_CAST_F32_TO_BF16, 4)
+    TL_CC(TL_CAST_F32_TO_F16, 16) TL_CC(TL_CAST_F32_TO_F16, 8) TL_CC(TL_CAST_F32_TO_F16, 4)
+    TL_CC(TL_CAST_BF16_TO_F32, 8) TL_CC(TL_CAST_BF16_TO_F32, 4) TL_CC(TL_CAST_BF16_TO_F32, 2)
+    TL_CC(TL_CAST_F16_TO_F32, 8) TL_CC(TL_CAST_F16_TO_F32, 4) TL_CC(TL_CAST_F16_TO_F32, 2)
+#undef TL_CC
+    return cudaErrorInvalidValue;
 }
 
 template cudaError_t launch_chunk<1>(const ChunkArgs&, int, int, cudaStream_t, bool);

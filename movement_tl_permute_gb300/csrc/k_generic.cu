@@ -14,7 +14,9 @@ namespace {
 
 // CK: the checked run -- each element's byte ranges are compared with the buffer
 // sizes first; an element outside is skipped and TL_ERR_BOUNDS recorded.
-template <int EB, int VM, bool CK>
+// CAST (TL_CAST_*): each element converted on the way (EB is the source's width;
+// dst offsets count destination elements).
+template <int EB, int VM, bool CK, int CAST = TL_CAST_NONE>
 __global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
@@ -53,7 +55,14 @@ __global__ void __launch_bounds__(256) k_generic(const GenericArgs a) {
                 continue;
             }
         }
-        if constexpr (VM == 0) {
+        if constexpr (CAST != TL_CAST_NONE) {
+            using C = dev::Cast<CAST>;
+            const uint32_t x = C::kSrc == 4 ? *reinterpret_cast<const uint32_t*>(a.src + so * 4)
+                                            : *reinterpret_cast<const uint16_t*>(a.src + so * 2);
+            const uint32_t y = C::cvt(x);
+            if constexpr (C::kDst == 4) *reinterpret_cast<uint32_t*>(a.dst + d * 4) = y;
+            else *reinterpret_cast<uint16_t*>(a.dst + d * 2) = (uint16_t)y;
+        } else if constexpr (VM == 0) {
             dev::copy_elem<EB>(a.dst + d * EB, a.src + so * EB);
         } else {
             using T = typename dev::Bits<EB>::T;
@@ -82,6 +91,25 @@ cudaError_t launch_generic(const GenericArgs& a, int grid, int block, cudaStream
             return launch_kernel(k_generic<EB, 1, false>, dim3(grid), dim3(block), 0, st, pdl, a);
     }
     return launch_kernel(k_generic<EB, 0, false>, dim3(grid), dim3(block), 0, st, pdl, a);
+}
+
+cudaError_t launch_generic_cast(int cast, const GenericArgs& a, int grid, int block,
+                               cudaStream_t st, bool pdl) {
+    switch (cast) {
+    case TL_CAST_F32_TO_BF16:
+        return launch_kernel(k_generic<4, 0, false, TL_CAST_F32_TO_BF16>, dim3(grid), dim3(block),
+                             0, st, pdl, a);
+    case TL_CAST_F32_TO_F16:
+        return launch_kernel(k_generic<4, 0, false, TL_CAST_F32_TO_F16>, dim3(grid), dim3(block),
+                             0, st, pdl, a);
+    case TL_CAST_BF16_TO_F32:
+        return launch_kernel(k_generic<2, 0, false, TL_CAST_BF16_TO_F32>, dim3(grid), dim3(block),
+                             0, st, pdl, a);
+    case TL_CAST_F16_TO_F32:
+        return launch_kernel(k_generic<2, 0, false, TL_CAST_F16_TO_F32>, dim3(grid), dim3(block),
+                             0, st, pdl, a);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template cudaError_t launch_generic<1>(const GenericArgs&, int, int, cudaStream_t, bool);

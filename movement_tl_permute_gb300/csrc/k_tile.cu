@@ -29,9 +29,13 @@ using namespace tile;
 
 // TB = tile height in rows of b (128 or 256); the consumers take a tile in 128-row
 // blocks.  Taller tiles halve the TMA requests and barrier round trips per byte.
-template <int EB, int TB>
+// CAST (TL_CAST_*): each element converted before its store (EB 4 -> 2 bytes, or
+// 2 -> 4); DEB is the destination's element width.
+template <int EB, int TB, int CAST = TL_CAST_NONE>
 __global__ void __launch_bounds__(kTileThreads)
 k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
+    constexpr int DEB = CAST == TL_CAST_NONE ? EB
+                        : (CAST == TL_CAST_F32_TO_BF16 || CAST == TL_CAST_F32_TO_F16) ? 2 : 4;
     constexpr uint32_t kBytes = (uint32_t)TB * kRowBytes;   // one stage
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full[kMaxTileStages];
@@ -70,7 +74,7 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
                 }
                 const TileCoord tc = tile_coord(t, a);
                 // one 16-byte store, published by the release below
-                sts128(smem_addr(&info[s]), pack_out<EB, TB>(tc, a));
+                sts128(smem_addr(&info[s]), pack_out<EB, TB, DEB>(tc, a));
                 mbar_arrive_expect_tx(&full[s], kBytes);
                 tma_load(smem + s * kBytes, &tmap, &full[s], a.rank,
                          (int)(tc.ta * kRowBytes), (int)(tc.tb * TB), (int)tc.bc[0],
@@ -95,11 +99,15 @@ k_tile(const __grid_constant__ CUtensorMap tmap, const TileArgs a) {
             if (lane == 0) report(a.status, TL_ERR_TIMEOUT);
             break;
         }
-        const TileOut o = unpack_out<EB>(lds128(smem_addr(&info[s])), a);
+        const TileOut o = unpack_out<DEB>(lds128(smem_addr(&info[s])), a);
         const uint32_t base = smem_addr(smem + s * kBytes);
 #pragma unroll
-        for (int rb0 = 0; rb0 < TB; rb0 += kRows)
-            if (rb0 == 0 || rb0 < o.rows) consume<EB>(base, o, warp, lane, rb0);
+        for (int rb0 = 0; rb0 < TB; rb0 += kRows) {
+            if (rb0 != 0 && rb0 >= o.rows) continue;
+            if constexpr (CAST == TL_CAST_NONE) consume<EB>(base, o, warp, lane, rb0);
+            else if constexpr (DEB == 2) consume_narrow<CAST>(base, o, warp, lane, rb0);
+            else consume_widen<CAST>(base, o, warp, lane, rb0);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -120,6 +128,36 @@ cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cud
                         bool pdl) {
     return launch_kernel(k_tile<EB, TB>, dim3(grid), dim3(kTileThreads),
                          tile_smem_bytes(a.stages, TB), st, pdl, map, a);
+}
+
+// the converting tile kernels (128-row tiles)
+cudaError_t launch_tile_cast(int cast, const CUtensorMap& map, const TileArgs& a, int grid,
+                             cudaStream_t st, bool pdl) {
+    switch (cast) {
+    case TL_CAST_F32_TO_BF16:
+        return launch_kernel(k_tile<4, 128, TL_CAST_F32_TO_BF16>, dim3(grid), dim3(kTileThreads),
+                             tile_smem_bytes(a.stages, 128), st, pdl, map, a);
+    case TL_CAST_F32_TO_F16:
+        return launch_kernel(k_tile<4, 128, TL_CAST_F32_TO_F16>, dim3(grid), dim3(kTileThreads),
+                             tile_smem_bytes(a.stages, 128), st, pdl, map, a);
+    case TL_CAST_BF16_TO_F32:
+        return launch_kernel(k_tile<2, 128, TL_CAST_BF16_TO_F32>, dim3(grid), dim3(kTileThreads),
+                             tile_smem_bytes(a.stages, 128), st, pdl, map, a);
+    case TL_CAST_F16_TO_F32:
+        return launch_kernel(k_tile<2, 128, TL_CAST_F16_TO_F32>, dim3(grid), dim3(kTileThreads),
+                             tile_smem_bytes(a.stages, 128), st, pdl, map, a);
+    }
+    return cudaErrorInvalidValue;
+}
+
+const void* tile_cast_kernel(int cast) {
+    switch (cast) {
+    case TL_CAST_F32_TO_BF16: return reinterpret_cast<const void*>(&k_tile<4, 128, TL_CAST_F32_TO_BF16>);
+    case TL_CAST_F32_TO_F16: return reinterpret_cast<const void*>(&k_tile<4, 128, TL_CAST_F32_TO_F16>);
+    case TL_CAST_BF16_TO_F32: return reinterpret_cast<const void*>(&k_tile<2, 128, TL_CAST_BF16_TO_F32>);
+    case TL_CAST_F16_TO_F32: return reinterpret_cast<const void*>(&k_tile<2, 128, TL_CAST_F16_TO_F32>);
+    }
+    return nullptr;
 }
 
 #define TL_INST(EB, TB)                                                                     \

@@ -216,6 +216,92 @@ __device__ __forceinline__ void consume<1>(uint32_t tile, const TileOut& o, int 
         put<1>(o, 4 * word + cc, row0, make_uint4(w[cc][0], w[cc][1], w[cc][2], w[cc][3]));
 }
 
+// ---------------------------------------------------------------------------
+// Fused permute + cast: the same column reads, each element converted before the
+// store.  N converted elements of DEB bytes go to tile column `col` from row `row`
+// (words: the N elements packed little-endian).
+template <int DEB, int N>
+__device__ __forceinline__ void put_cast(const TileOut& o, int col, int row,
+                                         const uint32_t (&w)[N * DEB / 4]) {
+    uint8_t* p = o.base + (int64_t)col * o.cstride + row * DEB;
+    if (o.full || (col < o.cols && o.vec && row + N <= o.rows)) {
+        if constexpr (N * DEB == 8) {
+            *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+        } else {
+            stg128(p, make_uint4(w[0], w[1], w[2], w[3]));
+            stg128(p + 16, make_uint4(w[4], w[5], w[6], w[7]));
+        }
+        return;
+    }
+    if (col >= o.cols) return;
+#pragma unroll
+    for (int e = 0; e < N; ++e) {
+        if (row + e >= o.rows) break;
+        if constexpr (DEB == 2)
+            *reinterpret_cast<uint16_t*>(p + 2 * e) = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+        else
+            *reinterpret_cast<uint32_t*>(p + 4 * e) = w[e];
+    }
+}
+
+// Column reads of consume<4> (four rows of one fp32 column per lane), converted to
+// four 16-bit elements: 8 bytes per lane and column.
+template <int CAST>
+__device__ __forceinline__ void consume_narrow(uint32_t tile, const TileOut& o, int warp,
+                                               int lane, int rb0) {
+    const int cw = lane & 3, g = lane >> 2, x = (lane >> 3) & 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int u = warp + kConsumerWarps * i;
+        const int cb = u & 7, rb = u >> 3;
+        const int col = 4 * cb + cw;
+        const int row0 = rb0 + rb * 32 + 4 * g;
+        uint32_t r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) r[k] = lds32(tile + swz(row0 + (k ^ x), 4 * col));
+        cswap(x & 1, r[0], r[1]);
+        cswap(x & 1, r[2], r[3]);
+        cswap(x & 2, r[0], r[2]);
+        cswap(x & 2, r[1], r[3]);
+        const uint32_t w[2] = {Cast<CAST>::cvt(r[0]) | (Cast<CAST>::cvt(r[1]) << 16),
+                               Cast<CAST>::cvt(r[2]) | (Cast<CAST>::cvt(r[3]) << 16)};
+        put_cast<2, 4>(o, col, row0, w);
+    }
+}
+
+// Column reads of consume<2> (eight rows of two 16-bit columns per lane), converted
+// to fp32: 32 bytes per lane and column.
+template <int CAST>
+__device__ __forceinline__ void consume_widen(uint32_t tile, const TileOut& o, int warp,
+                                              int lane, int rb0) {
+    const int cw = lane & 3, g = lane >> 2, x = g;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int u = warp + kConsumerWarps * i;
+        const int cb = u & 7, rb = u >> 3;
+        const int word = 4 * cb + cw;
+        const int row0 = rb0 + rb * 64 + 8 * g;
+        uint32_t r[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) r[k] = lds32(tile + swz(row0 + (k ^ x), 4 * word));
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) cswap(x & 1, r[k], r[k + 1]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (!(k & 2)) cswap(x & 2, r[k], r[k + 2]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cswap(x & 4, r[k], r[k + 4]);
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            lo[k] = Cast<CAST>::cvt(r[k] & 0xFFFFu);
+            hi[k] = Cast<CAST>::cvt(r[k] >> 16);
+        }
+        put_cast<4, 8>(o, 2 * word, row0, lo);
+        put_cast<4, 8>(o, 2 * word + 1, row0, hi);
+    }
+}
+
 // Tile t -> (ta, tb, batch coordinates).  Within a batch item tiles are visited in
 // groups of `group_b` tile rows, b fastest inside a group, so concurrently
 // running CTAs write runs of many 128-byte lines (one group spanning all of b
@@ -269,8 +355,9 @@ __device__ __forceinline__ TileCoord tile_coord(int64_t t, const TileArgs& a) {
     return r;
 }
 
-// Destination record of the tile at coordinates tc (tiles of TB rows).
-template <int EB, int TB = kRows>
+// Destination record of the tile at coordinates tc (tiles of TB rows; DEB: the
+// destination element bytes, EB's unless the permute converts).
+template <int EB, int TB = kRows, int DEB = EB>
 __device__ __forceinline__ TileOut make_out(const TileCoord& tc, const TileArgs& a) {
     constexpr int TA = kRowBytes / EB;
     const int64_t a0 = tc.ta * TA, b0 = tc.tb * TB;
@@ -278,8 +365,8 @@ __device__ __forceinline__ TileOut make_out(const TileCoord& tc, const TileArgs&
 #pragma unroll
     for (int i = 0; i < 3; ++i) base += tc.bc[i] * a.bds[i];
     TileOut o;
-    o.base = a.dst + base * EB;
-    o.cstride = a.ds_a * EB;
+    o.base = a.dst + base * DEB;
+    o.cstride = a.ds_a * DEB;
     o.cols = (int32_t)min((int64_t)TA, a.ext_a - a0);
     o.rows = (int32_t)min((int64_t)TB, a.ext_b - b0);
     o.vec = a.vec_store;
@@ -291,19 +378,19 @@ __device__ __forceinline__ TileOut make_out(const TileCoord& tc, const TileArgs&
 // 16-byte store, each consumer warp reads it with one 16-byte load): the dst
 // address, then valid columns (bits 0-8), valid rows (9-17) and "full" (bit 18).
 // The column stride and the run alignment are the same for every tile.
-template <int EB, int TB = kRows>
+template <int EB, int TB = kRows, int DEB = EB>
 __device__ __forceinline__ uint4 pack_out(const TileCoord& tc, const TileArgs& a) {
-    const TileOut o = make_out<EB, TB>(tc, a);
+    const TileOut o = make_out<EB, TB, DEB>(tc, a);
     const uint64_t p = reinterpret_cast<uint64_t>(o.base);
     return make_uint4((uint32_t)p, (uint32_t)(p >> 32),
                       (uint32_t)o.cols | ((uint32_t)o.rows << 9) | ((uint32_t)o.full << 18), 0u);
 }
 
-template <int EB>
+template <int DEB>
 __device__ __forceinline__ TileOut unpack_out(const uint4 v, const TileArgs& a) {
     TileOut o;
     o.base = reinterpret_cast<uint8_t*>((uint64_t)v.x | ((uint64_t)v.y << 32));
-    o.cstride = a.ds_a * EB;
+    o.cstride = a.ds_a * DEB;
     o.cols = (int32_t)(v.z & 511u);
     o.rows = (int32_t)((v.z >> 9) & 511u);
     o.full = (int32_t)((v.z >> 18) & 1u);

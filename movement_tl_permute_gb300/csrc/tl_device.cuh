@@ -4,7 +4,10 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cstdint>
+
+#include "../../include/tl_permute.h"
 
 namespace tl {
 namespace dev {
@@ -24,6 +27,59 @@ __device__ __forceinline__ void copy_elem(uint8_t* d, const uint8_t* s) {
     using T = typename Bits<EB>::T;
     *reinterpret_cast<T*>(d) = *reinterpret_cast<const T*>(s);
 }
+
+// ---------------------------------------------------------------------------
+// Element conversions of the fused permute + cast (IEEE 754, ties to even).  NaNs
+// keep their sign and upper payload bits (the lowest payload bit set if those are
+// all zero) when narrowed, and their payload when widened.
+// ---------------------------------------------------------------------------
+// binary32 -> bfloat16: the upper half rounded to nearest even by adding 0x7FFF
+// plus the kept half's lowest bit before truncating (finite and infinite values;
+// a carry out of the largest finite value gives infinity, as it should).
+__device__ __forceinline__ uint32_t f32_to_bf16(uint32_t b) {
+    if ((b & 0x7FFFFFFFu) > 0x7F800000u) {
+        const uint32_t pay = (b >> 16) & 0x7Fu;
+        return ((b >> 16) & 0x8000u) | 0x7F80u | (pay ? pay : 1u);
+    }
+    return (b + 0x7FFFu + ((b >> 16) & 1u)) >> 16;
+}
+// binary32 -> binary16 (CUDA's round-to-nearest-even conversion for numbers)
+__device__ __forceinline__ uint32_t f32_to_f16(uint32_t b) {
+    if ((b & 0x7FFFFFFFu) > 0x7F800000u) {
+        const uint32_t pay = (b & 0x7FFFFFu) >> 13;
+        return ((b >> 16) & 0x8000u) | 0x7C00u | (pay ? pay : 1u);
+    }
+    return __half_as_ushort(__float2half_rn(__uint_as_float(b)));
+}
+// bfloat16 -> binary32: exact
+__device__ __forceinline__ uint32_t bf16_to_f32(uint32_t h) { return (h & 0xFFFFu) << 16; }
+// binary16 -> binary32: exact (CUDA's conversion for numbers)
+__device__ __forceinline__ uint32_t f16_to_f32(uint32_t h) {
+    h &= 0xFFFFu;
+    if ((h & 0x7C00u) == 0x7C00u && (h & 0x3FFu))
+        return ((h & 0x8000u) << 16) | 0x7F800000u | ((h & 0x3FFu) << 13);
+    return __float_as_uint(__half2float(__ushort_as_half((unsigned short)h)));
+}
+
+// Cast c: source / destination element bytes and the conversion of one element.
+template <int CAST> struct Cast;
+template <> struct Cast<TL_CAST_NONE> {};
+template <> struct Cast<TL_CAST_F32_TO_BF16> {
+    static constexpr int kSrc = 4, kDst = 2;
+    __device__ static uint32_t cvt(uint32_t x) { return f32_to_bf16(x); }
+};
+template <> struct Cast<TL_CAST_F32_TO_F16> {
+    static constexpr int kSrc = 4, kDst = 2;
+    __device__ static uint32_t cvt(uint32_t x) { return f32_to_f16(x); }
+};
+template <> struct Cast<TL_CAST_BF16_TO_F32> {
+    static constexpr int kSrc = 2, kDst = 4;
+    __device__ static uint32_t cvt(uint32_t x) { return bf16_to_f32(x); }
+};
+template <> struct Cast<TL_CAST_F16_TO_F32> {
+    static constexpr int kSrc = 2, kDst = 4;
+    __device__ static uint32_t cvt(uint32_t x) { return f16_to_f32(x); }
+};
 
 // ---------------------------------------------------------------------------
 // Division of unsigned 32-bit numerators by a divisor fixed at launch time

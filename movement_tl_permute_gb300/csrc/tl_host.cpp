@@ -1084,15 +1084,26 @@ int64_t plan_block(Plan* p, int64_t tile_bytes) {
 
 int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
               const int64_t* src_strides, const int64_t* dst_strides, int eb, uint32_t flags,
-              int64_t src_bytes, int64_t dst_bytes, Plan* plan) {
+              int64_t src_bytes, int64_t dst_bytes, Plan* plan, int cast) {
     Plan p;
     if (!valid_eb(eb)) return TL_ERR_ELEM_BYTES;
+    // a cast fixes both element sizes: elem_bytes must be its source's
+    int deb = eb;
+    if (cast != TL_CAST_NONE) {
+        if (cast < TL_CAST_NONE || cast > TL_CAST_F16_TO_F32) return TL_ERR_ARG;
+        const bool narrow = cast == TL_CAST_F32_TO_BF16 || cast == TL_CAST_F32_TO_F16;
+        if (eb != (narrow ? 4 : 2)) return TL_ERR_ELEM_BYTES;
+        deb = narrow ? 2 : 4;
+    }
+    p.cast = cast;
+    p.deb = deb;
     if (ndim < 0 || ndim > kMaxDims) return TL_ERR_ARG;
     if (ndim > 0 && (!shape || !src_strides || !dst_strides)) return TL_ERR_ARG;
     uint32_t forced = flags & TL_PATH_MASK;
     if (forced > TL_PATH_BLOCK) return TL_ERR_ARG;
     const bool checked = (flags & TL_FLAG_DEBUG_CHECKS) != 0;
     if ((flags & TL_FLAG_TEST_SKIP_HOST_BOUNDS) && !checked) return TL_ERR_ARG;
+    if (checked && cast != TL_CAST_NONE) return TL_ERR_ARG;   // the checked run moves bits
     if (checked) {                 // the checked run is the generic kernel
         if (forced != TL_PATH_AUTO && forced != TL_PATH_GENERIC) return TL_ERR_PATH;
         forced = TL_PATH_GENERIC;
@@ -1109,15 +1120,15 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         return TL_OK;
     }
     if (!src || !dst) return TL_ERR_ARG;
-    const int align = eb < 16 ? eb : 16;
-    if (!aligned(abs_addr(src), align) || !aligned(abs_addr(dst), align)) return TL_ERR_ALIGN;
+    const int align = eb < 16 ? eb : 16, dalign = deb < 16 ? deb : 16;
+    if (!aligned(abs_addr(src), align) || !aligned(abs_addr(dst), dalign)) return TL_ERR_ALIGN;
 
     int64_t sspan, dspan;
     if (!layout_span(ndim, shape, src_strides, &sspan) ||
         !layout_span(ndim, shape, dst_strides, &dspan))
         return TL_ERR_RANGE;
     int64_t sbytes, dbytes;
-    if (!mul_ok(sspan + 1, eb, &sbytes) || !mul_ok(dspan + 1, eb, &dbytes)) return TL_ERR_RANGE;
+    if (!mul_ok(sspan + 1, eb, &sbytes) || !mul_ok(dspan + 1, deb, &dbytes)) return TL_ERR_RANGE;
     p.sbytes = sbytes;
     p.dbytes = dbytes;
     if (((src_bytes > 0 && sbytes > src_bytes) || (dst_bytes > 0 && dbytes > dst_bytes)) &&
@@ -1158,18 +1169,20 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     // the warp path can be chosen (aliased buffers, forced, or a tiny tensor).
     const bool warp_wanted = ranges_meet || forced == TL_PATH_WARP ||
                              (forced == TL_PATH_AUTO && total <= kWarpAutoMaxElems);
-    const bool warp_ok = warp_wanted && plan_warp(&p);
+    // (under a cast only the chunk, tile and generic kernels convert)
+    const bool casting = cast != TL_CAST_NONE;
+    const bool warp_ok = !casting && warp_wanted && plan_warp(&p);
     bool chunk_ok = false;
     if (srt.n == 0 || (srt.ds[srt.n - 1] == 1 && srt.ss[srt.n - 1] == 1)) chunk_ok = true;
     const bool plane = plan_plane(&p);
-    const bool rows = plane && rows_ok(p, s0, d0);
-    const bool cols = plane && cols_ok(p, s0, d0);
+    const bool rows = !casting && plane && rows_ok(p, s0, d0);
+    const bool cols = !casting && plane && cols_ok(p, s0, d0);
     const bool tile = plane && tile_ok(p, s0);
-    const bool panel = plane && panel_ok(p);
+    const bool panel = !casting && plane && panel_ok(p);
 
     int path = 0;
     if (ranges_meet) {
-        if (!(s0 == d0 && warp_ok && warp_in_place_ok(p))) return TL_ERR_ALIAS;
+        if (casting || !(s0 == d0 && warp_ok && warp_in_place_ok(p))) return TL_ERR_ALIAS;
         if (forced != TL_PATH_AUTO && forced != TL_PATH_WARP) return TL_ERR_PATH;
         p.in_place = true;
         path = TL_PATH_WARP;
@@ -1189,12 +1202,12 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     case TL_PATH_WARP: path = warp_ok ? TL_PATH_WARP : 0; break;
     case TL_PATH_ROWS: path = rows ? TL_PATH_ROWS : 0; break;
     case TL_PATH_TILE: path = tile ? TL_PATH_TILE : 0; break;
-    case TL_PATH_CLUSTER: path = tile ? TL_PATH_CLUSTER : 0; break;
+    case TL_PATH_CLUSTER: path = tile && !casting ? TL_PATH_CLUSTER : 0; break;
     case TL_PATH_PANEL: path = panel ? TL_PATH_PANEL : 0; break;
     case TL_PATH_COLS: path = cols ? TL_PATH_COLS : 0; break;
     case TL_PATH_BLOCK: {
         Plan q = p;
-        path = plan_block(&q) > 0 ? TL_PATH_BLOCK : 0;
+        path = !casting && plan_block(&q) > 0 ? TL_PATH_BLOCK : 0;
         break;
     }
     }
@@ -1212,7 +1225,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     // move short runs on one side (high-rank permutes of short axes) when its own
     // shorter run is 128 bytes or more and at least twice as long (or as long, where
     // the panel tile would be stored element by element).
-    if (forced == TL_PATH_AUTO && !ranges_meet && srt.n >= 3 &&
+    if (forced == TL_PATH_AUTO && !ranges_meet && srt.n >= 3 && !casting &&
         (path == TL_PATH_PANEL || path == TL_PATH_GENERIC)) {
         Plan q = p;
         const int64_t brun = plan_block(&q);
@@ -1256,20 +1269,36 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         p.outer = o;
         p.rows = total / row;
         p.tiles = p.rows;                  // work units: rows
-        int vb = 16;
-        auto fits = [&](int64_t v) { return v % vb == 0; };
-        while (vb > 1) {
-            bool ok = fits(row * eb) && fits(s0) && fits(d0);
-            for (int i = 0; i < o.n && ok; ++i) ok = fits(o.ss[i] * eb) && fits(o.ds[i] * eb);
-            if (ok) break;
-            vb >>= 1;
+        if (!casting) {
+            int vb = 16;
+            auto fits = [&](int64_t v) { return v % vb == 0; };
+            while (vb > 1) {
+                bool ok = fits(row * eb) && fits(s0) && fits(d0);
+                for (int i = 0; i < o.n && ok; ++i)
+                    ok = ok && fits(o.ss[i] * eb) && fits(o.ds[i] * eb);
+                if (ok) break;
+                vb >>= 1;
+            }
+            p.vec_bytes = vb;
+        } else {
+            // vectors of 4, 2 or 1 elements, aligned on both sides (vec_bytes: the
+            // source side's vector)
+            int ve = 4;
+            while (ve > 1) {
+                const int64_t sv = (int64_t)ve * eb, dv = (int64_t)ve * deb;
+                bool ok = row % ve == 0 && s0 % sv == 0 && d0 % dv == 0;
+                for (int i = 0; i < o.n && ok; ++i)
+                    ok = (o.ss[i] * eb) % sv == 0 && (o.ds[i] * deb) % dv == 0;
+                if (ok) break;
+                ve >>= 1;
+            }
+            p.vec_bytes = ve * eb;
         }
-        p.vec_bytes = vb;
     } else if (path == TL_PATH_TILE || path == TL_PATH_CLUSTER) {
         p.tile_cols = 128 / eb;
         p.tile_rows = 128;
-        bool vs = (d0 % 16 == 0) && (p.ds_a * eb) % 16 == 0;
-        for (int i = 0; i < p.batch.n; ++i) vs = vs && (p.batch.ds[i] * eb) % 16 == 0;
+        bool vs = (d0 % 16 == 0) && (p.ds_a * deb) % 16 == 0;
+        for (int i = 0; i < p.batch.n; ++i) vs = vs && (p.batch.ds[i] * deb) % 16 == 0;
         p.vec_store = vs;
         p.vec_bytes = vs ? 16 : eb;
         const int64_t ta = (p.ext_a + p.tile_cols - 1) / p.tile_cols;

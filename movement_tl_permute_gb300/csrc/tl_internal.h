@@ -49,7 +49,9 @@ struct BlockPlan {
 
 struct Plan {
     int path = 0;          // TL_PATH_*; 0 with total == 0 means "nothing to do"
-    int eb = 0;            // element bytes
+    int eb = 0;            // element bytes (of the source under a cast)
+    int cast = 0;          // TL_CAST_*
+    int deb = 0;           // destination element bytes
     int64_t total = 0;     // elements
     int64_t sbytes = 0, dbytes = 0;   // bytes each layout reaches from its base
     Axes sorted;           // unit axes dropped, sorted by dst stride (descending), merged
@@ -99,7 +101,8 @@ struct Plan {
 // Validates the call and fills `plan`.  Pure host code, no CUDA calls.
 int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
               const int64_t* src_strides, const int64_t* dst_strides, int elem_bytes,
-              uint32_t flags, int64_t src_bytes, int64_t dst_bytes, Plan* plan);
+              uint32_t flags, int64_t src_bytes, int64_t dst_bytes, Plan* plan,
+              int cast = TL_CAST_NONE);
 
 // Panel ring: stages per CTA and the dynamic shared memory the kernels are set up
 // for; plan_panel shrinks a tile until its ring fits.

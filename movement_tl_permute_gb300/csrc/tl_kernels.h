@@ -54,6 +54,9 @@ struct GenericArgs {
 };
 template <int EB>
 cudaError_t launch_generic(const GenericArgs& a, int grid, int block, cudaStream_t st, bool pdl);
+// the generic kernel converting every element (TL_CAST_*; dst offsets in dst elements)
+cudaError_t launch_generic_cast(int cast, const GenericArgs& a, int grid, int block,
+                               cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- chunk
 struct ChunkArgs {
@@ -72,6 +75,10 @@ struct ChunkArgs {
 };
 template <int VB>
 cudaError_t launch_chunk(const ChunkArgs& a, int grid, int block, cudaStream_t st, bool pdl);
+// the chunk kernel converting every element: vb = source vector bytes (4, 2 or 1
+// elements), ss in source bytes, ds in destination bytes
+cudaError_t launch_chunk_cast(int cast, int vb, const ChunkArgs& a, int grid, int block,
+                              cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- tile (TMA)
 constexpr int kMaxClusterStages = 8;   // ring depth limit of each cluster ring
@@ -108,6 +115,11 @@ const void* tile_kernel();
 template <int EB, int TB>
 cudaError_t launch_tile(const CUtensorMap& map, const TileArgs& a, int grid, cudaStream_t st,
                         bool pdl);
+
+// the converting tile kernels (TL_CAST_*, 128-row tiles)
+cudaError_t launch_tile_cast(int cast, const CUtensorMap& map, const TileArgs& a, int grid,
+                             cudaStream_t st, bool pdl);
+const void* tile_cast_kernel(int cast);
 
 // tile path with a 2-CTA cluster and a DSMEM hand-off (k_cluster.cu)
 int cluster_smem_bytes(int slots);   // staging + receive slots

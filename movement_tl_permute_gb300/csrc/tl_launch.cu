@@ -146,6 +146,11 @@ int get_device_info(DevInfo* out) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kPanelMaxSmem) != cudaSuccess)
                     return TL_ERR_CUDA;
+            if (i < 4 && cudaFuncSetAttribute(tile_cast_kernel(i + 1),
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              tile_smem_bytes(kTileRingBytes / (128 * 128),
+                                                              128)) != cudaSuccess)
+                return TL_ERR_CUDA;
             if (cudaFuncSetAttribute(block_kernel(1 << i),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kBlockMaxSmem) != cudaSuccess)
@@ -493,7 +498,8 @@ void apply_panel_tile(Plan& p, const tl_permute_opts* o) {
 
 // The tile path's tile height is a launch choice: re-count the tiles for it.
 void apply_tile_rows(Plan& p, const TileTuning& tt) {
-    if (p.path != TL_PATH_TILE || tt.rows == p.tile_rows) return;
+    // (the converting tile kernels take 128-row tiles only)
+    if (p.path != TL_PATH_TILE || tt.rows == p.tile_rows || p.cast != TL_CAST_NONE) return;
     p.tile_rows = tt.rows;
     const int64_t ta = (p.ext_a + p.tile_cols - 1) / p.tile_cols;
     const int64_t tb = (p.ext_b + p.tile_rows - 1) / p.tile_rows;
@@ -552,8 +558,7 @@ struct Prepared {
 struct PlanKey {
     int32_t dev, ndim, eb, smis, dmis;
     uint32_t flags;
-    int32_t o[9];                  // the tuning options of tl_permute_opts
-    int32_t pad;
+    int32_t o[10];                 // the tuning options and the cast of tl_permute_opts
     int64_t shape[kMaxDims], ss[kMaxDims], ds[kMaxDims];
 };
 
@@ -619,10 +624,11 @@ int prepare(const void* src, const void* dst, int ndim, const int64_t* shape,
         key.dmis = (int32_t)(reinterpret_cast<uintptr_t>(dst) & 15);
         key.flags = flags;
         if (opts) {
-            const int32_t o[9] = {opts->max_ctas, opts->tile_group, opts->tile_stages,
-                                  opts->tile_ctas_per_sm, opts->tile_l2_promotion,
-                                  opts->tile_rows, opts->cluster_recv_stages,
-                                  opts->cluster_consumer_warps, opts->panel_tile_kib};
+            const int32_t o[10] = {opts->max_ctas, opts->tile_group, opts->tile_stages,
+                                   opts->tile_ctas_per_sm, opts->tile_l2_promotion,
+                                   opts->tile_rows, opts->cluster_recv_stages,
+                                   opts->cluster_consumer_warps, opts->panel_tile_kib,
+                                   opts->cast};
             std::memcpy(key.o, o, sizeof o);
         }
         for (int i = 0; i < ndim; ++i) {
@@ -658,7 +664,7 @@ int prepare(const void* src, const void* dst, int ndim, const int64_t* shape,
     }
     Prepared pr;
     int rc = make_plan(src, dst, ndim, shape, ss, ds, eb, flags, opts ? opts->src_bytes : 0,
-                       opts ? opts->dst_bytes : 0, &pr.p);
+                       opts ? opts->dst_bytes : 0, &pr.p, opts ? opts->cast : TL_CAST_NONE);
     if (rc != TL_OK) return rc;
     pr.tt = tile_tuning(opts);
     tile_defaults(pr.p, opts, pr.tt);
@@ -712,6 +718,12 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             a.ext[i] = p.sorted.ext[i]; a.ss[i] = p.sorted.ss[i]; a.ds[i] = p.sorted.ds[i];
         }
         a.checked = (flags & TL_FLAG_DEBUG_CHECKS) ? 1 : 0;
+        if (p.cast != TL_CAST_NONE) {
+            a.use32 = a.total < (1LL << 32) ? 1 : 0;
+            if (a.use32) fill_divs(a.n, a.ext, a.div);
+            err = launch_generic_cast(p.cast, a, l.grid, l.block, st, pdl);
+            break;
+        }
         if (a.checked) {
             a.src_bytes = opts ? opts->src_bytes : 0;
             a.dst_bytes = opts ? opts->dst_bytes : 0;
@@ -742,9 +754,13 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         for (int i = 0; i < a.n; ++i) {
             a.ext[i] = p.outer.ext[i];
             a.ss[i] = p.outer.ss[i] * eb;
-            a.ds[i] = p.outer.ds[i] * eb;
+            a.ds[i] = p.outer.ds[i] * p.deb;
         }
         if (a.use32) fill_divs(a.n, a.ext, a.div);
+        if (p.cast != TL_CAST_NONE) {
+            err = launch_chunk_cast(p.cast, p.vec_bytes, a, l.grid, l.block, st, pdl);
+            break;
+        }
         switch (p.vec_bytes) {
         case 16: err = launch_chunk<16>(a, l.grid, l.block, st, pdl); break;
         case 8: err = launch_chunk<8>(a, l.grid, l.block, st, pdl); break;
@@ -791,6 +807,10 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             a.stages = tt.cluster_stages;
             a.recv_stages = tt.cluster_recv;
             err = launch_cluster(eb, tt.cluster_warps, map, a, l.grid, st, pdl);
+            break;
+        }
+        if (p.cast != TL_CAST_NONE) {
+            err = launch_tile_cast(p.cast, map, a, l.grid, st, pdl);
             break;
         }
         if (p.tile_rows == 256) {

@@ -499,6 +499,77 @@ def test_per_cta_times_are_recorded_without_changing_the_result():
 
 
 # ---------------------------------------------------------------------------
+# fused permute + cast
+# ---------------------------------------------------------------------------
+CAST_WIDTHS = {"f32_to_bf16": (4, 2), "f32_to_f16": (4, 2), "bf16_to_f32": (2, 4),
+               "f16_to_f32": (2, 4)}
+
+
+def check_cast(shape, ss, ds, cast, path="auto", seed=0, src_off=0, dst_off=0):
+    """The converting permute on the GPU against oracle.permute_cast, canaries around
+    and between the destination's elements."""
+    seb, deb = CAST_WIDTHS[cast]
+    n_src = (src_off + _span(shape, ss) + 1) * seb
+    n_dst = MARGIN + (dst_off + _span(shape, ds) + 1) * deb + MARGIN
+    src = workloads.random_bits(max(16, n_src), seed)
+    want = np.full(n_dst, CANARY, dtype=np.uint8)
+    oracle.permute_cast(src, want, shape, ss, ds, cast, src_offset=src_off,
+                        dst_offset=MARGIN // deb + dst_off)
+    s_gpu = torch.from_numpy(src).cuda()
+    d_gpu = torch.full((n_dst,), CANARY, dtype=torch.uint8, device="cuda")
+    tl.tl_permute_ex(s_gpu.data_ptr() + src_off * seb, d_gpu.data_ptr() + MARGIN + dst_off * deb,
+                     shape, ss, ds, seb, torch.cuda.current_stream().cuda_stream, path=path,
+                     cast=cast)
+    torch.cuda.synchronize()
+    got = d_gpu.cpu().numpy()
+    if not np.array_equal(got, want):
+        bad = np.nonzero(got != want)[0]
+        raise AssertionError("%d bytes differ (first at %d) for %s shape=%s path=%s"
+                             % (bad.size, bad[0], cast, shape, path))
+
+
+@pytest.mark.parametrize("cast", sorted(CAST_WIDTHS))
+def test_cast_on_the_tile_path(cast):
+    """Converting 2-D and batched transposes on the TMA tile kernel: random bits
+    (NaN and infinity patterns included), ragged tiles, element-wise edges."""
+    seb, _ = CAST_WIDTHS[cast]
+    a = 128 // seb
+    for i, (shape, ss, ds) in enumerate((((300, 2 * a), (2 * a, 1), (1, 300)),
+                                         ((128, 3 * a), (3 * a, 1), (1, 128)),
+                                         ((33, a + a // 2 if seb == 4 else 2 * a), None, None),
+                                         ((5, 130, a), (130 * a, a, 1), (130 * a, 1, 130)))):
+        if ss is None:
+            ss, ds = (shape[1], 1), (1, shape[0])
+        check_cast(shape, ss, ds, cast, "tile", seed=600 + i)
+        check_cast(shape, ss, ds, cast, "auto", seed=610 + i)
+    # dst rows off the 16-byte grid: the element-wise stores
+    check_cast((37, 2 * a), (2 * a, 1), (1, 37), cast, "tile", seed=620, dst_off=1)
+
+
+@pytest.mark.parametrize("cast", sorted(CAST_WIDTHS))
+def test_cast_on_the_chunk_and_generic_paths(cast):
+    """Converting permutes whose innermost axis is contiguous on both sides (chunk
+    kernel, vectors of 4, 2 and 1 elements) and strided layouts (generic kernel)."""
+    rng = np.random.default_rng(630)
+    for i in range(8):
+        inner = int(rng.choice([4, 8, 12, 64, 130]))
+        outer = tuple(int(x) for x in rng.integers(1, 7, size=int(rng.integers(1, 4))))
+        shape = outer + (inner,)
+        perm = tuple(int(p) for p in rng.permutation(len(outer))) + (len(outer),)
+        ss, ds = perm_layouts(shape, perm)
+        off = (0, 1, 2)[i % 3]
+        check_cast(shape, ss, ds, cast, "chunk", seed=640 + i, src_off=off, dst_off=(i // 3) % 2)
+        check_cast(shape, ss, ds, cast, "generic", seed=650 + i, src_off=off)
+    # a strided gather and a broadcast on the generic kernel
+    check_cast((9, 14), (2, 37), (14, 1), cast, "generic", seed=660)
+    check_cast((4, 6, 5), (0, 5, 1), (30, 5, 1), cast, "generic", seed=661)
+    # paths that move bits only decline a cast
+    with pytest.raises(tl.TLError) as e:
+        check_cast((64, 256), (256, 1), (1, 64), cast, "panel", seed=662)
+    assert e.value.name == "TL_ERR_PATH"
+
+
+# ---------------------------------------------------------------------------
 # edge cases
 # ---------------------------------------------------------------------------
 def test_tensor_level_permute_matches_torch():

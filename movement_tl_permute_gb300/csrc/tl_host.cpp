@@ -1222,9 +1222,9 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         plan_panel(&q, 0);
     };
     // The block tile takes layouts of canonical rank 3 or more whose panel tile would
-    // move short runs on one side (high-rank permutes of short axes) when its own
-    // shorter run is 128 bytes or more and at least twice as long (or as long, where
-    // the panel tile would be stored element by element).
+    // move short runs on one side and store them element by element (high-rank
+    // permutes of short axes) when its own shorter run is 128 bytes or more and at
+    // least as long.
     if (forced == TL_PATH_AUTO && !ranges_meet && srt.n >= 3 && !casting &&
         (path == TL_PATH_PANEL || path == TL_PATH_GENERIC)) {
         Plan q = p;
@@ -1245,13 +1245,13 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
                 r_vec = r.panel_vec;
                 r_run = r.panel_run;
             }
-            // (a panel tile stored as 16-byte dst runs keeps the panel unless the block
-            // runs are twice as long; element-stored panel tiles yield at equal runs:
-            // measured on GB300, 9^8 fp32 permutes whose panel tiles are 81 x 81 with
-            // element stores run 1.2-1.4x faster as blocks, reversed 8^8 / 10^8 fp32
-            // and a 6-D fp32 permute with 16-byte runs 0.6-0.8x)
+            // (a panel tile stored as 16-byte dst runs keeps the panel: the block
+            // kernel stores element by element; measured on GB300, reversed 8^8 / 10^8
+            // fp32 and 6-D fp32 permutes with 16-byte panel runs ran 0.6-0.8x as
+            // blocks, while 9^8 fp32 permutes whose panel tiles store elements ran
+            // 1.2-1.4x faster as blocks at equal runs)
             const bool vec = path == TL_PATH_PANEL && (r_vec || r_run);
-            if (brun >= 2 * prun || (!vec && brun >= prun)) path = TL_PATH_BLOCK;
+            if (!vec && brun >= prun) path = TL_PATH_BLOCK;
         }
     }
     p.path = path;

@@ -904,13 +904,16 @@ int64_t block_stage_off(const BlockPlan& b, int eb, int pitch, int64_t i, int64_
     for (int k = 0; k < b.nj; ++k) e[k] = b.tile[b.jax[k]];
     digits(j, b.nj, e, d);
     for (int k = 0; k < b.nj; ++k) coord[b.jax[k]] = d[k];
-    int64_t sp = 0, r = 0, rw = 1;
+    int64_t sp = 0, r = 0, rw = 1, soff = 0;
     for (int k = 0; k < b.ns; ++k) sp += coord[b.sax[k]] * b.ss[b.sax[k]];
     for (int k = 0; k < b.nr; ++k) {
         r += coord[b.rax[k]] * rw;
         rw *= b.tile[b.rax[k]];
+        soff += coord[b.rax[k]] * b.ss[b.rax[k]];
     }
-    return r * pitch + sp * eb;
+    // each src run sits at its own offset inside its first 16-byte block (the tile's
+    // base taken as aligned)
+    return r * pitch + ((soff * eb) & 15) + sp * eb;
 }
 
 int block_pitch(const BlockPlan& b, int eb) {

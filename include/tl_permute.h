@@ -176,12 +176,13 @@ TL_API int tl_permute(const void *src, void *dst, int ndim, const int64_t *shape
                                2..16 elements, <= 24 bytes): 16-byte pixel loads, register
                                transpose, one 16-byte store per plane */
 #define TL_PATH_BLOCK 9u    /* a tile of up to four axes that is a few long contiguous runs
-                               on both sides (high-rank permutes of short axes): src runs
-                               staged in smem by cp.async, stores along the dst runs */
+                               on both sides (high-rank permutes of short axes): each src
+                               run one bulk copy into smem, stores along the dst runs */
 #define TL_PATH_MASK 0xFu
-/* Test hook for the cluster path (the producer CTA skips its DSMEM hand-off) and for
+/* Test hook for the cluster path (the producer CTA skips its DSMEM hand-off), for
  * panel tiles loaded by TMA phase maps (the loading thread skips one phase load of its
- * first tile): the bounded wait (50 ms under the hook) must expire and report
+ * first tile) and for the block path (the producer warp skips the first src-run copy
+ * of its first tile): the bounded wait (50 ms under the hook) must expire and report
  * TL_ERR_TIMEOUT in dev_status; the kernel returns without a fault. */
 #define TL_FLAG_TEST_DROP_HANDOFF (1u << 8)
 /* Launch without programmatic dependent launch (by default a permute may be scheduled
@@ -281,7 +282,7 @@ typedef struct tl_plan_info {
     int32_t grid, block;           /* launch shape (0 without a device) */
     int32_t smem_bytes;            /* dynamic shared memory per CTA */
     int32_t pitch;                 /* panel path: shared-memory bytes per tile row;
-                                      block path: per src run */
+                                      block path: between neighbouring src runs */
     int32_t panel_mode;            /* panel path: 0 rows of 16-byte blocks, 1 one run,
                                       2 rows loaded by TMA phase maps into a phase-major
                                       stage (a row pitch off the 16-byte grid), 3 the
@@ -301,6 +302,10 @@ typedef struct tl_plan_info {
                                       was merged with the next src axis (src dense across
                                       the two); the inner extent, each tile row's dst
                                       offset then splits a into its two axes */
+    int32_t block_runs;            /* block path: dst runs a warp of the store walk covers
+                                      at once (1: consecutive elements in dst order, on
+                                      into the next run; 2 .. 32: as many runs, an equal
+                                      share of consecutive pieces in each) */
 } tl_plan_info;
 
 TL_API int tl_plan(const void *src, const void *dst, int ndim, const int64_t *shape,

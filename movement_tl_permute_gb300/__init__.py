@@ -83,7 +83,7 @@ class TlPlanInfo(ctypes.Structure):
                 ("mask", _i32), ("tile_rows", _i32), ("tile_cols", _i32), ("tiles", _i64),
                 ("grid", _i32), ("block", _i32), ("smem_bytes", _i32), ("pitch", _i32),
                 ("panel_mode", _i32), ("panel_b1", _i32), ("panel_vec", _i32),
-                ("panel_wrot", _i32), ("panel_a1", _i32)]
+                ("panel_wrot", _i32), ("panel_a1", _i32), ("block_runs", _i32)]
 
 
 def library_path() -> str:
@@ -317,7 +317,7 @@ def tl_plan(src_ptr: int, dst_ptr: int, shape, src_strides, dst_strides, elem_by
                 smem_bytes=info.smem_bytes, pitch=info.pitch, panel_mode=info.panel_mode,
                 panel_b1=info.panel_b1, panel_vec=info.panel_vec,
                 panel_wrot=(info.panel_wrot & 0xFF, info.panel_wrot >> 8),
-                panel_a1=info.panel_a1)
+                panel_a1=info.panel_a1, block_runs=info.block_runs)
 
 
 def _bytes_after(t) -> int:

@@ -7,29 +7,53 @@
 // contiguous runs on both sides: the src run is the chain of T's axes from src
 // stride 1, each of src stride the product of the extents before it, and the other
 // axes of T index the src runs; the dst run and its index axes likewise from dst
-// stride 1.  Each CTA runs a ring of kBlockStages shared-memory stages: every src run
-// of a tile is copied as the aligned 16-byte blocks covering it (cp.async, landing at
-// the run's own offset inside its first block), and while the copies of the next
-// tiles fly, the landed tile is stored along its dst runs, consecutive threads
-// writing consecutive dst addresses.  Per-CTA tables built once in shared memory turn
-// (dst run j, position i) into (src run, position inside it) with adds only; the
-// run pitch is chosen on the host by replaying the store walk's warp reads on the
-// bank model of the TVM "permute_layout" page ("Algorithm", step 2).  Element
-// offsets follow the strided addressing of "Buffers and memory", "Declaring buffers".
+// stride 1.
+//
+// Stage layout.  Every axis of T has a shared-memory byte stride: a src-run axis its
+// src byte stride, a src-run index axis a stride the host picks congruent to its src
+// byte stride modulo 16 (with room between runs for the 16-byte blocks around each).
+// An element then sits in the stage at the same offset modulo 16 as in src, so each
+// src run is one bulk copy of the aligned 16-byte blocks covering it, and the stage
+// offset of element (dst run j, position i) is TA[i] + TB[j] from two per-CTA tables
+// -- one add, whatever the runs' offsets inside their blocks.  The strides are chosen
+// on the host by replaying the store walk's warp reads on the bank model of the TVM
+// "permute_layout" page ("Algorithm", step 2).
+//
+// Warps.  One producer warp issues the bulk copies of each tile (its lanes take the
+// runs in turn) into a ring of kBlockStages stages, completion counted on the stage's
+// mbarrier; the consumer warps store each landed tile along its dst runs, each thread
+// V consecutive dst elements per step (one vector store when the dst runs allow it),
+// consecutive threads taking consecutive pieces.  Waits are bounded: a wait that
+// expires reports TL_ERR_TIMEOUT, and the CTA leaves once its own copies have landed
+// (or a longer bound has passed).  Element offsets follow the strided addressing of
+// "Buffers and memory", "Declaring buffers".
 #include "tl_kernels.h"
 
 namespace tl {
 namespace {
 
-__device__ __forceinline__ void cp_async16(uint32_t saddr, uintptr_t gaddr) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gaddr) : "memory");
+using dev::lds128;
+using dev::lds32;
+using dev::lds64;
+
+// One bulk copy global -> this CTA's shared memory, completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t sdst, uintptr_t gsrc, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(sdst), "l"(gsrc), "r"(bytes), "r"(bar)
+        : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
+
+__device__ __forceinline__ uint32_t lds8(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
 }
 
 struct BlockTile {
@@ -70,173 +94,372 @@ __device__ __forceinline__ BlockTile block_tile(int64_t t, const BlockArgs& a) {
     return r;
 }
 
-// Copies of one tile into stage `slot`: the 16-byte blocks covering each valid src
-// run; the first block's thread records where the run starts in the stage.
-template <int EB>
-__device__ __forceinline__ void block_issue(const BlockArgs& a, const BlockTile& ti,
-                                            uint32_t sbase, const uint4* TR, uint32_t* RB) {
-    const uintptr_t base = reinterpret_cast<uintptr_t>(a.src) + (uintptr_t)(ti.so * EB);
-    const uint32_t ls = a.ls_inner == a.Ls ? (uint32_t)a.Ls : (uint32_t)a.ls_inner * ti.vc;
-    const uint32_t nblk = (uint32_t)a.nblk, n = (uint32_t)a.Rs * nblk;
-    for (uint32_t g = threadIdx.x; g < n; g += kBlockThreads) {
-        const uint32_t r = dev::div_u32(g, a.d_nblk), k = g - r * nblk;
-        const uint4 tr = TR[r];
-        if (tr.z >= ti.vc) continue;                    // a run past the tile's chunk
-        const int64_t soff = (int64_t)((uint64_t)tr.x | ((uint64_t)tr.y << 32));
-        const uintptr_t run = base + (uintptr_t)(soff * EB);
-        const uint32_t mis = (uint32_t)(run & 15);
-        if (k == 0) RB[r] = r * (uint32_t)a.pitch + mis;
-        if (k < ((mis + ls * EB + 15) >> 4))
-            cp_async16(sbase + r * (uint32_t)a.pitch + 16 * k, (run & ~uintptr_t(15)) + 16 * k);
-    }
-}
+// A piece: V elements of EB bytes as 4-byte words (one word when V * EB < 4).
+template <int EB, int V>
+struct Piece {
+    static constexpr int kWords = V * EB < 4 ? 1 : V * EB / 4;
+    uint32_t w[kWords];
+};
 
-// Stores one landed tile along its dst runs: element (j, i) of the tile's dst runs
-// from the stage at RB[r_i + r_j] + (p_i + p_j) * EB, or, when every src run starts
-// at the same offset inside its 16-byte block (umis), at mis0 + T_i + T_j with the
-// tables holding r * pitch + p * EB.  Four elements per thread and step, so that
-// their table and stage reads overlap.
-template <int EB>
-__device__ __forceinline__ void block_drain(const BlockArgs& a, const BlockTile& ti,
-                                            const uint8_t* st, const uint2* TA, const uint4* TB,
-                                            const uint32_t* RB) {
-    using T = typename dev::Bits<EB>::T;
-    constexpr uint32_t U = 4;
-    T* d = reinterpret_cast<T*>(a.dst) + ti.dof;
-    const uint32_t Ld = (uint32_t)a.Ld, n = Ld * (uint32_t)a.Rd;
-    const uint32_t vc = ti.vc;
-    const uint8_t* st0 = st + (reinterpret_cast<uintptr_t>(a.src + ti.so * EB) & 15);
-    for (uint32_t f0 = threadIdx.x; f0 < n; f0 += U * kBlockThreads) {
+// Loads the V stage elements at sj + off[k] into a piece.
+template <int EB, int V>
+__device__ __forceinline__ void gather(Piece<EB, V>& pc, uint32_t sj, const uint32_t* off) {
+    if constexpr (EB >= 4) {
 #pragma unroll
-        for (uint32_t u = 0; u < U; ++u) {
-            const uint32_t f = f0 + u * kBlockThreads;
-            if (f >= n) break;
-            const uint32_t j = dev::div_u32(f, a.d_Ld), i = f - j * Ld;
-            const uint2 ta = TA[i];
-            const uint4 tb = TB[j];
-            if ((ta.y >> 16) + (tb.y >> 16) >= vc) continue;   // past the tile's chunk
-            const int64_t dofs = (int64_t)((uint64_t)tb.z | ((uint64_t)tb.w << 32));
-            const uint8_t* sp;
-            if (a.umis) {
-                sp = st0 + ta.x + tb.x;
+        for (int k = 0; k < V; ++k) {
+            if constexpr (EB == 16) {
+                const uint4 x = lds128(sj + off[k]);
+                pc.w[0] = x.x; pc.w[1] = x.y; pc.w[2] = x.z; pc.w[3] = x.w;
+            } else if constexpr (EB == 8) {
+                const uint2 x = lds64(sj + off[k]);
+                pc.w[2 * k] = x.x;
+                pc.w[2 * k + 1] = x.y;
             } else {
-                const uint32_t r = (ta.y & 0xffffu) + (tb.y & 0xffffu);
-                sp = st + RB[r] + (ta.x + tb.x) * EB;
+                pc.w[k] = lds32(sj + off[k]);
             }
-            d[dofs + i] = *reinterpret_cast<const T*>(sp);
+        }
+    } else {
+        constexpr int kPer = 4 / EB;                  // elements per word
+#pragma unroll
+        for (int q = 0; q < Piece<EB, V>::kWords; ++q) {
+            uint32_t x = 0;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) {
+                if (q * kPer + e < V) {
+                    const uint32_t y = EB == 2 ? lds16(sj + off[q * kPer + e])
+                                               : lds8(sj + off[q * kPer + e]);
+                    x |= y << (8 * EB * e);
+                }
+            }
+            pc.w[q] = x;
         }
     }
 }
 
-template <int EB>
-__global__ void __launch_bounds__(kBlockThreads) k_block(const BlockArgs a) {
+// Stores a piece as one vector at p (aligned to V * EB bytes).
+template <int EB, int V>
+__device__ __forceinline__ void put(uint8_t* p, const Piece<EB, V>& pc) {
+    if constexpr (V * EB == 16) {
+        dev::stg128(p, make_uint4(pc.w[0], pc.w[1], pc.w[2], pc.w[3]));
+    } else if constexpr (V * EB == 8) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(pc.w[0], pc.w[1]);
+    } else if constexpr (V * EB == 4) {
+        *reinterpret_cast<uint32_t*>(p) = pc.w[0];
+    } else if constexpr (V * EB == 2) {
+        *reinterpret_cast<uint16_t*>(p) = (uint16_t)pc.w[0];
+    } else {
+        *p = (uint8_t)pc.w[0];
+    }
+}
+
+// Where TA keeps dst-run position i: in order, except that for V >= 8 the four
+// entries q of every piece sit at (q * W + piece) * 4, so that the lanes of a warp
+// (consecutive pieces) read consecutive 16-byte words.
+template <int V>
+__device__ __forceinline__ uint32_t ta_slot(uint32_t i, uint32_t W) {
+    if constexpr (V >= 8) {
+        const uint32_t v = i / V, e = i - v * V;
+        return ((e >> 2) * W + v) * 4 + (e & 3);
+    } else {
+        return i;
+    }
+}
+
+// The V entries of TA of piece v (4-byte stage offsets).
+template <int V>
+__device__ __forceinline__ void load_offsets(uint32_t ta, uint32_t v, uint32_t W, uint32_t* off) {
+    if constexpr (V >= 4) {
+#pragma unroll
+        for (int q = 0; q < V / 4; ++q) {
+            const uint4 x = lds128(ta + 16 * (V >= 8 ? q * W + v : v));
+            off[4 * q] = x.x;
+            off[4 * q + 1] = x.y;
+            off[4 * q + 2] = x.z;
+            off[4 * q + 3] = x.w;
+        }
+    } else if constexpr (V == 2) {
+        const uint2 x = lds64(ta + 8 * v);
+        off[0] = x.x;
+        off[1] = x.y;
+    } else {
+        off[0] = lds32(ta + 4 * v);
+    }
+}
+
+template <int EB, int V>
+__global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const BlockArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full[kBlockStages];
+    __shared__ __align__(8) uint64_t empty[kBlockStages];
+    __shared__ __align__(16) uint4 info[kBlockStages];   // dof lo / hi, vc, origin mod 16
     const uint32_t sbase = dev::smem_addr(smem);
     const uint32_t stage = (uint32_t)a.stage_bytes;
-    uint2* TA = reinterpret_cast<uint2*>(smem + a.table_off);
-    uint4* TB = reinterpret_cast<uint4*>(TA + ((a.Ld + 1) & ~1));   // 16-byte aligned
-    uint4* TR = reinterpret_cast<uint4*>(TB + a.Rd);
-    uint32_t* RB = reinterpret_cast<uint32_t*>(TR + a.Rs);     // [kBlockStages][Rs]
+    uint32_t* TA = reinterpret_cast<uint32_t*>(smem + a.table_off);       // [Ld, padded to 4]
+    uint4* TB = reinterpret_cast<uint4*>(TA + ((a.Ld + 3) & ~3));        // [Rd]
+    uint4* TR = TB + a.Rd;                                                // [Rs]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // the tables (from the arguments only: before the dependency wait)
     for (int32_t i = threadIdx.x; i < a.Ld; i += kBlockThreads) {
-        int64_t x = i, sp = 0;
-        uint32_t r = 0, c = 0;
+        uint32_t x = (uint32_t)i, o = 0;
         for (int k = 0; k < a.nd; ++k) {
-            const int64_t dg = x % a.dext[k];
-            x /= a.dext[k];
-            sp += dg * a.dsp[k];
-            r += (uint32_t)dg * (uint32_t)a.drs[k];
-            if (k == a.dck) c = (uint32_t)dg;
+            const uint32_t q = x / (uint32_t)a.dext[k];
+            o += (x - q * (uint32_t)a.dext[k]) * a.dsq[k];
+            x = q;
         }
-        TA[i] = make_uint2(a.umis ? r * (uint32_t)a.pitch + (uint32_t)sp * EB : (uint32_t)sp,
-                           r | (c << 16));
+        TA[ta_slot<V>((uint32_t)i, (uint32_t)a.W)] = o;
     }
     for (int32_t j = threadIdx.x; j < a.Rd; j += kBlockThreads) {
-        int64_t x = j, sp = 0, dofs = 0;
-        uint32_t r = 0, c = 0;
+        uint32_t x = (uint32_t)j, o = 0, c = 0;
+        int64_t dofs = 0;
         for (int k = 0; k < a.nj; ++k) {
-            const int64_t dg = x % a.jext[k];
-            x /= a.jext[k];
-            sp += dg * a.jsp[k];
-            r += (uint32_t)dg * (uint32_t)a.jrs[k];
-            dofs += dg * a.jds[k];
-            if (k == a.jck) c = (uint32_t)dg;
+            const uint32_t q = x / (uint32_t)a.jext[k];
+            const uint32_t dg = x - q * (uint32_t)a.jext[k];
+            x = q;
+            o += dg * a.jsq[k];
+            dofs += (int64_t)dg * a.jds[k];
+            if (k == a.jck) c = dg;
         }
-        TB[j] = make_uint4(a.umis ? r * (uint32_t)a.pitch + (uint32_t)sp * EB : (uint32_t)sp,
-                           r | (c << 16), (uint32_t)(uint64_t)dofs,
-                           (uint32_t)((uint64_t)dofs >> 32));
+        dofs *= EB;                                          // in bytes
+        TB[j] = make_uint4(o, c, (uint32_t)(uint64_t)dofs, (uint32_t)((uint64_t)dofs >> 32));
     }
     for (int32_t r = threadIdx.x; r < a.Rs; r += kBlockThreads) {
-        int64_t x = r, soff = 0;
-        uint32_t c = 0;
+        uint32_t x = (uint32_t)r, o = 0, c = 0;
+        int64_t sb = 0;
         for (int k = 0; k < a.nr; ++k) {
-            const int64_t dg = x % a.rext[k];
-            x /= a.rext[k];
-            soff += dg * a.rss[k];
-            if (k == a.rck) c = (uint32_t)dg;
+            const uint32_t q = x / (uint32_t)a.rext[k];
+            const uint32_t dg = x - q * (uint32_t)a.rext[k];
+            x = q;
+            o += dg * a.rsq[k];
+            sb += (int64_t)dg * a.rsb[k];
+            if (k == a.rck) c = dg;
         }
-        TR[r] = make_uint4((uint32_t)(uint64_t)soff, (uint32_t)((uint64_t)soff >> 32), c, 0u);
+        TR[r] = make_uint4((uint32_t)(uint64_t)sb, (uint32_t)((uint64_t)sb >> 32), o, c);
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBlockStages; ++s) {
+            dev::mbar_init(&full[s], 32);                  // every producer lane arrives
+            dev::mbar_init(&empty[s], kBlockConsumerWarps);
+        }
+        dev::fence_barrier_init();
     }
     __syncthreads();
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
     dev::cta_start(a.cta_times);
 
-    const int64_t first = blockIdx.x, step = gridDim.x;
-    const int64_t mine = first < a.tiles ? (a.tiles - first + step - 1) / step : 0;
-    // Every thread commits one group per tile slot (empty groups included), so
-    // wait_group counts the same groups in every thread.
-    for (int s = 0; s < kBlockStages - 1; ++s) {
-        if (s < mine)
-            block_issue<EB>(a, block_tile(first + s * step, a), sbase + s * stage, TR,
-                            RB + s * a.Rs);
-        cp_async_commit();
+    if (warp == kBlockConsumerWarps) {
+        // ---------------- producer: one bulk copy per src run ---------------------------
+        uint32_t issued = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++issued) {
+            const uint32_t use = issued / kBlockStages, s = issued - use * kBlockStages;
+            if (use > 0) {
+                const bool got = dev::mbar_wait(&empty[s], (use - 1) & 1, a.timeout_ns);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                dev::fence_proxy_async_smem();   // the consumers' reads of the stage came first
+            }
+            const BlockTile ti = block_tile(t, a);
+            const uintptr_t base = reinterpret_cast<uintptr_t>(a.src) + (uintptr_t)(ti.so * EB);
+            const uint32_t tmis = (uint32_t)(base & 15);
+            // bytes of a src run in this tile, and the runs inside its chunk
+            const uint32_t len = (uint32_t)(a.ls_chunk ? a.ls_inner * ti.vc : a.Ls) * EB;
+            const uint32_t rlim = a.rck >= 0 ? ti.vc : 0xffffffffu;
+            const uint32_t sdst = sbase + s * stage + 16 + tmis;
+            if (lane == 0)
+                dev::sts128(dev::smem_addr(&info[s]),
+                            make_uint4((uint32_t)(uint64_t)ti.dof,
+                                       (uint32_t)((uint64_t)ti.dof >> 32), ti.vc, tmis));
+            uint32_t bytes = 0;
+            for (int32_t r = lane; r < a.Rs; r += 32) {
+                const uint4 tr = lds128(dev::smem_addr(&TR[r]));
+                if (tr.w >= rlim) continue;
+                const uintptr_t g = base + (uintptr_t)((uint64_t)tr.x | ((uint64_t)tr.y << 32));
+                bytes += ((uint32_t)(g & 15) + len + 15) & ~15u;
+            }
+            __syncwarp();
+            dev::mbar_arrive_expect_tx(&full[s], bytes);
+            const uint32_t bar = dev::smem_addr(&full[s]);
+            for (int32_t r = lane; r < a.Rs; r += 32) {
+                const uint4 tr = lds128(dev::smem_addr(&TR[r]));
+                if (tr.w >= rlim) continue;
+                if (a.drop_load && issued == 0 && r == 0) continue;   // test hook: the wait expires
+                const uintptr_t g = base + (uintptr_t)((uint64_t)tr.x | ((uint64_t)tr.y << 32));
+                const uint32_t mis = (uint32_t)(g & 15);
+                bulk_load(sdst + tr.z - mis, g - mis, (mis + len + 15) & ~15u, bar);
+            }
+        }
+        if (!ok && lane == 0) dev::report(a.status, TL_ERR_TIMEOUT);
+        // Do not leave while a copy may still write this CTA's shared memory (a longer
+        // bound than the wait that expired; past it the CTA leaves anyway).
+        for (uint32_t i = issued > kBlockStages ? issued - kBlockStages : 0; i < issued; ++i)
+            dev::mbar_wait(&full[i % kBlockStages], (i / kBlockStages) & 1,
+                           dev::kDrainFactor * a.timeout_ns);
+        dev::cta_finish(a.cta_times);
+        return;
     }
-    uint32_t slot = 0, ahead = kBlockStages - 1;
-    for (int64_t i = 0; i < mine; ++i) {
-        const int64_t nxt = i + kBlockStages - 1;
-        if (nxt < mine)
-            block_issue<EB>(a, block_tile(first + nxt * step, a), sbase + ahead * stage, TR,
-                            RB + ahead * a.Rs);
-        cp_async_commit();
-        cp_async_wait<kBlockStages - 1>();           // tile i has landed (this thread's part)
-        __syncthreads();                             // ... and every other thread's part
-        block_drain<EB>(a, block_tile(first + i * step, a), smem + slot * stage, TA, TB,
-                        RB + slot * a.Rs);
-        __syncthreads();                             // stage `slot` may be refilled
-        slot = slot + 1 == kBlockStages ? 0 : slot + 1;
-        ahead = ahead + 1 == kBlockStages ? 0 : ahead + 1;
+
+    // ---------------- consumers: store each tile along its dst runs ------------------
+    // Two walks over the pieces (V dst elements each, W per dst run), picked on the host
+    // with the bank model.  r_lg == 0: the consumer threads take consecutive pieces in
+    // dst order (a warp's pieces run on into the next dst run).  r_lg > 0: a warp-step
+    // takes a group of 32 >> r_lg consecutive pieces in each of 1 << r_lg consecutive
+    // dst runs, whose stage reads spread over more banks (lane = (pl, rl)).
+    const uint32_t W = (uint32_t)a.W, Rd = (uint32_t)a.Rd;
+    const uint32_t GW = (uint32_t)a.GW, GR = (uint32_t)a.GR;
+    const uint32_t dgw = (uint32_t)a.dgw, dgr = (uint32_t)a.dgr;
+    const uint32_t pw_lg = 5 - (uint32_t)a.r_lg;
+    const uint32_t pl = (uint32_t)lane & ((1u << pw_lg) - 1), rl = (uint32_t)lane >> pw_lg;
+    const uint32_t ct = threadIdx.x;                        // 0 .. consumer threads - 1
+    const uint32_t ta = dev::smem_addr(TA), tb = dev::smem_addr(TB);
+    uint32_t it = 0;
+    for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++it) {
+        const uint32_t use = it / kBlockStages, s = it - use * kBlockStages;
+        if (!dev::mbar_wait(&full[s], use & 1, a.timeout_ns)) {
+            if (lane == 0) dev::report(a.status, TL_ERR_TIMEOUT);
+            break;
+        }
+        const uint4 inf = lds128(dev::smem_addr(&info[s]));
+        const int64_t dof = (int64_t)((uint64_t)inf.x | ((uint64_t)inf.y << 32));
+        const uint32_t vc = inf.z;
+        const uint32_t sb = sbase + s * stage + 16 + inf.w;
+        // pieces of a dst run, and dst runs, inside this tile's chunk
+        const uint32_t wlim = a.ld_chunk ? (uint32_t)a.ld_inner * vc / V : W;
+        const uint32_t jlim = a.jck >= 0 ? vc : 0xffffffffu;
+        uint8_t* dt = a.dst + dof * EB;
+        // stores piece v of dst run j (when inside the chunk) from its loaded parts
+        auto store = [&](bool in, uint32_t v, const uint4& tj, const Piece<EB, V>& pc) {
+            if (in && v < wlim && tj.y < jlim)
+                put<EB, V>(dt + (int64_t)((uint64_t)tj.z | ((uint64_t)tj.w << 32)) + v * (V * EB),
+                           pc);
+        };
+        if (a.r_lg == 0) {
+            // single elements: two pieces per step (the second repeats the first past
+            // the last one, unstored), so that the table and stage reads of both are in
+            // flight together (measured on GB300: 9^8 fp32 permutes 4.6 -> 5.7 TB/s;
+            // wider pieces ran 0.8-1.0x as fast two at a time)
+            const uint32_t step = 32 * kBlockConsumerWarps;
+            const uint32_t dv = step % W, dj = step / W;
+            uint32_t v = ct % W, j = ct / W;
+            while (j < Rd) {
+                uint32_t v1 = v + dv, j1 = j + dj;             // the next piece
+                if (v1 >= W) {
+                    v1 -= W;
+                    ++j1;
+                }
+                const uint4 t0 = lds128(tb + 16 * j);
+                uint32_t o0[V];
+                load_offsets<V>(ta, v, W, o0);
+                Piece<EB, V> p0;
+                if constexpr (V == 1) {
+                    const bool two = j1 < Rd;
+                    const uint32_t vb = two ? v1 : v, jb = two ? j1 : j;
+                    const uint4 t1 = lds128(tb + 16 * jb);
+                    uint32_t o1[1];
+                    load_offsets<1>(ta, vb, W, o1);
+                    Piece<EB, 1> p1;
+                    gather<EB, 1>(p0, sb + t0.x, o0);
+                    gather<EB, 1>(p1, sb + t1.x, o1);
+                    store(true, v, t0, p0);
+                    store(two, vb, t1, p1);
+                    if (two) {                                  // past the second piece
+                        v1 += dv;
+                        j1 += dj;
+                        if (v1 >= W) {
+                            v1 -= W;
+                            ++j1;
+                        }
+                    }
+                } else {
+                    gather<EB, V>(p0, sb + t0.x, o0);
+                    store(true, v, t0, p0);
+                }
+                v = v1;
+                j = j1;
+            }
+        } else {
+            uint32_t gw = (uint32_t)warp % GW, gr = (uint32_t)warp / GW;
+            while (gr < GR) {
+                uint32_t v = (gw << pw_lg) + pl, j = (gr << a.r_lg) + rl;
+                const bool in = v < W && j < Rd;
+                v = in ? v : 0;                                 // (table reads stay inside)
+                j = in ? j : 0;
+                const uint4 t0 = lds128(tb + 16 * j);
+                uint32_t o0[V];
+                load_offsets<V>(ta, v, W, o0);
+                Piece<EB, V> p0;
+                gather<EB, V>(p0, sb + t0.x, o0);
+                store(in, v, t0, p0);
+                gw += dgw;
+                gr += dgr;
+                if (gw >= GW) {
+                    gw -= GW;
+                    ++gr;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(&empty[s]);
     }
-    cp_async_wait<0>();
     dev::cta_finish(a.cta_times);
+}
+
+using BlockFn = void (*)(const BlockArgs);
+
+template <int EB>
+BlockFn kernel_of(int v) {
+    if constexpr (EB == 1) {
+        switch (v) {
+        case 16: return &k_block<1, 16>;
+        case 8: return &k_block<1, 8>;
+        case 4: return &k_block<1, 4>;
+        case 2: return &k_block<1, 2>;
+        default: return &k_block<1, 1>;
+        }
+    } else if constexpr (EB == 2) {
+        switch (v) {
+        case 8: return &k_block<2, 8>;
+        case 4: return &k_block<2, 4>;
+        case 2: return &k_block<2, 2>;
+        default: return &k_block<2, 1>;
+        }
+    } else if constexpr (EB == 4) {
+        switch (v) {
+        case 4: return &k_block<4, 4>;
+        case 2: return &k_block<4, 2>;
+        default: return &k_block<4, 1>;
+        }
+    } else if constexpr (EB == 8) {
+        return v == 2 ? &k_block<8, 2> : &k_block<8, 1>;
+    } else {
+        return &k_block<16, 1>;
+    }
+}
+
+BlockFn block_fn(int eb, int v) {
+    switch (eb) {
+    case 1: return kernel_of<1>(v);
+    case 2: return kernel_of<2>(v);
+    case 4: return kernel_of<4>(v);
+    case 8: return kernel_of<8>(v);
+    default: return kernel_of<16>(v);
+    }
 }
 
 }  // namespace
 
 int block_smem_bytes(const BlockArgs& a) {
-    return a.table_off + 8 * ((a.Ld + 1) & ~1) + 16 * a.Rd + 16 * a.Rs + 4 * kBlockStages * a.Rs;
+    return a.table_off + 4 * ((a.Ld + 3) & ~3) + 16 * a.Rd + 16 * a.Rs;
 }
 
-const void* block_kernel(int eb) {
-    switch (eb) {
-    case 1: return reinterpret_cast<const void*>(&k_block<1>);
-    case 2: return reinterpret_cast<const void*>(&k_block<2>);
-    case 4: return reinterpret_cast<const void*>(&k_block<4>);
-    case 8: return reinterpret_cast<const void*>(&k_block<8>);
-    default: return reinterpret_cast<const void*>(&k_block<16>);
-    }
-}
+const void* block_kernel(int eb, int v) { return reinterpret_cast<const void*>(block_fn(eb, v)); }
 
 cudaError_t launch_block(int eb, const BlockArgs& a, int grid, cudaStream_t st, bool pdl) {
-    const int smem = block_smem_bytes(a);
-    switch (eb) {
-    case 1: return launch_kernel(k_block<1>, dim3(grid), dim3(kBlockThreads), smem, st, pdl, a);
-    case 2: return launch_kernel(k_block<2>, dim3(grid), dim3(kBlockThreads), smem, st, pdl, a);
-    case 4: return launch_kernel(k_block<4>, dim3(grid), dim3(kBlockThreads), smem, st, pdl, a);
-    case 8: return launch_kernel(k_block<8>, dim3(grid), dim3(kBlockThreads), smem, st, pdl, a);
-    default: return launch_kernel(k_block<16>, dim3(grid), dim3(kBlockThreads), smem, st, pdl, a);
-    }
+    return launch_kernel(block_fn(eb, a.V), dim3(grid), dim3(kBlockThreads), block_smem_bytes(a),
+                         st, pdl, a);
 }
 
 }  // namespace tl

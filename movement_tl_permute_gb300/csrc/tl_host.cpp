@@ -881,8 +881,8 @@ void plan_panel(Plan* p, int tile_bytes, int rows) {
 // axes is tried, with at most one axis split into chunks so the tile fits its bytes
 // (the last axis of each run it belongs to, so both runs stay dense); the tile whose
 // shorter run (capped at 512 bytes) is longest wins, then the bigger tile.  The
-// shared-memory pitch of the src runs is chosen by replaying the store walk's warp
-// reads on the bank model (hardware mode).
+// shared-memory strides of the src-run index axes are chosen by replaying the store
+// walk's warp reads on the bank model (hardware mode).
 namespace {
 
 // mixed-radix digits of x over `n` extents (innermost first)
@@ -893,52 +893,109 @@ void digits(int64_t x, int n, const int64_t* ext, int64_t* d) {
     }
 }
 
-// Stage offset in bytes of the element at dst-run position i of dst run j (mis 0):
-// the store walk's read, as the block kernel's tables compute it.
-int64_t block_stage_off(const BlockPlan& b, int eb, int pitch, int64_t i, int64_t j) {
-    int64_t coord[kBlockAxes] = {};
-    int64_t e[kBlockAxes], d[kBlockAxes];
-    for (int k = 0; k < b.nd; ++k) e[k] = b.tile[b.dax[k]];
-    digits(i, b.nd, e, d);
-    for (int k = 0; k < b.nd; ++k) coord[b.dax[k]] = d[k];
-    for (int k = 0; k < b.nj; ++k) e[k] = b.tile[b.jax[k]];
-    digits(j, b.nj, e, d);
-    for (int k = 0; k < b.nj; ++k) coord[b.jax[k]] = d[k];
-    int64_t sp = 0, r = 0, rw = 1, soff = 0;
-    for (int k = 0; k < b.ns; ++k) sp += coord[b.sax[k]] * b.ss[b.sax[k]];
+// Stage layout of a block tile (byte strides b.sq, stage bytes b.stage): the src-run
+// axes at their src byte strides; the src-run index axes, innermost first, each at
+// the smallest stride that is at least the span of the runs inside it and congruent
+// to its src byte stride modulo 16, plus 16 * extra[k].  A run's copy covers the
+// aligned 16-byte blocks around it, up to 15 bytes past either end, so one run spans
+// Ls * eb + 30 bytes; a 16-byte lead holds the tile origin's offset inside its block.
+// An element thus sits at the same offset modulo 16 in the stage as in src.
+int64_t block_layout(BlockPlan& b, int eb, const int* extra) {
+    for (int k = 0; k < b.ns; ++k) b.sq[b.sax[k]] = b.ss[b.sax[k]] * eb;
+    int64_t span = b.Ls * eb + 30;
     for (int k = 0; k < b.nr; ++k) {
-        r += coord[b.rax[k]] * rw;
-        rw *= b.tile[b.rax[k]];
-        soff += coord[b.rax[k]] * b.ss[b.rax[k]];
+        const int q = b.rax[k];
+        const int64_t want = (b.ss[q] * eb) & 15;
+        const int64_t P = span + ((want - span) & 15) + 16 * (extra ? extra[k] : 0);
+        b.sq[q] = P;
+        span += (b.tile[q] - 1) * P;
     }
-    // each src run sits at its own offset inside its first 16-byte block (the tile's
-    // base taken as aligned)
-    return r * pitch + ((soff * eb) & 15) + sp * eb;
+    b.stage = (16 + span + 15) & ~int64_t(15);
+    b.pitch = (int)(b.nr > 0 ? b.sq[b.rax[0]] : b.stage);
+    return b.stage;
 }
 
-int block_pitch(const BlockPlan& b, int eb) {
-    const int base = (int)((b.Ls * eb + 15 + 15) / 16 * 16);
-    const int64_t n = b.Ld * b.Rd;
-    int best = base;
-    int64_t best_cost = -1;
-    for (int extra = 0; extra < 8; ++extra) {
-        const int P = base + 16 * extra;
-        if (b.Rs * P > 48 * 1024) break;
-        int64_t cost = 0;
-        for (int64_t w = 0; w < 64 && 32 * w < n; ++w) {
+// Cost of the store walk under the layout in b, in L1 wavefronts per element: the
+// stage reads (each warp-wide read takes as many wavefronts as its worst bank
+// conflict, replayed on the bank model in hardware mode over the first warp-steps)
+// plus the 128-byte lines each warp-wide store touches.  r_lg == 0: a warp takes 32
+// consecutive pieces (b.vec dst elements each) in dst order, on into the next dst run;
+// r_lg > 0: 32 >> r_lg consecutive pieces in each of 1 << r_lg consecutive dst runs,
+// lanes without a piece counted as work lost.
+double block_drain_cost(const BlockPlan& b, int eb) {
+    int64_t ta[kBlockMaxLd], tb[kBlockMaxRuns];
+    auto fill = [&](int64_t* t, int64_t n, int na, const int* ax) {
+        for (int64_t x = 0; x < n; ++x) {
+            int64_t r = x, o = 0;
+            for (int k = 0; k < na; ++k) {
+                const int64_t e = b.tile[ax[k]];
+                o += (r % e) * b.sq[ax[k]];
+                r /= e;
+            }
+            t[x] = o;
+        }
+    };
+    fill(ta, b.Ld, b.nd, b.dax);
+    fill(tb, b.Rd, b.nj, b.jax);
+    const int64_t V = b.vec, W = b.Ld / V, R = int64_t(1) << b.r_lg, PW = 32 / R;
+    const bool flat = b.r_lg == 0;
+    const int64_t GW = flat ? 1 : (W + PW - 1) / PW, GR = flat ? 1 : (b.Rd + R - 1) / R;
+    const int64_t units = flat ? (W * b.Rd + 31) / 32 : GW * GR;
+    const int64_t steps = std::min<int64_t>(units, std::max<int64_t>(1, 64 / V));
+    int64_t waves = 0;
+    for (int64_t g = 0; g < steps; ++g)
+        for (int64_t k = 0; k < V; ++k) {
             int64_t o[32];
             for (int l = 0; l < 32; ++l) {
-                const int64_t f = 32 * w + l;
-                o[l] = f < n ? block_stage_off(b, eb, P, f % b.Ld, f / b.Ld) / eb : -1;
+                int64_t v, j;
+                if (flat) {
+                    v = (32 * g + l) % W;
+                    j = (32 * g + l) / W;
+                } else {
+                    v = (g % GW) * PW + l % PW;
+                    j = (g / GW) * R + l / PW;
+                }
+                o[l] = v < W && j < b.Rd ? (ta[v * V + k] + tb[j]) / eb : -1;
             }
-            cost += bank_degree(32, o, eb, true);
+            waves += bank_degree(32, o, eb, true);
         }
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = P;
-        }
+    const int64_t seg = (flat ? 32 : PW) * V * eb;           // bytes of a run segment
+    const double lines = (double)(flat ? 1 : R) * (double)((seg + 127) / 128);
+    const double lanes = flat ? 1.0 : (double)(W * b.Rd) / (double)(GW * PW * GR * R);
+    return ((double)waves / (double)steps + lines) / (32.0 * (double)V * lanes);
+}
+
+// The store walk and stage layout the cost above finds cheapest: runs per warp-step
+// 1 .. 32 and extra 16-byte steps for the two innermost src-run index axes (stages of
+// at most 48 KiB); the fewest runs per warp-step (the longest stores) within 3 % of
+// the best.
+void block_search(BlockPlan& b, int eb) {
+    int best_r = 0, best_e[6][2] = {};
+    double best_c[6];
+    const int n0 = b.nr > 0 ? 8 : 1, n1 = b.nr > 1 ? 8 : 1;
+    for (int r = 0; r <= 5; ++r) {
+        best_c[r] = -1;
+        b.r_lg = r;
+        for (int e0 = 0; e0 < n0; ++e0)
+            for (int e1 = 0; e1 < n1; ++e1) {
+                const int extra[kBlockAxes] = {e0, e1, 0, 0};
+                if (block_layout(b, eb, extra) > 48 * 1024) continue;
+                const double c = block_drain_cost(b, eb);
+                if (best_c[r] < 0 || c < best_c[r]) {
+                    best_c[r] = c;
+                    best_e[r][0] = e0;
+                    best_e[r][1] = e1;
+                }
+            }
     }
-    return best;
+    double lo = -1;
+    for (int r = 0; r <= 5; ++r)
+        if (best_c[r] >= 0 && (lo < 0 || best_c[r] < lo)) lo = best_c[r];
+    for (int r = 5; r >= 0; --r)
+        if (best_c[r] >= 0 && best_c[r] <= 1.03 * lo) best_r = r;
+    b.r_lg = best_r;
+    const int extra[kBlockAxes] = {best_e[best_r][0], best_e[best_r][1], 0, 0};
+    block_layout(b, eb, extra);
 }
 
 }  // namespace
@@ -946,9 +1003,9 @@ int block_pitch(const BlockPlan& b, int eb) {
 int64_t plan_block(Plan* p, int64_t tile_bytes) {
     const Axes& s = p->sorted;
     const int n = s.n, eb = p->eb;
-    // measured on GB300 (12^8 permutes, 9^8 permutes): 12 KiB tiles for 1- and 2-byte
-    // elements (u16 1.92 -> 2.08, u8 0.66 -> 1.24 TB/s against 32 KiB), 32 KiB for
-    // wider ones (fp32 2.59 at 12 KiB -> 2.89 TB/s)
+    // measured on GB300 (12^7 and 12^8 permutes, 9^8 permutes): 12 KiB tiles for 1- and
+    // 2-byte elements (12^8 u16 5.6 TB/s against 4.3 at 32 KiB, u8 3.6 against 2.4),
+    // 32 KiB for wider ones (9^8 fp32 5.7 TB/s against 4.3 at 12 KiB)
     if (tile_bytes <= 0) tile_bytes = eb <= 2 ? 12288 : 32768;
     if (n < 2) return 0;
     // the dense chains from src stride 1 and from dst stride 1
@@ -1055,7 +1112,7 @@ int64_t plan_block(Plan* p, int64_t tile_bytes) {
                 b.Rs = tot / b.Ls;
                 b.Rd = tot / b.Ld;
                 if (b.Ld > kBlockMaxLd || b.Rd > kBlockMaxRuns || b.Rs > kBlockMaxRuns) continue;
-                if (b.Ls >= (1 << 24) || b.Rs * ((b.Ls * eb + 30) / 16 * 16) > 48 * 1024) continue;
+                if (b.Ls >= (1 << 24) || block_layout(b, eb, nullptr) > 48 * 1024) continue;
                 const int64_t run = std::min(b.Ls, b.Ld) * eb;
                 const int64_t score = std::min<int64_t>(run, 512) * (int64_t(1) << 32) + tot;
                 if (score > best_score) {
@@ -1076,7 +1133,30 @@ int64_t plan_block(Plan* p, int64_t tile_bytes) {
         bt.ext[bt.n] = s.ext[q]; bt.ss[bt.n] = s.ss[q]; bt.ds[bt.n] = s.ds[q]; ++bt.n;
     }
     best.batch = bt;
-    best.pitch = block_pitch(best, eb);
+    // pieces of vec dst elements stored as one vector: whole pieces in every dst run
+    // (and in its part inside a chunk), each piece aligned in dst
+    auto in_dst_run = [&](int q) {
+        for (int k = 0; k < best.nd; ++k)
+            if (best.dax[k] == q) return true;
+        return false;
+    };
+    auto vec_ok = [&](int64_t v) {
+        if (best.Ld % v != 0 || p->dst_mis16 % (v * eb) != 0) return false;
+        if (best.chunk >= 0) {
+            const int c = best.chunk;
+            if (in_dst_run(c) && (best.Ld / best.tile[c]) % v != 0) return false;
+            if ((best.tile[c] * best.ds[c]) % v != 0) return false;
+        }
+        for (int k = 0; k < best.nj; ++k)
+            if (best.ds[best.jax[k]] % v != 0) return false;
+        for (int q = 0; q < bt.n; ++q)
+            if (bt.ds[q] % v != 0) return false;
+        return true;
+    };
+    int v = eb >= 16 ? 1 : 16 / eb;
+    while (v > 1 && !vec_ok(v)) v >>= 1;
+    best.vec = v;
+    block_search(best, eb);
     int64_t tiles = 1;
     for (int q = 0; q < best.nt; ++q) tiles *= (best.ext[q] + best.tile[q] - 1) / best.tile[q];
     for (int q = 0; q < bt.n; ++q) tiles *= bt.ext[q];
@@ -1225,16 +1305,14 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         plan_panel(&q, 0);
     };
     // The block tile takes layouts of canonical rank 3 or more whose panel tile would
-    // move short runs on one side and store them element by element (high-rank
-    // permutes of short axes) when its own shorter run is 128 bytes or more and at
-    // least as long.
+    // move short runs on one side (high-rank permutes of short axes) when its own
+    // shorter run is 128 bytes or more and at least as long.
     if (forced == TL_PATH_AUTO && !ranges_meet && srt.n >= 3 && !casting &&
         (path == TL_PATH_PANEL || path == TL_PATH_GENERIC)) {
         Plan q = p;
         const int64_t brun = plan_block(&q);
         if (brun >= 128) {
             int64_t prun = 0;
-            bool r_vec = false, r_run = false;
             if (path == TL_PATH_PANEL) {
                 Plan r = p;
                 setup_panel(r);
@@ -1245,16 +1323,11 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
                 const int64_t srun = packed ? ta * tb * eb : ta * eb;
                 const int64_t drun = r.panel_run ? ta * tb * eb : tb * eb;
                 prun = std::min(srun, drun);
-                r_vec = r.panel_vec;
-                r_run = r.panel_run;
             }
-            // (a panel tile stored as 16-byte dst runs keeps the panel: the block
-            // kernel stores element by element; measured on GB300, reversed 8^8 / 10^8
-            // fp32 and 6-D fp32 permutes with 16-byte panel runs ran 0.6-0.8x as
-            // blocks, while 9^8 fp32 permutes whose panel tiles store elements ran
-            // 1.2-1.4x faster as blocks at equal runs)
-            const bool vec = path == TL_PATH_PANEL && (r_vec || r_run);
-            if (!vec && brun >= prun) path = TL_PATH_BLOCK;
+            // (measured on GB300 against panel tiles stored as 16-byte dst runs:
+            // reversed 8^8 fp32 1.15x as blocks, 12^8 fp64 in the interleaved order
+            // 1.5x, reversed 10^8 fp32 equal at a shorter block run)
+            if (brun >= prun) path = TL_PATH_BLOCK;
         }
     }
     p.path = path;
@@ -1311,7 +1384,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         setup_panel(p);
     } else if (path == TL_PATH_BLOCK) {
         plan_block(&p);
-        p.vec_bytes = eb;
+        p.vec_bytes = p.blk.vec * eb;
     } else if (path == TL_PATH_COLS) {
         p.vec_bytes = 16;
         p.tile_cols = (int)p.ext_a;          // elements per pixel

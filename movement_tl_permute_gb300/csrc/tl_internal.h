@@ -43,7 +43,12 @@ struct BlockPlan {
     int nr = 0, rax[kBlockAxes] = {};  // src-run index axes
     int nj = 0, jax[kBlockAxes] = {};  // dst-run index axes
     int64_t Ls = 0, Rs = 0, Ld = 0, Rd = 0;   // run lengths and counts of a full tile
-    int pitch = 0;                     // shared-memory bytes per src run
+    int64_t sq[kBlockAxes] = {};       // shared-memory byte stride of each axis of T
+    int64_t stage = 0;                 // shared-memory bytes of one ring stage
+    int pitch = 0;                     // sq of the innermost src-run index axis (the
+                                       // distance between neighbouring src runs)
+    int vec = 1;                       // dst elements per store (dst runs permitting)
+    int r_lg = 0;                      // a store warp-step covers 1 << r_lg dst runs
     Axes batch;                        // the axes outside T (dst order, outermost first)
 };
 

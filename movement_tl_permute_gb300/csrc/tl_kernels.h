@@ -245,46 +245,53 @@ cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStr
 
 // ---------------------------------------------------------------- block
 // A tile of up to four axes (T) that is a few long contiguous runs on both sides.
-// Per-CTA tables (built once in shared memory) map a dst-run position i and a dst
-// run j to the src run and the position inside it: the element of (j, i) sits in the
-// stage at runbase[r_i + r_j] + (p_i + p_j) * EB, and in dst at dof + dst_j + i.
-constexpr int kBlockThreads = 256;
+// Every axis of T has a shared-memory byte stride (a src-run axis its src byte
+// stride; a src-run index axis one congruent to its src byte stride modulo 16), so
+// that each src run is one bulk copy of its 16-byte blocks and per-CTA tables (built
+// once in shared memory) give the stage offset of the element at dst-run position i
+// of dst run j as TA[i] + TB[j], and its dst offset as dof + dst_j + i.
+constexpr int kBlockConsumerWarps = 8;
+constexpr int kBlockThreads = 32 * (kBlockConsumerWarps + 1);   // + one producer warp
 constexpr int kBlockStages = 3;
+constexpr int kBlockCtasPerSm = 4;          // launch bounds: at most 56 registers a thread
 constexpr int kBlockMaxSmem = 200 * 1024;   // stages of at most 48 KiB + the tables
 struct BlockArgs {
     const uint8_t* src;
     uint8_t* dst;
     uint64_t* cta_times;         // measurement: per-CTA start / finish (or null)
-    // tables: the axes whose digits make i (dst-run axes), j (dst-run index axes)
-    // and r (src-run index axes), innermost first, with the tile's extents; for
-    // each, its src-run position stride (elements, 0 off the src run), its src-run
-    // index stride (0 on the src run), whether it is the chunked axis, and (j, r)
-    // its dst and src strides
+    int32_t* status;             // first error of the launch (or null)
+    uint64_t timeout_ns;         // bound of every mbarrier wait
+    int32_t drop_load;           // test hook: the first copy of the first tile is skipped
+    // the axes whose digits make i (dst-run axes), j (dst-run index axes) and r
+    // (src-run index axes), innermost first, with the tile's extents and each axis's
+    // shared-memory byte stride; (j) dst strides, (r) src byte strides
     int32_t nd, nj, nr;
     int32_t dext[4], jext[4], rext[4];
-    int64_t dsp[4], jsp[4];
-    int32_t drs[4], jrs[4];
-    int32_t dck, jck, rck;       // index of the chunked axis in each list (-1: none)
-    int64_t jds[4], rss[4];
+    uint32_t dsq[4], jsq[4], rsq[4];
+    int64_t jds[4], rsb[4];
+    int32_t jck, rck;            // index of the chunked axis in the j / r lists (-1: none)
+    int32_t ld_chunk, ls_chunk;  // the chunked axis is the dst run's / src run's last axis
     int32_t Ld, Rd, Rs, Ls;      // run lengths and counts of a full tile
-    int32_t ls_inner;            // src run length without the chunked axis (when it is
-                                 // the src run's last axis; else Ls)
-    int32_t pitch, nblk, stage_bytes;
+    int32_t ld_inner, ls_inner;  // run lengths without the chunked axis
+    int32_t V, W;                // store pieces: V elements, W per dst run
+    // a consumer warp-step: a group of 32 >> r_lg pieces in each of 1 << r_lg dst runs;
+    // GW x GR groups per tile; one step of the consumer warps advances dgw, dgr groups
+    int32_t r_lg, GW, GR, dgw, dgr;
+    int32_t stage_bytes;
     int32_t table_off;           // byte offset of the tables in dynamic shared memory
     // the chunked axis: extent, tile extent, chunks, strides
     int64_t c_ext, c_ss, c_ds, nc;
     int32_t c_k, use32;
     // tiles: chunk index fastest, then the batch axes (innermost first)
     int32_t nb;
-    int32_t umis;                // every src run at the same offset inside its 16-byte
-                                 // block (run and tile strides multiples of 16 bytes)
     int64_t tiles;
     int64_t bext[TL_MAX_DIMS], bss[TL_MAX_DIMS], bds[TL_MAX_DIMS];
-    dev::DivU32 d_nc, d_Ld, d_nblk;
+    dev::DivU32 d_nc;
     dev::DivU32 d_bext[TL_MAX_DIMS];
 };
 int block_smem_bytes(const BlockArgs& a);
-const void* block_kernel(int eb);
+// the kernel for elem_bytes eb storing v elements per step (v in 1 .. 16 / eb)
+const void* block_kernel(int eb, int v);
 cudaError_t launch_block(int eb, const BlockArgs& a, int grid, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- warp

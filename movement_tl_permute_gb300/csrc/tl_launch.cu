@@ -151,10 +151,11 @@ int get_device_info(DevInfo* out) {
                                               tile_smem_bytes(kTileRingBytes / (128 * 128),
                                                               128)) != cudaSuccess)
                 return TL_ERR_CUDA;
-            if (cudaFuncSetAttribute(block_kernel(1 << i),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kBlockMaxSmem) != cudaSuccess)
-                return TL_ERR_CUDA;
+            for (int v = 1; v <= (16 >> i); v <<= 1)
+                if (cudaFuncSetAttribute(block_kernel(1 << i, v),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kBlockMaxSmem) != cudaSuccess)
+                    return TL_ERR_CUDA;
             if (panel_tma_kernel(1 << i) &&
                 cudaFuncSetAttribute(panel_tma_kernel(1 << i),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -310,53 +311,50 @@ BlockArgs block_args(const Plan& p) {
     const BlockPlan& b = p.blk;
     const int eb = p.eb;
     BlockArgs a{};
-    int64_t rw[kBlockAxes] = {};           // src-run index weight of each axis of T
-    {
-        int64_t w = 1;
-        for (int k = 0; k < b.nr; ++k) {
-            rw[b.rax[k]] = w;
-            w *= b.tile[b.rax[k]];
-        }
-    }
-    auto in_srun = [&](int q) {
-        for (int k = 0; k < b.ns; ++k)
-            if (b.sax[k] == q) return true;
+    auto in_list = [](const int* l, int n, int q) {
+        for (int k = 0; k < n; ++k)
+            if (l[k] == q) return true;
         return false;
     };
     a.nd = b.nd;
     a.nj = b.nj;
     a.nr = b.nr;
-    a.dck = a.jck = a.rck = -1;
+    a.jck = a.rck = -1;
     for (int k = 0; k < b.nd; ++k) {
         const int q = b.dax[k];
         a.dext[k] = (int32_t)b.tile[q];
-        a.dsp[k] = in_srun(q) ? b.ss[q] : 0;
-        a.drs[k] = (int32_t)rw[q];
-        if (q == b.chunk) a.dck = k;
+        a.dsq[k] = (uint32_t)b.sq[q];
     }
     for (int k = 0; k < b.nj; ++k) {
         const int q = b.jax[k];
         a.jext[k] = (int32_t)b.tile[q];
-        a.jsp[k] = in_srun(q) ? b.ss[q] : 0;
-        a.jrs[k] = (int32_t)rw[q];
+        a.jsq[k] = (uint32_t)b.sq[q];
         a.jds[k] = b.ds[q];
         if (q == b.chunk) a.jck = k;
     }
     for (int k = 0; k < b.nr; ++k) {
         const int q = b.rax[k];
         a.rext[k] = (int32_t)b.tile[q];
-        a.rss[k] = b.ss[q];
+        a.rsq[k] = (uint32_t)b.sq[q];
+        a.rsb[k] = b.ss[q] * eb;
         if (q == b.chunk) a.rck = k;
     }
     a.Ld = (int32_t)b.Ld;
     a.Rd = (int32_t)b.Rd;
     a.Rs = (int32_t)b.Rs;
     a.Ls = (int32_t)b.Ls;
-    a.ls_inner = a.Ls;
-    if (b.chunk >= 0 && in_srun(b.chunk)) a.ls_inner = (int32_t)(b.Ls / b.tile[b.chunk]);
-    a.pitch = b.pitch;
-    a.nblk = (int32_t)((b.Ls * eb + 30) / 16);
-    a.stage_bytes = (int32_t)(b.Rs * b.pitch);
+    a.ld_chunk = b.chunk >= 0 && in_list(b.dax, b.nd, b.chunk) ? 1 : 0;
+    a.ls_chunk = b.chunk >= 0 && in_list(b.sax, b.ns, b.chunk) ? 1 : 0;
+    a.ld_inner = a.ld_chunk ? (int32_t)(b.Ld / b.tile[b.chunk]) : a.Ld;
+    a.ls_inner = a.ls_chunk ? (int32_t)(b.Ls / b.tile[b.chunk]) : a.Ls;
+    a.V = b.vec;
+    a.W = a.Ld / a.V;
+    a.r_lg = b.r_lg;
+    a.GW = (a.W + (32 >> a.r_lg) - 1) / (32 >> a.r_lg);
+    a.GR = (a.Rd + (1 << a.r_lg) - 1) >> a.r_lg;
+    a.dgw = kBlockConsumerWarps % a.GW;
+    a.dgr = kBlockConsumerWarps / a.GW;
+    a.stage_bytes = (int32_t)b.stage;
     a.table_off = kBlockStages * a.stage_bytes;
     if (b.chunk >= 0) {
         const int q = b.chunk;
@@ -379,14 +377,7 @@ BlockArgs block_args(const Plan& p) {
     }
     a.tiles = p.tiles;
     a.use32 = p.tiles < (1LL << 32) ? 1 : 0;
-    // every src run of a tile at the same offset inside its 16-byte block: the
-    // strides between runs are multiples of 16 bytes
-    bool um = true;
-    for (int k = 0; k < a.nr; ++k) um = um && (a.rss[k] * eb) % 16 == 0;
-    a.umis = um ? 1 : 0;
     a.d_nc = dev::make_divu32((uint32_t)a.nc);
-    a.d_Ld = dev::make_divu32((uint32_t)a.Ld);
-    a.d_nblk = dev::make_divu32((uint32_t)a.nblk);
     if (a.use32)
         for (int i = 0; i < a.nb; ++i) a.d_bext[i] = dev::make_divu32((uint32_t)a.bext[i]);
     return a;
@@ -458,9 +449,10 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         l.block = kBlockThreads;
         l.smem = block_smem_bytes(block_args(p));
         if (sms) {
-            // resident CTAs by shared memory (228 KiB per SM, 1 KiB reserved per CTA)
-            int per_sm = 233472 / (l.smem + 1024);
-            per_sm = per_sm < 1 ? 1 : per_sm > 8 ? 8 : per_sm;
+            // resident CTAs by shared memory (228 KiB per SM, 1 KiB reserved per CTA,
+            // plus the barriers and tile records) and by the kernel's launch bounds
+            int per_sm = 233472 / (l.smem + 1024 + 128);
+            per_sm = per_sm < 1 ? 1 : per_sm > kBlockCtasPerSm ? kBlockCtasPerSm : per_sm;
             l.grid = cap_grid(p.tiles, sms * per_sm, max_ctas);
         }
         break;
@@ -921,6 +913,10 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         a.src = s8;
         a.dst = d8;
         a.cta_times = opts ? opts->cta_times : nullptr;
+        a.status = opts ? opts->dev_status : nullptr;
+        const bool drop = (flags & TL_FLAG_TEST_DROP_HANDOFF) != 0;
+        a.timeout_ns = drop ? kTestTimeoutNs : kDefaultTimeoutNs;
+        a.drop_load = drop ? 1 : 0;
         err = launch_block(eb, a, l.grid, st, pdl);
         break;
     }
@@ -1048,6 +1044,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     info.panel_vec = p.panel_vec ? 1 : p.panel_run ? 2 : p.panel_words ? 3 : 0;
     info.panel_wrot = p.panel_wrot_s | (p.panel_wrot_m << 8);
     info.panel_a1 = (int32_t)p.panel_a1;
+    info.block_runs = p.path == TL_PATH_BLOCK ? 1 << p.blk.r_lg : 0;
     info.tiles = p.tiles;
     const Launch& l = pr.l;
     info.grid = l.grid;

@@ -18,7 +18,7 @@ from oracle import layout_ref as L
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-PATHS = ["auto", "generic", "chunk", "tile", "rows", "warp", "cluster", "panel", "cols"]
+PATHS = ["auto", "generic", "chunk", "tile", "rows", "warp", "cluster", "panel", "cols", "block"]
 CANARY = 0x3C
 
 

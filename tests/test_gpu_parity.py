@@ -479,6 +479,27 @@ def test_block_path_named_layouts(eb):
         check(shape, ss, ds, eb, "auto", seed=460 + i, src_off=1, dst_off=1)
 
 
+@pytest.mark.parametrize("eb", WIDTHS)
+def test_block_store_walks(eb):
+    """Both store walks of the block kernel -- consecutive pieces in dst order, and
+    groups of pieces across 2-32 dst runs -- with pieces of several elements stored as
+    one vector (aligned dst) and of one element (dst one element off), on layouts whose
+    bank costs pick each."""
+    layouts = (((12,) * 5, (4, 2, 0, 1, 3)), ((12,) * 6, (5, 3, 1, 0, 2, 4)),
+               ((8,) * 6, (5, 4, 3, 2, 1, 0)), ((16,) * 5, (4, 3, 2, 1, 0)),
+               ((7, 9, 5, 11, 6), (3, 0, 4, 2, 1)))
+    runs, vecs = set(), set()
+    for i, (shape, perm) in enumerate(layouts):
+        ss, ds = perm_layouts(shape, perm)
+        plan = tl.tl_plan(1 << 32, 1 << 44, shape, ss, ds, eb, path="block")
+        runs.add(plan["block_runs"])
+        vecs.add(plan["vec_bytes"])
+        check(shape, ss, ds, eb, "block", seed=470 + i)
+        check(shape, ss, ds, eb, "block", seed=480 + i, dst_off=1)
+    assert 1 in runs and max(runs) > 1, runs
+    assert 16 in vecs, vecs
+
+
 def test_per_cta_times_are_recorded_without_changing_the_result():
     """The measurement option: the tile, rows, panel and block kernels write each
     CTA's start and finish time, every CTA of the grid tl_plan reports once, and the
@@ -692,6 +713,26 @@ def test_panel_tma_timeout_is_reported_and_context_survives():
     assert int(status.item()) == -12          # TL_ERR_TIMEOUT
     status.zero_()
     check(shape, ss, ds, 2, "panel", seed=19, dev_status=status.data_ptr())
+    assert int(status.item()) == 0
+
+
+def test_block_copy_timeout_is_reported_and_context_survives():
+    """A block tile whose src-run copy never lands (the test hook skips the first
+    copy of each CTA's first tile): the consumers' bounded waits expire, the status
+    word reads TL_ERR_TIMEOUT, and the context still runs the same permute correctly."""
+    shape = (12,) * 5
+    ss, ds = perm_layouts(shape, (4, 2, 0, 1, 3))
+    assert tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, 2, path="block")["path"] == "block"
+    n = int(np.prod(shape))
+    src = torch.zeros(n, dtype=torch.int16, device="cuda")
+    dst = torch.zeros(n, dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    tl.permute(src, dst, shape, ss, ds, path="block", flags=tl.TL_FLAG_TEST_DROP_HANDOFF,
+               dev_status=status.data_ptr())
+    torch.cuda.synchronize()
+    assert int(status.item()) == -12          # TL_ERR_TIMEOUT
+    status.zero_()
+    check(shape, ss, ds, 2, "block", seed=23, dev_status=status.data_ptr())
     assert int(status.item()) == 0
 
 

@@ -228,7 +228,8 @@ typedef struct tl_permute_opts {
                              default: the whole extent) */
     int32_t tile_stages;  /* shared-memory ring depth: 2..12 (tile, 128-row tiles),
                              2..6 (tile, 256-row tiles); cluster: staging ring, 1..8 */
-    int32_t tile_ctas_per_sm;  /* resident CTAs per SM the grid is sized for */
+    int32_t tile_ctas_per_sm;  /* resident CTAs per SM the grid is sized for (block
+                                  path: at most this many, 1..4) */
     int32_t tile_l2_promotion; /* L2 fill size of the TMA loads (tile path, panel phase
                                   maps): 64, 128, 256, or -1 = none */
     int32_t tile_rows;    /* tile height in rows of the dst-contiguous axis: 128 or 256
@@ -236,7 +237,10 @@ typedef struct tl_permute_opts {
                              plane extents exceed 16); other values select the default */
     int32_t cluster_recv_stages; /* cluster: receive ring depth, 1..8 (staging + receive
                                     slots at most 12) */
-    int32_t cluster_consumer_warps; /* cluster: consumer warps per CTA, 4 or 8 */
+    int32_t cluster_consumer_warps; /* cluster: consumer warps per CTA, 4 or 8; block:
+                                       at most this many, 1..17 (by default as many as
+                                       the SM's registers allow at the CTAs per SM its
+                                       shared memory holds) */
     int32_t panel_tile_kib;       /* panel path: tile size, 4..48 KiB (default 32, or 24
                                      with an extent of 16 or less); block path: its
                                      tile's bytes */

@@ -187,11 +187,15 @@ __device__ __forceinline__ void load_offsets(uint32_t ta, uint32_t v, uint32_t W
 }
 
 template <int EB, int V>
-__global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const BlockArgs a) {
+__global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ __align__(8) uint64_t full[kBlockStages];
     __shared__ __align__(8) uint64_t empty[kBlockStages];
     __shared__ __align__(16) uint4 info[kBlockStages];   // dof lo / hi, vc, origin mod 16
+    // bytes the copies of a whole tile move, by the tile origin's offset inside its
+    // 16-byte block
+    __shared__ uint32_t tot[16];
+    __shared__ int32_t landed[kBlockStages];
     const uint32_t sbase = dev::smem_addr(smem);
     const uint32_t stage = (uint32_t)a.stage_bytes;
     uint32_t* TA = reinterpret_cast<uint32_t*>(smem + a.table_off);       // [Ld, padded to 4]
@@ -200,7 +204,9 @@ __global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // the tables (from the arguments only: before the dependency wait)
-    for (int32_t i = threadIdx.x; i < a.Ld; i += kBlockThreads) {
+    if (threadIdx.x < 16) tot[threadIdx.x] = 0;
+    __syncthreads();
+    for (int32_t i = threadIdx.x; i < a.Ld; i += blockDim.x) {
         uint32_t x = (uint32_t)i, o = 0;
         for (int k = 0; k < a.nd; ++k) {
             const uint32_t q = x / (uint32_t)a.dext[k];
@@ -209,7 +215,7 @@ __global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const 
         }
         TA[ta_slot<V>((uint32_t)i, (uint32_t)a.W)] = o;
     }
-    for (int32_t j = threadIdx.x; j < a.Rd; j += kBlockThreads) {
+    for (int32_t j = threadIdx.x; j < a.Rd; j += blockDim.x) {
         uint32_t x = (uint32_t)j, o = 0, c = 0;
         int64_t dofs = 0;
         for (int k = 0; k < a.nj; ++k) {
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const 
         dofs *= EB;                                          // in bytes
         TB[j] = make_uint4(o, c, (uint32_t)(uint64_t)dofs, (uint32_t)((uint64_t)dofs >> 32));
     }
-    for (int32_t r = threadIdx.x; r < a.Rs; r += kBlockThreads) {
+    for (int32_t r = threadIdx.x; r < a.Rs; r += blockDim.x) {
         uint32_t x = (uint32_t)r, o = 0, c = 0;
         int64_t sb = 0;
         for (int k = 0; k < a.nr; ++k) {
@@ -235,11 +241,13 @@ __global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const 
             if (k == a.rck) c = dg;
         }
         TR[r] = make_uint4((uint32_t)(uint64_t)sb, (uint32_t)((uint64_t)sb >> 32), o, c);
+        for (uint32_t m = 0; m < 16; m += EB)
+            atomicAdd(&tot[m], (((m + (uint32_t)sb) & 15) + (uint32_t)a.Ls * EB + 15) & ~15u);
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kBlockStages; ++s) {
-            dev::mbar_init(&full[s], 32);                  // every producer lane arrives
-            dev::mbar_init(&empty[s], kBlockConsumerWarps);
+            dev::mbar_init(&full[s], 1);                   // producer lane 0 arrives
+            dev::mbar_init(&empty[s], (uint32_t)a.cw);
         }
         dev::fence_barrier_init();
     }
@@ -248,7 +256,7 @@ __global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const 
     dev::allow_dependent_launch();
     dev::cta_start(a.cta_times);
 
-    if (warp == kBlockConsumerWarps) {
+    if (warp == a.cw) {
         // ---------------- producer: one bulk copy per src run ---------------------------
         uint32_t issued = 0;
         bool ok = true;
@@ -269,27 +277,41 @@ __global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const 
             const uint32_t len = (uint32_t)(a.ls_chunk ? a.ls_inner * ti.vc : a.Ls) * EB;
             const uint32_t rlim = a.rck >= 0 ? ti.vc : 0xffffffffu;
             const uint32_t sdst = sbase + s * stage + 16 + tmis;
-            if (lane == 0)
+            uint32_t bytes;
+            if (ti.vc == (uint32_t)a.c_k) {
+                bytes = tot[tmis];                         // a whole tile: every run, in full
+            } else {
+                uint32_t mine = 0;
+                for (int32_t r = lane; r < a.Rs; r += 32) {
+                    const uint4 tr = lds128(dev::smem_addr(&TR[r]));
+                    if (tr.w < rlim) mine += (((tmis + tr.x) & 15) + len + 15) & ~15u;
+                }
+                bytes = __reduce_add_sync(0xffffffffu, mine);
+            }
+            if (lane == 0) {
                 dev::sts128(dev::smem_addr(&info[s]),
                             make_uint4((uint32_t)(uint64_t)ti.dof,
                                        (uint32_t)((uint64_t)ti.dof >> 32), ti.vc, tmis));
-            uint32_t bytes = 0;
-            for (int32_t r = lane; r < a.Rs; r += 32) {
-                const uint4 tr = lds128(dev::smem_addr(&TR[r]));
-                if (tr.w >= rlim) continue;
-                const uintptr_t g = base + (uintptr_t)((uint64_t)tr.x | ((uint64_t)tr.y << 32));
-                bytes += ((uint32_t)(g & 15) + len + 15) & ~15u;
+                dev::mbar_arrive_expect_tx(&full[s], bytes);      // before any copy lands
             }
             __syncwarp();
-            dev::mbar_arrive_expect_tx(&full[s], bytes);
             const uint32_t bar = dev::smem_addr(&full[s]);
-            for (int32_t r = lane; r < a.Rs; r += 32) {
-                const uint4 tr = lds128(dev::smem_addr(&TR[r]));
-                if (tr.w >= rlim) continue;
-                if (a.drop_load && issued == 0 && r == 0) continue;   // test hook: the wait expires
-                const uintptr_t g = base + (uintptr_t)((uint64_t)tr.x | ((uint64_t)tr.y << 32));
-                const uint32_t mis = (uint32_t)(g & 15);
-                bulk_load(sdst + tr.z - mis, g - mis, (mis + len + 15) & ~15u, bar);
+            // the next run's table entry is read before this run's copy is issued
+            int32_t r = lane;
+            uint4 tr = make_uint4(0, 0, 0, 0);
+            if (r < a.Rs) tr = lds128(dev::smem_addr(&TR[r]));
+            while (r < a.Rs) {
+                const int32_t rn = r + 32;
+                uint4 trn = make_uint4(0, 0, 0, 0);
+                if (rn < a.Rs) trn = lds128(dev::smem_addr(&TR[rn]));
+                const bool drop = a.drop_load && issued == 0 && r == 0;   // test hook
+                if (tr.w < rlim && !drop) {
+                    const uintptr_t g = base + (uintptr_t)((uint64_t)tr.x | ((uint64_t)tr.y << 32));
+                    const uint32_t mis = (uint32_t)(g & 15);
+                    bulk_load(sdst + tr.z - mis, g - mis, (mis + len + 15) & ~15u, bar);
+                }
+                r = rn;
+                tr = trn;
             }
         }
         if (!ok && lane == 0) dev::report(a.status, TL_ERR_TIMEOUT);
@@ -309,8 +331,8 @@ __global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const 
     // takes a group of 32 >> r_lg consecutive pieces in each of 1 << r_lg consecutive
     // dst runs, whose stage reads spread over more banks (lane = (pl, rl)).
     const uint32_t W = (uint32_t)a.W, Rd = (uint32_t)a.Rd;
-    const uint32_t GW = (uint32_t)a.GW, GR = (uint32_t)a.GR;
-    const uint32_t dgw = (uint32_t)a.dgw, dgr = (uint32_t)a.dgr;
+    const uint32_t GW = (uint32_t)a.GW, GR = (uint32_t)a.GR, cw = (uint32_t)a.cw;
+    const uint32_t dgw = cw % GW, dgr = cw / GW;            // one step of the consumer warps
     const uint32_t pw_lg = 5 - (uint32_t)a.r_lg;
     const uint32_t pl = (uint32_t)lane & ((1u << pw_lg) - 1), rl = (uint32_t)lane >> pw_lg;
     const uint32_t ct = threadIdx.x;                        // 0 .. consumer threads - 1
@@ -318,7 +340,14 @@ __global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const 
     uint32_t it = 0;
     for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++it) {
         const uint32_t use = it / kBlockStages, s = it - use * kBlockStages;
-        if (!dev::mbar_wait(&full[s], use & 1, a.timeout_ns)) {
+        // consumer warp 0 waits for the stage; the others sleep on a named barrier and
+        // then take the completed phase themselves (one try, for its acquire)
+        if (warp == 0) {
+            const bool got = dev::mbar_wait(&full[s], use & 1, a.timeout_ns);
+            if (lane == 0) landed[s] = got ? 1 : 0;
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(32 * cw) : "memory");
+        if (!landed[s] || !dev::mbar_wait(&full[s], use & 1, a.timeout_ns)) {
             if (lane == 0) dev::report(a.status, TL_ERR_TIMEOUT);
             break;
         }
@@ -341,7 +370,7 @@ __global__ void __launch_bounds__(kBlockThreads, kBlockCtasPerSm) k_block(const 
             // the last one, unstored), so that the table and stage reads of both are in
             // flight together (measured on GB300: 9^8 fp32 permutes 4.6 -> 5.7 TB/s;
             // wider pieces ran 0.8-1.0x as fast two at a time)
-            const uint32_t step = 32 * kBlockConsumerWarps;
+            const uint32_t step = 32 * cw;
             const uint32_t dv = step % W, dj = step / W;
             uint32_t v = ct % W, j = ct / W;
             while (j < Rd) {
@@ -458,7 +487,7 @@ int block_smem_bytes(const BlockArgs& a) {
 const void* block_kernel(int eb, int v) { return reinterpret_cast<const void*>(block_fn(eb, v)); }
 
 cudaError_t launch_block(int eb, const BlockArgs& a, int grid, cudaStream_t st, bool pdl) {
-    return launch_kernel(block_fn(eb, a.V), dim3(grid), dim3(kBlockThreads), block_smem_bytes(a),
+    return launch_kernel(block_fn(eb, a.V), dim3(grid), dim3(32 * (a.cw + 1)), block_smem_bytes(a),
                          st, pdl, a);
 }
 

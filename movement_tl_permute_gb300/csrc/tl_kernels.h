@@ -250,10 +250,15 @@ cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStr
 // that each src run is one bulk copy of its 16-byte blocks and per-CTA tables (built
 // once in shared memory) give the stage offset of the element at dst-run position i
 // of dst run j as TA[i] + TB[j], and its dst offset as dof + dst_j + i.
-constexpr int kBlockConsumerWarps = 8;
-constexpr int kBlockThreads = 32 * (kBlockConsumerWarps + 1);   // + one producer warp
+// A CTA is cw consumer warps and one producer warp.  The launch bounds (at most 18
+// warps, two CTAs per SM) hold a thread to 56 registers, so an SM keeps 36 warps:
+// four CTAs of 8 consumer warps, three of 11 or two of 17, by the CTAs its shared
+// memory holds.
+constexpr int kBlockMaxWarps = 18;
+constexpr int kBlockSmWarps = 36;
+constexpr int kBlockDefaultWarps = 9;       // 8 consumer warps unless asked otherwise
 constexpr int kBlockStages = 3;
-constexpr int kBlockCtasPerSm = 4;          // launch bounds: at most 56 registers a thread
+constexpr int kBlockCtasPerSm = 4;
 constexpr int kBlockMaxSmem = 200 * 1024;   // stages of at most 48 KiB + the tables
 struct BlockArgs {
     const uint8_t* src;
@@ -275,8 +280,9 @@ struct BlockArgs {
     int32_t ld_inner, ls_inner;  // run lengths without the chunked axis
     int32_t V, W;                // store pieces: V elements, W per dst run
     // a consumer warp-step: a group of 32 >> r_lg pieces in each of 1 << r_lg dst runs;
-    // GW x GR groups per tile; one step of the consumer warps advances dgw, dgr groups
-    int32_t r_lg, GW, GR, dgw, dgr;
+    // GW x GR groups per tile
+    int32_t r_lg, GW, GR;
+    int32_t cw;                  // consumer warps (the CTA is cw + 1 warps)
     int32_t stage_bytes;
     int32_t table_off;           // byte offset of the tables in dynamic shared memory
     // the chunked axis: extent, tile extent, chunks, strides

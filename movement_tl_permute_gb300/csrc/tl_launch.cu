@@ -48,6 +48,7 @@ struct TileTuning {
     int cluster_recv = 0;   // its receive ring depth (0 = by layout, cluster_defaults)
     int cluster_warps = 4;  // its consumer warps (8 or 4)
     int cluster_ctas = 0;   // its CTAs per SM (0 = by layout; tile_ctas_per_sm overrides)
+    int block_warps = 0;    // block path: consumer warps at most (0 = as many as fit)
 };
 
 // Tile-path ring depth and grid by element width.  Throughput against the tiles in
@@ -95,6 +96,8 @@ TileTuning tile_tuning(const tl_permute_opts* o) {
         t.cluster_recv = o->cluster_recv_stages;
     if (o->cluster_consumer_warps == 4 || o->cluster_consumer_warps == 8)
         t.cluster_warps = o->cluster_consumer_warps;
+    if (o->cluster_consumer_warps >= 1 && o->cluster_consumer_warps < kBlockMaxWarps)
+        t.block_warps = o->cluster_consumer_warps;
     if (o->tile_ctas_per_sm > 0) t.ctas_per_sm = o->tile_ctas_per_sm;
     if (o->tile_rows == 256) t.rows = 256;
     const int max_stages = kTileRingBytes / (t.rows * 128);
@@ -352,8 +355,6 @@ BlockArgs block_args(const Plan& p) {
     a.r_lg = b.r_lg;
     a.GW = (a.W + (32 >> a.r_lg) - 1) / (32 >> a.r_lg);
     a.GR = (a.Rd + (1 << a.r_lg) - 1) >> a.r_lg;
-    a.dgw = kBlockConsumerWarps % a.GW;
-    a.dgr = kBlockConsumerWarps / a.GW;
     a.stage_bytes = (int32_t)b.stage;
     a.table_off = kBlockStages * a.stage_bytes;
     if (b.chunk >= 0) {
@@ -446,15 +447,20 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         }
         break;
     case TL_PATH_BLOCK: {
-        l.block = kBlockThreads;
         l.smem = block_smem_bytes(block_args(p));
-        if (sms) {
-            // resident CTAs by shared memory (228 KiB per SM, 1 KiB reserved per CTA,
-            // plus the barriers and tile records) and by the kernel's launch bounds
-            int per_sm = 233472 / (l.smem + 1024 + 128);
-            per_sm = per_sm < 1 ? 1 : per_sm > kBlockCtasPerSm ? kBlockCtasPerSm : per_sm;
-            l.grid = cap_grid(p.tiles, sms * per_sm, max_ctas);
-        }
+        // resident CTAs by shared memory (228 KiB per SM, 1 KiB reserved per CTA, plus
+        // the barriers and tile records), at most four; 8 consumer warps (measured on
+        // GB300 at two CTAs per SM: 9^8 fp32 permutes 5.7 TB/s against 5.3 with 17 and
+        // 5.3 with 4; permutes of many short runs ran up to 9 % faster with 4, which
+        // the tuning option asks for)
+        int per_sm = 233472 / (l.smem + 1024 + 128);
+        per_sm = per_sm < 1 ? 1 : per_sm > kBlockCtasPerSm ? kBlockCtasPerSm : per_sm;
+        if (tt.ctas_per_sm > 0 && tt.ctas_per_sm < per_sm) per_sm = tt.ctas_per_sm;
+        int warps = std::min(kBlockDefaultWarps, kBlockSmWarps / per_sm);
+        if (tt.block_warps > 0)
+            warps = std::min(kBlockMaxWarps, std::min(kBlockSmWarps / per_sm, tt.block_warps + 1));
+        l.block = 32 * warps;
+        if (sms) l.grid = cap_grid(p.tiles, sms * per_sm, max_ctas);
         break;
     }
     case TL_PATH_ROWS:
@@ -912,6 +918,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         BlockArgs a = block_args(p);
         a.src = s8;
         a.dst = d8;
+        a.cw = l.block / 32 - 1;
         a.cta_times = opts ? opts->cta_times : nullptr;
         a.status = opts ? opts->dev_status : nullptr;
         const bool drop = (flags & TL_FLAG_TEST_DROP_HANDOFF) != 0;

@@ -904,6 +904,33 @@ def test_block_path_taken_for_high_rank_short_axes():
     assert plan((10,) * 8, tuple(range(7, -1, -1)), 4) == "panel"
 
 
+def test_block_launch_shape_and_tuning():
+    """The block CTA is its consumer warps and one producer warp: 8 consumer warps by
+    default, at most as many as the caller asks (1..17), and never more than the SM's
+    registers hold at the CTAs per SM its shared memory allows (36 warps per SM)."""
+    shape = (9,) * 8
+    ss = L.row_major_strides(shape)
+    pst = L.row_major_strides(shape)
+    perm = (1, 4, 2, 3, 7, 5, 6, 0)
+    ds = [0] * 8
+    for i, p in enumerate(perm):
+        ds[p] = pst[i]
+
+    def plan(**kw):
+        return tl.tl_plan(1 << 40, 1 << 42, shape, ss, ds, 4, path="block", **kw)
+    base = plan()
+    per_sm = min(4, 233472 // (base["smem_bytes"] + 1024 + 128))
+    assert base["block"] == 9 * 32
+    assert plan(cluster_consumer_warps=4)["block"] == 5 * 32
+    assert plan(cluster_consumer_warps=17)["block"] == 32 * min(18, 36 // per_sm)
+    assert plan(cluster_consumer_warps=40)["block"] == 9 * 32      # out of range: default
+    assert plan(tile_ctas_per_sm=1, cluster_consumer_warps=17)["block"] == 18 * 32
+    small = plan(panel_tile_kib=8)                                 # more CTAs per SM
+    per_small = min(4, 233472 // (small["smem_bytes"] + 1024 + 128))
+    assert plan(panel_tile_kib=8, cluster_consumer_warps=17)["block"] == \
+        32 * min(18, 36 // per_small)
+
+
 def _random_thread_axis(rng):
     """A valid thread-axis layout: 32 lanes split over 1-2 axes and P registers over
     0-2 axes, each side's strides dense in a random order, the axes shuffled."""

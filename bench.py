@@ -60,7 +60,7 @@ KERNEL_NAMES = {"tile": "k_tile", "cluster": "k_cluster", "rows": "k_rows", "chu
 DTYPES = {"sf_transpose": "f32", "tile_transpose": "f16", "mx_sf": "u8", "attention": "bf16",
           "t2d_u8": "u8", "t2d_f16": "f16", "t2d_f32": "f32", "t2d_f64": "f64",
           "t2d_v16": "16-byte", "t2d_odd_f32": "f32", "hwc_chw_u8": "u8", "nd6_f32": "f32",
-          "nd8_f32": "f32"}
+          "nd8_f32": "f32", "nd8_u16": "u16"}
 
 
 # ---------------------------------------------------------------------------
@@ -412,7 +412,8 @@ CONFIG_RUNS = [("tile_transpose", "tile_transpose", "auto"),
                ("mx_sf", "mx_sf", "auto"), ("attention", "attention", "auto"),
                ("t2d_u8", "t2d_u8", "auto"), ("t2d_f16", "t2d_f16", "auto"),
                ("t2d_f32", "t2d_f32", "auto"), ("t2d_f64", "t2d_f64", "auto"),
-               ("t2d_v16", "t2d_v16", "auto")]
+               ("t2d_v16", "t2d_v16", "auto"), ("nd8_f32", "nd8_f32", "auto"),
+               ("nd8_u16", "nd8_u16", "auto")]
 
 
 def all_configs(args, tl, dev, stream, head_name, head_src):

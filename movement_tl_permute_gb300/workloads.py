@@ -38,6 +38,8 @@ Three more describe general permutes whose layouts a TMA tensor map cannot take
 ``nd8_f32``        float32 (9,)*8 permuted (1,4,2,3,7,5,6,0): a high-rank permute
                    of short axes whose src- and dst-contiguous axes are 36 bytes
                    long (172 MB).
+``nd8_u16``        uint16 (12,)*8 permuted (7,5,3,1,0,2,4,6): the interleaved
+                   order of twelve-element axes, runs of 24 bytes (860 MB).
 =================  =========================================================
 """
 from __future__ import annotations
@@ -122,6 +124,14 @@ def _nd8(lead):
                     ("general",))
 
 
+def _nd8_u16(lead):
+    shape = (lead,) + (12,) * 7
+    n = lead * 12 ** 7
+    return Workload("nd8_u16", 2, shape, _rm(shape), _perm_dst(shape, (7, 5, 3, 1, 0, 2, 4, 6)),
+                    n, n, 59, "bits", "uint16 %s permuted (7,5,3,1,0,2,4,6)" % (shape,),
+                    ("general",))
+
+
 WORKLOADS = {
     w.name: w for w in [
         Workload("sf_transpose", 4, (2, 1, 4, 32), (128, 128, 32, 1), (128, 128, 1, 4),
@@ -145,6 +155,7 @@ WORKLOADS = {
         _hwc_chw(8192),
         _nd6(16),
         _nd8(9),
+        _nd8_u16(12),
     ]
 }
 
@@ -169,6 +180,8 @@ def scaled(w: Workload, leading: int) -> Workload:
         return _nd6(leading)
     if w.name == "nd8_f32":             # the leading axis is innermost in dst
         return _nd8(leading)
+    if w.name == "nd8_u16":             # the leading axis sits inside dst's order
+        return _nd8_u16(leading)
     ratio_src = w.src_elems // w.shape[0]
     ratio_dst = w.dst_elems // w.shape[0]
     return Workload(w.name, w.elem_bytes, (leading,) + tuple(w.shape[1:]), w.src_strides,

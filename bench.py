@@ -59,7 +59,7 @@ KERNEL_NAMES = {"tile": "k_tile", "cluster": "k_cluster", "rows": "k_rows", "chu
                 "warp": "k_warp", "generic": "k_generic"}
 DTYPES = {"sf_transpose": "f32", "tile_transpose": "f16", "mx_sf": "u8", "attention": "bf16",
           "t2d_u8": "u8", "t2d_f16": "f16", "t2d_f32": "f32", "t2d_f64": "f64",
-          "t2d_v16": "16-byte", "t2d_odd_f32": "f32", "hwc_chw_u8": "u8", "nd6_f32": "f32",
+          "t2d_v16": "16-byte", "t2d_odd_f32": "f32", "t2d_odd_u8": "u8", "hwc_chw_u8": "u8", "nd6_f32": "f32",
           "nd8_f32": "f32", "nd8_u16": "u16"}
 
 

@@ -32,6 +32,8 @@ Three more describe general permutes whose layouts a TMA tensor map cannot take
 =================  =========================================================
 ``t2d_odd_f32``    float32 16383 x 16385 row-major -> column-major: row pitches
                    that are not multiples of 16 bytes (1 GiB).
+``t2d_odd_u8``     uint8 32767 x 32769 row-major -> column-major: odd row pitches
+                   on both sides (1 GiB).
 ``hwc_chw_u8``     uint8 image 8192 x 8192 x 3 channels (HWC) -> 3 planes (CHW).
 ``nd6_f32``        float32 (16,16,16,16,64,64) permuted (5,3,1,4,2,0): four
                    batch axes around the transposed plane (1 GiB).
@@ -152,6 +154,7 @@ WORKLOADS = {
         _t2d("t2d_f64", 8, 8192, 16384, 53),
         _t2d("t2d_v16", 16, 8192, 8192, 54),
         _t2d("t2d_odd_f32", 4, 16383, 16385, 55),
+        _t2d("t2d_odd_u8", 1, 32767, 32769, 60),
         _hwc_chw(8192),
         _nd6(16),
         _nd8(9),

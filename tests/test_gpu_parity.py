@@ -740,7 +740,7 @@ def test_block_copy_timeout_is_reported_and_context_survives():
 # every bench workload at full size, in the launch configuration the bench times
 # ---------------------------------------------------------------------------
 FULL = ["sf_transpose", "tile_transpose", "mx_sf", "attention", "t2d_u8", "t2d_f16", "t2d_f32",
-        "t2d_f64", "t2d_v16", "t2d_odd_f32", "hwc_chw_u8", "nd6_f32", "nd8_f32", "nd8_u16"]
+        "t2d_f64", "t2d_v16", "t2d_odd_f32", "t2d_odd_u8", "hwc_chw_u8", "nd6_f32", "nd8_f32", "nd8_u16"]
 
 
 def _full(name, path="auto"):

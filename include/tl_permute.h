@@ -238,9 +238,10 @@ typedef struct tl_permute_opts {
     int32_t cluster_recv_stages; /* cluster: receive ring depth, 1..8 (staging + receive
                                     slots at most 12) */
     int32_t cluster_consumer_warps; /* cluster: consumer warps per CTA, 4 or 8; block:
-                                       at most this many, 1..17 (by default as many as
-                                       the SM's registers allow at the CTAs per SM its
-                                       shared memory holds) */
+                                       this many, 1..17, as far as the SM's registers
+                                       allow at the CTAs per SM its shared memory holds
+                                       (by default 8, or 4 for tiles of 48 src runs or
+                                       more) */
     int32_t panel_tile_kib;       /* panel path: tile size, 4..48 KiB (default 32, or 24
                                      with an extent of 16 or less); block path: its
                                      tile's bytes */

@@ -256,7 +256,7 @@ cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStr
 // memory holds.
 constexpr int kBlockMaxWarps = 18;
 constexpr int kBlockSmWarps = 36;
-constexpr int kBlockDefaultWarps = 9;       // 8 consumer warps unless asked otherwise
+constexpr int kBlockDefaultWarps = 9;       // 8 consumer warps (4 for tiles of many runs)
 constexpr int kBlockStages = 3;
 constexpr int kBlockCtasPerSm = 4;
 constexpr int kBlockMaxSmem = 200 * 1024;   // stages of at most 48 KiB + the tables

@@ -500,6 +500,20 @@ def test_block_store_walks(eb):
     assert 16 in vecs, vecs
 
 
+@pytest.mark.parametrize("eb", [1, 4])
+def test_block_consumer_warp_counts(eb):
+    """The block kernel with 1, 3 and 17 consumer warps, and at one CTA per SM: the same
+    bytes as the oracle (the walks' step over the consumer threads changes with the
+    count)."""
+    for i, (shape, perm) in enumerate((((12,) * 5, (4, 2, 0, 1, 3)),
+                                       ((9,) * 6, (1, 4, 2, 3, 5, 0)))):
+        ss, ds = perm_layouts(shape, perm)
+        for k, kw in enumerate((dict(cluster_consumer_warps=1), dict(cluster_consumer_warps=3),
+                                dict(cluster_consumer_warps=17),
+                                dict(tile_ctas_per_sm=1, cluster_consumer_warps=17))):
+            check(shape, ss, ds, eb, "block", seed=490 + 10 * i + k, dst_off=k % 2, **kw)
+
+
 def test_per_cta_times_are_recorded_without_changing_the_result():
     """The measurement option: the tile, rows, panel and block kernels write each
     CTA's start and finish time, every CTA of the grid tl_plan reports once, and the

@@ -906,8 +906,9 @@ def test_block_path_taken_for_high_rank_short_axes():
 
 def test_block_launch_shape_and_tuning():
     """The block CTA is its consumer warps and one producer warp: 8 consumer warps by
-    default, at most as many as the caller asks (1..17), and never more than the SM's
-    registers hold at the CTAs per SM its shared memory allows (36 warps per SM)."""
+    default (4 for tiles of 48 src runs or more), as many as the caller asks (1..17),
+    and never more than the SM's registers hold at the CTAs per SM its shared memory
+    allows (36 warps per SM)."""
     shape = (9,) * 8
     ss = L.row_major_strides(shape)
     pst = L.row_major_strides(shape)
@@ -925,6 +926,12 @@ def test_block_launch_shape_and_tuning():
     assert plan(cluster_consumer_warps=17)["block"] == 32 * min(18, 36 // per_sm)
     assert plan(cluster_consumer_warps=40)["block"] == 9 * 32      # out of range: default
     assert plan(tile_ctas_per_sm=1, cluster_consumer_warps=17)["block"] == 18 * 32
+    perm2 = (6, 7, 2, 1, 4, 5, 3, 0)                              # tiles of 81 src runs
+    pst2 = L.row_major_strides(tuple(shape[p] for p in perm2))
+    ds2 = [0] * 8
+    for i, p in enumerate(perm2):
+        ds2[p] = pst2[i]
+    assert tl.tl_plan(1 << 40, 1 << 42, shape, ss, ds2, 4, path="block")["block"] == 5 * 32
     small = plan(panel_tile_kib=8)                                 # more CTAs per SM
     per_small = min(4, 233472 // (small["smem_bytes"] + 1024 + 128))
     assert plan(panel_tile_kib=8, cluster_consumer_warps=17)["block"] == \

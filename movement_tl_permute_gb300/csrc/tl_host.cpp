@@ -1313,6 +1313,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         const int64_t brun = plan_block(&q);
         if (brun >= 128) {
             int64_t prun = 0;
+            bool pvec = false;                 // the panel tile stores 16-byte dst runs
             if (path == TL_PATH_PANEL) {
                 Plan r = p;
                 setup_panel(r);
@@ -1323,11 +1324,14 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
                 const int64_t srun = packed ? ta * tb * eb : ta * eb;
                 const int64_t drun = r.panel_run ? ta * tb * eb : tb * eb;
                 prun = std::min(srun, drun);
+                pvec = r.panel_vec || r.panel_run;
             }
-            // (measured on GB300 against panel tiles stored as 16-byte dst runs:
-            // reversed 8^8 fp32 1.15x as blocks, 12^8 fp64 in the interleaved order
-            // 1.5x, reversed 10^8 fp32 equal at a shorter block run)
-            if (brun >= prun) path = TL_PATH_BLOCK;
+            // Against a panel tile stored as 16-byte dst runs the block tile needs few
+            // src runs: measured on GB300, reversed 8^8 fp32 (64 runs a tile) 1.19x as
+            // blocks and 12^8 fp64 in the interleaved order (24) 1.48x, but `nd6_f32`
+            // (128 runs of 256 bytes) 0.38x and reversed 16^7 fp32 (256 runs) 0.33x:
+            // their stages hold one CTA per SM.
+            if (brun >= prun && !(pvec && q.blk.Rs > 100)) path = TL_PATH_BLOCK;
         }
     }
     p.path = path;

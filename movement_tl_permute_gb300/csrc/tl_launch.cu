@@ -450,14 +450,15 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         l.smem = block_smem_bytes(block_args(p));
         // resident CTAs by shared memory (228 KiB per SM, 1 KiB reserved per CTA, plus
         // the barriers and tile records), at most four; 8 consumer warps, 4 for tiles of
-        // 48 src runs or more (measured on GB300, ten layouts: 8 against 4 ran 1.08-1.17x
+        // 48 src runs or more at two CTAs per SM or more (measured on GB300, ten layouts: 8 against 4 ran 1.08-1.17x
         // on tiles of 9 and 36 runs -- 9^8 fp32, 12^7 and 12^8 u16 --, 4 ran 1.04-1.09x
         // on tiles of 64-100 runs -- other 9^8 orders, reversed 8^8 and 10^8, 12^8 u8 --
         // and equal at 24 and 48; 17 ran slower everywhere but one)
         int per_sm = 233472 / (l.smem + 1024 + 128);
         per_sm = per_sm < 1 ? 1 : per_sm > kBlockCtasPerSm ? kBlockCtasPerSm : per_sm;
         if (tt.ctas_per_sm > 0 && tt.ctas_per_sm < per_sm) per_sm = tt.ctas_per_sm;
-        int warps = std::min(p.blk.Rs >= 48 ? 5 : kBlockDefaultWarps, kBlockSmWarps / per_sm);
+        const bool many = p.blk.Rs >= 48 && per_sm >= 2;   // (one CTA per SM keeps 8)
+        int warps = std::min(many ? 5 : kBlockDefaultWarps, kBlockSmWarps / per_sm);
         if (tt.block_warps > 0)
             warps = std::min(kBlockMaxWarps, std::min(kBlockSmWarps / per_sm, tt.block_warps + 1));
         l.block = 32 * warps;

@@ -888,7 +888,8 @@ def test_block_path_taken_for_high_rank_short_axes():
     """The planner gives the block tile to the high-rank permutes of short axes whose
     panel tiles move shorter runs (reversed 8^8 fp32 too, whose panel tiles store
     16-byte runs), and keeps the panel where its runs are the longer ones (reversed
-    10^8 fp32: block runs of 200 bytes against panel runs of 208)."""
+    10^8 fp32: block runs of 200 bytes against panel runs of 208) and where it stores
+    16-byte runs against a block tile of more than 100 src runs (6-D fp32, 16^7 fp32)."""
     def plan(shape, perm, eb):
         ss = L.row_major_strides(shape)
         pst = L.row_major_strides(tuple(shape[p] for p in perm))
@@ -902,6 +903,9 @@ def test_block_path_taken_for_high_rank_short_axes():
     assert plan((12,) * 8, (7, 5, 3, 1, 0, 2, 4, 6), 8) == "block"
     assert plan((8,) * 8, tuple(range(7, -1, -1)), 4) == "block"
     assert plan((10,) * 8, tuple(range(7, -1, -1)), 4) == "panel"
+    # panel tiles of 16-byte dst runs against block tiles of more than 100 src runs
+    assert plan((16, 16, 16, 16, 64, 64), (5, 3, 1, 4, 2, 0), 4) == "panel"
+    assert plan((16,) * 7, tuple(range(6, -1, -1)), 4) == "panel"
 
 
 def test_block_launch_shape_and_tuning():

@@ -908,6 +908,23 @@ def test_block_path_taken_for_high_rank_short_axes():
     assert plan((16,) * 7, tuple(range(6, -1, -1)), 4) == "panel"
 
 
+def test_every_workload_keeps_its_measured_path():
+    """The planner's path for every named workload at full size, as measured fastest
+    on GB300 (a rule change that moves one shows here before it costs throughput)."""
+    from movement_tl_permute_gb300 import workloads
+    want = {"sf_transpose": "warp", "tile_transpose": "tile", "mx_sf": "rows",
+            "attention": "chunk", "t2d_u8": "tile", "t2d_f16": "tile", "t2d_f32": "tile",
+            "t2d_f64": "tile", "t2d_v16": "tile", "t2d_odd_f32": "panel",
+            "t2d_odd_u8": "panel", "hwc_chw_u8": "cols", "nd6_f32": "panel",
+            "nd8_f32": "block", "nd8_u16": "block"}
+    assert set(want) == set(workloads.WORKLOADS)
+    for name, path in want.items():
+        w = workloads.get(name)
+        got = tl.tl_plan(1 << 40, 1 << 43, w.shape, w.src_strides, w.dst_strides,
+                         w.elem_bytes)["path"]
+        assert got == path, (name, got)
+
+
 def test_block_launch_shape_and_tuning():
     """The block CTA is its consumer warps and one producer warp: 8 consumer warps by
     default (4 for tiles of 48 src runs or more), as many as the caller asks (1..17),

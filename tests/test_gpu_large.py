@@ -1,5 +1,5 @@
-"""Maximum sizes: every kernel path past 2^32 bytes (and the generic path past 2^32
-elements), so that 64-bit offsets are exercised end to end.
+"""Maximum sizes: every kernel path past 2^32 bytes (and the generic and block paths
+past 2^32 elements), so that 64-bit offsets are exercised end to end.
 
 The outputs are too large for the whole-tensor oracle loop, so the oracle
 evaluates the definition one coordinate at a time (``oracle.sample``) at
@@ -90,6 +90,19 @@ def test_rows_path_past_4gib():
     # MX scale-factor blocks: (2^25 + 4096, 4, 32) uint8, 4.3 GB
     nb = (1 << 25) + 4096
     check_sampled((nb, 4, 32), (128, 32, 1), (128, 1, 4), 1, "rows", seed=73)
+
+
+def test_block_path_past_4gib():
+    # (126, 12^7) uint8 in the interleaved order (7,5,3,1,0,2,4,6): 4.5 GB each way,
+    # 4.5e9 elements; and (18, 12^7) fp64, 5.2 GB each way
+    for shape, eb, seed in (((126,) + (12,) * 7, 1, 76), ((18,) + (12,) * 7, 8, 77)):
+        perm = (7, 5, 3, 1, 0, 2, 4, 6)
+        ss = L.row_major_strides(shape)
+        pst = L.row_major_strides(tuple(shape[p] for p in perm))
+        ds = [0] * len(shape)
+        for i, p in enumerate(perm):
+            ds[p] = pst[i]
+        check_sampled(shape, ss, tuple(ds), eb, "block", seed=seed)
 
 
 def test_generic_path_past_2_32_elements():

@@ -56,6 +56,8 @@ __device__ __forceinline__ uint32_t lds16(uint32_t a) {
     return v;
 }
 
+constexpr uint32_t kEndRecord = 0xFFFFFFFFu;   // the vc of the record that ends a pipeline
+
 struct BlockTile {
     int64_t so, dof;   // element offsets of the tile's origin in src and dst
     uint32_t vc;       // valid extent of the chunked axis in this tile
@@ -189,22 +191,33 @@ __device__ __forceinline__ void load_offsets(uint32_t ta, uint32_t v, uint32_t W
 template <int EB, int V>
 __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ __align__(8) uint64_t full[kBlockStages];
-    __shared__ __align__(8) uint64_t empty[kBlockStages];
-    __shared__ __align__(16) uint4 info[kBlockStages];   // dof lo / hi, vc, origin mod 16
+    // per pipeline: its ring's barriers and tile records (dof lo / hi, vc, origin mod 16)
+    __shared__ __align__(8) uint64_t full_[kBlockMaxGroups][kBlockStages];
+    __shared__ __align__(8) uint64_t empty_[kBlockMaxGroups][kBlockStages];
+    __shared__ __align__(16) uint4 info_[kBlockMaxGroups][kBlockStages];
+    __shared__ int32_t landed_[kBlockMaxGroups][kBlockStages];
     // bytes the copies of a whole tile move, by the tile origin's offset inside its
     // 16-byte block
     __shared__ uint32_t tot[16];
-    __shared__ int32_t landed[kBlockStages];
-    const uint32_t sbase = dev::smem_addr(smem);
+    __shared__ uint32_t next_tile;        // the CTA's tiles handed out so far
     const uint32_t stage = (uint32_t)a.stage_bytes;
+    // this warp's pipeline: cw consumer warps and a producer warp, the pipelines side by
+    // side in the CTA
+    const int wpg = a.cw + 1;
+    const int grp = (int)(threadIdx.x >> 5) / wpg;
+    uint64_t* full = full_[grp];
+    uint64_t* empty = empty_[grp];
+    uint4* info = info_[grp];
+    int32_t* landed = landed_[grp];
+    const uint32_t sbase = dev::smem_addr(smem) + (uint32_t)grp * kBlockStages * stage;
     uint32_t* TA = reinterpret_cast<uint32_t*>(smem + a.table_off);       // [Ld, padded to 4]
     uint4* TB = reinterpret_cast<uint4*>(TA + ((a.Ld + 3) & ~3));        // [Rd]
     uint4* TR = TB + a.Rd;                                                // [Rs]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = (int)(threadIdx.x >> 5) - grp * wpg, lane = threadIdx.x & 31;
 
     // the tables (from the arguments only: before the dependency wait)
     if (threadIdx.x < 16) tot[threadIdx.x] = 0;
+    if (threadIdx.x == 0) next_tile = 0;
     __syncthreads();
     for (int32_t i = threadIdx.x; i < a.Ld; i += blockDim.x) {
         uint32_t x = (uint32_t)i, o = 0;
@@ -245,10 +258,11 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
             atomicAdd(&tot[m], (((m + (uint32_t)sb) & 15) + (uint32_t)a.Ls * EB + 15) & ~15u);
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kBlockStages; ++s) {
-            dev::mbar_init(&full[s], 1);                   // producer lane 0 arrives
-            dev::mbar_init(&empty[s], (uint32_t)a.cw);
-        }
+        for (int g = 0; g < a.groups; ++g)
+            for (int s = 0; s < kBlockStages; ++s) {
+                dev::mbar_init(&full_[g][s], 1);           // producer lane 0 arrives
+                dev::mbar_init(&empty_[g][s], (uint32_t)a.cw);
+            }
         dev::fence_barrier_init();
     }
     __syncthreads();
@@ -258,9 +272,13 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
 
     if (warp == a.cw) {
         // ---------------- producer: one bulk copy per src run ---------------------------
+        // The CTA's tiles are blockIdx.x + k * gridDim.x; its pipelines take them in
+        // turn from a shared counter (with one pipeline: in order), so that a pipeline
+        // running slower takes fewer.  A tile past the end goes to the consumers as an
+        // end record.
         uint32_t issued = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++issued) {
+        for (;; ++issued) {
             const uint32_t use = issued / kBlockStages, s = issued - use * kBlockStages;
             if (use > 0) {
                 const bool got = dev::mbar_wait(&empty[s], (use - 1) & 1, a.timeout_ns);
@@ -269,6 +287,21 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
                     break;
                 }
                 dev::fence_proxy_async_smem();   // the consumers' reads of the stage came first
+            }
+            uint32_t k = issued;                           // one pipeline: in order
+            if (a.groups > 1) {
+                if (lane == 0) k = atomicAdd(&next_tile, 1u);
+                k = __shfl_sync(0xffffffffu, k, 0);
+            }
+            const int64_t t = (int64_t)blockIdx.x + (int64_t)k * gridDim.x;
+            if (t >= a.tiles) {
+                if (lane == 0) {
+                    dev::sts128(dev::smem_addr(&info[s]), make_uint4(0, 0, kEndRecord, 0));
+                    dev::mbar_arrive_expect_tx(&full[s], 0);
+                }
+                __syncwarp();
+                ++issued;
+                break;
             }
             const BlockTile ti = block_tile(t, a);
             const uintptr_t base = reinterpret_cast<uintptr_t>(a.src) + (uintptr_t)(ti.so * EB);
@@ -335,10 +368,10 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
     const uint32_t dgw = cw % GW, dgr = cw / GW;            // one step of the consumer warps
     const uint32_t pw_lg = 5 - (uint32_t)a.r_lg;
     const uint32_t pl = (uint32_t)lane & ((1u << pw_lg) - 1), rl = (uint32_t)lane >> pw_lg;
-    const uint32_t ct = threadIdx.x;                        // 0 .. consumer threads - 1
+    const uint32_t ct = (uint32_t)warp * 32 + lane;         // 0 .. consumer threads - 1
     const uint32_t ta = dev::smem_addr(TA), tb = dev::smem_addr(TB);
     uint32_t it = 0;
-    for (int64_t t = blockIdx.x; t < a.tiles; t += gridDim.x, ++it) {
+    for (;; ++it) {
         const uint32_t use = it / kBlockStages, s = it - use * kBlockStages;
         // consumer warp 0 waits for the stage; the others sleep on a named barrier and
         // then take the completed phase themselves (one try, for its acquire)
@@ -346,12 +379,16 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
             const bool got = dev::mbar_wait(&full[s], use & 1, a.timeout_ns);
             if (lane == 0) landed[s] = got ? 1 : 0;
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(32 * cw) : "memory");
+        if (grp == 0)
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * cw) : "memory");
+        else
+            asm volatile("bar.sync 2, %0;" ::"r"(32 * cw) : "memory");
         if (!landed[s] || !dev::mbar_wait(&full[s], use & 1, a.timeout_ns)) {
             if (lane == 0) dev::report(a.status, TL_ERR_TIMEOUT);
             break;
         }
         const uint4 inf = lds128(dev::smem_addr(&info[s]));
+        if (inf.z == kEndRecord) break;
         const int64_t dof = (int64_t)((uint64_t)inf.x | ((uint64_t)inf.y << 32));
         const uint32_t vc = inf.z;
         const uint32_t sb = sbase + s * stage + 16 + inf.w;
@@ -487,8 +524,8 @@ int block_smem_bytes(const BlockArgs& a) {
 const void* block_kernel(int eb, int v) { return reinterpret_cast<const void*>(block_fn(eb, v)); }
 
 cudaError_t launch_block(int eb, const BlockArgs& a, int grid, cudaStream_t st, bool pdl) {
-    return launch_kernel(block_fn(eb, a.V), dim3(grid), dim3(32 * (a.cw + 1)), block_smem_bytes(a),
-                         st, pdl, a);
+    return launch_kernel(block_fn(eb, a.V), dim3(grid), dim3(32 * (a.cw + 1) * a.groups),
+                         block_smem_bytes(a), st, pdl, a);
 }
 
 }  // namespace tl

@@ -250,7 +250,10 @@ cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStr
 // that each src run is one bulk copy of its 16-byte blocks and per-CTA tables (built
 // once in shared memory) give the stage offset of the element at dst-run position i
 // of dst run j as TA[i] + TB[j], and its dst offset as dof + dst_j + i.
-// A CTA is cw consumer warps and one producer warp.  The launch bounds (at most 18
+// A pipeline is cw consumer warps and one producer warp with its own ring; a CTA runs
+// one pipeline, or two side by side that share the tables and take the CTA's tiles from
+// a shared counter (where two rings fit an SM: one CTA per SM then, so that no CTA's
+// warps are favoured over another's by the schedulers).  The launch bounds (at most 18
 // warps, two CTAs per SM) hold a thread to 56 registers, so an SM keeps 36 warps:
 // four CTAs of 8 consumer warps, three of 11 or two of 17, by the CTAs its shared
 // memory holds.
@@ -258,8 +261,9 @@ constexpr int kBlockMaxWarps = 18;
 constexpr int kBlockSmWarps = 36;
 constexpr int kBlockDefaultWarps = 9;       // 8 consumer warps (4 for tiles of many runs)
 constexpr int kBlockStages = 3;
+constexpr int kBlockMaxGroups = 2;
 constexpr int kBlockCtasPerSm = 4;
-constexpr int kBlockMaxSmem = 200 * 1024;   // stages of at most 48 KiB + the tables
+constexpr int kBlockMaxSmem = 226 * 1024;   // stages of at most 48 KiB + the tables
 struct BlockArgs {
     const uint8_t* src;
     uint8_t* dst;
@@ -282,7 +286,8 @@ struct BlockArgs {
     // a consumer warp-step: a group of 32 >> r_lg pieces in each of 1 << r_lg dst runs;
     // GW x GR groups per tile
     int32_t r_lg, GW, GR;
-    int32_t cw;                  // consumer warps (the CTA is cw + 1 warps)
+    int32_t cw;                  // consumer warps of a pipeline (cw + 1 warps each)
+    int32_t groups;              // pipelines of the CTA (1 or 2)
     int32_t stage_bytes;
     int32_t table_off;           // byte offset of the tables in dynamic shared memory
     // the chunked axis: extent, tile extent, chunks, strides

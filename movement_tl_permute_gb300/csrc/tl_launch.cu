@@ -310,7 +310,32 @@ struct Launch {
 
 // The block kernel's arguments from the plan (pointers left null): the tables' axes,
 // the chunked axis, the batch axes innermost first, and the shared-memory layout.
-BlockArgs block_args(const Plan& p) {
+// Resident rings (pipelines) per SM of the block path: as many single-pipeline CTAs as
+// the shared memory holds (228 KiB per SM, 1 KiB reserved per CTA, plus the barriers
+// and tile records), at most four, or the tuning option's count; where exactly two fit
+// (and the option asks nothing) one CTA runs both pipelines.
+int block_ring_sms(const Plan& p, const TileTuning& tt, int* groups) {
+    const BlockPlan& b = p.blk;
+    const int64_t tables = 4 * ((b.Ld + 3) & ~3) + 16 * b.Rd + 16 * b.Rs;
+    const int64_t one = kBlockStages * b.stage + tables;
+    int per_sm = (int)(233472 / (one + 1024 + 256));
+    per_sm = per_sm < 1 ? 1 : per_sm > kBlockCtasPerSm ? kBlockCtasPerSm : per_sm;
+    *groups = 1;
+    if (tt.ctas_per_sm > 0) {
+        if (tt.ctas_per_sm < per_sm) per_sm = tt.ctas_per_sm;
+    } else if (per_sm == 2) {
+        *groups = 2;
+    }
+    return per_sm;
+}
+
+int block_ctas_per_sm(const Plan& p, const TileTuning& tt) {
+    int groups;
+    const int rings = block_ring_sms(p, tt, &groups);
+    return rings / groups;
+}
+
+BlockArgs block_args(const Plan& p, const TileTuning& tt) {
     const BlockPlan& b = p.blk;
     const int eb = p.eb;
     BlockArgs a{};
@@ -356,7 +381,20 @@ BlockArgs block_args(const Plan& p) {
     a.GW = (a.W + (32 >> a.r_lg) - 1) / (32 >> a.r_lg);
     a.GR = (a.Rd + (1 << a.r_lg) - 1) >> a.r_lg;
     a.stage_bytes = (int32_t)b.stage;
-    a.table_off = kBlockStages * a.stage_bytes;
+    // pipelines and consumer warps: 8 consumer warps, 4 for tiles of 48 src runs or more
+    // at two rings per SM or more (measured on GB300, ten layouts: 8 against 4 ran
+    // 1.08-1.17x on tiles of 9 and 36 runs -- 9^8 fp32, 12^7 and 12^8 u16 --, 4 ran
+    // 1.04-1.09x on tiles of 64-100 runs -- other 9^8 orders, reversed 8^8 and 10^8,
+    // 12^8 u8 -- and equal at 24 and 48; 17 ran slower everywhere but one); an SM keeps
+    // 36 warps at most, a CTA 18
+    int groups;
+    const int rings = block_ring_sms(p, tt, &groups);
+    a.groups = groups;
+    int warps = (b.Rs >= 48 && rings >= 2) ? 5 : kBlockDefaultWarps;
+    if (tt.block_warps > 0) warps = tt.block_warps + 1;
+    warps = std::min(warps, std::min(kBlockSmWarps / rings, kBlockMaxWarps / groups));
+    a.cw = warps - 1;
+    a.table_off = groups * kBlockStages * a.stage_bytes;
     if (b.chunk >= 0) {
         const int q = b.chunk;
         a.c_ext = b.ext[q];
@@ -447,22 +485,10 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         }
         break;
     case TL_PATH_BLOCK: {
-        l.smem = block_smem_bytes(block_args(p));
-        // resident CTAs by shared memory (228 KiB per SM, 1 KiB reserved per CTA, plus
-        // the barriers and tile records), at most four; 8 consumer warps, 4 for tiles of
-        // 48 src runs or more at two CTAs per SM or more (measured on GB300, ten layouts: 8 against 4 ran 1.08-1.17x
-        // on tiles of 9 and 36 runs -- 9^8 fp32, 12^7 and 12^8 u16 --, 4 ran 1.04-1.09x
-        // on tiles of 64-100 runs -- other 9^8 orders, reversed 8^8 and 10^8, 12^8 u8 --
-        // and equal at 24 and 48; 17 ran slower everywhere but one)
-        int per_sm = 233472 / (l.smem + 1024 + 128);
-        per_sm = per_sm < 1 ? 1 : per_sm > kBlockCtasPerSm ? kBlockCtasPerSm : per_sm;
-        if (tt.ctas_per_sm > 0 && tt.ctas_per_sm < per_sm) per_sm = tt.ctas_per_sm;
-        const bool many = p.blk.Rs >= 48 && per_sm >= 2;   // (one CTA per SM keeps 8)
-        int warps = std::min(many ? 5 : kBlockDefaultWarps, kBlockSmWarps / per_sm);
-        if (tt.block_warps > 0)
-            warps = std::min(kBlockMaxWarps, std::min(kBlockSmWarps / per_sm, tt.block_warps + 1));
-        l.block = 32 * warps;
-        if (sms) l.grid = cap_grid(p.tiles, sms * per_sm, max_ctas);
+        const BlockArgs a = block_args(p, tt);
+        l.smem = block_smem_bytes(a);
+        l.block = 32 * (a.cw + 1) * a.groups;
+        if (sms) l.grid = cap_grid(p.tiles, sms * block_ctas_per_sm(p, tt), max_ctas);
         break;
     }
     case TL_PATH_ROWS:
@@ -917,10 +943,9 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
         break;
     }
     case TL_PATH_BLOCK: {
-        BlockArgs a = block_args(p);
+        BlockArgs a = block_args(p, tt);
         a.src = s8;
         a.dst = d8;
-        a.cw = l.block / 32 - 1;
         a.cta_times = opts ? opts->cta_times : nullptr;
         a.status = opts ? opts->dev_status : nullptr;
         const bool drop = (flags & TL_FLAG_TEST_DROP_HANDOFF) != 0;

@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
     uint64_t* empty = empty_[grp];
     uint4* info = info_[grp];
     int32_t* landed = landed_[grp];
-    const uint32_t sbase = dev::smem_addr(smem) + (uint32_t)grp * kBlockStages * stage;
+    const uint32_t sbase = dev::smem_addr(smem) + (uint32_t)grp * (uint32_t)a.ring_bytes;
     uint32_t* TA = reinterpret_cast<uint32_t*>(smem + a.table_off);       // [Ld, padded to 4]
     uint4* TB = reinterpret_cast<uint4*>(TA + ((a.Ld + 3) & ~3));        // [Rd]
     uint4* TR = TB + a.Rd;                                                // [Rs]

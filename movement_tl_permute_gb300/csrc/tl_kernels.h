@@ -289,6 +289,8 @@ struct BlockArgs {
     int32_t cw;                  // consumer warps of a pipeline (cw + 1 warps each)
     int32_t groups;              // pipelines of the CTA (1 or 2)
     int32_t stage_bytes;
+    int32_t ring_bytes;          // one pipeline's stages, on a 128-byte boundary (the same
+                                 // bank phase for every pipeline)
     int32_t table_off;           // byte offset of the tables in dynamic shared memory
     // the chunked axis: extent, tile extent, chunks, strides
     int64_t c_ext, c_ss, c_ds, nc;

@@ -317,7 +317,7 @@ struct Launch {
 int block_ring_sms(const Plan& p, const TileTuning& tt, int* groups) {
     const BlockPlan& b = p.blk;
     const int64_t tables = 4 * ((b.Ld + 3) & ~3) + 16 * b.Rd + 16 * b.Rs;
-    const int64_t one = kBlockStages * b.stage + tables;
+    const int64_t one = ((kBlockStages * b.stage + 127) & ~int64_t(127)) + tables;
     int per_sm = (int)(233472 / (one + 1024 + 256));
     per_sm = per_sm < 1 ? 1 : per_sm > kBlockCtasPerSm ? kBlockCtasPerSm : per_sm;
     *groups = 1;
@@ -394,7 +394,8 @@ BlockArgs block_args(const Plan& p, const TileTuning& tt) {
     if (tt.block_warps > 0) warps = tt.block_warps + 1;
     warps = std::min(warps, std::min(kBlockSmWarps / rings, kBlockMaxWarps / groups));
     a.cw = warps - 1;
-    a.table_off = groups * kBlockStages * a.stage_bytes;
+    a.ring_bytes = (kBlockStages * a.stage_bytes + 127) & ~127;
+    a.table_off = groups * a.ring_bytes;
     if (b.chunk >= 0) {
         const int q = b.chunk;
         a.c_ext = b.ext[q];

@@ -149,6 +149,49 @@ def test_random_panel_layouts_every_store_mode():
     assert {0, 1, 2, 3, "rotated"} <= modes, modes
 
 
+def test_random_block_layouts_every_walk():
+    """The block kernel on seeded high-rank permutes of short axes (3-8 axes of 2-12),
+    every width, unaligned bases, random consumer-warp counts and tile sizes, each
+    against the oracle; both store walks and both vector and single-element pieces must
+    occur."""
+    rng = np.random.default_rng(777)
+    seen = set()
+    done = 0
+    for i in range(400):
+        nd = int(rng.integers(3, 9))
+        shape = tuple(int(x) for x in rng.integers(2, 13, size=nd))
+        if int(np.prod(shape)) > (1 << 21):
+            continue
+        perm = tuple(int(p) for p in rng.permutation(nd))
+        ss = L.row_major_strides(shape)
+        pst = L.row_major_strides(tuple(shape[p] for p in perm))
+        ds = [0] * nd
+        for k, p in enumerate(perm):
+            ds[p] = pst[k]
+        ds = tuple(ds)
+        eb = int(rng.choice([1, 2, 4, 8, 16]))
+        so = int(rng.integers(0, 3)) if rng.random() < 0.4 else 0
+        do = int(rng.integers(0, 3)) if rng.random() < 0.4 else 0
+        opts = {}
+        if rng.random() < 0.3:
+            opts["cluster_consumer_warps"] = int(rng.integers(1, 18))
+        if rng.random() < 0.3:
+            opts["panel_tile_kib"] = int(rng.choice([4, 8, 16, 24, 32, 48]))
+        try:
+            plan = tl.tl_plan((1 << 20) + so * eb, (1 << 36) + 256 + do * eb, shape, ss, ds, eb,
+                              path="block", **opts)
+        except tl.TLError as e:
+            assert e.name == "TL_ERR_PATH", e
+            continue
+        seen.add(("runs", plan["block_runs"] > 1))
+        seen.add(("vec", plan["vec_bytes"] > eb))
+        got, want = _run(shape, ss, ds, eb, so, do, "block", seed=7000 + i, **opts)
+        assert np.array_equal(got, want), (shape, ss, ds, eb, so, do, opts)
+        done += 1
+    assert done >= 150
+    assert {("runs", False), ("runs", True), ("vec", False), ("vec", True)} <= seen, seen
+
+
 def test_concurrent_calls_from_host_threads():
     """Eight host threads, each on its own stream, permute different layouts at once."""
     rng = np.random.default_rng(99)

@@ -19,14 +19,16 @@
 // on the host by replaying the store walk's warp reads on the bank model of the TVM
 // "permute_layout" page ("Algorithm", step 2).
 //
-// Warps.  One producer warp issues the bulk copies of each tile (its lanes take the
+// Pipelines.  A producer warp issues the bulk copies of each tile (its lanes take the
 // runs in turn) into a ring of kBlockStages stages, completion counted on the stage's
-// mbarrier; the consumer warps store each landed tile along its dst runs, each thread
-// V consecutive dst elements per step (one vector store when the dst runs allow it),
-// consecutive threads taking consecutive pieces.  Waits are bounded: a wait that
-// expires reports TL_ERR_TIMEOUT, and the CTA leaves once its own copies have landed
-// (or a longer bound has passed).  Element offsets follow the strided addressing of
-// "Buffers and memory", "Declaring buffers".
+// mbarrier; its consumer warps store each landed tile along its dst runs, each thread
+// V consecutive dst elements per piece (one vector store when the dst runs allow it),
+// in one of the walks the host picks (consecutive pieces in dst order, or groups of
+// pieces across several dst runs).  A CTA runs one pipeline over its tiles in order, or
+// two side by side that take its tiles from a shared counter.  Waits are bounded: a
+// wait that expires reports TL_ERR_TIMEOUT, and the CTA leaves once its own copies have
+// landed (or a longer bound has passed).  Element offsets follow the strided addressing
+// of "Buffers and memory", "Declaring buffers".
 #include "tl_kernels.h"
 
 namespace tl {

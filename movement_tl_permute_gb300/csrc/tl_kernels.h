@@ -295,7 +295,7 @@ struct BlockArgs {
     // the chunked axis: extent, tile extent, chunks, strides
     int64_t c_ext, c_ss, c_ds, nc;
     int32_t c_k, use32;
-    // tiles: chunk index fastest, then the batch axes (innermost first)
+    // tiles: chunk index fastest, then the batch axes (smallest src stride first)
     int32_t nb;
     int64_t tiles;
     int64_t bext[TL_MAX_DIMS], bss[TL_MAX_DIMS], bds[TL_MAX_DIMS];

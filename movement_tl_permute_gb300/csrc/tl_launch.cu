@@ -418,12 +418,21 @@ BlockArgs block_args(const Plan& p, const TileTuning& tt) {
         a.c_k = 1;
         a.nc = 1;
     }
+    // the batch axes innermost first by src stride: tiles reading neighbouring src runs
+    // (which share DRAM blocks at the run ends) are then in flight together (measured on
+    // GB300, against dst order: 12^8 u16 in the interleaved order read 1.27x -> 1.00x its
+    // bytes, 12^8 fp32 1.10x -> 1.04x and 7 % less time, 9^8 fp32 unchanged)
     a.nb = b.batch.n;
-    for (int i = 0; i < a.nb; ++i) {           // innermost (smallest dst stride) first
-        const int j = a.nb - 1 - i;
-        a.bext[i] = b.batch.ext[j];
-        a.bss[i] = b.batch.ss[j];
-        a.bds[i] = b.batch.ds[j];
+    {
+        int ord[TL_MAX_DIMS];
+        for (int i = 0; i < a.nb; ++i) ord[i] = i;
+        std::sort(ord, ord + a.nb, [&](int x, int y) { return b.batch.ss[x] < b.batch.ss[y]; });
+        for (int i = 0; i < a.nb; ++i) {
+            const int j = ord[i];
+            a.bext[i] = b.batch.ext[j];
+            a.bss[i] = b.batch.ss[j];
+            a.bds[i] = b.batch.ds[j];
+        }
     }
     a.tiles = p.tiles;
     a.use32 = p.tiles < (1LL << 32) ? 1 : 0;

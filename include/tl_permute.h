@@ -247,8 +247,9 @@ typedef struct tl_permute_opts {
                                      tile's bytes */
     int32_t cast;         /* TL_CAST_*: convert every element on the way (elem_bytes
                              and src_strides are the source type's, dst_strides the
-                             destination type's); the tile, chunk and generic paths
-                             take casts, a forced other path returns TL_ERR_PATH */
+                             destination type's); the tile, chunk, block and generic
+                             paths take casts, a forced other path returns
+                             TL_ERR_PATH */
     uint64_t *cta_times;  /* nullable DEVICE array (measurement): the tile, rows, panel
                              and block kernels write each CTA's start and finish time
                              (%globaltimer, ns) to cta_times[2 * b] and [2 * b + 1] for

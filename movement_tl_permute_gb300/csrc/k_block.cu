@@ -156,6 +156,32 @@ __device__ __forceinline__ void put(uint8_t* p, const Piece<EB, V>& pc) {
     }
 }
 
+// Bytes of a dst element: the source's, or the cast's target type's.
+template <int EB, int CAST>
+__host__ __device__ constexpr int dst_bytes() {
+    if constexpr (CAST == TL_CAST_NONE) return EB;
+    else return dev::Cast<CAST>::kDst;
+}
+
+// Loads the V stage elements at sj + off[k] (CAST's source type), converts each, and
+// packs them as a piece of the destination type.
+template <int CAST, int V>
+__device__ __forceinline__ void gather_cast(Piece<dev::Cast<CAST>::kDst, V>& pc, uint32_t sj,
+                                            const uint32_t* off) {
+    using C = dev::Cast<CAST>;
+    if constexpr (C::kDst == 2) {                   // fp32 -> 16-bit: two elements a word
+#pragma unroll
+        for (int q = 0; q < Piece<2, V>::kWords; ++q) {
+            uint32_t x = C::cvt(lds32(sj + off[2 * q]));
+            if (2 * q + 1 < V) x |= C::cvt(lds32(sj + off[2 * q + 1])) << 16;
+            pc.w[q] = x;
+        }
+    } else {                                        // 16-bit -> fp32: one element a word
+#pragma unroll
+        for (int k = 0; k < V; ++k) pc.w[k] = C::cvt(lds16(sj + off[k]));
+    }
+}
+
 // Where TA keeps dst-run position i: in order, except that for V >= 8 the four
 // entries q of every piece sit at (q * W + piece) * 4, so that the lanes of a warp
 // (consecutive pieces) read consecutive 16-byte words.
@@ -190,8 +216,16 @@ __device__ __forceinline__ void load_offsets(uint32_t ta, uint32_t v, uint32_t W
     }
 }
 
-template <int EB, int V>
+template <int EB, int V, int CAST = TL_CAST_NONE>
 __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArgs a) {
+    // dst element bytes (the cast's target type) and a piece of V of them
+    constexpr int DEB = dst_bytes<EB, CAST>();
+    using PieceT = Piece<DEB, V>;
+    // loads piece v of a dst run from the stage (converting under a cast)
+    auto load_piece = [](PieceT& pc, uint32_t sj, const uint32_t* off) {
+        if constexpr (CAST == TL_CAST_NONE) gather<EB, V>(pc, sj, off);
+        else gather_cast<CAST, V>(pc, sj, off);
+    };
     extern __shared__ __align__(16) uint8_t smem[];
     // per pipeline: its ring's barriers and tile records (dof lo / hi, vc, origin mod 16)
     __shared__ __align__(8) uint64_t full_[kBlockMaxGroups][kBlockStages];
@@ -241,7 +275,7 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
             dofs += (int64_t)dg * a.jds[k];
             if (k == a.jck) c = dg;
         }
-        dofs *= EB;                                          // in bytes
+        dofs *= DEB;                                         // in bytes
         TB[j] = make_uint4(o, c, (uint32_t)(uint64_t)dofs, (uint32_t)((uint64_t)dofs >> 32));
     }
     for (int32_t r = threadIdx.x; r < a.Rs; r += blockDim.x) {
@@ -397,11 +431,11 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
         // pieces of a dst run, and dst runs, inside this tile's chunk
         const uint32_t wlim = a.ld_chunk ? (uint32_t)a.ld_inner * vc / V : W;
         const uint32_t jlim = a.jck >= 0 ? vc : 0xffffffffu;
-        uint8_t* dt = a.dst + dof * EB;
+        uint8_t* dt = a.dst + dof * DEB;
         // stores piece v of dst run j (when inside the chunk) from its loaded parts
-        auto store = [&](bool in, uint32_t v, const uint4& tj, const Piece<EB, V>& pc) {
+        auto store = [&](bool in, uint32_t v, const uint4& tj, const PieceT& pc) {
             if (in && v < wlim && tj.y < jlim)
-                put<EB, V>(dt + (int64_t)((uint64_t)tj.z | ((uint64_t)tj.w << 32)) + v * (V * EB),
+                put<DEB, V>(dt + (int64_t)((uint64_t)tj.z | ((uint64_t)tj.w << 32)) + v * (V * DEB),
                            pc);
         };
         if (a.r_lg == 0) {
@@ -421,16 +455,16 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
                 const uint4 t0 = lds128(tb + 16 * j);
                 uint32_t o0[V];
                 load_offsets<V>(ta, v, W, o0);
-                Piece<EB, V> p0;
+                PieceT p0;
                 if constexpr (V == 1) {
                     const bool two = j1 < Rd;
                     const uint32_t vb = two ? v1 : v, jb = two ? j1 : j;
                     const uint4 t1 = lds128(tb + 16 * jb);
                     uint32_t o1[1];
                     load_offsets<1>(ta, vb, W, o1);
-                    Piece<EB, 1> p1;
-                    gather<EB, 1>(p0, sb + t0.x, o0);
-                    gather<EB, 1>(p1, sb + t1.x, o1);
+                    PieceT p1;
+                    load_piece(p0, sb + t0.x, o0);
+                    load_piece(p1, sb + t1.x, o1);
                     store(true, v, t0, p0);
                     store(two, vb, t1, p1);
                     if (two) {                                  // past the second piece
@@ -442,7 +476,7 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
                         }
                     }
                 } else {
-                    gather<EB, V>(p0, sb + t0.x, o0);
+                    load_piece(p0, sb + t0.x, o0);
                     store(true, v, t0, p0);
                 }
                 v = v1;
@@ -458,8 +492,8 @@ __global__ void __launch_bounds__(32 * kBlockMaxWarps, 2) k_block(const BlockArg
                 const uint4 t0 = lds128(tb + 16 * j);
                 uint32_t o0[V];
                 load_offsets<V>(ta, v, W, o0);
-                Piece<EB, V> p0;
-                gather<EB, V>(p0, sb + t0.x, o0);
+                PieceT p0;
+                load_piece(p0, sb + t0.x, o0);
                 store(in, v, t0, p0);
                 gw += dgw;
                 gr += dgr;
@@ -507,7 +541,33 @@ BlockFn kernel_of(int v) {
     }
 }
 
-BlockFn block_fn(int eb, int v) {
+template <int CAST>
+BlockFn cast_kernel_of(int v) {
+    constexpr int SEB = dev::Cast<CAST>::kSrc;
+    if constexpr (dev::Cast<CAST>::kDst == 2) {          // pieces of 1, 2, 4 or 8 16-bit elements
+        switch (v) {
+        case 8: return &k_block<SEB, 8, CAST>;
+        case 4: return &k_block<SEB, 4, CAST>;
+        case 2: return &k_block<SEB, 2, CAST>;
+        default: return &k_block<SEB, 1, CAST>;
+        }
+    } else {                                            // pieces of 1, 2 or 4 fp32 elements
+        switch (v) {
+        case 4: return &k_block<SEB, 4, CAST>;
+        case 2: return &k_block<SEB, 2, CAST>;
+        default: return &k_block<SEB, 1, CAST>;
+        }
+    }
+}
+
+BlockFn block_fn(int eb, int v, int cast) {
+    switch (cast) {
+    case TL_CAST_F32_TO_BF16: return cast_kernel_of<TL_CAST_F32_TO_BF16>(v);
+    case TL_CAST_F32_TO_F16: return cast_kernel_of<TL_CAST_F32_TO_F16>(v);
+    case TL_CAST_BF16_TO_F32: return cast_kernel_of<TL_CAST_BF16_TO_F32>(v);
+    case TL_CAST_F16_TO_F32: return cast_kernel_of<TL_CAST_F16_TO_F32>(v);
+    default: break;
+    }
     switch (eb) {
     case 1: return kernel_of<1>(v);
     case 2: return kernel_of<2>(v);
@@ -523,10 +583,12 @@ int block_smem_bytes(const BlockArgs& a) {
     return a.table_off + 4 * ((a.Ld + 3) & ~3) + 16 * a.Rd + 16 * a.Rs;
 }
 
-const void* block_kernel(int eb, int v) { return reinterpret_cast<const void*>(block_fn(eb, v)); }
+const void* block_kernel(int eb, int v, int cast) {
+    return reinterpret_cast<const void*>(block_fn(eb, v, cast));
+}
 
 cudaError_t launch_block(int eb, const BlockArgs& a, int grid, cudaStream_t st, bool pdl) {
-    return launch_kernel(block_fn(eb, a.V), dim3(grid), dim3(32 * (a.cw + 1) * a.groups),
+    return launch_kernel(block_fn(eb, a.V, a.cast), dim3(grid), dim3(32 * (a.cw + 1) * a.groups),
                          block_smem_bytes(a), st, pdl, a);
 }
 

@@ -922,7 +922,7 @@ int64_t block_layout(BlockPlan& b, int eb, const int* extra) {
 // consecutive pieces (b.vec dst elements each) in dst order, on into the next dst run;
 // r_lg > 0: 32 >> r_lg consecutive pieces in each of 1 << r_lg consecutive dst runs,
 // lanes without a piece counted as work lost.
-double block_drain_cost(const BlockPlan& b, int eb) {
+double block_drain_cost(const BlockPlan& b, int eb, int deb) {
     int64_t ta[kBlockMaxLd], tb[kBlockMaxRuns];
     auto fill = [&](int64_t* t, int64_t n, int na, const int* ax) {
         for (int64_t x = 0; x < n; ++x) {
@@ -959,7 +959,7 @@ double block_drain_cost(const BlockPlan& b, int eb) {
             }
             waves += bank_degree(32, o, eb, true);
         }
-    const int64_t seg = (flat ? 32 : PW) * V * eb;           // bytes of a run segment
+    const int64_t seg = (flat ? 32 : PW) * V * deb;          // bytes of a run segment
     const double lines = (double)(flat ? 1 : R) * (double)((seg + 127) / 128);
     const double lanes = flat ? 1.0 : (double)(W * b.Rd) / (double)(GW * PW * GR * R);
     return ((double)waves / (double)steps + lines) / (32.0 * (double)V * lanes);
@@ -969,7 +969,7 @@ double block_drain_cost(const BlockPlan& b, int eb) {
 // 1 .. 32 and extra 16-byte steps for the two innermost src-run index axes (stages of
 // at most 48 KiB); the fewest runs per warp-step (the longest stores) within 3 % of
 // the best.
-void block_search(BlockPlan& b, int eb) {
+void block_search(BlockPlan& b, int eb, int deb) {
     int best_r = 0, best_e[6][2] = {};
     double best_c[6];
     const int n0 = b.nr > 0 ? 8 : 1, n1 = b.nr > 1 ? 8 : 1;
@@ -980,7 +980,7 @@ void block_search(BlockPlan& b, int eb) {
             for (int e1 = 0; e1 < n1; ++e1) {
                 const int extra[kBlockAxes] = {e0, e1, 0, 0};
                 if (block_layout(b, eb, extra) > 48 * 1024) continue;
-                const double c = block_drain_cost(b, eb);
+                const double c = block_drain_cost(b, eb, deb);
                 if (best_c[r] < 0 || c < best_c[r]) {
                     best_c[r] = c;
                     best_e[r][0] = e0;
@@ -1002,7 +1002,7 @@ void block_search(BlockPlan& b, int eb) {
 
 int64_t plan_block(Plan* p, int64_t tile_bytes) {
     const Axes& s = p->sorted;
-    const int n = s.n, eb = p->eb;
+    const int n = s.n, eb = p->eb, deb = p->deb > 0 ? p->deb : p->eb;   // (dst element bytes)
     // measured on GB300 (12^7 and 12^8 permutes, 9^8 permutes): 12 KiB tiles for 1- and
     // 2-byte elements (12^8 u16 5.6 TB/s against 4.3 at 32 KiB, u8 3.6 against 2.4),
     // 32 KiB for wider ones (9^8 fp32 5.7 TB/s against 4.3 at 12 KiB)
@@ -1141,7 +1141,7 @@ int64_t plan_block(Plan* p, int64_t tile_bytes) {
         return false;
     };
     auto vec_ok = [&](int64_t v) {
-        if (best.Ld % v != 0 || p->dst_mis16 % (v * eb) != 0) return false;
+        if (best.Ld % v != 0 || p->dst_mis16 % (v * deb) != 0) return false;
         if (best.chunk >= 0) {
             const int c = best.chunk;
             if (in_dst_run(c) && (best.Ld / best.tile[c]) % v != 0) return false;
@@ -1153,10 +1153,10 @@ int64_t plan_block(Plan* p, int64_t tile_bytes) {
             if (bt.ds[q] % v != 0) return false;
         return true;
     };
-    int v = eb >= 16 ? 1 : 16 / eb;
+    int v = deb >= 16 ? 1 : 16 / deb;
     while (v > 1 && !vec_ok(v)) v >>= 1;
     best.vec = v;
-    block_search(best, eb);
+    block_search(best, eb, deb);
     int64_t tiles = 1;
     for (int q = 0; q < best.nt; ++q) tiles *= (best.ext[q] + best.tile[q] - 1) / best.tile[q];
     for (int q = 0; q < bt.n; ++q) tiles *= bt.ext[q];
@@ -1290,7 +1290,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     case TL_PATH_COLS: path = cols ? TL_PATH_COLS : 0; break;
     case TL_PATH_BLOCK: {
         Plan q = p;
-        path = !casting && plan_block(&q) > 0 ? TL_PATH_BLOCK : 0;
+        path = plan_block(&q) > 0 ? TL_PATH_BLOCK : 0;
         break;
     }
     }
@@ -1307,7 +1307,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     // The block tile takes layouts of canonical rank 3 or more whose panel tile would
     // move short runs on one side (high-rank permutes of short axes) when its own
     // shorter run is 128 bytes or more and at least as long.
-    if (forced == TL_PATH_AUTO && !ranges_meet && srt.n >= 3 && !casting &&
+    if (forced == TL_PATH_AUTO && !ranges_meet && srt.n >= 3 &&
         (path == TL_PATH_PANEL || path == TL_PATH_GENERIC)) {
         Plan q = p;
         const int64_t brun = plan_block(&q);
@@ -1388,7 +1388,7 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
         setup_panel(p);
     } else if (path == TL_PATH_BLOCK) {
         plan_block(&p);
-        p.vec_bytes = p.blk.vec * eb;
+        p.vec_bytes = p.blk.vec * deb;
     } else if (path == TL_PATH_COLS) {
         p.vec_bytes = 16;
         p.tile_cols = (int)p.ext_a;          // elements per pixel

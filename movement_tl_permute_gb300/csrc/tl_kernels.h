@@ -288,6 +288,7 @@ struct BlockArgs {
     int32_t r_lg, GW, GR;
     int32_t cw;                  // consumer warps of a pipeline (cw + 1 warps each)
     int32_t groups;              // pipelines of the CTA (1 or 2)
+    int32_t cast;                // TL_CAST_*: every element converted on the way
     int32_t stage_bytes;
     int32_t ring_bytes;          // one pipeline's stages, on a 128-byte boundary (the same
                                  // bank phase for every pipeline)
@@ -303,8 +304,9 @@ struct BlockArgs {
     dev::DivU32 d_bext[TL_MAX_DIMS];
 };
 int block_smem_bytes(const BlockArgs& a);
-// the kernel for elem_bytes eb storing v elements per step (v in 1 .. 16 / eb)
-const void* block_kernel(int eb, int v);
+// the kernel for elem_bytes eb storing v dst elements per step (v in 1 .. 16 / dst
+// element bytes), converting under `cast` (TL_CAST_*)
+const void* block_kernel(int eb, int v, int cast = TL_CAST_NONE);
 cudaError_t launch_block(int eb, const BlockArgs& a, int grid, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- warp

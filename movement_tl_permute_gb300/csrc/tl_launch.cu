@@ -169,6 +169,14 @@ int get_device_info(DevInfo* out) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kBlockMaxSmem) != cudaSuccess)
                     return TL_ERR_CUDA;
+            // the converting block kernels (fp32 -> 16-bit: pieces of up to 8, 16-bit ->
+            // fp32: up to 4)
+            if (i < 4)
+                for (int v = 1; v <= (i < 2 ? 8 : 4); v <<= 1)
+                    if (cudaFuncSetAttribute(block_kernel(i < 2 ? 4 : 2, v, i + 1),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kBlockMaxSmem) != cudaSuccess)
+                        return TL_ERR_CUDA;
             if (panel_tma_kernel(1 << i) &&
                 cudaFuncSetAttribute(panel_tma_kernel(1 << i),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -385,6 +393,7 @@ BlockArgs block_args(const Plan& p, const TileTuning& tt) {
     a.ls_chunk = b.chunk >= 0 && in_list(b.sax, b.ns, b.chunk) ? 1 : 0;
     a.ld_inner = a.ld_chunk ? (int32_t)(b.Ld / b.tile[b.chunk]) : a.Ld;
     a.ls_inner = a.ls_chunk ? (int32_t)(b.Ls / b.tile[b.chunk]) : a.Ls;
+    a.cast = p.cast;
     a.V = b.vec;
     a.W = a.Ld / a.V;
     a.r_lg = b.r_lg;

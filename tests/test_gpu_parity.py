@@ -604,6 +604,25 @@ def test_cast_on_the_chunk_and_generic_paths(cast):
     assert e.value.name == "TL_ERR_PATH"
 
 
+@pytest.mark.parametrize("cast", sorted(CAST_WIDTHS))
+def test_cast_on_the_block_path(cast):
+    """Converting high-rank permutes of short axes on the block kernel: vector and
+    single-element dst pieces, both store walks, chunked tiles, unaligned bases, and the
+    planner's own choice of the block tile for a layout no other converting kernel
+    takes as a whole."""
+    layouts = (((12,) * 5, (4, 2, 0, 1, 3)), ((9,) * 6, (1, 4, 2, 3, 5, 0)),
+               ((7, 9, 5, 11, 6), (3, 0, 4, 2, 1)), ((8,) * 6, (5, 4, 3, 2, 1, 0)))
+    for i, (shape, perm) in enumerate(layouts):
+        ss, ds = perm_layouts(shape, perm)
+        check_cast(shape, ss, ds, cast, "block", seed=670 + i)
+        check_cast(shape, ss, ds, cast, "block", seed=680 + i, src_off=1, dst_off=(i % 2))
+    shape, perm = (9,) * 6, (1, 4, 2, 3, 5, 0)
+    ss, ds = perm_layouts(shape, perm)
+    seb, _ = CAST_WIDTHS[cast]
+    assert tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, seb, cast=cast)["path"] == "block"
+    check_cast(shape, ss, ds, cast, "auto", seed=690)
+
+
 # ---------------------------------------------------------------------------
 # edge cases
 # ---------------------------------------------------------------------------

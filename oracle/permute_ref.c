@@ -66,7 +66,7 @@ static void permute_range(const unsigned char *src, unsigned char *dst, int ndim
     }
 }
 
-/* Number of OpenMP threads this build can use (1 without OpenMP). */
+/* Number of OpenMP threads the compiled oracle can use (1 without OpenMP). */
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP

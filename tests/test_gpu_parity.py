@@ -753,20 +753,23 @@ def test_block_copy_timeout_is_reported_and_context_survives():
     """A block tile whose src-run copy never lands (the test hook skips the first
     copy of each CTA's first tile): the consumers' bounded waits expire, the status
     word reads TL_ERR_TIMEOUT, and the context still runs the same permute correctly."""
-    shape = (12,) * 5
-    ss, ds = perm_layouts(shape, (4, 2, 0, 1, 3))
-    assert tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, 2, path="block")["path"] == "block"
-    n = int(np.prod(shape))
-    src = torch.zeros(n, dtype=torch.int16, device="cuda")
-    dst = torch.zeros(n, dtype=torch.int16, device="cuda")
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    tl.permute(src, dst, shape, ss, ds, path="block", flags=tl.TL_FLAG_TEST_DROP_HANDOFF,
-               dev_status=status.data_ptr())
-    torch.cuda.synchronize()
-    assert int(status.item()) == -12          # TL_ERR_TIMEOUT
-    status.zero_()
-    check(shape, ss, ds, 2, "block", seed=23, dev_status=status.data_ptr())
-    assert int(status.item()) == 0
+    # one pipeline per CTA (12^5 u16), and two in one CTA (9^6 fp32, 576 threads)
+    for shape, perm, dtype, eb in (((12,) * 5, (4, 2, 0, 1, 3), torch.int16, 2),
+                                   ((9,) * 6, (1, 4, 2, 3, 5, 0), torch.int32, 4)):
+        ss, ds = perm_layouts(shape, perm)
+        plan = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, eb, path="block")
+        assert plan["path"] == "block"
+        n = int(np.prod(shape))
+        src = torch.zeros(n, dtype=dtype, device="cuda")
+        dst = torch.zeros(n, dtype=dtype, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        tl.permute(src, dst, shape, ss, ds, path="block", flags=tl.TL_FLAG_TEST_DROP_HANDOFF,
+                   dev_status=status.data_ptr())
+        torch.cuda.synchronize()
+        assert int(status.item()) == -12          # TL_ERR_TIMEOUT
+        status.zero_()
+        check(shape, ss, ds, eb, "block", seed=23, dev_status=status.data_ptr())
+        assert int(status.item()) == 0
 
 
 # ---------------------------------------------------------------------------

@@ -677,6 +677,179 @@ k_panel_tma(const __grid_constant__ PanelMaps maps, const PanelArgs a) {
     dev::cta_finish(a.cta_times);
 }
 
+// ---------------------------------------------------------------- the skew walk
+// 1-byte elements whose dst rows (the columns a of the plane) sit at an odd pitch Pd:
+// the dst rows start at offsets that differ modulo 16, so no walk of the tile rows
+// gives 16-byte stores.  Instead each lane stores whole 16-byte-aligned pieces of dst
+// rows: the piece of dst row x starting at tile row r is aligned when
+// r = phase(x) (mod 16), and phase(x + 1) = phase(x) + delta with delta = -Pd mod 16,
+// odd, so the 16 columns of a strip take each phase once.  A lane owns a strip of 16
+// columns and a block of 16 tile rows; taking the columns in phase order, the
+// piece of step k starts at row 16 * block + k: the rows the lane reads slide by one
+// per step, a window of 16 stage rows of the strip kept in registers (31 rows read for
+// 16 pieces).  The strips start e columns into the tile, e chosen so that the strip's
+// first column has phase 0; both e and the phases stay the same from tile to tile (the
+// tile sides are multiples of 16), so each tile owns the pieces starting in its rows,
+// and the first tile of a plane row or column also stores the few elements before its
+// first pieces.
+//
+// Stage: tile row r (0 .. kSkewRows + 14) holds the 16-byte blocks around its src
+// bytes (columns 0 .. ta + 14) at r * pitch + 16 * (r / 16), each element at its src
+// offset modulo 16, as the cp.async copy puts it; the lanes of a warp read rows 16
+// apart, which the 16 bytes added per 16 rows put in distinct bank groups.  A row's 16
+// columns of a strip are read as the two aligned 16-byte words around them and
+// shifted into place in registers.
+
+__host__ __device__ constexpr uint32_t inv16(uint32_t d) {           // the inverse of an odd d modulo 16
+    uint32_t x = 1;
+    while (((d * x) & 15u) != 1u) x += 2;
+    return x;
+}
+
+__device__ __forceinline__ const PanelTile skew_tile(int64_t t, const PanelArgs& a) {
+    return panel_tile<false, false>(t, a);
+}
+
+// Start the copies of one tile and its 15 extra rows and columns into the stage `sb`.
+__device__ __forceinline__ void issue_skew(const PanelArgs& a, const PanelTile& ti, uint32_t sb) {
+    const uintptr_t base = reinterpret_cast<uintptr_t>(a.src + ti.so);
+    const uint32_t ncols = (uint32_t)min(a.ext_a - ti.a0, (int64_t)a.ta + 15);
+    const uint32_t nrows = (uint32_t)min(a.ext_b - ti.b0, (int64_t)kSkewRows + 15);
+    const uint32_t nblk = (uint32_t)a.nblk, pitch = (uint32_t)a.pitch;
+    const uint32_t n = nrows * nblk;
+    for (uint32_t g = threadIdx.x; g < n; g += blockDim.x) {
+        const uint32_t r = dev::div_u32(g, a.d_nblk), k = g - r * nblk;
+        const uintptr_t row = base + (uintptr_t)((int64_t)r * a.ss_b);
+        const uint32_t blocks = ((uint32_t)(row & 15) + ncols + 15) >> 4;
+        if (k < blocks)
+            cp_async16(sb + r * pitch + 16 * (r >> 4) + 16 * k, (row & ~uintptr_t(15)) + 16 * k);
+    }
+}
+
+// Store one landed tile (stage at shared-window offset st0) as 16-byte dst pieces.
+template <uint32_t DELTA>
+__device__ __forceinline__ void drain_skew(const PanelArgs& a, const PanelTile& ti,
+                                           uint32_t st0) {
+    constexpr uint32_t DINV = inv16(DELTA);
+    extern __shared__ __align__(16) uint8_t smem_sk[];
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t blk = lane & 15, strip = 2 * warp + (lane >> 4);
+    const uint32_t ta = (uint32_t)a.ta, pitch = (uint32_t)a.pitch;
+    uint8_t* const d = a.dst + ti.dof;
+    const int64_t Pd = a.ds_a;
+    // the tile's first column has phase rho0; strips start at column e, of phase 0
+    const uint32_t rho0 = (16u - ((uint32_t)reinterpret_cast<uintptr_t>(d) & 15u)) & 15u;
+    const uint32_t e = ((16u - rho0) * DINV) & 15u;
+    const uint32_t mis0 = (uint32_t)reinterpret_cast<uintptr_t>(a.src + ti.so) & 15u;
+    const uint32_t ds16 = (uint32_t)a.vdelta;            // src row pitch mod 16
+    const uint32_t xlim = (uint32_t)min(a.ext_a - ti.a0, (int64_t)ta + 16);
+    const uint32_t ylim = (uint32_t)min(a.ext_b - ti.b0, (int64_t)kSkewRows + 16);
+    // stage byte of (row r, column x)
+    auto at = [&](uint32_t r, uint32_t x) -> uint8_t {
+        return smem_sk[st0 + r * pitch + 16 * (r >> 4) + ((mis0 + r * ds16) & 15u) + x];
+    };
+    // the lane's 16 columns of stage row 16 * blk + c, in column order
+    const uint32_t lbase = st0 + blk * (16 * pitch + 16) + 16 * strip;
+    auto load_row = [&](uint32_t c, uint32_t (&w)[4]) {
+        const uint32_t u = ((mis0 + c * ds16) & 15u) + e;          // 0 .. 30
+        const uint32_t off = lbase + c * pitch + 16 * (c >> 4) + (u & 16u);
+        const uint4 A = *reinterpret_cast<const uint4*>(&smem_sk[off]);
+        const uint4 B = *reinterpret_cast<const uint4*>(&smem_sk[off + 16]);
+        const uint32_t lo = u & 15u;
+        const bool h2 = (lo & 8u) != 0, h1 = (lo & 4u) != 0;
+        const uint32_t v[6] = {h2 ? A.z : A.x, h2 ? A.w : A.y, h2 ? B.x : A.z,
+                               h2 ? B.y : A.w, h2 ? B.z : B.x, h2 ? B.w : B.y};
+        uint32_t y[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) y[i] = h1 ? v[i + 1] : v[i];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = __funnelshift_r(y[i], y[i + 1], 8 * (lo & 3u));
+    };
+    uint32_t W[16][4];
+#pragma unroll
+    for (uint32_t c = 0; c < 16; ++c) load_row(c, W[c]);
+    const uint32_t x0 = e + 16 * strip;
+    uint8_t* const dl = d + (int64_t)x0 * Pd + 16 * blk;
+#pragma unroll
+    for (uint32_t k = 0; k < 16; ++k) {
+        // step k: column x0 + j of phase k, rows 16 * blk + k .. + 15 (window slots)
+        const uint32_t j = (k * DINV) & 15u, wi = j >> 2, sel = (j & 3u) | (((j & 3u) + 4u) << 4);
+        uint32_t o[4];
+#pragma unroll
+        for (uint32_t q = 0; q < 4; ++q) {
+            const uint32_t t0 = __byte_perm(W[(k + 4 * q) & 15][wi], W[(k + 4 * q + 1) & 15][wi], sel);
+            const uint32_t t1 = __byte_perm(W[(k + 4 * q + 2) & 15][wi], W[(k + 4 * q + 3) & 15][wi], sel);
+            o[q] = __byte_perm(t0, t1, 0x5410);
+        }
+        const uint32_t r0 = 16 * blk + k;
+        if (x0 + j < xlim && r0 < ylim) {
+            uint8_t* dp = dl + (int64_t)j * Pd + k;
+            if (r0 + 16 <= ylim) {
+                dev::stg128(dp, make_uint4(o[0], o[1], o[2], o[3]));
+            } else {       // the last rows of the plane
+#pragma unroll
+                for (uint32_t i = 0; i < 16; ++i)
+                    if (r0 + i < ylim) dp[i] = (uint8_t)(o[i >> 2] >> (8 * (i & 3u)));
+            }
+        }
+        if (k < 15) load_row(16 + k, W[k]);
+    }
+    // Elements no tile's pieces reach: the rows before each column's first piece (the
+    // plane's first row block), and the columns before the first strip (its first
+    // column block), element by element.
+    if (ti.b0 == 0) {
+        const uint32_t xs = ti.a0 == 0 ? 0u : e, xe = min(ta + e, xlim);
+        const uint32_t nr = min(15u, ylim);
+        if (xe > xs) {
+            const uint32_t n = (xe - xs) * 16;
+            for (uint32_t f = threadIdx.x; f < n; f += blockDim.x) {
+                const uint32_t r = f & 15u, x = xs + (f >> 4);
+                if (r < nr) d[(int64_t)x * Pd + r] = at(r, x);
+            }
+        }
+    }
+    if (ti.a0 == 0) {
+        const uint32_t xe = min(e, xlim), nr = min((uint32_t)kSkewRows, ylim);
+        const uint32_t n = xe * kSkewRows;
+        for (uint32_t f = threadIdx.x; f < n; f += blockDim.x) {
+            const uint32_t r = f % kSkewRows, x = f / kSkewRows;
+            if (r < nr) d[(int64_t)x * Pd + r] = at(r, x);
+        }
+    }
+}
+
+// Persistent CTAs of 32 * warps threads, a ring of kSkewStages stages filled by
+// cp.async (every thread copies part of each tile, then all wait and drain it).
+template <uint32_t DELTA>
+__global__ void __launch_bounds__(kPanelThreads, 1) k_panel_skew(const PanelArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const uint32_t sbase = dev::smem_addr(smem);
+    const uint32_t stage = (uint32_t)a.stage_bytes;
+    dev::grid_dependency_wait();
+    dev::allow_dependent_launch();
+    dev::cta_start(a.cta_times);
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t mine = first < a.tiles ? (a.tiles - first + step - 1) / step : 0;
+    for (int s = 0; s < kSkewStages - 1; ++s) {
+        if (s < mine) issue_skew(a, skew_tile(first + s * step, a), sbase + s * stage);
+        cp_async_commit();
+    }
+    uint32_t slot = 0, ahead = kSkewStages - 1;
+    for (int64_t i = 0; i < mine; ++i) {
+        const int64_t nxt = i + kSkewStages - 1;
+        if (nxt < mine) issue_skew(a, skew_tile(first + nxt * step, a), sbase + ahead * stage);
+        cp_async_commit();
+        cp_async_wait<kSkewStages - 1>();
+        __syncthreads();
+        drain_skew<DELTA>(a, skew_tile(first + i * step, a), slot * stage);
+        __syncthreads();
+        slot = slot + 1 == kSkewStages ? 0 : slot + 1;
+        ahead = ahead + 1 == kSkewStages ? 0 : ahead + 1;
+    }
+    cp_async_wait<0>();
+    dev::cta_finish(a.cta_times);
+}
+
 }  // namespace
 
 // The planner takes TMA phase maps for 2-byte elements only (measured; the other
@@ -707,6 +880,28 @@ const void* panel_kernel(int eb, bool vec, bool am) {
     case 8: return vec ? pick<8, true>(am) : pick<8, false>(am);
     default: return pick<16, false>(am);
     }
+}
+
+const void* panel_skew_kernel(int delta) {
+    switch (delta) {
+    case 1: return reinterpret_cast<const void*>(&k_panel_skew<1>);
+    case 3: return reinterpret_cast<const void*>(&k_panel_skew<3>);
+    case 5: return reinterpret_cast<const void*>(&k_panel_skew<5>);
+    case 7: return reinterpret_cast<const void*>(&k_panel_skew<7>);
+    case 9: return reinterpret_cast<const void*>(&k_panel_skew<9>);
+    case 11: return reinterpret_cast<const void*>(&k_panel_skew<11>);
+    case 13: return reinterpret_cast<const void*>(&k_panel_skew<13>);
+    case 15: return reinterpret_cast<const void*>(&k_panel_skew<15>);
+    default: return nullptr;
+    }
+}
+
+cudaError_t launch_panel_skew(const PanelArgs& a, int grid, int block, int smem,
+                              cudaStream_t st, bool pdl) {
+    using Kernel = void (*)(const PanelArgs);
+    const Kernel k = reinterpret_cast<Kernel>(panel_skew_kernel((int)((16 - (a.ds_a & 15)) & 15)));
+    if (!k || block <= 0 || block > kPanelThreads || block % 32 != 0) return cudaErrorInvalidValue;
+    return launch_kernel(k, dim3(grid), dim3(block), smem, st, pdl, a);
 }
 
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,

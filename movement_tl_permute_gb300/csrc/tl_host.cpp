@@ -760,8 +760,39 @@ void panel_merge_a(Plan* p) {
     }
 }
 
+// The skew walk (1-byte elements whose dst rows sit at an odd pitch, one a and one b
+// axis): no tile row's dst run is on the 16-byte grid, so the word walk would pack
+// every element from a 1-byte shared load; the skew walk stores 16-byte pieces of the
+// dst rows instead.  Planes of at least 64 x 64.
+static bool panel_skew_ok(const Plan& p) {
+    return p.eb == 1 && p.cast == TL_CAST_NONE && !p.panel_elem_stores && p.panel_b1 == 0 &&
+           p.panel_a1 == 0 && p.ds_a > 0 && (p.ds_a & 1) == 1 && p.ss_b > 0 && p.ext_a >= 64 &&
+           p.ext_b >= 64;
+}
+
 void plan_panel(Plan* p, int tile_bytes, int rows) {
     const int eb = p->eb;
+    p->panel_skew = false;
+    if (panel_skew_ok(*p)) {
+        // tiles of 256 x 256 (8 warps) or, asked for tiles of 32 KiB or less, 128 x 256
+        const int warps = tile_bytes > 0 && tile_bytes <= 32768 ? 4 : 8;
+        p->panel_skew = true;
+        p->panel_skew_warps = warps;
+        p->tile_cols = 32 * warps;
+        p->tile_rows = kSkewRows;
+        p->panel_mode = 0;
+        p->panel_aligned = p->panel_vec = p->panel_run = p->panel_words = false;
+        p->panel_tma = p->panel_phase = false;
+        p->panel_wrot_s = p->panel_wrot_m = 0;
+        p->pitch = skew_pitch(p->tile_cols);
+        p->panel_nblk = p->tile_cols / 16 + 2;
+        p->panel_stage = skew_stage_bytes(p->tile_cols);
+        const int64_t na = (p->ext_a + p->tile_cols - 1) / p->tile_cols;
+        const int64_t nb = (p->ext_b + kSkewRows - 1) / kSkewRows;
+        p->tiles = na * nb * p->batch_total;
+        p->vec_bytes = 16;
+        return;
+    }
     const bool tiny = p->ext_a <= 16 || p->ext_b <= 16;
     if (tile_bytes <= 0) tile_bytes = tiny ? 24576 : 32768;
     const int64_t E = tile_bytes / eb;

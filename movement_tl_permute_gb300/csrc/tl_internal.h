@@ -93,6 +93,8 @@ struct Plan {
     bool panel_phase = false;           // PANEL: phase-major stages (TMA or cp.async)
     int panel_phi_lg = 0;               // PANEL (TMA): log2 of the phase count phi
     int panel_phase_bytes = 0;          // PANEL (TMA): shared-memory bytes of one phase block
+    bool panel_skew = false;            // PANEL: the skew walk (1-byte, odd dst row pitch)
+    int panel_skew_warps = 0;           // PANEL (skew): warps per CTA, 32 columns of a each
     int64_t tiles = 0;
     BlockPlan blk;                      // BLOCK
 
@@ -113,6 +115,19 @@ int make_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
 // for; plan_panel shrinks a tile until its ring fits.
 constexpr int kPanelStages = 3;
 constexpr int kPanelMaxSmem = 160 * 1024;
+
+// The panel path's skew walk (1-byte elements whose dst rows sit at an odd pitch):
+// tiles of 32 * warps columns of a by kSkewRows rows of b, each staged with up to 15
+// rows and 15 columns past it, in a ring of kSkewStages stages.  Stage row r holds
+// the 16-byte blocks around the row's src bytes at r * pitch + 16 * (r / 16), pitch =
+// columns + 32 bytes.
+constexpr int kSkewRows = 256;
+constexpr int kSkewStages = 2;
+constexpr int skew_pitch(int ta) { return ta + 32; }
+constexpr int skew_stage_bytes(int ta) {
+    return ((kSkewRows + 15) * skew_pitch(ta) + 16 * (kSkewRows / 16 + 1) + 127) / 128 * 128;
+}
+static_assert(kSkewStages * skew_stage_bytes(256) <= kPanelMaxSmem, "skew ring too large");
 
 // Tile shape and shared-memory layout of the panel path for tiles of about
 // tile_bytes (0: the default size; tuning options may redo it).  Measured on

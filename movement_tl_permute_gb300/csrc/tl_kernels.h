@@ -223,7 +223,8 @@ struct PanelArgs {
     int32_t drop_load;           // test hook: skip one phase load of the first tile
     // a may be two src-contiguous axes merged (amerged = 1): a = hi * a1 + lo, dst
     // offset lo * ds_a + hi * ds_a2 (a fits 32 bits)
-    int32_t amerged, pad3;
+    int32_t amerged;
+    int32_t skew;                // the skew walk's kernel (k_panel_skew) is launched
     int64_t ds_a2;
     dev::DivU32 d_a1;
     int64_t timeout_ns;
@@ -242,6 +243,11 @@ const void* panel_tma_kernel(int eb);
 const void* panel_kernel(int eb, bool vec, bool am);
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,
                          bool pdl);
+// The skew walk (1-byte elements, dst row pitch odd): one kernel per dst row pitch
+// modulo 16 (`delta` = -pitch mod 16, odd), 32 columns of a per warp of `block`.
+const void* panel_skew_kernel(int delta);
+cudaError_t launch_panel_skew(const PanelArgs& a, int grid, int block, int smem,
+                              cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- block
 // A tile of up to four axes (T) that is a few long contiguous runs on both sides.

@@ -177,6 +177,11 @@ int get_device_info(DevInfo* out) {
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kBlockMaxSmem) != cudaSuccess)
                         return TL_ERR_CUDA;
+            for (int delta = 1; i == 0 && delta < 16; delta += 2)
+                if (cudaFuncSetAttribute(panel_skew_kernel(delta),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPanelMaxSmem) != cudaSuccess)
+                    return TL_ERR_CUDA;
             if (panel_tma_kernel(1 << i) &&
                 cudaFuncSetAttribute(panel_tma_kernel(1 << i),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -496,6 +501,22 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         }
         break;
     case TL_PATH_PANEL:
+        if (p.panel_skew) {
+            l.block = 32 * p.panel_skew_warps;
+            l.smem = kSkewStages * p.panel_stage;
+            if (sms) {
+                int per_sm = 0;
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                        &per_sm, panel_skew_kernel((int)((16 - (p.ds_a & 15)) & 15)), l.block,
+                        l.smem) != cudaSuccess ||
+                    per_sm < 1) {
+                    cudaGetLastError();
+                    per_sm = 1;
+                }
+                l.grid = cap_grid(p.tiles, sms * per_sm, max_ctas);
+            }
+            break;
+        }
         l.block = kPanelThreads;
         l.smem = kPanelStages * p.panel_stage;   // <= kPanelMaxSmem for tiles of <= 32 KiB
         if (p.panel_tma) l.smem += 128;           // the stages start on a 128-byte boundary
@@ -955,6 +976,13 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             a.d_nblk = dev::make_divu32((uint32_t)p.panel_nblk);
             a.aligned = 0;
         }
+        if (p.panel_skew) {
+            a.skew = 1;
+            a.nblk = p.panel_nblk;
+            a.d_nblk = dev::make_divu32((uint32_t)p.panel_nblk);
+            err = launch_panel_skew(a, l.grid, l.block, l.smem, st, pdl);
+            break;
+        }
         if (p.panel_tma) {
             PanelMaps maps;
             // 64-byte L2 fills unless the caller asked for another (measured best for
@@ -1104,7 +1132,7 @@ int tl_plan(const void* src, const void* dst, int ndim, const int64_t* shape,
     }
     info.panel_mode = p.panel_tma ? 2 : p.panel_phase ? 3 : p.panel_mode;
     info.panel_b1 = (int32_t)p.panel_b1;
-    info.panel_vec = p.panel_vec ? 1 : p.panel_run ? 2 : p.panel_words ? 3 : 0;
+    info.panel_vec = p.panel_vec ? 1 : p.panel_run ? 2 : p.panel_words ? 3 : p.panel_skew ? 4 : 0;
     info.panel_wrot = p.panel_wrot_s | (p.panel_wrot_m << 8);
     info.panel_a1 = (int32_t)p.panel_a1;
     info.block_runs = p.path == TL_PATH_BLOCK ? 1 << p.blk.r_lg : 0;

@@ -278,6 +278,41 @@ def test_panel_vector_stores(eb, kib):
         check(shape, ss, ds, eb, "panel", seed=330 + i, dst_off=1, panel_tile_kib=kib)
 
 
+def _skew_cases():
+    """1-byte plane transposes whose dst rows sit at an odd pitch: every pitch residue
+    modulo 16, ragged tiles on both sides, planes of exactly whole tiles and of the
+    smallest size the walk takes, padded src rows, and batch items whose dst bases
+    differ modulo 16 (a different column phase per item)."""
+    out = []
+    for i, delta in enumerate(range(1, 16, 2)):
+        B, A = 300 + 37 * i, 270 + 53 * i             # b: dst-contiguous, a: src-contiguous
+        Pd = B + ((-B - delta) % 16)                    # dst row pitch, -Pd = delta mod 16
+        Ps = A + (i % 3) * 5
+        out.append(((B, A), (Ps, 1), (1, Pd)))
+    out.append(((512, 512), (512, 1), (1, 513)))
+    out.append(((64, 64), (65, 1), (1, 67)))
+    out.append(((1000, 700), (707, 1), (1, 1003)))
+    out.append(((3, 130, 200), (200 * 131 + 7, 200, 1), (200 * 131 + 5, 1, 131)))
+    return out
+
+
+@pytest.mark.parametrize("kib", [0, 32])
+def test_panel_skew_walk(kib):
+    """The skew walk (16-byte pieces of dst rows at an odd pitch, 256- and 128-column
+    tiles) against the oracle, with aligned and unaligned bases; the same layouts with
+    element stores forced take the word walk."""
+    for i, (shape, ss, ds) in enumerate(_skew_cases()):
+        for so, do in ((0, 0), (1, 0), (0, 7), (13, 5)):
+            plan = tl.tl_plan((1 << 20) + so, (1 << 36) + do, shape, ss, ds, 1, path="panel",
+                              panel_tile_kib=kib)
+            assert plan["panel_vec"] == 4 and plan["tile_cols"] == (128 if kib else 256), plan
+            check(shape, ss, ds, 1, "panel", seed=900 + 10 * i + so + do, src_off=so,
+                  dst_off=do, panel_tile_kib=kib)
+        off = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, 1, path="panel",
+                         flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
+        assert off["panel_vec"] != 4
+
+
 @pytest.mark.parametrize("eb", [2, 4, 8])
 def test_panel_tma_phase_maps(eb):
     """Block rows whose pitch is off the 16-byte grid, loaded by TMA phase maps (rows

@@ -465,6 +465,34 @@ def _vec_rows_ok(tb, eb):
     return (tb * eb) % 16 == 0 and tb * eb >= 128 and 4 * units >= 24 * groups
 
 
+def _check_skew_layout(p):
+    """The skew walk's stage (1-byte elements, odd dst row pitch): tiles of 32 columns
+    of a per warp by 256 rows of b, rows of ta + 32 bytes 16 bytes further per 16 rows,
+    two stages.  Lane l of warp w reads, for each of its window rows c = 0..30, the two
+    aligned 16-byte words around its 16 columns of stage row 16 (l mod 16) + c (strip
+    2w + l // 16): for every src offset u = 0..30 of those columns both reads must be
+    conflict-free on the bank model (8 lanes a wavefront), and the copy of a row (16-byte
+    blocks, consecutive threads) too."""
+    ta, tb, pitch = p["tile_cols"], p["tile_rows"], p["pitch"]
+    assert tb == 256 and ta in (128, 256) and pitch == ta + 32
+    assert p["panel_vec"] == 4 and p["vec_bytes"] == 16 and p["panel_mode"] == 0
+    stage = -(-(271 * pitch + 16 * 17) // 128) * 128
+    assert p["smem_bytes"] == 2 * stage and p["block"] in (0, ta)     # 32 threads per 32 columns
+    row = lambda r: r * pitch + 16 * (r // 16)
+    assert row(270) + pitch <= stage
+    for w in range(ta // 32):
+        for c in range(31):
+            for u in range(31):
+                for half in (0, 16):
+                    offs = [(row(16 * (l % 16) + c) + 16 * (2 * w + l // 16) + (u & 16) + half) // 16
+                            for l in range(32)]
+                    assert L.bank_conflict_degree(offs, 16, "hardware") == 1, (w, c, u)
+    nblk = ta // 16 + 2
+    for g0 in range(0, 271 * nblk, 32):
+        offs = [(row(g // nblk) + 16 * (g % nblk)) // 16 for g in range(g0, min(g0 + 32, 271 * nblk))]
+        assert L.bank_conflict_degree(offs, 16, "hardware") <= 2
+
+
 @pytest.mark.parametrize("shape,perm,eb", PANEL_LAYOUTS)
 def test_panel_layout_against_the_bank_model(shape, perm, eb):
     """The shared-memory layout the planner picks for the panel kernel, replayed
@@ -530,6 +558,12 @@ def test_panel_layout_against_the_bank_model(shape, perm, eb):
         ext_b = [x for x, d in zip(p["extent"], p["dst_str"]) if d == 1][0]
         ds_a = [d for x, d in zip(p["src_str"], p["dst_str"]) if x == 1][0]
         run = not vec and eb <= 4 and tb <= 16 and tb == ext_b and ds_a == tb and not b1
+        # else, 1-byte elements at an odd dst row pitch (planes of 64 x 64 or more):
+        # 16-byte dst pieces by the skew walk
+        ext_a = [x for x, s_ in zip(p["extent"], p["src_str"]) if s_ == 1][0]
+        if not vec and not run and eb == 1 and not b1 and ds_a % 2 == 1 and min(ext_a, ext_b) >= 64:
+            _check_skew_layout(p)
+            return
         # else 4-byte words per dst row for 1-byte elements (one b axis)
         words = not vec and not run and eb == 1 and not b1
         assert p["panel_vec"] == (1 if vec else 2 if run else 3 if words else 0)
@@ -664,12 +698,12 @@ def test_planner_invariants_on_random_layouts():
             if plan["path"] == "panel":
                 # store and copy modes, and the panel ring within its shared memory
                 mode, store = plan["panel_mode"], plan["panel_vec"]
-                assert mode in (0, 1, 2, 3) and store in (0, 1, 2, 3)
+                assert mode in (0, 1, 2, 3) and store in (0, 1, 2, 3, 4)
                 assert plan["smem_bytes"] <= 160 * 1024 + 128
-                assert plan["vec_bytes"] == (16 if store in (1, 2) else 4 if store == 3 else eb)
+                assert plan["vec_bytes"] == (16 if store in (1, 2, 4) else 4 if store == 3 else eb)
                 if mode in (2, 3):          # phase-major stages: rows off the 16-byte grid
                     assert store == 0 and eb in (2, 4, 8) and (mode == 2) == (eb == 2)
-                if store == 3:
+                if store in (3, 4):
                     assert eb == 1 and mode == 0
                 seen.add(("panel", mode, store))
             if plan["path"] == "cols":

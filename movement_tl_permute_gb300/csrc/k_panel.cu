@@ -710,25 +710,50 @@ __device__ __forceinline__ const PanelTile skew_tile(int64_t t, const PanelArgs&
     return panel_tile<false, false>(t, a);
 }
 
-// Start the copies of one tile and its 15 extra rows and columns into the stage `sb`.
-__device__ __forceinline__ void issue_skew(const PanelArgs& a, const PanelTile& ti, uint32_t sb) {
-    const uintptr_t base = reinterpret_cast<uintptr_t>(a.src + ti.so);
+// Start the copies of one tile and its 15 extra rows and columns into the stage `sb`:
+// thread t copies block k = t mod nblk of rows t / nblk, + rstep, + 2 rstep, ...
+// (rstep = threads / nblk), so consecutive threads read consecutive blocks of a row.
+__device__ __forceinline__ void issue_skew(const PanelArgs& a, const PanelTile& ti, uint32_t sb,
+                                           uint32_t k, uint32_t r0, uint32_t rstep) {
     const uint32_t ncols = (uint32_t)min(a.ext_a - ti.a0, (int64_t)a.ta + 15);
     const uint32_t nrows = (uint32_t)min(a.ext_b - ti.b0, (int64_t)kSkewRows + 15);
-    const uint32_t nblk = (uint32_t)a.nblk, pitch = (uint32_t)a.pitch;
-    const uint32_t n = nrows * nblk;
-    for (uint32_t g = threadIdx.x; g < n; g += blockDim.x) {
-        const uint32_t r = dev::div_u32(g, a.d_nblk), k = g - r * nblk;
-        const uintptr_t row = base + (uintptr_t)((int64_t)r * a.ss_b);
-        const uint32_t blocks = ((uint32_t)(row & 15) + ncols + 15) >> 4;
-        if (k < blocks)
+    const uint32_t pitch = (uint32_t)a.pitch;
+    const int64_t rowstep = (int64_t)rstep * a.ss_b;
+    uintptr_t row = reinterpret_cast<uintptr_t>(a.src + ti.so + (int64_t)r0 * a.ss_b);
+    for (uint32_t r = r0; r < nrows; r += rstep, row += rowstep)
+        if (16 * k < (uint32_t)(row & 15) + ncols)       // block k holds a byte of the row
             cp_async16(sb + r * pitch + 16 * (r >> 4) + 16 * k, (row & ~uintptr_t(15)) + 16 * k);
-    }
 }
 
-// Store one landed tile (stage at shared-window offset st0) as 16-byte dst pieces.
+// The tile's column phase: its strips start at column e (the first column of phase 0);
+// mis0 is the offset modulo 16 of its first src element.
+struct SkewPhase {
+    uint32_t e, mis0;
+};
+template <uint32_t DELTA>
+__device__ __forceinline__ SkewPhase skew_phase(const PanelArgs& a, const PanelTile& ti) {
+    constexpr uint32_t DINV = inv16(DELTA);
+    const uint32_t rho0 = (16u - ((uint32_t)reinterpret_cast<uintptr_t>(a.dst + ti.dof) & 15u)) & 15u;
+    SkewPhase ph;
+    ph.e = ((16u - rho0) * DINV) & 15u;
+    ph.mis0 = (uint32_t)reinterpret_cast<uintptr_t>(a.src + ti.so) & 15u;
+    return ph;
+}
+
+// Row c (0..30) of a lane's window, relative to the lane's first row: the byte offset
+// of the aligned 16-byte word holding the row's strip column 0 (bits 0..23) and that
+// column's offset inside it (bits 24..27); the same for every lane of the tile.
+__device__ __forceinline__ uint32_t skew_row_entry(const PanelArgs& a, const SkewPhase& ph,
+                                                   uint32_t c) {
+    const uint32_t u = ((ph.mis0 + c * (uint32_t)a.vdelta) & 15u) + ph.e;       // 0 .. 30
+    return (c * (uint32_t)a.pitch + 16 * (c >> 4) + (u & 16u)) | ((u & 15u) << 24);
+}
+
+// Store one landed tile (stage at shared-window offset st0) as 16-byte dst pieces;
+// rowtab holds the tile's skew_row_entry values.
 template <uint32_t DELTA>
 __device__ __forceinline__ void drain_skew(const PanelArgs& a, const PanelTile& ti,
+                                           const SkewPhase& ph, const uint32_t* rowtab,
                                            uint32_t st0) {
     constexpr uint32_t DINV = inv16(DELTA);
     extern __shared__ __align__(16) uint8_t smem_sk[];
@@ -737,10 +762,7 @@ __device__ __forceinline__ void drain_skew(const PanelArgs& a, const PanelTile& 
     const uint32_t ta = (uint32_t)a.ta, pitch = (uint32_t)a.pitch;
     uint8_t* const d = a.dst + ti.dof;
     const int64_t Pd = a.ds_a;
-    // the tile's first column has phase rho0; strips start at column e, of phase 0
-    const uint32_t rho0 = (16u - ((uint32_t)reinterpret_cast<uintptr_t>(d) & 15u)) & 15u;
-    const uint32_t e = ((16u - rho0) * DINV) & 15u;
-    const uint32_t mis0 = (uint32_t)reinterpret_cast<uintptr_t>(a.src + ti.so) & 15u;
+    const uint32_t e = ph.e, mis0 = ph.mis0;
     const uint32_t ds16 = (uint32_t)a.vdelta;            // src row pitch mod 16
     const uint32_t xlim = (uint32_t)min(a.ext_a - ti.a0, (int64_t)ta + 16);
     const uint32_t ylim = (uint32_t)min(a.ext_b - ti.b0, (int64_t)kSkewRows + 16);
@@ -751,11 +773,11 @@ __device__ __forceinline__ void drain_skew(const PanelArgs& a, const PanelTile& 
     // the lane's 16 columns of stage row 16 * blk + c, in column order
     const uint32_t lbase = st0 + blk * (16 * pitch + 16) + 16 * strip;
     auto load_row = [&](uint32_t c, uint32_t (&w)[4]) {
-        const uint32_t u = ((mis0 + c * ds16) & 15u) + e;          // 0 .. 30
-        const uint32_t off = lbase + c * pitch + 16 * (c >> 4) + (u & 16u);
+        const uint32_t t = rowtab[c];
+        const uint32_t off = lbase + (t & 0xFFFFFFu);
         const uint4 A = *reinterpret_cast<const uint4*>(&smem_sk[off]);
         const uint4 B = *reinterpret_cast<const uint4*>(&smem_sk[off + 16]);
-        const uint32_t lo = u & 15u;
+        const uint32_t lo = t >> 24;
         const bool h2 = (lo & 8u) != 0, h1 = (lo & 4u) != 0;
         const uint32_t v[6] = {h2 ? A.z : A.x, h2 ? A.w : A.y, h2 ? B.x : A.z,
                                h2 ? B.y : A.w, h2 ? B.z : B.x, h2 ? B.w : B.y};
@@ -823,6 +845,7 @@ __device__ __forceinline__ void drain_skew(const PanelArgs& a, const PanelTile& 
 template <uint32_t DELTA>
 __global__ void __launch_bounds__(kPanelThreads, 1) k_panel_skew(const PanelArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ uint32_t rowtab[32];
     const uint32_t sbase = dev::smem_addr(smem);
     const uint32_t stage = (uint32_t)a.stage_bytes;
     dev::grid_dependency_wait();
@@ -830,18 +853,26 @@ __global__ void __launch_bounds__(kPanelThreads, 1) k_panel_skew(const PanelArgs
     dev::cta_start(a.cta_times);
     const int64_t first = blockIdx.x, step = gridDim.x;
     const int64_t mine = first < a.tiles ? (a.tiles - first + step - 1) / step : 0;
+    // this thread's copy block and first row (threads past rstep * nblk copy nothing)
+    const uint32_t nblk = (uint32_t)a.nblk;
+    const uint32_t r0 = dev::div_u32(threadIdx.x, a.d_nblk), k = threadIdx.x - r0 * nblk;
+    const uint32_t rstep = dev::div_u32(blockDim.x, a.d_nblk);
+    const uint32_t cr0 = r0 < rstep ? r0 : (uint32_t)kSkewRows + 16;
     for (int s = 0; s < kSkewStages - 1; ++s) {
-        if (s < mine) issue_skew(a, skew_tile(first + s * step, a), sbase + s * stage);
+        if (s < mine) issue_skew(a, skew_tile(first + s * step, a), sbase + s * stage, k, cr0, rstep);
         cp_async_commit();
     }
     uint32_t slot = 0, ahead = kSkewStages - 1;
     for (int64_t i = 0; i < mine; ++i) {
         const int64_t nxt = i + kSkewStages - 1;
-        if (nxt < mine) issue_skew(a, skew_tile(first + nxt * step, a), sbase + ahead * stage);
+        if (nxt < mine) issue_skew(a, skew_tile(first + nxt * step, a), sbase + ahead * stage, k, cr0, rstep);
         cp_async_commit();
+        const PanelTile ti = skew_tile(first + i * step, a);
+        const SkewPhase ph = skew_phase<DELTA>(a, ti);
+        if (threadIdx.x < 31) rowtab[threadIdx.x] = skew_row_entry(a, ph, threadIdx.x);
         cp_async_wait<kSkewStages - 1>();
         __syncthreads();
-        drain_skew<DELTA>(a, skew_tile(first + i * step, a), slot * stage);
+        drain_skew<DELTA>(a, ti, ph, rowtab, slot * stage);
         __syncthreads();
         slot = slot + 1 == kSkewStages ? 0 : slot + 1;
         ahead = ahead + 1 == kSkewStages ? 0 : ahead + 1;

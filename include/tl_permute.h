@@ -227,7 +227,8 @@ typedef struct tl_permute_opts {
     int32_t tile_group;   /* tile rows visited together (tile and panel visit order;
                              default: the whole extent) */
     int32_t tile_stages;  /* shared-memory ring depth: 2..12 (tile, 128-row tiles),
-                             2..6 (tile, 256-row tiles); cluster: staging ring, 1..8 */
+                             2..6 (tile, 256-row tiles); cluster: staging ring, 1..8;
+                             panel skew walk (panel_vec 4): 1 or 2 stages per CTA */
     int32_t tile_ctas_per_sm;  /* resident CTAs per SM the grid is sized for (block
                                   path: at most this many, 1..4) */
     int32_t tile_l2_promotion; /* L2 fill size of the TMA loads (tile path, panel phase
@@ -299,7 +300,9 @@ typedef struct tl_plan_info {
                                       runs along their rows, 2 as 16-byte pieces of the
                                       single dst run of a tile (a short dst-contiguous
                                       axis), 3 as 4-byte words per dst row (1-byte block
-                                      rows off the 16-byte grid), 0 element by element
+                                      rows off the 16-byte grid), 4 as 16-byte pieces of
+                                      dst rows at an odd pitch (1-byte elements, the skew
+                                      walk), 0 element by element
                                       (4-byte words for packed rows of 1- and 2-byte
                                       elements) */
     int32_t panel_wrot;            /* panel path, modes stored as 4-byte words: the lanes'

@@ -840,10 +840,12 @@ __device__ __forceinline__ void drain_skew(const PanelArgs& a, const PanelTile& 
     }
 }
 
-// Persistent CTAs of 32 * warps threads, a ring of kSkewStages stages filled by
-// cp.async (every thread copies part of each tile, then all wait and drain it).
-template <uint32_t DELTA>
-__global__ void __launch_bounds__(kPanelThreads, 1) k_panel_skew(const PanelArgs a) {
+// Persistent CTAs of 32 * warps threads, a ring of STAGES stages filled by cp.async
+// (every thread copies part of each tile, then all wait and drain it).  One stage per
+// CTA runs two CTAs per SM (at most 128 registers a thread), each loading while the
+// other drains; two stages run one CTA per SM that loads the next tile while it drains.
+template <uint32_t DELTA, int STAGES>
+__global__ void __launch_bounds__(kPanelThreads, STAGES == 1 ? 2 : 1) k_panel_skew(const PanelArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint32_t rowtab[32];
     const uint32_t sbase = dev::smem_addr(smem);
@@ -858,24 +860,24 @@ __global__ void __launch_bounds__(kPanelThreads, 1) k_panel_skew(const PanelArgs
     const uint32_t r0 = dev::div_u32(threadIdx.x, a.d_nblk), k = threadIdx.x - r0 * nblk;
     const uint32_t rstep = dev::div_u32(blockDim.x, a.d_nblk);
     const uint32_t cr0 = r0 < rstep ? r0 : (uint32_t)kSkewRows + 16;
-    for (int s = 0; s < kSkewStages - 1; ++s) {
+    for (int s = 0; s < STAGES - 1; ++s) {
         if (s < mine) issue_skew(a, skew_tile(first + s * step, a), sbase + s * stage, k, cr0, rstep);
         cp_async_commit();
     }
-    uint32_t slot = 0, ahead = kSkewStages - 1;
+    uint32_t slot = 0, ahead = STAGES - 1;
     for (int64_t i = 0; i < mine; ++i) {
-        const int64_t nxt = i + kSkewStages - 1;
+        const int64_t nxt = i + STAGES - 1;
         if (nxt < mine) issue_skew(a, skew_tile(first + nxt * step, a), sbase + ahead * stage, k, cr0, rstep);
         cp_async_commit();
         const PanelTile ti = skew_tile(first + i * step, a);
         const SkewPhase ph = skew_phase<DELTA>(a, ti);
         if (threadIdx.x < 31) rowtab[threadIdx.x] = skew_row_entry(a, ph, threadIdx.x);
-        cp_async_wait<kSkewStages - 1>();
+        cp_async_wait<STAGES - 1>();
         __syncthreads();
         drain_skew<DELTA>(a, ti, ph, rowtab, slot * stage);
         __syncthreads();
-        slot = slot + 1 == kSkewStages ? 0 : slot + 1;
-        ahead = ahead + 1 == kSkewStages ? 0 : ahead + 1;
+        slot = slot + 1 == STAGES ? 0 : slot + 1;
+        ahead = ahead + 1 == STAGES ? 0 : ahead + 1;
     }
     cp_async_wait<0>();
     dev::cta_finish(a.cta_times);
@@ -913,24 +915,32 @@ const void* panel_kernel(int eb, bool vec, bool am) {
     }
 }
 
-const void* panel_skew_kernel(int delta) {
+namespace {
+template <int STAGES>
+const void* skew_pick(int delta) {
     switch (delta) {
-    case 1: return reinterpret_cast<const void*>(&k_panel_skew<1>);
-    case 3: return reinterpret_cast<const void*>(&k_panel_skew<3>);
-    case 5: return reinterpret_cast<const void*>(&k_panel_skew<5>);
-    case 7: return reinterpret_cast<const void*>(&k_panel_skew<7>);
-    case 9: return reinterpret_cast<const void*>(&k_panel_skew<9>);
-    case 11: return reinterpret_cast<const void*>(&k_panel_skew<11>);
-    case 13: return reinterpret_cast<const void*>(&k_panel_skew<13>);
-    case 15: return reinterpret_cast<const void*>(&k_panel_skew<15>);
+    case 1: return reinterpret_cast<const void*>(&k_panel_skew<1, STAGES>);
+    case 3: return reinterpret_cast<const void*>(&k_panel_skew<3, STAGES>);
+    case 5: return reinterpret_cast<const void*>(&k_panel_skew<5, STAGES>);
+    case 7: return reinterpret_cast<const void*>(&k_panel_skew<7, STAGES>);
+    case 9: return reinterpret_cast<const void*>(&k_panel_skew<9, STAGES>);
+    case 11: return reinterpret_cast<const void*>(&k_panel_skew<11, STAGES>);
+    case 13: return reinterpret_cast<const void*>(&k_panel_skew<13, STAGES>);
+    case 15: return reinterpret_cast<const void*>(&k_panel_skew<15, STAGES>);
     default: return nullptr;
     }
 }
+}  // namespace
 
-cudaError_t launch_panel_skew(const PanelArgs& a, int grid, int block, int smem,
+const void* panel_skew_kernel(int delta, int stages) {
+    return stages == 1 ? skew_pick<1>(delta) : stages == 2 ? skew_pick<2>(delta) : nullptr;
+}
+
+cudaError_t launch_panel_skew(const PanelArgs& a, int stages, int grid, int block, int smem,
                               cudaStream_t st, bool pdl) {
     using Kernel = void (*)(const PanelArgs);
-    const Kernel k = reinterpret_cast<Kernel>(panel_skew_kernel((int)((16 - (a.ds_a & 15)) & 15)));
+    const Kernel k =
+        reinterpret_cast<Kernel>(panel_skew_kernel((int)((16 - (a.ds_a & 15)) & 15), stages));
     if (!k || block <= 0 || block > kPanelThreads || block % 32 != 0) return cudaErrorInvalidValue;
     return launch_kernel(k, dim3(grid), dim3(block), smem, st, pdl, a);
 }

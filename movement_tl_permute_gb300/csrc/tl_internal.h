@@ -122,7 +122,7 @@ constexpr int kPanelMaxSmem = 160 * 1024;
 // the 16-byte blocks around the row's src bytes at r * pitch + 16 * (r / 16), pitch =
 // columns + 32 bytes.
 constexpr int kSkewRows = 256;
-constexpr int kSkewStages = 2;
+constexpr int kSkewStages = 2;     // the most stages a CTA holds
 constexpr int skew_pitch(int ta) { return ta + 32; }
 constexpr int skew_stage_bytes(int ta) {
     return ((kSkewRows + 15) * skew_pitch(ta) + 16 * (kSkewRows / 16 + 1) + 127) / 128 * 128;

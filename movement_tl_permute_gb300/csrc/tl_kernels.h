@@ -244,9 +244,10 @@ const void* panel_kernel(int eb, bool vec, bool am);
 cudaError_t launch_panel(int eb, const PanelArgs& a, int grid, int smem, cudaStream_t st,
                          bool pdl);
 // The skew walk (1-byte elements, dst row pitch odd): one kernel per dst row pitch
-// modulo 16 (`delta` = -pitch mod 16, odd), 32 columns of a per warp of `block`.
-const void* panel_skew_kernel(int delta);
-cudaError_t launch_panel_skew(const PanelArgs& a, int grid, int block, int smem,
+// modulo 16 (`delta` = -pitch mod 16, odd) and ring depth (1 or 2 stages), 32 columns
+// of a per warp of `block`.
+const void* panel_skew_kernel(int delta, int stages);
+cudaError_t launch_panel_skew(const PanelArgs& a, int stages, int grid, int block, int smem,
                               cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- block

@@ -49,6 +49,7 @@ struct TileTuning {
     int cluster_warps = 4;  // its consumer warps (8 or 4)
     int cluster_ctas = 0;   // its CTAs per SM (0 = by layout; tile_ctas_per_sm overrides)
     int block_warps = 0;    // block path: consumer warps at most (0 = as many as fit)
+    int skew_stages = 0;    // panel skew walk: stages per CTA (0 = default)
 };
 
 // Tile-path ring depth and grid by element width.  Throughput against the tiles in
@@ -95,6 +96,14 @@ void cluster_defaults(const Plan& p, TileTuning& t) {
     if (t.cluster_ctas == 0) t.cluster_ctas = contiguous ? 0 : 2;
 }
 
+// Stages per CTA of the panel skew walk (tile_stages 1 or 2 overrides): one, two CTAs
+// per SM.  Measured on GB300 against one CTA of two stages (8 warps an SM either way at
+// two stages): odd-pitch u8 transposes 4.98 -> 5.02 (32767 x 32769), 4.54 -> 4.83
+// (16385 x 16383), 4.76 -> 4.97 (32769 x 32767), 4.88 -> 5.20 TB/s (20000 x 30001):
+// sixteen warps an SM hide more of the walk's latency than one CTA's own overlap of
+// copies and stores.
+int skew_stages(const TileTuning& t) { return t.skew_stages > 0 ? t.skew_stages : 1; }
+
 TileTuning tile_tuning(const tl_permute_opts* o) {
     TileTuning t;
     if (!o) return t;
@@ -109,6 +118,7 @@ TileTuning tile_tuning(const tl_permute_opts* o) {
     if (o->cluster_consumer_warps >= 1 && o->cluster_consumer_warps < kBlockMaxWarps)
         t.block_warps = o->cluster_consumer_warps;
     if (o->tile_ctas_per_sm > 0) t.ctas_per_sm = o->tile_ctas_per_sm;
+    if (o->tile_stages == 1 || o->tile_stages == 2) t.skew_stages = o->tile_stages;
     if (o->tile_rows == 256) t.rows = 256;
     const int max_stages = kTileRingBytes / (t.rows * 128);
     if (t.stages > max_stages) t.stages = max_stages;
@@ -178,10 +188,11 @@ int get_device_info(DevInfo* out) {
                                              kBlockMaxSmem) != cudaSuccess)
                         return TL_ERR_CUDA;
             for (int delta = 1; i == 0 && delta < 16; delta += 2)
-                if (cudaFuncSetAttribute(panel_skew_kernel(delta),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kPanelMaxSmem) != cudaSuccess)
-                    return TL_ERR_CUDA;
+                for (int stages = 1; stages <= kSkewStages; ++stages)
+                    if (cudaFuncSetAttribute(panel_skew_kernel(delta, stages),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kPanelMaxSmem) != cudaSuccess)
+                        return TL_ERR_CUDA;
             if (panel_tma_kernel(1 << i) &&
                 cudaFuncSetAttribute(panel_tma_kernel(1 << i),
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -502,13 +513,14 @@ Launch launch_shape(const Plan& p, const DevInfo* d, int32_t max_ctas, const Til
         break;
     case TL_PATH_PANEL:
         if (p.panel_skew) {
+            const int stages = skew_stages(tt);
             l.block = 32 * p.panel_skew_warps;
-            l.smem = kSkewStages * p.panel_stage;
+            l.smem = stages * p.panel_stage;
             if (sms) {
                 int per_sm = 0;
                 if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                        &per_sm, panel_skew_kernel((int)((16 - (p.ds_a & 15)) & 15)), l.block,
-                        l.smem) != cudaSuccess ||
+                        &per_sm, panel_skew_kernel((int)((16 - (p.ds_a & 15)) & 15), stages),
+                        l.block, l.smem) != cudaSuccess ||
                     per_sm < 1) {
                     cudaGetLastError();
                     per_sm = 1;
@@ -980,7 +992,7 @@ int run(const void* src, void* dst, int ndim, const int64_t* shape, const int64_
             a.skew = 1;
             a.nblk = p.panel_nblk;
             a.d_nblk = dev::make_divu32((uint32_t)p.panel_nblk);
-            err = launch_panel_skew(a, l.grid, l.block, l.smem, st, pdl);
+            err = launch_panel_skew(a, skew_stages(tt), l.grid, l.block, l.smem, st, pdl);
             break;
         }
         if (p.panel_tma) {

@@ -297,17 +297,18 @@ def _skew_cases():
 
 
 @pytest.mark.parametrize("kib", [0, 32])
-def test_panel_skew_walk(kib):
+@pytest.mark.parametrize("stages", [0, 1, 2])
+def test_panel_skew_walk(kib, stages):
     """The skew walk (16-byte pieces of dst rows at an odd pitch, 256- and 128-column
-    tiles) against the oracle, with aligned and unaligned bases; the same layouts with
-    element stores forced take the word walk."""
+    tiles, one or two stages per CTA) against the oracle, with aligned and unaligned
+    bases; the same layouts with element stores forced take the word walk."""
     for i, (shape, ss, ds) in enumerate(_skew_cases()):
         for so, do in ((0, 0), (1, 0), (0, 7), (13, 5)):
             plan = tl.tl_plan((1 << 20) + so, (1 << 36) + do, shape, ss, ds, 1, path="panel",
                               panel_tile_kib=kib)
             assert plan["panel_vec"] == 4 and plan["tile_cols"] == (128 if kib else 256), plan
             check(shape, ss, ds, 1, "panel", seed=900 + 10 * i + so + do, src_off=so,
-                  dst_off=do, panel_tile_kib=kib)
+                  dst_off=do, panel_tile_kib=kib, tile_stages=stages)
         off = tl.tl_plan(1 << 20, 1 << 36, shape, ss, ds, 1, path="panel",
                          flags=tl.TL_FLAG_PANEL_ELEMENT_STORES)
         assert off["panel_vec"] != 4

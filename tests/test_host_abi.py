@@ -467,8 +467,8 @@ def _vec_rows_ok(tb, eb):
 
 def _check_skew_layout(p):
     """The skew walk's stage (1-byte elements, odd dst row pitch): tiles of 32 columns
-    of a per warp by 256 rows of b, rows of ta + 32 bytes 16 bytes further per 16 rows,
-    two stages.  Lane l of warp w reads, for each of its window rows c = 0..30, the two
+    of a per warp by 256 rows of b, rows of ta + 32 bytes 16 bytes further per 16 rows.
+    Lane l of warp w reads, for each of its window rows c = 0..30, the two
     aligned 16-byte words around its 16 columns of stage row 16 (l mod 16) + c (strip
     2w + l // 16): for every src offset u = 0..30 of those columns both reads must be
     conflict-free on the bank model (8 lanes a wavefront), and the copy of a row (16-byte

@@ -413,7 +413,7 @@ CONFIG_RUNS = [("tile_transpose", "tile_transpose", "auto"),
                ("t2d_u8", "t2d_u8", "auto"), ("t2d_f16", "t2d_f16", "auto"),
                ("t2d_f32", "t2d_f32", "auto"), ("t2d_f64", "t2d_f64", "auto"),
                ("t2d_v16", "t2d_v16", "auto"), ("nd8_f32", "nd8_f32", "auto"),
-               ("nd8_u16", "nd8_u16", "auto")]
+               ("nd8_u16", "nd8_u16", "auto"), ("t2d_odd_u8", "t2d_odd_u8", "auto")]
 
 
 def all_configs(args, tl, dev, stream, head_name, head_src):
@@ -473,7 +473,8 @@ def all_configs(args, tl, dev, stream, head_name, head_src):
                            "bit_exact": bool(np.array_equal(d_gpu.cpu().numpy(), want))}
     del graph, s_gpu, d_gpu
 
-    # configs 2-5 (HBM-bound)
+    # configs 2-5 (HBM-bound), then the two high-rank block-path workloads and the odd-pitch
+    # u8 transpose
     for name, wname, path in CONFIG_RUNS:
         w = workloads.get(wname)
         src_np = head_src if wname == head_name else workloads.make_input(w)
@@ -708,8 +709,9 @@ def main(argv=None):
                          "holds all of them (auto: graph for the one-warp workload, whose "
                          "step is shorter than a host-side launch)"),
     ap.add_argument("--configs", choices=["auto", "all", "none"], default="auto",
-                    help="also measure every configuration of the metric (auto: with the "
-                         "default workload at full size on one GPU)")
+                    help="also measure every configuration of the metric and three layouts "
+                         "outside them (auto: with the default workload at full size on one "
+                         "GPU)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -26,11 +26,11 @@ def test_sampled_parity_compares_exactly_the_sampled_image():
 
 
 def test_config_runs_name_every_configuration():
-    """Every configuration of the metric, plus the two high-rank block-path workloads
-    (inputs larger than L2, like the rest)."""
+    """Every configuration of the metric, plus the two high-rank block-path workloads and
+    the odd-pitch u8 transpose (inputs larger than L2, like the rest)."""
     names = {wname for _, wname, _ in bench.CONFIG_RUNS}
     assert names == {"tile_transpose", "mx_sf", "attention", "t2d_u8", "t2d_f16", "t2d_f32",
-                     "t2d_f64", "t2d_v16", "nd8_f32", "nd8_u16"}
+                     "t2d_f64", "t2d_v16", "nd8_f32", "nd8_u16", "t2d_odd_u8"}
     for name in names:
         w = workloads.get(name)
         assert w.src_elems * w.elem_bytes > bench.L2_BYTES, name

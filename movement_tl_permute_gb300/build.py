@@ -89,6 +89,37 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     return LIB
 
 
+def kernel_resources() -> list:
+    """Spill bytes of every kernel and device function, as ptxas reports them (-v) for each
+    CUDA source compiled on its own into a scratch directory (the library is not touched):
+    a list of {"name", "spill_stores", "spill_loads"}."""
+    import re
+    import tempfile
+    cu, _, _ = _sources()
+    nvcc = _nvcc()
+    common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC, "-Xptxas", "-v"]
+    with tempfile.TemporaryDirectory() as tmp:
+        jobs = [[nvcc] + ARCH + common + ["-c", src, "-o", os.path.join(tmp, os.path.basename(src) + ".o")]
+                for src in cu]
+        with cf.ThreadPoolExecutor(max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
+            results = list(ex.map(_compile, jobs))
+    out, name = [], None
+    for c, rc, text in results:
+        if rc != 0:
+            raise RuntimeError("nvcc failed for " + c[-3] + ":\n" + text)
+        for line in text.splitlines():
+            m = re.search(r"Function properties for (\S+)", line)
+            if m:
+                name = m.group(1)
+                continue
+            m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", line)
+            if m and name:
+                out.append({"name": name, "spill_stores": int(m.group(1)),
+                            "spill_loads": int(m.group(2))})
+                name = None
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")

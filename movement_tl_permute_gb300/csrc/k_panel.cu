@@ -749,6 +749,15 @@ __device__ __forceinline__ uint32_t skew_row_entry(const PanelArgs& a, const Ske
     return (c * (uint32_t)a.pitch + 16 * (c >> 4) + (u & 16u)) | ((u & 15u) << 24);
 }
 
+// The first n < 16 bytes of a 16-byte piece (rows past the plane's end are not stored).
+__device__ __noinline__ void skew_store_part(uint8_t* dp, uint32_t w0, uint32_t w1, uint32_t w2,
+                                             uint32_t w3, uint32_t n) {
+    for (uint32_t i = 0; i < n; ++i) {
+        const uint32_t w = i < 4 ? w0 : i < 8 ? w1 : i < 12 ? w2 : w3;
+        dp[i] = (uint8_t)(w >> (8 * (i & 3u)));
+    }
+}
+
 // Store one landed tile (stage at shared-window offset st0) as 16-byte dst pieces;
 // rowtab holds the tile's skew_row_entry values.
 template <uint32_t DELTA>
@@ -762,14 +771,9 @@ __device__ __forceinline__ void drain_skew(const PanelArgs& a, const PanelTile& 
     const uint32_t ta = (uint32_t)a.ta, pitch = (uint32_t)a.pitch;
     uint8_t* const d = a.dst + ti.dof;
     const int64_t Pd = a.ds_a;
-    const uint32_t e = ph.e, mis0 = ph.mis0;
-    const uint32_t ds16 = (uint32_t)a.vdelta;            // src row pitch mod 16
+    const uint32_t e = ph.e;
     const uint32_t xlim = (uint32_t)min(a.ext_a - ti.a0, (int64_t)ta + 16);
     const uint32_t ylim = (uint32_t)min(a.ext_b - ti.b0, (int64_t)kSkewRows + 16);
-    // stage byte of (row r, column x)
-    auto at = [&](uint32_t r, uint32_t x) -> uint8_t {
-        return smem_sk[st0 + r * pitch + 16 * (r >> 4) + ((mis0 + r * ds16) & 15u) + x];
-    };
     // the lane's 16 columns of stage row 16 * blk + c, in column order
     const uint32_t lbase = st0 + blk * (16 * pitch + 16) + 16 * strip;
     auto load_row = [&](uint32_t c, uint32_t (&w)[4]) {
@@ -791,7 +795,10 @@ __device__ __forceinline__ void drain_skew(const PanelArgs& a, const PanelTile& 
 #pragma unroll
     for (uint32_t c = 0; c < 16; ++c) load_row(c, W[c]);
     const uint32_t x0 = e + 16 * strip;
-    uint8_t* const dl = d + (int64_t)x0 * Pd + 16 * blk;
+    // the piece of step k is at dst + (x0 + j) * Pd + 16 * blk + k; from one step to the
+    // next j grows by DINV, less 16 where it wraps
+    const int64_t up = (int64_t)DINV * Pd + 1, wrap = ((int64_t)DINV - 16) * Pd + 1;
+    uint8_t* dp = d + (int64_t)x0 * Pd + 16 * blk;
 #pragma unroll
     for (uint32_t k = 0; k < 16; ++k) {
         // step k: column x0 + j of phase k, rows 16 * blk + k .. + 15 (window slots)
@@ -805,20 +812,36 @@ __device__ __forceinline__ void drain_skew(const PanelArgs& a, const PanelTile& 
         }
         const uint32_t r0 = 16 * blk + k;
         if (x0 + j < xlim && r0 < ylim) {
-            uint8_t* dp = dl + (int64_t)j * Pd + k;
-            if (r0 + 16 <= ylim) {
+            if (r0 + 16 <= ylim)
                 dev::stg128(dp, make_uint4(o[0], o[1], o[2], o[3]));
-            } else {       // the last rows of the plane
-#pragma unroll
-                for (uint32_t i = 0; i < 16; ++i)
-                    if (r0 + i < ylim) dp[i] = (uint8_t)(o[i >> 2] >> (8 * (i & 3u)));
-            }
+            else           // the last rows of the plane
+                skew_store_part(dp, o[0], o[1], o[2], o[3], ylim - r0);
         }
-        if (k < 15) load_row(16 + k, W[k]);
+        if (k < 15) {
+            load_row(16 + k, W[k]);
+            dp += ((((k + 1) * DINV) & 15u) > j) ? up : wrap;
+        }
     }
-    // Elements no tile's pieces reach: the rows before each column's first piece (the
-    // plane's first row block), and the columns before the first strip (its first
-    // column block), element by element.
+}
+
+// Elements no tile's pieces reach: the rows before each column's first piece (the
+// plane's first row block), and the columns before the first strip (its first column
+// block), element by element.  Tile t's coordinates are derived again here, so that the
+// walk above holds none of them (the walk fits 128 registers a thread without spilling).
+template <uint32_t DELTA>
+__device__ __forceinline__ void drain_skew_edges(const PanelArgs& a, int64_t t, uint32_t st0) {
+    extern __shared__ __align__(16) uint8_t smem_ed[];
+    const PanelTile ti = skew_tile(t, a);
+    const SkewPhase ph = skew_phase<DELTA>(a, ti);
+    const uint32_t ta = (uint32_t)a.ta, pitch = (uint32_t)a.pitch, e = ph.e;
+    const uint32_t ds16 = (uint32_t)a.vdelta;
+    uint8_t* const d = a.dst + ti.dof;
+    const int64_t Pd = a.ds_a;
+    const uint32_t xlim = (uint32_t)min(a.ext_a - ti.a0, (int64_t)ta + 16);
+    const uint32_t ylim = (uint32_t)min(a.ext_b - ti.b0, (int64_t)kSkewRows + 16);
+    auto at = [&](uint32_t r, uint32_t x) -> uint8_t {
+        return smem_ed[st0 + r * pitch + 16 * (r >> 4) + ((ph.mis0 + r * ds16) & 15u) + x];
+    };
     if (ti.b0 == 0) {
         const uint32_t xs = ti.a0 == 0 ? 0u : e, xe = min(ta + e, xlim);
         const uint32_t nr = min(15u, ylim);
@@ -853,28 +876,37 @@ __global__ void __launch_bounds__(kPanelThreads, STAGES == 1 ? 2 : 1) k_panel_sk
     dev::grid_dependency_wait();
     dev::allow_dependent_launch();
     dev::cta_start(a.cta_times);
-    const int64_t first = blockIdx.x, step = gridDim.x;
-    const int64_t mine = first < a.tiles ? (a.tiles - first + step - 1) / step : 0;
-    // this thread's copy block and first row (threads past rstep * nblk copy nothing)
-    const uint32_t nblk = (uint32_t)a.nblk;
-    const uint32_t r0 = dev::div_u32(threadIdx.x, a.d_nblk), k = threadIdx.x - r0 * nblk;
-    const uint32_t rstep = dev::div_u32(blockDim.x, a.d_nblk);
-    const uint32_t cr0 = r0 < rstep ? r0 : (uint32_t)kSkewRows + 16;
-    for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < mine) issue_skew(a, skew_tile(first + s * step, a), sbase + s * stage, k, cr0, rstep);
+    // (a CTA's tile count fits 32 bits: the grid is at most a few CTAs per SM)
+    const uint32_t mine = blockIdx.x < a.tiles
+        ? (uint32_t)((a.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x) : 0u;
+    auto tile_of = [&](uint32_t i) { return (int64_t)blockIdx.x + (int64_t)i * gridDim.x; };
+    // this thread's copy block and first row (threads past rstep * nblk copy nothing),
+    // derived again for each copy so that the walk holds none of it
+    auto issue = [&](uint32_t i, uint32_t sb) {
+        const uint32_t nblk = (uint32_t)a.nblk;
+        const uint32_t r0 = dev::div_u32(threadIdx.x, a.d_nblk), k = threadIdx.x - r0 * nblk;
+        const uint32_t rstep = dev::div_u32(blockDim.x, a.d_nblk);
+        const uint32_t cr0 = r0 < rstep ? r0 : (uint32_t)kSkewRows + 16;
+        issue_skew(a, skew_tile(tile_of(i), a), sb, k, cr0, rstep);
+    };
+    for (uint32_t s = 0; s < STAGES - 1; ++s) {
+        if (s < mine) issue(s, sbase + s * stage);
         cp_async_commit();
     }
     uint32_t slot = 0, ahead = STAGES - 1;
-    for (int64_t i = 0; i < mine; ++i) {
-        const int64_t nxt = i + STAGES - 1;
-        if (nxt < mine) issue_skew(a, skew_tile(first + nxt * step, a), sbase + ahead * stage, k, cr0, rstep);
+    for (uint32_t i = 0; i < mine; ++i) {
+        const uint32_t nxt = i + STAGES - 1;
+        if (nxt < mine) issue(nxt, sbase + ahead * stage);
         cp_async_commit();
-        const PanelTile ti = skew_tile(first + i * step, a);
+        const int64_t t = tile_of(i);
+        const PanelTile ti = skew_tile(t, a);
         const SkewPhase ph = skew_phase<DELTA>(a, ti);
+        const bool edge = ti.b0 == 0 || ti.a0 == 0;
         if (threadIdx.x < 31) rowtab[threadIdx.x] = skew_row_entry(a, ph, threadIdx.x);
         cp_async_wait<STAGES - 1>();
         __syncthreads();
         drain_skew<DELTA>(a, ti, ph, rowtab, slot * stage);
+        if (edge) drain_skew_edges<DELTA>(a, t, slot * stage);
         __syncthreads();
         slot = slot + 1 == STAGES ? 0 : slot + 1;
         ahead = ahead + 1 == STAGES ? 0 : ahead + 1;

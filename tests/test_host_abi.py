@@ -1048,3 +1048,13 @@ def test_thread_axis_check_matches_the_oracle():
     assert valid >= 200
     with pytest.raises(tl.TLError):
         tl.tl_thread_axis_check((32, 8), (1, 1), (0, 1))
+
+
+def test_no_kernel_spills_registers():
+    """ptxas -v on every CUDA source: no kernel or device function spills a register
+    (spill stores and loads go through local memory on the hot path)."""
+    from movement_tl_permute_gb300 import build
+    res = build.kernel_resources()
+    assert len(res) > 50 and any("k_panel_skew" in r["name"] for r in res)
+    bad = [r for r in res if r["spill_stores"] or r["spill_loads"]]
+    assert not bad, bad

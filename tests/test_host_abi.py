@@ -1058,3 +1058,52 @@ def test_no_kernel_spills_registers():
     assert len(res) > 50 and any("k_panel_skew" in r["name"] for r in res)
     bad = [r for r in res if r["spill_stores"] or r["spill_loads"]]
     assert not bad, bad
+
+
+def _inv16(d):
+    return next(x for x in range(1, 16, 2) if (d * x) % 16 == 1)
+
+
+@pytest.mark.parametrize("ext_a,ext_b,pd,dmis,ta", [
+    (300, 270, 303, 0, 256), (300, 270, 303, 7, 128), (513, 290, 529, 3, 256),
+    (64, 64, 67, 15, 256), (290, 513, 521, 9, 128), (600, 260, 601, 12, 256)])
+def test_skew_walk_pieces_cover_the_plane(ext_a, ext_b, pd, dmis, ta):
+    """The skew walk's ownership, replayed on the host with the kernel's formulas: tiles of
+    ta columns (a) by 256 rows (b); strips start e columns into each tile, e = -rho0 / delta
+    mod 16 with rho0 the tile's first dst offset to the next 16-byte boundary and delta =
+    -pd mod 16; the lane (strip, block) stores at step k the piece of column e + 16 strip +
+    (k / delta mod 16) starting at row 16 block + k.  Every full piece must start on a
+    16-byte boundary, no two pieces may overlap, and the pieces plus the first row and column
+    blocks' element stores must cover every element of the plane."""
+    delta = (-pd) % 16
+    dinv = _inv16(delta)
+    base = 4096 + dmis                       # dst byte address of element (a=0, b=0)
+    hits = np.zeros((ext_a, ext_b), dtype=np.int32)
+    edge = np.zeros((ext_a, ext_b), dtype=bool)
+    for a0 in range(0, ext_a, ta):
+        for b0 in range(0, ext_b, 256):
+            d = base + a0 * pd + b0
+            rho0 = (16 - d % 16) % 16
+            e = ((16 - rho0) * dinv) % 16
+            xlim, ylim = min(ext_a - a0, ta + 16), min(ext_b - b0, 256 + 16)
+            for strip in range(ta // 16):
+                x0 = e + 16 * strip
+                for blk in range(16):
+                    for k in range(16):
+                        j = (k * dinv) % 16
+                        r0 = 16 * blk + k
+                        if x0 + j >= xlim or r0 >= ylim:
+                            continue
+                        n = min(16, ylim - r0)
+                        if n == 16:
+                            assert (d + (x0 + j) * pd + r0) % 16 == 0
+                        hits[a0 + x0 + j, b0 + r0:b0 + r0 + n] += 1
+            if b0 == 0:
+                xs = 0 if a0 == 0 else e
+                for x in range(xs, min(ta + e, xlim)):
+                    edge[a0 + x, 0:min(15, ylim)] = True
+            if a0 == 0:
+                for x in range(min(e, xlim)):
+                    edge[x, b0:b0 + min(256, ylim)] = True
+    assert hits.max() <= 1                    # pieces never overlap
+    assert ((hits == 1) | edge).all()         # and with the edge stores cover the plane

@@ -1107,3 +1107,20 @@ def test_skew_walk_pieces_cover_the_plane(ext_a, ext_b, pd, dmis, ta):
                     edge[x, b0:b0 + min(256, ylim)] = True
     assert hits.max() <= 1                    # pieces never overlap
     assert ((hits == 1) | edge).all()         # and with the edge stores cover the plane
+
+
+def test_skew_walk_eligibility():
+    """The panel path takes the skew walk for 1-byte planes whose dst rows sit at an odd
+    pitch, both extents at least 64, unless element stores are asked for; other widths,
+    even pitches and small planes keep the other store modes."""
+    def vec(shape, ss, ds, eb=1, **kw):
+        return tl.tl_plan(SRC, DST, shape, ss, ds, eb, path="panel", **kw)["panel_vec"]
+    assert vec((300, 270), (270, 1), (1, 303)) == 4
+    assert vec((64, 64), (65, 1), (1, 65)) == 4
+    assert vec((300, 270), (270, 1), (1, 302)) != 4              # even dst pitch
+    assert vec((63, 270), (270, 1), (1, 63)) != 4                # b extent under 64
+    assert vec((300, 63), (63, 1), (1, 303)) != 4                # a extent under 64
+    assert vec((300, 270), (270, 1), (1, 303), eb=2) != 4        # 2-byte elements
+    assert vec((300, 270), (270, 1), (1, 303),
+               flags=tl.TL_FLAG_PANEL_ELEMENT_STORES) != 4
+    assert tl.tl_plan(SRC, DST, (300, 270), (270, 1), (1, 303), 1)["path"] == "panel"

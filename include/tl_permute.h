@@ -244,8 +244,9 @@ typedef struct tl_permute_opts {
                                        (by default 8, or 4 for tiles of 48 src runs or
                                        more) */
     int32_t panel_tile_kib;       /* panel path: tile size, 4..48 KiB (default 32, or 24
-                                     with an extent of 16 or less); block path: its
-                                     tile's bytes */
+                                     with an extent of 16 or less; the skew walk: 256 x
+                                     256 elements, 128 x 256 at 32 KiB or less); block
+                                     path: its tile's bytes */
     int32_t cast;         /* TL_CAST_*: convert every element on the way (elem_bytes
                              and src_strides are the source type's, dst_strides the
                              destination type's); the tile, chunk, block and generic
